@@ -1,0 +1,201 @@
+"""Thin Python binding over the C ABI in include/pw.h.
+
+Only argument marshalling happens here: torch tensors are turned into device
+pointers and streams; every step of the layer runs in libpw.so's kernels.
+PyTorch provides device memory (the page pool buffer, activations, scratch)
+and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+import torch
+
+from ._lib import (LUTP, U8P3, U16P3, U32P6, LayerDesc, PoolStats, check, lib)
+
+BITS_ALLOWED = (3, 4, 5, 6, 16)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _host(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        a = a.astype(dtype)
+    return a
+
+
+def pack_planes(code6: np.ndarray):
+    """Library packer: six uint32 plane arrays for a uint8 code matrix [R, C]."""
+    code6 = _host(code6, np.uint8)
+    R, Cc = code6.shape
+    outs = [np.zeros(R * Cc // 32, dtype=np.uint32) for _ in range(6)]
+    arr = U32P6(*[o.ctypes.data for o in outs])
+    check(lib.pw_pack_planes(code6.ctypes.data, R, Cc, C.byref(arr)), "pw_pack_planes")
+    return outs
+
+
+def pack_f16(w16: np.ndarray) -> np.ndarray:
+    w = _host(w16, np.float16)
+    R, Cc = w.shape
+    out = np.zeros(R * Cc, dtype=np.uint16)
+    check(lib.pw_pack_f16(w.ctypes.data, R, Cc, out.ctypes.data), "pw_pack_f16")
+    return out
+
+
+class Pool:
+    """Page pool over one device buffer (a torch uint8 tensor)."""
+
+    def __init__(self, nbytes: int, page_bytes: int = 2 << 20, device=None, buffer=None):
+        if buffer is None:
+            dev = device if device is not None else ("cuda" if torch.cuda.is_available() else "cpu")
+            buffer = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+        self.buffer = buffer
+        base = buffer.data_ptr()
+        pad = (-base) % 256
+        self.handle = C.c_void_p()
+        check(lib.pw_pool_create(base + pad, buffer.numel() - pad, page_bytes, C.byref(self.handle)),
+              "pw_pool_create")
+
+    def stats(self) -> dict:
+        s = PoolStats()
+        check(lib.pw_pool_get_stats(self.handle, C.byref(s)), "pw_pool_get_stats")
+        return {f: getattr(s, f) for f, _ in PoolStats._fields_}
+
+    def close(self):
+        if self.handle:
+            check(lib.pw_pool_destroy(self.handle), "pw_pool_destroy")
+            self.handle = C.c_void_p()
+
+
+class Layer:
+    """One MoE layer: page-table handle plus the hot-path calls."""
+
+    def __init__(self, pool: Pool, d: int, ffn: int, n_experts: int, top_k: int,
+                 renormalize: int, shared_ffn: int = 0):
+        self.pool = pool
+        self.desc = LayerDesc(d, ffn, n_experts, top_k, renormalize, shared_ffn)
+        self.handle = C.c_void_p()
+        check(lib.pw_layer_create(pool.handle, C.byref(self.desc), C.byref(self.handle)), "pw_layer_create")
+        self.d, self.ffn, self.E, self.K = d, ffn, n_experts, top_k
+        self.renormalize, self.shared_ffn = renormalize, shared_ffn
+
+    # -- setup ---------------------------------------------------------------
+    def load_expert(self, e: int, bits: int, code6, luts, w16=None, stream=None):
+        """code6: 3 uint8 [R,C]; luts: 3 x [LUT_3..LUT_6] fp16; w16: 3 fp16 [R,C] or None."""
+        c = [_host(m, np.uint8) for m in code6]
+        lt = [[_host(t, np.float16) for t in row] for row in luts]
+        ws = [_host(m, np.float16) for m in w16] if w16 is not None else None
+        a_code = U8P3(*[m.ctypes.data for m in c])
+        a_lut = LUTP(*[(C.c_void_p * 4)(*[t.ctypes.data for t in row]) for row in lt])
+        a_w16 = U16P3(*[m.ctypes.data for m in ws]) if ws is not None else U16P3(None, None, None)
+        check(lib.pw_layer_load_expert(self.handle, e, bits, C.byref(a_code), C.byref(a_lut),
+                                       C.byref(a_w16), _s(stream)), f"pw_layer_load_expert(e={e})")
+
+    def load_shared(self, w16, stream=None):
+        ws = [_host(m, np.float16) for m in w16]
+        arr = U16P3(*[m.ctypes.data for m in ws])
+        check(lib.pw_layer_load_shared(self.handle, C.byref(arr), _s(stream)), "pw_layer_load_shared")
+
+    def destroy(self):
+        if self.handle:
+            check(lib.pw_layer_destroy(self.handle), "pw_layer_destroy")
+            self.handle = C.c_void_p()
+
+    # -- precision -------------------------------------------------------------
+    def set_expert_bitwidth(self, e: int, bits: int, stream=None):
+        check(lib.pw_set_expert_bitwidth(self.handle, e, bits, _s(stream)), "pw_set_expert_bitwidth")
+
+    def try_set_expert_bitwidth(self, e: int, bits: int, stream=None) -> int:
+        return lib.pw_set_expert_bitwidth(self.handle, e, bits, _s(stream))
+
+    def get_expert_bitwidth(self, e: int) -> int:
+        b = C.c_int32(0)
+        check(lib.pw_get_expert_bitwidth(self.handle, e, C.byref(b)), "pw_get_expert_bitwidth")
+        return b.value
+
+    def workspace_size(self, T: int) -> int:
+        n = C.c_size_t(0)
+        check(lib.pw_workspace_size(self.handle, T, C.byref(n)), "pw_workspace_size")
+        return n.value
+
+    def check_device(self, stream=None) -> int:
+        return lib.pw_layer_check_device(self.handle, _s(stream))
+
+    # -- hot path ----------------------------------------------------------------
+    def route_topk(self, x, wr, bias, T, idx, w, counts=None, stream=None):
+        check(lib.pw_route_topk(self.handle, _p(x), _p(wr), _p(bias), T, _p(idx), _p(w), _p(counts),
+                                _s(stream)), "pw_route_topk")
+
+    def permute(self, idx, T, x, offsets, perm_src, inv_slot, x_perm, ws, stream=None):
+        check(lib.pw_permute(self.handle, _p(idx), T, _p(x), _p(offsets), _p(perm_src), _p(inv_slot),
+                             _p(x_perm), _p(ws), ws.numel() * ws.element_size(), _s(stream)), "pw_permute")
+
+    def expert_ffn_bitplane(self, x_perm, offsets, T, y_perm, ws, stream=None):
+        check(lib.pw_expert_ffn_bitplane(self.handle, _p(x_perm), _p(offsets), T, _p(y_perm), _p(ws),
+                                         ws.numel() * ws.element_size(), _s(stream)), "pw_expert_ffn_bitplane")
+
+    def shared_ffn(self, x, T, y_shared, ws, stream=None):
+        check(lib.pw_shared_ffn(self.handle, _p(x), T, _p(y_shared), _p(ws), ws.numel() * ws.element_size(),
+                                _s(stream)), "pw_shared_ffn")
+
+    def combine(self, y_perm, inv_slot, w, T, y_shared, y, stream=None):
+        check(lib.pw_combine(self.handle, _p(y_perm), _p(inv_slot), _p(w), T, _p(y_shared), _p(y), _s(stream)),
+              "pw_combine")
+
+    def debug_dequant(self, e: int, m: int, out, stream=None):
+        check(lib.pw_debug_dequant(self.handle, e, m, _p(out), _s(stream)), "pw_debug_dequant")
+
+    def page_address(self, e: int, p: int, vpage: int) -> int:
+        a = C.c_uint64(0)
+        check(lib.pw_debug_page_address(self.handle, e, p, vpage, C.byref(a)), "pw_debug_page_address")
+        return a.value
+
+
+class Buffers:
+    """Device buffers for one layer call at up to T_max tokens (reused every step)."""
+
+    def __init__(self, layer: Layer, T_max: int, device="cuda"):
+        d, K, E = layer.d, layer.K, layer.E
+        S = T_max * K
+        self.T_max = T_max
+        self.idx = torch.empty((T_max, K), dtype=torch.int32, device=device)
+        self.w = torch.empty((T_max, K), dtype=torch.float32, device=device)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=device)
+        self.perm_src = torch.empty(S, dtype=torch.int32, device=device)
+        self.inv_slot = torch.empty(S, dtype=torch.int32, device=device)
+        self.x_perm = torch.empty((S, d), dtype=torch.float16, device=device)
+        self.y_perm = torch.empty((S, d), dtype=torch.float32, device=device)
+        self.y_shared = (torch.empty((T_max, d), dtype=torch.float32, device=device)
+                         if layer.shared_ffn else None)
+        self.y = torch.empty((T_max, d), dtype=torch.float16, device=device)
+        self.ws = torch.empty(max(layer.workspace_size(T_max), 256), dtype=torch.uint8, device=device)
+
+
+def moe_forward(layer: Layer, x, wr, bias, buf: Buffers, stream=None):
+    """The whole hot path for x [T, d] (device fp16); returns buf.y[:T]."""
+    T = x.shape[0]
+    layer.route_topk(x, wr, bias, T, buf.idx, buf.w, None, stream)
+    layer.permute(buf.idx, T, x, buf.offsets, buf.perm_src, buf.inv_slot, buf.x_perm, buf.ws, stream)
+    layer.expert_ffn_bitplane(buf.x_perm, buf.offsets, T, buf.y_perm, buf.ws, stream)
+    ysh = None
+    if layer.shared_ffn:
+        layer.shared_ffn(x, T, buf.y_shared, buf.ws, stream)
+        ysh = buf.y_shared
+    layer.combine(buf.y_perm, buf.inv_slot, buf.w, T, ysh, buf.y, stream)
+    return buf.y[:T]

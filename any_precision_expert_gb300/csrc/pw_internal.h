@@ -1,0 +1,57 @@
+// Internal declarations shared by the host runtime and the CUDA kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pw.h"
+
+namespace pw {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kPlanes = 6;           // planes of the 6-bit parent code
+constexpr int kTileRows = 16;        // rows per stored tile
+constexpr int kChunkCols = 64;       // columns per stored chunk
+
+// Per-layer parameter block handed to kernels by value.  All pointers are
+// device addresses inside the layer's resident pool run.
+struct DevLayer {
+  int d, f, E, K, renorm, fs;
+  int pmax;      // virtual pages per plane block (expert, plane)
+  int pmax16;    // virtual pages per fp16 block (expert)
+  int tmax;      // row stride of the tile maps
+  const int* bits;                      // [E] current bitwidth
+  const unsigned long long* plane_pt;   // [E][6][pmax] page base addresses
+  const unsigned long long* f16_pt;     // [E][pmax16]
+  const uint2* tmap;                    // [3][tmax] plane tile -> (vpage, byte offset)
+  const uint2* tmap16;                  // [3][tmax] fp16 tile -> (vpage, byte offset)
+  const unsigned long long* lut_base;   // [E] LUT block of each expert
+  unsigned lut_off[3][4];               // byte offset of LUT_b (b = 3 + i) of matrix m
+  const __half* shared16[3];            // packed fp16 shared FFN (gate, up, down) or null
+  int* err;                             // device error word
+};
+
+// Scratch carved out of the caller's workspace for one hot-path call.
+struct FfnScratch {
+  __half* h;        // [n_slots][ffn] fp16 activations between gate/up and down
+};
+
+int sm_count();
+
+cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s);
+cudaError_t launch_route(const DevLayer& L, const __half* x, const __half* wr, const float* bias,
+                         int T, int* idx, float* w, int* counts, cudaStream_t s);
+size_t permute_ws_bytes(int S, int E);
+cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __half* x,
+                           int* offsets, int* perm_src, int* inv_slot, __half* x_perm,
+                           int* hist_ws, cudaStream_t s);
+// mode 0: routed experts over permuted slots; mode 1: the shared fp16 FFN over all T tokens.
+cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* offsets, int n_slots,
+                       float* y, __half* h_ws, cudaStream_t s);
+cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* inv_slot,
+                           const float* w, int T, const float* y_shared, __half* y, cudaStream_t s);
+cudaError_t launch_debug_dequant(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
+
+}  // namespace pw

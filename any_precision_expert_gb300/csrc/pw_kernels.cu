@@ -1,0 +1,338 @@
+// Router top-K, stable permutation, weighted combine and the bitwidth write.
+//
+// Routing and the combine are the standard MoE gate around PagedWeight's
+// experts (write-up zhichai.net/topic/178446964, "三层感知" names the router's
+// per-expert routing statistics); the permutation groups the (token, k) slots
+// by expert so each expert streams its planes once per batch.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "pw_device.cuh"
+
+namespace pw {
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// ---------------------------------------------------------------------------
+// bitwidth word (the stream-ordered commit of a precision change)
+// ---------------------------------------------------------------------------
+
+__global__ void set_bits_kernel(int* bits, int e, int b) { bits[e] = b; }
+
+cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s) {
+  set_bits_kernel<<<1, 1, 0, s>>>(bits, e, b);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// router: logits, softmax over E, top-K (ties to the lower index)
+// ---------------------------------------------------------------------------
+
+constexpr int kRouteTok = 8;      // tokens per CTA
+constexpr int kRouteThreads = 256;
+
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
+  const __half2* ha = reinterpret_cast<const __half2*>(&a);
+  const __half2* hb = reinterpret_cast<const __half2*>(&b);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = __half22float2(ha[i]);
+    const float2 fb = __half22float2(hb[i]);
+    acc = fmaf(fa.x, fb.x, acc);
+    acc = fmaf(fa.y, fb.y, acc);
+  }
+  return acc;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const __half* __restrict__ x,
+                                                              const __half* __restrict__ wr,
+                                                              const float* __restrict__ bias, int T,
+                                                              int* __restrict__ idx, float* __restrict__ wout,
+                                                              int* __restrict__ counts) {
+  extern __shared__ uint4 smem_route[];
+  const int d = L.d, E = L.E, K = L.K;
+  const int d8 = d / 8;
+  uint4* xs = smem_route;                                         // [kRouteTok][d/8]
+  float* logit = reinterpret_cast<float*>(xs + kRouteTok * d8);   // [kRouteTok][E]
+  const int t0 = blockIdx.x * kRouteTok;
+  const int nt = min(kRouteTok, T - t0);
+  const uint4* x4 = reinterpret_cast<const uint4*>(x) + (size_t)t0 * d8;
+  for (int i = threadIdx.x; i < nt * d8; i += blockDim.x) xs[i] = x4[i];
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += kRouteThreads / 32) {
+    float acc[kRouteTok];
+#pragma unroll
+    for (int t = 0; t < kRouteTok; ++t) acc[t] = 0.f;
+    const uint4* wrow = reinterpret_cast<const uint4*>(wr) + (size_t)e * d8;
+    for (int c = lane; c < d8; c += 32) {
+      const uint4 wv = __ldg(wrow + c);
+#pragma unroll
+      for (int t = 0; t < kRouteTok; ++t)
+        if (t < nt) acc[t] += dot8(wv, xs[t * d8 + c]);
+    }
+#pragma unroll
+    for (int t = 0; t < kRouteTok; ++t) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && t < nt) logit[t * E + e] = v + (bias ? bias[e] : 0.f);
+    }
+  }
+  __syncthreads();
+
+  if (warp < nt) {
+    const int t = t0 + warp;
+    const float* lg = logit + warp * E;
+    constexpr int kPer = kMaxExperts / 32;
+    float v[kPer];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? lg[e] : -INFINITY;
+      m = fmaxf(m, v[i]);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) z += (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+
+    unsigned taken = 0;  // bit i: expert lane + 32 i already chosen
+    float wsel[kMaxTopK];
+    int esel[kMaxTopK];
+    float wsum = 0.f;
+    for (int k = 0; k < K; ++k) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      esel[k] = be;
+      wsel[k] = expf(bv - m) / z;
+      wsum += wsel[k];
+    }
+    if (lane == 0) {
+      for (int k = 0; k < K; ++k) {
+        idx[(size_t)t * K + k] = esel[k];
+        wout[(size_t)t * K + k] = L.renorm ? wsel[k] / wsum : wsel[k];
+        if (counts) atomicAdd(counts + esel[k], 1);
+      }
+    }
+  }
+}
+
+cudaError_t launch_route(const DevLayer& L, const __half* x, const __half* wr, const float* bias, int T, int* idx,
+                         float* w, int* counts, cudaStream_t s) {
+  const size_t smem = (size_t)kRouteTok * L.d * sizeof(__half) + (size_t)kRouteTok * L.E * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = (T + kRouteTok - 1) / kRouteTok;
+  route_kernel<<<grid, kRouteThreads, smem, s>>>(L, x, wr, bias, T, idx, w, counts);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// stable permutation: per-chunk histograms, then ranked scatter
+// ---------------------------------------------------------------------------
+
+constexpr int kPermChunk = 1024;
+constexpr int kPermThreads = 256;
+
+size_t permute_ws_bytes(int S, int E) {
+  const int nblk = (S + kPermChunk - 1) / kPermChunk;
+  return (size_t)(nblk > 0 ? nblk : 1) * E * sizeof(int);
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(DevLayer L, const int* __restrict__ idx, int S,
+                                                                 int* __restrict__ hist) {
+  __shared__ int h[kMaxExperts];
+  const int E = L.E;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  const int s0 = blockIdx.x * kPermChunk, s1 = min(S, s0 + kPermChunk);
+  for (int s = s0 + threadIdx.x; s < s1; s += blockDim.x) {
+    const int e = idx[s];
+    if ((unsigned)e < (unsigned)E)
+      atomicAdd(&h[e], 1);
+    else
+      atomicExch(L.err, 2);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[blockIdx.x * E + i] = h[i];
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(DevLayer L, const int* __restrict__ idx, int S,
+                                                                    const int* __restrict__ hist, int nblk,
+                                                                    int* __restrict__ offsets,
+                                                                    int* __restrict__ perm_src,
+                                                                    int* __restrict__ inv_slot,
+                                                                    const __half* __restrict__ x,
+                                                                    __half* __restrict__ x_perm) {
+  __shared__ int base[kMaxExperts], run[kMaxExperts], scan[kMaxExperts];
+  __shared__ int wcnt[kPermThreads / 32][kMaxExperts];
+  __shared__ int pos_buf[kPermChunk];
+  const int E = L.E, K = L.K, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  // bucket starts (exclusive scan of the totals) and this chunk's base per expert
+  int pre = 0, tot = 0;
+  if (tid < E) {
+    for (int c = 0; c < nblk; ++c) {
+      const int v = hist[c * E + tid];
+      tot += v;
+      if (c < (int)blockIdx.x) pre += v;
+    }
+    scan[tid] = tot;
+  }
+  __syncthreads();
+  // Hillis-Steele inclusive scan over E <= 256 entries
+  for (int o = 1; o < kMaxExperts; o <<= 1) {
+    int v = 0;
+    if (tid < E && tid >= o) v = scan[tid - o];
+    __syncthreads();
+    if (tid < E) scan[tid] += v;
+    __syncthreads();
+  }
+  if (tid < E) {
+    const int start = scan[tid] - tot;
+    base[tid] = start + pre;
+    run[tid] = 0;
+    if (blockIdx.x == 0) offsets[tid] = start;
+  }
+  if (blockIdx.x == 0 && tid == 0) offsets[E] = S;
+  __syncthreads();
+
+  const int s0 = blockIdx.x * kPermChunk;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r = 0; r < kPermChunk / kPermThreads; ++r) {
+    for (int i = tid; i < (kPermThreads / 32) * kMaxExperts; i += kPermThreads) (&wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int slot = s0 + r * kPermThreads + tid;
+    const bool valid = slot < S;
+    int e = valid ? idx[slot] : -1;
+    if ((unsigned)e >= (unsigned)E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int prior = 0;
+      for (int w = 0; w < warp; ++w) prior += wcnt[w][e];
+      const int pos = base[e] + run[e] + prior + rank;
+      perm_src[pos] = slot / K;
+      inv_slot[slot] = pos;
+      pos_buf[r * kPermThreads + tid] = pos;
+    } else {
+      pos_buf[r * kPermThreads + tid] = -1;
+    }
+    __syncthreads();
+    if (tid < E) {
+      int add = 0;
+      for (int w = 0; w < kPermThreads / 32; ++w) add += wcnt[w][tid];
+      run[tid] += add;
+    }
+    __syncthreads();
+  }
+
+  if (x_perm) {
+    const int d8 = L.d / 8;
+    const uint4* x4 = reinterpret_cast<const uint4*>(x);
+    uint4* xp4 = reinterpret_cast<uint4*>(x_perm);
+    for (int j = warp; j < kPermChunk; j += kPermThreads / 32) {
+      const int slot = s0 + j;
+      const int pos = pos_buf[j];
+      if (slot >= S || pos < 0) continue;
+      const uint4* src = x4 + (size_t)(slot / K) * d8;
+      uint4* dst = xp4 + (size_t)pos * d8;
+      for (int c = lane; c < d8; c += 32) dst[c] = src[c];
+    }
+  }
+}
+
+cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __half* x, int* offsets, int* perm_src,
+                           int* inv_slot, __half* x_perm, int* hist_ws, cudaStream_t s) {
+  const int S = T * L.K;
+  if (S == 0) {
+    cudaError_t e = cudaMemsetAsync(offsets, 0, sizeof(int) * (L.E + 1), s);
+    return e;
+  }
+  const int nblk = (S + kPermChunk - 1) / kPermChunk;
+  perm_hist_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws);
+  perm_scatter_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws, nblk, offsets, perm_src, inv_slot, x,
+                                                    x_perm);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// weighted combine: y[t] = sum_k w[t,k] y_perm[inv_slot[t*K+k]] (+ y_shared[t])
+// ---------------------------------------------------------------------------
+
+constexpr int kCombThreads = 128;
+
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(DevLayer L, const float* __restrict__ y_perm,
+                                                               const int* __restrict__ inv_slot,
+                                                               const float* __restrict__ w, int T,
+                                                               const float* __restrict__ y_shared,
+                                                               __half* __restrict__ y) {
+  const int t = blockIdx.x;
+  const int d = L.d, K = L.K;
+  const int c4 = blockIdx.y * kCombThreads + threadIdx.x;  // float4 column index
+  if (c4 * 4 >= d) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < K; ++k) {
+    const float wk = w[(size_t)t * K + k];
+    const int slot = inv_slot[(size_t)t * K + k];
+    const float4 v = reinterpret_cast<const float4*>(y_perm + (size_t)slot * d)[c4];
+    acc.x = fmaf(wk, v.x, acc.x);
+    acc.y = fmaf(wk, v.y, acc.y);
+    acc.z = fmaf(wk, v.z, acc.z);
+    acc.w = fmaf(wk, v.w, acc.w);
+  }
+  if (y_shared) {
+    const float4 v = reinterpret_cast<const float4*>(y_shared + (size_t)t * d)[c4];
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+  uint2 out;
+  out.x = *reinterpret_cast<uint32_t*>(&lo);
+  out.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(y + (size_t)t * d)[c4] = out;
+}
+
+cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* inv_slot, const float* w, int T,
+                           const float* y_shared, __half* y, cudaStream_t s) {
+  const dim3 grid(T, (L.d / 4 + kCombThreads - 1) / kCombThreads);
+  combine_kernel<<<grid, kCombThreads, 0, s>>>(L, y_perm, inv_slot, w, T, y_shared, y);
+  return cudaGetLastError();
+}
+
+}  // namespace pw

@@ -1,0 +1,835 @@
+// Host runtime: status codes, the page pool, the per-expert page table, layer
+// lifecycle, bitwidth changes and argument validation for the hot-path calls.
+//
+// PagedWeight (zhichai.net/topic/178446964, "核心洞察") keeps each expert's
+// bit-planes as pages so that precision can be lowered by detaching the low
+// planes; "安全边界与异步搬运" commits changes at a safe boundary.  Here:
+//  * a pool of fixed-size pages carved from one caller-owned device buffer;
+//  * a plane block = plane p of gate/up/down of one expert, paged with no
+//    16-row tile straddling a page; an fp16 block = the expert's fp16 page;
+//  * the device page table holds the page base addresses of every block;
+//  * lowering only rewrites the device bitwidth word (stream ordered) and moves
+//    the freed blocks to a reclaim queue guarded by a CUDA event (the safe
+//    boundary); raising re-maps blocks that are still intact.
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <set>
+#include <vector>
+
+#include "pw_internal.h"
+
+using namespace pw;
+
+struct pw_pool_s;
+struct pw_layer_s;
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+bool g_sim = false;                // host-simulated device (tests without a GPU)
+uint64_t g_sim_issued = 0, g_sim_done = 0;
+
+pw_status cuda_fail(cudaError_t e) {
+  g_last_cuda = (int)e;
+  return PW_ERR_CUDA;
+}
+
+#define PW_CUDA(call)                                  \
+  do {                                                 \
+    cudaError_t _e = (call);                           \
+    if (_e != cudaSuccess) return cuda_fail(_e);       \
+  } while (0)
+
+#define PW_TRY(call)                                   \
+  do {                                                 \
+    pw_status _s = (call);                             \
+    if (_s != PW_OK) return _s;                        \
+  } while (0)
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+pw_status dev_h2d(void* dst, const void* src, size_t n, cudaStream_t s) {
+  if (n == 0) return PW_OK;
+  if (g_sim) {
+    memcpy(dst, src, n);
+    return PW_OK;
+  }
+  PW_CUDA(cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s));
+  return PW_OK;
+}
+
+pw_status dev_zero(void* dst, size_t n, cudaStream_t s) {
+  if (n == 0) return PW_OK;
+  if (g_sim) {
+    memset(dst, 0, n);
+    return PW_OK;
+  }
+  PW_CUDA(cudaMemsetAsync(dst, 0, n, s));
+  return PW_OK;
+}
+
+pw_status dev_sync(cudaStream_t s) {
+  if (g_sim) return PW_OK;
+  PW_CUDA(cudaStreamSynchronize(s));
+  return PW_OK;
+}
+
+// The safe boundary of one bitwidth change.
+struct Event {
+  cudaEvent_t ev = nullptr;
+  uint64_t seq = 0;
+  ~Event() {
+    if (ev) cudaEventDestroy(ev);
+  }
+  bool done() const {
+    if (g_sim) return seq <= g_sim_done;
+    return cudaEventQuery(ev) == cudaSuccess;
+  }
+  void wait() const {
+    if (!g_sim) cudaEventSynchronize(ev);
+  }
+};
+
+pw_status make_event(cudaStream_t s, std::shared_ptr<Event>* out) {
+  auto ev = std::make_shared<Event>();
+  if (g_sim) {
+    ev->seq = ++g_sim_issued;
+  } else {
+    PW_CUDA(cudaEventCreateWithFlags(&ev->ev, cudaEventDisableTiming));
+    cudaError_t e = cudaEventRecord(ev->ev, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  *out = ev;
+  return PW_OK;
+}
+
+enum BlockState { B_NONE = 0, B_MAPPED = 1, B_RECLAIM = 2 };
+
+struct Block {
+  BlockState st = B_NONE;
+  std::vector<int> pages;         // physical page ids, indexed by virtual page
+  std::shared_ptr<Event> ev;      // set while reclaimable
+  uint64_t fifo_key = 0;
+};
+
+}  // namespace
+
+struct pw_pool_s {
+  char* base = nullptr;
+  size_t bytes = 0, page_bytes = 0, npages = 0;
+  std::set<int> free_pages;                 // ordered: paged blocks take the lowest ids
+  std::vector<uint8_t> kind;                // 0 free, 1 paged, 2 resident
+  std::map<uint64_t, Block*> reclaim;       // oldest first
+  uint64_t fifo_counter = 0;
+  size_t mapped_pages = 0, reclaim_pages = 0, resident_bytes = 0;
+  int n_layers = 0;
+
+  char* page_addr(int p) const { return base + (size_t)p * page_bytes; }
+
+  void to_reclaim(Block& b, std::shared_ptr<Event> ev) {
+    b.st = B_RECLAIM;
+    b.ev = std::move(ev);
+    b.fifo_key = ++fifo_counter;
+    reclaim[b.fifo_key] = &b;
+    mapped_pages -= b.pages.size();
+    reclaim_pages += b.pages.size();
+  }
+  void remap(Block& b) {  // reclaimable -> mapped (raise)
+    reclaim.erase(b.fifo_key);
+    b.ev.reset();
+    b.st = B_MAPPED;
+    reclaim_pages -= b.pages.size();
+    mapped_pages += b.pages.size();
+  }
+  void release(Block& b) {  // any state -> none, pages back to the free set
+    if (b.st == B_RECLAIM) {
+      reclaim.erase(b.fifo_key);
+      reclaim_pages -= b.pages.size();
+    } else if (b.st == B_MAPPED) {
+      mapped_pages -= b.pages.size();
+    }
+    for (int p : b.pages) {
+      kind[p] = 0;
+      free_pages.insert(p);
+    }
+    b.pages.clear();
+    b.ev.reset();
+    b.st = B_NONE;
+  }
+  // Take n pages for a new mapped block.  Reclaimable blocks are given up
+  // oldest first, and only once their safe-boundary event has completed
+  // (waited for on a real device; in host-sim mode pending ones are skipped).
+  pw_status take_pages(size_t n, std::vector<int>* out) {
+    size_t avail = free_pages.size();
+    for (auto& kv : reclaim)
+      if (!g_sim || kv.second->ev->done()) avail += kv.second->pages.size();
+    if (avail < n) return PW_ERR_OOM;
+    while (free_pages.size() < n) {
+      Block* victim = nullptr;
+      for (auto& kv : reclaim)
+        if (!g_sim || kv.second->ev->done()) {
+          victim = kv.second;
+          break;
+        }
+      if (!victim) return PW_ERR_OOM;
+      victim->ev->wait();
+      release(*victim);
+    }
+    out->clear();
+    for (size_t i = 0; i < n; ++i) {
+      int p = *free_pages.begin();
+      free_pages.erase(free_pages.begin());
+      kind[p] = 1;
+      out->push_back(p);
+    }
+    mapped_pages += n;
+    return PW_OK;
+  }
+  // n contiguous pages from the top of the buffer for resident data.
+  int take_resident(size_t n) {
+    if (n == 0 || n > npages) return -1;
+    for (long top = (long)npages - 1; top >= (long)n - 1; --top) {
+      bool ok = true;
+      for (long i = top; i > top - (long)n; --i)
+        if (kind[i] != 0) {
+          ok = false;
+          top = i;  // skip past the occupied page
+          break;
+        }
+      if (ok) {
+        int first = (int)(top - (long)n + 1);
+        for (size_t i = 0; i < n; ++i) {
+          kind[first + i] = 2;
+          free_pages.erase(first + (int)i);
+        }
+        resident_bytes += n * page_bytes;
+        return first;
+      }
+    }
+    return -1;
+  }
+  void give_back_resident(int first, size_t n) {
+    for (size_t i = 0; i < n; ++i) {
+      kind[first + i] = 0;
+      free_pages.insert(first + (int)i);
+    }
+    resident_bytes -= n * page_bytes;
+  }
+};
+
+struct pw_layer_s {
+  pw_pool_s* pool = nullptr;
+  pw_layer_desc desc{};
+  int R[3], C[3];
+  int tmax = 0, pmax = 0, pmax16 = 0;
+  std::vector<uint2> tmap, tmap16;           // [3][tmax]
+  size_t lut_block_bytes = 0;
+  unsigned lut_off[3][4];
+  int res_first = -1;
+  size_t res_npages = 0;
+  char* res_base = nullptr;
+  // device tables (inside the resident run)
+  int* d_bits = nullptr;
+  int* d_err = nullptr;
+  unsigned long long* d_plane_pt = nullptr;
+  unsigned long long* d_f16_pt = nullptr;
+  uint2* d_tmap = nullptr;
+  uint2* d_tmap16 = nullptr;
+  unsigned long long* d_lut_base = nullptr;
+  char* d_luts = nullptr;
+  __half* d_shared[3] = {nullptr, nullptr, nullptr};
+  // host mirrors
+  std::vector<int> bits;                     // 0 = not loaded
+  std::vector<Block> planes;                 // [E][6]
+  std::vector<Block> f16;                    // [E]
+  std::vector<unsigned long long> h_plane_pt, h_f16_pt;
+  bool shared_loaded = false;
+
+  Block& plane(int e, int p) { return planes[(size_t)e * kPlanes + p]; }
+
+  DevLayer dev() const {
+    DevLayer L{};
+    L.d = desc.d;
+    L.f = desc.ffn;
+    L.E = desc.n_experts;
+    L.K = desc.top_k;
+    L.renorm = desc.renormalize;
+    L.fs = desc.shared_ffn;
+    L.pmax = pmax;
+    L.pmax16 = pmax16;
+    L.tmax = tmax;
+    L.bits = d_bits;
+    L.plane_pt = d_plane_pt;
+    L.f16_pt = d_f16_pt;
+    L.tmap = d_tmap;
+    L.tmap16 = d_tmap16;
+    L.lut_base = d_lut_base;
+    memcpy(L.lut_off, lut_off, sizeof(lut_off));
+    for (int m = 0; m < 3; ++m) L.shared16[m] = shared_loaded ? d_shared[m] : nullptr;
+    L.err = d_err;
+    return L;
+  }
+};
+
+namespace {
+
+// Lay tiles of the three matrices one after another into virtual pages, never
+// letting a tile straddle a page.  Returns the number of virtual pages used.
+int build_tile_map(const int R[3], const int C[3], size_t tile_bytes_per_col, size_t page_bytes,
+                   int tmax, std::vector<uint2>* map) {
+  map->assign((size_t)3 * tmax, make_uint2(0, 0));
+  size_t vpage = 0, off = 0;
+  for (int m = 0; m < 3; ++m) {
+    const size_t tb = tile_bytes_per_col * (size_t)C[m];
+    if (tb > page_bytes) return -1;
+    for (int tau = 0; tau < R[m] / kTileRows; ++tau) {
+      if (off + tb > page_bytes) {
+        ++vpage;
+        off = 0;
+      }
+      (*map)[(size_t)m * tmax + tau] = make_uint2((unsigned)vpage, (unsigned)off);
+      off += tb;
+    }
+  }
+  return (int)vpage + 1;
+}
+
+bool valid_bits(int b) { return b == 3 || b == 4 || b == 5 || b == 6 || b == 16; }
+
+pw_status check_layer(pw_layer_t l) { return l ? PW_OK : PW_ERR_INVALID_ARG; }
+
+pw_status write_bits(pw_layer_t l, int e, int b, cudaStream_t s) {
+  if (g_sim) {
+    l->d_bits[e] = b;
+    return PW_OK;
+  }
+  PW_CUDA(launch_set_bits(l->d_bits, e, b, s));
+  return PW_OK;
+}
+
+pw_status upload_pt_rows(pw_layer_t l, int e, cudaStream_t s) {
+  const size_t prow = (size_t)kPlanes * l->pmax;
+  PW_TRY(dev_h2d(l->d_plane_pt + (size_t)e * prow, l->h_plane_pt.data() + (size_t)e * prow,
+                 prow * sizeof(unsigned long long), s));
+  PW_TRY(dev_h2d(l->d_f16_pt + (size_t)e * l->pmax16, l->h_f16_pt.data() + (size_t)e * l->pmax16,
+                 (size_t)l->pmax16 * sizeof(unsigned long long), s));
+  return PW_OK;
+}
+
+// Copy a block image (virtual pages) page by page to its physical pages.
+pw_status upload_block(pw_layer_t l, const Block& b, const std::vector<char>& img, cudaStream_t s) {
+  const size_t pb = l->pool->page_bytes;
+  for (size_t v = 0; v < b.pages.size(); ++v) {
+    const size_t n = std::min(pb, img.size() - v * pb);
+    PW_TRY(dev_h2d(l->pool->page_addr(b.pages[v]), img.data() + v * pb, n, s));
+  }
+  return PW_OK;
+}
+
+void release_expert(pw_layer_t l, int e) {
+  for (int p = 0; p < kPlanes; ++p) l->pool->release(l->plane(e, p));
+  l->pool->release(l->f16[e]);
+  l->bits[e] = 0;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// status
+// ---------------------------------------------------------------------------
+
+extern "C" const char* pw_status_str(pw_status s) {
+  switch (s) {
+    case PW_OK: return "PW_OK";
+    case PW_ERR_INVALID_ARG: return "PW_ERR_INVALID_ARG";
+    case PW_ERR_UNSUPPORTED: return "PW_ERR_UNSUPPORTED";
+    case PW_ERR_OOM: return "PW_ERR_OOM";
+    case PW_ERR_NOT_RESIDENT: return "PW_ERR_NOT_RESIDENT";
+    case PW_ERR_CUDA: return "PW_ERR_CUDA";
+    case PW_ERR_TIMEOUT: return "PW_ERR_TIMEOUT";
+    case PW_ERR_DEVICE_CHECK: return "PW_ERR_DEVICE_CHECK";
+  }
+  return "PW_ERR_UNKNOWN";
+}
+
+extern "C" pw_status pw_last_cuda_error(int* cuda_err) {
+  if (!cuda_err) return PW_ERR_INVALID_ARG;
+  *cuda_err = g_last_cuda;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_testing_host_sim(int enable) {
+  g_sim = enable != 0;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_testing_complete_events(void) {
+  g_sim_done = g_sim_issued;
+  return PW_OK;
+}
+
+// ---------------------------------------------------------------------------
+// pool
+// ---------------------------------------------------------------------------
+
+extern "C" pw_status pw_pool_create(void* dev_base, size_t bytes, size_t page_bytes, pw_pool_t* out) {
+  if (!dev_base || !out || (reinterpret_cast<uintptr_t>(dev_base) & 255)) return PW_ERR_INVALID_ARG;
+  if (page_bytes < (64u << 10) || page_bytes % (64u << 10)) return PW_ERR_INVALID_ARG;
+  if (bytes < page_bytes) return PW_ERR_OOM;
+  auto* p = new pw_pool_s();
+  p->base = static_cast<char*>(dev_base);
+  p->bytes = bytes;
+  p->page_bytes = page_bytes;
+  p->npages = bytes / page_bytes;
+  p->kind.assign(p->npages, 0);
+  for (size_t i = 0; i < p->npages; ++i) p->free_pages.insert((int)i);
+  *out = p;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_pool_destroy(pw_pool_t pool) {
+  if (!pool) return PW_ERR_INVALID_ARG;
+  if (pool->n_layers) return PW_ERR_INVALID_ARG;
+  delete pool;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_pool_get_stats(pw_pool_t pool, pw_pool_stats* out) {
+  if (!pool || !out) return PW_ERR_INVALID_ARG;
+  out->total_pages = pool->npages;
+  out->free_pages = pool->free_pages.size();
+  out->mapped_pages = pool->mapped_pages;
+  out->reclaimable_pages = pool->reclaim_pages;
+  out->resident_bytes = pool->resident_bytes;
+  out->page_bytes = pool->page_bytes;
+  return PW_OK;
+}
+
+// ---------------------------------------------------------------------------
+// layer lifecycle
+// ---------------------------------------------------------------------------
+
+extern "C" pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, pw_layer_t* out) {
+  if (!pool || !desc || !out) return PW_ERR_INVALID_ARG;
+  const pw_layer_desc& D = *desc;
+  if (D.d <= 0 || D.ffn <= 0 || D.d % 64 || D.ffn % 64) return PW_ERR_INVALID_ARG;
+  if (D.n_experts < 1 || D.n_experts > kMaxExperts) return PW_ERR_INVALID_ARG;
+  if (D.top_k < 1 || D.top_k > kMaxTopK || D.top_k > D.n_experts) return PW_ERR_INVALID_ARG;
+  if (D.renormalize != 0 && D.renormalize != 1) return PW_ERR_INVALID_ARG;
+  if (D.shared_ffn < 0 || D.shared_ffn % 64) return PW_ERR_INVALID_ARG;
+  if (D.d > 16384 || D.ffn > 32768 || D.shared_ffn > 32768) return PW_ERR_UNSUPPORTED;
+
+  auto l = std::make_unique<pw_layer_s>();
+  l->pool = pool;
+  l->desc = D;
+  const int E = D.n_experts;
+  l->R[0] = l->R[1] = D.ffn;
+  l->C[0] = l->C[1] = D.d;
+  l->R[2] = D.d;
+  l->C[2] = D.ffn;
+  l->tmax = std::max(D.ffn, D.d) / kTileRows;
+  l->pmax = build_tile_map(l->R, l->C, 2, pool->page_bytes, l->tmax, &l->tmap);
+  l->pmax16 = build_tile_map(l->R, l->C, 32, pool->page_bytes, l->tmax, &l->tmap16);
+  if (l->pmax < 0 || l->pmax16 < 0) return PW_ERR_UNSUPPORTED;  // page too small for one tile
+
+  size_t lb = 0;
+  for (int m = 0; m < 3; ++m)
+    for (int i = 0; i < 4; ++i) {
+      l->lut_off[m][i] = (unsigned)lb;
+      lb += (size_t)l->R[m] * (1u << (i + 3)) * 2;
+    }
+  l->lut_block_bytes = align_up(lb, 256);
+
+  // resident run: small tables, LUT blocks, shared FFN
+  size_t off = 0;
+  auto carve = [&](size_t n) {
+    size_t o = off;
+    off = align_up(off + n, 256);
+    return o;
+  };
+  const size_t o_bits = carve(sizeof(int) * E);
+  const size_t o_err = carve(16);
+  const size_t o_ppt = carve(sizeof(unsigned long long) * (size_t)E * kPlanes * l->pmax);
+  const size_t o_fpt = carve(sizeof(unsigned long long) * (size_t)E * l->pmax16);
+  const size_t o_tmap = carve(sizeof(uint2) * 3 * (size_t)l->tmax);
+  const size_t o_tmap16 = carve(sizeof(uint2) * 3 * (size_t)l->tmax);
+  const size_t o_lutb = carve(sizeof(unsigned long long) * E);
+  const size_t o_luts = carve(l->lut_block_bytes * E);
+  size_t o_sh[3] = {0, 0, 0};
+  if (D.shared_ffn) {
+    o_sh[0] = carve((size_t)D.shared_ffn * D.d * 2);
+    o_sh[1] = carve((size_t)D.shared_ffn * D.d * 2);
+    o_sh[2] = carve((size_t)D.d * D.shared_ffn * 2);
+  }
+  l->res_npages = (off + pool->page_bytes - 1) / pool->page_bytes;
+  l->res_first = pool->take_resident(l->res_npages);
+  if (l->res_first < 0) return PW_ERR_OOM;
+  l->res_base = pool->page_addr(l->res_first);
+  char* rb = l->res_base;
+  l->d_bits = reinterpret_cast<int*>(rb + o_bits);
+  l->d_err = reinterpret_cast<int*>(rb + o_err);
+  l->d_plane_pt = reinterpret_cast<unsigned long long*>(rb + o_ppt);
+  l->d_f16_pt = reinterpret_cast<unsigned long long*>(rb + o_fpt);
+  l->d_tmap = reinterpret_cast<uint2*>(rb + o_tmap);
+  l->d_tmap16 = reinterpret_cast<uint2*>(rb + o_tmap16);
+  l->d_lut_base = reinterpret_cast<unsigned long long*>(rb + o_lutb);
+  l->d_luts = rb + o_luts;
+  for (int m = 0; m < 3; ++m) l->d_shared[m] = D.shared_ffn ? reinterpret_cast<__half*>(rb + o_sh[m]) : nullptr;
+
+  l->bits.assign(E, 0);
+  l->planes.resize((size_t)E * kPlanes);
+  l->f16.resize(E);
+  l->h_plane_pt.assign((size_t)E * kPlanes * l->pmax, 0ull);
+  l->h_f16_pt.assign((size_t)E * l->pmax16, 0ull);
+  std::vector<unsigned long long> lutb(E);
+  for (int e = 0; e < E; ++e)
+    lutb[e] = reinterpret_cast<unsigned long long>(l->d_luts + (size_t)e * l->lut_block_bytes);
+
+  cudaStream_t s = nullptr;
+  pw_status st = PW_OK;
+  if (st == PW_OK) st = dev_zero(rb, o_ppt, s);  // bits + error word
+  if (st == PW_OK) st = dev_zero(l->d_plane_pt, (o_tmap - o_ppt), s);
+  if (st == PW_OK) st = dev_h2d(l->d_tmap, l->tmap.data(), sizeof(uint2) * l->tmap.size(), s);
+  if (st == PW_OK) st = dev_h2d(l->d_tmap16, l->tmap16.data(), sizeof(uint2) * l->tmap16.size(), s);
+  if (st == PW_OK) st = dev_h2d(l->d_lut_base, lutb.data(), sizeof(unsigned long long) * E, s);
+  if (st == PW_OK) st = dev_sync(s);
+  if (st != PW_OK) {
+    pool->give_back_resident(l->res_first, l->res_npages);
+    return st;
+  }
+  pool->n_layers++;
+  *out = l.release();
+  return PW_OK;
+}
+
+extern "C" pw_status pw_layer_destroy(pw_layer_t l) {
+  PW_TRY(check_layer(l));
+  if (!g_sim) cudaDeviceSynchronize();
+  for (int e = 0; e < l->desc.n_experts; ++e) release_expert(l, e);
+  l->pool->give_back_resident(l->res_first, l->res_npages);
+  l->pool->n_layers--;
+  delete l;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_layer_load_expert(pw_layer_t l, int e, int bits, const uint8_t* const code6[3],
+                                          const uint16_t* const lut[3][4], const uint16_t* const w16[3],
+                                          void* stream) {
+  PW_TRY(check_layer(l));
+  if (e < 0 || e >= l->desc.n_experts || !valid_bits(bits) || !code6 || !lut) return PW_ERR_INVALID_ARG;
+  for (int m = 0; m < 3; ++m) {
+    if (!code6[m]) return PW_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+      if (!lut[m][i]) return PW_ERR_INVALID_ARG;
+    if (bits == 16 && (!w16 || !w16[m])) return PW_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = as_stream(stream);
+  pw_pool_s* pool = l->pool;
+  // kernels still reading the old pages must finish before they are reused
+  PW_TRY(dev_sync(s));
+  release_expert(l, e);
+
+  const int np = bits == 16 ? kPlanes : bits;
+  std::vector<std::vector<int>> pages(np + 1);
+  for (int p = 0; p < np; ++p) {
+    pw_status st = pool->take_pages(l->pmax, &pages[p]);
+    if (st != PW_OK) {
+      for (int q = 0; q < p; ++q)
+        for (int pg : pages[q]) {
+          pool->kind[pg] = 0;
+          pool->free_pages.insert(pg);
+          pool->mapped_pages--;
+        }
+      return st;
+    }
+  }
+  if (bits == 16) {
+    pw_status st = pool->take_pages(l->pmax16, &pages[np]);
+    if (st != PW_OK) {
+      for (int q = 0; q < np; ++q)
+        for (int pg : pages[q]) {
+          pool->kind[pg] = 0;
+          pool->free_pages.insert(pg);
+          pool->mapped_pages--;
+        }
+      return st;
+    }
+  }
+
+  // pack and upload planes
+  const size_t pb = pool->page_bytes;
+  std::vector<std::vector<char>> img(np, std::vector<char>((size_t)l->pmax * pb, 0));
+  for (int m = 0; m < 3; ++m) {
+    const int R = l->R[m], C = l->C[m];
+    const size_t nw = (size_t)R * C / 32;
+    std::vector<uint32_t> packed((size_t)kPlanes * nw);
+    uint32_t* outs[6];
+    for (int p = 0; p < 6; ++p) outs[p] = packed.data() + p * nw;
+    PW_TRY(pw_pack_planes(code6[m], R, C, outs));
+    const size_t tb = 2 * (size_t)C;  // bytes of one 16-row tile of one plane
+    for (int tau = 0; tau < R / kTileRows; ++tau) {
+      const uint2 loc = l->tmap[(size_t)m * l->tmax + tau];
+      for (int p = 0; p < np; ++p)
+        memcpy(img[p].data() + (size_t)loc.x * pb + loc.y, outs[p] + (size_t)tau * (tb / 4), tb);
+    }
+  }
+  for (int p = 0; p < np; ++p) {
+    Block& b = l->plane(e, p);
+    b.pages = pages[p];
+    b.st = B_MAPPED;
+    PW_TRY(upload_block(l, b, img[p], s));
+    for (int v = 0; v < l->pmax; ++v)
+      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] =
+          reinterpret_cast<unsigned long long>(pool->page_addr(b.pages[v]));
+  }
+  img.clear();
+  if (bits == 16) {
+    std::vector<char> im((size_t)l->pmax16 * pb, 0);
+    for (int m = 0; m < 3; ++m) {
+      const int R = l->R[m], C = l->C[m];
+      std::vector<uint16_t> packed((size_t)R * C);
+      PW_TRY(pw_pack_f16(w16[m], R, C, packed.data()));
+      const size_t tb = 32 * (size_t)C;
+      for (int tau = 0; tau < R / kTileRows; ++tau) {
+        const uint2 loc = l->tmap16[(size_t)m * l->tmax + tau];
+        memcpy(im.data() + (size_t)loc.x * pb + loc.y, packed.data() + (size_t)tau * (tb / 2), tb);
+      }
+    }
+    Block& b = l->f16[e];
+    b.pages = pages[np];
+    b.st = B_MAPPED;
+    PW_TRY(upload_block(l, b, im, s));
+    for (int v = 0; v < l->pmax16; ++v)
+      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(pool->page_addr(b.pages[v]));
+  }
+  // LUTs (all four bitwidths stay resident)
+  char* lb = l->d_luts + (size_t)e * l->lut_block_bytes;
+  for (int m = 0; m < 3; ++m)
+    for (int i = 0; i < 4; ++i)
+      PW_TRY(dev_h2d(lb + l->lut_off[m][i], lut[m][i], (size_t)l->R[m] * (1u << (i + 3)) * 2, s));
+  PW_TRY(upload_pt_rows(l, e, s));
+  PW_TRY(write_bits(l, e, bits, s));
+  PW_TRY(dev_sync(s));
+  l->bits[e] = bits;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_layer_load_shared(pw_layer_t l, const uint16_t* const w16[3], void* stream) {
+  PW_TRY(check_layer(l));
+  if (l->desc.shared_ffn == 0) return PW_ERR_INVALID_ARG;
+  if (!w16 || !w16[0] || !w16[1] || !w16[2]) return PW_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  const int d = l->desc.d, fs = l->desc.shared_ffn;
+  const int R[3] = {fs, fs, d}, C[3] = {d, d, fs};
+  for (int m = 0; m < 3; ++m) {
+    std::vector<uint16_t> packed((size_t)R[m] * C[m]);
+    PW_TRY(pw_pack_f16(w16[m], R[m], C[m], packed.data()));
+    PW_TRY(dev_h2d(l->d_shared[m], packed.data(), packed.size() * 2, s));
+    PW_TRY(dev_sync(s));
+  }
+  l->shared_loaded = true;
+  return PW_OK;
+}
+
+// ---------------------------------------------------------------------------
+// bitwidth changes (the paging mechanism)
+// ---------------------------------------------------------------------------
+
+extern "C" pw_status pw_set_expert_bitwidth(pw_layer_t l, int e, int bits, void* stream) {
+  PW_TRY(check_layer(l));
+  if (e < 0 || e >= l->desc.n_experts || !valid_bits(bits)) return PW_ERR_INVALID_ARG;
+  const int cur = l->bits[e];
+  if (cur == 0) return PW_ERR_INVALID_ARG;  // never loaded
+  if (cur == bits) return PW_OK;
+  const int need = bits == 16 ? kPlanes : bits;
+  // every block the new bitwidth reads must still hold its data
+  for (int p = 0; p < need; ++p)
+    if (l->plane(e, p).st == B_NONE) return PW_ERR_NOT_RESIDENT;
+  if (bits == 16 && l->f16[e].st == B_NONE) return PW_ERR_NOT_RESIDENT;
+
+  cudaStream_t s = as_stream(stream);
+  PW_TRY(write_bits(l, e, bits, s));
+  // raise: re-map still-intact blocks (their page-table entries never changed)
+  for (int p = 0; p < need; ++p)
+    if (l->plane(e, p).st == B_RECLAIM) l->pool->remap(l->plane(e, p));
+  if (bits == 16 && l->f16[e].st == B_RECLAIM) l->pool->remap(l->f16[e]);
+  // lower: blocks no longer read become reclaimable after the safe boundary
+  std::vector<Block*> drop;
+  for (int p = need; p < kPlanes; ++p)
+    if (l->plane(e, p).st == B_MAPPED) drop.push_back(&l->plane(e, p));
+  if (bits != 16 && l->f16[e].st == B_MAPPED) drop.push_back(&l->f16[e]);
+  if (!drop.empty()) {
+    std::shared_ptr<Event> ev;
+    PW_TRY(make_event(s, &ev));
+    for (Block* b : drop) l->pool->to_reclaim(*b, ev);
+  }
+  l->bits[e] = bits;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_get_expert_bitwidth(pw_layer_t l, int e, int* bits) {
+  PW_TRY(check_layer(l));
+  if (!bits || e < 0 || e >= l->desc.n_experts) return PW_ERR_INVALID_ARG;
+  *bits = l->bits[e];
+  return PW_OK;
+}
+
+// ---------------------------------------------------------------------------
+// workspace and hot-path entry points
+// ---------------------------------------------------------------------------
+
+namespace {
+
+struct WsLayout {
+  size_t perm_off, perm_bytes, h_off, h_bytes, hs_off, hs_bytes, total;
+};
+
+WsLayout ws_layout(const pw_layer_s* l, int T) {
+  WsLayout w{};
+  const size_t S = (size_t)T * l->desc.top_k;
+  w.perm_off = 0;
+  w.perm_bytes = align_up(permute_ws_bytes((int)S, l->desc.n_experts), 256);
+  w.h_off = w.perm_off + w.perm_bytes;
+  w.h_bytes = align_up(S * l->desc.ffn * 2, 256);
+  w.hs_off = w.h_off + w.h_bytes;
+  w.hs_bytes = align_up((size_t)T * l->desc.shared_ffn * 2, 256);
+  w.total = w.hs_off + w.hs_bytes;
+  return w;
+}
+
+pw_status device_only() { return g_sim ? PW_ERR_UNSUPPORTED : PW_OK; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+pw_status all_loaded(const pw_layer_s* l) {
+  for (int b : l->bits)
+    if (b == 0) return PW_ERR_INVALID_ARG;
+  return PW_OK;
+}
+
+pw_status launched(cudaError_t e) { return e == cudaSuccess ? PW_OK : cuda_fail(e); }
+
+}  // namespace
+
+extern "C" pw_status pw_workspace_size(pw_layer_t l, int T, size_t* bytes) {
+  PW_TRY(check_layer(l));
+  if (T < 0 || !bytes) return PW_ERR_INVALID_ARG;
+  *bytes = ws_layout(l, T).total;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_route_topk(pw_layer_t l, const void* x, const void* wr, const float* bias, int T,
+                                   int32_t* idx, float* w, int32_t* expert_count, void* stream) {
+  PW_TRY(check_layer(l));
+  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !wr || !idx || !w)) return PW_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || !aligned16(wr))) return PW_ERR_INVALID_ARG;
+  PW_TRY(device_only());
+  if (T == 0) return PW_OK;
+  return launched(launch_route(l->dev(), static_cast<const __half*>(x), static_cast<const __half*>(wr), bias, T,
+                               idx, w, expert_count, as_stream(stream)));
+}
+
+extern "C" pw_status pw_permute(pw_layer_t l, const int32_t* idx, int T, const void* x, int32_t* offsets,
+                                int32_t* perm_src, int32_t* inv_slot, void* x_perm, void* ws, size_t ws_bytes,
+                                void* stream) {
+  PW_TRY(check_layer(l));
+  if (T < 0 || !offsets) return PW_ERR_INVALID_ARG;
+  if (T > 0 && (!idx || !perm_src || !inv_slot || !ws)) return PW_ERR_INVALID_ARG;
+  if ((x == nullptr) != (x_perm == nullptr)) return PW_ERR_INVALID_ARG;
+  if (x && (!aligned16(x) || !aligned16(x_perm))) return PW_ERR_INVALID_ARG;
+  const WsLayout W = ws_layout(l, T);
+  if (T > 0 && ws_bytes < W.perm_off + W.perm_bytes) return PW_ERR_OOM;
+  PW_TRY(device_only());
+  char* wsb = static_cast<char*>(ws);
+  return launched(launch_permute(l->dev(), idx, T, static_cast<const __half*>(x), offsets, perm_src, inv_slot,
+                                 static_cast<__half*>(x_perm), reinterpret_cast<int*>(wsb + W.perm_off),
+                                 as_stream(stream)));
+}
+
+extern "C" pw_status pw_expert_ffn_bitplane(pw_layer_t l, const void* x_perm, const int32_t* offsets, int T,
+                                            float* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  PW_TRY(check_layer(l));
+  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (T == 0) return device_only();
+  if (!x_perm || !offsets || !y_perm || !ws) return PW_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(y_perm)) return PW_ERR_INVALID_ARG;
+  const WsLayout W = ws_layout(l, T);
+  if (ws_bytes < W.h_off + W.h_bytes) return PW_ERR_OOM;
+  PW_TRY(all_loaded(l));
+  PW_TRY(device_only());
+  char* wsb = static_cast<char*>(ws);
+  return launched(launch_ffn(l->dev(), 0, static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
+                             reinterpret_cast<__half*>(wsb + W.h_off), as_stream(stream)));
+}
+
+extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_shared, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  PW_TRY(check_layer(l));
+  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (l->desc.shared_ffn == 0 || !l->shared_loaded) return PW_ERR_INVALID_ARG;
+  if (T == 0) return device_only();
+  if (!x || !y_shared || !ws || !aligned16(x) || !aligned16(y_shared)) return PW_ERR_INVALID_ARG;
+  const WsLayout W = ws_layout(l, T);
+  if (ws_bytes < W.total) return PW_ERR_OOM;
+  PW_TRY(device_only());
+  char* wsb = static_cast<char*>(ws);
+  return launched(launch_ffn(l->dev(), 1, static_cast<const __half*>(x), nullptr, T, y_shared,
+                             reinterpret_cast<__half*>(wsb + W.hs_off), as_stream(stream)));
+}
+
+extern "C" pw_status pw_combine(pw_layer_t l, const float* y_perm, const int32_t* inv_slot, const float* w, int T,
+                                const float* y_shared, void* y, void* stream) {
+  PW_TRY(check_layer(l));
+  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (T > 0 && (!y_perm || !inv_slot || !w || !y)) return PW_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared))))
+    return PW_ERR_INVALID_ARG;
+  PW_TRY(device_only());
+  if (T == 0) return PW_OK;
+  return launched(launch_combine(l->dev(), y_perm, inv_slot, w, T, y_shared, static_cast<__half*>(y),
+                                 as_stream(stream)));
+}
+
+extern "C" pw_status pw_layer_check_device(pw_layer_t l, void* stream) {
+  PW_TRY(check_layer(l));
+  int err[4] = {0, 0, 0, 0};
+  if (g_sim) {
+    memcpy(err, l->d_err, sizeof(err));
+    memset(l->d_err, 0, sizeof(err));
+  } else {
+    cudaStream_t s = as_stream(stream);
+    PW_CUDA(cudaMemcpyAsync(err, l->d_err, sizeof(err), cudaMemcpyDeviceToHost, s));
+    PW_CUDA(cudaStreamSynchronize(s));
+    PW_CUDA(cudaMemsetAsync(l->d_err, 0, sizeof(err), s));
+    PW_CUDA(cudaStreamSynchronize(s));
+  }
+  if (err[0] == 1) return PW_ERR_TIMEOUT;
+  if (err[0] != 0) return PW_ERR_DEVICE_CHECK;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_debug_dequant(pw_layer_t l, int e, int m, void* out, void* stream) {
+  PW_TRY(check_layer(l));
+  if (e < 0 || e >= l->desc.n_experts || m < 0 || m > 2 || !out) return PW_ERR_INVALID_ARG;
+  if (l->bits[e] == 0) return PW_ERR_INVALID_ARG;
+  PW_TRY(device_only());
+  return launched(launch_debug_dequant(l->dev(), e, m, static_cast<__half*>(out), as_stream(stream)));
+}
+
+extern "C" pw_status pw_debug_page_address(pw_layer_t l, int e, int p, int vpage, uint64_t* addr) {
+  PW_TRY(check_layer(l));
+  if (!addr || e < 0 || e >= l->desc.n_experts || p < 0 || p > kPlanes || vpage < 0) return PW_ERR_INVALID_ARG;
+  const Block& b = p < kPlanes ? l->planes[(size_t)e * kPlanes + p] : l->f16[e];
+  if (b.st == B_NONE || vpage >= (int)b.pages.size()) {
+    *addr = 0;
+    return PW_OK;
+  }
+  *addr = reinterpret_cast<uint64_t>(l->pool->page_addr(b.pages[vpage]));
+  return PW_OK;
+}

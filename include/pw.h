@@ -1,0 +1,253 @@
+/*
+ * pw.h - C ABI of the GB300 routed any-precision MoE expert layer.
+ *
+ * The method: PagedWeight (Yang, Zhao, Dasgupta, Misailovic; write-up at
+ * zhichai.net/topic/178446964).  Section "核心洞察" of that page: every expert
+ * weight is an any-precision code kept as bit-planes plus a lookup table
+ * (LUT), switchable among 3, 4, 5, 6 bits or a 16-bit fallback, and the planes
+ * are managed like pages so that an expert's precision can be lowered by
+ * detaching planes.  Section "安全边界与异步搬运": changes commit at a "safe
+ * boundary".  The second write-up (time-frame.cloud, "方法与技术路线") adds a
+ * "virtual page table" through which kernels read the weights.
+ *
+ * This header exposes one MoE layer's hot path on one GPU:
+ *   pw_route_topk -> pw_permute -> pw_expert_ffn_bitplane (+ pw_shared_ffn)
+ *   -> pw_combine,   and   pw_set_expert_bitwidth.
+ *
+ * Conventions for every function
+ *  - Return value: pw_status.  Arguments are validated on the host before any
+ *    work is enqueued; a failed check has no side effects.
+ *  - "device" pointers are CUDA device memory owned by the caller (e.g. torch
+ *    tensors); "host" pointers are ordinary host memory owned by the caller.
+ *    The library never allocates device memory: weights, LUTs and its small
+ *    tables live in a pool carved from a caller-provided device buffer.
+ *  - Hot-path calls are asynchronous on the given stream (a cudaStream_t passed
+ *    as void*, NULL = legacy default stream) and never synchronise it.
+ *  - Matrices are row-major and "out x in": gate [ffn][d], up [ffn][d],
+ *    down [d][ffn]; a row is an output channel.
+ *  - fp16 data is passed as raw IEEE binary16 (uint16_t / void*).
+ *  - Shapes: d and ffn (and shared_ffn) must be multiples of 64, n_experts in
+ *    [1, 256], top_k in [1, min(8, n_experts)].
+ *  - A layer handle is not thread-safe: use one host thread per handle.
+ */
+#ifndef PW_H
+#define PW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PW_OK = 0,
+  PW_ERR_INVALID_ARG = 1,   /* bad pointer, size, index or bitwidth */
+  PW_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve (shape, mode) */
+  PW_ERR_OOM = 3,           /* pool or workspace too small */
+  PW_ERR_NOT_RESIDENT = 4,  /* raising precision needs planes no longer in the pool */
+  PW_ERR_CUDA = 5,          /* a CUDA call failed; see pw_last_cuda_error */
+  PW_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up (device error word) */
+  PW_ERR_DEVICE_CHECK = 7   /* a device-side bounds check fired (device error word) */
+} pw_status;
+
+typedef struct pw_pool_s* pw_pool_t;
+typedef struct pw_layer_s* pw_layer_t;
+
+/* Human-readable name of a status. */
+const char* pw_status_str(pw_status s);
+
+/* The cudaError_t value behind the most recent PW_ERR_CUDA on this thread. */
+pw_status pw_last_cuda_error(int* cuda_err);
+
+/* ---------------------------------------------------------------------------
+ * Page pool
+ * ---------------------------------------------------------------------------
+ * A pool hands out fixed-size pages of a caller-provided device buffer.  Pages
+ * hold bit-planes and fp16 fallback pages (paged, freed when an expert's
+ * precision drops); LUTs, the page table itself and the shared FFN are
+ * "resident" allocations taken from the end of the buffer.
+ *   dev_base   device pointer, 256-byte aligned; must outlive the pool.
+ *   bytes      usable size of the buffer.
+ *   page_bytes page size: multiple of 64 KiB, at least 64 KiB (2 MiB usual).
+ */
+pw_status pw_pool_create(void* dev_base, size_t bytes, size_t page_bytes, pw_pool_t* out);
+pw_status pw_pool_destroy(pw_pool_t pool);   /* all layers on it must be destroyed first */
+
+typedef struct {
+  size_t total_pages, free_pages, mapped_pages, reclaimable_pages;
+  size_t resident_bytes, page_bytes;
+} pw_pool_stats;
+pw_status pw_pool_get_stats(pw_pool_t pool, pw_pool_stats* out);
+
+/* ---------------------------------------------------------------------------
+ * Layer lifecycle (setup; not on the timed path; may synchronise the stream)
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int d;            /* hidden size, multiple of 64 */
+  int ffn;          /* expert FFN size, multiple of 64 */
+  int n_experts;    /* routed experts E, 1..256 */
+  int top_k;        /* K, 1..min(8, E) */
+  int renormalize;  /* 1: the K kept router weights are rescaled to sum 1 */
+  int shared_ffn;   /* size of an always-on fp16 shared FFN, 0 = none */
+} pw_layer_desc;
+
+pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, pw_layer_t* out);
+pw_status pw_layer_destroy(pw_layer_t layer);  /* returns every page and resident block */
+
+/*
+ * Upload one expert and map it at `bits` (3, 4, 5, 6 or 16).
+ *   code6[m]   host uint8 [rows][cols] 6-bit parent codes (values 0..63) of
+ *              matrix m = 0 gate, 1 up, 2 down.  Plane p holds bit (5 - p);
+ *              planes 0..min(bits,6)-1 are packed and paged (all six when
+ *              bits == 16, so that lowering from 16 moves no data).
+ *   lut[m][i]  host fp16 [rows][2^(i+3)]: LUT_b for b = i + 3, all four kept
+ *              resident (the dequantised weight is LUT_b[row][code6 >> (6-b)]).
+ *   w16[m]     host fp16 [rows][cols] fallback page, required iff bits == 16,
+ *              else may be NULL (then the expert can never be raised to 16).
+ * Re-loading an expert first releases its previous pages.
+ * Synchronises `stream` before returning (host buffers may be freed after).
+ */
+pw_status pw_layer_load_expert(pw_layer_t layer, int e, int bits,
+                               const uint8_t* const code6[3],
+                               const uint16_t* const lut[3][4],
+                               const uint16_t* const w16[3], void* stream);
+
+/* Upload the fp16 shared FFN: w16[0] gate [shared_ffn][d], w16[1] up, w16[2] down [d][shared_ffn]. */
+pw_status pw_layer_load_shared(pw_layer_t layer, const uint16_t* const w16[3], void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Hot path
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Router (PagedWeight write-up, "三层感知", routing statistics; the router
+ * itself is the standard MoE gate).  For each token t:
+ *   l = W_r x_t + bias (fp32 accumulation of fp16 products),
+ *   p = softmax(l) over all E experts,
+ *   idx[t][0..K) = the K largest l, descending, exact ties to the lower index,
+ *   w[t][k] = p[idx[t][k]], divided by their sum when renormalize is set.
+ *   x       device fp16 [T][d]          wr  device fp16 [E][d]
+ *   bias    device fp32 [E] or NULL     idx device int32 [T][K]   w device fp32 [T][K]
+ *   expert_count  device int32 [E] or NULL: if given, incremented by the number
+ *           of (t, k) slots routed to each expert ("routing mass" counters);
+ *           the caller zeroes it.
+ * T may be 0 (nothing is launched).
+ */
+pw_status pw_route_topk(pw_layer_t layer, const void* x, const void* wr, const float* bias,
+                        int T, int32_t* idx, float* w, int32_t* expert_count, void* stream);
+
+/*
+ * Stable permutation of the S = T*K slots (flat index t*K + k) by expert:
+ * inside an expert's bucket the slots keep ascending flat order.
+ *   offsets  device int32 [E+1]: bucket e is [offsets[e], offsets[e+1])
+ *   perm_src device int32 [S]:   token of each sorted slot
+ *   inv_slot device int32 [S]:   sorted position of flat slot t*K + k
+ *   x        device fp16 [T][d] and x_perm device fp16 [S][d]: if both are
+ *            non-NULL, x_perm[i] = x[perm_src[i]].
+ *   ws       device scratch of at least pw_workspace_size() bytes.
+ * Deterministic (no atomics decide any order).
+ */
+pw_status pw_permute(pw_layer_t layer, const int32_t* idx, int T, const void* x,
+                     int32_t* offsets, int32_t* perm_src, int32_t* inv_slot, void* x_perm,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Routed expert SwiGLU FFN over the permuted slots.  For each expert e with
+ * tokens (bucket of `offsets`) at its current bitwidth b_e:
+ *   W = LUT_b[row][code_b] built from planes 0..b-1 only (planes >= b are never
+ *       read), or the fp16 page when b_e == 16,
+ *   h = silu(W_gate x) * (W_up x)   (fp32 accumulation; h rounded to fp16),
+ *   y_perm[slot] = W_down h          (fp32).
+ *   x_perm  device fp16 [T*K][d]     offsets device int32 [E+1]
+ *   y_perm  device fp32 [T*K][d]     ws device scratch (pw_workspace_size)
+ */
+pw_status pw_expert_ffn_bitplane(pw_layer_t layer, const void* x_perm, const int32_t* offsets,
+                                 int T, float* y_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* fp16 shared FFN on all T tokens: y_shared [T][d] fp32 (layers with shared_ffn > 0). */
+pw_status pw_shared_ffn(pw_layer_t layer, const void* x, int T, float* y_shared,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Weighted combine:
+ *   y[t] = sum_{k<K} w[t][k] * y_perm[inv_slot[t*K+k]]  (+ y_shared[t])
+ * summed in k order in fp32, rounded to fp16.  The shared FFN output is added
+ * unweighted.  y_shared may be NULL.  y device fp16 [T][d].
+ */
+pw_status pw_combine(pw_layer_t layer, const float* y_perm, const int32_t* inv_slot,
+                     const float* w, int T, const float* y_shared, void* y, void* stream);
+
+/*
+ * Change one expert's precision (write-up "核心洞察": lower the least
+ * sensitive experts under KV-cache pressure; "安全边界与异步搬运": commit at a
+ * safe boundary).
+ * Lowering b -> b' moves no weight data: the device bitwidth word is written
+ * in stream order (kernels enqueued later read only planes < b'), and the pages
+ * of planes b'..b-1 (and the fp16 page when leaving 16) become reclaimable.
+ * They are handed to other owners only after an event recorded here has
+ * completed, i.e. after every kernel enqueued before this call is done.
+ * Raising succeeds only while every needed page is still reclaimable
+ * (otherwise PW_ERR_NOT_RESIDENT and nothing changes).  Never synchronises.
+ */
+pw_status pw_set_expert_bitwidth(pw_layer_t layer, int e, int bits, void* stream);
+
+/* Host mirror of an expert's current bitwidth (0 if not loaded). */
+pw_status pw_get_expert_bitwidth(pw_layer_t layer, int e, int* bits);
+
+/* Scratch bytes that pw_permute / pw_expert_ffn_bitplane / pw_shared_ffn need for T tokens. */
+pw_status pw_workspace_size(pw_layer_t layer, int T, size_t* bytes);
+
+/*
+ * Reads (synchronously) and clears the layer's device error word, set by
+ * bounded device-side waits or bounds checks of earlier launches.
+ * PW_OK if nothing was flagged, else PW_ERR_TIMEOUT / PW_ERR_DEVICE_CHECK.
+ */
+pw_status pw_layer_check_device(pw_layer_t layer, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host utilities and debugging
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Pack 6-bit codes [R][C] (host) into six plane arrays planes_out[p] of
+ * R*C/32 uint32 words each (plane p = bit 5-p), in the stored word order:
+ *   tile = r / 16, chunk = c / 64; g = r%16 % 8, rowsel = r%16 / 8;
+ *   s = c%64 / 16, colhalf = c%16 / 8, t = c%8 / 2, h = c % 2;
+ *   lane = 4g + t, k = 2 rowsel + colhalf, q = 8k + 4h + s;
+ *   plane p keeps the bit at position (q + 5 - p) mod 32 of word
+ *   tile*(C/64)*32 + [group*128 + 4*lane + i] for chunk 4*group + i of a full
+ *   group of four chunks, or [G*128 + r*lane + i] in a final group of r < 4 chunks.
+ */
+pw_status pw_pack_planes(const uint8_t* code6, int R, int C, uint32_t* const planes_out[6]);
+
+/*
+ * Pack an fp16 matrix [R][C] into the stored fp16-page order: half index
+ * (((tile*(C/64) + chunk)*4 + s)*32 + lane)*8 + 2a + h with a = rowsel + 2 colhalf.
+ */
+pw_status pw_pack_f16(const uint16_t* w, int R, int C, uint16_t* out);
+
+/*
+ * Debug: write expert e's matrix m (0 gate, 1 up, 2 down) as the kernels see it
+ * at its current bitwidth, dequantised, into out (device fp16 [rows][cols]).
+ * Uses the same device decode routines as the FFN kernels.
+ */
+pw_status pw_debug_dequant(pw_layer_t layer, int e, int m, void* out, void* stream);
+
+/* Debug: device address of virtual page `vpage` of expert e's plane p (p = 6: fp16 page), or 0. */
+pw_status pw_debug_page_address(pw_layer_t layer, int e, int p, int vpage, uint64_t* addr);
+
+/*
+ * Testing hook: host-simulated device (call before creating any pool).  The
+ * pool buffer is then host memory, uploads are memcpy, events complete only
+ * when pw_testing_complete_events() is called, and every compute entry point
+ * returns PW_ERR_UNSUPPORTED.  Used to test pool / page-table bookkeeping on
+ * machines without a GPU.  enable = 0 restores normal operation.
+ */
+pw_status pw_testing_host_sim(int enable);
+pw_status pw_testing_complete_events(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PW_H */

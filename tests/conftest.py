@@ -26,3 +26,21 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def _ensure_library():
+    """Build libpw.so in-tree if it is missing or older than its sources."""
+    pkg = os.path.join(ROOT, "any_precision_expert_gb300")
+    lib = os.path.join(pkg, "libpw.so")
+    srcs = [os.path.join(pkg, "csrc", f) for f in os.listdir(os.path.join(pkg, "csrc"))]
+    srcs.append(os.path.join(ROOT, "include", "pw.h"))
+    if os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(s) for s in srcs):
+        return
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("_pw_build", os.path.join(pkg, "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+
+
+_ensure_library()

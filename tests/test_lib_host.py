@@ -1,0 +1,220 @@
+"""Library checks that need no GPU: exported symbols, host packers against the
+oracle's packer, and page-pool / page-table bookkeeping in host-sim mode."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import any_precision_expert_gb300 as pw
+from any_precision_expert_gb300 import _lib
+from oracle import pw_oracle as O
+from synth import get_config, make_expert
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "pw.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pw_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_function_is_exported():
+    names = _declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(_lib.lib, n), n
+        assert n in _lib.EXPORTED, n
+
+
+def test_status_strings():
+    assert _lib.lib.pw_status_str(0) == b"PW_OK"
+    assert _lib.lib.pw_status_str(4) == b"PW_ERR_NOT_RESIDENT"
+
+
+@pytest.mark.parametrize("R,C", [(16, 64), (32, 256), (48, 320), (64, 704), (16, 1408), (32, 2816)])
+def test_library_packers_match_oracle(R, C):
+    rng = np.random.default_rng(R * 7 + C)
+    code6 = rng.integers(0, 64, size=(R, C), dtype=np.uint8)
+    for a, b in zip(pw.pack_planes(code6), O.pack_planes(code6)):
+        assert np.array_equal(a, b)
+    w = rng.standard_normal((R, C)).astype(np.float16)
+    assert np.array_equal(pw.pack_f16(w), O.pack_f16(w))
+
+
+def test_packer_rejects_bad_shapes():
+    code6 = np.zeros((16, 96), dtype=np.uint8)
+    with pytest.raises(pw.PwError):
+        pw.pack_planes(code6)
+
+
+# ---------------------------------------------------------------------------
+# host-simulated device: pool and page table without a GPU
+# ---------------------------------------------------------------------------
+
+PAGE = 64 << 10
+
+
+@pytest.fixture
+def sim():
+    _lib.lib.pw_testing_host_sim(1)
+    yield
+    _lib.lib.pw_testing_host_sim(0)
+
+
+def _layer(pool, E=4, d=128, f=128, K=2):
+    return pw.Layer(pool, d, f, E, K, 1)
+
+
+def _expert(e, d=128, f=128, w16=True):
+    cfg = get_config("tiny", d=d, f=f)
+    return make_expert(cfg, e, seed=11, with_w16=w16)
+
+
+def _load(layer, e, bits, ex):
+    layer.load_expert(e, bits, ex["code6"], ex["lut"], ex["w16"] if bits == 16 else None, stream=0)
+
+
+def _page_bytes(pool, addr, n):
+    base = pool.buffer.data_ptr()
+    off = addr - base
+    return pool.buffer[off:off + n].numpy()
+
+
+def test_load_places_packed_tiles_in_pages(sim):
+    import torch  # noqa: F401
+    pool = pw.Pool(48 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool)
+    ex = _expert(0)
+    _load(layer, 0, 4, ex)
+    st = pool.stats()
+    assert st["mapped_pages"] == 4  # four planes, one page each at this size
+    # plane p of the gate matrix: 8 tiles of 2*d bytes from the start of page 0 of the block
+    ref = O.pack_planes(ex["code6"][0])
+    for p in range(4):
+        addr = layer.page_address(0, p, 0)
+        assert addr != 0
+        got = _page_bytes(pool, addr, ref[p].nbytes).view(np.uint32)
+        assert np.array_equal(got, ref[p])
+        # down matrix follows gate and up in the same page
+        refd = O.pack_planes(ex["code6"][2])[p]
+        got = _page_bytes(pool, addr + 2 * ref[p].nbytes, refd.nbytes).view(np.uint32)
+        assert np.array_equal(got, refd)
+    assert layer.page_address(0, 4, 0) == 0  # planes >= b are never uploaded
+    layer.destroy()
+    assert pool.stats()["free_pages"] == pool.stats()["total_pages"]
+    pool.close()
+
+
+def test_lower_raise_moves_no_data(sim):
+    pool = pw.Pool(48 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool)
+    ex = _expert(1)
+    _load(layer, 1, 16, ex)
+    st = pool.stats()
+    assert st["mapped_pages"] == 6 + 2  # six planes + two fp16 pages
+    addrs = [layer.page_address(1, p, 0) for p in range(6)]
+    layer.set_expert_bitwidth(1, 3, stream=0)
+    assert layer.get_expert_bitwidth(1) == 3
+    st = pool.stats()
+    assert st["mapped_pages"] == 3 and st["reclaimable_pages"] == 5
+    layer.set_expert_bitwidth(1, 5, stream=0)  # raise from still-intact pages
+    assert [layer.page_address(1, p, 0) for p in range(6)] == addrs
+    st = pool.stats()
+    assert st["mapped_pages"] == 5 and st["reclaimable_pages"] == 3
+    layer.set_expert_bitwidth(1, 16, stream=0)
+    assert pool.stats()["reclaimable_pages"] == 0
+    layer.destroy()
+    pool.close()
+
+
+def test_raise_without_planes_is_not_resident(sim):
+    pool = pw.Pool(48 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool)
+    _load(layer, 0, 3, _expert(0))
+    assert layer.try_set_expert_bitwidth(0, 4) == 4  # PW_ERR_NOT_RESIDENT
+    assert layer.try_set_expert_bitwidth(0, 16) == 4
+    assert layer.get_expert_bitwidth(0) == 3
+    layer.destroy()
+    pool.close()
+
+
+def test_freed_pages_wait_for_the_safe_boundary(sim):
+    # 6 resident pages (LUTs and tables) + expert 0 at 6 planes + experts 1, 2 at
+    # 3 planes leave one free page in a 19-page pool
+    pool = pw.Pool(19 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool)
+    _load(layer, 0, 6, _expert(0))
+    _load(layer, 1, 3, _expert(1))
+    _load(layer, 2, 3, _expert(2))
+    assert pool.stats()["free_pages"] == 1
+    layer.set_expert_bitwidth(0, 3, stream=0)        # planes 3..5 -> reclaimable
+    assert pool.stats()["reclaimable_pages"] == 3
+    ex = _expert(3)
+    with pytest.raises(pw.PwError) as ei:             # safe boundary not reached: no reuse
+        _load(layer, 3, 3, ex)
+    assert ei.value.status == 3
+    assert layer.try_set_expert_bitwidth(0, 6) == 0   # still intact: raise works
+    layer.set_expert_bitwidth(0, 3, stream=0)
+    _lib.lib.pw_testing_complete_events()
+    _load(layer, 3, 3, ex)                            # now the freed pages are reused
+    assert layer.try_set_expert_bitwidth(0, 6) == 4   # those planes are gone
+    assert layer.get_expert_bitwidth(0) == 3
+    layer.destroy()
+    pool.close()
+
+
+def test_invalid_arguments_have_no_side_effects(sim):
+    pool = pw.Pool(48 * PAGE, page_bytes=PAGE, device="cpu")
+    with pytest.raises(pw.PwError):
+        pw.Layer(pool, 96, 128, 4, 2, 1)       # d not a multiple of 64
+    with pytest.raises(pw.PwError):
+        pw.Layer(pool, 128, 128, 4, 5, 1)      # K > E
+    with pytest.raises(pw.PwError):
+        pw.Layer(pool, 128, 128, 300, 2, 1)    # E > 256
+    layer = _layer(pool)
+    before = pool.stats()
+    ex = _expert(0)
+    for bad_bits in (0, 2, 7, 8, 15, 17):
+        with pytest.raises(pw.PwError):
+            _load(layer, 0, bad_bits, ex)
+    with pytest.raises(pw.PwError):
+        _load(layer, 4, 3, ex)                 # expert out of range
+    with pytest.raises(pw.PwError):
+        layer.load_expert(0, 16, ex["code6"], ex["lut"], None, stream=0)  # 16 needs fp16 page
+    assert pool.stats() == before
+    _load(layer, 0, 4, ex)
+    for bad in (2, 7, 0):
+        assert layer.try_set_expert_bitwidth(0, bad) == 1
+    assert layer.try_set_expert_bitwidth(1, 3) == 1  # never loaded
+    assert layer.get_expert_bitwidth(0) == 4
+    layer.destroy()
+    pool.close()
+
+
+def test_pool_exhaustion_is_oom(sim):
+    pool = pw.Pool(12 * PAGE, page_bytes=PAGE, device="cpu")
+    with pytest.raises(pw.PwError) as ei:
+        _layer(pool, E=64)                     # LUT blocks do not fit
+    assert ei.value.status == 3
+    layer = _layer(pool, E=2)
+    _load(layer, 0, 3, _expert(0))
+    before = pool.stats()
+    with pytest.raises(pw.PwError) as ei:
+        _load(layer, 1, 16, _expert(1))
+    assert ei.value.status == 3
+    assert pool.stats()["mapped_pages"] == before["mapped_pages"]
+    layer.destroy()
+    pool.close()
+
+
+def test_compute_calls_refuse_in_host_sim(sim):
+    pool = pw.Pool(48 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool)
+    rc = _lib.lib.pw_route_topk(layer.handle, 256, 256, None, 1, 256, 256, None, None)
+    assert rc == 2
+    rc = _lib.lib.pw_combine(layer.handle, 256, 256, 256, 1, None, 256, None)
+    assert rc == 2
+    layer.destroy()
+    pool.close()

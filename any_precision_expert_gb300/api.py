@@ -93,7 +93,7 @@ class Layer:
         self.handle = C.c_void_p()
         check(lib.pw_layer_create(pool.handle, C.byref(self.desc), C.byref(self.handle)), "pw_layer_create")
         self.d, self.ffn, self.E, self.K = d, ffn, n_experts, top_k
-        self.renormalize, self.shared_ffn = renormalize, shared_ffn
+        self.renormalize, self.fs = renormalize, shared_ffn
 
     # -- setup ---------------------------------------------------------------
     def load_expert(self, e: int, bits: int, code6, luts, w16=None, stream=None):
@@ -182,7 +182,7 @@ class Buffers:
         self.x_perm = torch.empty((S, d), dtype=torch.float16, device=device)
         self.y_perm = torch.empty((S, d), dtype=torch.float32, device=device)
         self.y_shared = (torch.empty((T_max, d), dtype=torch.float32, device=device)
-                         if layer.shared_ffn else None)
+                         if layer.fs else None)
         self.y = torch.empty((T_max, d), dtype=torch.float16, device=device)
         self.ws = torch.empty(max(layer.workspace_size(T_max), 256), dtype=torch.uint8, device=device)
 
@@ -194,7 +194,7 @@ def moe_forward(layer: Layer, x, wr, bias, buf: Buffers, stream=None):
     layer.permute(buf.idx, T, x, buf.offsets, buf.perm_src, buf.inv_slot, buf.x_perm, buf.ws, stream)
     layer.expert_ffn_bitplane(buf.x_perm, buf.offsets, T, buf.y_perm, buf.ws, stream)
     ysh = None
-    if layer.shared_ffn:
+    if layer.fs:
         layer.shared_ffn(x, T, buf.y_shared, buf.ws, stream)
         ysh = buf.y_shared
     layer.combine(buf.y_perm, buf.inv_slot, buf.w, T, ysh, buf.y, stream)

@@ -17,6 +17,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
+
 #include "pw_device.cuh"
 
 namespace pw {
@@ -34,6 +36,7 @@ struct FfnParams {
   const __half* act;     // phase 0: x rows [slots][d]; phase 1: h rows [slots][fe]
   const int* offsets;    // routed: [E+1]
   int n_slots;
+  int max_tokens;        // experts with more tokens are left to the tensor-core GEMM
   __half* h;             // [slots][fe]
   float* y;              // [slots][d]
 };
@@ -187,7 +190,10 @@ __global__ void __launch_bounds__(kFfnThreads, 2) ffn_decode_kernel(FfnParams P)
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       int c = 0;
-      if (e < E) c = ((s_off[e + 1] - s_off[e] + kTok - 1) / kTok) * tiles;
+      if (e < E) {
+        const int n = s_off[e + 1] - s_off[e];
+        c = n <= P.max_tokens ? ((n + kTok - 1) / kTok) * tiles : 0;
+      }
       int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -316,11 +322,17 @@ cudaError_t allow_smem(Kern k, size_t bytes) {
 
 cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* offsets, int n_slots, float* y,
                        __half* h_ws, cudaStream_t s) {
+  // Experts with at most `thr` tokens take the mma.sync GEMV path; larger
+  // ones the tcgen05 GEMM.  No expert can have more tokens than the batch.
+  const int T = mode == 0 ? n_slots / L.K : n_slots;
+  const int thr = decode_max_tokens();
+  const bool big = T > thr;
   FfnParams P;
   P.L = L;
   P.mode = mode;
   P.offsets = offsets;
   P.n_slots = n_slots;
+  P.max_tokens = big ? thr : INT_MAX;
   P.h = h_ws;
   P.y = y;
   const int grid = sm_count() * 2;
@@ -333,9 +345,17 @@ cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* 
   P.phase = 0;
   P.act = x;
   ffn_decode_kernel<2><<<grid, kFfnThreads, smem0, s>>>(P);
+  if (big) {
+    e = launch_prefill(L, mode, 0, x, offsets, n_slots, thr, h_ws, y, s);
+    if (e != cudaSuccess) return e;
+  }
   P.phase = 1;
   P.act = h_ws;
   ffn_decode_kernel<1><<<grid, kFfnThreads, smem1, s>>>(P);
+  if (big) {
+    e = launch_prefill(L, mode, 1, h_ws, offsets, n_slots, thr, h_ws, y, s);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 

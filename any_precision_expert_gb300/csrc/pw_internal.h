@@ -50,6 +50,9 @@ cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __hal
 // mode 0: routed experts over permuted slots; mode 1: the shared fp16 FFN over all T tokens.
 cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* offsets, int n_slots,
                        float* y, __half* h_ws, cudaStream_t s);
+int decode_max_tokens();
+cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
+                           int n_slots, int min_tokens, __half* h, float* y, cudaStream_t s);
 cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* inv_slot,
                            const float* w, int T, const float* y_shared, __half* y, cudaStream_t s);
 cudaError_t launch_debug_dequant(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);

@@ -1,0 +1,475 @@
+// Prefill-side grouped expert GEMM on the 5th-generation tensor cores.
+//
+// For experts that receive many tokens the expert FFN is a dense contraction,
+// so it runs as a grouped GEMM: each CTA owns a tile of 128 weight rows x 256
+// tokens of one expert and walks the reduction in 64-column stages.  Warp
+// roles (one CTA per SM, persistent over a device-built tile list):
+//   * dequant warps (two per 64-row slab and matrix, alternating stages) read
+//     the expert's top-b bit-planes through the page table, decode them with
+//     the same mask/rotate + per-lane LUT scheme as the decode kernel, and
+//     write fp16 weights into shared memory in the 128-byte swizzled K-major
+//     layout; afterwards they are the epilogue (TMEM -> registers -> global);
+//   * four loader warps copy the tokens' activation rows into the same layout;
+//   * one thread issues tcgen05.mma (kind::f16, fp32 accumulators in tensor
+//     memory) and releases stages with tcgen05.commit.
+// Phase 0 accumulates gate and up side by side in TMEM (2 x 256 columns) and
+// writes h = silu(gate) * up as fp16; phase 1 (down) writes y as fp32.
+// Every wait is bounded: on a timeout the kernel flags the layer's error word
+// (PW_ERR_TIMEOUT), drains its MMAs and frees its tensor memory.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdlib>
+
+#include "pw_device.cuh"
+#include "pw_tc.cuh"
+
+namespace pw {
+
+constexpr int PF_BM = 128, PF_BN = 256, PF_BK = 64;
+constexpr uint32_t PF_A_BYTES = PF_BM * PF_BK * 2;  // 16 KB
+constexpr uint32_t PF_B_BYTES = PF_BN * PF_BK * 2;  // 32 KB
+constexpr int PF_BWARPS = 4;
+constexpr uint32_t PF_TAB_BYTES = 64 * 256;          // LUT table of one (matrix, 64-row slab), b <= 6
+
+template <int NM>
+struct Pf {
+  static constexpr int DQ = 4 * NM;                  // (matrix, slab, stage parity)
+  static constexpr int NS = NM == 2 ? 2 : 3;
+  static constexpr int WARPS = DQ + PF_BWARPS + 1;
+  static constexpr int THREADS = 32 * WARPS;
+  static constexpr uint32_t STAGE = NM * PF_A_BYTES + PF_B_BYTES;
+  static constexpr uint32_t TABS = NM * 2 * PF_TAB_BYTES;
+  static constexpr uint32_t BARS = 256;
+  static constexpr uint32_t SMEM = 1024 + NS * STAGE + TABS + BARS;
+  static constexpr uint32_t TMEM_COLS = NM == 2 ? 512 : 256;
+  static constexpr uint32_t FULL_COUNT = NM * 2 + PF_BWARPS;  // one arrival per producing warp
+  static constexpr int PAIRS = DQ / 2;                        // warps sharing one LUT table
+};
+
+struct PfParams {
+  DevLayer L;
+  int mode;             // 0 routed, 1 shared fp16 FFN
+  const __half* act;    // [slots][K] fp16 (x_perm / x for phase 0, h for phase 1)
+  const int* offsets;   // routed: [E+1]
+  int n_slots;
+  int min_tokens;       // experts with more tokens than this are handled here
+  __half* h;            // phase 0 output [slots][fe]
+  float* y;             // phase 1 output [slots][d]
+};
+
+struct PfTile {
+  int e, mt, nt, slot0, nvalid;
+};
+
+__device__ __forceinline__ PfTile pf_tile(int t, const int* s_pref, const int* s_off, int E, int mtiles) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_pref[mid] <= t) lo = mid; else hi = mid;
+  }
+  PfTile T;
+  T.e = lo;
+  const int local = t - s_pref[lo];
+  T.mt = local % mtiles;
+  T.nt = local / mtiles;
+  T.slot0 = s_off[lo] + T.nt * PF_BN;
+  T.nvalid = min(PF_BN, s_off[lo + 1] - T.slot0);
+  return T;
+}
+
+__device__ __forceinline__ uint32_t sw128_offset(int row, int c16) {
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((c16 ^ (row & 7)) << 4));
+}
+
+// Decode one 64-column stage of this lane's two rows (g, g+8 of its 16-row
+// tile) into out[s][q]: q = 0 row g cols 16s..+7, 1 row g cols 16s+8..+15,
+// 2 row g+8 cols 16s..+7, 3 row g+8 cols 16s+8..+15 (fp16 x 8 each).
+template <int B>
+__device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint32_t tab, uint32_t lb0,
+                                                 uint32_t lb1, uint4 (&out)[4][4]) {
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    uint32_t a[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      uint32_t wt[B];
+#pragma unroll
+      for (int p = 0; p < B; ++p) wt[p] = w[t][p];
+      decode_step_lut<B>(wt, s, tab, lb0, lb1, a[t]);
+    }
+    out[s][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
+    out[s][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
+    out[s][2] = make_uint4(a[0][1], a[1][1], a[2][1], a[3][1]);
+    out[s][3] = make_uint4(a[0][3], a[1][3], a[2][3], a[3][3]);
+  }
+}
+
+template <int B>
+__device__ __forceinline__ void pf_load_planes(const char* const (&pb)[6], int kb, int nk, int g,
+                                               uint32_t (&w)[4][B]) {
+  const int G = nk / 4, rem = nk % 4, gamma = kb / 4, i = kb % 4;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int ln = 4 * g + t;
+    const int word = gamma < G ? gamma * 128 + ln * 4 + i : G * 128 + ln * rem + i;
+#pragma unroll
+    for (int p = 0; p < B; ++p)
+      w[t][p] = pb[p] ? *reinterpret_cast<const uint32_t*>(pb[p] + (size_t)word * 4) : 0u;
+  }
+}
+
+template <int NM>
+__global__ void __launch_bounds__(Pf<NM>::THREADS, 1) ffn_prefill_kernel(PfParams Q) {
+  using C = Pf<NM>;
+  extern __shared__ unsigned char pf_raw[];
+  __shared__ int s_pref[kMaxExperts + 1];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_bits[kMaxExperts];
+
+  const DevLayer& L = Q.L;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool routed = Q.mode == 0;
+  const int E = routed ? L.E : 1;
+  const int fe = routed ? L.f : L.fs;
+  const int K = NM == 2 ? L.d : fe;   // reduction length
+  const int R = NM == 2 ? fe : L.d;   // output rows
+  const int mtiles = (R + PF_BM - 1) / PF_BM;
+  const int nkb = K / PF_BK;
+
+  if (routed) {
+    for (int i = tid; i <= E; i += C::THREADS) s_off[i] = Q.offsets[i];
+    for (int i = tid; i < E; i += C::THREADS) s_bits[i] = L.bits[i];
+  } else if (tid == 0) {
+    s_off[0] = 0;
+    s_off[1] = Q.n_slots;
+    s_bits[0] = 16;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int c = 0;
+      if (e < E) {
+        const int n = s_off[e + 1] - s_off[e];
+        c = n > Q.min_tokens ? mtiles * ((n + PF_BN - 1) / PF_BN) : 0;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) s_pref[e] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_pref[E] = run;
+  }
+  __syncthreads();
+  const int total = s_pref[E];
+  if ((int)blockIdx.x >= total) return;  // uniform across the CTA
+
+  // shared memory carve-up (stage buffers 1024-byte aligned for the swizzle)
+  const uint32_t raw = smem_u32(pf_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = pf_raw + (base - raw);
+  const uint32_t tabs = base + C::NS * C::STAGE;
+  const uint32_t bars = tabs + C::TABS;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (C::NS + s); };
+  const uint32_t acc_full = bars + 16u * C::NS;
+  const uint32_t acc_empty = acc_full + 8;
+  const uint32_t fin_bar = acc_full + 16;
+  const uint32_t tmem_slot = acc_full + 24;
+  const uint32_t pair_bars = acc_full + 40;  // one per LUT-sharing warp pair
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (C::NS * C::STAGE + C::TABS + 16u * C::NS + 32));
+  uint32_t* tmem_slot_g = reinterpret_cast<uint32_t*>(gbase + (C::NS * C::STAGE + C::TABS + 16u * C::NS + 24));
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(full_bar(s), C::FULL_COUNT);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, C::DQ);
+    mbar_init(fin_bar, 1);
+    for (int i = 0; i < C::PAIRS; ++i) mbar_init(pair_bars + 8u * i, 2);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_g;
+
+  if (warp < C::DQ) {
+    // ---------------- dequant warps, then epilogue ----------------
+    const int mi = NM == 2 ? (warp >> 2) : 0;
+    const int mm = NM == 2 ? mi : 2;  // matrix index: 0 gate, 1 up, 2 down
+    const int slab = (warp >> 1) & 1, par = warp & 1;
+    const uint32_t pair_bar = pair_bars + 8u * (warp >> 1);
+    uint32_t pair_use = 0;
+    // both warps of the pair reach this point (bounded wait; false on abort)
+    auto pair_sync = [&]() {
+      if (lane == 0) mbar_arrive(pair_bar);
+      const bool r = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_use & 1, abort_flag, L.err));
+      ++pair_use;
+      return r;
+    };
+    const int tis = lane >> 3, g = lane & 7;
+    const uint32_t tab = tabs + (uint32_t)(mi * 2 + slab) * PF_TAB_BYTES;
+    uint32_t* tabg = reinterpret_cast<uint32_t*>(gbase + (tab - base));
+    const uint32_t lb0 = lane * 4, lb1 = 128 + lane * 4;
+    uint32_t it = 0, tc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const PfTile T = pf_tile(t, s_pref, s_off, E, mtiles);
+      const int b = s_bits[T.e];
+      const int row0 = T.mt * PF_BM + slab * 64 + tis * 16;  // this lane's 16-row tile
+      const bool tile_ok = row0 < R;
+      const int tau = row0 / 16;
+      if (b <= 6) {
+        ok = pair_sync();  // both warps of the pair finished the previous tile
+        if (!ok) break;
+        const int j = par * 32 + lane, rho = j >> 5, lx = j & 31;
+        int row = T.mt * PF_BM + slab * 64 + (lx >> 3) * 16 + (lx & 7) + 8 * rho;
+        row = min(row, R - 1);
+        const __half* lr = lut_rows(L, T.e, mm, b, row);
+        for (int v = 0; v < (1 << b); ++v) {
+          const uint32_t val = __half_as_ushort(lr[v]);
+          tabg[v * 64 + rho * 32 + lx] = val | (val << 16);
+        }
+        ok = pair_sync();
+        if (!ok) break;
+      }
+      const char* pb[6];
+#pragma unroll
+      for (int p = 0; p < 6; ++p) pb[p] = (tile_ok && b <= 6 && p < b) ? tile_addr(L, T.e, mm, p, tau) : nullptr;
+      const char* fb = nullptr;
+      if (tile_ok && b == 16)
+        fb = routed ? tile_addr(L, T.e, mm, kPlanes, tau)
+                    : reinterpret_cast<const char*>(L.shared16[mm]) + (size_t)tau * 32 * K;
+
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        if ((kb & 1) != par) continue;
+        const int s = it % C::NS;
+        const uint32_t ph = (it / C::NS) & 1;
+        uint4 out[4][4];
+        switch (b) {
+#define PW_PF_CASE(BB)                                                  \
+  case BB: {                                                            \
+    uint32_t w[4][BB];                                                  \
+    pf_load_planes<BB>(pb, kb, nkb, g, w);                              \
+    pf_decode_planes<BB>(w, tab, lb0, lb1, out);                        \
+    break;                                                              \
+  }
+          PW_PF_CASE(3)
+          PW_PF_CASE(4)
+          PW_PF_CASE(5)
+          PW_PF_CASE(6)
+#undef PW_PF_CASE
+          default: {  // fp16 page: the lane gathers the four fragment lanes (g, t)
+#pragma unroll
+            for (int st = 0; st < 4; ++st) {
+              uint4 a[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+                a[t] = fb ? *reinterpret_cast<const uint4*>(fb + ((size_t)(kb * 4 + st) * 32 + 4 * g + t) * 16)
+                          : make_uint4(0, 0, 0, 0);
+              out[st][0] = make_uint4(a[0].x, a[1].x, a[2].x, a[3].x);
+              out[st][1] = make_uint4(a[0].z, a[1].z, a[2].z, a[3].z);
+              out[st][2] = make_uint4(a[0].y, a[1].y, a[2].y, a[3].y);
+              out[st][3] = make_uint4(a[0].w, a[1].w, a[2].w, a[3].w);
+            }
+          }
+        }
+        if (!tile_ok) {
+#pragma unroll
+          for (int st = 0; st < 4; ++st)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) out[st][q] = make_uint4(0, 0, 0, 0);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err));
+        if (!ok) break;
+        const uint32_t A = base + s * C::STAGE + mi * PF_A_BYTES;
+#pragma unroll
+        for (int st = 0; st < 4; ++st)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = slab * 64 + tis * 16 + g + 8 * (q >> 1);
+            sts128(A + sw128_offset(r, 2 * st + (q & 1)), out[st][q]);
+          }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full_bar(s));
+      }
+      if (!ok) break;
+      // epilogue: this warp reads TMEM lanes 32*(warp%4).. of the tile's accumulators
+      ok = __all_sync(0xffffffffu, mbar_wait(acc_full, tc & 1, abort_flag, L.err));
+      if (!ok) break;
+      tc_fence_after();
+      const int lg = warp & 3;
+      const int row = T.mt * PF_BM + 32 * lg + lane;
+      const uint32_t tl = tmem + ((uint32_t)(32 * lg) << 16);
+      if (NM == 2) {
+        const int c0 = (warp >> 2) * 128;
+        for (int c = 0; c < 4; ++c) {
+          float gv[32], uv[32];
+          tmem_ld32(tl + c0 + 32 * c, gv);
+          tmem_ld32(tl + 256 + c0 + 32 * c, uv);
+          if (row < R) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int n = c0 + 32 * c + j;
+              if (n < T.nvalid)
+                Q.h[(size_t)(T.slot0 + n) * fe + row] = __float2half_rn(silu_f(gv[j]) * uv[j]);
+            }
+          }
+        }
+      } else {
+        for (int c = 0; c < 8; ++c) {
+          float acc[32];
+          tmem_ld32(tl + 32 * c, acc);
+          if (row < R) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int n = 32 * c + j;
+              if (n < T.nvalid) Q.y[(size_t)(T.slot0 + n) * L.d + row] = acc[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      ++tc;
+    }
+  } else if (warp < C::DQ + PF_BWARPS) {
+    // ---------------- activation loader warps ----------------
+    const int bt = tid - C::DQ * 32;  // 0..127
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const PfTile T = pf_tile(t, s_pref, s_off, E, mtiles);
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % C::NS;
+        const uint32_t ph = (it / C::NS) & 1;
+        uint4 v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int j = bt + 128 * q, n = j >> 3, c16 = j & 7;
+          v[q] = n < T.nvalid
+                     ? *reinterpret_cast<const uint4*>(Q.act + (size_t)(T.slot0 + n) * K + kb * PF_BK + c16 * 8)
+                     : make_uint4(0, 0, 0, 0);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err));
+        if (!ok) break;
+        const uint32_t Bs = base + s * C::STAGE + NM * PF_A_BYTES;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int j = bt + 128 * q, n = j >> 3, c16 = j & 7;
+          sts128(Bs + sw128_offset(n, c16), v[q]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full_bar(s));
+      }
+    }
+  } else if (lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_f16(PF_BM, PF_BN);
+    uint32_t it = 0, tc = 0;
+    bool issued = false, ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      ok = mbar_wait(acc_empty, (tc & 1) ^ 1, abort_flag, L.err);
+      if (!ok) break;
+      tc_fence_after();
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % C::NS;
+        const uint32_t ph = (it / C::NS) & 1;
+        ok = mbar_wait(full_bar(s), ph, abort_flag, L.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t st = base + s * C::STAGE;
+        const uint64_t bdesc = sw128_desc(st + NM * PF_A_BYTES);
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const uint64_t adesc = sw128_desc(st + m * PF_A_BYTES);
+#pragma unroll
+          for (int k = 0; k < PF_BK / 16; ++k)
+            umma_f16(tmem + m * PF_BN, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+        }
+        issued = true;
+        umma_commit(empty_bar(s));
+      }
+      if (!ok) break;
+      umma_commit(acc_full);
+      ++tc;
+    }
+    if (issued) {  // drain: every MMA must be done before tensor memory is freed
+      umma_commit(fin_bar);
+      volatile int never = 0;  // drain even after an abort
+      mbar_wait(fin_bar, 0, &never, L.err);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+namespace {
+template <typename Kern>
+cudaError_t allow_smem_pf(Kern k, size_t bytes) {
+  static int done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && done[dev] >= (int)bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && dev < 64) done[dev] = (int)bytes;
+  return e;
+}
+}  // namespace
+
+int decode_max_tokens() {
+  // experts with more tokens than this use the tensor-core GEMM (read per call)
+  const char* s = getenv("PW_DECODE_MAX_TOK");
+  const int v = s ? atoi(s) : 48;
+  return v < 0 ? 0 : v;
+}
+
+cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
+                           int n_slots, int min_tokens, __half* h, float* y, cudaStream_t s) {
+  PfParams Q;
+  Q.L = L;
+  Q.mode = mode;
+  Q.act = act;
+  Q.offsets = offsets;
+  Q.n_slots = n_slots;
+  Q.min_tokens = min_tokens;
+  Q.h = h;
+  Q.y = y;
+  const int grid = sm_count();
+  cudaError_t e;
+  if (phase == 0) {
+    e = allow_smem_pf(ffn_prefill_kernel<2>, Pf<2>::SMEM);
+    if (e != cudaSuccess) return e;
+    ffn_prefill_kernel<2><<<grid, Pf<2>::THREADS, Pf<2>::SMEM, s>>>(Q);
+  } else {
+    e = allow_smem_pf(ffn_prefill_kernel<1>, Pf<1>::SMEM);
+    if (e != cudaSuccess) return e;
+    ffn_prefill_kernel<1><<<grid, Pf<1>::THREADS, Pf<1>::SMEM, s>>>(Q);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pw

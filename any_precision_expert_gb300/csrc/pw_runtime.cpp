@@ -741,8 +741,8 @@ extern "C" pw_status pw_permute(pw_layer_t l, const int32_t* idx, int T, const v
   PW_TRY(check_layer(l));
   if (T < 0 || !offsets) return PW_ERR_INVALID_ARG;
   if (T > 0 && (!idx || !perm_src || !inv_slot || !ws)) return PW_ERR_INVALID_ARG;
-  if ((x == nullptr) != (x_perm == nullptr)) return PW_ERR_INVALID_ARG;
-  if (x && (!aligned16(x) || !aligned16(x_perm))) return PW_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr) != (x_perm == nullptr)) return PW_ERR_INVALID_ARG;
+  if (T > 0 && x && (!aligned16(x) || !aligned16(x_perm))) return PW_ERR_INVALID_ARG;
   const WsLayout W = ws_layout(l, T);
   if (T > 0 && ws_bytes < W.perm_off + W.perm_bytes) return PW_ERR_OOM;
   PW_TRY(device_only());

@@ -1,0 +1,495 @@
+"""Benchmark: routed bit-plane MoE layer (Qwen1.5-MoE-A2.7B-shaped) decode step on GB300.
+
+One step = the whole hot path (router top-K -> permutation -> bit-plane expert
+FFN -> fp16 shared FFN -> weighted combine) over one decode batch of T tokens
+through one layer.  Layer copies (same synthetic weights, distinct pages) are
+visited round-robin so weights stream from HBM, not L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T] [--impl reference]
+
+Prints one JSON line (rank 0).  With torchrun (N > 1) every rank runs an
+independent replica of the layer on its own GPU ("replicas only": the path has
+no exchange step); value = tokens of all ranks / max over ranks of the time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at 1 GB300; achieved HBM GB/s (decode) / tensor util (prefill)"
+WORKLOAD = "qwen1.5-moe-a2.7b-shaped layer decode"
+
+
+def _load_json(path):
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda"):
+    """Upload n_copies of one synthetic layer; returns a dict with host copies for the oracle."""
+    import torch
+
+    import any_precision_expert_gb300 as pw
+    from synth import bits_plan, get_config, make_expert, make_router, make_shared, make_tokens
+
+    cfg = get_config(cfg_name)
+    bits = bits_plan(cfg, seed)
+    wr, bias = make_router(cfg, seed)
+    experts = [make_expert(cfg, e, seed) for e in range(cfg.E)]
+    shared = make_shared(cfg, seed)
+    plane = 3 * cfg.d * cfg.f // 8
+    page = 2 << 20
+    per_layer = 0
+    for b in bits:
+        np_ = 6 if b == 16 else int(b)
+        per_layer += np_ * (plane // page + 2) * page
+        if b == 16:
+            per_layer += (3 * cfg.d * cfg.f * 2 // page + 3) * page
+    per_layer += cfg.E * (2 * cfg.f + cfg.d) * 240 + 3 * cfg.d * cfg.shared_ffn * 2 + 4 * page
+    pool = pw.Pool(n_copies * per_layer + (64 << 20), page_bytes=page, device=device)
+    layers = []
+    for _ in range(n_copies):
+        L = pw.Layer(pool, cfg.d, cfg.f, cfg.E, cfg.K, cfg.renormalize, cfg.shared_ffn)
+        for e, ex in enumerate(experts):
+            L.load_expert(e, int(bits[e]), ex["code6"], ex["lut"], ex["w16"])
+        if shared is not None:
+            L.load_shared(shared)
+        layers.append(L)
+    wr_d = torch.from_numpy(wr).to(device)
+    bias_d = torch.from_numpy(bias).to(device) if bias is not None else None
+    xs = [make_tokens(cfg, T, seed, stream=i) for i in range(n_copies)]
+    xs_d = [torch.from_numpy(x).to(device) for x in xs]
+    bufs = [pw.Buffers(L, T, device=device) for L in layers]
+    torch.cuda.synchronize()
+    return dict(cfg=cfg, bits=bits, wr=wr, bias=bias, experts=experts, shared=shared, pool=pool,
+                layers=layers, wr_d=wr_d, bias_d=bias_d, xs=xs, xs_d=xs_d, bufs=bufs, T=T)
+
+
+def algorithmic_bytes(cfg, bits, offsets, T):
+    """Bytes the method must move for one step (weights of routed experts at their
+    bitwidth plus their LUT_b rows, shared FFN, router, x in, y out)."""
+    d, f = cfg.d, cfg.f
+    n = np.diff(offsets)
+    ffn = 0
+    for e in range(cfg.E):
+        if n[e] == 0:
+            continue
+        b = int(bits[e])
+        ffn += 3 * d * f * 2 if b == 16 else 3 * d * f * b // 8 + (2 * f + d) * (1 << b) * 2
+    shared = 3 * d * cfg.shared_ffn * 2
+    router = d * cfg.E * 2
+    io = 2 * T * d * 2
+    return ffn, ffn + shared + router + io
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import any_precision_expert_gb300 as pw
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if ws == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    T, K, W = args.tokens, args.steps, args.warmup
+    wl = build_workload(n_copies=args.copies, T=T)
+    cfg, layers, bufs, xs_d = wl["cfg"], wl["layers"], wl["bufs"], wl["xs_d"]
+    NL = len(layers)
+    stream = torch.cuda.Stream()
+
+    def step(i, s):
+        j = i % NL
+        pw.moe_forward(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=s)
+
+    # warm-up (eager), then routing is fixed per copy: algorithmic bytes per step
+    with torch.cuda.stream(stream):
+        for i in range(max(W, NL)):
+            step(i, stream)
+    torch.cuda.synchronize()
+    ffn_bytes, step_bytes = [], []
+    for j in range(NL):
+        off = bufs[j].offsets.cpu().numpy()
+        fb, sb = algorithmic_bytes(cfg, wl["bits"], off, T)
+        ffn_bytes.append(fb)
+        step_bytes.append(sb)
+
+    # one CUDA graph of K steps, with events around each expert-FFN call.  The
+    # events are "external" graph nodes (timed when the graph runs); where the
+    # installed torch lacks them, each step is three graphs with ordinary
+    # events between them and the GPU is held briefly so the host can queue
+    # the whole timed region first.
+    import inspect
+    external = "external" in inspect.signature(torch.cuda.Event.__new__).parameters
+
+    def mk_event():
+        return torch.cuda.Event(enable_timing=True, external=True) if external else \
+            torch.cuda.Event(enable_timing=True)
+
+    ev_a = [mk_event() for _ in range(K)]
+    ev_b = [mk_event() for _ in range(K)]
+
+    def part_a(L, b, x):
+        L.route_topk(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, None, stream)
+        L.permute(b.idx, T, x, b.offsets, b.perm_src, b.inv_slot, b.x_perm, b.ws, stream)
+
+    def part_f(L, b, x):
+        L.expert_ffn_bitplane(b.x_perm, b.offsets, T, b.y_perm, b.ws, stream)
+
+    def part_c(L, b, x):
+        L.shared_ffn(x, T, b.y_shared, b.ws, stream)
+        L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared, b.y, stream)
+
+    launches_per_step = 1 + 2 + 2 + 2 + 1  # route, permute(2), ffn(2), shared(2), combine
+    if T > int(os.environ.get("PW_DECODE_MAX_TOK", "48")):
+        launches_per_step += 4  # tcgen05 GEMM kernels for experts above the threshold
+    if external:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                j = i % NL
+                part_a(layers[j], bufs[j], xs_d[j])
+                ev_a[i].record(stream)
+                part_f(layers[j], bufs[j], xs_d[j])
+                ev_b[i].record(stream)
+                part_c(layers[j], bufs[j], xs_d[j])
+
+        def timed_region():
+            g.replay()
+    else:
+        graphs = []
+        for j in range(NL):
+            trio = []
+            for part in (part_a, part_f, part_c):
+                gg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gg, stream=stream):
+                    part(layers[j], bufs[j], xs_d[j])
+                trio.append(gg)
+            graphs.append(trio)
+
+        def timed_region():
+            torch.cuda._sleep(int(60e6))  # hold the GPU while the host queues the region
+            for i in range(K):
+                ga, gf, gc = graphs[i % NL]
+                ga.replay()
+                ev_a[i].record(stream)
+                gf.replay()
+                ev_b[i].record(stream)
+                gc.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_soak = time.time()
+    with torch.cuda.stream(stream):
+        while time.time() - t_soak < args.soak:
+            timed_region()
+            torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    with torch.cuda.stream(stream):
+        if not external:
+            torch.cuda._sleep(int(60e6))
+        t0.record(stream)
+        if external:
+            g.replay()
+        else:
+            for i in range(K):
+                ga, gf, gc = graphs[i % NL]
+                ga.replay()
+                ev_a[i].record(stream)
+                gf.replay()
+                ev_b[i].record(stream)
+                gc.replay()
+        t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms)
+    ffn_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(K)]
+    ffn_avg_ms = sum(ffn_ms) / K
+    ffn_avg_bytes = sum(ffn_bytes[i % NL] for i in range(K)) / K
+    step_avg_bytes = sum(step_bytes[i % NL] for i in range(K)) / K
+
+    # end to end through the public API with pinned host buffers
+    x_host = [torch.from_numpy(x).pin_memory() for x in wl["xs"]]
+    y_host = torch.empty((T, cfg.d), dtype=torch.float16).pin_memory()
+    x_dev = torch.empty((T, cfg.d), dtype=torch.float16, device="cuda")
+    KE = min(K, args.e2e_steps)
+    barrier()
+    te = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(KE):
+            j = i % NL
+            x_dev.copy_(x_host[j], non_blocking=True)
+            y = pw.moe_forward(layers[j], x_dev, wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+            y_host.copy_(y, non_blocking=True)
+            stream.synchronize()
+    barrier()
+    e2e_s = max_over_ranks(time.perf_counter() - te)
+
+    peaks = _load_json(os.path.join(ROOT, "MEASURED_PEAKS.json"))
+    if peaks and peaks.get("hbm_gbs"):
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    else:
+        peak, peak_src = 6800.0, "fallback 6.8 TB/s"
+    achieved = ffn_avg_bytes / (ffn_avg_ms * 1e-3) / 1e9
+    traffic = _traffic_from_profile(T)
+    ok = all(L.check_device() == 0 for L in layers)
+
+    out = None
+    if rank == 0:
+        cpu = cpu_baseline(wl, seconds=args.cpu_seconds) if (ws == 1 and args.cpu_seconds > 0) else None
+        out = {
+            "metric": METRIC,
+            "value": ws * T * K / (ms_max * 1e-3),
+            "unit": "tokens/s",
+            "n_gpus": ws,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": ms_max / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16",
+            "data": "synthetic",
+            "config": {
+                "workload": f"{WORKLOAD} T={T} (d=2048, 60 experts ffn 1408 top-4, fp16 shared FFN 5632, "
+                            f"Zipf(1.1) router bias, greedy floor-respecting bitwidth plan)",
+                "tokens_per_step": T,
+                "bits_plan": {str(b): int((wl["bits"] == b).sum()) for b in (3, 4, 5, 6, 16)},
+                "layer_copies": NL,
+                "l2": f"inputs larger than L2: {NL} layer copies visited round-robin "
+                      f"({step_avg_bytes * (NL - 1) / 1e6:.0f} MB streamed between reuses of a copy)",
+                "timing": ("one CUDA graph of K steps with timed event nodes" if external else
+                           "three CUDA graphs per step, queued ahead of the GPU") + "; CUDA events on the launching stream",
+                "step_algorithmic_bytes": step_avg_bytes,
+                "hbm_GBps_step": step_avg_bytes / ((ms_max / K) * 1e-3) / 1e9,
+                "parallelism": "replicas" if ws > 1 else "single GPU",
+                "device_errors": not ok,
+            },
+            "roofline": {
+                "kernel": "expert FFN call (ffn_decode gate/up + down kernels)",
+                "bound": "hbm",
+                "achieved": achieved,
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": ffn_avg_bytes,
+                "avg_launch_ms": ffn_avg_ms,
+                "peak_source": peak_src,
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": T * cfg.d * 2,
+                    "d2h_bytes_per_step": T * cfg.d * 2, "steps": KE,
+                    "note": "public API (moe_forward) per step: pinned H2D of x, layer, D2H of y, host sync"},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clk,
+        }
+    for L in layers:
+        L.destroy()
+    wl["pool"].close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return out
+
+
+def _traffic_from_profile(T):
+    """DRAM bytes per FFN call from the committed ncu summary, if it matches the current kernel."""
+    prof = _load_json(os.path.join(ROOT, "profiles", "ffn_decode_qwen_traffic.json"))
+    if not prof or int(prof.get("tokens", -1)) != T:
+        return None
+    if prof.get("source_hash") != kernel_source_hash():
+        return None
+    return prof.get("dram_bytes_per_call")
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("pw_ffn.cu", "pw_device.cuh"):
+        with open(os.path.join(ROOT, "any_precision_expert_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle as it stands
+# ---------------------------------------------------------------------------
+
+def _threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, seconds=20.0):
+    """Time the oracle on a bounded sample (the first tokens of the batch)."""
+    from oracle import pw_oracle as O
+
+    cfg = wl["cfg"]
+    x = wl["xs"][0]
+    done, tokens, t_start = 0, 0, time.perf_counter()
+    n = 1
+    while time.perf_counter() - t_start < seconds and done < 64:
+        O.moe_tokens(x, wl["wr"], wl["bias"], lambda e: wl["experts"][e], wl["bits"], cfg.K, cfg.renormalize,
+                     list(range(done % x.shape[0], done % x.shape[0] + n)), shared=wl["shared"])
+        done += 1
+        tokens += n
+    el = time.perf_counter() - t_start
+    return {"value": tokens / el, "unit": "tokens/s", "cores": _threads(), "kind": "oracle",
+            "sample": f"{tokens} decode tokens of the same layer, one token per oracle call "
+                      f"({el:.1f} s of CPU work, numpy fp64, BLAS threads={_threads()}, os.cpu_count={os.cpu_count()})"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    from synth import bits_plan, get_config, make_expert, make_router, make_shared, make_tokens
+    from oracle import pw_oracle as O
+
+    cfg = get_config("qwen")
+    T = args.tokens
+    bits = bits_plan(cfg, 0)
+    wr, bias = make_router(cfg, 0)
+    experts = [make_expert(cfg, e, 0) for e in range(cfg.E)]
+    shared = make_shared(cfg, 0)
+    x = make_tokens(cfg, T, 0, stream=0)
+
+    def one(i):
+        t = i % T
+        O.moe_tokens(x, wr, bias, lambda e: experts[e], bits, cfg.K, cfg.renormalize, [t], shared=shared)
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(args.warmup + i)
+    el = time.perf_counter() - t0
+    v = args.steps / el
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD} T={T} (same layer as the GPU arm)", "tokens_per_step": 1},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _threads(), "kind": "oracle",
+                             "sample": "one decode token of the batch per step (numpy fp64 oracle)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--copies", type=int, default=6)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load for the clock record")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
+    out = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -53,7 +53,7 @@ def test_route_topk(name, T, kw):
     cfg = get_config(name, **kw)
     wr, bias = make_router(cfg, seed=1)
     x = make_tokens(cfg, T, seed=1)
-    pool = pw.Pool(64 << 20)
+    pool = pw.Pool(cfg.E * (2 * cfg.f + cfg.d) * 240 + (64 << 20))  # resident LUTs of every expert
     layer = pw.Layer(pool, cfg.d, cfg.f, cfg.E, cfg.K, cfg.renormalize)
     try:
         xd = torch.from_numpy(x).cuda()
@@ -232,6 +232,67 @@ def test_empty_batch():
         y = pw.moe_forward(gl.layer, x, gl.wr_d, gl.bias_d, buf)
         torch.cuda.synchronize()
         assert y.shape == (0, cfg.d)
+        assert gl.layer.check_device() == 0
+    finally:
+        gl.close()
+
+
+# ---------------------------------------------------------------------------
+# prefill path: experts with many tokens go through the tcgen05 GEMM
+# ---------------------------------------------------------------------------
+
+@pytest.fixture
+def decode_max_tok(monkeypatch):
+    def set_(v):
+        monkeypatch.setenv("PW_DECODE_MAX_TOK", str(v))
+    return set_
+
+
+def test_prefill_tiny_all_bitwidths(decode_max_tok):
+    cfg = get_config("tiny")
+    gl = GpuLayer(cfg, seed=8)
+    try:
+        decode_max_tok(16)
+        r = gl.check_forward(gl.tokens(400))   # ~100 tokens per expert: ragged 256-token tiles
+        assert r["buf"].idx is not None
+        assert gl.layer.check_device() == 0
+    finally:
+        gl.close()
+
+
+def test_prefill_matches_decode_path(decode_max_tok):
+    cfg = get_config("tiny", d=1024, f=2048, E=4, K=2)
+    gl = GpuLayer(cfg, seed=9, bits=[3, 5, 16, 6], with_w16=False)
+    try:
+        x = gl.tokens(300)
+        decode_max_tok(0)            # every expert through tcgen05
+        a = gl.check_forward(x)
+        decode_max_tok(100000)       # every expert through mma.sync
+        b = gl.check_forward(x)
+        assert np.abs(a["y"] - b["y"]).max() < 4e-3 * (1 + np.abs(b["y"]).max())
+        assert gl.layer.check_device() == 0
+    finally:
+        gl.close()
+
+
+def test_prefill_ragged_rows_e128_shape(decode_max_tok):
+    # ffn = 704 rows is 5.5 tiles of 128 rows for gate/up
+    cfg = get_config("e128", E=8, K=2)
+    gl = GpuLayer(cfg, seed=10, bits=[3, 4, 6, 16, 5, 3, 4, 6], with_w16=False)
+    try:
+        decode_max_tok(8)
+        gl.check_forward(gl.tokens(260))
+        assert gl.layer.check_device() == 0
+    finally:
+        gl.close()
+
+
+def test_prefill_shared_ffn(decode_max_tok):
+    cfg = get_config("qwen", E=6, K=2, shared_ffn=512)
+    gl = GpuLayer(cfg, seed=11, with_w16=False)
+    try:
+        decode_max_tok(32)
+        gl.check_forward(gl.tokens(200))
         assert gl.layer.check_device() == 0
     finally:
         gl.close()

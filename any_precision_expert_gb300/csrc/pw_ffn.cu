@@ -307,18 +307,6 @@ __global__ void __launch_bounds__(kFfnThreads, 2) ffn_decode_kernel(FfnParams P)
   }
 }
 
-namespace {
-template <typename Kern>
-cudaError_t allow_smem(Kern k, size_t bytes) {
-  static int done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && done[dev] >= (int)bytes) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess && dev < 64) done[dev] = (int)bytes;
-  return e;
-}
-}  // namespace
 
 cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* offsets, int n_slots, float* y,
                        __half* h_ws, cudaStream_t s) {
@@ -338,9 +326,9 @@ cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* 
   const int grid = sm_count() * 2;
   const size_t smem0 = 2 * kTabBytes + (size_t)kFfnWarps * 2 * kNT * 32 * 16;
   const size_t smem1 = 1 * kTabBytes + (size_t)kFfnWarps * 1 * kNT * 32 * 16;
-  cudaError_t e = allow_smem(ffn_decode_kernel<2>, smem0);
+  cudaError_t e = ensure_smem((const void*)ffn_decode_kernel<2>, smem0);
   if (e != cudaSuccess) return e;
-  e = allow_smem(ffn_decode_kernel<1>, smem1);
+  e = ensure_smem((const void*)ffn_decode_kernel<1>, smem1);
   if (e != cudaSuccess) return e;
   P.phase = 0;
   P.act = x;
@@ -433,7 +421,7 @@ __global__ void __launch_bounds__(kFfnThreads) debug_dequant_kernel(DevLayer L, 
 
 cudaError_t launch_debug_dequant(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {
   const int R = m < 2 ? L.f : L.d;
-  cudaError_t err = allow_smem(debug_dequant_kernel, kTabBytes);
+  cudaError_t err = ensure_smem((const void*)debug_dequant_kernel, kTabBytes);
   if (err != cudaSuccess) return err;
   debug_dequant_kernel<<<R / 16, kFfnThreads, kTabBytes, s>>>(L, e, m, out);
   return cudaGetLastError();

@@ -39,6 +39,8 @@ struct FfnScratch {
 };
 
 int sm_count();
+// Opt a kernel into `bytes` of dynamic shared memory (once per kernel and device).
+cudaError_t ensure_smem(const void* kernel, size_t bytes);
 
 cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s);
 cudaError_t launch_route(const DevLayer& L, const __half* x, const __half* wr, const float* bias,

@@ -7,6 +7,10 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "pw_device.cuh"
 
 namespace pw {
@@ -16,6 +20,19 @@ int sm_count() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 1;
+}
+
+cudaError_t ensure_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = done[std::make_pair(kernel, dev)];
+  if (have >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -150,7 +167,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const 
 cudaError_t launch_route(const DevLayer& L, const __half* x, const __half* wr, const float* bias, int T, int* idx,
                          float* w, int* counts, cudaStream_t s) {
   const size_t smem = (size_t)kRouteTok * L.d * sizeof(__half) + (size_t)kRouteTok * L.E * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem((const void*)route_kernel, smem);
   if (e != cudaSuccess) return e;
   const int grid = (T + kRouteTok - 1) / kRouteTok;
   route_kernel<<<grid, kRouteThreads, smem, s>>>(L, x, wr, bias, T, idx, w, counts);

@@ -427,18 +427,6 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1) ffn_prefill_kernel(PfParam
   }
 }
 
-namespace {
-template <typename Kern>
-cudaError_t allow_smem_pf(Kern k, size_t bytes) {
-  static int done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && done[dev] >= (int)bytes) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess && dev < 64) done[dev] = (int)bytes;
-  return e;
-}
-}  // namespace
 
 int decode_max_tokens() {
   // experts with more tokens than this use the tensor-core GEMM (read per call)
@@ -461,11 +449,11 @@ cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half*
   const int grid = sm_count();
   cudaError_t e;
   if (phase == 0) {
-    e = allow_smem_pf(ffn_prefill_kernel<2>, Pf<2>::SMEM);
+    e = ensure_smem((const void*)ffn_prefill_kernel<2>, Pf<2>::SMEM);
     if (e != cudaSuccess) return e;
     ffn_prefill_kernel<2><<<grid, Pf<2>::THREADS, Pf<2>::SMEM, s>>>(Q);
   } else {
-    e = allow_smem_pf(ffn_prefill_kernel<1>, Pf<1>::SMEM);
+    e = ensure_smem((const void*)ffn_prefill_kernel<1>, Pf<1>::SMEM);
     if (e != cudaSuccess) return e;
     ffn_prefill_kernel<1><<<grid, Pf<1>::THREADS, Pf<1>::SMEM, s>>>(Q);
   }

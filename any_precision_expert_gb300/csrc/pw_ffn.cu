@@ -1,19 +1,27 @@
 // Grouped expert SwiGLU FFN for decode-sized batches, reading bit-planes
 // through the per-expert page table.
 //
-// PagedWeight (zhichai.net/topic/178446964, "核心洞察"): each expert weight is
-// an any-precision code stored as bit-planes plus a LUT; at bitwidth b only the
-// top b planes exist for the kernel, so bytes read scale with b/16 of fp16.
+// PagedWeight (write-up "内存的饥饿游戏", section 核心洞察): each expert weight
+// is an any-precision code stored as bit-planes plus a LUT; at bitwidth b only
+// the top b planes are read, so bytes scale with b/16 of fp16.
 //
-// Work item = (expert, 32-token chunk, 16-row tile of the output).  A CTA of 8
-// warps splits the reduction dimension into groups of four 64-column chunks;
-// each lane loads one 16-byte word run per plane per group (coalesced, read
-// once), turns the planes into codes with masks and rotations, looks the codes
-// up in a per-lane copy of the tile's LUT in shared memory, and feeds the fp16
-// weights straight into mma.sync m16n8k16 (weights as A, tokens as B).  Phase
-// 0 computes gate and up for the same rows and writes h = silu(g) * u (fp16);
-// phase 1 computes down and writes y (fp32).  The item list is derived on the
-// device from the expert offsets, so no host synchronisation is needed.
+// Work item = (expert, 32-token chunk, block of `rw` 16-row output tiles).  The
+// 8 warps of a CTA cover the block: 8/rw warps per tile split the reduction
+// into units (256-column plane groups, or 64-column chunks of fp16 pages) and
+// are reduced through shared memory when 8/rw > 1.  Every lane streams its own
+// weight words with cp.async into a private ring of shared memory, three units
+// ahead of the one it decodes, so a warp keeps several kilobytes in flight
+// without spending registers.  Codes are decoded with masks and one rotation
+// per four codes; 3-bit codes are looked up with byte permutes from LUT
+// registers, 4..6-bit codes in per-lane shared-memory LUT copies; the fp16
+// weights feed mma.sync m16n8k16 (weights as A, tokens as B, fp32
+// accumulation).  Activations are read through L1 so the warps of a block
+// share them.  rw is the largest of 8, 4, 2, 1 that still gives every CTA an
+// item (and whose LUT tables fit in 64 KB).  Two kernel classes: b in {3, 16}
+// (no tables, two CTAs per SM) and b in {4, 5, 6} (tables).  Phase 0 computes
+// gate and up for the same rows and writes h = silu(g) * u (fp16); phase 1
+// computes down and writes y (fp32).  Items are derived on the device from the
+// expert offsets, so no host synchronisation is needed.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -25,9 +33,27 @@ namespace pw {
 
 constexpr int kFfnThreads = 256;
 constexpr int kFfnWarps = kFfnThreads / 32;
-constexpr int kTok = 32;            // tokens per work item
-constexpr int kNT = kTok / 8;       // mma n-tiles per item
-constexpr int kTabBytes = 64 * 256; // LUT table of one matrix at b <= 6
+constexpr int kTok = 32;               // tokens per work item
+constexpr int kNT = kTok / 8;          // mma n-tiles per item
+constexpr int kTabBudget = 64 * 1024;  // LUT tables of one item (table class)
+constexpr int kTabBytes = 64 * 256;    // LUT table of one 16-row tile of one matrix at b = 6
+
+// Kernel classes: 0 = bitwidths 3 and 16 (register LUT / no LUT), 1 = 4, 5, 6.
+__host__ __device__ constexpr bool in_class(int b, int cls) {
+  return cls == 0 ? (b == 3 || b == 16) : (b >= 4 && b <= 6);
+}
+
+template <int NM, int CLS>
+struct Dec {
+  static constexpr int RING = CLS == 0 ? 3 : 2;                 // units in flight per lane
+  static constexpr int UNIT = CLS == 0 ? NM * 4 * 16 : NM * 6 * 16;  // bytes per lane per unit
+  static constexpr int WARP_RING = RING * UNIT * 32;
+  static constexpr int TABS = CLS == 0 ? 0 : kTabBudget;
+  static constexpr int RED = kFfnWarps * NM * kNT * 32 * 16;
+  static constexpr int RINGS = kFfnWarps * WARP_RING > RED ? kFfnWarps * WARP_RING : RED;
+  static constexpr int SMEM = TABS + RINGS;
+  static constexpr int MIN_BLOCKS = CLS == 0 ? 2 : 1;
+};
 
 struct FfnParams {
   DevLayer L;
@@ -41,115 +67,148 @@ struct FfnParams {
   float* y;              // [slots][d]
 };
 
-template <int NM>
-__device__ __forceinline__ void store_partials(float* red, int warp, int lane, const float (&acc)[NM][kNT][4]) {
-#pragma unroll
-  for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
-      reinterpret_cast<float4*>(red)[((warp * NM + mi) * kNT + nt) * 32 + lane] =
-          make_float4(acc[mi][nt][0], acc[mi][nt][1], acc[mi][nt][2], acc[mi][nt][3]);
+// Largest number of 16-row tiles per item whose LUT tables fit the budget.
+__device__ __forceinline__ int rw_cap(int b, int NM) {
+  if (b == 3 || b == 16) return 8;
+  return min(8, kTabBudget / (NM * (1 << b) * 256));
 }
 
-// Main loop of one item for a bit-plane expert at bitwidth B.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// 3-bit codes: byte-permute lookups from registers.
+// lut[r] = {lo bytes of entries 0-3, lo 4-7, hi 0-3, hi 4-7} of row g (r = 0)
+// or g + 8 (r = 1).  Plane p keeps code bit 2-p of weight (s, nibble n) at bit
+// 4n + s + 5 - p; masking with rotl(0x11111111, s+5-p) and rotating right by
+// s+3 puts the code of (s, n) in nibble n (bit 3 clear), so the low half
+// selects row g's four codes and the high half row g+8's.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void decode_step_prmt3(const uint32_t (&w)[3], const int s, const uint32_t (&lut)[2][4],
+                                                  uint32_t (&a)[4]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int p = 0; p < 3; ++p) m |= w[p] & rotl_c(0x11111111u, s + 5 - p);
+  const uint32_t sel0 = rotr(m, s + 3), sel1 = rotr(m, s + 19);
+  uint32_t lo = prmt(lut[0][0], lut[0][1], sel0), hi = prmt(lut[0][2], lut[0][3], sel0);
+  a[0] = prmt(lo, hi, 0x5140u);
+  a[2] = prmt(lo, hi, 0x7362u);
+  lo = prmt(lut[1][0], lut[1][1], sel1);
+  hi = prmt(lut[1][2], lut[1][3], sel1);
+  a[1] = prmt(lo, hi, 0x5140u);
+  a[3] = prmt(lo, hi, 0x7362u);
+}
+
+__device__ __forceinline__ void load_lut3(const __half* row, uint32_t (&r)[4]) {
+  const uint4 v = *reinterpret_cast<const uint4*>(row);
+  r[0] = prmt(v.x, v.y, 0x6420u);
+  r[1] = prmt(v.z, v.w, 0x6420u);
+  r[2] = prmt(v.x, v.y, 0x7531u);
+  r[3] = prmt(v.z, v.w, 0x7531u);
+}
+
+__device__ __forceinline__ void load_bfrag(const __half* act, const int (&rowoff)[kNT], int NT, int col,
+                                           uint32_t (&bf)[kNT][2]) {
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    if (nt < NT) {
+      const __half* xp = act + rowoff[nt] + col;
+      bf[nt][0] = *reinterpret_cast<const uint32_t*>(xp);
+      bf[nt][1] = *reinterpret_cast<const uint32_t*>(xp + 8);
+    }
+  }
+}
+
+// Issue the copies of plane group gamma (NM matrices, B planes) into ring slot `slot`:
+// slot layout [matrix*B + plane][lane] x 16 bytes.
 template <int B, int NM>
-__device__ __forceinline__ void item_planes(const FfnParams& P, const char* const* s_base, uint32_t tab0, int K,
-                                            const int (&rowoff)[kNT], int NT, float (&acc)[NM][kNT][4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ void issue_group(const char* const (&base)[NM][6], int gamma, int G, int rem, int lane,
+                                            uint32_t slot) {
+  if (gamma < G) {
+    const size_t off = (size_t)(gamma * 128 + lane * 4) * 4;
+#pragma unroll
+    for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+      for (int p = 0; p < B; ++p) cp_async16(slot + ((mi * B + p) * 32 + lane) * 16, base[mi][p] + off);
+  } else {
+    const size_t off = (size_t)(G * 128 + lane * rem) * 4;
+#pragma unroll
+    for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+      for (int p = 0; p < B; ++p)
+        for (int i = 0; i < rem; ++i) cp_async4(slot + ((mi * B + p) * 32 + lane) * 16 + 4 * i, base[mi][p] + off + 4 * i);
+  }
+}
+
+// K loop of one warp over its plane groups (gamma = g0, g0 + gstep, ...).
+// lut3: register LUTs (B == 3); tab: smem table of (tile, matrix 0) (B >= 4).
+template <int B, int NM, int RING>
+__device__ __forceinline__ void warp_planes(const __half* act, const char* const (&base)[NM][6], int K, int g0,
+                                            int gstep, const int (&rowoff)[kNT], int NT,
+                                            const uint32_t (&lut3)[NM][2][4], uint32_t tab, uint32_t tab_stride,
+                                            uint32_t ring, float (&acc)[NM][kNT][4]) {
+  const int lane = threadIdx.x & 31;
   const int nk = K / 64, G = nk / 4, rem = nk % 4, NG = G + (rem ? 1 : 0);
   const uint32_t lb0 = lane * 4, lb1 = 128 + lane * 4;
-  const __half* act = P.act;
-  for (int gamma = warp; gamma < NG; gamma += kFfnWarps) {
-    uint32_t wv[NM][B][4];
-    const bool full = gamma < G;
-    const int nch = full ? 4 : rem;
-    if (full) {
-      const size_t off = (size_t)(gamma * 128 + lane * 4) * 4;
+  constexpr uint32_t kSlot = NM * B * 32 * 16;
+  const int nu = g0 < NG ? (NG - 1 - g0) / gstep + 1 : 0;
 #pragma unroll
-      for (int mi = 0; mi < NM; ++mi)
+  for (int i = 0; i < RING - 1; ++i) {
+    if (i < nu) issue_group<B, NM>(base, g0 + i * gstep, G, rem, lane, ring + (i % RING) * kSlot);
+    cp_commit();
+  }
+  for (int i = 0; i < nu; ++i) {
+    const int inext = i + RING - 1;
+    if (inext < nu) issue_group<B, NM>(base, g0 + inext * gstep, G, rem, lane, ring + (inext % RING) * kSlot);
+    cp_commit();
+    cp_wait<RING - 1>();
+    const int gamma = g0 + i * gstep;
+    const uint32_t slot = ring + (i % RING) * kSlot;
+    uint32_t cur[NM][B][4];
 #pragma unroll
-        for (int p = 0; p < B; ++p) {
-          const uint4 v = ldg_stream(s_base[mi * kPlanes + p] + off);
-          wv[mi][p][0] = v.x;
-          wv[mi][p][1] = v.y;
-          wv[mi][p][2] = v.z;
-          wv[mi][p][3] = v.w;
-        }
-    } else {
-      const size_t off = (size_t)(G * 128 + lane * rem) * 4;
+    for (int mi = 0; mi < NM; ++mi)
 #pragma unroll
-      for (int mi = 0; mi < NM; ++mi)
+      for (int p = 0; p < B; ++p) {
+        const uint4 v = lds128(slot + ((mi * B + p) * 32 + lane) * 16);
+        cur[mi][p][0] = v.x;
+        cur[mi][p][1] = v.y;
+        cur[mi][p][2] = v.z;
+        cur[mi][p][3] = v.w;
+      }
+    const int nch = gamma < G ? 4 : rem;
 #pragma unroll
-        for (int p = 0; p < B; ++p)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) wv[mi][p][i] = i < rem ? ldg_stream32(s_base[mi * kPlanes + p] + off + 4 * i) : 0u;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (i >= nch) break;
-      const int kappa = 4 * gamma + i;
+    for (int c = 0; c < 4; ++c) {
+      if (c >= nch) break;
+      const int kappa = 4 * gamma + c;
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        const int col = kappa * 64 + s * 16;
         uint32_t bf[kNT][2];
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          if (nt < NT) {
-            const __half* xp = act + rowoff[nt] + col;
-            bf[nt][0] = *reinterpret_cast<const uint32_t*>(xp);
-            bf[nt][1] = *reinterpret_cast<const uint32_t*>(xp + 8);
-          }
-        }
+        load_bfrag(act, rowoff, NT, kappa * 64 + s * 16, bf);
 #pragma unroll
         for (int mi = 0; mi < NM; ++mi) {
           uint32_t w[B];
 #pragma unroll
-          for (int p = 0; p < B; ++p) w[p] = wv[mi][p][i];
+          for (int p = 0; p < B; ++p) w[p] = cur[mi][p][c];
           uint32_t a[4];
-          decode_step_lut<B>(w, s, tab0 + mi * kTabBytes, lb0, lb1, a);
-#pragma unroll
-          for (int nt = 0; nt < kNT; ++nt)
-            if (nt < NT) mma16816(acc[mi][nt], a, bf[nt][0], bf[nt][1]);
-        }
-      }
-    }
-  }
-}
-
-// Main loop of one item for fp16 weights (fallback pages or the shared FFN).
-template <int NM>
-__device__ __forceinline__ void item_f16(const FfnParams& P, const char* const* s_base16, int K,
-                                         const int (&rowoff)[kNT], int NT, float (&acc)[NM][kNT][4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nk = K / 64;
-  const __half* act = P.act;
-  // chunks are split across warps in the same groups of four as the planes
-  const int G = nk / 4, rem = nk % 4, NG = G + (rem ? 1 : 0);
-  for (int gamma = warp; gamma < NG; gamma += kFfnWarps) {
-    const int nch = gamma < G ? 4 : rem;
-    for (int i = 0; i < nch; ++i) {
-      const int kappa = 4 * gamma + i;
-      uint4 A[NM][4];
-#pragma unroll
-      for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          A[mi][s] = ldg_stream(s_base16[mi] + ((size_t)(kappa * 4 + s) * 32 + lane) * 16);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int col = kappa * 64 + s * 16;
-        uint32_t bf[kNT][2];
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          if (nt < NT) {
-            const __half* xp = act + rowoff[nt] + col;
-            bf[nt][0] = *reinterpret_cast<const uint32_t*>(xp);
-            bf[nt][1] = *reinterpret_cast<const uint32_t*>(xp + 8);
+          if constexpr (B == 3) {
+            decode_step_prmt3(w, s, lut3[mi], a);
+          } else {
+            decode_step_lut<B>(w, s, tab + mi * tab_stride, lb0, lb1, a);
           }
-        }
-#pragma unroll
-        for (int mi = 0; mi < NM; ++mi) {
-          const uint32_t a[4] = {A[mi][s].x, A[mi][s].y, A[mi][s].z, A[mi][s].w};
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt)
             if (nt < NT) mma16816(acc[mi][nt], a, bf[nt][0], bf[nt][1]);
@@ -157,16 +216,63 @@ __device__ __forceinline__ void item_f16(const FfnParams& P, const char* const* 
       }
     }
   }
+  cp_wait<0>();
 }
 
-template <int NM>
-__global__ void __launch_bounds__(kFfnThreads, 2) ffn_decode_kernel(FfnParams P) {
+// K loop of one warp over its 64-column chunks of fp16 weights (fallback pages
+// or the shared FFN): chunk kappa = k0, k0 + kstep, ...
+template <int NM, int RING>
+__device__ __forceinline__ void warp_f16(const __half* act, const char* const (&base16)[NM], int K, int k0,
+                                         int kstep, const int (&rowoff)[kNT], int NT, uint32_t ring,
+                                         float (&acc)[NM][kNT][4]) {
+  const int lane = threadIdx.x & 31;
+  const int nk = K / 64;
+  constexpr uint32_t kSlot = NM * 4 * 32 * 16;
+  const int nu = k0 < nk ? (nk - 1 - k0) / kstep + 1 : 0;
+  auto issue = [&](int kappa, uint32_t slot) {
+#pragma unroll
+    for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        cp_async16(slot + ((mi * 4 + s) * 32 + lane) * 16, base16[mi] + ((size_t)(kappa * 4 + s) * 32 + lane) * 16);
+  };
+#pragma unroll
+  for (int i = 0; i < RING - 1; ++i) {
+    if (i < nu) issue(k0 + i * kstep, ring + (i % RING) * kSlot);
+    cp_commit();
+  }
+  for (int i = 0; i < nu; ++i) {
+    const int inext = i + RING - 1;
+    if (inext < nu) issue(k0 + inext * kstep, ring + (inext % RING) * kSlot);
+    cp_commit();
+    cp_wait<RING - 1>();
+    const int kappa = k0 + i * kstep;
+    const uint32_t slot = ring + (i % RING) * kSlot;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t bf[kNT][2];
+      load_bfrag(act, rowoff, NT, kappa * 64 + s * 16, bf);
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi) {
+        const uint4 v = lds128(slot + ((mi * 4 + s) * 32 + lane) * 16);
+        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+          if (nt < NT) mma16816(acc[mi][nt], a, bf[nt][0], bf[nt][1]);
+      }
+    }
+  }
+  cp_wait<0>();
+}
+
+template <int NM, int CLS>
+__global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_decode_kernel(FfnParams P) {
+  using D = Dec<NM, CLS>;
   extern __shared__ __align__(16) unsigned char smem_ffn[];
   __shared__ int s_pref[kMaxExperts + 1];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_bits[kMaxExperts];
-  __shared__ const char* s_base[NM * kPlanes];
-  __shared__ const char* s_base16[NM];
+  __shared__ int s_rw;
 
   const DevLayer& L = P.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -186,14 +292,25 @@ __global__ void __launch_bounds__(kFfnThreads, 2) ffn_decode_kernel(FfnParams P)
   }
   __syncthreads();
   if (warp == 0) {
+    // items at the largest tile-block size that still feeds every CTA
+    auto count = [&](int e, int RW) {
+      const int n = s_off[e + 1] - s_off[e];
+      if (n == 0 || n > P.max_tokens || !in_class(s_bits[e], CLS)) return 0;
+      const int rw = min(RW, rw_cap(s_bits[e], NM));
+      return ((n + kTok - 1) / kTok) * ((tiles + rw - 1) / rw);
+    };
+    int RW = 8;
+    for (; RW > 1; RW >>= 1) {
+      int tot = 0;
+      for (int e = lane; e < E; e += 32) tot += count(e, RW);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      if (tot >= (int)gridDim.x) break;
+    }
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      int c = 0;
-      if (e < E) {
-        const int n = s_off[e + 1] - s_off[e];
-        c = n <= P.max_tokens ? ((n + kTok - 1) / kTok) * tiles : 0;
-      }
+      const int c = e < E ? count(e, RW) : 0;
       int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -203,13 +320,19 @@ __global__ void __launch_bounds__(kFfnThreads, 2) ffn_decode_kernel(FfnParams P)
       if (e < E) s_pref[e] = run + incl - c;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) s_pref[E] = run;
+    if (lane == 0) {
+      s_pref[E] = run;
+      s_rw = RW;
+    }
   }
   __syncthreads();
   const int total = s_pref[E];
+  const int RW = s_rw;
 
-  float* red = reinterpret_cast<float*>(smem_ffn + NM * kTabBytes);
   const uint32_t tab0 = smem_u32(smem_ffn);
+  const uint32_t rings = tab0 + D::TABS;
+  const uint32_t ring = rings + warp * D::WARP_RING;
+  float* red = reinterpret_cast<float*>(smem_ffn + D::TABS);  // aliases the rings after the K loop
 
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
     int lo = 0, hi = E;  // find e with s_pref[e] <= item < s_pref[e+1]
@@ -218,47 +341,39 @@ __global__ void __launch_bounds__(kFfnThreads, 2) ffn_decode_kernel(FfnParams P)
       if (s_pref[mid] <= item) lo = mid; else hi = mid;
     }
     const int e = lo;
+    const int b = s_bits[e];
+    const int n_e = s_off[e + 1] - s_off[e];
+    const int nch = (n_e + kTok - 1) / kTok;
     const int local = item - s_pref[e];
-    const int tau = local % tiles, chunk = local / tiles;
+    // token chunks of one tile block are adjacent, so their weight re-reads hit L2
+    const int blk = local / nch, chunk = local % nch;
+    const int rw = min(RW, rw_cap(b, NM));
+    const int wpt = kFfnWarps / rw;                 // warps per tile
+    const int tile0 = blk * rw;
+    const int ntl = min(rw, tiles - tile0);         // tiles in this item
+    const int jt = warp / wpt, kpart = warp % wpt;  // this warp's tile and reduction part
+    const bool active = jt < ntl;
+    const int tau = tile0 + (active ? jt : 0);
     const int slot0 = s_off[e] + chunk * kTok;
     const int ntok = min(kTok, s_off[e + 1] - slot0);
     const int NT = (ntok + 7) >> 3;
-    const int b = s_bits[e];
+    const uint32_t tstride = CLS == 1 ? (uint32_t)(1 << b) * 256u : 0u;
 
-    if (tid < NM * kPlanes) {
-      const int mi = tid / kPlanes, p = tid % kPlanes;
-      const int m = P.phase == 0 ? mi : 2;
-      s_base[tid] = (routed && p < b && b <= 6) ? tile_addr(L, e, m, p, tau) : nullptr;
-    }
-    if (tid < NM) {
-      const int m = P.phase == 0 ? tid : 2;
-      if (routed)
-        s_base16[tid] = b == 16 ? tile_addr(L, e, m, kPlanes, tau) : nullptr;
-      else
-        s_base16[tid] = reinterpret_cast<const char*>(L.shared16[m]) + (size_t)tau * 32 * K;
-    }
-    if (b <= 6) {
-      for (int mi = 0; mi < NM; ++mi) {
+    if (CLS == 1) {  // per-lane LUT copies of every (tile, matrix) of the item
+      for (int q = 0; q < ntl * NM; ++q) {
+        const int j = q / NM, mi = q % NM;
         const int m = P.phase == 0 ? mi : 2;
-        uint32_t* tab = reinterpret_cast<uint32_t*>(smem_ffn + mi * kTabBytes);
-        const __half* lr = lut_rows(L, e, m, b, tau * kTileRows);
+        uint32_t* tab = reinterpret_cast<uint32_t*>(smem_ffn + q * tstride);
+        const __half* lr = lut_rows(L, e, m, b, (tile0 + j) * kTileRows);
         switch (b) {
-          case 3: build_lut_table<3>(lr, tab, tid, kFfnThreads); break;
           case 4: build_lut_table<4>(lr, tab, tid, kFfnThreads); break;
           case 5: build_lut_table<5>(lr, tab, tid, kFfnThreads); break;
           default: build_lut_table<6>(lr, tab, tid, kFfnThreads); break;
         }
       }
+      __syncthreads();
     }
-    __syncthreads();
 
-    // B-fragment row offsets: token n = nt*8 + g (clamped into the item), column 2t
-    int rowoff[kNT];
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-      const int tok = min(nt * 8 + (lane >> 2), ntok - 1);
-      rowoff[nt] = (slot0 + tok) * K + 2 * (lane & 3);
-    }
     float acc[NM][kNT][4];
 #pragma unroll
     for (int mi = 0; mi < NM; ++mi)
@@ -267,54 +382,123 @@ __global__ void __launch_bounds__(kFfnThreads, 2) ffn_decode_kernel(FfnParams P)
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[mi][nt][r] = 0.f;
 
-    switch (b) {
-      case 3: item_planes<3, NM>(P, s_base, tab0, K, rowoff, NT, acc); break;
-      case 4: item_planes<4, NM>(P, s_base, tab0, K, rowoff, NT, acc); break;
-      case 5: item_planes<5, NM>(P, s_base, tab0, K, rowoff, NT, acc); break;
-      case 6: item_planes<6, NM>(P, s_base, tab0, K, rowoff, NT, acc); break;
-      case 16: item_f16<NM>(P, s_base16, K, rowoff, NT, acc); break;
-      default:
-        if (tid == 0) atomicExch(L.err, 3);
-        break;
-    }
-    store_partials<NM>(red, warp, lane, acc);
-    __syncthreads();
-
-    // cross-warp reduction and epilogue: element (token j, row r) of the tile
-    for (int idx = tid; idx < kTok * kTileRows; idx += kFfnThreads) {
-      const int j = idx >> 4, r = idx & 15;
-      if (j >= ntok) continue;
-      const int nt = j >> 3, jj = j & 7;
-      const int ln = 4 * (r & 7) + (jj >> 1);
-      const int reg = 2 * (r >> 3) + (jj & 1);
-      float sum[NM];
+    if (active) {
+      // B-fragment row offsets: token n = nt*8 + g (clamped into the item), column 2t
+      int rowoff[kNT];
 #pragma unroll
-      for (int mi = 0; mi < NM; ++mi) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kFfnWarps; ++w) v += red[(((w * NM + mi) * kNT + nt) * 32 + ln) * 4 + reg];
-        sum[mi] = v;
+      for (int nt = 0; nt < kNT; ++nt) {
+        const int tok = min(nt * 8 + (lane >> 2), ntok - 1);
+        rowoff[nt] = (slot0 + tok) * K + 2 * (lane & 3);
       }
-      const int row = tau * kTileRows + r;
-      if (NM == 2) {
-        const float hv = silu_f(sum[0]) * sum[NM - 1];
-        P.h[(size_t)(slot0 + j) * fe + row] = __float2half_rn(hv);
+      if (CLS == 0 && b == 16) {
+        const char* b16[NM];
+#pragma unroll
+        for (int mi = 0; mi < NM; ++mi) {
+          const int m = P.phase == 0 ? mi : 2;
+          b16[mi] = routed ? tile_addr(L, e, m, kPlanes, tau)
+                           : reinterpret_cast<const char*>(L.shared16[m]) + (size_t)tau * 32 * K;
+        }
+        warp_f16<NM, D::RING>(P.act, b16, K, kpart, wpt, rowoff, NT, ring, acc);
       } else {
-        P.y[(size_t)(slot0 + j) * L.d + row] = sum[0];
+        const char* base[NM][6];
+#pragma unroll
+        for (int mi = 0; mi < NM; ++mi) {
+          const int m = P.phase == 0 ? mi : 2;
+#pragma unroll
+          for (int p = 0; p < 6; ++p) base[mi][p] = p < b ? tile_addr(L, e, m, p, tau) : nullptr;
+        }
+        uint32_t lut3[NM][2][4];
+        const uint32_t tab = tab0 + (uint32_t)(jt * NM) * tstride;
+        if (CLS == 0) {
+#pragma unroll
+          for (int mi = 0; mi < NM; ++mi) {
+            const int m = P.phase == 0 ? mi : 2;
+            const __half* lr = lut_rows(L, e, m, 3, tau * kTileRows);
+            load_lut3(lr + (lane >> 2) * 8, lut3[mi][0]);
+            load_lut3(lr + ((lane >> 2) + 8) * 8, lut3[mi][1]);
+          }
+          warp_planes<3, NM, D::RING>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc);
+        } else {
+          switch (b) {
+            case 4: warp_planes<4, NM, D::RING>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
+            case 5: warp_planes<5, NM, D::RING>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
+            default: warp_planes<6, NM, D::RING>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
+          }
+        }
+      }
+    }
+
+    // epilogue: C fragment (row g / g+8, token nt*8 + 2t + {0,1})
+    const int g = lane >> 2, t = lane & 3;
+    if (wpt == 1) {
+      if (active) {
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = nt * 8 + 2 * t + (r & 1);
+            const int row = tau * kTileRows + g + 8 * (r >> 1);
+            if (j < ntok) {
+              if (NM == 2)
+                P.h[(size_t)(slot0 + j) * fe + row] = __float2half_rn(silu_f(acc[0][nt][r]) * acc[NM - 1][nt][r]);
+              else
+                P.y[(size_t)(slot0 + j) * L.d + row] = acc[0][nt][r];
+            }
+          }
+      }
+    } else {
+      __syncthreads();  // every warp is done with its ring
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+          reinterpret_cast<float4*>(red)[((warp * NM + mi) * kNT + nt) * 32 + lane] =
+              make_float4(acc[mi][nt][0], acc[mi][nt][1], acc[mi][nt][2], acc[mi][nt][3]);
+      __syncthreads();
+      // element (tile j, token jj, row r): sum the wpt partials of tile j
+      for (int idx = tid; idx < ntl * kTok * kTileRows; idx += kFfnThreads) {
+        const int jtile = idx / (kTok * kTileRows), rest = idx % (kTok * kTileRows);
+        const int jj = rest >> 4, r = rest & 15;
+        if (jj >= ntok) continue;
+        const int nt = jj >> 3, j8 = jj & 7;
+        const int ln = 4 * (r & 7) + (j8 >> 1);
+        const int reg = 2 * (r >> 3) + (j8 & 1);
+        float sum[NM];
+#pragma unroll
+        for (int mi = 0; mi < NM; ++mi) {
+          float v = 0.f;
+          for (int w = jtile * wpt; w < (jtile + 1) * wpt; ++w)
+            v += red[(((w * NM + mi) * kNT + nt) * 32 + ln) * 4 + reg];
+          sum[mi] = v;
+        }
+        const int row = (tile0 + jtile) * kTileRows + r;
+        if (NM == 2)
+          P.h[(size_t)(slot0 + jj) * fe + row] = __float2half_rn(silu_f(sum[0]) * sum[NM - 1]);
+        else
+          P.y[(size_t)(slot0 + jj) * L.d + row] = sum[0];
       }
     }
     __syncthreads();
   }
 }
 
+template <int NM, int CLS>
+static cudaError_t launch_decode_class(const FfnParams& P, int grid_per_sm, cudaStream_t s) {
+  using D = Dec<NM, CLS>;
+  cudaError_t e = ensure_smem((const void*)ffn_decode_kernel<NM, CLS>, D::SMEM);
+  if (e != cudaSuccess) return e;
+  ffn_decode_kernel<NM, CLS><<<sm_count() * grid_per_sm, kFfnThreads, D::SMEM, s>>>(P);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* offsets, int n_slots, float* y,
-                       __half* h_ws, cudaStream_t s) {
-  // Experts with at most `thr` tokens take the mma.sync GEMV path; larger
-  // ones the tcgen05 GEMM.  No expert can have more tokens than the batch.
+                       __half* h_ws, int class_mask, cudaStream_t s) {
+  // Experts with at most `thr` tokens take the mma.sync path; larger ones the
+  // tcgen05 GEMM.  No expert can have more tokens than the batch.
   const int T = mode == 0 ? n_slots / L.K : n_slots;
   const int thr = decode_max_tokens();
   const bool big = T > thr;
+  if (mode != 0) class_mask = 1;
   FfnParams P;
   P.L = L;
   P.mode = mode;
@@ -323,26 +507,24 @@ cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* 
   P.max_tokens = big ? thr : INT_MAX;
   P.h = h_ws;
   P.y = y;
-  const int grid = sm_count() * 2;
-  const size_t smem0 = 2 * kTabBytes + (size_t)kFfnWarps * 2 * kNT * 32 * 16;
-  const size_t smem1 = 1 * kTabBytes + (size_t)kFfnWarps * 1 * kNT * 32 * 16;
-  cudaError_t e = ensure_smem((const void*)ffn_decode_kernel<2>, smem0);
-  if (e != cudaSuccess) return e;
-  e = ensure_smem((const void*)ffn_decode_kernel<1>, smem1);
-  if (e != cudaSuccess) return e;
-  P.phase = 0;
-  P.act = x;
-  ffn_decode_kernel<2><<<grid, kFfnThreads, smem0, s>>>(P);
-  if (big) {
-    e = launch_prefill(L, mode, 0, x, offsets, n_slots, thr, h_ws, y, s);
-    if (e != cudaSuccess) return e;
-  }
-  P.phase = 1;
-  P.act = h_ws;
-  ffn_decode_kernel<1><<<grid, kFfnThreads, smem1, s>>>(P);
-  if (big) {
-    e = launch_prefill(L, mode, 1, h_ws, offsets, n_slots, thr, h_ws, y, s);
-    if (e != cudaSuccess) return e;
+  cudaError_t e;
+  for (int phase = 0; phase < 2; ++phase) {
+    P.phase = phase;
+    P.act = phase == 0 ? x : h_ws;
+    if (class_mask & 1) {
+      e = phase == 0 ? launch_decode_class<2, 0>(P, Dec<2, 0>::MIN_BLOCKS, s)
+                     : launch_decode_class<1, 0>(P, Dec<1, 0>::MIN_BLOCKS, s);
+      if (e != cudaSuccess) return e;
+    }
+    if (class_mask & 2) {
+      e = phase == 0 ? launch_decode_class<2, 1>(P, Dec<2, 1>::MIN_BLOCKS, s)
+                     : launch_decode_class<1, 1>(P, Dec<1, 1>::MIN_BLOCKS, s);
+      if (e != cudaSuccess) return e;
+    }
+    if (big) {
+      e = launch_prefill(L, mode, phase, P.act, offsets, n_slots, thr, h_ws, y, s);
+      if (e != cudaSuccess) return e;
+    }
   }
   return cudaGetLastError();
 }

@@ -50,7 +50,7 @@ cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s) {
 // router: logits, softmax over E, top-K (ties to the lower index)
 // ---------------------------------------------------------------------------
 
-constexpr int kRouteTok = 8;      // tokens per CTA
+constexpr int kRouteTok = 4;      // tokens per CTA
 constexpr int kRouteThreads = 256;
 
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
@@ -84,24 +84,51 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const 
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += kRouteThreads / 32) {
-    float acc[kRouteTok];
+  // Each warp takes experts warp, warp + 8, ... in batches of four: the lane's
+  // 16-byte pieces of all four W_r rows are loaded before any is used, so a
+  // batch costs one memory round trip.
+  constexpr int kEB = 4;
+  const int per_lane = (d8 + 31) / 32;  // uint4 pieces of one row per lane (<= 64 for d <= 16384)
+  for (int e0 = warp * kEB; e0 < E; e0 += (kRouteThreads / 32) * kEB) {
+    float acc[kEB][kRouteTok];
 #pragma unroll
-    for (int t = 0; t < kRouteTok; ++t) acc[t] = 0.f;
-    const uint4* wrow = reinterpret_cast<const uint4*>(wr) + (size_t)e * d8;
-    for (int c = lane; c < d8; c += 32) {
-      const uint4 wv = __ldg(wrow + c);
+    for (int q = 0; q < kEB; ++q)
 #pragma unroll
-      for (int t = 0; t < kRouteTok; ++t)
-        if (t < nt) acc[t] += dot8(wv, xs[t * d8 + c]);
+      for (int t = 0; t < kRouteTok; ++t) acc[q][t] = 0.f;
+    for (int c0 = 0; c0 < per_lane; c0 += 4) {
+      uint4 wv[kEB][4];
+#pragma unroll
+      for (int q = 0; q < kEB; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = (c0 + i) * 32 + lane;
+          wv[q][i] = (e0 + q < E && c < d8) ? __ldg(reinterpret_cast<const uint4*>(wr) + (size_t)(e0 + q) * d8 + c)
+                                            : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = (c0 + i) * 32 + lane;
+        if (c < d8) {
+#pragma unroll
+          for (int t = 0; t < kRouteTok; ++t) {
+            if (t < nt) {
+              const uint4 xv = xs[t * d8 + c];
+#pragma unroll
+              for (int q = 0; q < kEB; ++q) acc[q][t] += dot8(wv[q][i], xv);
+            }
+          }
+        }
+      }
     }
 #pragma unroll
-    for (int t = 0; t < kRouteTok; ++t) {
-      float v = acc[t];
+    for (int q = 0; q < kEB; ++q)
 #pragma unroll
-      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0 && t < nt) logit[t * E + e] = v + (bias ? bias[e] : 0.f);
-    }
+      for (int t = 0; t < kRouteTok; ++t) {
+        float v = acc[q][t];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0 && t < nt && e0 + q < E) logit[t * E + e0 + q] = v + (bias ? bias[e0 + q] : 0.f);
+      }
   }
   __syncthreads();
 
@@ -208,12 +235,9 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(DevLayer L, 
                                                                     const int* __restrict__ hist, int nblk,
                                                                     int* __restrict__ offsets,
                                                                     int* __restrict__ perm_src,
-                                                                    int* __restrict__ inv_slot,
-                                                                    const __half* __restrict__ x,
-                                                                    __half* __restrict__ x_perm) {
+                                                                    int* __restrict__ inv_slot) {
   __shared__ int base[kMaxExperts], run[kMaxExperts], scan[kMaxExperts];
   __shared__ int wcnt[kPermThreads / 32][kMaxExperts];
-  __shared__ int pos_buf[kPermChunk];
   const int E = L.E, K = L.K, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
@@ -264,9 +288,6 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(DevLayer L, 
       const int pos = base[e] + run[e] + prior + rank;
       perm_src[pos] = slot / K;
       inv_slot[slot] = pos;
-      pos_buf[r * kPermThreads + tid] = pos;
-    } else {
-      pos_buf[r * kPermThreads + tid] = -1;
     }
     __syncthreads();
     if (tid < E) {
@@ -277,19 +298,15 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(DevLayer L, 
     __syncthreads();
   }
 
-  if (x_perm) {
-    const int d8 = L.d / 8;
-    const uint4* x4 = reinterpret_cast<const uint4*>(x);
-    uint4* xp4 = reinterpret_cast<uint4*>(x_perm);
-    for (int j = warp; j < kPermChunk; j += kPermThreads / 32) {
-      const int slot = s0 + j;
-      const int pos = pos_buf[j];
-      if (slot >= S || pos < 0) continue;
-      const uint4* src = x4 + (size_t)(slot / K) * d8;
-      uint4* dst = xp4 + (size_t)pos * d8;
-      for (int c = lane; c < d8; c += 32) dst[c] = src[c];
-    }
-  }
+}
+
+// x_perm[i] = x[perm_src[i]]: one thread per 16-byte piece.
+__global__ void __launch_bounds__(256) perm_gather_kernel(const int* __restrict__ perm_src, int S, int d8,
+                                                          const uint4* __restrict__ x, uint4* __restrict__ x_perm) {
+  const long long k = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (k >= (long long)S * d8) return;
+  const int i = (int)(k / d8), c = (int)(k % d8);
+  x_perm[(size_t)i * d8 + c] = x[(size_t)perm_src[i] * d8 + c];
 }
 
 cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __half* x, int* offsets, int* perm_src,
@@ -301,8 +318,12 @@ cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __hal
   }
   const int nblk = (S + kPermChunk - 1) / kPermChunk;
   perm_hist_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws);
-  perm_scatter_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws, nblk, offsets, perm_src, inv_slot, x,
-                                                    x_perm);
+  perm_scatter_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws, nblk, offsets, perm_src, inv_slot);
+  if (x_perm) {
+    const long long pieces = (long long)S * (L.d / 8);
+    perm_gather_kernel<<<(unsigned)((pieces + 255) / 256), 256, 0, s>>>(
+        perm_src, S, L.d / 8, reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x_perm));
+  }
   return cudaGetLastError();
 }
 

@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1) ffn_prefill_kernel(PfParam
 int decode_max_tokens() {
   // experts with more tokens than this use the tensor-core GEMM (read per call)
   const char* s = getenv("PW_DECODE_MAX_TOK");
-  const int v = s ? atoi(s) : 48;
+  const int v = s ? atoi(s) : 256;
   return v < 0 ? 0 : v;
 }
 

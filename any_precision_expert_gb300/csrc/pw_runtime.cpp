@@ -714,6 +714,19 @@ pw_status all_loaded(const pw_layer_s* l) {
 
 pw_status launched(cudaError_t e) { return e == cudaSuccess ? PW_OK : cuda_fail(e); }
 
+// Which decode kernel classes the layer can need: bit 0 for experts that can
+// run at 3 or 16 bits (every loaded expert can be lowered to 3), bit 1 for
+// experts with at least four planes still resident (4..6 bits reachable).
+int class_mask(const pw_layer_s* l) {
+  int m = 0;
+  for (int e = 0; e < l->desc.n_experts; ++e) {
+    if (l->bits[e] == 0) continue;
+    m |= 1;
+    if (l->planes[(size_t)e * kPlanes + 3].st != B_NONE) m |= 2;
+  }
+  return m;
+}
+
 }  // namespace
 
 extern "C" pw_status pw_workspace_size(pw_layer_t l, int T, size_t* bytes) {
@@ -765,7 +778,7 @@ extern "C" pw_status pw_expert_ffn_bitplane(pw_layer_t l, const void* x_perm, co
   PW_TRY(device_only());
   char* wsb = static_cast<char*>(ws);
   return launched(launch_ffn(l->dev(), 0, static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
-                             reinterpret_cast<__half*>(wsb + W.h_off), as_stream(stream)));
+                             reinterpret_cast<__half*>(wsb + W.h_off), class_mask(l), as_stream(stream)));
 }
 
 extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_shared, void* ws, size_t ws_bytes,
@@ -780,7 +793,7 @@ extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_
   PW_TRY(device_only());
   char* wsb = static_cast<char*>(ws);
   return launched(launch_ffn(l->dev(), 1, static_cast<const __half*>(x), nullptr, T, y_shared,
-                             reinterpret_cast<__half*>(wsb + W.hs_off), as_stream(stream)));
+                             reinterpret_cast<__half*>(wsb + W.hs_off), 1, as_stream(stream)));
 }
 
 extern "C" pw_status pw_combine(pw_layer_t l, const float* y_perm, const int32_t* inv_slot, const float* w, int T,
@@ -833,3 +846,4 @@ extern "C" pw_status pw_debug_page_address(pw_layer_t l, int e, int p, int vpage
   *addr = reinterpret_cast<uint64_t>(l->pool->page_addr(b.pages[vpage]));
   return PW_OK;
 }
+

@@ -231,7 +231,7 @@ def run_gpu(args):
         L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared, b.y, stream)
 
     launches_per_step = 1 + 2 + 2 + 2 + 1  # route, permute(2), ffn(2), shared(2), combine
-    if T > int(os.environ.get("PW_DECODE_MAX_TOK", "48")):
+    if T > int(os.environ.get("PW_DECODE_MAX_TOK", "256")):
         launches_per_step += 4  # tcgen05 GEMM kernels for experts above the threshold
     if external:
         g = torch.cuda.CUDAGraph()

@@ -25,7 +25,8 @@ def assert_close(got, ref, tol=TOL, what=""):
 
 
 def pool_bytes(cfg, bits, page=2 << 20, layers=1, slack=64 << 20):
-    d, f, E = cfg.d, cfg.f, cfg.E
+    d, f, E = int(cfg.d), int(cfg.f), int(cfg.E)
+    bits = [int(b) for b in bits]
     plane = 3 * d * f // 8
     pages = 0
     for b in bits:

@@ -60,4 +60,12 @@ cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* in
                            const float* w, int T, const float* y_shared, __half* y, cudaStream_t s);
 cudaError_t launch_debug_dequant(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
 
+// Host-side checks shared by the expert-FFN entry points: validates the
+// arguments of a routed FFN call for T tokens and returns the layer's kernel
+// parameters, the decode kernel classes it needs and the bytes of h scratch.
+pw_status ffn_call_args(pw_layer_t layer, const void* x_perm, const int32_t* offsets, int T, const float* y_perm,
+                        DevLayer* dev, int* class_mask, size_t* h_bytes);
+// Records a CUDA error for pw_last_cuda_error and returns PW_ERR_CUDA.
+pw_status record_cuda_error(cudaError_t e);
+
 }  // namespace pw

@@ -847,3 +847,23 @@ extern "C" pw_status pw_debug_page_address(pw_layer_t l, int e, int p, int vpage
   return PW_OK;
 }
 
+// ---------------------------------------------------------------------------
+// helpers for other entry points (pw_internal.h)
+// ---------------------------------------------------------------------------
+
+pw_status pw::record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+pw_status pw::ffn_call_args(pw_layer_t l, const void* x_perm, const int32_t* offsets, int T, const float* y_perm,
+                            DevLayer* dev, int* cmask, size_t* h_bytes) {
+  PW_TRY(check_layer(l));
+  if (T < 0 || !dev || !cmask || !h_bytes) return PW_ERR_INVALID_ARG;
+  if (T == 0) return device_only();
+  if (!x_perm || !offsets || !y_perm) return PW_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(y_perm)) return PW_ERR_INVALID_ARG;
+  PW_TRY(all_loaded(l));
+  PW_TRY(device_only());
+  *dev = l->dev();
+  *cmask = class_mask(l);
+  *h_bytes = (size_t)T * l->desc.top_k * l->desc.ffn * 2;
+  return PW_OK;
+}

@@ -165,6 +165,27 @@ pw_status pw_permute(pw_layer_t layer, const int32_t* idx, int T, const void* x,
 pw_status pw_expert_ffn_bitplane(pw_layer_t layer, const void* x_perm, const int32_t* offsets,
                                  int T, float* y_perm, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Same computation as pw_expert_ffn_bitplane, for callers that cannot
+ * allocate device memory when they run the layer -- e.g. a serving engine that
+ * has given all of HBM to its weight pool and KV cache and permits no further
+ * cudaMalloc, or a host program that only passes in pre-allocated inputs and
+ * outputs.  The paper has no counterpart; it is an addition of this library.
+ *
+ * Instead of a caller workspace the call uses one fixed array of 8 MiB in the
+ * library's own device memory (every GPU that loads the library holds it until
+ * the process exits), so T * top_k * ffn * 2 bytes must not exceed 8 MiB
+ * (PW_ERR_OOM otherwise; nothing is launched).  No device memory is allocated
+ * by this call.  Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the array: calls whose
+ * kernels overlap on the GPU (different streams, or different layers run
+ * concurrently) race on it, so serialise them.  Nothing in it has to start at
+ * zero; it keeps the last call's data.
+ */
+pw_status pw_expert_ffn_bitplane_noalloc(pw_layer_t layer, const void* x_perm, const int32_t* offsets,
+                                         int T, float* y_perm, void* stream);
+
 /* fp16 shared FFN on all T tokens: y_shared [T][d] fp32 (layers with shared_ffn > 0). */
 pw_status pw_shared_ffn(pw_layer_t layer, const void* x, int T, float* y_shared,
                         void* ws, size_t ws_bytes, void* stream);

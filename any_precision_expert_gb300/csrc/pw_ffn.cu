@@ -33,26 +33,27 @@ namespace pw {
 
 constexpr int kFfnThreads = 256;
 constexpr int kFfnWarps = kFfnThreads / 32;
-constexpr int kTok = 32;               // tokens per work item
+constexpr int kTok = 16;               // tokens per work item
 constexpr int kNT = kTok / 8;          // mma n-tiles per item
 constexpr int kTabBudget = 64 * 1024;  // LUT tables of one item (table class)
 constexpr int kTabBytes = 64 * 256;    // LUT table of one 16-row tile of one matrix at b = 6
 
-// Kernel classes: 0 = bitwidths 3 and 16 (register LUT / no LUT), 1 = 4, 5, 6.
+// Kernel classes: 0 = 3-bit codes (register LUT), 1 = 4, 5, 6 bits (shared-memory
+// LUTs), 2 = fp16 pages.  Separate kernels keep each path's registers apart.
 __host__ __device__ constexpr bool in_class(int b, int cls) {
-  return cls == 0 ? (b == 3 || b == 16) : (b >= 4 && b <= 6);
+  return cls == 0 ? b == 3 : cls == 2 ? b == 16 : (b >= 4 && b <= 6);
 }
 
 template <int NM, int CLS>
 struct Dec {
-  static constexpr int RING = CLS == 0 ? 3 : 2;                 // units in flight per lane
-  static constexpr int UNIT = CLS == 0 ? NM * 4 * 16 : NM * 6 * 16;  // bytes per lane per unit
+  static constexpr int RING = CLS == 1 ? 2 : 3;  // units in flight per lane
+  static constexpr int UNIT = CLS == 0 ? NM * 3 * 16 : CLS == 2 ? NM * 4 * 16 : NM * 6 * 16;  // bytes per lane
   static constexpr int WARP_RING = RING * UNIT * 32;
-  static constexpr int TABS = CLS == 0 ? 0 : kTabBudget;
+  static constexpr int TABS = CLS == 1 ? kTabBudget : 0;
   static constexpr int RED = kFfnWarps * NM * kNT * 32 * 16;
   static constexpr int RINGS = kFfnWarps * WARP_RING > RED ? kFfnWarps * WARP_RING : RED;
   static constexpr int SMEM = TABS + RINGS;
-  static constexpr int MIN_BLOCKS = CLS == 0 ? 2 : 1;
+  static constexpr int MIN_BLOCKS = CLS == 1 ? 1 : 2;
 };
 
 struct FfnParams {
@@ -135,8 +136,8 @@ __device__ __forceinline__ void load_bfrag(const __half* act, const int (&rowoff
 
 // Issue the copies of plane group gamma (NM matrices, B planes) into ring slot `slot`:
 // slot layout [matrix*B + plane][lane] x 16 bytes.
-template <int B, int NM>
-__device__ __forceinline__ void issue_group(const char* const (&base)[NM][6], int gamma, int G, int rem, int lane,
+template <int B, int NM, int PB>
+__device__ __forceinline__ void issue_group(const char* const (&base)[NM][PB], int gamma, int G, int rem, int lane,
                                             uint32_t slot) {
   if (gamma < G) {
     const size_t off = (size_t)(gamma * 128 + lane * 4) * 4;
@@ -156,8 +157,8 @@ __device__ __forceinline__ void issue_group(const char* const (&base)[NM][6], in
 
 // K loop of one warp over its plane groups (gamma = g0, g0 + gstep, ...).
 // lut3: register LUTs (B == 3); tab: smem table of (tile, matrix 0) (B >= 4).
-template <int B, int NM, int RING>
-__device__ __forceinline__ void warp_planes(const __half* act, const char* const (&base)[NM][6], int K, int g0,
+template <int B, int NM, int RING, int PB>
+__device__ __forceinline__ void warp_planes(const __half* act, const char* const (&base)[NM][PB], int K, int g0,
                                             int gstep, const int (&rowoff)[kNT], int NT,
                                             const uint32_t (&lut3)[NM][2][4], uint32_t tab, uint32_t tab_stride,
                                             uint32_t ring, float (&acc)[NM][kNT][4]) {
@@ -168,12 +169,19 @@ __device__ __forceinline__ void warp_planes(const __half* act, const char* const
   const int nu = g0 < NG ? (NG - 1 - g0) / gstep + 1 : 0;
 #pragma unroll
   for (int i = 0; i < RING - 1; ++i) {
-    if (i < nu) issue_group<B, NM>(base, g0 + i * gstep, G, rem, lane, ring + (i % RING) * kSlot);
+    if (i < nu) issue_group<B, NM, PB>(base, g0 + i * gstep, G, rem, lane, ring + (i % RING) * kSlot);
     cp_commit();
   }
+  // B fragments (tokens) of the next chunk are loaded while the current one is computed
+  uint32_t bcur[4][kNT][2], bnxt[4][kNT][2];
+  auto bload = [&](int kappa, uint32_t (&b)[4][kNT][2]) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) load_bfrag(act, rowoff, NT, kappa * 64 + s * 16, b[s]);
+  };
+  if (nu > 0) bload(4 * g0, bcur);
   for (int i = 0; i < nu; ++i) {
     const int inext = i + RING - 1;
-    if (inext < nu) issue_group<B, NM>(base, g0 + inext * gstep, G, rem, lane, ring + (inext % RING) * kSlot);
+    if (inext < nu) issue_group<B, NM, PB>(base, g0 + inext * gstep, G, rem, lane, ring + (inext % RING) * kSlot);
     cp_commit();
     cp_wait<RING - 1>();
     const int gamma = g0 + i * gstep;
@@ -194,10 +202,10 @@ __device__ __forceinline__ void warp_planes(const __half* act, const char* const
     for (int c = 0; c < 4; ++c) {
       if (c >= nch) break;
       const int kappa = 4 * gamma + c;
+      const int knext = c + 1 < nch ? kappa + 1 : (i + 1 < nu ? 4 * (gamma + gstep) : -1);
+      if (knext >= 0) bload(knext, bnxt);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        uint32_t bf[kNT][2];
-        load_bfrag(act, rowoff, NT, kappa * 64 + s * 16, bf);
 #pragma unroll
         for (int mi = 0; mi < NM; ++mi) {
           uint32_t w[B];
@@ -211,9 +219,16 @@ __device__ __forceinline__ void warp_planes(const __half* act, const char* const
           }
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt)
-            if (nt < NT) mma16816(acc[mi][nt], a, bf[nt][0], bf[nt][1]);
+            if (nt < NT) mma16816(acc[mi][nt], a, bcur[s][nt][0], bcur[s][nt][1]);
         }
       }
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          bcur[s][nt][0] = bnxt[s][nt][0];
+          bcur[s][nt][1] = bnxt[s][nt][1];
+        }
     }
   }
   cp_wait<0>();
@@ -241,26 +256,38 @@ __device__ __forceinline__ void warp_f16(const __half* act, const char* const (&
     if (i < nu) issue(k0 + i * kstep, ring + (i % RING) * kSlot);
     cp_commit();
   }
+  uint32_t bcur[4][kNT][2], bnxt[4][kNT][2];
+  auto bload = [&](int kappa, uint32_t (&b)[4][kNT][2]) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) load_bfrag(act, rowoff, NT, kappa * 64 + s * 16, b[s]);
+  };
+  if (nu > 0) bload(k0, bcur);
   for (int i = 0; i < nu; ++i) {
     const int inext = i + RING - 1;
     if (inext < nu) issue(k0 + inext * kstep, ring + (inext % RING) * kSlot);
     cp_commit();
     cp_wait<RING - 1>();
     const int kappa = k0 + i * kstep;
+    if (i + 1 < nu) bload(kappa + kstep, bnxt);
     const uint32_t slot = ring + (i % RING) * kSlot;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      uint32_t bf[kNT][2];
-      load_bfrag(act, rowoff, NT, kappa * 64 + s * 16, bf);
 #pragma unroll
       for (int mi = 0; mi < NM; ++mi) {
         const uint4 v = lds128(slot + ((mi * 4 + s) * 32 + lane) * 16);
         const uint32_t a[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt)
-          if (nt < NT) mma16816(acc[mi][nt], a, bf[nt][0], bf[nt][1]);
+          if (nt < NT) mma16816(acc[mi][nt], a, bcur[s][nt][0], bcur[s][nt][1]);
       }
     }
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        bcur[s][nt][0] = bnxt[s][nt][0];
+        bcur[s][nt][1] = bnxt[s][nt][1];
+      }
   }
   cp_wait<0>();
 }
@@ -358,6 +385,7 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
     const int ntok = min(kTok, s_off[e + 1] - slot0);
     const int NT = (ntok + 7) >> 3;
     const uint32_t tstride = CLS == 1 ? (uint32_t)(1 << b) * 256u : 0u;
+    (void)routed;
 
     if (CLS == 1) {  // per-lane LUT copies of every (tile, matrix) of the item
       for (int q = 0; q < ntl * NM; ++q) {
@@ -390,7 +418,7 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
         const int tok = min(nt * 8 + (lane >> 2), ntok - 1);
         rowoff[nt] = (slot0 + tok) * K + 2 * (lane & 3);
       }
-      if (CLS == 0 && b == 16) {
+      if constexpr (CLS == 2) {
         const char* b16[NM];
 #pragma unroll
         for (int mi = 0; mi < NM; ++mi) {
@@ -400,16 +428,17 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
         }
         warp_f16<NM, D::RING>(P.act, b16, K, kpart, wpt, rowoff, NT, ring, acc);
       } else {
-        const char* base[NM][6];
+        constexpr int PB = CLS == 0 ? 3 : 6;  // plane pointers this class can use
+        const char* base[NM][PB];
 #pragma unroll
         for (int mi = 0; mi < NM; ++mi) {
           const int m = P.phase == 0 ? mi : 2;
 #pragma unroll
-          for (int p = 0; p < 6; ++p) base[mi][p] = p < b ? tile_addr(L, e, m, p, tau) : nullptr;
+          for (int p = 0; p < PB; ++p) base[mi][p] = p < b ? tile_addr(L, e, m, p, tau) : nullptr;
         }
         uint32_t lut3[NM][2][4];
         const uint32_t tab = tab0 + (uint32_t)(jt * NM) * tstride;
-        if (CLS == 0) {
+        if constexpr (CLS == 0) {
 #pragma unroll
           for (int mi = 0; mi < NM; ++mi) {
             const int m = P.phase == 0 ? mi : 2;
@@ -417,12 +446,12 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
             load_lut3(lr + (lane >> 2) * 8, lut3[mi][0]);
             load_lut3(lr + ((lane >> 2) + 8) * 8, lut3[mi][1]);
           }
-          warp_planes<3, NM, D::RING>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc);
+          warp_planes<3, NM, D::RING, PB>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc);
         } else {
           switch (b) {
-            case 4: warp_planes<4, NM, D::RING>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
-            case 5: warp_planes<5, NM, D::RING>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
-            default: warp_planes<6, NM, D::RING>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
+            case 4: warp_planes<4, NM, D::RING, PB>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
+            case 5: warp_planes<5, NM, D::RING, PB>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
+            default: warp_planes<6, NM, D::RING, PB>(P.act, base, K, kpart, wpt, rowoff, NT, lut3, tab, tstride, ring, acc); break;
           }
         }
       }
@@ -498,7 +527,7 @@ cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* 
   const int T = mode == 0 ? n_slots / L.K : n_slots;
   const int thr = decode_max_tokens();
   const bool big = T > thr;
-  if (mode != 0) class_mask = 1;
+  if (mode != 0) class_mask = 4;
   FfnParams P;
   P.L = L;
   P.mode = mode;
@@ -519,6 +548,11 @@ cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* 
     if (class_mask & 2) {
       e = phase == 0 ? launch_decode_class<2, 1>(P, Dec<2, 1>::MIN_BLOCKS, s)
                      : launch_decode_class<1, 1>(P, Dec<1, 1>::MIN_BLOCKS, s);
+      if (e != cudaSuccess) return e;
+    }
+    if (class_mask & 4) {
+      e = phase == 0 ? launch_decode_class<2, 2>(P, Dec<2, 2>::MIN_BLOCKS, s)
+                     : launch_decode_class<1, 2>(P, Dec<1, 2>::MIN_BLOCKS, s);
       if (e != cudaSuccess) return e;
     }
     if (big) {

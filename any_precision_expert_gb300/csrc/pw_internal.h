@@ -50,7 +50,8 @@ cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __hal
                            int* offsets, int* perm_src, int* inv_slot, __half* x_perm,
                            int* hist_ws, cudaStream_t s);
 // mode 0: routed experts over permuted slots; mode 1: the shared fp16 FFN over all T tokens.
-// class_mask: bit 0 launch the kernel for bitwidths 3 and 16, bit 1 the one for 4, 5, 6.
+// class_mask: bit 0 launch the decode kernel for 3-bit experts, bit 1 the one for 4, 5, 6 bits,
+// bit 2 the one for fp16 pages.
 cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* offsets, int n_slots,
                        float* y, __half* h_ws, int class_mask, cudaStream_t s);
 int decode_max_tokens();

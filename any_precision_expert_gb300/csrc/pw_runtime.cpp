@@ -714,15 +714,18 @@ pw_status all_loaded(const pw_layer_s* l) {
 
 pw_status launched(cudaError_t e) { return e == cudaSuccess ? PW_OK : cuda_fail(e); }
 
-// Which decode kernel classes the layer can need: bit 0 for experts that can
-// run at 3 or 16 bits (every loaded expert can be lowered to 3), bit 1 for
-// experts with at least four planes still resident (4..6 bits reachable).
+// Which decode kernel classes the layer can need: bit 0 for 3-bit experts
+// (every loaded expert can be lowered to 3 bits), bit 1 for experts with at
+// least four planes still resident (4..6 bits reachable), bit 2 for experts
+// whose fp16 page is still resident (16 bits reachable).  A class whose
+// bitwidths no expert can reach without a reload is not launched.
 int class_mask(const pw_layer_s* l) {
   int m = 0;
   for (int e = 0; e < l->desc.n_experts; ++e) {
     if (l->bits[e] == 0) continue;
     m |= 1;
     if (l->planes[(size_t)e * kPlanes + 3].st != B_NONE) m |= 2;
+    if (l->f16[e].st != B_NONE) m |= 4;
   }
   return m;
 }

@@ -28,7 +28,15 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s at 1 GB300; achieved HBM GB/s (decode) / tensor util (prefill)"
-WORKLOAD = "qwen1.5-moe-a2.7b-shaped layer decode"
+
+# name -> (description, default tokens, default layer copies)
+WORKLOADS = {
+    "qwen": ("qwen1.5-moe-a2.7b-shaped layer (d=2048, 60 experts ffn 1408 top-4, fp16 shared FFN 5632, "
+             "Zipf(1.1) router bias, greedy floor-respecting bitwidth plan)", 64, 6),
+    "mixtral": ("mixtral-8x7b-shaped layer (d=4096, 8 experts ffn 14336 top-2, bitwidths 6/5/4/3 cycled)", 4096, 2),
+    "e128": ("128-expert layer (d=2816, ffn 704, top-8, Zipf(1.2) bias, 45@3 45@4 30@6 8@16 bits)", 8192, 2),
+    "tiny": ("tiny layer (d=512, 8 experts ffn 1024 top-2, mixed 3/4/5/6/16 bits)", 16, 8),
+}
 
 
 def _load_json(path):
@@ -183,7 +191,7 @@ def run_gpu(args):
         return float(t.item())
 
     T, K, W = args.tokens, args.steps, args.warmup
-    wl = build_workload(n_copies=args.copies, T=T)
+    wl = build_workload(args.workload, n_copies=args.copies, T=T)
     cfg, layers, bufs, xs_d = wl["cfg"], wl["layers"], wl["bufs"], wl["xs_d"]
     NL = len(layers)
     stream = torch.cuda.Stream()
@@ -227,12 +235,16 @@ def run_gpu(args):
         L.expert_ffn_bitplane(b.x_perm, b.offsets, T, b.y_perm, b.ws, stream)
 
     def part_c(L, b, x):
-        L.shared_ffn(x, T, b.y_shared, b.ws, stream)
-        L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared, b.y, stream)
+        if cfg.shared_ffn:
+            L.shared_ffn(x, T, b.y_shared, b.ws, stream)
+        L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared if cfg.shared_ffn else None, b.y, stream)
 
     launches_per_step = 1 + 2 + 2 + 2 + 1  # route, permute(2), ffn(2), shared(2), combine
+    launches_per_step += 2  # the 4/5/6-bit decode class (launched when such planes are resident)
     if T > int(os.environ.get("PW_DECODE_MAX_TOK", "256")):
-        launches_per_step += 4  # tcgen05 GEMM kernels for experts above the threshold
+        launches_per_step += 2  # tcgen05 GEMM kernels for experts above the threshold
+    if not cfg.shared_ffn:
+        launches_per_step -= 2
     if external:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -324,8 +336,16 @@ def run_gpu(args):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     else:
         peak, peak_src = 6800.0, "fallback 6.8 TB/s"
-    achieved = ffn_avg_bytes / (ffn_avg_ms * 1e-3) / 1e9
-    traffic = _traffic_from_profile(T)
+    ffn_flops = 2.0 * T * cfg.K * 3 * cfg.d * cfg.f  # routed expert FFN, algorithmic
+    tflops = ffn_flops / (ffn_avg_ms * 1e-3) / 1e12
+    gbs = ffn_avg_bytes / (ffn_avg_ms * 1e-3) / 1e9
+    # decode batches are bound by weight bytes, prefill batches by the tensor pipe
+    tensor_bound = T * cfg.K / cfg.E >= 256
+    if tensor_bound:
+        tpk = float(peaks["bf16_tflops"]) if peaks and peaks.get("bf16_tflops") else 1900.0
+        tpk_src = ("measured (MEASURED_PEAKS.json bf16_tflops; fp16 runs at the bf16 rate)"
+                   if peaks and peaks.get("bf16_tflops") else "fallback 1.9 PFLOP/s")
+    traffic = _traffic_from_profile(args.workload, T)
     ok = all(L.check_device() == 0 for L in layers)
 
     out = None
@@ -345,8 +365,7 @@ def run_gpu(args):
             "dtype": "f16",
             "data": "synthetic",
             "config": {
-                "workload": f"{WORKLOAD} T={T} (d=2048, 60 experts ffn 1408 top-4, fp16 shared FFN 5632, "
-                            f"Zipf(1.1) router bias, greedy floor-respecting bitwidth plan)",
+                "workload": f"{WORKLOADS[args.workload][0]}, {T} tokens per step",
                 "tokens_per_step": T,
                 "bits_plan": {str(b): int((wl["bits"] == b).sum()) for b in (3, 4, 5, 6, 16)},
                 "layer_copies": NL,
@@ -356,21 +375,35 @@ def run_gpu(args):
                            "three CUDA graphs per step, queued ahead of the GPU") + "; CUDA events on the launching stream",
                 "step_algorithmic_bytes": step_avg_bytes,
                 "hbm_GBps_step": step_avg_bytes / ((ms_max / K) * 1e-3) / 1e9,
+                "ffn_GBps": gbs,
+                "ffn_TFLOPs": tflops,
                 "parallelism": "replicas" if ws > 1 else "single GPU",
                 "device_errors": not ok,
             },
-            "roofline": {
-                "kernel": "expert FFN call (ffn_decode gate/up + down kernels)",
+            "roofline": ({
+                "kernel": "expert FFN call (decode and tcgen05 GEMM kernels, gate/up + down)",
+                "bound": "tensor",
+                "achieved": tflops,
+                "peak": tpk,
+                "unit": "TFLOP/s",
+                "frac": tflops / tpk,
+                "traffic": traffic,
+                "algorithmic_flops_per_launch": ffn_flops,
+                "algorithmic_bytes_per_launch": ffn_avg_bytes,
+                "avg_launch_ms": ffn_avg_ms,
+                "peak_source": tpk_src,
+            } if tensor_bound else {
+                "kernel": "expert FFN call (decode and tcgen05 GEMM kernels, gate/up + down)",
                 "bound": "hbm",
-                "achieved": achieved,
+                "achieved": gbs,
                 "peak": peak,
                 "unit": "GB/s",
-                "frac": achieved / peak,
+                "frac": gbs / peak,
                 "traffic": traffic,
                 "algorithmic_bytes_per_launch": ffn_avg_bytes,
                 "avg_launch_ms": ffn_avg_ms,
                 "peak_source": peak_src,
-            },
+            }),
             "cpu_baseline": cpu,
             "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": T * cfg.d * 2,
                     "d2h_bytes_per_step": T * cfg.d * 2, "steps": KE,
@@ -386,9 +419,9 @@ def run_gpu(args):
     return out
 
 
-def _traffic_from_profile(T):
+def _traffic_from_profile(workload, T):
     """DRAM bytes per FFN call from the committed ncu summary, if it matches the current kernel."""
-    prof = _load_json(os.path.join(ROOT, "profiles", "ffn_decode_qwen_traffic.json"))
+    prof = _load_json(os.path.join(ROOT, "profiles", f"ffn_traffic_{workload}_T{T}.json"))
     if not prof or int(prof.get("tokens", -1)) != T:
         return None
     if prof.get("source_hash") != kernel_source_hash():
@@ -399,7 +432,7 @@ def _traffic_from_profile(T):
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("pw_ffn.cu", "pw_device.cuh"):
+    for f in ("pw_ffn.cu", "pw_prefill.cu", "pw_device.cuh", "pw_tc.cuh"):
         with open(os.path.join(ROOT, "any_precision_expert_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -444,7 +477,7 @@ def run_reference(args):
     from synth import bits_plan, get_config, make_expert, make_router, make_shared, make_tokens
     from oracle import pw_oracle as O
 
-    cfg = get_config("qwen")
+    cfg = get_config(args.workload)
     T = args.tokens
     bits = bits_plan(cfg, 0)
     wr, bias = make_router(cfg, 0)
@@ -467,7 +500,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD} T={T} (same layer as the GPU arm)", "tokens_per_step": 1},
+            "config": {"workload": f"{WORKLOADS[args.workload][0]}, {T} tokens per step (same layer as the GPU arm)",
+                       "tokens_per_step": 1},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _threads(), "kind": "oracle",
                              "sample": "one decode token of the batch per step (numpy fp64 oracle)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -478,14 +512,19 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--tokens", type=int, default=64)
-    ap.add_argument("--copies", type=int, default=6)
+    ap.add_argument("--workload", default="qwen", choices=sorted(WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--copies", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load for the clock record")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
+    if args.tokens is None:
+        args.tokens = WORKLOADS[args.workload][1]
+    if args.copies is None:
+        args.copies = WORKLOADS[args.workload][2]
     out = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if out is not None:
         print(json.dumps(out), flush=True)

@@ -511,6 +511,152 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Warp-independent variant for 3-bit codes and fp16 pages: one warp owns a
+// work item (expert, 16-token chunk, 16-row tile) over the whole reduction,
+// so the only block-wide synchronisation is the item-list setup.  Every lane
+// keeps RING units of its own weight words in flight with cp.async.
+// ---------------------------------------------------------------------------
+constexpr int kWarpThreads = 128;  // four independent warps per CTA
+
+template <int NM, int B>
+struct WDec {
+  static constexpr int RING = B == 16 ? 3 : 4;
+  static constexpr int UNIT = B == 16 ? NM * 4 * 16 : NM * B * 16;  // bytes per lane per unit
+  static constexpr int WARP_RING = RING * UNIT * 32;
+  static constexpr int SMEM = (kWarpThreads / 32) * WARP_RING;
+};
+
+template <int NM, int B>
+__global__ void __launch_bounds__(kWarpThreads, 4) ffn_warp_kernel(FfnParams P) {
+  using D = WDec<NM, B>;
+  extern __shared__ __align__(16) unsigned char smem_w[];
+  __shared__ int s_pref[kMaxExperts + 1];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_bits[kMaxExperts];
+
+  const DevLayer& L = P.L;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool routed = P.mode == 0;
+  const int E = routed ? L.E : 1;
+  const int fe = routed ? L.f : L.fs;
+  const int K = P.phase == 0 ? L.d : fe;
+  const int tiles = P.phase == 0 ? fe / kTileRows : L.d / kTileRows;
+
+  if (routed) {
+    for (int i = tid; i <= E; i += kWarpThreads) s_off[i] = P.offsets[i];
+    for (int i = tid; i < E; i += kWarpThreads) s_bits[i] = L.bits[i];
+  } else if (tid == 0) {
+    s_off[0] = 0;
+    s_off[1] = P.n_slots;
+    s_bits[0] = 16;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int c = 0;
+      if (e < E) {
+        const int n = s_off[e + 1] - s_off[e];
+        if (n > 0 && n <= P.max_tokens && s_bits[e] == B) c = ((n + kTok - 1) / kTok) * tiles;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) s_pref[e] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_pref[E] = run;
+  }
+  __syncthreads();
+  const int total = s_pref[E];
+  const uint32_t ring = smem_u32(smem_w) + warp * D::WARP_RING;
+  const int nwarps = gridDim.x * (kWarpThreads / 32);
+
+  for (int item = blockIdx.x * (kWarpThreads / 32) + warp; item < total; item += nwarps) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pref[mid] <= item) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int n_e = s_off[e + 1] - s_off[e];
+    const int nch = (n_e + kTok - 1) / kTok;
+    const int local = item - s_pref[e];
+    const int tau = local / nch, chunk = local % nch;  // chunks of one tile on neighbouring warps
+    const int slot0 = s_off[e] + chunk * kTok;
+    const int ntok = min(kTok, s_off[e + 1] - slot0);
+    const int NT = (ntok + 7) >> 3;
+
+    int rowoff[kNT];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      const int tok = min(nt * 8 + (lane >> 2), ntok - 1);
+      rowoff[nt] = (slot0 + tok) * K + 2 * (lane & 3);
+    }
+    float acc[NM][kNT][4];
+#pragma unroll
+    for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[mi][nt][r] = 0.f;
+
+    if constexpr (B == 16) {
+      const char* b16[NM];
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi) {
+        const int m = P.phase == 0 ? mi : 2;
+        b16[mi] = routed ? tile_addr(L, e, m, kPlanes, tau)
+                         : reinterpret_cast<const char*>(L.shared16[m]) + (size_t)tau * 32 * K;
+      }
+      warp_f16<NM, D::RING>(P.act, b16, K, 0, 1, rowoff, NT, ring, acc);
+    } else {
+      const char* base[NM][3];
+      uint32_t lut3[NM][2][4];
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi) {
+        const int m = P.phase == 0 ? mi : 2;
+#pragma unroll
+        for (int p = 0; p < 3; ++p) base[mi][p] = tile_addr(L, e, m, p, tau);
+        const __half* lr = lut_rows(L, e, m, 3, tau * kTileRows);
+        load_lut3(lr + (lane >> 2) * 8, lut3[mi][0]);
+        load_lut3(lr + ((lane >> 2) + 8) * 8, lut3[mi][1]);
+      }
+      warp_planes<3, NM, D::RING, 3>(P.act, base, K, 0, 1, rowoff, NT, lut3, 0u, 0u, ring, acc);
+    }
+
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int j = nt * 8 + 2 * t + (r & 1);
+        const int row = tau * kTileRows + g + 8 * (r >> 1);
+        if (j < ntok) {
+          if (NM == 2)
+            P.h[(size_t)(slot0 + j) * fe + row] = __float2half_rn(silu_f(acc[0][nt][r]) * acc[NM - 1][nt][r]);
+          else
+            P.y[(size_t)(slot0 + j) * L.d + row] = acc[0][nt][r];
+        }
+      }
+  }
+}
+
+template <int NM, int B>
+static cudaError_t launch_warp_class(const FfnParams& P, cudaStream_t s) {
+  using D = WDec<NM, B>;
+  cudaError_t e = ensure_smem((const void*)ffn_warp_kernel<NM, B>, D::SMEM);
+  if (e != cudaSuccess) return e;
+  ffn_warp_kernel<NM, B><<<sm_count() * 4, kWarpThreads, D::SMEM, s>>>(P);
+  return cudaGetLastError();
+}
+
 template <int NM, int CLS>
 static cudaError_t launch_decode_class(const FfnParams& P, int grid_per_sm, cudaStream_t s) {
   using D = Dec<NM, CLS>;
@@ -541,8 +687,7 @@ cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* 
     P.phase = phase;
     P.act = phase == 0 ? x : h_ws;
     if (class_mask & 1) {
-      e = phase == 0 ? launch_decode_class<2, 0>(P, Dec<2, 0>::MIN_BLOCKS, s)
-                     : launch_decode_class<1, 0>(P, Dec<1, 0>::MIN_BLOCKS, s);
+      e = phase == 0 ? launch_warp_class<2, 3>(P, s) : launch_warp_class<1, 3>(P, s);
       if (e != cudaSuccess) return e;
     }
     if (class_mask & 2) {
@@ -551,8 +696,7 @@ cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* 
       if (e != cudaSuccess) return e;
     }
     if (class_mask & 4) {
-      e = phase == 0 ? launch_decode_class<2, 2>(P, Dec<2, 2>::MIN_BLOCKS, s)
-                     : launch_decode_class<1, 2>(P, Dec<1, 2>::MIN_BLOCKS, s);
+      e = phase == 0 ? launch_warp_class<2, 16>(P, s) : launch_warp_class<1, 16>(P, s);
       if (e != cudaSuccess) return e;
     }
     if (big) {

@@ -9,13 +9,15 @@
 //     the same mask/rotate + per-lane LUT scheme as the decode kernel, and
 //     write fp16 weights into shared memory in the 128-byte swizzled K-major
 //     layout; afterwards they are the epilogue (TMEM -> registers -> global);
-//   * four loader warps copy the tokens' activation rows into the same layout;
+//   * one thread loads the tokens' activation tile of every stage with a TMA
+//     tensor copy (128-byte swizzle; rows past the end of the tensor read as zeros);
 //   * one thread issues tcgen05.mma (kind::f16, fp32 accumulators in tensor
 //     memory) and releases stages with tcgen05.commit.
 // Phase 0 accumulates gate and up side by side in TMEM (2 x 256 columns) and
 // writes h = silu(gate) * up as fp16; phase 1 (down) writes y as fp32.
 // Every wait is bounded: on a timeout the kernel flags the layer's error word
 // (PW_ERR_TIMEOUT), drains its MMAs and frees its tensor memory.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -30,7 +32,7 @@ namespace pw {
 constexpr int PF_BM = 128, PF_BN = 256, PF_BK = 64;
 constexpr uint32_t PF_A_BYTES = PF_BM * PF_BK * 2;  // 16 KB
 constexpr uint32_t PF_B_BYTES = PF_BN * PF_BK * 2;  // 32 KB
-constexpr int PF_BWARPS = 4;
+constexpr int PF_BWARPS = 1;  // the TMA producer warp
 constexpr uint32_t PF_TAB_BYTES = 64 * 256;          // LUT table of one (matrix, 64-row slab), b <= 6
 
 template <int NM>
@@ -44,7 +46,7 @@ struct Pf {
   static constexpr uint32_t BARS = 256;
   static constexpr uint32_t SMEM = 1024 + NS * STAGE + TABS + BARS;
   static constexpr uint32_t TMEM_COLS = NM == 2 ? 512 : 256;
-  static constexpr uint32_t FULL_COUNT = NM * 2 + PF_BWARPS;  // one arrival per producing warp
+  static constexpr uint32_t FULL_COUNT = NM * 2 + 1;  // dequant warps + the TMA producer's expect_tx
   static constexpr int PAIRS = DQ / 2;                        // warps sharing one LUT table
 };
 
@@ -121,7 +123,8 @@ __device__ __forceinline__ void pf_load_planes(const char* const (&pb)[6], int k
 }
 
 template <int NM>
-__global__ void __launch_bounds__(Pf<NM>::THREADS, 1) ffn_prefill_kernel(PfParams Q) {
+__global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
+    ffn_prefill_kernel(PfParams Q, const __grid_constant__ CUtensorMap act_map) {
   using C = Pf<NM>;
   extern __shared__ unsigned char pf_raw[];
   __shared__ int s_pref[kMaxExperts + 1];
@@ -351,34 +354,21 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1) ffn_prefill_kernel(PfParam
       ++tc;
     }
   } else if (warp < C::DQ + PF_BWARPS) {
-    // ---------------- activation loader warps ----------------
-    const int bt = tid - C::DQ * 32;  // 0..127
-    uint32_t it = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const PfTile T = pf_tile(t, s_pref, s_off, E, mtiles);
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % C::NS;
-        const uint32_t ph = (it / C::NS) & 1;
-        uint4 v[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int j = bt + 128 * q, n = j >> 3, c16 = j & 7;
-          v[q] = n < T.nvalid
-                     ? *reinterpret_cast<const uint4*>(Q.act + (size_t)(T.slot0 + n) * K + kb * PF_BK + c16 * 8)
-                     : make_uint4(0, 0, 0, 0);
+    // ---------------- activation producer: one TMA copy per stage ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const PfTile T = pf_tile(t, s_pref, s_off, E, mtiles);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % C::NS;
+          const uint32_t ph = (it / C::NS) & 1;
+          ok = mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err);
+          if (!ok) break;
+          const uint32_t Bs = base + s * C::STAGE + NM * PF_A_BYTES;
+          mbar_arrive_expect_tx(full_bar(s), PF_B_BYTES);
+          tma_load_2d(Bs, &act_map, kb * PF_BK, T.slot0, full_bar(s));
         }
-        ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err));
-        if (!ok) break;
-        const uint32_t Bs = base + s * C::STAGE + NM * PF_A_BYTES;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int j = bt + 128 * q, n = j >> 3, c16 = j & 7;
-          sts128(Bs + sw128_offset(n, c16), v[q]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar(s));
       }
     }
   } else if (lane == 0) {
@@ -435,6 +425,28 @@ int decode_max_tokens() {
   return v < 0 ? 0 : v;
 }
 
+namespace {
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+}  // namespace
+
 cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
                            int n_slots, int min_tokens, __half* h, float* y, cudaStream_t s) {
   PfParams Q;
@@ -446,16 +458,30 @@ cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half*
   Q.min_tokens = min_tokens;
   Q.h = h;
   Q.y = y;
+  // activation tensor [n_slots][K] fp16, boxes of 64 columns x 256 rows, 128-byte swizzle
+  const int fe = mode == 0 ? L.f : L.fs;
+  const int K = phase == 0 ? L.d : fe;
+  EncodeTiled enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)n_slots};
+  const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)PF_BK, (cuuint32_t)PF_BN};
+  const cuuint32_t estride[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(act), gdim, gstride, box, estride,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const int grid = sm_count();
   cudaError_t e;
   if (phase == 0) {
     e = ensure_smem((const void*)ffn_prefill_kernel<2>, Pf<2>::SMEM);
     if (e != cudaSuccess) return e;
-    ffn_prefill_kernel<2><<<grid, Pf<2>::THREADS, Pf<2>::SMEM, s>>>(Q);
+    ffn_prefill_kernel<2><<<grid, Pf<2>::THREADS, Pf<2>::SMEM, s>>>(Q, map);
   } else {
     e = ensure_smem((const void*)ffn_prefill_kernel<1>, Pf<1>::SMEM);
     if (e != cudaSuccess) return e;
-    ffn_prefill_kernel<1><<<grid, Pf<1>::THREADS, Pf<1>::SMEM, s>>>(Q);
+    ffn_prefill_kernel<1><<<grid, Pf<1>::THREADS, Pf<1>::SMEM, s>>>(Q, map);
   }
   return cudaGetLastError();
 }

@@ -54,6 +54,7 @@ _SIGS = {
     "pw_expert_ffn_bitplane": (i32, [vp, vp, vp, i32, vp, vp, sz, vp]),
     "pw_expert_ffn_bitplane_noalloc": (i32, [vp, vp, vp, i32, vp, vp]),
     "pw_shared_ffn": (i32, [vp, vp, i32, vp, vp, sz, vp]),
+    "pw_moe_ffn": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]),
     "pw_combine": (i32, [vp, vp, vp, vp, i32, vp, vp, vp]),
     "pw_set_expert_bitwidth": (i32, [vp, i32, i32, vp]),
     "pw_get_expert_bitwidth": (i32, [vp, i32, P_i32]),

@@ -154,6 +154,10 @@ class Layer:
         check(lib.pw_shared_ffn(self.handle, _p(x), T, _p(y_shared), _p(ws), ws.numel() * ws.element_size(),
                                 _s(stream)), "pw_shared_ffn")
 
+    def moe_ffn(self, x, x_perm, offsets, T, y_perm, y_shared, ws, stream=None):
+        check(lib.pw_moe_ffn(self.handle, _p(x), _p(x_perm), _p(offsets), T, _p(y_perm), _p(y_shared), _p(ws),
+                             ws.numel() * ws.element_size(), _s(stream)), "pw_moe_ffn")
+
     def combine(self, y_perm, inv_slot, w, T, y_shared, y, stream=None):
         check(lib.pw_combine(self.handle, _p(y_perm), _p(inv_slot), _p(w), T, _p(y_shared), _p(y), _s(stream)),
               "pw_combine")
@@ -192,10 +196,7 @@ def moe_forward(layer: Layer, x, wr, bias, buf: Buffers, stream=None):
     T = x.shape[0]
     layer.route_topk(x, wr, bias, T, buf.idx, buf.w, None, stream)
     layer.permute(buf.idx, T, x, buf.offsets, buf.perm_src, buf.inv_slot, buf.x_perm, buf.ws, stream)
-    layer.expert_ffn_bitplane(buf.x_perm, buf.offsets, T, buf.y_perm, buf.ws, stream)
-    ysh = None
-    if layer.fs:
-        layer.shared_ffn(x, T, buf.y_shared, buf.ws, stream)
-        ysh = buf.y_shared
+    ysh = buf.y_shared if layer.fs else None
+    layer.moe_ffn(x, buf.x_perm, buf.offsets, T, buf.y_perm, ysh, buf.ws, stream)
     layer.combine(buf.y_perm, buf.inv_slot, buf.w, T, ysh, buf.y, stream)
     return buf.y[:T]

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpw.so")
 
-SOURCES = ["pw_runtime.cpp", "pw_pack.cpp", "pw_kernels.cu", "pw_ffn.cu", "pw_prefill.cu", "pw_noalloc.cu"]
+SOURCES = ["pw_runtime.cpp", "pw_pack.cpp", "pw_kernels.cu", "pw_ffn.cu", "pw_decode.cu", "pw_prefill.cu",
+           "pw_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

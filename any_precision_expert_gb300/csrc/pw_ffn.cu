@@ -27,14 +27,12 @@
 
 #include <climits>
 
-#include "pw_device.cuh"
+#include "pw_gemv.cuh"
 
 namespace pw {
 
 constexpr int kFfnThreads = 256;
 constexpr int kFfnWarps = kFfnThreads / 32;
-constexpr int kTok = 16;               // tokens per work item
-constexpr int kNT = kTok / 8;          // mma n-tiles per item
 constexpr int kTabBudget = 64 * 1024;  // LUT tables of one item (table class)
 constexpr int kTabBytes = 64 * 256;    // LUT table of one 16-row tile of one matrix at b = 6
 
@@ -74,222 +72,47 @@ __device__ __forceinline__ int rw_cap(int b, int NM) {
   return min(8, kTabBudget / (NM * (1 << b) * 256));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-// ---------------------------------------------------------------------------
-// 3-bit codes: byte-permute lookups from registers.
-// lut[r] = {lo bytes of entries 0-3, lo 4-7, hi 0-3, hi 4-7} of row g (r = 0)
-// or g + 8 (r = 1).  Plane p keeps code bit 2-p of weight (s, nibble n) at bit
-// 4n + s + 5 - p; masking with rotl(0x11111111, s+5-p) and rotating right by
-// s+3 puts the code of (s, n) in nibble n (bit 3 clear), so the low half
-// selects row g's four codes and the high half row g+8's.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void decode_step_prmt3(const uint32_t (&w)[3], const int s, const uint32_t (&lut)[2][4],
-                                                  uint32_t (&a)[4]) {
-  uint32_t m = 0;
+// Per-lane LUT tables (layout of build_lut_table) of the ntl tiles and NM
+// matrices of one item, table q = tile * NM + matrix.  Every thread first loads
+// its (at most two) 16-byte runs of eight LUT entries, then writes them out, so
+// the item pays one global-load latency instead of one per table and entry.
+template <int B, int NM>
+__device__ __forceinline__ void build_item_tables(const DevLayer& L, int e, int phase, int tile0, int ntl,
+                                                  unsigned char* smem, int tid) {
+  constexpr int V = 1 << B;
+  constexpr int RUNS = V / 8;              // 16-byte runs per LUT row
+  constexpr int PER_TABLE = 16 * RUNS;     // runs per 16-row table
+  constexpr int MAX_PER_THREAD = (kTabBudget / (V * 256)) * PER_TABLE / kFfnThreads;
+  static_assert(MAX_PER_THREAD >= 1 && MAX_PER_THREAD <= 2, "table build sized for two runs per thread");
+  const int units = ntl * NM * PER_TABLE;
+  uint4 v[MAX_PER_THREAD];
 #pragma unroll
-  for (int p = 0; p < 3; ++p) m |= w[p] & rotl_c(0x11111111u, s + 5 - p);
-  const uint32_t sel0 = rotr(m, s + 3), sel1 = rotr(m, s + 19);
-  uint32_t lo = prmt(lut[0][0], lut[0][1], sel0), hi = prmt(lut[0][2], lut[0][3], sel0);
-  a[0] = prmt(lo, hi, 0x5140u);
-  a[2] = prmt(lo, hi, 0x7362u);
-  lo = prmt(lut[1][0], lut[1][1], sel1);
-  hi = prmt(lut[1][2], lut[1][3], sel1);
-  a[1] = prmt(lo, hi, 0x5140u);
-  a[3] = prmt(lo, hi, 0x7362u);
-}
-
-__device__ __forceinline__ void load_lut3(const __half* row, uint32_t (&r)[4]) {
-  const uint4 v = *reinterpret_cast<const uint4*>(row);
-  r[0] = prmt(v.x, v.y, 0x6420u);
-  r[1] = prmt(v.z, v.w, 0x6420u);
-  r[2] = prmt(v.x, v.y, 0x7531u);
-  r[3] = prmt(v.z, v.w, 0x7531u);
-}
-
-__device__ __forceinline__ void load_bfrag(const __half* act, const int (&rowoff)[kNT], int NT, int col,
-                                           uint32_t (&bf)[kNT][2]) {
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
-    if (nt < NT) {
-      const __half* xp = act + rowoff[nt] + col;
-      bf[nt][0] = *reinterpret_cast<const uint32_t*>(xp);
-      bf[nt][1] = *reinterpret_cast<const uint32_t*>(xp + 8);
+  for (int k = 0; k < MAX_PER_THREAD; ++k) {
+    const int u = tid + k * kFfnThreads;
+    if (u < units) {
+      const int q = u / PER_TABLE, w = u % PER_TABLE;
+      const int m = phase == 0 ? q % NM : 2;
+      const int rg = w / RUNS, v0 = (w % RUNS) * 8;
+      const __half* lr = lut_rows(L, e, m, B, (tile0 + q / NM) * kTileRows);
+      v[k] = *reinterpret_cast<const uint4*>(lr + rg * V + v0);
     }
   }
-}
-
-// Issue the copies of plane group gamma (NM matrices, B planes) into ring slot `slot`:
-// slot layout [matrix*B + plane][lane] x 16 bytes.
-template <int B, int NM, int PB>
-__device__ __forceinline__ void issue_group(const char* const (&base)[NM][PB], int gamma, int G, int rem, int lane,
-                                            uint32_t slot) {
-  if (gamma < G) {
-    const size_t off = (size_t)(gamma * 128 + lane * 4) * 4;
 #pragma unroll
-    for (int mi = 0; mi < NM; ++mi)
+  for (int k = 0; k < MAX_PER_THREAD; ++k) {
+    const int u = tid + k * kFfnThreads;
+    if (u < units) {
+      const int q = u / PER_TABLE, w = u % PER_TABLE;
+      const int rg = w / RUNS, v0 = (w % RUNS) * 8;
+      uint4* tab = reinterpret_cast<uint4*>(smem + (size_t)q * V * 256);
+      const uint32_t wv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
-      for (int p = 0; p < B; ++p) cp_async16(slot + ((mi * B + p) * 32 + lane) * 16, base[mi][p] + off);
-  } else {
-    const size_t off = (size_t)(G * 128 + lane * rem) * 4;
-#pragma unroll
-    for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-      for (int p = 0; p < B; ++p)
-        for (int i = 0; i < rem; ++i) cp_async4(slot + ((mi * B + p) * 32 + lane) * 16 + 4 * i, base[mi][p] + off + 4 * i);
-  }
-}
-
-// K loop of one warp over its plane groups (gamma = g0, g0 + gstep, ...).
-// lut3: register LUTs (B == 3); tab: smem table of (tile, matrix 0) (B >= 4).
-template <int B, int NM, int RING, int PB>
-__device__ __forceinline__ void warp_planes(const __half* act, const char* const (&base)[NM][PB], int K, int g0,
-                                            int gstep, const int (&rowoff)[kNT], int NT,
-                                            const uint32_t (&lut3)[NM][2][4], uint32_t tab, uint32_t tab_stride,
-                                            uint32_t ring, float (&acc)[NM][kNT][4]) {
-  const int lane = threadIdx.x & 31;
-  const int nk = K / 64, G = nk / 4, rem = nk % 4, NG = G + (rem ? 1 : 0);
-  const uint32_t lb0 = lane * 4, lb1 = 128 + lane * 4;
-  constexpr uint32_t kSlot = NM * B * 32 * 16;
-  const int nu = g0 < NG ? (NG - 1 - g0) / gstep + 1 : 0;
-#pragma unroll
-  for (int i = 0; i < RING - 1; ++i) {
-    if (i < nu) issue_group<B, NM, PB>(base, g0 + i * gstep, G, rem, lane, ring + (i % RING) * kSlot);
-    cp_commit();
-  }
-  // B fragments (tokens) of the next chunk are loaded while the current one is computed
-  uint32_t bcur[4][kNT][2], bnxt[4][kNT][2];
-  auto bload = [&](int kappa, uint32_t (&b)[4][kNT][2]) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) load_bfrag(act, rowoff, NT, kappa * 64 + s * 16, b[s]);
-  };
-  if (nu > 0) bload(4 * g0, bcur);
-  for (int i = 0; i < nu; ++i) {
-    const int inext = i + RING - 1;
-    if (inext < nu) issue_group<B, NM, PB>(base, g0 + inext * gstep, G, rem, lane, ring + (inext % RING) * kSlot);
-    cp_commit();
-    cp_wait<RING - 1>();
-    const int gamma = g0 + i * gstep;
-    const uint32_t slot = ring + (i % RING) * kSlot;
-    uint32_t cur[NM][B][4];
-#pragma unroll
-    for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-      for (int p = 0; p < B; ++p) {
-        const uint4 v = lds128(slot + ((mi * B + p) * 32 + lane) * 16);
-        cur[mi][p][0] = v.x;
-        cur[mi][p][1] = v.y;
-        cur[mi][p][2] = v.z;
-        cur[mi][p][3] = v.w;
-      }
-    const int nch = gamma < G ? 4 : rem;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (c >= nch) break;
-      const int kappa = 4 * gamma + c;
-      const int knext = c + 1 < nch ? kappa + 1 : (i + 1 < nu ? 4 * (gamma + gstep) : -1);
-      if (knext >= 0) bload(knext, bnxt);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-#pragma unroll
-        for (int mi = 0; mi < NM; ++mi) {
-          uint32_t w[B];
-#pragma unroll
-          for (int p = 0; p < B; ++p) w[p] = cur[mi][p][c];
-          uint32_t a[4];
-          if constexpr (B == 3) {
-            decode_step_prmt3(w, s, lut3[mi], a);
-          } else {
-            decode_step_lut<B>(w, s, tab + mi * tab_stride, lb0, lb1, a);
-          }
-#pragma unroll
-          for (int nt = 0; nt < kNT; ++nt)
-            if (nt < NT) mma16816(acc[mi][nt], a, bcur[s][nt][0], bcur[s][nt][1]);
-        }
-      }
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          bcur[s][nt][0] = bnxt[s][nt][0];
-          bcur[s][nt][1] = bnxt[s][nt][1];
-        }
-    }
-  }
-  cp_wait<0>();
-}
-
-// K loop of one warp over its 64-column chunks of fp16 weights (fallback pages
-// or the shared FFN): chunk kappa = k0, k0 + kstep, ...
-template <int NM, int RING>
-__device__ __forceinline__ void warp_f16(const __half* act, const char* const (&base16)[NM], int K, int k0,
-                                         int kstep, const int (&rowoff)[kNT], int NT, uint32_t ring,
-                                         float (&acc)[NM][kNT][4]) {
-  const int lane = threadIdx.x & 31;
-  const int nk = K / 64;
-  constexpr uint32_t kSlot = NM * 4 * 32 * 16;
-  const int nu = k0 < nk ? (nk - 1 - k0) / kstep + 1 : 0;
-  auto issue = [&](int kappa, uint32_t slot) {
-#pragma unroll
-    for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        cp_async16(slot + ((mi * 4 + s) * 32 + lane) * 16, base16[mi] + ((size_t)(kappa * 4 + s) * 32 + lane) * 16);
-  };
-#pragma unroll
-  for (int i = 0; i < RING - 1; ++i) {
-    if (i < nu) issue(k0 + i * kstep, ring + (i % RING) * kSlot);
-    cp_commit();
-  }
-  uint32_t bcur[4][kNT][2], bnxt[4][kNT][2];
-  auto bload = [&](int kappa, uint32_t (&b)[4][kNT][2]) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) load_bfrag(act, rowoff, NT, kappa * 64 + s * 16, b[s]);
-  };
-  if (nu > 0) bload(k0, bcur);
-  for (int i = 0; i < nu; ++i) {
-    const int inext = i + RING - 1;
-    if (inext < nu) issue(k0 + inext * kstep, ring + (inext % RING) * kSlot);
-    cp_commit();
-    cp_wait<RING - 1>();
-    const int kappa = k0 + i * kstep;
-    if (i + 1 < nu) bload(kappa + kstep, bnxt);
-    const uint32_t slot = ring + (i % RING) * kSlot;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-#pragma unroll
-      for (int mi = 0; mi < NM; ++mi) {
-        const uint4 v = lds128(slot + ((mi * 4 + s) * 32 + lane) * 16);
-        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-          if (nt < NT) mma16816(acc[mi][nt], a, bcur[s][nt][0], bcur[s][nt][1]);
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t val = (wv[i >> 1] >> (16 * (i & 1))) & 0xffffu;
+        const uint32_t dup = val | (val << 16);
+        tab[((v0 + i) * 256 + rg * 16) / 16] = make_uint4(dup, dup, dup, dup);
       }
     }
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        bcur[s][nt][0] = bnxt[s][nt][0];
-        bcur[s][nt][1] = bnxt[s][nt][1];
-      }
   }
-  cp_wait<0>();
 }
 
 template <int NM, int CLS>
@@ -299,7 +122,8 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
   __shared__ int s_pref[kMaxExperts + 1];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_bits[kMaxExperts];
-  __shared__ int s_rw;
+  __shared__ short s_ord[kMaxExperts];  // experts of the class, by bitwidth then index
+  __shared__ int s_rw, s_ne;
 
   const DevLayer& L = P.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -334,26 +158,40 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
       for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
       if (tot >= (int)gridDim.x) break;
     }
+    // experts ordered by bitwidth, so that the CTAs running at the same time
+    // mostly execute the decode path of one bitwidth
+    int ne = 0;
+    for (int b = 3; b <= 16; ++b) {
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool in = e < E && s_bits[e] == b && count(e, RW) > 0;
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        if (in) s_ord[ne + __popc(m & ((1u << lane) - 1))] = (short)e;
+        ne += __popc(m);
+      }
+    }
     int run = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int c = e < E ? count(e, RW) : 0;
+    for (int k0 = 0; k0 < ne; k0 += 32) {
+      const int k = k0 + lane;
+      const int c = k < ne ? count(s_ord[k], RW) : 0;
       int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      if (e < E) s_pref[e] = run + incl - c;
+      if (k < ne) s_pref[k] = run + incl - c;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) {
-      s_pref[E] = run;
+      s_pref[ne] = run;
+      s_ne = ne;
       s_rw = RW;
     }
   }
   __syncthreads();
-  const int total = s_pref[E];
+  const int ne = s_ne;
+  const int total = s_pref[ne];
   const int RW = s_rw;
 
   const uint32_t tab0 = smem_u32(smem_ffn);
@@ -362,16 +200,16 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
   float* red = reinterpret_cast<float*>(smem_ffn + D::TABS);  // aliases the rings after the K loop
 
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    int lo = 0, hi = E;  // find e with s_pref[e] <= item < s_pref[e+1]
+    int lo = 0, hi = ne;  // find k with s_pref[k] <= item < s_pref[k+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (s_pref[mid] <= item) lo = mid; else hi = mid;
     }
-    const int e = lo;
+    const int e = s_ord[lo];
     const int b = s_bits[e];
     const int n_e = s_off[e + 1] - s_off[e];
     const int nch = (n_e + kTok - 1) / kTok;
-    const int local = item - s_pref[e];
+    const int local = item - s_pref[lo];
     // token chunks of one tile block are adjacent, so their weight re-reads hit L2
     const int blk = local / nch, chunk = local % nch;
     const int rw = min(RW, rw_cap(b, NM));
@@ -388,16 +226,10 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
     (void)routed;
 
     if (CLS == 1) {  // per-lane LUT copies of every (tile, matrix) of the item
-      for (int q = 0; q < ntl * NM; ++q) {
-        const int j = q / NM, mi = q % NM;
-        const int m = P.phase == 0 ? mi : 2;
-        uint32_t* tab = reinterpret_cast<uint32_t*>(smem_ffn + q * tstride);
-        const __half* lr = lut_rows(L, e, m, b, (tile0 + j) * kTileRows);
-        switch (b) {
-          case 4: build_lut_table<4>(lr, tab, tid, kFfnThreads); break;
-          case 5: build_lut_table<5>(lr, tab, tid, kFfnThreads); break;
-          default: build_lut_table<6>(lr, tab, tid, kFfnThreads); break;
-        }
+      switch (b) {
+        case 4: build_item_tables<4, NM>(L, e, P.phase, tile0, ntl, smem_ffn, tid); break;
+        case 5: build_item_tables<5, NM>(L, e, P.phase, tile0, ntl, smem_ffn, tid); break;
+        default: build_item_tables<6, NM>(L, e, P.phase, tile0, ntl, smem_ffn, tid); break;
       }
       __syncthreads();
     }
@@ -512,151 +344,6 @@ __global__ void __launch_bounds__(kFfnThreads, Dec<NM, CLS>::MIN_BLOCKS) ffn_dec
 }
 
 
-// ---------------------------------------------------------------------------
-// Warp-independent variant for 3-bit codes and fp16 pages: one warp owns a
-// work item (expert, 16-token chunk, 16-row tile) over the whole reduction,
-// so the only block-wide synchronisation is the item-list setup.  Every lane
-// keeps RING units of its own weight words in flight with cp.async.
-// ---------------------------------------------------------------------------
-constexpr int kWarpThreads = 128;  // four independent warps per CTA
-
-template <int NM, int B>
-struct WDec {
-  static constexpr int RING = B == 16 ? 3 : 4;
-  static constexpr int UNIT = B == 16 ? NM * 4 * 16 : NM * B * 16;  // bytes per lane per unit
-  static constexpr int WARP_RING = RING * UNIT * 32;
-  static constexpr int SMEM = (kWarpThreads / 32) * WARP_RING;
-};
-
-template <int NM, int B>
-__global__ void __launch_bounds__(kWarpThreads, 4) ffn_warp_kernel(FfnParams P) {
-  using D = WDec<NM, B>;
-  extern __shared__ __align__(16) unsigned char smem_w[];
-  __shared__ int s_pref[kMaxExperts + 1];
-  __shared__ int s_off[kMaxExperts + 1];
-  __shared__ int s_bits[kMaxExperts];
-
-  const DevLayer& L = P.L;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool routed = P.mode == 0;
-  const int E = routed ? L.E : 1;
-  const int fe = routed ? L.f : L.fs;
-  const int K = P.phase == 0 ? L.d : fe;
-  const int tiles = P.phase == 0 ? fe / kTileRows : L.d / kTileRows;
-
-  if (routed) {
-    for (int i = tid; i <= E; i += kWarpThreads) s_off[i] = P.offsets[i];
-    for (int i = tid; i < E; i += kWarpThreads) s_bits[i] = L.bits[i];
-  } else if (tid == 0) {
-    s_off[0] = 0;
-    s_off[1] = P.n_slots;
-    s_bits[0] = 16;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int run = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      int c = 0;
-      if (e < E) {
-        const int n = s_off[e + 1] - s_off[e];
-        if (n > 0 && n <= P.max_tokens && s_bits[e] == B) c = ((n + kTok - 1) / kTok) * tiles;
-      }
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (e < E) s_pref[e] = run + incl - c;
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) s_pref[E] = run;
-  }
-  __syncthreads();
-  const int total = s_pref[E];
-  const uint32_t ring = smem_u32(smem_w) + warp * D::WARP_RING;
-  const int nwarps = gridDim.x * (kWarpThreads / 32);
-
-  for (int item = blockIdx.x * (kWarpThreads / 32) + warp; item < total; item += nwarps) {
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_pref[mid] <= item) lo = mid; else hi = mid;
-    }
-    const int e = lo;
-    const int n_e = s_off[e + 1] - s_off[e];
-    const int nch = (n_e + kTok - 1) / kTok;
-    const int local = item - s_pref[e];
-    const int tau = local / nch, chunk = local % nch;  // chunks of one tile on neighbouring warps
-    const int slot0 = s_off[e] + chunk * kTok;
-    const int ntok = min(kTok, s_off[e + 1] - slot0);
-    const int NT = (ntok + 7) >> 3;
-
-    int rowoff[kNT];
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-      const int tok = min(nt * 8 + (lane >> 2), ntok - 1);
-      rowoff[nt] = (slot0 + tok) * K + 2 * (lane & 3);
-    }
-    float acc[NM][kNT][4];
-#pragma unroll
-    for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) acc[mi][nt][r] = 0.f;
-
-    if constexpr (B == 16) {
-      const char* b16[NM];
-#pragma unroll
-      for (int mi = 0; mi < NM; ++mi) {
-        const int m = P.phase == 0 ? mi : 2;
-        b16[mi] = routed ? tile_addr(L, e, m, kPlanes, tau)
-                         : reinterpret_cast<const char*>(L.shared16[m]) + (size_t)tau * 32 * K;
-      }
-      warp_f16<NM, D::RING>(P.act, b16, K, 0, 1, rowoff, NT, ring, acc);
-    } else {
-      const char* base[NM][3];
-      uint32_t lut3[NM][2][4];
-#pragma unroll
-      for (int mi = 0; mi < NM; ++mi) {
-        const int m = P.phase == 0 ? mi : 2;
-#pragma unroll
-        for (int p = 0; p < 3; ++p) base[mi][p] = tile_addr(L, e, m, p, tau);
-        const __half* lr = lut_rows(L, e, m, 3, tau * kTileRows);
-        load_lut3(lr + (lane >> 2) * 8, lut3[mi][0]);
-        load_lut3(lr + ((lane >> 2) + 8) * 8, lut3[mi][1]);
-      }
-      warp_planes<3, NM, D::RING, 3>(P.act, base, K, 0, 1, rowoff, NT, lut3, 0u, 0u, ring, acc);
-    }
-
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int j = nt * 8 + 2 * t + (r & 1);
-        const int row = tau * kTileRows + g + 8 * (r >> 1);
-        if (j < ntok) {
-          if (NM == 2)
-            P.h[(size_t)(slot0 + j) * fe + row] = __float2half_rn(silu_f(acc[0][nt][r]) * acc[NM - 1][nt][r]);
-          else
-            P.y[(size_t)(slot0 + j) * L.d + row] = acc[0][nt][r];
-        }
-      }
-  }
-}
-
-template <int NM, int B>
-static cudaError_t launch_warp_class(const FfnParams& P, cudaStream_t s) {
-  using D = WDec<NM, B>;
-  cudaError_t e = ensure_smem((const void*)ffn_warp_kernel<NM, B>, D::SMEM);
-  if (e != cudaSuccess) return e;
-  ffn_warp_kernel<NM, B><<<sm_count() * 4, kWarpThreads, D::SMEM, s>>>(P);
-  return cudaGetLastError();
-}
-
 template <int NM, int CLS>
 static cudaError_t launch_decode_class(const FfnParams& P, int grid_per_sm, cudaStream_t s) {
   using D = Dec<NM, CLS>;
@@ -666,41 +353,49 @@ static cudaError_t launch_decode_class(const FfnParams& P, int grid_per_sm, cuda
   return cudaGetLastError();
 }
 
-cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* offsets, int n_slots, float* y,
-                       __half* h_ws, int class_mask, cudaStream_t s) {
-  // Experts with at most `thr` tokens take the mma.sync path; larger ones the
-  // tcgen05 GEMM.  No expert can have more tokens than the batch.
-  const int T = mode == 0 ? n_slots / L.K : n_slots;
+cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* offsets, int n_slots, float* y_perm,
+                           __half* h, const __half* x_sh, int T, float* y_sh, __half* hs, int class_mask,
+                           cudaStream_t s) {
+  // Experts with at most `thr` tokens take the decode kernels; larger ones the
+  // tcgen05 GEMM.  No expert can have more tokens than the batch, and the
+  // shared FFN sees every token.
   const int thr = decode_max_tokens();
+  const bool routed = offsets != nullptr && n_slots > 0;
   const bool big = T > thr;
-  if (mode != 0) class_mask = 4;
-  FfnParams P;
-  P.L = L;
-  P.mode = mode;
-  P.offsets = offsets;
-  P.n_slots = n_slots;
-  P.max_tokens = big ? thr : INT_MAX;
-  P.h = h_ws;
-  P.y = y;
+  const bool shared_decode = x_sh != nullptr && T > 0 && !big;
   cudaError_t e;
-  for (int phase = 0; phase < 2; ++phase) {
-    P.phase = phase;
-    P.act = phase == 0 ? x : h_ws;
-    if (class_mask & 1) {
-      e = phase == 0 ? launch_warp_class<2, 3>(P, s) : launch_warp_class<1, 3>(P, s);
-      if (e != cudaSuccess) return e;
-    }
-    if (class_mask & 2) {
+  if (routed && (class_mask & 2)) {  // 4, 5, 6-bit experts: CTA-level kernel with LUT tables
+    FfnParams P;
+    P.L = L;
+    P.mode = 0;
+    P.offsets = offsets;
+    P.n_slots = n_slots;
+    P.max_tokens = big ? thr : INT_MAX;
+    P.h = h;
+    P.y = y_perm;
+    for (int phase = 0; phase < 2; ++phase) {
+      P.phase = phase;
+      P.act = phase == 0 ? x_perm : h;
       e = phase == 0 ? launch_decode_class<2, 1>(P, Dec<2, 1>::MIN_BLOCKS, s)
                      : launch_decode_class<1, 1>(P, Dec<1, 1>::MIN_BLOCKS, s);
       if (e != cudaSuccess) return e;
     }
-    if (class_mask & 4) {
-      e = phase == 0 ? launch_warp_class<2, 16>(P, s) : launch_warp_class<1, 16>(P, s);
+  }
+  const int bit_mask = routed ? ((class_mask & 1) ? 1 : 0) | ((class_mask & 4) ? 2 : 0) : 0;
+  if (bit_mask || shared_decode) {
+    e = launch_uni(L, shared_decode ? x_sh : nullptr, bit_mask ? x_perm : nullptr, bit_mask ? offsets : nullptr, T,
+                   bit_mask, big ? thr : T, h, hs, y_perm, y_sh, s);
+    if (e != cudaSuccess) return e;
+  }
+  for (int phase = 0; phase < 2; ++phase) {
+    if (routed && big) {
+      e = launch_prefill(L, 0, phase, phase == 0 ? x_perm : h, offsets, n_slots, thr, h, y_perm, s);
       if (e != cudaSuccess) return e;
     }
-    if (big) {
-      e = launch_prefill(L, mode, phase, P.act, offsets, n_slots, thr, h_ws, y, s);
+  }
+  for (int phase = 0; phase < 2; ++phase) {
+    if (x_sh != nullptr && T > 0 && big) {
+      e = launch_prefill(L, 1, phase, phase == 0 ? x_sh : hs, nullptr, T, thr, hs, y_sh, s);
       if (e != cudaSuccess) return e;
     }
   }

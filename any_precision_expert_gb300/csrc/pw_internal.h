@@ -14,6 +14,12 @@ constexpr int kMaxTopK = 8;
 constexpr int kPlanes = 6;           // planes of the 6-bit parent code
 constexpr int kTileRows = 16;        // rows per stored tile
 constexpr int kChunkCols = 64;       // columns per stored chunk
+constexpr int kSyncHeader = 32;      // claim and exit counters of the persistent decode kernel
+constexpr int kSyncChunks = 64;      // 16-token chunks per group tracked by its phase counters
+
+// Words of a layer's sync area: header, then gate/up and down tile counters
+// for every (group, chunk), a group being a routed expert or the shared FFN.
+inline size_t sync_words(int E) { return kSyncHeader + 2 * (size_t)(E + 1) * kSyncChunks; }
 
 // Per-layer parameter block handed to kernels by value.  All pointers are
 // device addresses inside the layer's resident pool run.
@@ -31,6 +37,7 @@ struct DevLayer {
   unsigned lut_off[3][4];               // byte offset of LUT_b (b = 3 + i) of matrix m
   const __half* shared16[3];            // packed fp16 shared FFN (gate, up, down) or null
   int* err;                             // device error word
+  int* sync;                            // [sync_words(E)] zero between launches
 };
 
 // Scratch carved out of the caller's workspace for one hot-path call.
@@ -49,11 +56,18 @@ size_t permute_ws_bytes(int S, int E);
 cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __half* x,
                            int* offsets, int* perm_src, int* inv_slot, __half* x_perm,
                            int* hist_ws, cudaStream_t s);
-// mode 0: routed experts over permuted slots; mode 1: the shared fp16 FFN over all T tokens.
-// class_mask: bit 0 launch the decode kernel for 3-bit experts, bit 1 the one for 4, 5, 6 bits,
-// bit 2 the one for fp16 pages.
-cudaError_t launch_ffn(const DevLayer& L, int mode, const __half* x, const int* offsets, int n_slots,
-                       float* y, __half* h_ws, int class_mask, cudaStream_t s);
+// Expert FFN of one layer call.  Routed experts over permuted slots when
+// offsets is non-null (x_perm, y_perm, h [n_slots][ffn]); the shared fp16 FFN
+// over all T tokens when x_sh is non-null (y_sh, hs [T][shared_ffn]).
+// class_mask: bit 0 routed 3-bit experts may occur, bit 1 4..6-bit ones, bit 2
+// fp16 pages.
+cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* offsets, int n_slots, float* y_perm,
+                           __half* h, const __half* x_sh, int T, float* y_sh, __half* hs, int class_mask,
+                           cudaStream_t s);
+// Persistent decode kernel for routed 3-bit / fp16 experts (bit_mask bits 0 / 1)
+// with at most max_tokens tokens and, when x is non-null, the shared FFN.
+cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
+                       int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s);
 int decode_max_tokens();
 cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
                            int n_slots, int min_tokens, __half* h, float* y, cudaStream_t s);

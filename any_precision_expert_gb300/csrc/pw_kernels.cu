@@ -50,8 +50,7 @@ cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s) {
 // router: logits, softmax over E, top-K (ties to the lower index)
 // ---------------------------------------------------------------------------
 
-constexpr int kRouteTok = 4;      // tokens per CTA
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 512;
 
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
   const __half2* ha = reinterpret_cast<const __half2*>(&a);
@@ -67,6 +66,7 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
   return acc;
 }
 
+template <int kRouteTok>  // tokens per CTA
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const __half* __restrict__ x,
                                                               const __half* __restrict__ wr,
                                                               const float* __restrict__ bias, int T,
@@ -84,38 +84,40 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const 
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Each warp takes experts warp, warp + 8, ... in batches of four: the lane's
-  // 16-byte pieces of all four W_r rows are loaded before any is used, so a
-  // batch costs one memory round trip.
-  constexpr int kEB = 4;
-  const int per_lane = (d8 + 31) / 32;  // uint4 pieces of one row per lane (<= 64 for d <= 16384)
-  for (int e0 = warp * kEB; e0 < E; e0 += (kRouteThreads / 32) * kEB) {
+  // Work unit = (four experts, one 1024-column slice of d): a lane loads its
+  // four 16-byte pieces of the four W_r rows at once (one memory round trip
+  // per unit) and the warps share the units.  Slice sums are added in slice
+  // order afterwards, so the logits do not depend on the schedule.
+  constexpr int kEB = 4, kPieces = 4;
+  const int ns = (d8 + 32 * kPieces - 1) / (32 * kPieces);
+  const int nb = (E + kEB - 1) / kEB;
+  float* part = logit + kRouteTok * E;  // [ns][kRouteTok][E]
+  for (int u = warp; u < nb * ns; u += kRouteThreads / 32) {
+    const int e0 = (u / ns) * kEB, sl = u % ns;
+    uint4 wv[kEB][kPieces];
+#pragma unroll
+    for (int q = 0; q < kEB; ++q)
+#pragma unroll
+      for (int i = 0; i < kPieces; ++i) {
+        const int c = (sl * kPieces + i) * 32 + lane;
+        wv[q][i] = (e0 + q < E && c < d8) ? __ldg(reinterpret_cast<const uint4*>(wr) + (size_t)(e0 + q) * d8 + c)
+                                          : make_uint4(0, 0, 0, 0);
+      }
     float acc[kEB][kRouteTok];
 #pragma unroll
     for (int q = 0; q < kEB; ++q)
 #pragma unroll
       for (int t = 0; t < kRouteTok; ++t) acc[q][t] = 0.f;
-    for (int c0 = 0; c0 < per_lane; c0 += 4) {
-      uint4 wv[kEB][4];
 #pragma unroll
-      for (int q = 0; q < kEB; ++q)
+    for (int i = 0; i < kPieces; ++i) {
+      const int c = (sl * kPieces + i) * 32 + lane;
+      if (c < d8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = (c0 + i) * 32 + lane;
-          wv[q][i] = (e0 + q < E && c < d8) ? __ldg(reinterpret_cast<const uint4*>(wr) + (size_t)(e0 + q) * d8 + c)
-                                            : make_uint4(0, 0, 0, 0);
-        }
+        for (int t = 0; t < kRouteTok; ++t) {
+          if (t < nt) {
+            const uint4 xv = xs[t * d8 + c];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = (c0 + i) * 32 + lane;
-        if (c < d8) {
-#pragma unroll
-          for (int t = 0; t < kRouteTok; ++t) {
-            if (t < nt) {
-              const uint4 xv = xs[t * d8 + c];
-#pragma unroll
-              for (int q = 0; q < kEB; ++q) acc[q][t] += dot8(wv[q][i], xv);
-            }
+            for (int q = 0; q < kEB; ++q) acc[q][t] += dot8(wv[q][i], xv);
           }
         }
       }
@@ -127,8 +129,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const 
         float v = acc[q][t];
 #pragma unroll
         for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0 && t < nt && e0 + q < E) logit[t * E + e0 + q] = v + (bias ? bias[e0 + q] : 0.f);
+        if (lane == 0 && t < nt && e0 + q < E) part[((size_t)sl * kRouteTok + t) * E + e0 + q] = v;
       }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nt * E; i += kRouteThreads) {
+    const int t = i / E, e = i % E;
+    float v = bias ? bias[e] : 0.f;
+    for (int sl = 0; sl < ns; ++sl) v += part[((size_t)sl * kRouteTok + t) * E + e];
+    logit[t * E + e] = v;
   }
   __syncthreads();
 
@@ -191,14 +200,26 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const 
   }
 }
 
+template <int TPC>
+static cudaError_t launch_route_tpc(const DevLayer& L, const __half* x, const __half* wr, const float* bias, int T,
+                                   int* idx, float* w, int* counts, cudaStream_t s) {
+  const int ns = (L.d / 8 + 127) / 128;  // 1024-column slices of d
+  const size_t smem = (size_t)TPC * L.d * sizeof(__half) + (size_t)(1 + ns) * TPC * L.E * sizeof(float);
+  cudaError_t e = ensure_smem((const void*)route_kernel<TPC>, smem);
+  if (e != cudaSuccess) return e;
+  route_kernel<TPC><<<(T + TPC - 1) / TPC, kRouteThreads, smem, s>>>(L, x, wr, bias, T, idx, w, counts);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const DevLayer& L, const __half* x, const __half* wr, const float* bias, int T, int* idx,
                          float* w, int* counts, cudaStream_t s) {
-  const size_t smem = (size_t)kRouteTok * L.d * sizeof(__half) + (size_t)kRouteTok * L.E * sizeof(float);
-  cudaError_t e = ensure_smem((const void*)route_kernel, smem);
-  if (e != cudaSuccess) return e;
-  const int grid = (T + kRouteTok - 1) / kRouteTok;
-  route_kernel<<<grid, kRouteThreads, smem, s>>>(L, x, wr, bias, T, idx, w, counts);
-  return cudaGetLastError();
+  // small batches: one token per CTA so the router's weight rows are read by
+  // many SMs in parallel; large batches: eight tokens per CTA to reuse them
+  const int per_sm = T / sm_count();
+  if (per_sm < 2) return launch_route_tpc<1>(L, x, wr, bias, T, idx, w, counts, s);
+  if (per_sm < 8) return launch_route_tpc<2>(L, x, wr, bias, T, idx, w, counts, s);
+  if (per_sm < 32) return launch_route_tpc<4>(L, x, wr, bias, T, idx, w, counts, s);
+  return launch_route_tpc<8>(L, x, wr, bias, T, idx, w, counts, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -241,16 +262,28 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(DevLayer L, 
   const int E = L.E, K = L.K, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
-  // bucket starts (exclusive scan of the totals) and this chunk's base per expert
+  // bucket starts (exclusive scan of the totals) and this chunk's base per expert;
+  // with a single chunk (hist == nullptr) the chunk counts its own slots
   int pre = 0, tot = 0;
-  if (tid < E) {
+  if (hist == nullptr) {
+    for (int i = tid; i < E; i += blockDim.x) scan[i] = 0;
+    __syncthreads();
+    for (int sl = tid; sl < S; sl += blockDim.x) {
+      const int e = idx[sl];
+      if ((unsigned)e < (unsigned)E) atomicAdd(&scan[e], 1);
+      else atomicExch(L.err, 2);
+    }
+    __syncthreads();
+    if (tid < E) tot = scan[tid];
+    __syncthreads();
+  } else if (tid < E) {
     for (int c = 0; c < nblk; ++c) {
       const int v = hist[c * E + tid];
       tot += v;
       if (c < (int)blockIdx.x) pre += v;
     }
-    scan[tid] = tot;
   }
+  if (tid < E) scan[tid] = tot;
   __syncthreads();
   // Hillis-Steele inclusive scan over E <= 256 entries
   for (int o = 1; o < kMaxExperts; o <<= 1) {
@@ -317,8 +350,12 @@ cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __hal
     return e;
   }
   const int nblk = (S + kPermChunk - 1) / kPermChunk;
-  perm_hist_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws);
-  perm_scatter_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws, nblk, offsets, perm_src, inv_slot);
+  if (nblk == 1) {
+    perm_scatter_kernel<<<1, kPermThreads, 0, s>>>(L, idx, S, nullptr, 1, offsets, perm_src, inv_slot);
+  } else {
+    perm_hist_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws);
+    perm_scatter_kernel<<<nblk, kPermThreads, 0, s>>>(L, idx, S, hist_ws, nblk, offsets, perm_src, inv_slot);
+  }
   if (x_perm) {
     const long long pieces = (long long)S * (L.d / 8);
     perm_gather_kernel<<<(unsigned)((pieces + 255) / 256), 256, 0, s>>>(

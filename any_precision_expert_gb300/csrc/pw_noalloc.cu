@@ -56,7 +56,8 @@ extern "C" pw_status pw_expert_ffn_bitplane_noalloc(pw_layer_t layer, const void
   void* scratch = nullptr;
   cudaError_t e = scratch_address(&scratch);
   if (e != cudaSuccess) return pw::record_cuda_error(e);
-  e = pw::launch_ffn(dev, 0, static_cast<const __half*>(x_perm), offsets, T * dev.K, y_perm,
-                     static_cast<__half*>(scratch), class_mask, reinterpret_cast<cudaStream_t>(stream));
+  e = pw::launch_moe_ffn(dev, static_cast<const __half*>(x_perm), offsets, T * dev.K, y_perm,
+                         static_cast<__half*>(scratch), nullptr, T, nullptr, nullptr, class_mask,
+                         reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PW_OK : pw::record_cuda_error(e);
 }

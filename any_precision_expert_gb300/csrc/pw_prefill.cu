@@ -422,7 +422,8 @@ int decode_max_tokens() {
   // experts with more tokens than this use the tensor-core GEMM (read per call)
   const char* s = getenv("PW_DECODE_MAX_TOK");
   const int v = s ? atoi(s) : 256;
-  return v < 0 ? 0 : v;
+  // the persistent decode kernel tracks at most kSyncChunks chunks of kTok tokens per expert
+  return v < 0 ? 0 : v > kSyncChunks * 16 ? kSyncChunks * 16 : v;
 }
 
 namespace {

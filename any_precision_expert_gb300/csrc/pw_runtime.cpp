@@ -236,6 +236,7 @@ struct pw_layer_s {
   // device tables (inside the resident run)
   int* d_bits = nullptr;
   int* d_err = nullptr;
+  int* d_sync = nullptr;
   unsigned long long* d_plane_pt = nullptr;
   unsigned long long* d_f16_pt = nullptr;
   uint2* d_tmap = nullptr;
@@ -272,6 +273,7 @@ struct pw_layer_s {
     memcpy(L.lut_off, lut_off, sizeof(lut_off));
     for (int m = 0; m < 3; ++m) L.shared16[m] = shared_loaded ? d_shared[m] : nullptr;
     L.err = d_err;
+    L.sync = d_sync;
     return L;
   }
 };
@@ -454,6 +456,7 @@ extern "C" pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, 
   };
   const size_t o_bits = carve(sizeof(int) * E);
   const size_t o_err = carve(16);
+  const size_t o_sync = carve(sizeof(int) * sync_words(E));
   const size_t o_ppt = carve(sizeof(unsigned long long) * (size_t)E * kPlanes * l->pmax);
   const size_t o_fpt = carve(sizeof(unsigned long long) * (size_t)E * l->pmax16);
   const size_t o_tmap = carve(sizeof(uint2) * 3 * (size_t)l->tmax);
@@ -473,6 +476,7 @@ extern "C" pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, 
   char* rb = l->res_base;
   l->d_bits = reinterpret_cast<int*>(rb + o_bits);
   l->d_err = reinterpret_cast<int*>(rb + o_err);
+  l->d_sync = reinterpret_cast<int*>(rb + o_sync);
   l->d_plane_pt = reinterpret_cast<unsigned long long*>(rb + o_ppt);
   l->d_f16_pt = reinterpret_cast<unsigned long long*>(rb + o_fpt);
   l->d_tmap = reinterpret_cast<uint2*>(rb + o_tmap);
@@ -492,7 +496,7 @@ extern "C" pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, 
 
   cudaStream_t s = nullptr;
   pw_status st = PW_OK;
-  if (st == PW_OK) st = dev_zero(rb, o_ppt, s);  // bits + error word
+  if (st == PW_OK) st = dev_zero(rb, o_ppt, s);  // bits, error word, sync area
   if (st == PW_OK) st = dev_zero(l->d_plane_pt, (o_tmap - o_ppt), s);
   if (st == PW_OK) st = dev_h2d(l->d_tmap, l->tmap.data(), sizeof(uint2) * l->tmap.size(), s);
   if (st == PW_OK) st = dev_h2d(l->d_tmap16, l->tmap16.data(), sizeof(uint2) * l->tmap16.size(), s);
@@ -780,8 +784,9 @@ extern "C" pw_status pw_expert_ffn_bitplane(pw_layer_t l, const void* x_perm, co
   PW_TRY(all_loaded(l));
   PW_TRY(device_only());
   char* wsb = static_cast<char*>(ws);
-  return launched(launch_ffn(l->dev(), 0, static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
-                             reinterpret_cast<__half*>(wsb + W.h_off), class_mask(l), as_stream(stream)));
+  return launched(launch_moe_ffn(l->dev(), static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
+                                 reinterpret_cast<__half*>(wsb + W.h_off), nullptr, T, nullptr, nullptr,
+                                 class_mask(l), as_stream(stream)));
 }
 
 extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_shared, void* ws, size_t ws_bytes,
@@ -795,8 +800,29 @@ extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_
   if (ws_bytes < W.total) return PW_ERR_OOM;
   PW_TRY(device_only());
   char* wsb = static_cast<char*>(ws);
-  return launched(launch_ffn(l->dev(), 1, static_cast<const __half*>(x), nullptr, T, y_shared,
-                             reinterpret_cast<__half*>(wsb + W.hs_off), 1, as_stream(stream)));
+  return launched(launch_moe_ffn(l->dev(), nullptr, nullptr, 0, nullptr, nullptr, static_cast<const __half*>(x), T,
+                                 y_shared, reinterpret_cast<__half*>(wsb + W.hs_off), 0, as_stream(stream)));
+}
+
+extern "C" pw_status pw_moe_ffn(pw_layer_t l, const void* x, const void* x_perm, const int32_t* offsets, int T,
+                                float* y_perm, float* y_shared, void* ws, size_t ws_bytes, void* stream) {
+  PW_TRY(check_layer(l));
+  if (T < 0) return PW_ERR_INVALID_ARG;
+  const bool sh = l->desc.shared_ffn != 0;
+  if (sh && !l->shared_loaded) return PW_ERR_INVALID_ARG;
+  if (T == 0) return device_only();
+  if (!x_perm || !offsets || !y_perm || !ws) return PW_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(y_perm)) return PW_ERR_INVALID_ARG;
+  if (sh && (!x || !y_shared || !aligned16(x) || !aligned16(y_shared))) return PW_ERR_INVALID_ARG;
+  const WsLayout W = ws_layout(l, T);
+  if (ws_bytes < W.total) return PW_ERR_OOM;
+  PW_TRY(all_loaded(l));
+  PW_TRY(device_only());
+  char* wsb = static_cast<char*>(ws);
+  return launched(launch_moe_ffn(l->dev(), static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
+                                 reinterpret_cast<__half*>(wsb + W.h_off), sh ? static_cast<const __half*>(x) : nullptr,
+                                 T, sh ? y_shared : nullptr, reinterpret_cast<__half*>(wsb + W.hs_off), class_mask(l),
+                                 as_stream(stream)));
 }
 
 extern "C" pw_status pw_combine(pw_layer_t l, const float* y_perm, const int32_t* inv_slot, const float* w, int T,
@@ -823,6 +849,8 @@ extern "C" pw_status pw_layer_check_device(pw_layer_t l, void* stream) {
     PW_CUDA(cudaMemcpyAsync(err, l->d_err, sizeof(err), cudaMemcpyDeviceToHost, s));
     PW_CUDA(cudaStreamSynchronize(s));
     PW_CUDA(cudaMemsetAsync(l->d_err, 0, sizeof(err), s));
+    // a kernel that gave up on a wait may have left its counters half-way
+    if (err[0] != 0) PW_CUDA(cudaMemsetAsync(l->d_sync, 0, sizeof(int) * sync_words(l->desc.n_experts), s));
     PW_CUDA(cudaStreamSynchronize(s));
   }
   if (err[0] == 1) return PW_ERR_TIMEOUT;

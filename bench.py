@@ -92,8 +92,9 @@ def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda"):
 
 
 def algorithmic_bytes(cfg, bits, offsets, T):
-    """Bytes the method must move for one step (weights of routed experts at their
-    bitwidth plus their LUT_b rows, shared FFN, router, x in, y out)."""
+    """Bytes the method must move: (expert-FFN call, whole step).  The FFN call
+    reads the weights of the routed experts at their bitwidth plus their LUT_b
+    rows and the shared FFN; the step adds the router weights, x in and y out."""
     d, f = cfg.d, cfg.f
     n = np.diff(offsets)
     ffn = 0
@@ -105,7 +106,7 @@ def algorithmic_bytes(cfg, bits, offsets, T):
     shared = 3 * d * cfg.shared_ffn * 2
     router = d * cfg.E * 2
     io = 2 * T * d * 2
-    return ffn, ffn + shared + router + io
+    return ffn + shared, ffn + shared + router + io
 
 
 # ---------------------------------------------------------------------------
@@ -232,19 +233,12 @@ def run_gpu(args):
         L.permute(b.idx, T, x, b.offsets, b.perm_src, b.inv_slot, b.x_perm, b.ws, stream)
 
     def part_f(L, b, x):
-        L.expert_ffn_bitplane(b.x_perm, b.offsets, T, b.y_perm, b.ws, stream)
+        L.moe_ffn(x, b.x_perm, b.offsets, T, b.y_perm, b.y_shared if cfg.shared_ffn else None, b.ws, stream)
 
     def part_c(L, b, x):
-        if cfg.shared_ffn:
-            L.shared_ffn(x, T, b.y_shared, b.ws, stream)
         L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared if cfg.shared_ffn else None, b.y, stream)
 
-    launches_per_step = 1 + 2 + 2 + 2 + 1  # route, permute(2), ffn(2), shared(2), combine
-    launches_per_step += 2  # the 4/5/6-bit decode class (launched when such planes are resident)
-    if T > int(os.environ.get("PW_DECODE_MAX_TOK", "256")):
-        launches_per_step += 2  # tcgen05 GEMM kernels for experts above the threshold
-    if not cfg.shared_ffn:
-        launches_per_step -= 2
+    launches_per_step = _launches_per_step(cfg, wl["bits"], T)
     if external:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -336,7 +330,7 @@ def run_gpu(args):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     else:
         peak, peak_src = 6800.0, "fallback 6.8 TB/s"
-    ffn_flops = 2.0 * T * cfg.K * 3 * cfg.d * cfg.f  # routed expert FFN, algorithmic
+    ffn_flops = 2.0 * T * 3 * cfg.d * (cfg.K * cfg.f + cfg.shared_ffn)  # routed + shared FFN, algorithmic
     tflops = ffn_flops / (ffn_avg_ms * 1e-3) / 1e12
     gbs = ffn_avg_bytes / (ffn_avg_ms * 1e-3) / 1e9
     # decode batches are bound by weight bytes, prefill batches by the tensor pipe
@@ -381,7 +375,7 @@ def run_gpu(args):
                 "device_errors": not ok,
             },
             "roofline": ({
-                "kernel": "expert FFN call (decode and tcgen05 GEMM kernels, gate/up + down)",
+                "kernel": "expert FFN call pw_moe_ffn (routed experts + shared FFN)",
                 "bound": "tensor",
                 "achieved": tflops,
                 "peak": tpk,
@@ -393,7 +387,7 @@ def run_gpu(args):
                 "avg_launch_ms": ffn_avg_ms,
                 "peak_source": tpk_src,
             } if tensor_bound else {
-                "kernel": "expert FFN call (decode and tcgen05 GEMM kernels, gate/up + down)",
+                "kernel": "expert FFN call pw_moe_ffn (routed experts + shared FFN)",
                 "bound": "hbm",
                 "achieved": gbs,
                 "peak": peak,
@@ -417,6 +411,26 @@ def run_gpu(args):
     if ws > 1:
         dist.destroy_process_group()
     return out
+
+
+def _launches_per_step(cfg, bits, T):
+    """Kernels one step launches: router, permutation (histogram + scatter for
+    more than 1024 slots, or one fused kernel), row gather, the 4/5/6-bit decode
+    kernel pair (when such planes are resident), the persistent decode kernel
+    (3-bit / fp16 experts and the shared FFN), the tcgen05 GEMM pair for experts
+    (and a shared FFN) above the token threshold, and the combine."""
+    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "256")), 1024)
+    S = T * cfg.K
+    n = 1 + (2 if S > 1024 else 1) + 1
+    if any(b in (4, 5, 6, 16) for b in np.asarray(bits).tolist()):
+        n += 2  # planes 3..5 are resident for 4..6-bit and fp16 experts
+    big = T > thr
+    n += 1  # persistent decode kernel
+    if big:
+        n += 2
+        if cfg.shared_ffn:
+            n += 2
+    return n + 1
 
 
 def _traffic_from_profile(workload, T):

@@ -11,7 +11,8 @@
  * "virtual page table" through which kernels read the weights.
  *
  * This header exposes one MoE layer's hot path on one GPU:
- *   pw_route_topk -> pw_permute -> pw_expert_ffn_bitplane (+ pw_shared_ffn)
+ *   pw_route_topk -> pw_permute -> pw_expert_ffn_bitplane (+ pw_shared_ffn, or both
+ *   in one pw_moe_ffn)
  *   -> pw_combine,   and   pw_set_expert_bitwidth.
  *
  * Conventions for every function
@@ -189,6 +190,19 @@ pw_status pw_expert_ffn_bitplane_noalloc(pw_layer_t layer, const void* x_perm, c
 /* fp16 shared FFN on all T tokens: y_shared [T][d] fp32 (layers with shared_ffn > 0). */
 pw_status pw_shared_ffn(pw_layer_t layer, const void* x, int T, float* y_shared,
                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * pw_expert_ffn_bitplane and, for layers with a shared FFN, pw_shared_ffn in
+ * one call: decode-sized work of both runs in one persistent kernel, so the
+ * shared FFN's weight stream overlaps the routed experts'.  Same results as
+ * the two calls.  x [T][d] and y_shared [T][d] are ignored (may be NULL) when
+ * the layer has no shared FFN.  ws must hold pw_workspace_size(T) bytes.
+ *
+ * The FFN calls of one layer keep progress counters in the layer's device
+ * state: run them on one stream (they may not overlap on the GPU).
+ */
+pw_status pw_moe_ffn(pw_layer_t layer, const void* x, const void* x_perm, const int32_t* offsets,
+                     int T, float* y_perm, float* y_shared, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Weighted combine:

@@ -86,6 +86,7 @@ class GpuLayer:
     def check_forward(self, x16, buf=None, tol=TOL):
         """Run the layer, compare routing (near ties allowed) and the output."""
         y, buf = self.forward(x16, buf)
+        assert self.layer.check_device() == 0, "device error word set (timeout or bounds check)"
         T = x16.shape[0]
         ref = self.oracle(x16)
         gidx = buf.idx[:T].cpu().numpy()

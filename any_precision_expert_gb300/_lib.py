@@ -49,6 +49,7 @@ _SIGS = {
     "pw_layer_destroy": (i32, [vp]),
     "pw_layer_load_expert": (i32, [vp, i32, i32, C.POINTER(U8P3), C.POINTER(LUTP), C.POINTER(U16P3), vp]),
     "pw_layer_load_shared": (i32, [vp, C.POINTER(U16P3), vp]),
+    "pw_layer_copy_expert": (i32, [vp, i32, vp, i32, i32, vp]),
     "pw_route_topk": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, vp]),
     "pw_permute": (i32, [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
     "pw_expert_ffn_bitplane": (i32, [vp, vp, vp, i32, vp, vp, sz, vp]),

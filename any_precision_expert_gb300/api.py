@@ -107,6 +107,11 @@ class Layer:
         check(lib.pw_layer_load_expert(self.handle, e, bits, C.byref(a_code), C.byref(a_lut),
                                        C.byref(a_w16), _s(stream)), f"pw_layer_load_expert(e={e})")
 
+    def copy_expert(self, e: int, src: "Layer", e_src: int, bits: int, stream=None):
+        """Device-to-device copy of src's expert e_src (at `bits`) into expert e."""
+        check(lib.pw_layer_copy_expert(self.handle, e, src.handle, e_src, bits, _s(stream)),
+              f"pw_layer_copy_expert(e={e})")
+
     def load_shared(self, w16, stream=None):
         ws = [_host(m, np.float16) for m in w16]
         arr = U16P3(*[m.ctypes.data for m in ws])

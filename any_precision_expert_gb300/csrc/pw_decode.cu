@@ -1,5 +1,6 @@
-// Persistent decode-side expert FFN: one launch runs gate/up and down for
-// every routed expert at 3 bits or on its fp16 page, and the fp16 shared FFN.
+// Persistent decode-side expert FFN: gate/up and down for every routed expert
+// with few tokens (3, 4, 5, 6 bits or its fp16 page) and for the fp16 shared
+// FFN, in at most two launches (one for 4..6-bit experts, one for the rest).
 //
 // PagedWeight (write-up "内存的饥饿游戏", section 核心洞察): an expert at
 // bitwidth b streams only its top b bit-planes, found through the per-expert
@@ -7,26 +8,31 @@
 // streams its fp16 page.  Decode batches route a few tokens to each expert, so
 // the time goes into streaming weights.
 //
-// Work item = (group, phase, 16-token chunk, block of four 16-row output
-// tiles); a group is a routed expert or the shared FFN.  A CTA of four warps
-// takes one item: the chunk's activations are staged once into shared memory
-// (K-blocks of 1024 columns, double-buffered, XOR-swizzled rows) and each
-// warp streams one tile's weights through its own cp.async ring, reading the
-// token fragments from the staged block with ldmatrix.  3-bit codes are
-// decoded with byte permutes from register LUTs; the fp16 weights feed
-// mma.sync m16n8k16 (weights as A, tokens as B, fp32 accumulation).  Gate/up
-// writes h = silu(g) * u in fp16, down writes y in fp32.
+// A CTA (four warps) takes one work item at a time and stages the item's
+// token rows once into shared memory (K-blocks of 768 columns,
+// double-buffered, rows XOR-swizzled for conflict-free ldmatrix).  Two item
+// shapes:
+//  - block item (3-bit experts, fp16 pages, shared FFN): (group, phase,
+//    16-token chunk, four 16-row tiles); each warp owns one tile and streams
+//    its weights through a private cp.async ring.  3-bit codes are decoded
+//    with byte permutes from register LUTs.
+//  - split item (4, 5, 6-bit experts): (group, phase, chunk, one tile); the
+//    four warps take interleaved 128-column pieces of the tile's reduction,
+//    look codes up in one CTA-wide LUT table (per-lane copies of the row pair
+//    g / g+8, so no bank conflicts) and add their partial sums in warp order.
+// The weights feed mma.sync m16n8k16 (weights as A, tokens as B, fp32
+// accumulation).  Gate/up writes h = silu(g) * u in fp16, down writes y in
+// fp32.
 //
-// CTAs claim items from one counter in a fixed order: every gate/up item
+// CTAs of a launch claim items from one counter in a fixed order: every gate/up item
 // (phase 0) before every down item (phase 1); inside a phase the shared FFN
-// first, then fp16 experts, then 3-bit experts (longest items first).  A down
-// item waits until all gate/up tiles of its (group, chunk) are done; those
-// items were claimed earlier by running CTAs and never wait, so every wait
-// ends.  The waits are bounded anyway: past the limit the kernel records a
-// timeout in the layer's error word and carries on.  The phase counters are
-// returned to zero by the last down block of each (group, chunk) and the
-// claim counter by the last CTA to leave, so the next launch (or graph
-// replay) starts from zero.
+// first, then fp16, 3-bit and 4..6-bit experts.  A down item waits until all
+// gate/up tiles of its (group, chunk) are done; those items were claimed
+// earlier by running CTAs and never wait, so every wait ends.  The waits are
+// bounded anyway: past the limit the kernel records a timeout in the layer's
+// error word and carries on.  The phase counters are returned to zero by the
+// last down tile of each (group, chunk) and the claim counter by the last CTA
+// to leave, so the next launch (or graph replay) starts from zero.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -37,24 +43,33 @@
 namespace pw {
 
 constexpr int kCtaThreads = 128;
-constexpr int kCtaWarps = kCtaThreads / 32;          // = tiles per item
+constexpr int kCtaWarps = kCtaThreads / 32;           // tiles of a block item
 constexpr int kCtaBlocksPerSm = 2;
-constexpr int kSlabCols = 1024;                      // columns of one staged K-block
-constexpr int kSlabRows = kTok;                      // token rows of the staged block
-constexpr int kSlabHalf = kSlabRows * kSlabCols * 2; // bytes of one K-block buffer
-constexpr int kRingBytes = 8 * 1024;                 // cp.async weight ring of one warp
-constexpr int kCtaSmem = 2 * kSlabHalf + kCtaWarps * kRingBytes;
-constexpr long long kSpinLimit = 1ll << 22;          // polls of a phase counter (about a second)
+constexpr int kSlabCols = 768;                        // columns of one staged K-block
+constexpr int kSlabRows = kTok;                       // token rows of a staged K-block
+constexpr int kSlabHalf = kSlabRows * kSlabCols * 2;  // bytes of one K-block buffer
+constexpr int kTabBytes = 64 * 256;                   // LUT table of a split item (b <= 6, two matrices)
+constexpr int kRingSplit = 10 * 1024;                 // cp.async weight ring of one warp (split items)
+constexpr int kRingBlock = 14 * 1024;                 // ... (block items: no LUT table to hold)
+constexpr int kCtaSmem = 2 * kSlabHalf + kCtaWarps * kRingBlock;
+static_assert(kTabBytes + kCtaWarps * kRingSplit <= kCtaWarps * kRingBlock, "split layout must fit");
+constexpr long long kSpinLimit = 1ll << 22;           // polls of a phase counter (about a second)
 
-// Weight units: one matrix of a plane group (4 chunks) of 3-bit words, or one
-// matrix of one fp16 chunk.  Ring depth = slots that fit the warp's ring; at
-// most one more than the units of a K-block (the staging of the next K-block
-// is then complete when its first unit is).
-constexpr int kSlot3 = 3 * 32 * 16;
-constexpr int kSlot16 = 4 * 32 * 16;
-constexpr int kRing3 = kRingBytes / kSlot3 < 5 ? kRingBytes / kSlot3 : 5;
-constexpr int kRing16 = kRingBytes / kSlot16;
-static_assert(kRing3 >= 2 && kRing16 >= 2, "ring too small");
+// Weight units streamed by a warp: one matrix of
+//   KIND_P3: a plane group (4 chunks, 256 columns) of 3-bit words, 16 B per lane and plane;
+//   KIND_F16: one fp16 chunk (64 columns), 4 x 16 B per lane;
+//   KIND_PB: half a plane group (2 chunks, 128 columns) of B-bit words, 8 B per lane and plane.
+enum { KIND_P3 = 0, KIND_F16 = 1, KIND_PB = 2 };
+
+template <int KIND, int B, int RB>
+struct Unit {
+  static constexpr int COLS = KIND == KIND_P3 ? 256 : KIND == KIND_F16 ? 64 : 128;
+  static constexpr int LANE_BYTES = KIND == KIND_P3 ? 3 * 16 : KIND == KIND_F16 ? 4 * 16 : B * 8;
+  static constexpr int SLOT = LANE_BYTES * 32;
+  static constexpr int R = RB / SLOT > 8 ? 8 : RB / SLOT;  // ring depth
+  static_assert(RB / SLOT >= 3, "ring too shallow");
+  static_assert(kSlabCols % COLS == 0, "units must not straddle K-blocks");
+};
 
 struct UniParams {
   DevLayer L;
@@ -62,7 +77,7 @@ struct UniParams {
   const __half* xp;    // [n_slots][d] routed input rows, or null (no routed groups)
   const int* offsets;  // [E+1] slot offsets of the experts
   int T;
-  int bit_mask;        // routed bitwidths taken: bit 0 -> 3 bits, bit 1 -> fp16 page
+  int bit_mask;        // routed bitwidths taken: bit 0 -> 3 bits, bit 1 -> fp16 page, bit 2 -> 4..6 bits
   int max_tokens;      // routed experts with more tokens are left to the tensor-core GEMM
   __half* h;           // [n_slots][f]
   __half* hs;          // [T][fs]
@@ -74,6 +89,30 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Wait until at most n (clamped to 7) of this thread's newest cp.async groups are pending.
+__device__ __forceinline__ void cp_wait_dyn(int n) {
+  switch (n < 7 ? n : 7) {
+    case 0: cp_wait<0>(); break;
+    case 1: cp_wait<1>(); break;
+    case 2: cp_wait<2>(); break;
+    case 3: cp_wait<3>(); break;
+    case 4: cp_wait<4>(); break;
+    case 5: cp_wait<5>(); break;
+    case 6: cp_wait<6>(); break;
+    default: cp_wait<7>(); break;
+  }
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -113,88 +152,216 @@ __device__ __forceinline__ void slab_bfrag(uint32_t buf, int kc, int NT, uint32_
   }
 }
 
-// Ring-slot wait at unit i, the K-block barrier and the staging of the next
-// K-block.  Returns the slab buffer of unit i's K-block.
-__device__ __forceinline__ uint32_t kblock_step(int i, int upb, int K, const __half* act, const int* s_tok,
-                                                int rows, uint32_t slab) {
-  const int kb = i / upb;
-  if (i % upb == 0) {
-    __syncthreads();  // everyone's copies of K-block kb landed; K-block kb-1 is no longer read
-    if (kb >= 1 && (kb + 1) * kSlabCols < K) {
-      stage_kblock(act, s_tok, rows, K, kb + 1, slab + ((kb + 1) & 1) * kSlabHalf);
-      cp_commit();
-    }
+// Decode mma step s of one chunk of B-bit codes into the A fragment through
+// the CTA's LUT table: entry (v, matrix m, lane) at byte v*256 + m*128 +
+// 4*lane holds LUT[row g][v] in its low and LUT[row g+8][v] in its high half
+// (g = lane / 4).  lbm = m*128 + 4*lane.  Plane masking as in decode_step_lut.
+template <int B>
+__device__ __forceinline__ void decode_step_tab(const uint32_t (&w)[B], const int s, uint32_t tab, uint32_t lbm,
+                                                uint32_t (&a)[4]) {
+  uint32_t R[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int p = 0; p < B; ++p) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
+    R[h] = rotr(m, 4 * h + s + 6 - B);
   }
-  return slab + (kb & 1) * kSlabHalf;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // k = 2 * rowsel + colhalf
+    const uint32_t sel = 0x5504u | ((uint32_t)k << 4);
+    const uint32_t e0 = lds32(tab + prmt(R[0], lbm, sel));
+    const uint32_t e1 = lds32(tab + prmt(R[1], lbm, sel));
+    const int reg = (k == 0) ? 0 : (k == 1) ? 2 : (k == 2) ? 1 : 3;
+    a[reg] = prmt(e0, e1, (k >> 1) ? 0x7632u : 0x5410u);
+  }
 }
 
-// K loop of one warp over 3-bit plane groups: unit u = (group u / NM, matrix u % NM).
+// LUT table of a split item: both matrices of tile tau at bitwidth B.
+template <int B, int NM>
+__device__ __forceinline__ void build_tab(const DevLayer& L, int e, int tau, unsigned char* tab) {
+  constexpr int V = 1 << B;
+  constexpr int RUNS = V / 8;  // 8-entry runs per LUT row
+  constexpr int UNITS = NM * 8 * RUNS;
+  for (int u = threadIdx.x; u < UNITS; u += kCtaThreads) {
+    const int mi = u / (8 * RUNS), g = (u / RUNS) % 8, v0 = (u % RUNS) * 8;
+    const __half* lr = lut_rows(L, e, NM == 2 ? mi : 2, B, tau * kTileRows);
+    const uint4 lo = *reinterpret_cast<const uint4*>(lr + g * V + v0);
+    const uint4 hi = *reinterpret_cast<const uint4*>(lr + (g + 8) * V + v0);
+    const uint32_t l4[4] = {lo.x, lo.y, lo.z, lo.w}, h4[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t pair = prmt(l4[i >> 1], h4[i >> 1], (i & 1) ? 0x7632u : 0x5410u);
+      *reinterpret_cast<uint4*>(tab + (v0 + i) * 256 + mi * 128 + g * 16) = make_uint4(pair, pair, pair, pair);
+    }
+  }
+}
+
+// Weight sources of one warp's K loop.
 template <int NM>
-__device__ __forceinline__ void cta_planes3(const char* const (&base)[NM][3], int K, int NT,
-                                            const uint32_t (&lut3)[NM][2][4], uint32_t ring, uint32_t slab,
-                                            const __half* act, const int* s_tok, int rows,
-                                            float (&acc)[NM][kNT][4]) {
-  constexpr int R = kRing3;
+struct WSrc {
+  const char* p[NM][6];  // plane tiles (KIND_P3 / KIND_PB) or the fp16 tile in p[m][0]
+  uint32_t lut3[NM][2][4];
+};
+
+// K loop of one warp: units u = u0, u0 + ustride, ... of one tile (unit u =
+// (column block u / NM, matrix u % NM)).  Every warp of the CTA runs it for
+// the same item and passes the same K-block barriers; the token rows of
+// K-block kb are staged at the start of K-block kb - 1.
+template <int KIND, int B, int NM, int RB>
+__device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0, int ustride, uint32_t ring,
+                                      uint32_t slab, uint32_t tab, const __half* act, const int* s_tok,
+                                      float (&acc)[NM][kNT][4]) {
+  using U = Unit<KIND, B, RB>;
+  constexpr int R = U::R;
   const int lane = threadIdx.x & 31;
-  const int nk = K / 64, G = nk / 4, rem = nk % 4, NG = G + (rem ? 1 : 0);
-  const int nu = NG * NM, upb = (kSlabCols / 256) * NM;
-  auto issue = [&](int u) {
-    const int gamma = u / NM, mi = u % NM;
-    const uint32_t slot = ring + (u % R) * kSlot3;
-    const char* bp[3];
+  const int rows = NT * 8;
+  const int nk = K / 64, G = nk / 4, rem = nk % 4;
+  const int ncb = (K + U::COLS - 1) / U::COLS;  // column blocks
+  const int nu = ncb * NM;
+  const int mine = u0 < nu ? (nu - u0 + ustride - 1) / ustride : 0;
+  const int kbs = (K + kSlabCols - 1) / kSlabCols;
+
+  auto issue = [&](int i) {
+    const int u = u0 + i * ustride, cb = u / NM, mi = u % NM;
+    const uint32_t slot = ring + (i % R) * U::SLOT;
+    const char* const* pp = (NM == 1 || mi == 0) ? src.p[0] : src.p[NM - 1];
+    if constexpr (KIND == KIND_F16) {
 #pragma unroll
-    for (int p = 0; p < 3; ++p) bp[p] = (NM == 1 || mi == 0) ? base[0][p] : base[NM - 1][p];
-    if (gamma < G) {
-      const size_t off = (size_t)(gamma * 128 + lane * 4) * 4;
+      for (int s = 0; s < 4; ++s)
+        cp_async16(slot + (s * 32 + lane) * 16, pp[0] + ((size_t)(cb * 4 + s) * 32 + lane) * 16);
+    } else if constexpr (KIND == KIND_P3) {
+      if (cb < G) {
+        const size_t off = (size_t)(cb * 128 + lane * 4) * 4;
 #pragma unroll
-      for (int p = 0; p < 3; ++p) cp_async16(slot + (p * 32 + lane) * 16, bp[p] + off);
+        for (int p = 0; p < 3; ++p) cp_async16(slot + (p * 32 + lane) * 16, pp[p] + off);
+      } else {
+        const size_t off = (size_t)(G * 128 + lane * rem) * 4;
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+          for (int k = 0; k < rem; ++k) cp_async4(slot + (p * 32 + lane) * 16 + 4 * k, pp[p] + off + 4 * k);
+      }
     } else {
-      const size_t off = (size_t)(G * 128 + lane * rem) * 4;
+      const int gamma = cb >> 1, j = cb & 1;
+      if (gamma < G) {
+        const size_t off = (size_t)(gamma * 128 + lane * 4 + 2 * j) * 4;
 #pragma unroll
-      for (int p = 0; p < 3; ++p)
-        for (int k = 0; k < rem; ++k) cp_async4(slot + (p * 32 + lane) * 16 + 4 * k, bp[p] + off + 4 * k);
+        for (int p = 0; p < B; ++p) cp_async8(slot + (p * 32 + lane) * 8, pp[p] + off);
+      } else {
+        const int cnt = min(2, rem - 2 * j);
+        const size_t off = (size_t)(G * 128 + lane * rem + 2 * j) * 4;
+#pragma unroll
+        for (int p = 0; p < B; ++p)
+          for (int k = 0; k < cnt; ++k) cp_async4(slot + (p * 32 + lane) * 8 + 4 * k, pp[p] + off + 4 * k);
+      }
     }
   };
+
+  // K-blocks 0 and 1 go with the first ring group
+  stage_kblock(act, s_tok, rows, K, 0, slab);
+  if (kbs > 1) stage_kblock(act, s_tok, rows, K, 1, slab + kSlabHalf);
+  int since_stage = 0;  // groups committed after the newest staging group
 #pragma unroll
   for (int i = 0; i < R - 1; ++i) {
-    if (i < nu) issue(i);
+    if (i < mine) issue(i);
     cp_commit();
+    if (i > 0) ++since_stage;
   }
-  for (int i = 0; i < nu; ++i) {
-    if (i + R - 1 < nu) issue(i + R - 1);
-    cp_commit();
-    cp_wait<R - 1>();
-    const uint32_t buf = kblock_step(i, upb, K, act, s_tok, rows, slab);
-    const int gamma = i / NM, mi = i % NM;
-    const uint32_t slot = ring + (i % R) * kSlot3;
-    uint32_t w[3][4];
-#pragma unroll
-    for (int p = 0; p < 3; ++p) {
-      const uint4 v = lds128(slot + (p * 32 + lane) * 16);
-      w[p][0] = v.x;
-      w[p][1] = v.y;
-      w[p][2] = v.z;
-      w[p][3] = v.w;
+  int kb_cur = -1;
+  auto advance_to = [&](int kb) {
+    while (kb_cur < kb) {
+      ++kb_cur;
+      cp_wait_dyn(since_stage);  // this thread's copies of K-block kb_cur have landed
+      __syncthreads();           // ... and everyone's; K-block kb_cur - 1 is no longer read
+      if (kb_cur >= 1 && kb_cur + 1 < kbs) {
+        stage_kblock(act, s_tok, rows, K, kb_cur + 1, slab + ((kb_cur + 1) & 1) * kSlabHalf);
+        cp_commit();
+        since_stage = 0;
+      }
     }
-    const int nch = gamma < G ? 4 : rem;
-    const int kc0 = (gamma % (kSlabCols / 256)) * 256;
-    // the matrix is fixed for the whole unit: branch once, then four fully
+  };
+
+#pragma unroll 1
+  for (int i = 0; i < mine; ++i) {
+    if (i + R - 1 < mine) issue(i + R - 1);
+    cp_commit();
+    ++since_stage;
+    const int u = u0 + i * ustride, cb = u / NM, mi = u % NM;
+    const int kb = (cb * U::COLS) / kSlabCols;
+    advance_to(kb);
+    cp_wait<R - 1>();  // unit i has landed
+    const uint32_t buf = slab + (kb & 1) * kSlabHalf;
+    const int kc0 = (cb * U::COLS) % kSlabCols;
+    const uint32_t slot = ring + (i % R) * U::SLOT;
+    // the matrix is fixed for the whole unit: branch once, then fully
     // unrolled chunks of independent decode + mma chains
     auto compute = [&](auto tag) {
       constexpr int m = decltype(tag)::value;
+      if constexpr (KIND == KIND_F16) {
+        uint32_t bf[kNT][4][2];
+        slab_bfrag(buf, kc0, NT, bf);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c < nch) {
-          uint32_t bf[kNT][4][2];
-          slab_bfrag(buf, kc0 + c * 64, NT, bf);
+        for (int s = 0; s < 4; ++s) {
+          const uint4 v = lds128(slot + (s * 32 + lane) * 16);
+          const uint32_t a[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int s = 0; s < 4; ++s) {
+          for (int nt = 0; nt < kNT; ++nt)
+            if (nt < NT) mma16816(acc[m][nt], a, bf[nt][s][0], bf[nt][s][1]);
+        }
+      } else if constexpr (KIND == KIND_P3) {
+        uint32_t w[3][4];
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+          const uint4 v = lds128(slot + (p * 32 + lane) * 16);
+          w[p][0] = v.x;
+          w[p][1] = v.y;
+          w[p][2] = v.z;
+          w[p][3] = v.w;
+        }
+        const int nch = cb < G ? 4 : rem;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c < nch) {
+            uint32_t bf[kNT][4][2];
+            slab_bfrag(buf, kc0 + c * 64, NT, bf);
+            // decode the chunk's four steps first (independent chains), then the mma's
             const uint32_t wc[3] = {w[0][c], w[1][c], w[2][c]};
-            uint32_t a[4];
-            decode_step_prmt3(wc, s, lut3[m], a);
+            uint32_t a[4][4];
 #pragma unroll
-            for (int nt = 0; nt < kNT; ++nt)
-              if (nt < NT) mma16816(acc[m][nt], a, bf[nt][s][0], bf[nt][s][1]);
+            for (int s = 0; s < 4; ++s) decode_step_prmt3(wc, s, src.lut3[m], a[s]);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+              for (int nt = 0; nt < kNT; ++nt)
+                if (nt < NT) mma16816(acc[m][nt], a[s], bf[nt][s][0], bf[nt][s][1]);
+          }
+        }
+      } else {
+        uint32_t w[B][2];
+#pragma unroll
+        for (int p = 0; p < B; ++p) {
+          const uint2 v = lds64(slot + (p * 32 + lane) * 8);
+          w[p][0] = v.x;
+          w[p][1] = v.y;
+        }
+        const int nch = (cb >> 1) < G ? 2 : min(2, rem - 2 * (cb & 1));
+        const uint32_t lbm = m * 128 + lane * 4;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (c < nch) {
+            uint32_t bf[kNT][4][2];
+            slab_bfrag(buf, kc0 + c * 64, NT, bf);
+            uint32_t wc[B];
+#pragma unroll
+            for (int p = 0; p < B; ++p) wc[p] = w[p][c];
+            uint32_t a[4][4];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) decode_step_tab<B>(wc, s, tab, lbm, a[s]);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+              for (int nt = 0; nt < kNT; ++nt)
+                if (nt < NT) mma16816(acc[m][nt], a[s], bf[nt][s][0], bf[nt][s][1]);
           }
         }
       }
@@ -202,53 +369,7 @@ __device__ __forceinline__ void cta_planes3(const char* const (&base)[NM][3], in
     if (NM == 1 || mi == 0) compute(std::integral_constant<int, 0>{});
     else compute(std::integral_constant<int, NM - 1>{});
   }
-  cp_wait<0>();
-}
-
-// K loop of one warp over fp16 chunks: unit u = (chunk u / NM, matrix u % NM).
-template <int NM>
-__device__ __forceinline__ void cta_f16(const char* const (&b16)[NM], int K, int NT, uint32_t ring, uint32_t slab,
-                                        const __half* act, const int* s_tok, int rows, float (&acc)[NM][kNT][4]) {
-  constexpr int R = kRing16;
-  const int lane = threadIdx.x & 31;
-  const int nk = K / 64;
-  const int nu = nk * NM, upb = (kSlabCols / 64) * NM;
-  auto issue = [&](int u) {
-    const int kappa = u / NM, mi = u % NM;
-    const uint32_t slot = ring + (u % R) * kSlot16;
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-      cp_async16(slot + (s * 32 + lane) * 16,
-                 ((NM == 1 || mi == 0) ? b16[0] : b16[NM - 1]) + ((size_t)(kappa * 4 + s) * 32 + lane) * 16);
-  };
-#pragma unroll
-  for (int i = 0; i < R - 1; ++i) {
-    if (i < nu) issue(i);
-    cp_commit();
-  }
-  uint32_t bf[kNT][4][2];
-  for (int i = 0; i < nu; ++i) {
-    if (i + R - 1 < nu) issue(i + R - 1);
-    cp_commit();
-    cp_wait<R - 1>();
-    const uint32_t buf = kblock_step(i, upb, K, act, s_tok, rows, slab);
-    const int kappa = i / NM, mi = i % NM;
-    if (mi == 0) slab_bfrag(buf, (kappa % (kSlabCols / 64)) * 64, NT, bf);
-    const uint32_t slot = ring + (i % R) * kSlot16;
-    auto compute = [&](auto tag) {
-      constexpr int m = decltype(tag)::value;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint4 v = lds128(slot + (s * 32 + lane) * 16);
-        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-          if (nt < NT) mma16816(acc[m][nt], a, bf[nt][s][0], bf[nt][s][1]);
-      }
-    };
-    if (NM == 1 || mi == 0) compute(std::integral_constant<int, 0>{});
-    else compute(std::integral_constant<int, NM - 1>{});
-  }
+  advance_to(kbs - 1);
   cp_wait<0>();
 }
 
@@ -272,46 +393,101 @@ __device__ __forceinline__ void tile_store(const float (&acc)[NM][kNT][4], int t
     }
 }
 
-// One warp's tile of an item.
+struct ItemArgs {
+  const __half* act;  // token rows of this phase
+  int e;              // expert (routed)
+  bool sh;            // shared FFN
+  int K, NT, row0, ntok, ld;
+  __half* h;
+  float* y;
+};
+
+// Block item: warp w computes tile tau0 + w over the whole reduction.
 template <int NM, int B>
-__device__ __forceinline__ void cta_tile(const DevLayer& L, const __half* act, int e, bool sh, int tau, int K,
-                                         int NT, int row0, int ntok, int ld, __half* h, float* y, uint32_t ring,
-                                         uint32_t slab, const int* s_tok) {
+__device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A, int tau, uint32_t ring,
+                                           uint32_t slab, const int* s_tok) {
   const int lane = threadIdx.x & 31;
-  const int rows = NT * 8;
   float acc[NM][kNT][4] = {};
-  if constexpr (B == 16) {
-    const char* b16[NM];
+  WSrc<NM> src;
 #pragma unroll
-    for (int mi = 0; mi < NM; ++mi) {
-      const int m = NM == 2 ? mi : 2;
-      b16[mi] = sh ? reinterpret_cast<const char*>(L.shared16[m]) + (size_t)tau * 32 * K
-                   : tile_addr(L, e, m, kPlanes, tau);
+  for (int mi = 0; mi < NM; ++mi) {
+    const int m = NM == 2 ? mi : 2;
+    if constexpr (B == 16) {
+      src.p[mi][0] = A.sh ? reinterpret_cast<const char*>(L.shared16[m]) + (size_t)tau * 32 * A.K
+                          : tile_addr(L, A.e, m, kPlanes, tau);
+    } else {
+#pragma unroll
+      for (int p = 0; p < 3; ++p) src.p[mi][p] = tile_addr(L, A.e, m, p, tau);
+      const __half* lr = lut_rows(L, A.e, m, 3, tau * kTileRows);
+      load_lut3(lr + (lane >> 2) * 8, src.lut3[mi][0]);
+      load_lut3(lr + ((lane >> 2) + 8) * 8, src.lut3[mi][1]);
     }
-    cta_f16<NM>(b16, K, NT, ring, slab, act, s_tok, rows, acc);
-  } else {
-    const char* base[NM][3];
-    uint32_t lut3[NM][2][4];
-#pragma unroll
-    for (int mi = 0; mi < NM; ++mi) {
-      const int m = NM == 2 ? mi : 2;
-#pragma unroll
-      for (int p = 0; p < 3; ++p) base[mi][p] = tile_addr(L, e, m, p, tau);
-      const __half* lr = lut_rows(L, e, m, 3, tau * kTileRows);
-      load_lut3(lr + (lane >> 2) * 8, lut3[mi][0]);
-      load_lut3(lr + ((lane >> 2) + 8) * 8, lut3[mi][1]);
-    }
-    cta_planes3<NM>(base, K, NT, lut3, ring, slab, act, s_tok, rows, acc);
   }
-  tile_store<NM>(acc, tau, row0, ntok, ld, h, y);
+  if constexpr (B == 16) kloop<KIND_F16, 16, NM, kRingBlock>(src, A.K, A.NT, 0, 1, ring, slab, 0u, A.act, s_tok, acc);
+  else kloop<KIND_P3, 3, NM, kRingBlock>(src, A.K, A.NT, 0, 1, ring, slab, 0u, A.act, s_tok, acc);
+  tile_store<NM>(acc, tau, A.row0, A.ntok, A.ld, A.h, A.y);
 }
 
-__global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_uni_kernel(UniParams P) {
+// Split item: the four warps share tile tau; partial sums are added in warp order.
+template <int NM, int B>
+__device__ __forceinline__ void split_item(const DevLayer& L, const ItemArgs& A, int tau, uint32_t ring,
+                                           uint32_t slab, unsigned char* tab_ptr, const int* s_tok) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  build_tab<B, NM>(L, A.e, tau, tab_ptr);  // ordered before use by the first K-block barrier
+  float acc[NM][kNT][4] = {};
+  WSrc<NM> src;
+#pragma unroll
+  for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+    for (int p = 0; p < 6; ++p) src.p[mi][p] = p < B ? tile_addr(L, A.e, NM == 2 ? mi : 2, p, tau) : nullptr;
+  kloop<KIND_PB, B, NM, kRingSplit>(src, A.K, A.NT, warp, kCtaWarps, ring, slab, smem_u32(tab_ptr), A.act, s_tok,
+                                    acc);
+  __syncthreads();  // the staged rows are no longer read: reuse them for the partial sums
+  float4* red = reinterpret_cast<float4*>(__cvta_shared_to_generic(slab));
+#pragma unroll
+  for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+      red[((warp * NM + mi) * kNT + nt) * 32 + lane] =
+          make_float4(acc[mi][nt][0], acc[mi][nt][1], acc[mi][nt][2], acc[mi][nt][3]);
+  __syncthreads();
+  if (warp == 0) {
+    float sum[NM][kNT][4];
+#pragma unroll
+    for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        float4 v = red[(mi * kNT + nt) * 32 + lane];
+#pragma unroll
+        for (int w = 1; w < kCtaWarps; ++w) {
+          const float4 o = red[((w * NM + mi) * kNT + nt) * 32 + lane];
+          v.x += o.x;
+          v.y += o.y;
+          v.z += o.z;
+          v.w += o.w;
+        }
+        sum[mi][nt][0] = v.x;
+        sum[mi][nt][1] = v.y;
+        sum[mi][nt][2] = v.z;
+        sum[mi][nt][3] = v.w;
+      }
+    tile_store<NM>(sum, tau, A.row0, A.ntok, A.ld, A.h, A.y);
+  }
+}
+
+__device__ __forceinline__ bool is_split(int b) { return b >= 4 && b <= 6; }
+
+// SPLIT = false: block items (3-bit and fp16 experts, shared FFN); SPLIT = true:
+// split items (4, 5, 6-bit experts).  Two instantiations keep each set of
+// paths in its own register allocation; their groups are disjoint, so they
+// share the layer's phase counters and use separate claim counters.
+template <bool SPLIT>
+__global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(UniParams P) {
   extern __shared__ __align__(128) unsigned char smem_uni[];
-  __shared__ int s_base[kMaxExperts + 1];  // first input row of each group
-  __shared__ int s_n[kMaxExperts + 1];     // tokens of each group
-  __shared__ short s_b[kMaxExperts + 1];   // bitwidth of each group
-  __shared__ short s_ord[kMaxExperts + 1]; // groups in claim order
+  __shared__ int s_base[kMaxExperts + 1];   // first input row of each group
+  __shared__ int s_n[kMaxExperts + 1];      // tokens of each group
+  __shared__ short s_b[kMaxExperts + 1];    // bitwidth of each group
+  __shared__ short s_ord[kMaxExperts + 1];  // groups in claim order
   __shared__ int s_pref[2][kMaxExperts + 2];
   __shared__ int s_ng, s_it;
   __shared__ int s_tok[kSlabRows];
@@ -319,9 +495,9 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_uni_kernel(U
   const DevLayer& L = P.L;
   const int E = L.E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int* const q = L.sync;                              // claim counter, CTA exit counter
-  int* const done0 = L.sync + kSyncHeader;            // [E+1][kSyncChunks] gate/up tile blocks done
-  int* const done1 = done0 + (E + 1) * kSyncChunks;   // [E+1][kSyncChunks] down tile blocks done
+  int* const q = L.sync + (SPLIT ? 2 : 0);           // claim counter, CTA exit counter
+  int* const done0 = L.sync + kSyncHeader;           // [E+1][kSyncChunks] gate/up tiles done
+  int* const done1 = done0 + (E + 1) * kSyncChunks;  // [E+1][kSyncChunks] down tiles done
 
   for (int g = tid; g <= E; g += kCtaThreads) {
     int base = 0, n = 0, b = 16;
@@ -330,10 +506,11 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_uni_kernel(U
         base = P.offsets[g];
         n = P.offsets[g + 1] - base;
         b = L.bits[g];
-        const bool take = (b == 3 && (P.bit_mask & 1)) || (b == 16 && (P.bit_mask & 2));
+        const bool take = SPLIT ? is_split(b) && (P.bit_mask & 4)
+                                : (b == 3 && (P.bit_mask & 1)) || (b == 16 && (P.bit_mask & 2));
         if (!take || n > P.max_tokens) n = 0;
       }
-    } else if (P.x) {
+    } else if (P.x && !SPLIT) {
       n = P.T;
     }
     s_base[g] = base;
@@ -342,13 +519,16 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_uni_kernel(U
   }
   __syncthreads();
   if (warp == 0) {
-    // claim order: shared FFN, fp16 experts, 3-bit experts
+    // claim order: shared FFN, fp16 experts, 3-bit experts, 4..6-bit experts
     int ng = 0;
-    for (int pass = 0; pass < 3; ++pass) {
+    for (int pass = 0; pass < 4; ++pass) {
       for (int g0 = 0; g0 <= E; g0 += 32) {
         const int g = g0 + lane;
         bool in = false;
-        if (g <= E && s_n[g] > 0) in = pass == 0 ? g == E : pass == 1 ? (g < E && s_b[g] == 16) : s_b[g] == 3;
+        if (g <= E && s_n[g] > 0) {
+          const int b = s_b[g];
+          in = pass == 0 ? g == E : g == E ? false : pass == 1 ? b == 16 : pass == 2 ? b == 3 : is_split(b);
+        }
         const unsigned m = __ballot_sync(0xffffffffu, in);
         if (in) s_ord[ng + __popc(m & ((1u << lane) - 1))] = (short)g;
         ng += __popc(m);
@@ -363,7 +543,8 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_uni_kernel(U
           const int g = s_ord[k];
           const int fe = g == E ? L.fs : L.f;
           const int tiles = ph == 0 ? fe / kTileRows : L.d / kTileRows;
-          c = ((s_n[g] + kTok - 1) / kTok) * (tiles / kCtaWarps);
+          const int per_chunk = SPLIT ? tiles : tiles / kCtaWarps;
+          c = ((s_n[g] + kTok - 1) / kTok) * per_chunk;
         }
         int incl = c;
 #pragma unroll
@@ -379,11 +560,13 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_uni_kernel(U
     if (lane == 0) s_ng = ng;
   }
   const uint32_t slab = smem_u32(smem_uni);
-  const uint32_t ring = slab + 2 * kSlabHalf + warp * kRingBytes;
+  unsigned char* const tab_ptr = smem_uni + 2 * kSlabHalf;  // split items only
+  const uint32_t ring = SPLIT ? slab + 2 * kSlabHalf + kTabBytes + warp * kRingSplit
+                              : slab + 2 * kSlabHalf + warp * kRingBlock;
 
   for (;;) {
     if (tid == 0) s_it = atomicAdd(q, 1);
-    __syncthreads();  // also: the previous item no longer reads the slab or s_tok
+    __syncthreads();  // also: the previous item no longer reads shared memory
     const int ng = s_ng;
     const int total0 = s_pref[0][ng];
     const int it = s_it;
@@ -398,24 +581,30 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_uni_kernel(U
     }
     const int g = s_ord[lo];
     const bool sh = g == E;
+    const int b = s_b[g];
     const int n = s_n[g];
     const int nch = (n + kTok - 1) / kTok;
     const int local = li - pref[lo];
-    const int blk = local / nch, chunk = local % nch;  // chunks of one tile block are claimed together
-    const int row0 = s_base[g] + chunk * kTok;
-    const int ntok = min(kTok, n - chunk * kTok);
-    const int NT = (ntok + 7) >> 3;
+    const int blk = local / nch, chunk = local % nch;  // chunks of one tile (block) are claimed together
     const int fe = sh ? L.fs : L.f;
-    const int K = phase == 0 ? L.d : fe;
     const int tiles = phase == 0 ? fe / kTileRows : L.d / kTileRows;
-    const int b = s_b[g];
     const int sidx = g * kSyncChunks + chunk;
-    const int tau = blk * kCtaWarps + warp;
-    const __half* act = phase == 0 ? (sh ? P.x : P.xp) : (sh ? P.hs : P.h);
 
-    if (tid < kSlabRows) s_tok[tid] = row0 + min(tid, ntok - 1);
+    ItemArgs A;
+    A.e = g;
+    A.sh = sh;
+    A.row0 = s_base[g] + chunk * kTok;
+    A.ntok = min(kTok, n - chunk * kTok);
+    A.NT = (A.ntok + 7) >> 3;
+    A.K = phase == 0 ? L.d : fe;
+    A.act = phase == 0 ? (sh ? P.x : P.xp) : (sh ? P.hs : P.h);
+    A.ld = phase == 0 ? fe : L.d;
+    A.h = sh ? P.hs : P.h;
+    A.y = sh ? P.ys : P.y;
+
+    if (tid < kSlabRows) s_tok[tid] = A.row0 + min(tid, A.ntok - 1);
     if (phase == 1 && tid == 0) {  // h of this chunk must be complete
-      const int need = fe / kTileRows / kCtaWarps;
+      const int need = fe / kTileRows;
       long long spins = 0;
       while (ld_acquire(done0 + sidx) < need) {
         if (++spins > kSpinLimit) {
@@ -426,24 +615,39 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_uni_kernel(U
       }
     }
     __syncthreads();
-    stage_kblock(act, s_tok, NT * 8, K, 0, slab);
-    if (K > kSlabCols) stage_kblock(act, s_tok, NT * 8, K, 1, slab + kSlabHalf);
-    if (phase == 0) {
-      __half* ho = sh ? P.hs : P.h;
-      if (b == 16) cta_tile<2, 16>(L, act, g, sh, tau, K, NT, row0, ntok, fe, ho, nullptr, ring, slab, s_tok);
-      else cta_tile<2, 3>(L, act, g, sh, tau, K, NT, row0, ntok, fe, ho, nullptr, ring, slab, s_tok);
+    if constexpr (SPLIT) {
+      const int tau = blk;
+      if (phase == 0) {
+        switch (b) {
+          case 4: split_item<2, 4>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
+          case 5: split_item<2, 5>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
+          default: split_item<2, 6>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
+        }
+      } else {
+        switch (b) {
+          case 4: split_item<1, 4>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
+          case 5: split_item<1, 5>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
+          default: split_item<1, 6>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
+        }
+      }
     } else {
-      float* yo = sh ? P.ys : P.y;
-      if (b == 16) cta_tile<1, 16>(L, act, g, sh, tau, K, NT, row0, ntok, L.d, nullptr, yo, ring, slab, s_tok);
-      else cta_tile<1, 3>(L, act, g, sh, tau, K, NT, row0, ntok, L.d, nullptr, yo, ring, slab, s_tok);
+      const int tau = blk * kCtaWarps + warp;
+      if (phase == 0) {
+        if (b == 16) block_item<2, 16>(L, A, tau, ring, slab, s_tok);
+        else block_item<2, 3>(L, A, tau, ring, slab, s_tok);
+      } else {
+        if (b == 16) block_item<1, 16>(L, A, tau, ring, slab, s_tok);
+        else block_item<1, 3>(L, A, tau, ring, slab, s_tok);
+      }
     }
-    __syncthreads();  // every tile of the block is stored
+    __syncthreads();  // every tile of the item is stored
     if (tid == 0) {
+      const int done_tiles = SPLIT ? 1 : kCtaWarps;
       __threadfence();
       if (phase == 0) {
-        atomicAdd(done0 + sidx, 1);
-      } else if (atomicAdd(done1 + sidx, 1) == tiles / kCtaWarps - 1) {
-        // the last down block of this (group, chunk) clears both counters
+        atomicAdd(done0 + sidx, done_tiles);
+      } else if (atomicAdd(done1 + sidx, done_tiles) == tiles - done_tiles) {
+        // the last down tiles of this (group, chunk) clear both counters
         atomicExch(done0 + sidx, 0);
         atomicExch(done1 + sidx, 0);
       }
@@ -463,8 +667,6 @@ cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm,
                        int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s) {
   if (max_tokens > kSyncChunks * kTok) return cudaErrorInvalidValue;
   if (x && T > kSyncChunks * kTok) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_smem((const void*)ffn_uni_kernel, kCtaSmem);
-  if (e != cudaSuccess) return e;
   UniParams P;
   P.L = L;
   P.x = x;
@@ -477,8 +679,21 @@ cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm,
   P.hs = hs;
   P.y = y;
   P.ys = ys;
-  ffn_uni_kernel<<<sm_count() * kCtaBlocksPerSm, kCtaThreads, kCtaSmem, s>>>(P);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (bit_mask & 4) {
+    e = ensure_smem((const void*)ffn_cta_kernel<true>, kCtaSmem);
+    if (e != cudaSuccess) return e;
+    ffn_cta_kernel<true><<<sm_count() * kCtaBlocksPerSm, kCtaThreads, kCtaSmem, s>>>(P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if ((bit_mask & 3) || x) {
+    e = ensure_smem((const void*)ffn_cta_kernel<false>, kCtaSmem);
+    if (e != cudaSuccess) return e;
+    ffn_cta_kernel<false><<<sm_count() * kCtaBlocksPerSm, kCtaThreads, kCtaSmem, s>>>(P);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace pw

@@ -14,7 +14,7 @@ constexpr int kMaxTopK = 8;
 constexpr int kPlanes = 6;           // planes of the 6-bit parent code
 constexpr int kTileRows = 16;        // rows per stored tile
 constexpr int kChunkCols = 64;       // columns per stored chunk
-constexpr int kSyncHeader = 32;      // claim and exit counters of the persistent decode kernel
+constexpr int kSyncHeader = 32;      // claim and exit counters of the persistent decode kernels
 constexpr int kSyncChunks = 64;      // 16-token chunks per group tracked by its phase counters
 
 // Words of a layer's sync area: header, then gate/up and down tile counters
@@ -64,11 +64,13 @@ cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __hal
 cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* offsets, int n_slots, float* y_perm,
                            __half* h, const __half* x_sh, int T, float* y_sh, __half* hs, int class_mask,
                            cudaStream_t s);
-// Persistent decode kernel for routed 3-bit / fp16 experts (bit_mask bits 0 / 1)
-// with at most max_tokens tokens and, when x is non-null, the shared FFN.
+// Persistent decode kernels for routed 3-bit / fp16 / 4..6-bit experts
+// (bit_mask bits 0 / 1 / 2) with at most max_tokens tokens and, when x is
+// non-null, the shared FFN.
 cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
                        int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s);
 int decode_max_tokens();
+int decode_max_tokens_shared();
 cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
                            int n_slots, int min_tokens, __half* h, float* y, cudaStream_t s);
 cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* inv_slot,

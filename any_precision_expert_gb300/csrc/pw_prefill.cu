@@ -418,13 +418,18 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
 }
 
 
-int decode_max_tokens() {
-  // experts with more tokens than this use the tensor-core GEMM (read per call)
-  const char* s = getenv("PW_DECODE_MAX_TOK");
-  const int v = s ? atoi(s) : 256;
-  // the persistent decode kernel tracks at most kSyncChunks chunks of kTok tokens per expert
+static int env_tokens(const char* name, int dflt) {
+  const char* s = getenv(name);
+  const int v = s ? atoi(s) : dflt;
+  // the persistent decode kernels track at most kSyncChunks chunks of 16 tokens per group
   return v < 0 ? 0 : v > kSyncChunks * 16 ? kSyncChunks * 16 : v;
 }
+
+// Routed experts with more tokens than this use the tensor-core GEMM (read per call).
+int decode_max_tokens() { return env_tokens("PW_DECODE_MAX_TOK", 64); }
+
+// The shared FFN (every token of the batch) uses the tensor-core GEMM above this batch size.
+int decode_max_tokens_shared() { return env_tokens("PW_DECODE_MAX_TOK_SHARED", 256); }
 
 namespace {
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

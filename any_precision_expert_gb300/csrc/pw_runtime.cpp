@@ -63,6 +63,16 @@ pw_status dev_h2d(void* dst, const void* src, size_t n, cudaStream_t s) {
   return PW_OK;
 }
 
+pw_status dev_d2d(void* dst, const void* src, size_t n, cudaStream_t s) {
+  if (n == 0) return PW_OK;
+  if (g_sim) {
+    memcpy(dst, src, n);
+    return PW_OK;
+  }
+  PW_CUDA(cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToDevice, s));
+  return PW_OK;
+}
+
 pw_status dev_zero(void* dst, size_t n, cudaStream_t s) {
   if (n == 0) return PW_OK;
   if (g_sim) {
@@ -333,6 +343,37 @@ pw_status upload_block(pw_layer_t l, const Block& b, const std::vector<char>& im
   return PW_OK;
 }
 
+// Pages for the blocks an expert at `bits` reads: np plane blocks, plus the
+// fp16 block at 16 bits (pages[np]).  All or nothing.
+pw_status take_expert_pages(pw_layer_t l, int bits, std::vector<std::vector<int>>* pages) {
+  pw_pool_s* pool = l->pool;
+  const int np = bits == 16 ? kPlanes : bits;
+  pages->assign(np + 1, {});
+  auto give_back = [&](int upto) {
+    for (int q = 0; q < upto; ++q)
+      for (int pg : (*pages)[q]) {
+        pool->kind[pg] = 0;
+        pool->free_pages.insert(pg);
+        pool->mapped_pages--;
+      }
+  };
+  for (int p = 0; p < np; ++p) {
+    pw_status st = pool->take_pages(l->pmax, &(*pages)[p]);
+    if (st != PW_OK) {
+      give_back(p);
+      return st;
+    }
+  }
+  if (bits == 16) {
+    pw_status st = pool->take_pages(l->pmax16, &(*pages)[np]);
+    if (st != PW_OK) {
+      give_back(np);
+      return st;
+    }
+  }
+  return PW_OK;
+}
+
 void release_expert(pw_layer_t l, int e) {
   for (int p = 0; p < kPlanes; ++p) l->pool->release(l->plane(e, p));
   l->pool->release(l->f16[e]);
@@ -539,31 +580,8 @@ extern "C" pw_status pw_layer_load_expert(pw_layer_t l, int e, int bits, const u
   release_expert(l, e);
 
   const int np = bits == 16 ? kPlanes : bits;
-  std::vector<std::vector<int>> pages(np + 1);
-  for (int p = 0; p < np; ++p) {
-    pw_status st = pool->take_pages(l->pmax, &pages[p]);
-    if (st != PW_OK) {
-      for (int q = 0; q < p; ++q)
-        for (int pg : pages[q]) {
-          pool->kind[pg] = 0;
-          pool->free_pages.insert(pg);
-          pool->mapped_pages--;
-        }
-      return st;
-    }
-  }
-  if (bits == 16) {
-    pw_status st = pool->take_pages(l->pmax16, &pages[np]);
-    if (st != PW_OK) {
-      for (int q = 0; q < np; ++q)
-        for (int pg : pages[q]) {
-          pool->kind[pg] = 0;
-          pool->free_pages.insert(pg);
-          pool->mapped_pages--;
-        }
-      return st;
-    }
-  }
+  std::vector<std::vector<int>> pages;
+  PW_TRY(take_expert_pages(l, bits, &pages));
 
   // pack and upload planes
   const size_t pb = pool->page_bytes;
@@ -616,6 +634,60 @@ extern "C" pw_status pw_layer_load_expert(pw_layer_t l, int e, int bits, const u
   for (int m = 0; m < 3; ++m)
     for (int i = 0; i < 4; ++i)
       PW_TRY(dev_h2d(lb + l->lut_off[m][i], lut[m][i], (size_t)l->R[m] * (1u << (i + 3)) * 2, s));
+  PW_TRY(upload_pt_rows(l, e, s));
+  PW_TRY(write_bits(l, e, bits, s));
+  PW_TRY(dev_sync(s));
+  l->bits[e] = bits;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_layer_copy_expert(pw_layer_t l, int e, pw_layer_t src, int e_src, int bits,
+                                          void* stream) {
+  PW_TRY(check_layer(l));
+  PW_TRY(check_layer(src));
+  if (e < 0 || e >= l->desc.n_experts || e_src < 0 || e_src >= src->desc.n_experts || !valid_bits(bits))
+    return PW_ERR_INVALID_ARG;
+  if (l == src && e == e_src) return PW_ERR_INVALID_ARG;
+  if (l->desc.d != src->desc.d || l->desc.ffn != src->desc.ffn || l->pool->page_bytes != src->pool->page_bytes)
+    return PW_ERR_INVALID_ARG;
+  if (src->bits[e_src] == 0) return PW_ERR_INVALID_ARG;
+  const int np = bits == 16 ? kPlanes : bits;
+  // only blocks the source reads at its current bitwidth: reclaimable ones
+  // could be handed to the copy itself
+  for (int p = 0; p < np; ++p)
+    if (src->plane(e_src, p).st != B_MAPPED) return PW_ERR_NOT_RESIDENT;
+  if (bits == 16 && src->f16[e_src].st != B_MAPPED) return PW_ERR_NOT_RESIDENT;
+
+  cudaStream_t s = as_stream(stream);
+  PW_TRY(dev_sync(s));  // kernels still reading the old pages must finish before they are reused
+  release_expert(l, e);
+  std::vector<std::vector<int>> pages;
+  PW_TRY(take_expert_pages(l, bits, &pages));
+  const size_t pb = l->pool->page_bytes;
+  // same shapes give the same tile maps: copy page by page
+  for (int p = 0; p < np; ++p) {
+    Block& b = l->plane(e, p);
+    const Block& sb = src->plane(e_src, p);
+    b.pages = pages[p];
+    b.st = B_MAPPED;
+    for (int v = 0; v < l->pmax; ++v) {
+      PW_TRY(dev_d2d(l->pool->page_addr(b.pages[v]), src->pool->page_addr(sb.pages[v]), pb, s));
+      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] =
+          reinterpret_cast<unsigned long long>(l->pool->page_addr(b.pages[v]));
+    }
+  }
+  if (bits == 16) {
+    Block& b = l->f16[e];
+    const Block& sb = src->f16[e_src];
+    b.pages = pages[np];
+    b.st = B_MAPPED;
+    for (int v = 0; v < l->pmax16; ++v) {
+      PW_TRY(dev_d2d(l->pool->page_addr(b.pages[v]), src->pool->page_addr(sb.pages[v]), pb, s));
+      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(l->pool->page_addr(b.pages[v]));
+    }
+  }
+  PW_TRY(dev_d2d(l->d_luts + (size_t)e * l->lut_block_bytes, src->d_luts + (size_t)e_src * src->lut_block_bytes,
+                 l->lut_block_bytes, s));
   PW_TRY(upload_pt_rows(l, e, s));
   PW_TRY(write_bits(l, e, bits, s));
   PW_TRY(dev_sync(s));

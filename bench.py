@@ -36,6 +36,9 @@ WORKLOADS = {
     "mixtral": ("mixtral-8x7b-shaped layer (d=4096, 8 experts ffn 14336 top-2, bitwidths 6/5/4/3 cycled)", 4096, 2),
     "e128": ("128-expert layer (d=2816, ffn 704, top-8, Zipf(1.2) bias, 45@3 45@4 30@6 8@16 bits)", 8192, 2),
     "tiny": ("tiny layer (d=512, 8 experts ffn 1024 top-2, mixed 3/4/5/6/16 bits)", 16, 8),
+    "sweep": ("32-layer mixtral-8x7b-shaped decode step (d=4096, 8 experts ffn 14336 top-2 per layer, "
+              "bits [6,5,4,3,16][(e+l) mod 5], 2 MiB plane pages; every step a seeded 25% of the "
+              "(layer, expert) pairs get a new bitwidth by page-table unmap / remap)", 64, 1),
 }
 
 
@@ -415,22 +418,243 @@ def run_gpu(args):
 
 def _launches_per_step(cfg, bits, T):
     """Kernels one step launches: router, permutation (histogram + scatter for
-    more than 1024 slots, or one fused kernel), row gather, the 4/5/6-bit decode
-    kernel pair (when such planes are resident), the persistent decode kernel
-    (3-bit / fp16 experts and the shared FFN), the tcgen05 GEMM pair for experts
-    (and a shared FFN) above the token threshold, and the combine."""
-    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "256")), 1024)
+    more than 1024 slots, or one fused kernel), row gather, the persistent
+    decode kernel for 4/5/6-bit experts (when such planes are resident) and the
+    one for 3-bit / fp16 experts and the shared FFN, the tcgen05 GEMM pair for
+    experts above the token threshold and for a shared FFN above its own, and
+    the combine."""
+    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "64")), 1024)
+    thr_s = min(int(os.environ.get("PW_DECODE_MAX_TOK_SHARED", "256")), 1024)
     S = T * cfg.K
     n = 1 + (2 if S > 1024 else 1) + 1
     if any(b in (4, 5, 6, 16) for b in np.asarray(bits).tolist()):
-        n += 2  # planes 3..5 are resident for 4..6-bit and fp16 experts
-    big = T > thr
-    n += 1  # persistent decode kernel
-    if big:
+        n += 1  # planes 3..5 are resident for 4..6-bit and fp16 experts
+    n += 1
+    if T > thr:
         n += 2
-        if cfg.shared_ffn:
-            n += 2
+    if cfg.shared_ffn and T > thr_s:
+        n += 2
     return n + 1
+
+
+# ---------------------------------------------------------------------------
+# 32-layer decode sweep with bitwidth changes between steps
+# ---------------------------------------------------------------------------
+
+def _expert_pages(cfg, b, page):
+    plane = 3 * cfg.d * cfg.f // 8
+    n = (6 if b == 16 else b) * (plane // page + 3)
+    if b == 16:
+        n += 3 * cfg.d * cfg.f * 2 // page + 4
+    return n
+
+
+def build_sweep(T, seed=0, device="cuda"):
+    """32 layers built from one uploaded set of experts: a source layer holds the
+    8 synthetic experts at 16 bits (six planes + fp16 page) and every layer gets
+    device copies of them at its initial bitwidths (distinct pages, so each
+    layer streams its own bytes); routers and inputs differ per layer."""
+    import torch
+
+    import any_precision_expert_gb300 as pw
+    from synth import bits_plan, get_config, make_expert, make_router, make_tokens
+
+    cfg = get_config("sweep")
+    page = 2 << 20
+    n_layers = cfg.n_layers
+    init = [bits_plan(cfg, seed, layer=l) for l in range(n_layers)]
+    lut = cfg.E * (2 * cfg.f + cfg.d) * 240
+    pages = cfg.E * _expert_pages(cfg, 16, page)
+    for l in range(n_layers):
+        pages += sum(_expert_pages(cfg, int(b), page) for b in init[l])
+    nbytes = pages * page + (n_layers + 1) * (lut + 4 * page) + (256 << 20)
+    pool = pw.Pool(nbytes, page_bytes=page, device=device)
+    src = pw.Layer(pool, cfg.d, cfg.f, cfg.E, cfg.K, cfg.renormalize, 0)
+    experts = []
+    for e in range(cfg.E):
+        ex = make_expert(cfg, e, seed, layer=0, with_w16=True)
+        src.load_expert(e, 16, ex["code6"], ex["lut"], ex["w16"])
+        experts.append({"code6": ex["code6"], "lut": ex["lut"], "w16": ex["w16"]})
+    layers, wr, bias, xs = [], [], [], []
+    for l in range(n_layers):
+        L = pw.Layer(pool, cfg.d, cfg.f, cfg.E, cfg.K, cfg.renormalize, 0)
+        for e in range(cfg.E):
+            L.copy_expert(e, src, e, int(init[l][e]))
+        layers.append(L)
+        w, bb = make_router(cfg, seed, layer=l)
+        wr.append(w)
+        bias.append(bb)
+        xs.append(make_tokens(cfg, T, seed, layer=l))
+    return dict(cfg=cfg, pool=pool, src=src, layers=layers, init=init, experts=experts, wr=wr, bias=bias, xs=xs,
+                wr_d=[torch.from_numpy(w).to(device) for w in wr],
+                bias_d=[torch.from_numpy(b).to(device) if b is not None else None for b in bias],
+                xs_d=[torch.from_numpy(x).to(device) for x in xs],
+                bufs=[pw.Buffers(L, T, device=device) for L in layers], T=T)
+
+
+def run_sweep(args):
+    import torch
+    import torch.distributed as dist
+
+    import any_precision_expert_gb300 as pw
+    from synth.workloads import sweep_changes
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if ws == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    T, K, W = args.tokens, args.steps, args.warmup
+    sw = build_sweep(T)
+    cfg, layers, bufs = sw["cfg"], sw["layers"], sw["bufs"]
+    NL = len(layers)
+    stream = torch.cuda.Stream()
+
+    def forward_all():
+        for l in range(NL):
+            pw.moe_forward(layers[l], sw["xs_d"][l], sw["wr_d"][l], sw["bias_d"][l], bufs[l], stream=stream)
+
+    cur = [b.copy() for b in sw["init"]]
+    plan = [sweep_changes(cfg, i, sw["init"]) for i in range(W + K)]
+
+    def apply(i):
+        for l, e, b in plan[i]:
+            layers[l].set_expert_bitwidth(e, b, stream=stream)
+            cur[l][e] = b
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            apply(i)
+            forward_all()
+    torch.cuda.synchronize()
+    active = [np.diff(bufs[l].offsets.cpu().numpy()) > 0 for l in range(NL)]  # routing is fixed per layer
+
+    def step_bytes():
+        tot = 0
+        for l in range(NL):
+            for e in range(cfg.E):
+                if active[l][e]:
+                    b = int(cur[l][e])
+                    tot += 3 * cfg.d * cfg.f * 2 if b == 16 else 3 * cfg.d * cfg.f * b // 8 + (2 * cfg.f + cfg.d) * (1 << b) * 2
+            tot += cfg.d * cfg.E * 2 + 2 * T * cfg.d * 2
+        return tot
+
+    # the 32 layers run as one CUDA graph; it reads bitwidths and page tables
+    # from device memory, so the changes made between replays take effect
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        forward_all()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak:
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+    byts = []
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(W, W + K):
+            apply(i)
+            byts.append(step_bytes())
+            g.replay()
+        t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1))
+    ok = all(L.check_device() == 0 for L in layers)
+
+    # end to end: host inputs in, host outputs back, every layer, every step
+    x_host = [torch.from_numpy(x).pin_memory() for x in sw["xs"]]
+    y_host = [torch.empty((T, cfg.d), dtype=torch.float16).pin_memory() for _ in range(NL)]
+    x_dev = [torch.empty((T, cfg.d), dtype=torch.float16, device="cuda") for _ in range(NL)]
+    KE = min(K, args.e2e_steps)
+    barrier()
+    te = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(KE):
+            for l in range(NL):
+                x_dev[l].copy_(x_host[l], non_blocking=True)
+                y = pw.moe_forward(layers[l], x_dev[l], sw["wr_d"][l], sw["bias_d"][l], bufs[l], stream=stream)
+                y_host[l].copy_(y, non_blocking=True)
+            stream.synchronize()
+    barrier()
+    e2e_s = max_over_ranks(time.perf_counter() - te)
+
+    peaks = _load_json(os.path.join(ROOT, "MEASURED_PEAKS.json"))
+    if peaks and peaks.get("hbm_gbs"):
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    else:
+        peak, peak_src = 6800.0, "fallback 6.8 TB/s"
+    avg_bytes = sum(byts) / len(byts)
+    gbs = avg_bytes / (ms / K * 1e-3) / 1e9
+    out = None
+    if rank == 0:
+        cpu = sweep_cpu_baseline(sw, args.cpu_seconds) if (ws == 1 and args.cpu_seconds > 0) else None
+        out = {
+            "metric": METRIC, "value": ws * T * K / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws, "steps": K,
+            "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"{WORKLOADS['sweep'][0]}, {T} tokens per step through all {NL} layers",
+                       "tokens_per_step": T, "layers": NL,
+                       "bitwidth_changes_per_step": len(plan[W]),
+                       "l2": f"inputs larger than L2: {avg_bytes / 1e6:.0f} MB of weights streamed per step",
+                       "timing": "bitwidth calls (host page lists + one stream-ordered 4-byte write each) and "
+                                 "one CUDA graph of the 32 layers per step, inside CUDA events on the stream",
+                       "step_algorithmic_bytes": avg_bytes, "parallelism": "replicas" if ws > 1 else "single GPU",
+                       "device_errors": not ok},
+            "roofline": {"kernel": "32-layer decode step (per layer: router, permutation, persistent FFN, combine)",
+                         "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_ms": ms / K,
+                         "peak_source": peak_src},
+            "cpu_baseline": cpu,
+            "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": NL * T * cfg.d * 2,
+                    "d2h_bytes_per_step": NL * T * cfg.d * 2, "steps": KE,
+                    "note": "public API (moe_forward) per layer: pinned H2D of x, layer, D2H of y; host sync per step"},
+            "gpu_launches": (NL * _launches_per_step(cfg, sw["init"][0], T) + len(plan[W])) * K,
+            "clocks": clk,
+        }
+    for L in layers:
+        L.destroy()
+    sw["src"].destroy()
+    sw["pool"].close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return out
+
+
+def sweep_cpu_baseline(sw, seconds=20.0):
+    """The oracle on one decode token of layer 0, extrapolated to the 32 layers."""
+    from oracle import pw_oracle as O
+
+    cfg = sw["cfg"]
+    t_start = time.perf_counter()
+    n = 0
+    while n < 1 or (time.perf_counter() - t_start < seconds and n < 4):
+        O.moe_tokens(sw["xs"][0], sw["wr"][0], sw["bias"][0], lambda e: sw["experts"][e], sw["init"][0], cfg.K,
+                     cfg.renormalize, [n % sw["T"]])
+        n += 1
+    per_layer = (time.perf_counter() - t_start) / n
+    return {"value": 1.0 / (per_layer * len(sw["layers"])), "unit": "tokens/s", "cores": _threads(),
+            "kind": "oracle",
+            "sample": f"{n} decode tokens through layer 0 at its initial bitwidths, x{len(sw['layers'])} extrapolated "
+                      f"to the 32 layers ({per_layer:.1f} s per token-layer, numpy fp64)"}
 
 
 def _traffic_from_profile(workload, T):
@@ -509,7 +733,10 @@ def run_reference(args):
     for i in range(args.steps):
         one(args.warmup + i)
     el = time.perf_counter() - t0
-    v = args.steps / el
+    # the sweep's metric counts a token through all of its layers: one timed
+    # layer, extrapolated
+    n_layers = cfg.n_layers if args.workload == "sweep" else 1
+    v = args.steps / (el * n_layers)
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -517,7 +744,8 @@ def run_reference(args):
             "config": {"workload": f"{WORKLOADS[args.workload][0]}, {T} tokens per step (same layer as the GPU arm)",
                        "tokens_per_step": 1},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _threads(), "kind": "oracle",
-                             "sample": "one decode token of the batch per step (numpy fp64 oracle)"},
+                             "sample": "one decode token of the batch per step (numpy fp64 oracle)"
+                                       + (f", one layer timed, x{n_layers} extrapolated" if n_layers > 1 else "")},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -539,7 +767,12 @@ def main():
         args.tokens = WORKLOADS[args.workload][1]
     if args.copies is None:
         args.copies = WORKLOADS[args.workload][2]
-    out = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.impl == "reference":
+        out = run_reference(args)
+    elif args.workload == "sweep":
+        out = run_sweep(args)
+    else:
+        out = run_gpu(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 

@@ -114,6 +114,20 @@ pw_status pw_layer_load_expert(pw_layer_t layer, int e, int bits,
                                const uint16_t* const lut[3][4],
                                const uint16_t* const w16[3], void* stream);
 
+/*
+ * Give expert e of `layer` a copy of expert e_src of `src` at bitwidth `bits`
+ * (planes 0..bits-1, or all six planes and the fp16 page for 16), together
+ * with its LUTs, by device-to-device copies in stream order.  Both layers
+ * must have the same d and ffn and pools with the same page size (the pools
+ * may differ).  Every copied block must be one the source reads at its
+ * current bitwidth (PW_ERR_NOT_RESIDENT otherwise; a lowered expert's
+ * reclaimable planes are not copied).  Like pw_layer_load_expert it
+ * synchronises the stream first, replaces whatever expert e held and returns
+ * after the copies are done.  Setup call (e.g. building many layers from one
+ * uploaded set of experts); not for the hot path.
+ */
+pw_status pw_layer_copy_expert(pw_layer_t layer, int e, pw_layer_t src, int e_src, int bits, void* stream);
+
 /* Upload the fp16 shared FFN: w16[0] gate [shared_ffn][d], w16[1] up, w16[2] down [d][shared_ffn]. */
 pw_status pw_layer_load_shared(pw_layer_t layer, const uint16_t* const w16[3], void* stream);
 

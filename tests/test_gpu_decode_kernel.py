@@ -94,6 +94,7 @@ def test_shared_ffn_across_the_decode_threshold(monkeypatch):
     gl = GpuLayer(cfg, seed=6, bits=[3, 16, 3, 3, 16, 3, 3, 3], with_w16=False)
     try:
         monkeypatch.setenv("PW_DECODE_MAX_TOK", "64")
+        monkeypatch.setenv("PW_DECODE_MAX_TOK_SHARED", "64")
         for T in (64, 65):  # shared FFN on the decode kernel, then on the tensor-core GEMM
             gl.check_forward(gl.tokens(T))
     finally:

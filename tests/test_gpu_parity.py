@@ -243,8 +243,9 @@ def test_empty_batch():
 
 @pytest.fixture
 def decode_max_tok(monkeypatch):
-    def set_(v):
+    def set_(v):  # routed experts and the shared FFN switch at the same batch size
         monkeypatch.setenv("PW_DECODE_MAX_TOK", str(v))
+        monkeypatch.setenv("PW_DECODE_MAX_TOK_SHARED", str(v))
     return set_
 
 

@@ -218,3 +218,38 @@ def test_compute_calls_refuse_in_host_sim(sim):
     assert rc == 2
     layer.destroy()
     pool.close()
+
+
+def test_copy_expert_between_layers(sim):
+    pool = pw.Pool(96 * PAGE, page_bytes=PAGE, device="cpu")
+    a = _layer(pool)
+    b = _layer(pool)
+    ex = _expert(2)
+    _load(a, 2, 16, ex)
+    for bits in (3, 5, 16):
+        b.copy_expert(1, a, 2, bits, stream=0)
+        assert b.get_expert_bitwidth(1) == bits
+        np_ = 6 if bits == 16 else bits
+        for p in range(6):
+            src, dst = a.page_address(2, p, 0), b.page_address(1, p, 0)
+            if p < np_:
+                assert dst != 0 and dst != src
+                assert np.array_equal(_page_bytes(pool, dst, PAGE), _page_bytes(pool, src, PAGE))
+            else:
+                assert dst == 0
+    # the fp16 page came along at 16 bits
+    assert np.array_equal(_page_bytes(pool, b.page_address(1, 6, 0), PAGE), _page_bytes(pool, a.page_address(2, 6, 0), PAGE))
+    # a lowered source no longer offers its detached planes
+    a.set_expert_bitwidth(2, 4, stream=0)
+    with pytest.raises(pw.PwError) as ei:
+        b.copy_expert(0, a, 2, 5, stream=0)
+    assert ei.value.status == 4
+    b.copy_expert(0, a, 2, 4, stream=0)
+    # shapes must agree
+    c = pw.Layer(pool, 128, 192, 4, 2, 1)
+    with pytest.raises(pw.PwError):
+        c.copy_expert(0, a, 2, 3, stream=0)
+    for L in (a, b, c):
+        L.destroy()
+    assert pool.stats()["free_pages"] == pool.stats()["total_pages"]
+    pool.close()

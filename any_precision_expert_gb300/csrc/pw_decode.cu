@@ -9,17 +9,18 @@
 // the time goes into streaming weights.
 //
 // A CTA (four warps) takes one work item at a time and stages the item's
-// token rows once into shared memory (K-blocks of 768 columns,
-// double-buffered, rows XOR-swizzled for conflict-free ldmatrix).  Two item
-// shapes:
+// token rows (up to 32) once into shared memory (K-blocks of 384 columns,
+// double-buffered, rows XOR-swizzled for conflict-free ldmatrix).  Weights
+// stream through per-warp cp.async rings addressed through the page table.
+// Item shapes:
 //  - block item (3-bit experts, fp16 pages, shared FFN): (group, phase,
-//    16-token chunk, four 16-row tiles); each warp owns one tile and streams
-//    its weights through a private cp.async ring.  3-bit codes are decoded
-//    with byte permutes from register LUTs.
-//  - split item (4, 5, 6-bit experts): (group, phase, chunk, one tile); the
-//    four warps take interleaved 128-column pieces of the tile's reduction,
-//    look codes up in one CTA-wide LUT table (per-lane copies of the row pair
-//    g / g+8, so no bank conflicts) and add their partial sums in warp order.
+//    32-token chunk, four 16-row tiles), one tile per warp over the whole
+//    reduction.  3-bit codes are decoded with byte permutes from register
+//    LUTs.
+//  - split item (4, 5, 6-bit experts, own launch): (group, phase, 32-token
+//    chunk, one tile); warps 0-1 stream gate and 2-3 up (all four for down)
+//    over interleaved 128-column units and look codes up in one CTA-wide LUT
+//    table (per-lane copies of the row pair g / g+8, so no bank conflicts).
 // The weights feed mma.sync m16n8k16 (weights as A, tokens as B, fp32
 // accumulation).  Gate/up writes h = silu(g) * u in fp16, down writes y in
 // fp32.
@@ -44,31 +45,37 @@ namespace pw {
 
 constexpr int kCtaThreads = 128;
 constexpr int kCtaWarps = kCtaThreads / 32;           // tiles of a block item
-constexpr int kCtaBlocksPerSm = 2;
-constexpr int kSlabCols = 768;                        // columns of one staged K-block
-constexpr int kSlabRows = kTok;                       // token rows of a staged K-block
-constexpr int kSlabHalf = kSlabRows * kSlabCols * 2;  // bytes of one K-block buffer
 constexpr int kTabBytes = 64 * 256;                   // LUT table of a split item (b <= 6, two matrices)
-constexpr int kRingSplit = 10 * 1024;                 // cp.async weight ring of one warp (split items)
-constexpr int kRingBlock = 14 * 1024;                 // ... (block items: no LUT table to hold)
-constexpr int kCtaSmem = 2 * kSlabHalf + kCtaWarps * kRingBlock;
-static_assert(kTabBytes + kCtaWarps * kRingSplit <= kCtaWarps * kRingBlock, "split layout must fit");
 constexpr long long kSpinLimit = 1ll << 22;           // polls of a phase counter (about a second)
 
+// Geometry of the two kernels: items take up to 32 tokens (a weight tile is
+// streamed and decoded once for up to 32 tokens).  The 3-bit / fp16 kernel
+// stages 256-column K-blocks and runs three CTAs per SM (at most 168
+// registers a thread); the 4..6-bit kernel stages 384-column K-blocks, holds
+// a LUT table and runs two.
+template <bool SPLIT>
+struct Geo {
+  static constexpr int TOK = 32;                          // tokens per item
+  static constexpr int NTM = TOK / 8;                     // mma n-tiles per item
+  static constexpr int SCOLS = SPLIT ? 384 : 256;         // columns of one staged K-block
+  static constexpr int HALF = TOK * SCOLS * 2;            // bytes of one K-block buffer
+  static constexpr int RB = SPLIT ? 10 * 1024 : 9 * 1024;  // cp.async weight ring of one warp
+  static constexpr int BLOCKS = SPLIT ? 2 : 3;            // CTAs per SM
+  static constexpr int SMEM = 2 * HALF + (SPLIT ? kTabBytes : 0) + kCtaWarps * RB;
+};
+
 // Weight units streamed by a warp: one matrix of
-//   KIND_P3: a plane group (4 chunks, 256 columns) of 3-bit words, 16 B per lane and plane;
 //   KIND_F16: one fp16 chunk (64 columns), 4 x 16 B per lane;
 //   KIND_PB: half a plane group (2 chunks, 128 columns) of B-bit words, 8 B per lane and plane.
-enum { KIND_P3 = 0, KIND_F16 = 1, KIND_PB = 2 };
+enum { KIND_F16 = 1, KIND_PB = 2 };
 
 template <int KIND, int B, int RB>
 struct Unit {
-  static constexpr int COLS = KIND == KIND_P3 ? 256 : KIND == KIND_F16 ? 64 : 128;
-  static constexpr int LANE_BYTES = KIND == KIND_P3 ? 3 * 16 : KIND == KIND_F16 ? 4 * 16 : B * 8;
+  static constexpr int COLS = KIND == KIND_F16 ? 64 : 128;
+  static constexpr int LANE_BYTES = KIND == KIND_F16 ? 4 * 16 : B * 8;
   static constexpr int SLOT = LANE_BYTES * 32;
   static constexpr int R = RB / SLOT > 8 ? 8 : RB / SLOT;  // ring depth
   static_assert(RB / SLOT >= 3, "ring too shallow");
-  static_assert(kSlabCols % COLS == 0, "units must not straddle K-blocks");
 };
 
 struct UniParams {
@@ -122,32 +129,37 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
 }
 
 // Byte offset of 16-byte piece j (8 columns) of token row r in a staged K-block.
+template <class G>
 __device__ __forceinline__ uint32_t slab_off(int r, int j) {
-  return (uint32_t)(r * (kSlabCols * 2) + ((j ^ (r & 7)) << 4));
+  return (uint32_t)(r * (G::SCOLS * 2) + ((j ^ (r & 7)) << 4));
 }
 
 // Copy K-block kb of the item's token rows into a slab buffer (all threads).
+template <class G>
 __device__ __forceinline__ void stage_kblock(const __half* act, const int* s_tok, int rows, int K, int kb,
                                              uint32_t buf) {
-  const int c0 = kb * kSlabCols;
-  const int ppr = min(kSlabCols, K - c0) >> 3;  // 16-byte pieces per row
+  const int c0 = kb * G::SCOLS;
+  const int ppr = min(G::SCOLS, K - c0) >> 3;  // 16-byte pieces per row
   const int n = rows * ppr;
   for (int p = threadIdx.x; p < n; p += kCtaThreads) {
     const int r = p / ppr, j = p - r * ppr;
-    cp_async16(buf + slab_off(r, j), act + (size_t)s_tok[r] * K + c0 + j * 8);
+    cp_async16(buf + slab_off<G>(r, j), act + (size_t)s_tok[r] * K + c0 + j * 8);
   }
 }
 
-// B fragments of one 64-column chunk (column kc of its K-block) for the n-tiles.
-__device__ __forceinline__ void slab_bfrag(uint32_t buf, int kc, int NT, uint32_t (&bf)[kNT][4][2]) {
+// B fragments of mma step s (16 columns at column kc + 16 s of its K-block)
+// for the n-tiles: one ldmatrix.x4 per pair of n-tiles (b0, b1 of each).
+// Rows past the item's tokens hold stale data; their n-tiles are not used.
+template <class G>
+__device__ __forceinline__ void slab_bstep(uint32_t buf, int kc, int s, int NT, uint32_t (&bf)[G::NTM][2]) {
   const int lane = threadIdx.x & 31;
+  const int mat = lane >> 3;
+  const int j = (kc >> 3) + 2 * s + (mat & 1);
 #pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
-    if (nt < NT) {
-      const int r = nt * 8 + (lane & 7);
-      const int j0 = (kc >> 3) + (lane >> 3);
-      ldsm_x4(buf + slab_off(r, j0), bf[nt][0][0], bf[nt][0][1], bf[nt][1][0], bf[nt][1][1]);
-      ldsm_x4(buf + slab_off(r, j0 + 4), bf[nt][2][0], bf[nt][2][1], bf[nt][3][0], bf[nt][3][1]);
+  for (int nt0 = 0; nt0 < G::NTM; nt0 += 2) {
+    if (nt0 < NT) {
+      const int r = (nt0 + (mat >> 1)) * 8 + (lane & 7);
+      ldsm_x4(buf + slab_off<G>(r, j), bf[nt0][0], bf[nt0][1], bf[nt0 + 1][0], bf[nt0 + 1][1]);
     }
   }
 }
@@ -200,7 +212,7 @@ __device__ __forceinline__ void build_tab(const DevLayer& L, int e, int tau, uns
 // Weight sources of one warp's K loop.
 template <int NM>
 struct WSrc {
-  const char* p[NM][6];  // plane tiles (KIND_P3 / KIND_PB) or the fp16 tile in p[m][0]
+  const char* p[NM][6];  // plane tiles (KIND_PB) or the fp16 tile in p[m][0]
   uint32_t lut3[NM][2][4];
 };
 
@@ -208,19 +220,20 @@ struct WSrc {
 // (column block u / NM, matrix u % NM)).  Every warp of the CTA runs it for
 // the same item and passes the same K-block barriers; the token rows of
 // K-block kb are staged at the start of K-block kb - 1.
-template <int KIND, int B, int NM, int RB>
+template <class G, int KIND, int B, int NM>
 __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0, int ustride, uint32_t ring,
                                       uint32_t slab, uint32_t tab, const __half* act, const int* s_tok,
-                                      float (&acc)[NM][kNT][4]) {
-  using U = Unit<KIND, B, RB>;
+                                      float (&acc)[NM][G::NTM][4]) {
+  using U = Unit<KIND, B, G::RB>;
+  static_assert(G::SCOLS % U::COLS == 0, "units must not straddle K-blocks");
   constexpr int R = U::R;
   const int lane = threadIdx.x & 31;
   const int rows = NT * 8;
-  const int nk = K / 64, G = nk / 4, rem = nk % 4;
+  const int nk = K / 64, GR = nk / 4, rem = nk % 4;
   const int ncb = (K + U::COLS - 1) / U::COLS;  // column blocks
   const int nu = ncb * NM;
   const int mine = u0 < nu ? (nu - u0 + ustride - 1) / ustride : 0;
-  const int kbs = (K + kSlabCols - 1) / kSlabCols;
+  const int kbs = (K + G::SCOLS - 1) / G::SCOLS;
 
   auto issue = [&](int i) {
     const int u = u0 + i * ustride, cb = u / NM, mi = u % NM;
@@ -230,26 +243,15 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
 #pragma unroll
       for (int s = 0; s < 4; ++s)
         cp_async16(slot + (s * 32 + lane) * 16, pp[0] + ((size_t)(cb * 4 + s) * 32 + lane) * 16);
-    } else if constexpr (KIND == KIND_P3) {
-      if (cb < G) {
-        const size_t off = (size_t)(cb * 128 + lane * 4) * 4;
-#pragma unroll
-        for (int p = 0; p < 3; ++p) cp_async16(slot + (p * 32 + lane) * 16, pp[p] + off);
-      } else {
-        const size_t off = (size_t)(G * 128 + lane * rem) * 4;
-#pragma unroll
-        for (int p = 0; p < 3; ++p)
-          for (int k = 0; k < rem; ++k) cp_async4(slot + (p * 32 + lane) * 16 + 4 * k, pp[p] + off + 4 * k);
-      }
     } else {
       const int gamma = cb >> 1, j = cb & 1;
-      if (gamma < G) {
+      if (gamma < GR) {
         const size_t off = (size_t)(gamma * 128 + lane * 4 + 2 * j) * 4;
 #pragma unroll
         for (int p = 0; p < B; ++p) cp_async8(slot + (p * 32 + lane) * 8, pp[p] + off);
       } else {
         const int cnt = min(2, rem - 2 * j);
-        const size_t off = (size_t)(G * 128 + lane * rem + 2 * j) * 4;
+        const size_t off = (size_t)(GR * 128 + lane * rem + 2 * j) * 4;
 #pragma unroll
         for (int p = 0; p < B; ++p)
           for (int k = 0; k < cnt; ++k) cp_async4(slot + (p * 32 + lane) * 8 + 4 * k, pp[p] + off + 4 * k);
@@ -258,8 +260,8 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
   };
 
   // K-blocks 0 and 1 go with the first ring group
-  stage_kblock(act, s_tok, rows, K, 0, slab);
-  if (kbs > 1) stage_kblock(act, s_tok, rows, K, 1, slab + kSlabHalf);
+  stage_kblock<G>(act, s_tok, rows, K, 0, slab);
+  if (kbs > 1) stage_kblock<G>(act, s_tok, rows, K, 1, slab + G::HALF);
   int since_stage = 0;  // groups committed after the newest staging group
 #pragma unroll
   for (int i = 0; i < R - 1; ++i) {
@@ -274,7 +276,7 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
       cp_wait_dyn(since_stage);  // this thread's copies of K-block kb_cur have landed
       __syncthreads();           // ... and everyone's; K-block kb_cur - 1 is no longer read
       if (kb_cur >= 1 && kb_cur + 1 < kbs) {
-        stage_kblock(act, s_tok, rows, K, kb_cur + 1, slab + ((kb_cur + 1) & 1) * kSlabHalf);
+        stage_kblock<G>(act, s_tok, rows, K, kb_cur + 1, slab + ((kb_cur + 1) & 1) * G::HALF);
         cp_commit();
         since_stage = 0;
       }
@@ -287,54 +289,26 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
     cp_commit();
     ++since_stage;
     const int u = u0 + i * ustride, cb = u / NM, mi = u % NM;
-    const int kb = (cb * U::COLS) / kSlabCols;
+    const int kb = (cb * U::COLS) / G::SCOLS;
     advance_to(kb);
     cp_wait<R - 1>();  // unit i has landed
-    const uint32_t buf = slab + (kb & 1) * kSlabHalf;
-    const int kc0 = (cb * U::COLS) % kSlabCols;
+    const uint32_t buf = slab + (kb & 1) * G::HALF;
+    const int kc0 = (cb * U::COLS) % G::SCOLS;
     const uint32_t slot = ring + (i % R) * U::SLOT;
     // the matrix is fixed for the whole unit: branch once, then fully
     // unrolled chunks of independent decode + mma chains
     auto compute = [&](auto tag) {
       constexpr int m = decltype(tag)::value;
       if constexpr (KIND == KIND_F16) {
-        uint32_t bf[kNT][4][2];
-        slab_bfrag(buf, kc0, NT, bf);
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
+          uint32_t bf[G::NTM][2];
+          slab_bstep<G>(buf, kc0, s, NT, bf);
           const uint4 v = lds128(slot + (s * 32 + lane) * 16);
           const uint32_t a[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int nt = 0; nt < kNT; ++nt)
-            if (nt < NT) mma16816(acc[m][nt], a, bf[nt][s][0], bf[nt][s][1]);
-        }
-      } else if constexpr (KIND == KIND_P3) {
-        uint32_t w[3][4];
-#pragma unroll
-        for (int p = 0; p < 3; ++p) {
-          const uint4 v = lds128(slot + (p * 32 + lane) * 16);
-          w[p][0] = v.x;
-          w[p][1] = v.y;
-          w[p][2] = v.z;
-          w[p][3] = v.w;
-        }
-        const int nch = cb < G ? 4 : rem;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c < nch) {
-            uint32_t bf[kNT][4][2];
-            slab_bfrag(buf, kc0 + c * 64, NT, bf);
-            // decode the chunk's four steps first (independent chains), then the mma's
-            const uint32_t wc[3] = {w[0][c], w[1][c], w[2][c]};
-            uint32_t a[4][4];
-#pragma unroll
-            for (int s = 0; s < 4; ++s) decode_step_prmt3(wc, s, src.lut3[m], a[s]);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-#pragma unroll
-              for (int nt = 0; nt < kNT; ++nt)
-                if (nt < NT) mma16816(acc[m][nt], a[s], bf[nt][s][0], bf[nt][s][1]);
-          }
+          for (int nt = 0; nt < G::NTM; ++nt)
+            if (nt < NT) mma16816(acc[m][nt], a, bf[nt][0], bf[nt][1]);
         }
       } else {
         uint32_t w[B][2];
@@ -344,24 +318,29 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
           w[p][0] = v.x;
           w[p][1] = v.y;
         }
-        const int nch = (cb >> 1) < G ? 2 : min(2, rem - 2 * (cb & 1));
-        const uint32_t lbm = m * 128 + lane * 4;
-#pragma unroll
+        const int nch = (cb >> 1) < GR ? 2 : min(2, rem - 2 * (cb & 1));
+        // the two chunks share one copy of the code (instruction-cache footprint)
+#pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           if (c < nch) {
-            uint32_t bf[kNT][4][2];
-            slab_bfrag(buf, kc0 + c * 64, NT, bf);
             uint32_t wc[B];
 #pragma unroll
-            for (int p = 0; p < B; ++p) wc[p] = w[p][c];
+            for (int p = 0; p < B; ++p) wc[p] = c ? w[p][1] : w[p][0];
+            // decode the chunk's four steps first (independent chains), then the mma's
             uint32_t a[4][4];
 #pragma unroll
-            for (int s = 0; s < 4; ++s) decode_step_tab<B>(wc, s, tab, lbm, a[s]);
+            for (int s = 0; s < 4; ++s) {
+              if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3[m], a[s]);
+              else decode_step_tab<B>(wc, s, tab, m * 128 + lane * 4, a[s]);
+            }
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
+            for (int s = 0; s < 4; ++s) {
+              uint32_t bf[G::NTM][2];
+              slab_bstep<G>(buf, kc0 + c * 64, s, NT, bf);
 #pragma unroll
-              for (int nt = 0; nt < kNT; ++nt)
-                if (nt < NT) mma16816(acc[m][nt], a[s], bf[nt][s][0], bf[nt][s][1]);
+              for (int nt = 0; nt < G::NTM; ++nt)
+                if (nt < NT) mma16816(acc[m][nt], a[s], bf[nt][0], bf[nt][1]);
+            }
           }
         }
       }
@@ -374,12 +353,12 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
 }
 
 // Epilogue of one tile: C fragment element (row g / g+8, token nt*8 + 2t + {0,1}).
-template <int NM>
-__device__ __forceinline__ void tile_store(const float (&acc)[NM][kNT][4], int tau, int row0, int ntok, int ld,
+template <int NM, int NTM>
+__device__ __forceinline__ void tile_store(const float (&acc)[NM][NTM][4], int tau, int row0, int ntok, int ld,
                                            __half* h, float* y) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
-  for (int nt = 0; nt < kNT; ++nt)
+  for (int nt = 0; nt < NTM; ++nt)
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int j = nt * 8 + 2 * t + (r & 1);
@@ -402,12 +381,14 @@ struct ItemArgs {
   float* y;
 };
 
-// Block item: warp w computes tile tau0 + w over the whole reduction.
+// Block item: warp w computes tile tau + w over the whole reduction.
 template <int NM, int B>
 __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A, int tau, uint32_t ring,
                                            uint32_t slab, const int* s_tok) {
-  const int lane = threadIdx.x & 31;
-  float acc[NM][kNT][4] = {};
+  using G = Geo<false>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tau += warp;
+  float acc[NM][G::NTM][4] = {};
   WSrc<NM> src;
 #pragma unroll
   for (int mi = 0; mi < NM; ++mi) {
@@ -423,55 +404,58 @@ __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A,
       load_lut3(lr + ((lane >> 2) + 8) * 8, src.lut3[mi][1]);
     }
   }
-  if constexpr (B == 16) kloop<KIND_F16, 16, NM, kRingBlock>(src, A.K, A.NT, 0, 1, ring, slab, 0u, A.act, s_tok, acc);
-  else kloop<KIND_P3, 3, NM, kRingBlock>(src, A.K, A.NT, 0, 1, ring, slab, 0u, A.act, s_tok, acc);
-  tile_store<NM>(acc, tau, A.row0, A.ntok, A.ld, A.h, A.y);
+  if constexpr (B == 16) kloop<G, KIND_F16, 16, NM>(src, A.K, A.NT, 0, 1, ring, slab, 0u, A.act, s_tok, acc);
+  else kloop<G, KIND_PB, 3, NM>(src, A.K, A.NT, 0, 1, ring, slab, 0u, A.act, s_tok, acc);
+  tile_store<NM, G::NTM>(acc, tau, A.row0, A.ntok, A.ld, A.h, A.y);
 }
 
-// Split item: the four warps share tile tau; partial sums are added in warp order.
+// Split item: the four warps share tile tau.  For gate/up, warps 0-1 stream
+// the gate matrix and warps 2-3 the up matrix (interleaved 128-column units),
+// so every warp runs the one-matrix loop; partial sums are added in warp order.
 template <int NM, int B>
 __device__ __forceinline__ void split_item(const DevLayer& L, const ItemArgs& A, int tau, uint32_t ring,
                                            uint32_t slab, unsigned char* tab_ptr, const int* s_tok) {
+  using G = Geo<true>;
+  constexpr int kNT = G::NTM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   build_tab<B, NM>(L, A.e, tau, tab_ptr);  // ordered before use by the first K-block barrier
-  float acc[NM][kNT][4] = {};
-  WSrc<NM> src;
+  const int mi = NM == 2 ? warp >> 1 : 0;  // this warp's matrix (index into the item's NM)
+  float acc[1][kNT][4] = {};
+  WSrc<1> src;
 #pragma unroll
-  for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-    for (int p = 0; p < 6; ++p) src.p[mi][p] = p < B ? tile_addr(L, A.e, NM == 2 ? mi : 2, p, tau) : nullptr;
-  kloop<KIND_PB, B, NM, kRingSplit>(src, A.K, A.NT, warp, kCtaWarps, ring, slab, smem_u32(tab_ptr), A.act, s_tok,
-                                    acc);
-  __syncthreads();  // the staged rows are no longer read: reuse them for the partial sums
+  for (int p = 0; p < 6; ++p) src.p[0][p] = p < B ? tile_addr(L, A.e, NM == 2 ? mi : 2, p, tau) : nullptr;
+  // the LUT table column of this warp's matrix: unit u of the one-matrix loop is matrix 0
+  const uint32_t tab = smem_u32(tab_ptr) + mi * 128;
+  if (NM == 2) kloop<G, KIND_PB, B, 1>(src, A.K, A.NT, warp & 1, 2, ring, slab, tab, A.act, s_tok, acc);
+  else kloop<G, KIND_PB, B, 1>(src, A.K, A.NT, warp, kCtaWarps, ring, slab, tab, A.act, s_tok, acc);
+  __syncthreads();  // the staged rows are no longer read
   float4* red = reinterpret_cast<float4*>(__cvta_shared_to_generic(slab));
 #pragma unroll
-  for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
-      red[((warp * NM + mi) * kNT + nt) * 32 + lane] =
-          make_float4(acc[mi][nt][0], acc[mi][nt][1], acc[mi][nt][2], acc[mi][nt][3]);
+  for (int nt = 0; nt < kNT; ++nt)
+    red[(warp * kNT + nt) * 32 + lane] = make_float4(acc[0][nt][0], acc[0][nt][1], acc[0][nt][2], acc[0][nt][3]);
   __syncthreads();
   if (warp == 0) {
+    constexpr int WPM = kCtaWarps / NM;  // warps per matrix
     float sum[NM][kNT][4];
 #pragma unroll
-    for (int mi = 0; mi < NM; ++mi)
+    for (int m = 0; m < NM; ++m)
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
-        float4 v = red[(mi * kNT + nt) * 32 + lane];
+        float4 v = red[((m * WPM) * kNT + nt) * 32 + lane];
 #pragma unroll
-        for (int w = 1; w < kCtaWarps; ++w) {
-          const float4 o = red[((w * NM + mi) * kNT + nt) * 32 + lane];
+        for (int w = 1; w < WPM; ++w) {
+          const float4 o = red[((m * WPM + w) * kNT + nt) * 32 + lane];
           v.x += o.x;
           v.y += o.y;
           v.z += o.z;
           v.w += o.w;
         }
-        sum[mi][nt][0] = v.x;
-        sum[mi][nt][1] = v.y;
-        sum[mi][nt][2] = v.z;
-        sum[mi][nt][3] = v.w;
+        sum[m][nt][0] = v.x;
+        sum[m][nt][1] = v.y;
+        sum[m][nt][2] = v.z;
+        sum[m][nt][3] = v.w;
       }
-    tile_store<NM>(sum, tau, A.row0, A.ntok, A.ld, A.h, A.y);
+    tile_store<NM, kNT>(sum, tau, A.row0, A.ntok, A.ld, A.h, A.y);
   }
 }
 
@@ -482,7 +466,8 @@ __device__ __forceinline__ bool is_split(int b) { return b >= 4 && b <= 6; }
 // paths in its own register allocation; their groups are disjoint, so they
 // share the layer's phase counters and use separate claim counters.
 template <bool SPLIT>
-__global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(UniParams P) {
+__global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kernel(UniParams P) {
+  using G = Geo<SPLIT>;
   extern __shared__ __align__(128) unsigned char smem_uni[];
   __shared__ int s_base[kMaxExperts + 1];   // first input row of each group
   __shared__ int s_n[kMaxExperts + 1];      // tokens of each group
@@ -490,7 +475,7 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(U
   __shared__ short s_ord[kMaxExperts + 1];  // groups in claim order
   __shared__ int s_pref[2][kMaxExperts + 2];
   __shared__ int s_ng, s_it;
-  __shared__ int s_tok[kSlabRows];
+  __shared__ int s_tok[G::TOK];
 
   const DevLayer& L = P.L;
   const int E = L.E;
@@ -544,7 +529,7 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(U
           const int fe = g == E ? L.fs : L.f;
           const int tiles = ph == 0 ? fe / kTileRows : L.d / kTileRows;
           const int per_chunk = SPLIT ? tiles : tiles / kCtaWarps;
-          c = ((s_n[g] + kTok - 1) / kTok) * per_chunk;
+          c = ((s_n[g] + G::TOK - 1) / G::TOK) * per_chunk;
         }
         int incl = c;
 #pragma unroll
@@ -560,9 +545,8 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(U
     if (lane == 0) s_ng = ng;
   }
   const uint32_t slab = smem_u32(smem_uni);
-  unsigned char* const tab_ptr = smem_uni + 2 * kSlabHalf;  // split items only
-  const uint32_t ring = SPLIT ? slab + 2 * kSlabHalf + kTabBytes + warp * kRingSplit
-                              : slab + 2 * kSlabHalf + warp * kRingBlock;
+  unsigned char* const tab_ptr = smem_uni + 2 * G::HALF;  // split items only
+  const uint32_t ring = slab + 2 * G::HALF + (SPLIT ? kTabBytes : 0) + warp * G::RB;
 
   for (;;) {
     if (tid == 0) s_it = atomicAdd(q, 1);
@@ -583,7 +567,7 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(U
     const bool sh = g == E;
     const int b = s_b[g];
     const int n = s_n[g];
-    const int nch = (n + kTok - 1) / kTok;
+    const int nch = (n + G::TOK - 1) / G::TOK;
     const int local = li - pref[lo];
     const int blk = local / nch, chunk = local % nch;  // chunks of one tile (block) are claimed together
     const int fe = sh ? L.fs : L.f;
@@ -593,8 +577,8 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(U
     ItemArgs A;
     A.e = g;
     A.sh = sh;
-    A.row0 = s_base[g] + chunk * kTok;
-    A.ntok = min(kTok, n - chunk * kTok);
+    A.row0 = s_base[g] + chunk * G::TOK;
+    A.ntok = min(G::TOK, n - chunk * G::TOK);
     A.NT = (A.ntok + 7) >> 3;
     A.K = phase == 0 ? L.d : fe;
     A.act = phase == 0 ? (sh ? P.x : P.xp) : (sh ? P.hs : P.h);
@@ -602,7 +586,7 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(U
     A.h = sh ? P.hs : P.h;
     A.y = sh ? P.ys : P.y;
 
-    if (tid < kSlabRows) s_tok[tid] = A.row0 + min(tid, A.ntok - 1);
+    if (tid < G::TOK) s_tok[tid] = A.row0 + min(tid, A.ntok - 1);
     if (phase == 1 && tid == 0) {  // h of this chunk must be complete
       const int need = fe / kTileRows;
       long long spins = 0;
@@ -631,7 +615,7 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(U
         }
       }
     } else {
-      const int tau = blk * kCtaWarps + warp;
+      const int tau = blk * kCtaWarps;
       if (phase == 0) {
         if (b == 16) block_item<2, 16>(L, A, tau, ring, slab, s_tok);
         else block_item<2, 3>(L, A, tau, ring, slab, s_tok);
@@ -664,9 +648,9 @@ __global__ void __launch_bounds__(kCtaThreads, kCtaBlocksPerSm) ffn_cta_kernel(U
 }
 
 cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
-                       int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s) {
-  if (max_tokens > kSyncChunks * kTok) return cudaErrorInvalidValue;
-  if (x && T > kSyncChunks * kTok) return cudaErrorInvalidValue;
+                       int bit_mask, int max_tokens, float split_share, __half* h, __half* hs, float* y, float* ys,
+                       cudaStream_t s) {
+  if (max_tokens > kSyncChunks * 16 || (x && T > kSyncChunks * 16)) return cudaErrorInvalidValue;
   UniParams P;
   P.L = L;
   P.x = x;
@@ -679,21 +663,39 @@ cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm,
   P.hs = hs;
   P.y = y;
   P.ys = ys;
-  cudaError_t e = cudaSuccess;
-  if (bit_mask & 4) {
-    e = ensure_smem((const void*)ffn_cta_kernel<true>, kCtaSmem);
-    if (e != cudaSuccess) return e;
-    ffn_cta_kernel<true><<<sm_count() * kCtaBlocksPerSm, kCtaThreads, kCtaSmem, s>>>(P);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  const bool split = (bit_mask & 4) != 0, block = (bit_mask & 3) || x;
+  cudaError_t e;
+  // The two kernels have disjoint groups and claim counters.  When the
+  // 4..6-bit experts hold a small share of the weight bytes, their kernel runs
+  // on the layer's side stream next to the other one (its latency-bound items
+  // overlap the weight streaming); when they hold most of the bytes it needs
+  // the whole GPU, and the kernels run one after the other.
+  const bool fork = split && block && L.side_stream && split_share < 0.3f;
+  cudaStream_t ss = fork ? static_cast<cudaStream_t>(L.side_stream) : s;
+  if (fork) {
+    if ((e = cudaEventRecord(static_cast<cudaEvent_t>(L.ev_fork), s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss, static_cast<cudaEvent_t>(L.ev_fork), 0)) != cudaSuccess) return e;
   }
-  if ((bit_mask & 3) || x) {
-    e = ensure_smem((const void*)ffn_cta_kernel<false>, kCtaSmem);
-    if (e != cudaSuccess) return e;
-    ffn_cta_kernel<false><<<sm_count() * kCtaBlocksPerSm, kCtaThreads, kCtaSmem, s>>>(P);
-    e = cudaGetLastError();
+  if (split) {
+    using G = Geo<true>;
+    if ((e = ensure_smem((const void*)ffn_cta_kernel<true>, G::SMEM)) != cudaSuccess) return e;
+    // side by side: one CTA per SM, so every SM keeps room for a CTA of the
+    // other kernel (whose grid fills the rest of the GPU as these CTAs leave)
+    const int grid = sm_count() * (fork ? 1 : G::BLOCKS);
+    ffn_cta_kernel<true><<<grid, kCtaThreads, G::SMEM, ss>>>(P);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  return e;
+  if (block) {
+    using G = Geo<false>;
+    if ((e = ensure_smem((const void*)ffn_cta_kernel<false>, G::SMEM)) != cudaSuccess) return e;
+    ffn_cta_kernel<false><<<sm_count() * G::BLOCKS, kCtaThreads, G::SMEM, s>>>(P);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (fork) {
+    if ((e = cudaEventRecord(static_cast<cudaEvent_t>(L.ev_join), ss)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(L.ev_join), 0)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace pw

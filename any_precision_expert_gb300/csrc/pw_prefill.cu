@@ -425,8 +425,11 @@ static int env_tokens(const char* name, int dflt) {
   return v < 0 ? 0 : v > kSyncChunks * 16 ? kSyncChunks * 16 : v;
 }
 
-// Routed experts with more tokens than this use the tensor-core GEMM (read per call).
-int decode_max_tokens() { return env_tokens("PW_DECODE_MAX_TOK", 64); }
+// Routed experts with more tokens than this use the tensor-core GEMM (read per
+// call).  Wide experts (ffn >= 4096: at least 32 row tiles of 128 per matrix)
+// fill the GPU with GEMM tiles from 33 tokens on; narrow ones only well above
+// a decode batch's share.
+int decode_max_tokens(int ffn) { return env_tokens("PW_DECODE_MAX_TOK", ffn >= 4096 ? 32 : 64); }
 
 // The shared FFN (every token of the batch) uses the tensor-core GEMM above this batch size.
 int decode_max_tokens_shared() { return env_tokens("PW_DECODE_MAX_TOK_SHARED", 256); }

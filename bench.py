@@ -423,7 +423,7 @@ def _launches_per_step(cfg, bits, T):
     one for 3-bit / fp16 experts and the shared FFN, the tcgen05 GEMM pair for
     experts above the token threshold and for a shared FFN above its own, and
     the combine."""
-    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "64")), 1024)
+    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "32" if cfg.f >= 4096 else "64")), 1024)
     thr_s = min(int(os.environ.get("PW_DECODE_MAX_TOK_SHARED", "256")), 1024)
     S = T * cfg.K
     n = 1 + (2 if S > 1024 else 1) + 1
@@ -670,7 +670,7 @@ def _traffic_from_profile(workload, T):
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("pw_ffn.cu", "pw_prefill.cu", "pw_device.cuh", "pw_tc.cuh"):
+    for f in ("pw_ffn.cu", "pw_decode.cu", "pw_gemv.cuh", "pw_prefill.cu", "pw_device.cuh", "pw_tc.cuh"):
         with open(os.path.join(ROOT, "any_precision_expert_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -23,8 +23,10 @@
 
 #include <climits>
 #include <cstdlib>
+#include <type_traits>
 
 #include "pw_device.cuh"
+#include "pw_gemv.cuh"
 #include "pw_tc.cuh"
 
 namespace pw {
@@ -100,6 +102,24 @@ __device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint
 #pragma unroll
       for (int p = 0; p < B; ++p) wt[p] = w[t][p];
       decode_step_lut<B>(wt, s, tab, lb0, lb1, a[t]);
+    }
+    out[s][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
+    out[s][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
+    out[s][2] = make_uint4(a[0][1], a[1][1], a[2][1], a[3][1]);
+    out[s][3] = make_uint4(a[0][3], a[1][3], a[2][3], a[3][3]);
+  }
+}
+
+// 3-bit codes: byte permutes from this lane's register LUTs (rows g, g+8).
+__device__ __forceinline__ void pf_decode_planes3(const uint32_t (&w)[4][3], const uint32_t (&lut3)[2][4],
+                                                  uint4 (&out)[4][4]) {
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    uint32_t a[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t wt[3] = {w[t][0], w[t][1], w[t][2]};
+      decode_step_prmt3(wt, s, lut3, a[t]);
     }
     out[s][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
     out[s][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
@@ -237,7 +257,12 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
       const int row0 = T.mt * PF_BM + slab * 64 + tis * 16;  // this lane's 16-row tile
       const bool tile_ok = row0 < R;
       const int tau = row0 / 16;
-      if (b <= 6) {
+      uint32_t lut3[2][4] = {};
+      if (b == 3) {  // register LUTs of this lane's row pair; no shared table
+        const int r0 = min(row0 + g, R - 1), r1 = min(row0 + g + 8, R - 1);
+        load_lut3(lut_rows(L, T.e, mm, 3, r0), lut3[0]);
+        load_lut3(lut_rows(L, T.e, mm, 3, r1), lut3[1]);
+      } else if (b <= 6) {
         ok = pair_sync();  // both warps of the pair finished the previous tile
         if (!ok) break;
         const int j = par * 32 + lane, rho = j >> 5, lx = j & 31;
@@ -259,25 +284,56 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
         fb = routed ? tile_addr(L, T.e, mm, kPlanes, tau)
                     : reinterpret_cast<const char*>(L.shared16[mm]) + (size_t)tau * 32 * K;
 
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        if ((kb & 1) != par) continue;
-        const int s = it % C::NS;
-        const uint32_t ph = (it / C::NS) & 1;
-        uint4 out[4][4];
-        switch (b) {
-#define PW_PF_CASE(BB)                                                  \
-  case BB: {                                                            \
-    uint32_t w[4][BB];                                                  \
-    pf_load_planes<BB>(pb, kb, nkb, g, w);                              \
-    pf_decode_planes<BB>(w, tab, lb0, lb1, out);                        \
-    break;                                                              \
-  }
-          PW_PF_CASE(3)
-          PW_PF_CASE(4)
-          PW_PF_CASE(5)
-          PW_PF_CASE(6)
-#undef PW_PF_CASE
-          default: {  // fp16 page: the lane gathers the four fragment lanes (g, t)
+      // this warp's stages kb = par, par + 2, ...: decode one while the plane
+      // words of the next are in flight
+      auto store_stage = [&](int kb, uint4 (&out)[4][4]) {
+        const int s = (it + kb) % C::NS;
+        const uint32_t ph = ((it + kb) / C::NS) & 1;
+        if (!tile_ok) {
+#pragma unroll
+          for (int st = 0; st < 4; ++st)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) out[st][q] = make_uint4(0, 0, 0, 0);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err))) return false;
+        const uint32_t A = base + s * C::STAGE + mi * PF_A_BYTES;
+#pragma unroll
+        for (int st = 0; st < 4; ++st)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = slab * 64 + tis * 16 + g + 8 * (q >> 1);
+            sts128(A + sw128_offset(r, 2 * st + (q & 1)), out[st][q]);
+          }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full_bar(s));
+        return true;
+      };
+      auto plane_loop = [&](auto tag) {
+        constexpr int BB = decltype(tag)::value;
+        uint32_t wn[4][BB];
+        if (par < nkb) pf_load_planes<BB>(pb, par, nkb, g, wn);
+        for (int kb = par; kb < nkb && ok; kb += 2) {
+          uint32_t w[4][BB];
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int p = 0; p < BB; ++p) w[t][p] = wn[t][p];
+          if (kb + 2 < nkb) pf_load_planes<BB>(pb, kb + 2, nkb, g, wn);
+          uint4 out[4][4];
+          if constexpr (BB == 3) pf_decode_planes3(w, lut3, out);
+          else pf_decode_planes<BB>(w, tab, lb0, lb1, out);
+          ok = store_stage(kb, out);
+        }
+      };
+      switch (b) {
+        case 3: plane_loop(std::integral_constant<int, 3>{}); break;
+        case 4: plane_loop(std::integral_constant<int, 4>{}); break;
+        case 5: plane_loop(std::integral_constant<int, 5>{}); break;
+        case 6: plane_loop(std::integral_constant<int, 6>{}); break;
+        default:  // fp16 page: the lane gathers the four fragment lanes (g, t)
+          for (int kb = par; kb < nkb && ok; kb += 2) {
+            uint4 out[4][4];
 #pragma unroll
             for (int st = 0; st < 4; ++st) {
               uint4 a[4];
@@ -290,28 +346,10 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
               out[st][2] = make_uint4(a[0].y, a[1].y, a[2].y, a[3].y);
               out[st][3] = make_uint4(a[0].w, a[1].w, a[2].w, a[3].w);
             }
+            ok = store_stage(kb, out);
           }
-        }
-        if (!tile_ok) {
-#pragma unroll
-          for (int st = 0; st < 4; ++st)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) out[st][q] = make_uint4(0, 0, 0, 0);
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err));
-        if (!ok) break;
-        const uint32_t A = base + s * C::STAGE + mi * PF_A_BYTES;
-#pragma unroll
-        for (int st = 0; st < 4; ++st)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = slab * 64 + tis * 16 + g + 8 * (q >> 1);
-            sts128(A + sw128_offset(r, 2 * st + (q & 1)), out[st][q]);
-          }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar(s));
       }
+      it += nkb;
       if (!ok) break;
       // epilogue: this warp reads TMEM lanes 32*(warp%4).. of the tile's accumulators
       ok = __all_sync(0xffffffffu, mbar_wait(acc_full, tc & 1, abort_flag, L.err));

@@ -164,6 +164,23 @@ class ClockSampler:
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def rank_max(v, ws, device):
+    """Max of v over the ranks of the process group (the job's time is the
+    slowest rank's)."""
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_rank, ws, seconds_max):
+    """Whole-job throughput: the tokens of all ranks over the slowest rank's time."""
+    return ws * tokens_per_rank / seconds_max
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -188,11 +205,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if ws == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(v, ws, "cuda")
 
     T, K, W = args.tokens, args.steps, args.warmup
     wl = build_workload(args.workload, n_copies=args.copies, T=T)
@@ -350,7 +363,7 @@ def run_gpu(args):
         cpu = cpu_baseline(wl, seconds=args.cpu_seconds) if (ws == 1 and args.cpu_seconds > 0) else None
         out = {
             "metric": METRIC,
-            "value": ws * T * K / (ms_max * 1e-3),
+            "value": job_value(T * K, ws, ms_max * 1e-3),
             "unit": "tokens/s",
             "n_gpus": ws,
             "steps": K,
@@ -510,11 +523,7 @@ def run_sweep(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if ws == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(v, ws, "cuda")
 
     T, K, W = args.tokens, args.steps, args.warmup
     sw = build_sweep(T)
@@ -608,7 +617,7 @@ def run_sweep(args):
     if rank == 0:
         cpu = sweep_cpu_baseline(sw, args.cpu_seconds) if (ws == 1 and args.cpu_seconds > 0) else None
         out = {
-            "metric": METRIC, "value": ws * T * K / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws, "steps": K,
+            "metric": METRIC, "value": job_value(T * K, ws, ms * 1e-3), "unit": "tokens/s", "n_gpus": ws, "steps": K,
             "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
             "config": {"workload": f"{WORKLOADS['sweep'][0]}, {T} tokens per step through all {NL} layers",

@@ -58,6 +58,19 @@ def pack_f16(w16: np.ndarray) -> np.ndarray:
     return out
 
 
+def _host_blocks(planes, w16):
+    """C arrays of host pointers (numpy arrays or torch tensors; None allowed)."""
+    def hp(a):
+        if a is None:
+            return None
+        return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
+    arr = None
+    if planes is not None:
+        arr = (U32P6 * 3)(*[U32P6(*[hp(planes[m][q]) for q in range(6)]) for m in range(3)])
+    w = U16P3(*[hp(w16[m]) for m in range(3)]) if w16 is not None else None
+    return arr, w
+
+
 class Pool:
     """Page pool over one device buffer (a torch uint8 tensor)."""
 
@@ -125,6 +138,27 @@ class Layer:
     # -- precision -------------------------------------------------------------
     def set_expert_bitwidth(self, e: int, bits: int, stream=None):
         check(lib.pw_set_expert_bitwidth(self.handle, e, bits, _s(stream)), "pw_set_expert_bitwidth")
+
+    def raise_expert_async(self, e: int, bits: int, planes=None, w16=None, copy_stream=None, stream=None):
+        """Raise expert e to `bits`, uploading missing planes from host memory on
+        copy_stream and committing on stream (pw_raise_expert_async).
+
+        planes: 3 lists (gate, up, down) of 6 packed plane arrays (pack_planes
+        output; entries may be None for planes still resident); w16: 3 packed
+        fp16 pages (pack_f16 output) when raising to 16.  numpy arrays or
+        (preferably pinned) torch tensors; the caller keeps them alive until
+        `stream` has passed this call.
+        """
+        arr, w = _host_blocks(planes, w16)
+        check(lib.pw_raise_expert_async(self.handle, e, bits, arr, w, _s(copy_stream), _s(stream)),
+              f"pw_raise_expert_async(e={e}, bits={bits})")
+
+    def prefetch_expert(self, e: int, bits: int, planes=None, w16=None, copy_stream=None):
+        """Upload the blocks expert e needs at `bits` on copy_stream without
+        raising it (pw_prefetch_expert); a later set_expert_bitwidth commits."""
+        arr, w = _host_blocks(planes, w16)
+        check(lib.pw_prefetch_expert(self.handle, e, bits, arr, w, _s(copy_stream)),
+              f"pw_prefetch_expert(e={e}, bits={bits})")
 
     def try_set_expert_bitwidth(self, e: int, bits: int, stream=None) -> int:
         return lib.pw_set_expert_bitwidth(self.handle, e, bits, _s(stream))

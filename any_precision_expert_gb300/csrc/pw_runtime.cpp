@@ -124,6 +124,7 @@ struct Block {
   BlockState st = B_NONE;
   std::vector<int> pages;         // physical page ids, indexed by virtual page
   std::shared_ptr<Event> ev;      // set while reclaimable
+  std::shared_ptr<Event> ready;   // set while an asynchronous upload into the block may be in flight
   uint64_t fifo_key = 0;
 };
 
@@ -169,6 +170,7 @@ struct pw_pool_s {
     }
     b.pages.clear();
     b.ev.reset();
+    b.ready.reset();
     b.st = B_NONE;
   }
   // Take n pages for a new mapped block.  Reclaimable blocks are given up
@@ -750,6 +752,16 @@ extern "C" pw_status pw_set_expert_bitwidth(pw_layer_t l, int e, int bits, void*
   if (bits == 16 && l->f16[e].st == B_NONE) return PW_ERR_NOT_RESIDENT;
 
   cudaStream_t s = as_stream(stream);
+  // blocks filled by an asynchronous upload: the commit waits for the copies
+  auto await_upload = [&](Block& b) -> pw_status {
+    if (b.ready) {
+      if (!g_sim) PW_CUDA(cudaStreamWaitEvent(s, b.ready->ev, 0));
+      b.ready.reset();
+    }
+    return PW_OK;
+  };
+  for (int p = 0; p < need; ++p) PW_TRY(await_upload(l->plane(e, p)));
+  if (bits == 16) PW_TRY(await_upload(l->f16[e]));
   PW_TRY(write_bits(l, e, bits, s));
   // raise: re-map still-intact blocks (their page-table entries never changed)
   for (int p = 0; p < need; ++p)
@@ -767,6 +779,132 @@ extern "C" pw_status pw_set_expert_bitwidth(pw_layer_t l, int e, int bits, void*
   }
   l->bits[e] = bits;
   return PW_OK;
+}
+
+namespace {
+
+pw_status dev_h2d_on(void* dst, const void* src, size_t n, cudaStream_t s) { return dev_h2d(dst, src, n, s); }
+
+// Copy the tiles of one block image from a packed host array: tiles of matrix
+// m are consecutive in the packed array and, page by page, in the block; runs
+// of tiles that stay inside one page go as one copy.
+pw_status upload_tiles(pw_layer_t l, const Block& b, const std::vector<uint2>& map, int m, const char* host,
+                       size_t tile_bytes, cudaStream_t s) {
+  const int ntiles = l->R[m] / kTileRows;
+  int tau = 0;
+  while (tau < ntiles) {
+    const uint2 loc = map[(size_t)m * l->tmax + tau];
+    int run = 1;
+    while (tau + run < ntiles) {
+      const uint2 nx = map[(size_t)m * l->tmax + tau + run];
+      if (nx.x != loc.x || nx.y != loc.y + run * tile_bytes) break;
+      ++run;
+    }
+    PW_TRY(dev_h2d_on(l->pool->page_addr(b.pages[loc.x]) + loc.y, host + (size_t)tau * tile_bytes,
+                      (size_t)run * tile_bytes, s));
+    tau += run;
+  }
+  return PW_OK;
+}
+
+}  // namespace
+
+extern "C" pw_status pw_prefetch_expert(pw_layer_t l, int e, int bits, const uint32_t* const planes_host[3][6],
+                                        const uint16_t* const w16_host[3], void* copy_stream) {
+  PW_TRY(check_layer(l));
+  if (e < 0 || e >= l->desc.n_experts || !valid_bits(bits)) return PW_ERR_INVALID_ARG;
+  if (l->bits[e] == 0) return PW_ERR_INVALID_ARG;  // never loaded
+  const int need = bits == 16 ? kPlanes : bits;
+  // the host data of every block that is gone
+  std::vector<int> missing;
+  for (int p = 0; p < need; ++p)
+    if (l->plane(e, p).st == B_NONE) {
+      for (int m = 0; m < 3; ++m)
+        if (!planes_host || !planes_host[m][p]) return PW_ERR_INVALID_ARG;
+      missing.push_back(p);
+    }
+  const bool f16_missing = bits == 16 && l->f16[e].st == B_NONE;
+  if (f16_missing)
+    for (int m = 0; m < 3; ++m)
+      if (!w16_host || !w16_host[m]) return PW_ERR_INVALID_ARG;
+
+  pw_pool_s* pool = l->pool;
+  cudaStream_t cs = as_stream(copy_stream);
+  // still-intact blocks are held (re-mapped) so that they cannot be handed out
+  // before the raise; they hold their data already
+  std::vector<Block*> held;
+  for (int p = 0; p < need; ++p)
+    if (l->plane(e, p).st == B_RECLAIM) {
+      pool->remap(l->plane(e, p));
+      held.push_back(&l->plane(e, p));
+    }
+  if (bits == 16 && l->f16[e].st == B_RECLAIM) {
+    pool->remap(l->f16[e]);
+    held.push_back(&l->f16[e]);
+  }
+  std::vector<std::vector<int>> pages(missing.size() + 1);
+  size_t taken = 0;
+  for (size_t i = 0; i < missing.size(); ++i, ++taken)
+    if (pool->take_pages(l->pmax, &pages[i]) != PW_OK) break;
+  bool ok = taken == missing.size();
+  if (ok && f16_missing) ok = pool->take_pages(l->pmax16, &pages[missing.size()]) == PW_OK;
+  if (!ok) {
+    for (size_t i = 0; i < taken; ++i)
+      for (int pg : pages[i]) {
+        pool->kind[pg] = 0;
+        pool->free_pages.insert(pg);
+        pool->mapped_pages--;
+      }
+    if (!held.empty()) {  // back to the reclaim queue, releasable at once
+      std::shared_ptr<Event> ev;
+      if (make_event(cs, &ev) == PW_OK)
+        for (Block* b : held) pool->to_reclaim(*b, ev);
+    }
+    return PW_ERR_OOM;
+  }
+  if (missing.empty() && !f16_missing) return PW_OK;
+  // copies on the copy stream, then the page-table rows (entries the current
+  // bitwidth reads keep their values; kernels never read planes >= bits[e])
+  for (size_t i = 0; i < missing.size(); ++i) {
+    const int p = missing[i];
+    Block& b = l->plane(e, p);
+    b.pages = pages[i];
+    b.st = B_MAPPED;
+    for (int m = 0; m < 3; ++m)
+      PW_TRY(upload_tiles(l, b, l->tmap, m, reinterpret_cast<const char*>(planes_host[m][p]),
+                          2 * (size_t)l->C[m], cs));
+    for (int v = 0; v < l->pmax; ++v)
+      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] =
+          reinterpret_cast<unsigned long long>(pool->page_addr(b.pages[v]));
+  }
+  if (f16_missing) {
+    Block& b = l->f16[e];
+    b.pages = pages[missing.size()];
+    b.st = B_MAPPED;
+    for (int m = 0; m < 3; ++m)
+      PW_TRY(upload_tiles(l, b, l->tmap16, m, reinterpret_cast<const char*>(w16_host[m]), 32 * (size_t)l->C[m],
+                          cs));
+    for (int v = 0; v < l->pmax16; ++v)
+      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(pool->page_addr(b.pages[v]));
+  }
+  PW_TRY(upload_pt_rows(l, e, cs));
+  std::shared_ptr<Event> ready;
+  PW_TRY(make_event(cs, &ready));
+  for (int p : missing) l->plane(e, p).ready = ready;
+  if (f16_missing) l->f16[e].ready = ready;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_raise_expert_async(pw_layer_t l, int e, int bits, const uint32_t* const planes_host[3][6],
+                                           const uint16_t* const w16_host[3], void* copy_stream, void* stream) {
+  PW_TRY(check_layer(l));
+  if (e < 0 || e >= l->desc.n_experts || !valid_bits(bits)) return PW_ERR_INVALID_ARG;
+  const int cur = l->bits[e];
+  if (cur == 0) return PW_ERR_INVALID_ARG;
+  const int have = cur == 16 ? kPlanes : cur;
+  if (bits == cur || (bits != 16 && bits <= have)) return PW_ERR_INVALID_ARG;  // not a raise
+  PW_TRY(pw_prefetch_expert(l, e, bits, planes_host, w16_host, copy_stream));
+  return pw_set_expert_bitwidth(l, e, bits, stream);
 }
 
 extern "C" pw_status pw_get_expert_bitwidth(pw_layer_t l, int e, int* bits) {

@@ -341,6 +341,8 @@ def run_gpu(args):
     barrier()
     e2e_s = max_over_ranks(time.perf_counter() - te)
 
+    paging = measure_paging(wl, stream, args.paging) if args.paging > 0 else None
+
     peaks = _load_json(os.path.join(ROOT, "MEASURED_PEAKS.json"))
     if peaks and peaks.get("hbm_gbs"):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
@@ -421,6 +423,8 @@ def run_gpu(args):
             "gpu_launches": launches_per_step * K,
             "clocks": clk,
         }
+        if paging is not None:
+            out["config"]["paging"] = paging
     for L in layers:
         L.destroy()
     wl["pool"].close()
@@ -666,6 +670,73 @@ def sweep_cpu_baseline(sw, seconds=20.0):
                       f"to the 32 layers ({per_layer:.1f} s per token-layer, numpy fp64)"}
 
 
+def measure_paging(wl, stream, n_steps):
+    """Decode throughput while precision is raised in the background (the
+    pages' asynchronous paging, write-up section 安全边界与异步搬运).  Every
+    step, on the step's layer copy: the expert raised at the copy's previous
+    visit goes back to 3 bits, the expert prefetched then is raised to 6 bits
+    (pw_set_expert_bitwidth: the commit, in stream order), and the next 3-bit
+    expert's three missing planes are uploaded from pinned host memory on a
+    copy stream (pw_prefetch_expert), to be committed at the next visit.
+    Eager steps with and without the paging, same routing."""
+    import torch
+
+    import any_precision_expert_gb300 as pw
+
+    layers, bufs, xs_d, T = wl["layers"], wl["bufs"], wl["xs_d"], wl["T"]
+    NL = len(layers)
+    three = [e for e in range(len(wl["bits"])) if int(wl["bits"][e]) == 3]
+    n_steps = min(n_steps, (len(three) - 1) * NL)
+    hold = {}
+
+    def planes_of(e):
+        if e not in hold:
+            hold[e] = [[torch.from_numpy(q).pin_memory() if p >= 3 else None
+                        for p, q in enumerate(pw.pack_planes(wl["experts"][e]["code6"][m]))] for m in range(3)]
+        return hold[e]
+
+    for e in three:
+        planes_of(e)
+    copy = torch.cuda.Stream()
+
+    def run(with_paging):
+        raised, fetched = {}, {}
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(n_steps):
+                j = i % NL
+                if with_paging:
+                    if j in raised:
+                        layers[j].set_expert_bitwidth(raised.pop(j), 3, stream=stream)
+                    if j in fetched:
+                        e = fetched.pop(j)
+                        layers[j].set_expert_bitwidth(e, 6, stream=stream)
+                        raised[j] = e
+                    e = three[(i // NL) % len(three)]
+                    layers[j].prefetch_expert(e, 6, planes=planes_of(e), copy_stream=copy)
+                    fetched[j] = e
+                pw.moe_forward(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+            t1.record(stream)
+        torch.cuda.synchronize()
+        for j, e in list(raised.items()) + list(fetched.items()):
+            layers[j].set_expert_bitwidth(e, 6, stream=stream)   # commit any pending prefetch first
+            layers[j].set_expert_bitwidth(e, 3, stream=stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    run(False)  # warm-up
+    base_ms = run(False)
+    pag_ms = run(True)
+    upload = 3 * 3 * (wl["cfg"].d * wl["cfg"].f // 8)
+    return {"steps": n_steps, "tokens_per_s_without": T * n_steps / (base_ms * 1e-3),
+            "tokens_per_s_with": T * n_steps / (pag_ms * 1e-3),
+            "loss_pct": 100.0 * (1.0 - base_ms / pag_ms), "upload_bytes_per_step": upload,
+            "note": "eager steps (no graph); per step one lower, one raise committing the previous visit's "
+                    "prefetch, one prefetch (three planes uploaded on a copy stream)"}
+
 def _traffic_from_profile(workload, T):
     """DRAM bytes per FFN call from the committed ncu summary, if it matches the current kernel."""
     prof = _load_json(os.path.join(ROOT, "profiles", f"ffn_traffic_{workload}_T{T}.json"))
@@ -770,6 +841,8 @@ def main():
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load for the clock record")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--paging", type=int, default=0,
+                    help="steps of the async-paging measurement (0: skip)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
     if args.tokens is None:

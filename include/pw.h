@@ -241,6 +241,41 @@ pw_status pw_combine(pw_layer_t layer, const float* y_perm, const int32_t* inv_s
  */
 pw_status pw_set_expert_bitwidth(pw_layer_t layer, int e, int bits, void* stream);
 
+/*
+ * Bring back the blocks expert e needs at `bits` without changing its
+ * bitwidth yet (write-up "安全边界与异步搬运": planes move in the background
+ * and the change commits later at a safe boundary).  Blocks still on the
+ * reclaim queue are taken off it (their data is intact).  Blocks that are
+ * gone get free pages (or reclaimable ones whose safe boundary has passed;
+ * the call waits for it if it must) and their data is copied from host
+ * memory on `copy_stream`, followed by the expert's page-table rows (entries
+ * of the planes the current bitwidth reads keep their values; kernels never
+ * read planes at or above it).  A later pw_set_expert_bitwidth raise on any
+ * stream waits for these copies before it commits.
+ *   planes_host[m][p]  plane p of matrix m as packed by pw_pack_planes
+ *                      (uint32 [R*C/32]); read for the missing planes only
+ *                      (others may be NULL; the whole array may be NULL when
+ *                      nothing is missing)
+ *   w16_host[m]        fp16 page of matrix m as packed by pw_pack_f16; read
+ *                      when bits == 16 and the fp16 block is missing
+ * Host buffers should be pinned for the copies to be asynchronous, and must
+ * stay valid until they complete.  PW_ERR_INVALID_ARG when a needed host
+ * array is NULL; PW_ERR_OOM (no change) when the pool has no room.
+ */
+pw_status pw_prefetch_expert(pw_layer_t layer, int e, int bits, const uint32_t* const planes_host[3][6],
+                             const uint16_t* const w16_host[3], void* copy_stream);
+
+/*
+ * pw_prefetch_expert followed by the raise pw_set_expert_bitwidth(e, bits,
+ * stream): `stream` waits for the copies and then writes the bitwidth word,
+ * so kernels enqueued on `stream` after this call read the new bitwidth and
+ * kernels enqueued before it keep the old one.  bits must be above the
+ * current bitwidth (16 above 6; PW_ERR_INVALID_ARG otherwise).  To keep the
+ * wait off the compute stream, prefetch a step ahead and raise later.
+ */
+pw_status pw_raise_expert_async(pw_layer_t layer, int e, int bits, const uint32_t* const planes_host[3][6],
+                                const uint16_t* const w16_host[3], void* copy_stream, void* stream);
+
 /* Host mirror of an expert's current bitwidth (0 if not loaded). */
 pw_status pw_get_expert_bitwidth(pw_layer_t layer, int e, int* bits);
 

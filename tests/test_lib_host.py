@@ -253,3 +253,60 @@ def test_copy_expert_between_layers(sim):
         L.destroy()
     assert pool.stats()["free_pages"] == pool.stats()["total_pages"]
     pool.close()
+
+
+def test_raise_async_uploads_missing_planes_only(sim):
+    pool = pw.Pool(64 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool)
+    ex = _expert(3)
+    _load(layer, 1, 3, ex)
+    packed = [pw.pack_planes(ex["code6"][m]) for m in range(3)]
+    with pytest.raises(pw.PwError):                      # planes 3, 4 are gone and none were given
+        layer.raise_expert_async(1, 5, stream=0, copy_stream=0)
+    layer.raise_expert_async(1, 5, planes=packed, stream=0, copy_stream=0)
+    assert layer.get_expert_bitwidth(1) == 5
+    for p in range(5):
+        addr = layer.page_address(1, p, 0)
+        got = _page_bytes(pool, addr, packed[0][p].nbytes).view(np.uint32)
+        assert np.array_equal(got, packed[0][p])        # gate tiles at the start of the block
+        got = _page_bytes(pool, addr + 2 * packed[0][p].nbytes, packed[2][p].nbytes).view(np.uint32)
+        assert np.array_equal(got, packed[2][p])        # down follows gate and up
+    addrs = [layer.page_address(1, p, 0) for p in range(5)]
+    layer.set_expert_bitwidth(1, 3, stream=0)
+    layer.raise_expert_async(1, 5, stream=0, copy_stream=0)  # still reclaimable: re-mapped, nothing copied
+    assert [layer.page_address(1, p, 0) for p in range(5)] == addrs
+    with pytest.raises(pw.PwError):
+        layer.raise_expert_async(1, 4, stream=0, copy_stream=0)  # not a raise
+    with pytest.raises(pw.PwError):
+        layer.raise_expert_async(1, 16, planes=packed, stream=0, copy_stream=0)  # fp16 page missing
+    w16 = [pw.pack_f16(m) for m in _expert(3, w16=True)["w16"]]
+    layer.raise_expert_async(1, 16, planes=packed, w16=w16, stream=0, copy_stream=0)
+    assert layer.get_expert_bitwidth(1) == 16
+    got = _page_bytes(pool, layer.page_address(1, 6, 0), w16[0].nbytes).view(np.uint16)
+    assert np.array_equal(got, w16[0])
+    layer.destroy()
+    assert pool.stats()["free_pages"] == pool.stats()["total_pages"]
+    pool.close()
+
+
+def test_prefetch_then_raise(sim):
+    pool = pw.Pool(64 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool)
+    ex = _expert(4)
+    _load(layer, 0, 3, ex)
+    packed = [pw.pack_planes(ex["code6"][m]) for m in range(3)]
+    assert layer.try_set_expert_bitwidth(0, 6) == 4          # planes 3..5 are not resident
+    layer.prefetch_expert(0, 6, planes=packed, copy_stream=0)
+    assert layer.get_expert_bitwidth(0) == 3                 # nothing committed yet
+    got = _page_bytes(pool, layer.page_address(0, 5, 0), packed[0][5].nbytes).view(np.uint32)
+    assert np.array_equal(got, packed[0][5])
+    layer.set_expert_bitwidth(0, 6, stream=0)                # the commit
+    assert layer.get_expert_bitwidth(0) == 6
+    layer.set_expert_bitwidth(0, 3, stream=0)                # lower: planes 3..5 reclaimable again
+    assert pool.stats()["reclaimable_pages"] == 3
+    layer.prefetch_expert(0, 5, copy_stream=0)               # held off the reclaim queue, no data needed
+    assert pool.stats()["reclaimable_pages"] == 1
+    layer.set_expert_bitwidth(0, 5, stream=0)
+    assert layer.get_expert_bitwidth(0) == 5
+    layer.destroy()
+    pool.close()

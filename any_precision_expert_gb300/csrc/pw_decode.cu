@@ -319,29 +319,36 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
           w[p][1] = v.y;
         }
         const int nch = (cb >> 1) < GR ? 2 : min(2, rem - 2 * (cb & 1));
-        // the two chunks share one copy of the code (instruction-cache footprint)
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          if (c < nch) {
-            uint32_t wc[B];
+        auto chunk = [&](int c) {
+          uint32_t wc[B];
 #pragma unroll
-            for (int p = 0; p < B; ++p) wc[p] = c ? w[p][1] : w[p][0];
-            // decode the chunk's four steps first (independent chains), then the mma's
-            uint32_t a[4][4];
+          for (int p = 0; p < B; ++p) wc[p] = c ? w[p][1] : w[p][0];
+          // decode the chunk's four steps first (independent chains), then the mma's
+          uint32_t a[4][4];
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3[m], a[s]);
-              else decode_step_tab<B>(wc, s, tab, m * 128 + lane * 4, a[s]);
-            }
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              uint32_t bf[G::NTM][2];
-              slab_bstep<G>(buf, kc0 + c * 64, s, NT, bf);
-#pragma unroll
-              for (int nt = 0; nt < G::NTM; ++nt)
-                if (nt < NT) mma16816(acc[m][nt], a[s], bf[nt][0], bf[nt][1]);
-            }
+          for (int s = 0; s < 4; ++s) {
+            if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3[m], a[s]);
+            else decode_step_tab<B>(wc, s, tab, m * 128 + lane * 4, a[s]);
           }
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            uint32_t bf[G::NTM][2];
+            slab_bstep<G>(buf, kc0 + c * 64, s, NT, bf);
+#pragma unroll
+            for (int nt = 0; nt < G::NTM; ++nt)
+              if (nt < NT) mma16816(acc[m][nt], a[s], bf[nt][0], bf[nt][1]);
+          }
+        };
+        if constexpr (B == 3) {
+          // register-LUT decode is short: both chunks unrolled (eight independent chains)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            if (c < nch) chunk(c);
+        } else {
+          // table lookups: the two chunks share one copy of the code (instruction-cache footprint)
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c)
+            if (c < nch) chunk(c);
         }
       }
     };

@@ -1,6 +1,6 @@
 // Persistent decode-side expert FFN: gate/up and down for every routed expert
 // with few tokens (3, 4, 5, 6 bits or its fp16 page) and for the fp16 shared
-// FFN, in at most two launches (one for 4..6-bit experts, one for the rest).
+// FFN, in one launch.
 //
 // PagedWeight (write-up "内存的饥饿游戏", section 核心洞察): an expert at
 // bitwidth b streams only its top b bit-planes, found through the per-expert
@@ -8,26 +8,30 @@
 // streams its fp16 page.  Decode batches route a few tokens to each expert, so
 // the time goes into streaming weights.
 //
-// A CTA (four warps) takes one work item at a time and stages the item's
-// token rows (up to 32) once into shared memory (K-blocks of 384 columns,
-// double-buffered, rows XOR-swizzled for conflict-free ldmatrix).  Weights
-// stream through per-warp cp.async rings addressed through the page table.
-// Item shapes:
-//  - block item (3-bit experts, fp16 pages, shared FFN): (group, phase,
-//    32-token chunk, four 16-row tiles), one tile per warp over the whole
-//    reduction.  3-bit codes are decoded with byte permutes from register
-//    LUTs.
-//  - split item (4, 5, 6-bit experts, own launch): (group, phase, 32-token
-//    chunk, one tile); warps 0-1 stream gate and 2-3 up (all four for down)
-//    over interleaved 128-column units and look codes up in one CTA-wide LUT
-//    table (per-lane copies of the row pair g / g+8, so no bank conflicts).
+// A CTA (four warps) takes one work item at a time: (group, phase, 32-token
+// chunk, two gate/up tiles or one to four down tiles).  It stages the item's
+// distinct token rows once into shared memory (double-buffered K-blocks of
+// 256 columns, or 512 / 1024 for one or two token tiles; rows XOR-swizzled
+// for conflict-free ldmatrix), and every warp streams one matrix of one
+// 16-row tile through its own cp.async ring, addressed through the page table
+// (gate/up: warps 0-1 the gate rows of the two tiles, warps 2-3 their up rows,
+// which reach the gate warps through shared memory for SwiGLU).  Down items of
+// groups with few tokens and a long reduction split each tile's reduction over
+// two or four warps (interleaved units, partial sums added in warp order), so
+// that their chains stay short.  Codes become weights by
+//  - 3 bits: byte permutes from register LUTs (whole plane groups, 16 B per
+//    lane and plane);
+//  - 4, 5, 6 bits: lookups in the warp's LUT table in shared memory (row
+//    pair g / g+8 per 32-bit entry); one code path for the three bitwidths;
+//  - fp16 pages: stored in mma fragment order, used as they are.
 // The weights feed mma.sync m16n8k16 (weights as A, tokens as B, fp32
 // accumulation).  Gate/up writes h = silu(g) * u in fp16, down writes y in
-// fp32.
+// fp32.  Each weight kind has a single copy of its loop body (the kernel's
+// instruction footprint stays small).
 //
-// CTAs of a launch claim items from one counter in a fixed order: every gate/up item
+// CTAs claim items from one counter in a fixed order: every gate/up item
 // (phase 0) before every down item (phase 1); inside a phase the shared FFN
-// first, then fp16, 3-bit and 4..6-bit experts.  A down item waits until all
+// first, then fp16, 4..6-bit and 3-bit experts.  A down item waits until all
 // gate/up tiles of its (group, chunk) are done; those items were claimed
 // earlier by running CTAs and never wait, so every wait ends.  The waits are
 // bounded anyway: past the limit the kernel records a timeout in the layer's
@@ -37,45 +41,42 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include <type_traits>
-
 #include "pw_gemv.cuh"
 
 namespace pw {
 
 constexpr int kCtaThreads = 128;
-constexpr int kCtaWarps = kCtaThreads / 32;           // tiles of a block item
-constexpr int kTabBytes = 64 * 256;                   // LUT table of a split item (b <= 6, two matrices)
-constexpr long long kSpinLimit = 1ll << 22;           // polls of a phase counter (about a second)
+constexpr int kCtaWarps = kCtaThreads / 32;
+constexpr int kTabW = 64 * 8 * 4;            // LUT table of one warp: 2^b entries x 8 row pairs x 4 B (b <= 6)
+constexpr long long kSpinLimit = 1ll << 22;  // polls of a phase counter (about a second)
 
-// Geometry of the two kernels: items take up to 32 tokens (a weight tile is
-// streamed and decoded once for up to 32 tokens).  The 3-bit / fp16 kernel
-// stages 256-column K-blocks and runs three CTAs per SM (at most 168
-// registers a thread); the 4..6-bit kernel stages 384-column K-blocks, holds
-// a LUT table and runs two.
-template <bool SPLIT>
+// Items take up to 32 tokens (a weight tile is streamed and decoded once for
+// up to 32 tokens).  Shared memory: two K-block buffers of token rows, a LUT
+// table and a weight ring per warp; three CTAs per SM.
 struct Geo {
-  static constexpr int TOK = 32;                          // tokens per item
-  static constexpr int NTM = TOK / 8;                     // mma n-tiles per item
-  static constexpr int SCOLS = SPLIT ? 384 : 256;         // columns of one staged K-block
-  static constexpr int HALF = TOK * SCOLS * 2;            // bytes of one K-block buffer
-  static constexpr int RB = SPLIT ? 10 * 1024 : 9 * 1024;  // cp.async weight ring of one warp
-  static constexpr int BLOCKS = SPLIT ? 2 : 3;            // CTAs per SM
-  static constexpr int SMEM = 2 * HALF + (SPLIT ? kTabBytes : 0) + kCtaWarps * RB;
+  static constexpr int TOK = 32;                // tokens per item
+  static constexpr int NTM = TOK / 8;           // mma n-tiles per item
+  static constexpr int SCOLS = 256;             // columns of one staged K-block at 32 tokens
+  static constexpr int HALF = TOK * SCOLS * 2;  // bytes of one K-block buffer
+  static constexpr int RB = 7 * 1024;           // cp.async weight ring of one warp
+  static constexpr int BLOCKS = 3;              // CTAs per SM
+  static constexpr int SMEM = 2 * HALF + kCtaWarps * (kTabW + RB);
 };
 
-// Weight units streamed by a warp: one matrix of
-//   KIND_F16: one fp16 chunk (64 columns), 4 x 16 B per lane;
-//   KIND_PB: half a plane group (2 chunks, 128 columns) of B-bit words, 8 B per lane and plane.
-enum { KIND_F16 = 1, KIND_PB = 2 };
+// Weight units streamed by a warp (one matrix of its tile):
+//   KIND_F16: 32 columns of the fp16 page, 2 x 16 B per lane;
+//   KIND_PB: half a plane group (2 chunks, 128 columns), 8 B per lane and plane (ring slots sized for 6 planes);
+//   KIND_PG: a whole plane group (4 chunks, 256 columns), 16 B per lane and plane.
+enum { KIND_F16 = 1, KIND_PB = 2, KIND_PG = 3 };
 
-template <int KIND, int B, int RB>
+template <int KIND, int B>
 struct Unit {
-  static constexpr int COLS = KIND == KIND_F16 ? 64 : 128;
-  static constexpr int LANE_BYTES = KIND == KIND_F16 ? 4 * 16 : B * 8;
+  static constexpr int COLS = KIND == KIND_F16 ? 32 : KIND == KIND_PB ? 128 : 256;
+  static constexpr int LANE_BYTES = KIND == KIND_F16 ? 2 * 16 : KIND == KIND_PB ? kPlanes * 8 : B * 16;
   static constexpr int SLOT = LANE_BYTES * 32;
-  static constexpr int R = RB / SLOT > 8 ? 8 : RB / SLOT;  // ring depth
-  static_assert(RB / SLOT >= 3, "ring too shallow");
+  static constexpr int R = Geo::RB / SLOT > 8 ? 8 : Geo::RB / SLOT;  // ring depth
+  static_assert(Geo::RB / SLOT >= 3, "ring too shallow");
+  static_assert(Geo::SCOLS % COLS == 0, "units must not straddle K-blocks");
 };
 
 struct UniParams {
@@ -108,6 +109,10 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Wait until at most n (clamped to 7) of this thread's newest cp.async groups are pending.
 __device__ __forceinline__ void cp_wait_dyn(int n) {
   switch (n < 7 ? n : 7) {
@@ -128,140 +133,165 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
-// Byte offset of 16-byte piece j (8 columns) of token row r in a staged K-block.
-template <class G>
-__device__ __forceinline__ uint32_t slab_off(int r, int j) {
-  return (uint32_t)(r * (G::SCOLS * 2) + ((j ^ (r & 7)) << 4));
+// log2 of the columns of one staged K-block for NT token tiles: the buffer
+// holds 32 rows of 256 columns, 16 rows of 512 or 8 rows of 1024.
+__device__ __forceinline__ int kblock_log2(int NT) { return NT == 1 ? 10 : NT == 2 ? 9 : 8; }
+static_assert(Geo::SCOLS == 256, "kblock_log2 assumes 256-column K-blocks at 32 tokens");
+
+// Byte offset of 16-byte piece j (8 columns) of token row r in a staged
+// K-block whose rows are rs bytes apart.
+__device__ __forceinline__ uint32_t slab_off(int r, int j, int rs) {
+  return (uint32_t)(r * rs + ((j ^ (r & 7)) << 4));
 }
 
-// Copy K-block kb of the item's token rows into a slab buffer (all threads).
-template <class G>
-__device__ __forceinline__ void stage_kblock(const __half* act, const int* s_tok, int rows, int K, int kb,
+// Copy K-block kb (kbw columns) of the item's srows distinct token rows into
+// a slab buffer (all threads).
+__device__ __forceinline__ void stage_kblock(const __half* act, const int* s_tok, int srows, int K, int kb, int kbw,
                                              uint32_t buf) {
-  const int c0 = kb * G::SCOLS;
-  const int ppr = min(G::SCOLS, K - c0) >> 3;  // 16-byte pieces per row
-  const int n = rows * ppr;
+  const int c0 = kb * kbw;
+  const int ppr = min(kbw, K - c0) >> 3;  // 16-byte pieces per row
+  const int n = srows * ppr;
   for (int p = threadIdx.x; p < n; p += kCtaThreads) {
     const int r = p / ppr, j = p - r * ppr;
-    cp_async16(buf + slab_off<G>(r, j), act + (size_t)s_tok[r] * K + c0 + j * 8);
+    cp_async16(buf + slab_off(r, j, kbw * 2), act + (size_t)s_tok[r] * K + c0 + j * 8);
   }
 }
 
 // B fragments of mma step s (16 columns at column kc + 16 s of its K-block)
 // for the n-tiles: one ldmatrix.x4 per pair of n-tiles (b0, b1 of each).
-// Rows past the item's tokens hold stale data; their n-tiles are not used.
-template <class G>
-__device__ __forceinline__ void slab_bstep(uint32_t buf, int kc, int s, int NT, uint32_t (&bf)[G::NTM][2]) {
+// Token rows past the staged ones read the last staged row; their results
+// are not stored.
+__device__ __forceinline__ void slab_bstep(uint32_t buf, int kc, int s, int NT, int srows, int rs,
+                                           uint32_t (&bf)[Geo::NTM][2]) {
   const int lane = threadIdx.x & 31;
   const int mat = lane >> 3;
   const int j = (kc >> 3) + 2 * s + (mat & 1);
 #pragma unroll
-  for (int nt0 = 0; nt0 < G::NTM; nt0 += 2) {
+  for (int nt0 = 0; nt0 < Geo::NTM; nt0 += 2) {
     if (nt0 < NT) {
-      const int r = (nt0 + (mat >> 1)) * 8 + (lane & 7);
-      ldsm_x4(buf + slab_off<G>(r, j), bf[nt0][0], bf[nt0][1], bf[nt0 + 1][0], bf[nt0 + 1][1]);
+      const int r = min((nt0 + (mat >> 1)) * 8 + (lane & 7), srows - 1);
+      ldsm_x4(buf + slab_off(r, j, rs), bf[nt0][0], bf[nt0][1], bf[nt0 + 1][0], bf[nt0 + 1][1]);
     }
   }
 }
 
-// Decode mma step s of one chunk of B-bit codes into the A fragment through
-// the CTA's LUT table: entry (v, matrix m, lane) at byte v*256 + m*128 +
-// 4*lane holds LUT[row g][v] in its low and LUT[row g+8][v] in its high half
-// (g = lane / 4).  lbm = m*128 + 4*lane.  Plane masking as in decode_step_lut.
-template <int B>
-__device__ __forceinline__ void decode_step_tab(const uint32_t (&w)[B], const int s, uint32_t tab, uint32_t lbm,
-                                                uint32_t (&a)[4]) {
+__device__ __forceinline__ void mma_tiles(float (&acc)[Geo::NTM][4], const uint32_t (&a)[4],
+                                          const uint32_t (&bf)[Geo::NTM][2], int NT) {
+#pragma unroll
+  for (int nt = 0; nt < Geo::NTM; ++nt)
+    if (nt < NT) mma16816(acc[nt], a, bf[nt][0], bf[nt][1]);
+}
+
+// Decode mma step s of one chunk of nb-bit codes (nb = 4..6) into the A
+// fragment through the warp's LUT table: entry (v, g) at byte 32 v + 4 g holds
+// LUT[row g][v] in its low and LUT[row g+8][v] in its high half; tabg = table
+// + 4 g (g = lane / 4).  Plane p keeps code bit nb-1-p of weight (h, s, byte
+// k) at bit 8k + 4h + s + 5 - p (mod 32): masking one bit per byte and
+// rotating right by 4h + s + 6 - nb leaves the codes of R[h] in the low nb
+// bits of its bytes.
+__device__ __forceinline__ void decode_step_rt(const uint32_t (&w)[kPlanes], int nb, const int s, uint32_t tabg,
+                                               uint32_t (&a)[4]) {
   uint32_t R[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t m = 0;
 #pragma unroll
-    for (int p = 0; p < B; ++p) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
-    R[h] = rotr(m, 4 * h + s + 6 - B);
+    for (int p = 0; p < kPlanes; ++p)
+      if (p < nb) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
+    R[h] = rotr(m, 4 * h + s + 6 - nb);
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {  // k = 2 * rowsel + colhalf
-    const uint32_t sel = 0x5504u | ((uint32_t)k << 4);
-    const uint32_t e0 = lds32(tab + prmt(R[0], lbm, sel));
-    const uint32_t e1 = lds32(tab + prmt(R[1], lbm, sel));
+    const uint32_t e0 = lds32(tabg + (prmt(R[0], 0u, 0x4440u | (uint32_t)k) << 5));
+    const uint32_t e1 = lds32(tabg + (prmt(R[1], 0u, 0x4440u | (uint32_t)k) << 5));
     const int reg = (k == 0) ? 0 : (k == 1) ? 2 : (k == 2) ? 1 : 3;
     a[reg] = prmt(e0, e1, (k >> 1) ? 0x7632u : 0x5410u);
   }
 }
 
-// LUT table of a split item: both matrices of tile tau at bitwidth B.
-template <int B, int NM>
-__device__ __forceinline__ void build_tab(const DevLayer& L, int e, int tau, unsigned char* tab) {
-  constexpr int V = 1 << B;
-  constexpr int RUNS = V / 8;  // 8-entry runs per LUT row
-  constexpr int UNITS = NM * 8 * RUNS;
-  for (int u = threadIdx.x; u < UNITS; u += kCtaThreads) {
-    const int mi = u / (8 * RUNS), g = (u / RUNS) % 8, v0 = (u % RUNS) * 8;
-    const __half* lr = lut_rows(L, e, NM == 2 ? mi : 2, B, tau * kTileRows);
+// The warp's LUT table for one 16-row tile at bitwidth b (4..6): lr = the
+// tile's LUT_b rows (16 x 2^b fp16, row-major).
+__device__ __forceinline__ void build_tab_warp(const __half* lr, int b, uint32_t tab) {
+  const int V = 1 << b, lane = threadIdx.x & 31;
+  for (int i = lane; i < V; i += 32) {  // (row pair g, run of 8 entries from v0)
+    const int g = i & 7, v0 = (i >> 3) * 8;
     const uint4 lo = *reinterpret_cast<const uint4*>(lr + g * V + v0);
     const uint4 hi = *reinterpret_cast<const uint4*>(lr + (g + 8) * V + v0);
     const uint32_t l4[4] = {lo.x, lo.y, lo.z, lo.w}, h4[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t pair = prmt(l4[i >> 1], h4[i >> 1], (i & 1) ? 0x7632u : 0x5410u);
-      *reinterpret_cast<uint4*>(tab + (v0 + i) * 256 + mi * 128 + g * 16) = make_uint4(pair, pair, pair, pair);
-    }
+    for (int j = 0; j < 8; ++j)
+      sts32(tab + ((v0 + j) * 8 + g) * 4, prmt(l4[j >> 1], h4[j >> 1], (j & 1) ? 0x7632u : 0x5410u));
   }
+  __syncwarp();
 }
 
 // Weight sources of one warp's K loop.
-template <int NM>
 struct WSrc {
-  const char* p[NM][6];  // plane tiles (KIND_PB) or the fp16 tile in p[m][0]
-  uint32_t lut3[NM][2][4];
+  const char* p[kPlanes];  // plane tiles, or the fp16 tile in p[0]
+  uint32_t lut3[2][4];     // 3 bits: register LUTs of rows g and g + 8
+  int nb;                  // 4..6 bits: planes streamed
+  uint32_t tabg;           // 4..6 bits: the warp's LUT table + 4 g
 };
 
-// K loop of one warp: units u = u0, u0 + ustride, ... of one tile (unit u =
-// (column block u / NM, matrix u % NM)).  Every warp of the CTA runs it for
-// the same item and passes the same K-block barriers; the token rows of
-// K-block kb are staged at the start of K-block kb - 1.
-template <class G, int KIND, int B, int NM>
-__device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0, int ustride, uint32_t ring,
-                                      uint32_t slab, uint32_t tab, const __half* act, const int* s_tok,
-                                      float (&acc)[NM][G::NTM][4]) {
-  using U = Unit<KIND, B, G::RB>;
-  static_assert(G::SCOLS % U::COLS == 0, "units must not straddle K-blocks");
+// K loop of one warp over the units cb = u0, u0 + us, ... of its tile (unit
+// cb = columns cb * COLS ...).  Every warp of the CTA runs it for the same
+// item and passes the same K-block barriers; the ntok distinct token rows of
+// K-block kb are staged at the start of K-block kb - 1.  B: 16 (fp16), 3, or
+// 0 (4..6 bits, src.nb).  pre() runs once the first weight units are in flight.
+template <int KIND, int B, class Pre>
+__device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, int u0, int us, uint32_t ring,
+                                      uint32_t slab, const __half* act, const int* s_tok,
+                                      float (&acc)[Geo::NTM][4], Pre&& pre) {
+  using G = Geo;
+  using U = Unit<KIND, B>;
   constexpr int R = U::R;
   const int lane = threadIdx.x & 31;
-  const int rows = NT * 8;
+  const int lkb = kblock_log2(NT), kbw = 1 << lkb, rs = kbw * 2;
   const int nk = K / 64, GR = nk / 4, rem = nk % 4;
-  const int ncb = (K + U::COLS - 1) / U::COLS;  // column blocks
-  const int nu = ncb * NM;
-  const int mine = u0 < nu ? (nu - u0 + ustride - 1) / ustride : 0;
-  const int kbs = (K + G::SCOLS - 1) / G::SCOLS;
+  const int nu = (K + U::COLS - 1) / U::COLS;
+  const int mine = u0 < nu ? (nu - u0 + us - 1) / us : 0;
+  const int kbs = (K + kbw - 1) / kbw;
+  const int nb = B == 0 ? src.nb : B;
 
   auto issue = [&](int i) {
-    const int u = u0 + i * ustride, cb = u / NM, mi = u % NM;
+    const int cb = u0 + i * us;
     const uint32_t slot = ring + (i % R) * U::SLOT;
-    const char* const* pp = (NM == 1 || mi == 0) ? src.p[0] : src.p[NM - 1];
     if constexpr (KIND == KIND_F16) {
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
-        cp_async16(slot + (s * 32 + lane) * 16, pp[0] + ((size_t)(cb * 4 + s) * 32 + lane) * 16);
+      for (int s = 0; s < 2; ++s)
+        cp_async16(slot + (s * 32 + lane) * 16, src.p[0] + ((size_t)(cb * 2 + s) * 32 + lane) * 16);
+    } else if constexpr (KIND == KIND_PG) {
+      if (cb < GR) {
+        const size_t off = (size_t)(cb * 128 + lane * 4) * 4;
+#pragma unroll
+        for (int p = 0; p < B; ++p) cp_async16(slot + (p * 32 + lane) * 16, src.p[p] + off);
+      } else {
+        const size_t off = (size_t)(GR * 128 + lane * rem) * 4;
+#pragma unroll
+        for (int p = 0; p < B; ++p)
+          for (int k = 0; k < rem; ++k) cp_async4(slot + (p * 32 + lane) * 16 + 4 * k, src.p[p] + off + 4 * k);
+      }
     } else {
       const int gamma = cb >> 1, j = cb & 1;
       if (gamma < GR) {
         const size_t off = (size_t)(gamma * 128 + lane * 4 + 2 * j) * 4;
 #pragma unroll
-        for (int p = 0; p < B; ++p) cp_async8(slot + (p * 32 + lane) * 8, pp[p] + off);
+        for (int p = 0; p < kPlanes; ++p)
+          if (p < nb) cp_async8(slot + (p * 32 + lane) * 8, src.p[p] + off);
       } else {
         const int cnt = min(2, rem - 2 * j);
         const size_t off = (size_t)(GR * 128 + lane * rem + 2 * j) * 4;
 #pragma unroll
-        for (int p = 0; p < B; ++p)
-          for (int k = 0; k < cnt; ++k) cp_async4(slot + (p * 32 + lane) * 8 + 4 * k, pp[p] + off + 4 * k);
+        for (int p = 0; p < kPlanes; ++p)
+          if (p < nb)
+            for (int k = 0; k < cnt; ++k) cp_async4(slot + (p * 32 + lane) * 8 + 4 * k, src.p[p] + off + 4 * k);
       }
     }
   };
 
   // K-blocks 0 and 1 go with the first ring group
-  stage_kblock<G>(act, s_tok, rows, K, 0, slab);
-  if (kbs > 1) stage_kblock<G>(act, s_tok, rows, K, 1, slab + G::HALF);
+  stage_kblock(act, s_tok, ntok, K, 0, kbw, slab);
+  if (kbs > 1) stage_kblock(act, s_tok, ntok, K, 1, kbw, slab + G::HALF);
   int since_stage = 0;  // groups committed after the newest staging group
 #pragma unroll
   for (int i = 0; i < R - 1; ++i) {
@@ -269,6 +299,7 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
     cp_commit();
     if (i > 0) ++since_stage;
   }
+  pre();
   int kb_cur = -1;
   auto advance_to = [&](int kb) {
     while (kb_cur < kb) {
@@ -276,7 +307,7 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
       cp_wait_dyn(since_stage);  // this thread's copies of K-block kb_cur have landed
       __syncthreads();           // ... and everyone's; K-block kb_cur - 1 is no longer read
       if (kb_cur >= 1 && kb_cur + 1 < kbs) {
-        stage_kblock<G>(act, s_tok, rows, K, kb_cur + 1, slab + ((kb_cur + 1) & 1) * G::HALF);
+        stage_kblock(act, s_tok, ntok, K, kb_cur + 1, kbw, slab + ((kb_cur + 1) & 1) * G::HALF);
         cp_commit();
         since_stage = 0;
       }
@@ -288,94 +319,105 @@ __device__ __forceinline__ void kloop(const WSrc<NM>& src, int K, int NT, int u0
     if (i + R - 1 < mine) issue(i + R - 1);
     cp_commit();
     ++since_stage;
-    const int u = u0 + i * ustride, cb = u / NM, mi = u % NM;
-    const int kb = (cb * U::COLS) / G::SCOLS;
+    const int cb = u0 + i * us;
+    const int kb = (cb * U::COLS) >> lkb;
     advance_to(kb);
-    cp_wait<R - 1>();  // unit i has landed
+    cp_wait<R - 1>();  // unit cb has landed
     const uint32_t buf = slab + (kb & 1) * G::HALF;
-    const int kc0 = (cb * U::COLS) % G::SCOLS;
+    const int kc0 = (cb * U::COLS) & (kbw - 1);
     const uint32_t slot = ring + (i % R) * U::SLOT;
-    // the matrix is fixed for the whole unit: branch once, then fully
-    // unrolled chunks of independent decode + mma chains
-    auto compute = [&](auto tag) {
-      constexpr int m = decltype(tag)::value;
-      if constexpr (KIND == KIND_F16) {
+    if constexpr (KIND == KIND_F16) {
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          uint32_t bf[G::NTM][2];
-          slab_bstep<G>(buf, kc0, s, NT, bf);
-          const uint4 v = lds128(slot + (s * 32 + lane) * 16);
-          const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+      for (int s = 0; s < 2; ++s) {
+        uint32_t bf[G::NTM][2];
+        slab_bstep(buf, kc0, s, NT, ntok, rs, bf);
+        const uint4 v = lds128(slot + (s * 32 + lane) * 16);
+        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+        mma_tiles(acc, a, bf, NT);
+      }
+    } else {
+      constexpr int W = KIND == KIND_PG ? 4 : 2;  // words (chunks) per lane and plane
+      constexpr int NP = KIND == KIND_PG ? B : kPlanes;
+      uint32_t w[NP][W];
 #pragma unroll
-          for (int nt = 0; nt < G::NTM; ++nt)
-            if (nt < NT) mma16816(acc[m][nt], a, bf[nt][0], bf[nt][1]);
-        }
-      } else {
-        uint32_t w[B][2];
-#pragma unroll
-        for (int p = 0; p < B; ++p) {
-          const uint2 v = lds64(slot + (p * 32 + lane) * 8);
+      for (int p = 0; p < NP; ++p) {
+        if constexpr (W == 4) {
+          const uint4 v = lds128(slot + (p * 32 + lane) * 16);
+          w[p][0] = v.x;
+          w[p][1] = v.y;
+          w[p][2] = v.z;
+          w[p][3] = v.w;
+        } else {
+          uint2 v = make_uint2(0u, 0u);
+          if (p < nb) v = lds64(slot + (p * 32 + lane) * 8);
           w[p][0] = v.x;
           w[p][1] = v.y;
         }
-        const int nch = (cb >> 1) < GR ? 2 : min(2, rem - 2 * (cb & 1));
-        auto chunk = [&](int c) {
-          uint32_t wc[B];
-#pragma unroll
-          for (int p = 0; p < B; ++p) wc[p] = c ? w[p][1] : w[p][0];
-          // decode the chunk's four steps first (independent chains), then the mma's
-          uint32_t a[4][4];
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3[m], a[s]);
-            else decode_step_tab<B>(wc, s, tab, m * 128 + lane * 4, a[s]);
-          }
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            uint32_t bf[G::NTM][2];
-            slab_bstep<G>(buf, kc0 + c * 64, s, NT, bf);
-#pragma unroll
-            for (int nt = 0; nt < G::NTM; ++nt)
-              if (nt < NT) mma16816(acc[m][nt], a[s], bf[nt][0], bf[nt][1]);
-          }
-        };
-        if constexpr (B == 3) {
-          // register-LUT decode is short: both chunks unrolled (eight independent chains)
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-            if (c < nch) chunk(c);
-        } else {
-          // table lookups: the two chunks share one copy of the code (instruction-cache footprint)
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c)
-            if (c < nch) chunk(c);
-        }
       }
-    };
-    if (NM == 1 || mi == 0) compute(std::integral_constant<int, 0>{});
-    else compute(std::integral_constant<int, NM - 1>{});
+      const int nch = W == 4 ? (cb < GR ? 4 : rem) : (cb >> 1) < GR ? 2 : min(2, rem - 2 * (cb & 1));
+      auto chunk = [&](int c) {
+        uint32_t wc[NP];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          if constexpr (W == 4) wc[p] = c == 0 ? w[p][0] : c == 1 ? w[p][1] : c == 2 ? w[p][2] : w[p][3];
+          else wc[p] = c ? w[p][1] : w[p][0];
+        }
+        // decode the chunk's four steps first (independent chains), then the mma's
+        uint32_t a[4][4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3, a[s]);
+          else decode_step_rt(wc, nb, s, src.tabg, a[s]);
+        }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          uint32_t bf[G::NTM][2];
+          slab_bstep(buf, kc0 + c * 64, s, NT, ntok, rs, bf);
+          mma_tiles(acc, a[s], bf, NT);
+        }
+      };
+      if constexpr (B == 3) {
+        // register-LUT decode is short: the unit's chunks unrolled (independent chains)
+#pragma unroll
+        for (int c = 0; c < W; ++c)
+          if (c < nch) chunk(c);
+      } else {
+        // table lookups: the chunks share one copy of the code
+#pragma unroll 1
+        for (int c = 0; c < W; ++c)
+          if (c < nch) chunk(c);
+      }
+    }
   }
   advance_to(kbs - 1);
   cp_wait<0>();
 }
 
 // Epilogue of one tile: C fragment element (row g / g+8, token nt*8 + 2t + {0,1}).
-template <int NM, int NTM>
-__device__ __forceinline__ void tile_store(const float (&acc)[NM][NTM][4], int tau, int row0, int ntok, int ld,
-                                           __half* h, float* y) {
+// Gate/up: h = silu(gate) * up in fp16; down: y in fp32.
+__device__ __forceinline__ void tile_store_h(const float (&gt)[Geo::NTM][4], const float (&up)[Geo::NTM][4], int tau,
+                                             int row0, int ntok, int ld, __half* h) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
-  for (int nt = 0; nt < NTM; ++nt)
+  for (int nt = 0; nt < Geo::NTM; ++nt)
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int j = nt * 8 + 2 * t + (r & 1);
       const int row = tau * kTileRows + g + 8 * (r >> 1);
-      if (j < ntok) {
-        if constexpr (NM == 2)
-          h[(size_t)(row0 + j) * ld + row] = __float2half_rn(silu_f(acc[0][nt][r]) * acc[1][nt][r]);
-        else
-          y[(size_t)(row0 + j) * ld + row] = acc[0][nt][r];
-      }
+      if (j < ntok) h[(size_t)(row0 + j) * ld + row] = __float2half_rn(silu_f(gt[nt][r]) * up[nt][r]);
+    }
+}
+
+__device__ __forceinline__ void tile_store_y(const float (&acc)[Geo::NTM][4], int tau, int row0, int ntok, int ld,
+                                             float* y) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < Geo::NTM; ++nt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = nt * 8 + 2 * t + (r & 1);
+      const int row = tau * kTileRows + g + 8 * (r >> 1);
+      if (j < ntok) y[(size_t)(row0 + j) * ld + row] = acc[nt][r];
     }
 }
 
@@ -383,98 +425,96 @@ struct ItemArgs {
   const __half* act;  // token rows of this phase
   int e;              // expert (routed)
   bool sh;            // shared FFN
+  int b;              // bitwidth
   int K, NT, row0, ntok, ld;
   __half* h;
   float* y;
 };
 
-// Block item: warp w computes tile tau + w over the whole reduction.
-template <int NM, int B>
-__device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A, int tau, uint32_t ring,
-                                           uint32_t slab, const int* s_tok) {
-  using G = Geo<false>;
+// One item.  Gate/up (NM = 2): warps 0-1 stream the gate rows of tiles tau
+// and tau + 1, warps 2-3 their up rows.  Down (NM = 1): S warps share each
+// tile (S = 1: warp w takes tile tau + w; S = 2: tiles tau, tau + 1; S = 4:
+// tile tau), slice k of a tile taking every S-th unit from unit k.  Partial
+// and up sums go through shared memory to the first warp of each tile, which
+// adds them in warp order and stores.  B: 16 (fp16 page), 3, or 0 (4..6
+// bits, A.b).
+template <int B>
+__device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A, int NM, int S, int tau,
+                                           uint32_t ring, uint32_t slab, uint32_t tab, const int* s_tok) {
+  constexpr int kNT = Geo::NTM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  tau += warp;
-  float acc[NM][G::NTM][4] = {};
-  WSrc<NM> src;
+  const int q = NM == 2 ? warp & 1 : warp;  // warp index within its matrix
+  const int t = tau + q / S;                 // this warp's tile
+  const int slice = q % S;
+  const int m = NM == 2 ? warp >> 1 : 2;     // and matrix
+  float acc[kNT][4] = {};
+  WSrc src;
+  if constexpr (B == 16) {
+    src.p[0] = A.sh ? reinterpret_cast<const char*>(L.shared16[m]) + (size_t)t * 32 * A.K
+                    : tile_addr(L, A.e, m, kPlanes, t);
+    kloop<KIND_F16, 16>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
+  } else if constexpr (B == 3) {
 #pragma unroll
-  for (int mi = 0; mi < NM; ++mi) {
-    const int m = NM == 2 ? mi : 2;
-    if constexpr (B == 16) {
-      src.p[mi][0] = A.sh ? reinterpret_cast<const char*>(L.shared16[m]) + (size_t)tau * 32 * A.K
-                          : tile_addr(L, A.e, m, kPlanes, tau);
-    } else {
+    for (int p = 0; p < 3; ++p) src.p[p] = tile_addr(L, A.e, m, p, t);
+    const __half* lr = lut_rows(L, A.e, m, 3, t * kTileRows);
+    load_lut3(lr + (lane >> 2) * 8, src.lut3[0]);
+    load_lut3(lr + ((lane >> 2) + 8) * 8, src.lut3[1]);
+    kloop<KIND_PG, 3>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
+  } else {
+    src.nb = A.b;
 #pragma unroll
-      for (int p = 0; p < 3; ++p) src.p[mi][p] = tile_addr(L, A.e, m, p, tau);
-      const __half* lr = lut_rows(L, A.e, m, 3, tau * kTileRows);
-      load_lut3(lr + (lane >> 2) * 8, src.lut3[mi][0]);
-      load_lut3(lr + ((lane >> 2) + 8) * 8, src.lut3[mi][1]);
-    }
+    for (int p = 0; p < kPlanes; ++p) src.p[p] = p < A.b ? tile_addr(L, A.e, m, p, t) : nullptr;
+    src.tabg = tab + (lane >> 2) * 4;
+    const __half* lr = lut_rows(L, A.e, m, A.b, t * kTileRows);
+    kloop<KIND_PB, 0>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc,
+                      [&] { build_tab_warp(lr, A.b, tab); });
   }
-  if constexpr (B == 16) kloop<G, KIND_F16, 16, NM>(src, A.K, A.NT, 0, 1, ring, slab, 0u, A.act, s_tok, acc);
-  else kloop<G, KIND_PB, 3, NM>(src, A.K, A.NT, 0, 1, ring, slab, 0u, A.act, s_tok, acc);
-  tile_store<NM, G::NTM>(acc, tau, A.row0, A.ntok, A.ld, A.h, A.y);
-}
-
-// Split item: the four warps share tile tau.  For gate/up, warps 0-1 stream
-// the gate matrix and warps 2-3 the up matrix (interleaved 128-column units),
-// so every warp runs the one-matrix loop; partial sums are added in warp order.
-template <int NM, int B>
-__device__ __forceinline__ void split_item(const DevLayer& L, const ItemArgs& A, int tau, uint32_t ring,
-                                           uint32_t slab, unsigned char* tab_ptr, const int* s_tok) {
-  using G = Geo<true>;
-  constexpr int kNT = G::NTM;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  build_tab<B, NM>(L, A.e, tau, tab_ptr);  // ordered before use by the first K-block barrier
-  const int mi = NM == 2 ? warp >> 1 : 0;  // this warp's matrix (index into the item's NM)
-  float acc[1][kNT][4] = {};
-  WSrc<1> src;
-#pragma unroll
-  for (int p = 0; p < 6; ++p) src.p[0][p] = p < B ? tile_addr(L, A.e, NM == 2 ? mi : 2, p, tau) : nullptr;
-  // the LUT table column of this warp's matrix: unit u of the one-matrix loop is matrix 0
-  const uint32_t tab = smem_u32(tab_ptr) + mi * 128;
-  if (NM == 2) kloop<G, KIND_PB, B, 1>(src, A.K, A.NT, warp & 1, 2, ring, slab, tab, A.act, s_tok, acc);
-  else kloop<G, KIND_PB, B, 1>(src, A.K, A.NT, warp, kCtaWarps, ring, slab, tab, A.act, s_tok, acc);
+  if (NM == 1 && S == 1) {
+    tile_store_y(acc, t, A.row0, A.ntok, A.ld, A.y);
+    return;
+  }
   __syncthreads();  // the staged rows are no longer read
   float4* red = reinterpret_cast<float4*>(__cvta_shared_to_generic(slab));
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt)
-    red[(warp * kNT + nt) * 32 + lane] = make_float4(acc[0][nt][0], acc[0][nt][1], acc[0][nt][2], acc[0][nt][3]);
+    red[(warp * kNT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
   __syncthreads();
-  if (warp == 0) {
-    constexpr int WPM = kCtaWarps / NM;  // warps per matrix
-    float sum[NM][kNT][4];
+  if (slice != 0 || m == 1) return;
+  // warp order: slices of the tile's (gate) rows, then of its up rows
+  auto add = [&](float (&sum)[kNT][4], int w) {
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        float4 v = red[((m * WPM) * kNT + nt) * 32 + lane];
-#pragma unroll
-        for (int w = 1; w < WPM; ++w) {
-          const float4 o = red[((m * WPM + w) * kNT + nt) * 32 + lane];
-          v.x += o.x;
-          v.y += o.y;
-          v.z += o.z;
-          v.w += o.w;
-        }
-        sum[m][nt][0] = v.x;
-        sum[m][nt][1] = v.y;
-        sum[m][nt][2] = v.z;
-        sum[m][nt][3] = v.w;
-      }
-    tile_store<NM, kNT>(sum, tau, A.row0, A.ntok, A.ld, A.h, A.y);
+    for (int nt = 0; nt < kNT; ++nt) {
+      const float4 v = red[(w * kNT + nt) * 32 + lane];
+      sum[nt][0] += v.x;
+      sum[nt][1] += v.y;
+      sum[nt][2] += v.z;
+      sum[nt][3] += v.w;
+    }
+  };
+  for (int k = 1; k < S; ++k) add(acc, warp + k);
+  if (NM == 1) {
+    tile_store_y(acc, t, A.row0, A.ntok, A.ld, A.y);
+  } else {
+    float up[kNT][4] = {};
+    for (int k = 0; k < S; ++k) add(up, 2 + warp + k);
+    tile_store_h(acc, up, t, A.row0, A.ntok, A.ld, A.h);
   }
 }
 
-__device__ __forceinline__ bool is_split(int b) { return b >= 4 && b <= 6; }
+// Warps sharing one down tile for a group of n tokens with reduction length
+// K: long reductions of one- or two-tile items are split.  Only batches of at
+// most 16 tokens (SPLITK) split; larger ones fill the GPU with whole tiles and
+// run a kernel without the split paths.
+template <bool SPLITK>
+__device__ __forceinline__ int down_split(int n, int K) {
+  return !SPLITK || K < 4096 || n > 16 ? 1 : n > 8 ? 2 : 4;
+}
 
-// SPLIT = false: block items (3-bit and fp16 experts, shared FFN); SPLIT = true:
-// split items (4, 5, 6-bit experts).  Two instantiations keep each set of
-// paths in its own register allocation; their groups are disjoint, so they
-// share the layer's phase counters and use separate claim counters.
-template <bool SPLIT>
-__global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kernel(UniParams P) {
-  using G = Geo<SPLIT>;
+__device__ __forceinline__ bool is_tab(int b) { return b >= 4 && b <= 6; }
+
+template <bool SPLITK>
+__global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniParams P) {
+  using G = Geo;
   extern __shared__ __align__(128) unsigned char smem_uni[];
   __shared__ int s_base[kMaxExperts + 1];   // first input row of each group
   __shared__ int s_n[kMaxExperts + 1];      // tokens of each group
@@ -487,7 +527,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
   const DevLayer& L = P.L;
   const int E = L.E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int* const q = L.sync + (SPLIT ? 2 : 0);           // claim counter, CTA exit counter
+  int* const q = L.sync;                             // claim counter, CTA exit counter
   int* const done0 = L.sync + kSyncHeader;           // [E+1][kSyncChunks] gate/up tiles done
   int* const done1 = done0 + (E + 1) * kSyncChunks;  // [E+1][kSyncChunks] down tiles done
 
@@ -498,11 +538,11 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
         base = P.offsets[g];
         n = P.offsets[g + 1] - base;
         b = L.bits[g];
-        const bool take = SPLIT ? is_split(b) && (P.bit_mask & 4)
-                                : (b == 3 && (P.bit_mask & 1)) || (b == 16 && (P.bit_mask & 2));
+        const bool take = (b == 3 && (P.bit_mask & 1)) || (b == 16 && (P.bit_mask & 2)) ||
+                          (is_tab(b) && (P.bit_mask & 4));
         if (!take || n > P.max_tokens) n = 0;
       }
-    } else if (P.x && !SPLIT) {
+    } else if (P.x) {
       n = P.T;
     }
     s_base[g] = base;
@@ -511,7 +551,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
   }
   __syncthreads();
   if (warp == 0) {
-    // claim order: shared FFN, fp16 experts, 3-bit experts, 4..6-bit experts
+    // claim order: shared FFN, fp16 experts, 4..6-bit experts, 3-bit experts
     int ng = 0;
     for (int pass = 0; pass < 4; ++pass) {
       for (int g0 = 0; g0 <= E; g0 += 32) {
@@ -519,7 +559,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
         bool in = false;
         if (g <= E && s_n[g] > 0) {
           const int b = s_b[g];
-          in = pass == 0 ? g == E : g == E ? false : pass == 1 ? b == 16 : pass == 2 ? b == 3 : is_split(b);
+          in = pass == 0 ? g == E : g == E ? false : pass == 1 ? b == 16 : pass == 2 ? is_tab(b) : b == 3;
         }
         const unsigned m = __ballot_sync(0xffffffffu, in);
         if (in) s_ord[ng + __popc(m & ((1u << lane) - 1))] = (short)g;
@@ -535,8 +575,8 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
           const int g = s_ord[k];
           const int fe = g == E ? L.fs : L.f;
           const int tiles = ph == 0 ? fe / kTileRows : L.d / kTileRows;
-          const int per_chunk = SPLIT ? tiles : tiles / kCtaWarps;
-          c = ((s_n[g] + G::TOK - 1) / G::TOK) * per_chunk;
+          const int per_item = ph == 0 ? 2 : kCtaWarps / down_split<SPLITK>(s_n[g], fe);
+          c = ((s_n[g] + G::TOK - 1) / G::TOK) * (tiles / per_item);
         }
         int incl = c;
 #pragma unroll
@@ -552,8 +592,8 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
     if (lane == 0) s_ng = ng;
   }
   const uint32_t slab = smem_u32(smem_uni);
-  unsigned char* const tab_ptr = smem_uni + 2 * G::HALF;  // split items only
-  const uint32_t ring = slab + 2 * G::HALF + (SPLIT ? kTabBytes : 0) + warp * G::RB;
+  const uint32_t tab = slab + 2 * G::HALF + warp * kTabW;
+  const uint32_t ring = slab + 2 * G::HALF + kCtaWarps * kTabW + warp * G::RB;
 
   for (;;) {
     if (tid == 0) s_it = atomicAdd(q, 1);
@@ -576,14 +616,17 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
     const int n = s_n[g];
     const int nch = (n + G::TOK - 1) / G::TOK;
     const int local = li - pref[lo];
-    const int blk = local / nch, chunk = local % nch;  // chunks of one tile (block) are claimed together
+    const int blk = local / nch, chunk = local % nch;  // chunks of one tile block are claimed together
     const int fe = sh ? L.fs : L.f;
     const int tiles = phase == 0 ? fe / kTileRows : L.d / kTileRows;
     const int sidx = g * kSyncChunks + chunk;
+    const int S = phase == 0 ? 1 : down_split<SPLITK>(n, fe);  // warps per tile
+    const int per_item = phase == 0 ? 2 : kCtaWarps / S;  // tiles of one item
 
     ItemArgs A;
     A.e = g;
     A.sh = sh;
+    A.b = b;
     A.row0 = s_base[g] + chunk * G::TOK;
     A.ntok = min(G::TOK, n - chunk * G::TOK);
     A.NT = (A.ntok + 7) >> 3;
@@ -593,7 +636,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
     A.h = sh ? P.hs : P.h;
     A.y = sh ? P.ys : P.y;
 
-    if (tid < G::TOK) s_tok[tid] = A.row0 + min(tid, A.ntok - 1);
+    if (tid < A.ntok) s_tok[tid] = A.row0 + tid;
     if (phase == 1 && tid == 0) {  // h of this chunk must be complete
       const int need = fe / kTileRows;
       long long spins = 0;
@@ -606,34 +649,14 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
       }
     }
     __syncthreads();
-    if constexpr (SPLIT) {
-      const int tau = blk;
-      if (phase == 0) {
-        switch (b) {
-          case 4: split_item<2, 4>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
-          case 5: split_item<2, 5>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
-          default: split_item<2, 6>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
-        }
-      } else {
-        switch (b) {
-          case 4: split_item<1, 4>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
-          case 5: split_item<1, 5>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
-          default: split_item<1, 6>(L, A, tau, ring, slab, tab_ptr, s_tok); break;
-        }
-      }
-    } else {
-      const int tau = blk * kCtaWarps;
-      if (phase == 0) {
-        if (b == 16) block_item<2, 16>(L, A, tau, ring, slab, s_tok);
-        else block_item<2, 3>(L, A, tau, ring, slab, s_tok);
-      } else {
-        if (b == 16) block_item<1, 16>(L, A, tau, ring, slab, s_tok);
-        else block_item<1, 3>(L, A, tau, ring, slab, s_tok);
-      }
-    }
+    const int tau = blk * per_item;
+    const int NM = phase == 0 ? 2 : 1;
+    if (b == 16) block_item<16>(L, A, NM, S, tau, ring, slab, tab, s_tok);
+    else if (b == 3) block_item<3>(L, A, NM, S, tau, ring, slab, tab, s_tok);
+    else block_item<0>(L, A, NM, S, tau, ring, slab, tab, s_tok);
     __syncthreads();  // every tile of the item is stored
     if (tid == 0) {
-      const int done_tiles = SPLIT ? 1 : kCtaWarps;
+      const int done_tiles = per_item;
       __threadfence();
       if (phase == 0) {
         atomicAdd(done0 + sidx, done_tiles);
@@ -655,9 +678,9 @@ __global__ void __launch_bounds__(kCtaThreads, Geo<SPLIT>::BLOCKS) ffn_cta_kerne
 }
 
 cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
-                       int bit_mask, int max_tokens, float split_share, __half* h, __half* hs, float* y, float* ys,
-                       cudaStream_t s) {
+                       int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s) {
   if (max_tokens > kSyncChunks * 16 || (x && T > kSyncChunks * 16)) return cudaErrorInvalidValue;
+  if (!bit_mask && !x) return cudaSuccess;
   UniParams P;
   P.L = L;
   P.x = x;
@@ -670,39 +693,15 @@ cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm,
   P.hs = hs;
   P.y = y;
   P.ys = ys;
-  const bool split = (bit_mask & 4) != 0, block = (bit_mask & 3) || x;
+  // The split paths depend on the batch size only, so a routed call, a shared
+  // call and the combined call compute every item the same way.
+  const bool splitk = T <= 16;
+  const void* fn = splitk ? (const void*)ffn_cta_kernel<true> : (const void*)ffn_cta_kernel<false>;
   cudaError_t e;
-  // The two kernels have disjoint groups and claim counters.  When the
-  // 4..6-bit experts hold a small share of the weight bytes, their kernel runs
-  // on the layer's side stream next to the other one (its latency-bound items
-  // overlap the weight streaming); when they hold most of the bytes it needs
-  // the whole GPU, and the kernels run one after the other.
-  const bool fork = split && block && L.side_stream && split_share < 0.3f;
-  cudaStream_t ss = fork ? static_cast<cudaStream_t>(L.side_stream) : s;
-  if (fork) {
-    if ((e = cudaEventRecord(static_cast<cudaEvent_t>(L.ev_fork), s)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(ss, static_cast<cudaEvent_t>(L.ev_fork), 0)) != cudaSuccess) return e;
-  }
-  if (split) {
-    using G = Geo<true>;
-    if ((e = ensure_smem((const void*)ffn_cta_kernel<true>, G::SMEM)) != cudaSuccess) return e;
-    // side by side: one CTA per SM, so every SM keeps room for a CTA of the
-    // other kernel (whose grid fills the rest of the GPU as these CTAs leave)
-    const int grid = sm_count() * (fork ? 1 : G::BLOCKS);
-    ffn_cta_kernel<true><<<grid, kCtaThreads, G::SMEM, ss>>>(P);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if (block) {
-    using G = Geo<false>;
-    if ((e = ensure_smem((const void*)ffn_cta_kernel<false>, G::SMEM)) != cudaSuccess) return e;
-    ffn_cta_kernel<false><<<sm_count() * G::BLOCKS, kCtaThreads, G::SMEM, s>>>(P);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if (fork) {
-    if ((e = cudaEventRecord(static_cast<cudaEvent_t>(L.ev_join), ss)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(L.ev_join), 0)) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  if ((e = ensure_smem(fn, Geo::SMEM)) != cudaSuccess) return e;
+  if (splitk) ffn_cta_kernel<true><<<sm_count() * Geo::BLOCKS, kCtaThreads, Geo::SMEM, s>>>(P);
+  else ffn_cta_kernel<false><<<sm_count() * Geo::BLOCKS, kCtaThreads, Geo::SMEM, s>>>(P);
+  return cudaGetLastError();
 }
 
 }  // namespace pw

@@ -46,8 +46,10 @@ __device__ __forceinline__ uint32_t ldg_stream32(const void* p) {
 }
 
 // D += A(16x16 fp16, row) * B(16x8 fp16, col), fp32 accumulate.
+// A pure register operation: not volatile, so the compiler may schedule it
+// among the shared-memory loads of the decode.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

@@ -18,7 +18,7 @@ constexpr int kTabBytes = 64 * 256;  // LUT table of one 16-row tile of one matr
 
 cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* offsets, int n_slots, float* y_perm,
                            __half* h, const __half* x_sh, int T, float* y_sh, __half* hs, int class_mask,
-                           float split_share, cudaStream_t s) {
+                           cudaStream_t s) {
   // Experts with at most `thr` tokens take the decode kernels; larger ones the
   // tcgen05 GEMM.  No expert can have more tokens than the batch, and the
   // shared FFN sees every token.
@@ -31,7 +31,7 @@ cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* o
       routed ? ((class_mask & 1) ? 1 : 0) | ((class_mask & 4) ? 2 : 0) | ((class_mask & 2) ? 4 : 0) : 0;
   if (bit_mask || shared_decode) {
     e = launch_uni(L, shared_decode ? x_sh : nullptr, bit_mask ? x_perm : nullptr, bit_mask ? offsets : nullptr, T,
-                   bit_mask, big ? thr : T, split_share, h, hs, y_perm, y_sh, s);
+                   bit_mask, big ? thr : T, h, hs, y_perm, y_sh, s);
     if (e != cudaSuccess) return e;
   }
   for (int phase = 0; phase < 2; ++phase) {

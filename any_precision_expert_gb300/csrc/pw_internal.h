@@ -38,11 +38,6 @@ struct DevLayer {
   const __half* shared16[3];            // packed fp16 shared FFN (gate, up, down) or null
   int* err;                             // device error word
   int* sync;                            // [sync_words(E)] zero between launches
-  // host-side handles (never dereferenced on the device): the layer's side
-  // stream and the fork / join events of the two decode kernels
-  void* side_stream;
-  void* ev_fork;
-  void* ev_join;
 };
 
 // Scratch carved out of the caller's workspace for one hot-path call.
@@ -68,15 +63,12 @@ cudaError_t launch_permute(const DevLayer& L, const int* idx, int T, const __hal
 // fp16 pages.
 cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* offsets, int n_slots, float* y_perm,
                            __half* h, const __half* x_sh, int T, float* y_sh, __half* hs, int class_mask,
-                           float split_share, cudaStream_t s);
-// Persistent decode kernels for routed 3-bit / fp16 / 4..6-bit experts
+                           cudaStream_t s);
+// Persistent decode kernel for routed 3-bit / fp16 / 4..6-bit experts
 // (bit_mask bits 0 / 1 / 2) with at most max_tokens tokens and, when x is
 // non-null, the shared FFN.
-// split_share: the 4..6-bit experts' share of the layer's weight bytes (sizes
-// that kernel's grid when both kernels run side by side).
 cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
-                       int bit_mask, int max_tokens, float split_share, __half* h, __half* hs, float* y, float* ys,
-                       cudaStream_t s);
+                       int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s);
 int decode_max_tokens(int ffn);
 int decode_max_tokens_shared();
 cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
@@ -89,7 +81,7 @@ cudaError_t launch_debug_dequant(const DevLayer& L, int e, int m, __half* out, c
 // arguments of a routed FFN call for T tokens and returns the layer's kernel
 // parameters, the decode kernel classes it needs and the bytes of h scratch.
 pw_status ffn_call_args(pw_layer_t layer, const void* x_perm, const int32_t* offsets, int T, const float* y_perm,
-                        DevLayer* dev, int* class_mask, float* split_share, size_t* h_bytes);
+                        DevLayer* dev, int* class_mask, size_t* h_bytes);
 // Records a CUDA error for pw_last_cuda_error and returns PW_ERR_CUDA.
 pw_status record_cuda_error(cudaError_t e);
 

@@ -50,15 +50,14 @@ extern "C" pw_status pw_expert_ffn_bitplane_noalloc(pw_layer_t layer, const void
   pw::DevLayer dev;
   int class_mask = 0;
   size_t h_bytes = 0;
-  float share = 0.f;
-  pw_status st = pw::ffn_call_args(layer, x_perm, offsets, T, y_perm, &dev, &class_mask, &share, &h_bytes);
+  pw_status st = pw::ffn_call_args(layer, x_perm, offsets, T, y_perm, &dev, &class_mask, &h_bytes);
   if (st != PW_OK || T == 0) return st;
   if (h_bytes > kNoAllocScratchBytes) return PW_ERR_OOM;
   void* scratch = nullptr;
   cudaError_t e = scratch_address(&scratch);
   if (e != cudaSuccess) return pw::record_cuda_error(e);
   e = pw::launch_moe_ffn(dev, static_cast<const __half*>(x_perm), offsets, T * dev.K, y_perm,
-                         static_cast<__half*>(scratch), nullptr, T, nullptr, nullptr, class_mask, share,
+                         static_cast<__half*>(scratch), nullptr, T, nullptr, nullptr, class_mask,
                          reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PW_OK : pw::record_cuda_error(e);
 }

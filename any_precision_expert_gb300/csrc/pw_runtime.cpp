@@ -249,8 +249,6 @@ struct pw_layer_s {
   int* d_bits = nullptr;
   int* d_err = nullptr;
   int* d_sync = nullptr;
-  cudaStream_t side = nullptr;       // side stream of the 4..6-bit decode kernel
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   unsigned long long* d_plane_pt = nullptr;
   unsigned long long* d_f16_pt = nullptr;
   uint2* d_tmap = nullptr;
@@ -288,9 +286,6 @@ struct pw_layer_s {
     for (int m = 0; m < 3; ++m) L.shared16[m] = shared_loaded ? d_shared[m] : nullptr;
     L.err = d_err;
     L.sync = d_sync;
-    L.side_stream = side;
-    L.ev_fork = ev_fork;
-    L.ev_join = ev_join;
     return L;
   }
 };
@@ -379,14 +374,6 @@ pw_status take_expert_pages(pw_layer_t l, int bits, std::vector<std::vector<int>
     }
   }
   return PW_OK;
-}
-
-void destroy_side(pw_layer_s* l) {
-  if (l->ev_join) cudaEventDestroy(l->ev_join);
-  if (l->ev_fork) cudaEventDestroy(l->ev_fork);
-  if (l->side) cudaStreamDestroy(l->side);
-  l->ev_join = l->ev_fork = nullptr;
-  l->side = nullptr;
 }
 
 void release_expert(pw_layer_t l, int e) {
@@ -558,14 +545,7 @@ extern "C" pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, 
   if (st == PW_OK) st = dev_h2d(l->d_tmap16, l->tmap16.data(), sizeof(uint2) * l->tmap16.size(), s);
   if (st == PW_OK) st = dev_h2d(l->d_lut_base, lutb.data(), sizeof(unsigned long long) * E, s);
   if (st == PW_OK) st = dev_sync(s);
-  if (st == PW_OK && !g_sim) {
-    cudaError_t e = cudaStreamCreateWithFlags(&l->side, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&l->ev_fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&l->ev_join, cudaEventDisableTiming);
-    if (e != cudaSuccess) st = cuda_fail(e);
-  }
   if (st != PW_OK) {
-    destroy_side(l.get());
     pool->give_back_resident(l->res_first, l->res_npages);
     return st;
   }
@@ -580,7 +560,6 @@ extern "C" pw_status pw_layer_destroy(pw_layer_t l) {
   for (int e = 0; e < l->desc.n_experts; ++e) release_expert(l, e);
   l->pool->give_back_resident(l->res_first, l->res_npages);
   l->pool->n_layers--;
-  destroy_side(l);
   delete l;
   return PW_OK;
 }
@@ -954,20 +933,6 @@ pw_status launched(cudaError_t e) { return e == cudaSuccess ? PW_OK : cuda_fail(
 // least four planes still resident (4..6 bits reachable), bit 2 for experts
 // whose fp16 page is still resident (16 bits reachable).  A class whose
 // bitwidths no expert can reach without a reload is not launched.
-// Share of the 4..6-bit experts in the layer's expert weight bytes at the
-// current bitwidths (sizes the grid of their decode kernel).
-float split_share(const pw_layer_s* l) {
-  double split = 0, all = 0;
-  for (int e = 0; e < l->desc.n_experts; ++e) {
-    const int b = l->bits[e];
-    const double w = b == 16 ? 16.0 : b;
-    all += w;
-    if (b >= 4 && b <= 6) split += w;
-  }
-  all += l->desc.shared_ffn ? 16.0 * l->desc.shared_ffn / l->desc.ffn : 0.0;
-  return all > 0 ? (float)(split / all) : 0.f;
-}
-
 int class_mask(const pw_layer_s* l) {
   int m = 0;
   for (int e = 0; e < l->desc.n_experts; ++e) {
@@ -1031,7 +996,7 @@ extern "C" pw_status pw_expert_ffn_bitplane(pw_layer_t l, const void* x_perm, co
   char* wsb = static_cast<char*>(ws);
   return launched(launch_moe_ffn(l->dev(), static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
                                  reinterpret_cast<__half*>(wsb + W.h_off), nullptr, T, nullptr, nullptr,
-                                 class_mask(l), split_share(l), as_stream(stream)));
+                                 class_mask(l), as_stream(stream)));
 }
 
 extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_shared, void* ws, size_t ws_bytes,
@@ -1046,7 +1011,7 @@ extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_
   PW_TRY(device_only());
   char* wsb = static_cast<char*>(ws);
   return launched(launch_moe_ffn(l->dev(), nullptr, nullptr, 0, nullptr, nullptr, static_cast<const __half*>(x), T,
-                                 y_shared, reinterpret_cast<__half*>(wsb + W.hs_off), 0, 0.f, as_stream(stream)));
+                                 y_shared, reinterpret_cast<__half*>(wsb + W.hs_off), 0, as_stream(stream)));
 }
 
 extern "C" pw_status pw_moe_ffn(pw_layer_t l, const void* x, const void* x_perm, const int32_t* offsets, int T,
@@ -1067,7 +1032,7 @@ extern "C" pw_status pw_moe_ffn(pw_layer_t l, const void* x, const void* x_perm,
   return launched(launch_moe_ffn(l->dev(), static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
                                  reinterpret_cast<__half*>(wsb + W.h_off), sh ? static_cast<const __half*>(x) : nullptr,
                                  T, sh ? y_shared : nullptr, reinterpret_cast<__half*>(wsb + W.hs_off), class_mask(l),
-                                 split_share(l), as_stream(stream)));
+                                 as_stream(stream)));
 }
 
 extern "C" pw_status pw_combine(pw_layer_t l, const float* y_perm, const int32_t* inv_slot, const float* w, int T,
@@ -1130,9 +1095,9 @@ extern "C" pw_status pw_debug_page_address(pw_layer_t l, int e, int p, int vpage
 pw_status pw::record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
 pw_status pw::ffn_call_args(pw_layer_t l, const void* x_perm, const int32_t* offsets, int T, const float* y_perm,
-                            DevLayer* dev, int* cmask, float* share, size_t* h_bytes) {
+                            DevLayer* dev, int* cmask, size_t* h_bytes) {
   PW_TRY(check_layer(l));
-  if (T < 0 || !dev || !cmask || !share || !h_bytes) return PW_ERR_INVALID_ARG;
+  if (T < 0 || !dev || !cmask || !h_bytes) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
   if (!x_perm || !offsets || !y_perm) return PW_ERR_INVALID_ARG;
   if (!aligned16(x_perm) || !aligned16(y_perm)) return PW_ERR_INVALID_ARG;
@@ -1140,7 +1105,6 @@ pw_status pw::ffn_call_args(pw_layer_t l, const void* x_perm, const int32_t* off
   PW_TRY(device_only());
   *dev = l->dev();
   *cmask = class_mask(l);
-  *share = split_share(l);
   *h_bytes = (size_t)T * l->desc.top_k * l->desc.ffn * 2;
   return PW_OK;
 }

@@ -4,7 +4,8 @@ after their gate/up tiles with device counters, and leaves those counters at
 zero for the next launch.
 
 Checks: the combined call gives bit-identical results to the separate routed
-and shared calls (every item is computed the same way whoever runs it), CUDA
+and shared calls (every item is computed the same way whoever runs it), down
+reductions split over several warps match the oracle at every bitwidth, CUDA
 graph replays give the eager result again and again, the decode / tensor-core
 threshold can be crossed by the shared FFN, and the layer output stays within
 the oracle's tolerance.
@@ -33,9 +34,10 @@ def _separate(gl, x, T):
     return buf
 
 
-@pytest.mark.parametrize("T", [1, 8, 64, 200])
-def test_combined_call_equals_separate_calls(T):
-    cfg = get_config("qwen", d=512, f=320, E=12, K=4, shared_ffn=768)
+@pytest.mark.parametrize("T,fs", [(1, 768), (8, 768), (64, 768), (200, 768), (1, 4096), (12, 4096)])
+def test_combined_call_equals_separate_calls(T, fs):
+    # fs = 4096: the shared FFN's down reduction is split over several warps per tile
+    cfg = get_config("qwen", d=512, f=320, E=12, K=4, shared_ffn=fs)
     gl = GpuLayer(cfg, seed=3, bits=[3, 16, 3, 4, 3, 5, 16, 6, 3, 3, 16, 3], with_w16=False)
     try:
         x = torch.from_numpy(gl.tokens(T)).cuda()
@@ -110,5 +112,19 @@ def test_many_chunks_per_expert():
         gl.bias_d = torch.from_numpy(gl.bias).cuda()
         r = gl.check_forward(gl.tokens(250))
         assert (r["buf"].idx[:250].cpu().numpy() == 1).all()
+    finally:
+        gl.close()
+
+
+@pytest.mark.parametrize("f", [4096, 4160])
+def test_split_down_reduction_all_bitwidths(f):
+    # Down reductions of 4096 or more columns for experts with at most 16
+    # tokens are shared by two (9..16 tokens) or four (1..8) warps per tile;
+    # f = 4160 ends in a ragged plane group.
+    cfg = get_config("tiny", d=512, f=f, E=5, K=2)
+    gl = GpuLayer(cfg, seed=5, bits=[3, 4, 5, 6, 16])
+    try:
+        for T in (1, 5, 12, 40):
+            gl.check_forward(gl.tokens(T))
     finally:
         gl.close()

@@ -254,7 +254,7 @@ def run_gpu(args):
     def part_c(L, b, x):
         L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared if cfg.shared_ffn else None, b.y, stream)
 
-    launches_per_step = _launches_per_step(cfg, wl["bits"], T)
+    launches_per_step = _launches_per_step(cfg, T)
     if external:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -433,19 +433,16 @@ def run_gpu(args):
     return out
 
 
-def _launches_per_step(cfg, bits, T):
+def _launches_per_step(cfg, T):
     """Kernels one step launches: router, permutation (histogram + scatter for
     more than 1024 slots, or one fused kernel), row gather, the persistent
-    decode kernel for 4/5/6-bit experts (when such planes are resident) and the
-    one for 3-bit / fp16 experts and the shared FFN, the tcgen05 GEMM pair for
-    experts above the token threshold and for a shared FFN above its own, and
-    the combine."""
+    decode kernel (routed experts of every bitwidth up to the token threshold
+    and the shared FFN up to its own), the tcgen05 GEMM pair for experts above
+    the token threshold and for a shared FFN above its own, and the combine."""
     thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "32" if cfg.f >= 4096 else "64")), 1024)
     thr_s = min(int(os.environ.get("PW_DECODE_MAX_TOK_SHARED", "256")), 1024)
     S = T * cfg.K
     n = 1 + (2 if S > 1024 else 1) + 1
-    if any(b in (4, 5, 6, 16) for b in np.asarray(bits).tolist()):
-        n += 1  # planes 3..5 are resident for 4..6-bit and fp16 experts
     n += 1
     if T > thr:
         n += 2
@@ -640,7 +637,7 @@ def run_sweep(args):
             "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": NL * T * cfg.d * 2,
                     "d2h_bytes_per_step": NL * T * cfg.d * 2, "steps": KE,
                     "note": "public API (moe_forward) per layer: pinned H2D of x, layer, D2H of y; host sync per step"},
-            "gpu_launches": (NL * _launches_per_step(cfg, sw["init"][0], T) + len(plan[W])) * K,
+            "gpu_launches": (NL * _launches_per_step(cfg, T) + len(plan[W])) * K,
             "clocks": clk,
         }
     for L in layers:

@@ -16,9 +16,9 @@
 // 16-row tile through its own cp.async ring, addressed through the page table
 // (gate/up: warps 0-1 the gate rows of the two tiles, warps 2-3 their up rows,
 // which reach the gate warps through shared memory for SwiGLU).  Down items of
-// groups with few tokens and a long reduction split each tile's reduction over
-// two or four warps (interleaved units, partial sums added in warp order), so
-// that their chains stay short.  Codes become weights by
+// groups with few tokens and a long reduction split each tile's reduction
+// over two or four warps (interleaved units, partial sums added in warp
+// order), so that their chains stay short.  Codes become weights by
 //  - 3 bits: byte permutes from register LUTs (whole plane groups, 16 B per
 //    lane and plane);
 //  - 4, 5, 6 bits: lookups in the warp's LUT table in shared memory (row
@@ -29,11 +29,12 @@
 // fp32.  Each weight kind has a single copy of its loop body (the kernel's
 // instruction footprint stays small).
 //
-// CTAs claim items from one counter in a fixed order: every gate/up item
-// (phase 0) before every down item (phase 1); inside a phase the shared FFN
-// first, then fp16, 4..6-bit and 3-bit experts.  A down item waits until all
-// gate/up tiles of its (group, chunk) are done; those items were claimed
-// earlier by running CTAs and never wait, so every wait ends.  The waits are
+// CTAs claim items from one counter in a fixed order: groups in the order
+// shared FFN, fp16, 4..6-bit, 3-bit experts; a group's down items (phase 1)
+// follow about one wave of CTAs after its gate/up items (phase 0), so that
+// long down items start early.  A down item waits until all gate/up tiles of
+// its (group, chunk) are done; those items were claimed earlier by running
+// CTAs and never wait, so every wait ends.  The waits are
 // bounded anyway: past the limit the kernel records a timeout in the layer's
 // error word and carries on.  The phase counters are returned to zero by the
 // last down tile of each (group, chunk) and the claim counter by the last CTA
@@ -502,9 +503,11 @@ __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A,
 }
 
 // Warps sharing one down tile for a group of n tokens with reduction length
-// K: long reductions of one- or two-tile items are split.  Only batches of at
-// most 16 tokens (SPLITK) split; larger ones fill the GPU with whole tiles and
-// run a kernel without the split paths.
+// K: reductions of 4096 columns or more are split in four (up to 8 tokens,
+// 1024-column K-blocks) or two (up to 16 tokens, 512-column K-blocks), so
+// every K-block still gives each warp of a tile a share of whole units.
+// Only batches of at most 16 tokens (SPLITK) split; larger ones fill the GPU
+// with whole tiles and run a kernel without the split paths.
 template <bool SPLITK>
 __device__ __forceinline__ int down_split(int n, int K) {
   return !SPLITK || K < 4096 || n > 16 ? 1 : n > 8 ? 2 : 4;
@@ -520,8 +523,9 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
   __shared__ int s_n[kMaxExperts + 1];      // tokens of each group
   __shared__ short s_b[kMaxExperts + 1];    // bitwidth of each group
   __shared__ short s_ord[kMaxExperts + 1];  // groups in claim order
-  __shared__ int s_pref[2][kMaxExperts + 2];
-  __shared__ int s_ng, s_it;
+  __shared__ int s_pref[2][kMaxExperts + 2];  // claim position of each group's gate/up and down segment
+  __shared__ short s_ins[kMaxExperts + 1];
+  __shared__ int s_ng, s_it, s_total;
   __shared__ int s_tok[G::TOK];
 
   const DevLayer& L = P.L;
@@ -589,7 +593,60 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
       }
       if (lane == 0) s_pref[ph][ng] = run;
     }
-    if (lane == 0) s_ng = ng;
+    // s_pref[ph] holds prefix counts C_ph of the segments.  The down segment
+    // of group k goes in front of the first gate/up segment that starts at
+    // least one wave (gridDim.x items) of gate/up items after the end of k's
+    // own gate/up segment, or after all of them; so down items never precede
+    // their gate/up items, and those are usually done when they are claimed.
+    __syncwarp();
+    constexpr int kPer = (kMaxExperts + 1 + 31) / 32;
+    const int wave = (int)gridDim.x;
+    int ins[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int k = lane + 32 * i;
+      ins[i] = ng;
+      if (k < ng) {
+        const int target = s_pref[0][k + 1] + wave;
+        int lo = k + 1, hi = ng;  // first j in [k + 1, ng] with C_0[j] >= target
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (s_pref[0][mid] >= target) hi = mid; else lo = mid + 1;
+        }
+        ins[i] = lo;
+        s_ins[k] = (short)lo;
+      }
+    }
+    __syncwarp();
+    int p0[kPer], p1[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int k = lane + 32 * i;
+      p0[i] = p1[i] = 0;
+      if (k < ng) {
+        p1[i] = s_pref[0][ins[i]] + s_pref[1][k];
+        int lo = 0, hi = ng;  // down segments placed in front of gate/up segment k
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (s_ins[mid] <= k) lo = mid + 1; else hi = mid;
+        }
+        p0[i] = s_pref[0][k] + s_pref[1][lo];
+      }
+    }
+    const int total = s_pref[0][ng] + s_pref[1][ng];
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int k = lane + 32 * i;
+      if (k < ng) {
+        s_pref[0][k] = p0[i];
+        s_pref[1][k] = p1[i];
+      }
+    }
+    if (lane == 0) {
+      s_ng = ng;
+      s_total = total;
+    }
   }
   const uint32_t slab = smem_u32(smem_uni);
   const uint32_t tab = slab + 2 * G::HALF + warp * kTabW;
@@ -599,23 +656,27 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     if (tid == 0) s_it = atomicAdd(q, 1);
     __syncthreads();  // also: the previous item no longer reads shared memory
     const int ng = s_ng;
-    const int total0 = s_pref[0][ng];
     const int it = s_it;
-    if (it >= total0 + s_pref[1][ng]) break;
-    const int phase = it >= total0 ? 1 : 0;
-    const int* pref = s_pref[phase];
-    const int li = phase ? it - total0 : it;
-    int lo = 0, hi = ng;  // pref[lo] <= li < pref[lo + 1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (pref[mid] <= li) lo = mid; else hi = mid;
+    if (it >= s_total) break;
+    // the segment holding item it: the latest segment start at or before it
+    int sk[2];
+#pragma unroll
+    for (int ph = 0; ph < 2; ++ph) {
+      int lo = -1, hi = ng - 1;  // last k with s_pref[ph][k] <= it (-1: none)
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_pref[ph][mid] <= it) lo = mid; else hi = mid - 1;
+      }
+      sk[ph] = lo;
     }
+    const int phase = sk[1] >= 0 && s_pref[1][sk[1]] > s_pref[0][sk[0]] ? 1 : 0;
+    const int lo = phase ? sk[1] : sk[0];
     const int g = s_ord[lo];
     const bool sh = g == E;
     const int b = s_b[g];
     const int n = s_n[g];
     const int nch = (n + G::TOK - 1) / G::TOK;
-    const int local = li - pref[lo];
+    const int local = it - s_pref[phase][lo];
     const int blk = local / nch, chunk = local % nch;  // chunks of one tile block are claimed together
     const int fe = sh ? L.fs : L.f;
     const int tiles = phase == 0 ? fe / kTileRows : L.d / kTileRows;

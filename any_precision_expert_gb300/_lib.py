@@ -61,6 +61,9 @@ _SIGS = {
     "pw_raise_expert_async": (i32, [vp, i32, i32, C.POINTER(U32P6 * 3), C.POINTER(U16P3), vp, vp]),
     "pw_prefetch_expert": (i32, [vp, i32, i32, C.POINTER(U32P6 * 3), C.POINTER(U16P3), vp]),
     "pw_get_expert_bitwidth": (i32, [vp, i32, P_i32]),
+    "pw_route_stats": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]),
+    "pw_expert_resident_bytes": (i32, [vp, i32, C.POINTER(C.c_uint64)]),
+    "pw_plan_bitwidths": (i32, [i32, vp, vp, vp, vp, vp, vp, C.c_uint64, vp, C.POINTER(C.c_uint64)]),
     "pw_workspace_size": (i32, [vp, i32, C.POINTER(sz)]),
     "pw_layer_check_device": (i32, [vp, vp]),
     "pw_pack_planes": (i32, [vp, i32, i32, C.POINTER(U32P6)]),

@@ -71,6 +71,36 @@ def _host_blocks(planes, w16):
     return arr, w
 
 
+LEVELS = (16, 6, 5, 4, 3)  # planner levels, least aggressive first
+
+
+def plan_bitwidths(sens, sizes, budget: int, mass=None, resid=None, floors=None, ceils=None):
+    """Staged greedy bitwidth plan (pw_plan_bitwidths): sens [E][4] damage at
+    3..6 bits, sizes [E][5] bytes at 16, 6, 5, 4, 3 bits, budget in bytes;
+    mass / resid [E] from Layer.route_stats (None switches a signal off).
+    Returns (bits int32 [E], bytes used, feasible)."""
+    sens = _host(np.asarray(sens, dtype=np.float64), np.float64)
+    E = sens.shape[0]
+    sizes = _host(np.asarray(sizes, dtype=np.uint64), np.uint64)
+    if sens.shape != (E, 4) or sizes.shape != (E, 5):
+        raise ValueError("sens must be [E][4] and sizes [E][5]")
+
+    def opt(a, dtype):
+        return None if a is None else _host(np.asarray(a, dtype=dtype).reshape(E), dtype)
+    mass, resid = opt(mass, np.float64), opt(resid, np.float64)
+    floors, ceils = opt(floors, np.int32), opt(ceils, np.int32)
+    bits = np.zeros(E, dtype=np.int32)
+    used = C.c_uint64(0)
+
+    def ptr(a):
+        return None if a is None else a.ctypes.data
+    st = lib.pw_plan_bitwidths(E, ptr(sens), ptr(mass), ptr(resid), ptr(floors), ptr(ceils), ptr(sizes),
+                               int(budget), bits.ctypes.data, C.byref(used))
+    if st not in (0, 3):  # PW_OK, PW_ERR_OOM (infeasible: the floors)
+        check(st, "pw_plan_bitwidths")
+    return bits, int(used.value), st == 0
+
+
 class Pool:
     """Page pool over one device buffer (a torch uint8 tensor)."""
 
@@ -168,6 +198,30 @@ class Layer:
         check(lib.pw_get_expert_bitwidth(self.handle, e, C.byref(b)), "pw_get_expert_bitwidth")
         return b.value
 
+    def expert_resident_bytes(self, bits: int) -> int:
+        n = C.c_uint64(0)
+        check(lib.pw_expert_resident_bytes(self.handle, bits, C.byref(n)), "pw_expert_resident_bytes")
+        return n.value
+
+    def plan_sizes(self):
+        """Bytes one expert holds at 16, 6, 5, 4, 3 bits (the planner's size row)."""
+        return [self.expert_resident_bytes(b) for b in LEVELS]
+
+    def apply_plan(self, bits, stream=None):
+        """Set every expert to its planned bitwidth in stream order (lowering
+        unmaps planes; raising re-maps planes still held).  Returns the experts
+        whose planes are gone and need pw_raise_expert_async with host data."""
+        missing = []
+        for e, b in enumerate(np.asarray(bits).tolist()):
+            if self.get_expert_bitwidth(e) == b:
+                continue
+            st = self.try_set_expert_bitwidth(e, int(b), stream)
+            if st == 4:  # PW_ERR_NOT_RESIDENT
+                missing.append(e)
+            else:
+                check(st, f"pw_set_expert_bitwidth(e={e}, bits={b})")
+        return missing
+
     def workspace_size(self, T: int) -> int:
         n = C.c_size_t(0)
         check(lib.pw_workspace_size(self.handle, T, C.byref(n)), "pw_workspace_size")
@@ -180,6 +234,10 @@ class Layer:
     def route_topk(self, x, wr, bias, T, idx, w, counts=None, stream=None):
         check(lib.pw_route_topk(self.handle, _p(x), _p(wr), _p(bias), T, _p(idx), _p(w), _p(counts),
                                 _s(stream)), "pw_route_topk")
+
+    def route_stats(self, x, idx, w, T, mass, resid, ws, stream=None):
+        check(lib.pw_route_stats(self.handle, _p(x), _p(idx), _p(w), T, _p(mass), _p(resid), _p(ws),
+                                 ws.numel() * ws.element_size(), _s(stream)), "pw_route_stats")
 
     def permute(self, idx, T, x, offsets, perm_src, inv_slot, x_perm, ws, stream=None):
         check(lib.pw_permute(self.handle, _p(idx), T, _p(x), _p(offsets), _p(perm_src), _p(inv_slot),

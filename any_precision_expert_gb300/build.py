@@ -19,8 +19,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpw.so")
 
-SOURCES = ["pw_runtime.cpp", "pw_pack.cpp", "pw_kernels.cu", "pw_ffn.cu", "pw_decode.cu", "pw_prefill.cu",
-           "pw_noalloc.cu"]
+SOURCES = ["pw_runtime.cpp", "pw_pack.cpp", "pw_planner.cpp", "pw_kernels.cu", "pw_ffn.cu", "pw_decode.cu",
+           "pw_prefill.cu", "pw_noalloc.cu"]
+# the planner compares doubles: no fused multiply-adds, so x86 and Arm hosts plan alike
+SOURCE_FLAGS = {"pw_planner.cpp": ["-Xcompiler", "-ffp-contract=off"]}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,7 +40,7 @@ def _flags(extra=()):
 
 def _compile(src: str, extra, verbose: bool):
     obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [_nvcc(), *_flags(extra), "-c", os.path.join(CSRC, src), "-o", obj]
+    cmd = [_nvcc(), *_flags([*extra, *SOURCE_FLAGS.get(src, [])]), "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -73,6 +73,9 @@ int decode_max_tokens(int ffn);
 int decode_max_tokens_shared();
 cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
                            int n_slots, int min_tokens, __half* h, float* y, cudaStream_t s);
+// Routing mass and prompt residual per expert (norms: T floats of scratch).
+cudaError_t launch_route_stats(const DevLayer& L, const __half* x, const int* idx, const float* w, int T,
+                               float* mass, float* resid, float* norms, cudaStream_t s);
 cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* inv_slot,
                            const float* w, int T, const float* y_shared, __half* y, cudaStream_t s);
 cudaError_t launch_debug_dequant(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);

@@ -410,4 +410,86 @@ cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* in
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// planner signals: routing mass and prompt residual per expert (write-up
+// "内存的饥饿游戏", section 三层感知: routing statistics and the
+// routing-weighted input norm)
+// ---------------------------------------------------------------------------
+
+constexpr int kStatThreads = 256;
+
+// ||x[t]||_2 for every token, one warp per token; lanes add strided
+// 8-element pieces, then a fixed butterfly: deterministic.
+__global__ void __launch_bounds__(kStatThreads) token_norm_kernel(const __half* __restrict__ x, int T, int d,
+                                                                 float* __restrict__ norms) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (kStatThreads / 32) + warp;
+  if (t >= T) return;
+  const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+  float acc = 0.f;
+  for (int j = lane; j < d / 8; j += 32) {
+    const uint4 v = row[j];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+      acc = fmaf(f.x, f.x, acc);
+      acc = fmaf(f.y, f.y, acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) norms[t] = sqrtf(acc);
+}
+
+// One CTA per expert: thread i adds the slots i, i + 256, ... routed to the
+// expert, then the CTA sums the threads in a fixed tree.
+__global__ void __launch_bounds__(kStatThreads) expert_stats_kernel(const int* __restrict__ idx,
+                                                                   const float* __restrict__ w,
+                                                                   const float* __restrict__ norms, int S, int K,
+                                                                   float* __restrict__ mass,
+                                                                   float* __restrict__ resid) {
+  __shared__ float sm[kStatThreads / 32], sr[kStatThreads / 32];
+  const int e = blockIdx.x;
+  float m = 0.f, r = 0.f;
+  for (int i = threadIdx.x; i < S; i += kStatThreads) {
+    if (idx[i] == e) {
+      const float wi = w[i];
+      m += wi;
+      r = fmaf(wi, norms[i / K], r);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m += __shfl_xor_sync(0xffffffffu, m, o);
+    r += __shfl_xor_sync(0xffffffffu, r, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sm[warp] = m;
+    sr[warp] = r;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tm = 0.f, tr = 0.f;
+    for (int k = 0; k < kStatThreads / 32; ++k) {
+      tm += sm[k];
+      tr += sr[k];
+    }
+    mass[e] = tm;
+    resid[e] = tr;
+  }
+}
+
+cudaError_t launch_route_stats(const DevLayer& L, const __half* x, const int* idx, const float* w, int T,
+                               float* mass, float* resid, float* norms, cudaStream_t s) {
+  if (T > 0) {
+    token_norm_kernel<<<(T + kStatThreads / 32 - 1) / (kStatThreads / 32), kStatThreads, 0, s>>>(x, T, L.d, norms);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  expert_stats_kernel<<<L.E, kStatThreads, 0, s>>>(idx, w, norms, T * L.K, L.K, mass, resid);
+  return cudaGetLastError();
+}
+
 }  // namespace pw

@@ -965,6 +965,27 @@ extern "C" pw_status pw_route_topk(pw_layer_t l, const void* x, const void* wr, 
                                idx, w, expert_count, as_stream(stream)));
 }
 
+extern "C" pw_status pw_route_stats(pw_layer_t l, const void* x, const int32_t* idx, const float* w, int T,
+                                    float* mass, float* resid, void* ws, size_t ws_bytes, void* stream) {
+  PW_TRY(check_layer(l));
+  if (T < 0 || !mass || !resid) return PW_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !idx || !w || !ws)) return PW_ERR_INVALID_ARG;
+  if (T > 0 && !aligned16(x)) return PW_ERR_INVALID_ARG;
+  if (T > 0 && ws_bytes < (size_t)T * sizeof(float)) return PW_ERR_OOM;
+  PW_TRY(device_only());
+  return launched(launch_route_stats(l->dev(), static_cast<const __half*>(x), idx, w, T, mass, resid,
+                                     static_cast<float*>(ws), as_stream(stream)));
+}
+
+extern "C" pw_status pw_expert_resident_bytes(pw_layer_t l, int bits, uint64_t* bytes) {
+  PW_TRY(check_layer(l));
+  if (!bytes || !valid_bits(bits)) return PW_ERR_INVALID_ARG;
+  const uint64_t pb = l->pool->page_bytes;
+  const uint64_t planes = (uint64_t)(bits == 16 ? kPlanes : bits) * (uint64_t)l->pmax;
+  *bytes = (planes + (bits == 16 ? (uint64_t)l->pmax16 : 0)) * pb;
+  return PW_OK;
+}
+
 extern "C" pw_status pw_permute(pw_layer_t l, const int32_t* idx, int T, const void* x, int32_t* offsets,
                                 int32_t* perm_src, int32_t* inv_slot, void* x_perm, void* ws, size_t ws_bytes,
                                 void* stream) {

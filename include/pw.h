@@ -282,6 +282,58 @@ pw_status pw_get_expert_bitwidth(pw_layer_t layer, int e, int* bits);
 /* Scratch bytes that pw_permute / pw_expert_ffn_bitplane / pw_shared_ffn need for T tokens. */
 pw_status pw_workspace_size(pw_layer_t layer, int T, size_t* bytes);
 
+/* ---------------------------------------------------------------------------
+ * Quality-aware bitwidth planning (PagedWeight write-up "内存的饥饿游戏",
+ * sections 三层感知 and 安全边界与异步搬运; budget M_w = M_total - M_kv and
+ * the greedy approximation from "动态量化优化MoE模型服务", 方法与技术路线).
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Online signals of the planner for one routed batch (the router's outputs):
+ *   mass[e]  = sum of w[t][k] over the slots with idx[t][k] == e
+ *              ("routing mass": protects busy experts),
+ *   resid[e] = sum of w[t][k] * ||x[t]||_2 over the same slots
+ *              ("prompt residual": the routing-weighted input norm).
+ *   x     device fp16 [T][d]      idx device int32 [T][K]   w device fp32 [T][K]
+ *   mass, resid  device fp32 [E], overwritten.
+ *   ws    device scratch of at least 4*T bytes (token norms).
+ * fp32 accumulation in a fixed order: deterministic.  T may be 0 (zeros).
+ */
+pw_status pw_route_stats(pw_layer_t layer, const void* x, const int32_t* idx, const float* w, int T,
+                         float* mass, float* resid, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Pool bytes one expert of this layer holds at bitwidth `bits` (3..6: that
+ * many plane blocks; 16: the fp16 block and all six plane blocks, so that
+ * lowering from 16 moves no data).  Host only; the planner's size table.
+ */
+pw_status pw_expert_resident_bytes(pw_layer_t layer, int bits, uint64_t* bytes);
+
+/*
+ * Staged greedy bitwidth plan under a byte budget (host only, no layer).
+ *   sens    host [E][4]  offline damage of each expert at 3, 4, 5, 6 bits
+ *                        (0 at 16); any non-negative scale
+ *   mass    host [E] or NULL, resid host [E] or NULL (pw_route_stats; NULL
+ *                        switches the factor off)
+ *   floors  host [E] or NULL (3): lowest bitwidth allowed per expert
+ *   ceils   host [E] or NULL (16): highest (the plan starts there)
+ *   sizes   host [E][5]  bytes of each expert at 16, 6, 5, 4, 3 bits
+ *   budget  bytes the experts may hold (M_w = M_total - M_kv - fixed)
+ *   bits    host [E] out: the plan;  used  host out: its bytes
+ * Expert weight = (mass_e / sum mass) * ((resid_e / mass_e) / (sum resid /
+ * sum mass)) (1 / E and 1 when a signal is NULL; ratio 1 for an expert
+ * without mass); damage(e, b) = weight_e * sens[e][b].  Stages lower the
+ * levels 16 -> 6 -> 5 -> 4 -> 3 one at a time, never below a floor; inside a
+ * stage, while over budget, the expert whose next step down costs the least
+ * damage per byte saved moves (ties: lower index).  Sums run in index order
+ * in double.  Returns PW_ERR_OOM (bits = floors, *used their bytes) when even
+ * the floors exceed the budget; PW_ERR_INVALID_ARG for bad arguments
+ * (E < 1, negative values, floors not in {3,4,5,6,16} or above ceils).
+ */
+pw_status pw_plan_bitwidths(int E, const double* sens, const double* mass, const double* resid,
+                            const int* floors, const int* ceils, const uint64_t* sizes, uint64_t budget,
+                            int* bits, uint64_t* used);
+
 /*
  * Reads (synchronously) and clears the layer's device error word, set by
  * bounded device-side waits or bounds checks of earlier launches.

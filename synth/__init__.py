@@ -7,7 +7,7 @@ no permutation, no dequantisation, no FFN.  Both the fp64 oracle tests and the
 GPU tests/bench take their inputs from here.
 """
 from .workloads import (CONFIGS, LayerConfig, get_config, make_router, make_expert,
-                        make_shared, make_tokens, bits_plan, zipf_bias)
+                        make_sensitivity, make_shared, make_tokens, bits_plan, zipf_bias)
 
-__all__ = ["CONFIGS", "LayerConfig", "get_config", "make_router", "make_expert",
+__all__ = ["CONFIGS", "LayerConfig", "get_config", "make_router", "make_expert", "make_sensitivity",
            "make_shared", "make_tokens", "bits_plan", "zipf_bias"]

@@ -28,7 +28,7 @@ from typing import List, Optional
 import numpy as np
 
 # generator purpose keys
-_ROUTER, _BIASPERM, _CODE, _LUT, _W16, _SHARED, _TOKENS, _BITS, _SWEEP = range(1, 10)
+_ROUTER, _BIASPERM, _CODE, _LUT, _W16, _SHARED, _TOKENS, _BITS, _SWEEP, _SENS = range(1, 11)
 
 BITS_ALLOWED = (3, 4, 5, 6, 16)
 
@@ -175,6 +175,19 @@ def bits_plan(cfg: LayerConfig, seed: int = 0, layer: int = 0) -> np.ndarray:
     if rule == "sweep":
         return np.array([(6, 5, 4, 3, 16)[(e + layer) % 5] for e in range(E)], dtype=np.int32)
     raise ValueError(rule)
+
+
+def make_sensitivity(cfg: LayerConfig, seed: int = 0, layer: int = 0) -> np.ndarray:
+    """Synthetic offline sensitivity table, float64 [E, 4] for b = 3, 4, 5, 6.
+
+    Stand-in for the Hessian-weighted sensitivity table that the write-up
+    builds offline from calibration data (section "三层感知"; no trained
+    weights or data exist here): expert e's damage at b bits is
+    s_e * 4^(6 - b) (quantisation noise power drops 4x per bit), with
+    s_e ~ lognormal(0, 1) drawn per (layer, expert).
+    """
+    s = _rng(seed, _SENS, layer).lognormal(0.0, 1.0, size=cfg.E)
+    return np.stack([s * 4.0 ** (6 - b) for b in (3, 4, 5, 6)], axis=1)
 
 
 def initial_bits_for(cfg: LayerConfig, e: int, seed: int = 0, layer: int = 0) -> int:

@@ -767,14 +767,15 @@ def _threads():
 
 
 def cpu_baseline(wl, seconds=20.0):
-    """Time the oracle on a bounded sample (the first tokens of the batch)."""
+    """Time the oracle on a bounded sample: tokens of the batch one per call
+    until `seconds` of CPU work (at most 1024 calls)."""
     from oracle import pw_oracle as O
 
     cfg = wl["cfg"]
     x = wl["xs"][0]
     done, tokens, t_start = 0, 0, time.perf_counter()
     n = 1
-    while time.perf_counter() - t_start < seconds and done < 64:
+    while time.perf_counter() - t_start < seconds and done < 1024:
         O.moe_tokens(x, wl["wr"], wl["bias"], lambda e: wl["experts"][e], wl["bits"], cfg.K, cfg.renormalize,
                      list(range(done % x.shape[0], done % x.shape[0] + n)), shared=wl["shared"])
         done += 1

@@ -128,3 +128,15 @@ def test_split_down_reduction_all_bitwidths(f):
             gl.check_forward(gl.tokens(T))
     finally:
         gl.close()
+
+
+def test_odd_shapes_all_bitwidths():
+    # d = 192 (three 64-column chunks per down tile row block, 12 down tiles)
+    # and f = 320 (five chunks: one whole plane group and a ragged one)
+    cfg = get_config("qwen", d=192, f=320, E=5, K=2, shared_ffn=320)
+    gl = GpuLayer(cfg, seed=9, bits=[3, 4, 5, 6, 16])
+    try:
+        for T in (1, 7, 40):
+            gl.check_forward(gl.tokens(T))
+    finally:
+        gl.close()

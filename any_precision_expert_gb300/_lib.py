@@ -57,6 +57,8 @@ _SIGS = {
     "pw_shared_ffn": (i32, [vp, vp, i32, vp, vp, sz, vp]),
     "pw_moe_ffn": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]),
     "pw_combine": (i32, [vp, vp, vp, vp, i32, vp, vp, vp]),
+    "pw_moe_forward": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]),
+    "pw_moe_forward_workspace_size": (i32, [vp, i32, C.POINTER(sz)]),
     "pw_set_expert_bitwidth": (i32, [vp, i32, i32, vp]),
     "pw_raise_expert_async": (i32, [vp, i32, i32, C.POINTER(U32P6 * 3), C.POINTER(U16P3), vp, vp]),
     "pw_prefetch_expert": (i32, [vp, i32, i32, C.POINTER(U32P6 * 3), C.POINTER(U16P3), vp]),

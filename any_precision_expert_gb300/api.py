@@ -222,6 +222,11 @@ class Layer:
                 check(st, f"pw_set_expert_bitwidth(e={e}, bits={b})")
         return missing
 
+    def forward_workspace_size(self, T: int) -> int:
+        n = C.c_size_t(0)
+        check(lib.pw_moe_forward_workspace_size(self.handle, T, C.byref(n)), "pw_moe_forward_workspace_size")
+        return n.value
+
     def workspace_size(self, T: int) -> int:
         n = C.c_size_t(0)
         check(lib.pw_workspace_size(self.handle, T, C.byref(n)), "pw_workspace_size")
@@ -255,6 +260,11 @@ class Layer:
         check(lib.pw_moe_ffn(self.handle, _p(x), _p(x_perm), _p(offsets), T, _p(y_perm), _p(y_shared), _p(ws),
                              ws.numel() * ws.element_size(), _s(stream)), "pw_moe_ffn")
 
+    def forward(self, x, wr, bias, T, idx, w, y, ws, stream=None):
+        """The whole layer (pw_moe_forward): routing into idx / w, output y."""
+        check(lib.pw_moe_forward(self.handle, _p(x), _p(wr), _p(bias), T, _p(idx), _p(w), _p(y), _p(ws),
+                                 ws.numel() * ws.element_size(), _s(stream)), "pw_moe_forward")
+
     def combine(self, y_perm, inv_slot, w, T, y_shared, y, stream=None):
         check(lib.pw_combine(self.handle, _p(y_perm), _p(inv_slot), _p(w), T, _p(y_shared), _p(y), _s(stream)),
               "pw_combine")
@@ -286,6 +296,14 @@ class Buffers:
                          if layer.fs else None)
         self.y = torch.empty((T_max, d), dtype=torch.float16, device=device)
         self.ws = torch.empty(max(layer.workspace_size(T_max), 256), dtype=torch.uint8, device=device)
+        self.fws = torch.empty(max(layer.forward_workspace_size(T_max), 256), dtype=torch.uint8, device=device)
+
+
+def moe_forward_fused(layer: Layer, x, wr, bias, buf: Buffers, stream=None):
+    """The whole hot path for x [T, d] in one library call (pw_moe_forward); returns buf.y[:T]."""
+    T = x.shape[0]
+    layer.forward(x, wr, bias, T, buf.idx, buf.w, buf.y, buf.fws, stream)
+    return buf.y[:T]
 
 
 def moe_forward(layer: Layer, x, wr, bias, buf: Buffers, stream=None):

@@ -29,6 +29,13 @@
 // fp32.  Each weight kind has a single copy of its loop body (the kernel's
 // instruction footprint stays small).
 //
+// Fused layer step (FUSED): given the router's output, the kernel also does
+// the permutation and the combine -- every CTA sorts the (at most 512) slots
+// by expert in shared memory itself (stable: ascending flat order inside an
+// expert), routed rows are staged straight from x, and when every down item
+// is done the CTAs add y[t] = sum_k w[t][k] y_perm[slot(t, k)] (+ the shared
+// FFN) in k order, as the separate combine does.
+//
 // CTAs claim items from one counter in a fixed order: groups in the order
 // shared FFN, fp16, 4..6-bit, 3-bit experts; a group's down items (phase 1)
 // follow about one wave of CTAs after its gate/up items (phase 0), so that
@@ -50,6 +57,7 @@ constexpr int kCtaThreads = 128;
 constexpr int kCtaWarps = kCtaThreads / 32;
 constexpr int kTabW = 64 * 8 * 4;            // LUT table of one warp: 2^b entries x 8 row pairs x 4 B (b <= 6)
 constexpr long long kSpinLimit = 1ll << 22;  // polls of a phase counter (about a second)
+constexpr int kFusedSlots = 512;             // routed slots (T * K) of a fused layer step
 
 // Items take up to 32 tokens (a weight tile is streamed and decoded once for
 // up to 32 tokens).  Shared memory: two K-block buffers of token rows, a LUT
@@ -92,6 +100,12 @@ struct UniParams {
   __half* hs;          // [T][fs]
   float* y;            // [n_slots][d]
   float* ys;           // [T][d]
+  // fused layer step only: the routing result replaces offsets / x_perm, and
+  // the kernel ends with the weighted combine
+  const int* idx;      // [T][K] experts of each token
+  const float* wk;     // [T][K] routing weights
+  __half* yout;        // [T][d] layer output
+  int* offsets_out;    // [E+1] slot offsets (written by CTA 0), or null
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -515,7 +529,7 @@ __device__ __forceinline__ int down_split(int n, int K) {
 
 __device__ __forceinline__ bool is_tab(int b) { return b >= 4 && b <= 6; }
 
-template <bool SPLITK>
+template <bool SPLITK, bool FUSED>
 __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniParams P) {
   using G = Geo;
   extern __shared__ __align__(128) unsigned char smem_uni[];
@@ -525,20 +539,86 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
   __shared__ short s_ord[kMaxExperts + 1];  // groups in claim order
   __shared__ int s_pref[2][kMaxExperts + 2];  // claim position of each group's gate/up and down segment
   __shared__ short s_ins[kMaxExperts + 1];
-  __shared__ int s_ng, s_it, s_total;
+  __shared__ int s_ng, s_it, s_total, s_total1;
   __shared__ int s_tok[G::TOK];
+  __shared__ int s_pos[kMaxTopK];
+  __shared__ float s_w[kMaxTopK];
+  __shared__ short s_perm[FUSED ? kFusedSlots : 1];  // fused: token of each sorted slot
 
   const DevLayer& L = P.L;
   const int E = L.E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int* const q = L.sync;                             // claim counter, CTA exit counter
+  int* const q = L.sync;                             // claim counter, CTA exit counter, -, -, down items done
   int* const done0 = L.sync + kSyncHeader;           // [E+1][kSyncChunks] gate/up tiles done
   int* const done1 = done0 + (E + 1) * kSyncChunks;  // [E+1][kSyncChunks] down tiles done
 
+  const int n_slots = P.T * L.K;  // routed slots (fused step)
+  if constexpr (FUSED) {
+    // slot counts per expert from the routing result, then their prefix
+    for (int g = tid; g <= E; g += kCtaThreads) s_n[g] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_slots; i += kCtaThreads) {
+      const int e = P.idx[i];
+      if ((unsigned)e < (unsigned)E) atomicAdd(&s_n[e], 1);
+      else atomicExch(L.err, 2);  // not a routing result: the slot is dropped
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int run = 0;
+      for (int g0 = 0; g0 < E; g0 += 32) {
+        const int g = g0 + lane;
+        const int c = g < E ? s_n[g] : 0;
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (g < E) s_base[g] = run + incl - c;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && P.offsets_out)
+      for (int g = tid; g <= E; g += kCtaThreads) P.offsets_out[g] = g < E ? s_base[g] : n_slots;
+    // token of every sorted slot (stable: ascending flat order inside an
+    // expert), one warp, 32 slots at a time; s_pref[0] holds the running
+    // position of each expert meanwhile
+    if (warp == 0) {
+      constexpr int kBatches = kFusedSlots / 32;
+      int ev[kBatches];  // every slot's expert, loaded at once (one memory round trip)
+#pragma unroll
+      for (int b = 0; b < kBatches; ++b) {
+        const int j = b * 32 + lane;
+        ev[b] = j < n_slots ? min(max(P.idx[j], 0), E - 1) : -1 - lane;
+      }
+      for (int g = lane; g < E; g += 32) s_pref[0][g] = s_base[g];
+      __syncwarp();
+#pragma unroll
+      for (int b = 0; b < kBatches; ++b) {
+        if (b * 32 < n_slots) {
+          const int j = b * 32 + lane, e = ev[b];
+          const unsigned same = __match_any_sync(0xffffffffu, e);
+          if (j < n_slots) {
+            const int pos = s_pref[0][e] + __popc(same & ((1u << lane) - 1));
+            if (pos < kFusedSlots) s_perm[pos] = (short)(j / L.K);
+          }
+          __syncwarp();
+          if (j < n_slots && (same & ((1u << lane) - 1)) == 0) s_pref[0][e] += __popc(same);
+          __syncwarp();
+        }
+      }
+    }
+    __syncthreads();
+  }
   for (int g = tid; g <= E; g += kCtaThreads) {
     int base = 0, n = 0, b = 16;
     if (g < E) {
-      if (P.offsets) {
+      if (FUSED) {
+        base = s_base[g];
+        n = s_n[g];
+        b = L.bits[g];
+      } else if (P.offsets) {
         base = P.offsets[g];
         n = P.offsets[g + 1] - base;
         b = L.bits[g];
@@ -546,7 +626,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
                           (is_tab(b) && (P.bit_mask & 4));
         if (!take || n > P.max_tokens) n = 0;
       }
-    } else if (P.x) {
+    } else if (P.x && L.fs) {  // the shared FFN (x doubles as the routed input of a fused step)
       n = P.T;
     }
     s_base[g] = base;
@@ -570,6 +650,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
         ng += __popc(m);
       }
     }
+    __syncwarp();
     for (int ph = 0; ph < 2; ++ph) {
       int run = 0;
       for (int k0 = 0; k0 < ng; k0 += 32) {
@@ -634,6 +715,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
       }
     }
     const int total = s_pref[0][ng] + s_pref[1][ng];
+    const int total1 = s_pref[1][ng];
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
@@ -646,6 +728,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     if (lane == 0) {
       s_ng = ng;
       s_total = total;
+      s_total1 = total1;
     }
   }
   const uint32_t slab = smem_u32(smem_uni);
@@ -692,12 +775,16 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     A.ntok = min(G::TOK, n - chunk * G::TOK);
     A.NT = (A.ntok + 7) >> 3;
     A.K = phase == 0 ? L.d : fe;
-    A.act = phase == 0 ? (sh ? P.x : P.xp) : (sh ? P.hs : P.h);
+    A.act = phase == 0 ? (sh || FUSED ? P.x : P.xp) : (sh ? P.hs : P.h);
     A.ld = phase == 0 ? fe : L.d;
     A.h = sh ? P.hs : P.h;
     A.y = sh ? P.ys : P.y;
 
-    if (tid < A.ntok) s_tok[tid] = A.row0 + tid;
+    if (FUSED && phase == 0 && !sh) {
+      if (tid < A.ntok) s_tok[tid] = s_perm[min(A.row0 + tid, kFusedSlots - 1)];  // tokens of the item's slots
+    } else if (tid < A.ntok) {
+      s_tok[tid] = A.row0 + tid;
+    }
     if (phase == 1 && tid == 0) {  // h of this chunk must be complete
       const int need = fe / kTileRows;
       long long spins = 0;
@@ -721,11 +808,75 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
       __threadfence();
       if (phase == 0) {
         atomicAdd(done0 + sidx, done_tiles);
-      } else if (atomicAdd(done1 + sidx, done_tiles) == tiles - done_tiles) {
-        // the last down tiles of this (group, chunk) clear both counters
-        atomicExch(done0 + sidx, 0);
-        atomicExch(done1 + sidx, 0);
+      } else {
+        if (atomicAdd(done1 + sidx, done_tiles) == tiles - done_tiles) {
+          // the last down tiles of this (group, chunk) clear both counters
+          atomicExch(done0 + sidx, 0);
+          atomicExch(done1 + sidx, 0);
+        }
+        if (FUSED) atomicAdd(q + 4, 1);
       }
+    }
+  }
+
+  if constexpr (FUSED) {
+    // combine once every down item is done (all were claimed, none waits on a later one)
+    if (tid == 0) {
+      long long spins = 0;
+      while (ld_acquire(q + 4) < s_total1) {
+        if (++spins > kSpinLimit) {
+          atomicExch(L.err, 1);
+          break;
+        }
+        __nanosleep(100);
+      }
+    }
+    __syncthreads();
+    const int K = L.K, d4 = L.d / 4;
+    for (int t = blockIdx.x; t < P.T; t += gridDim.x) {
+      for (int k = warp; k < K; k += kCtaWarps) {
+        // sorted slot of (t, k): the one slot of token t in expert e's bucket
+        const int flat = t * K + k, e = min(max(P.idx[flat], 0), E - 1);
+        const int lo = s_base[e], hi = min(lo + s_n[e], kFusedSlots);
+        int pos = lo;
+        for (int p0 = lo; p0 < hi; p0 += 32) {
+          const int pp = p0 + lane;
+          const unsigned m = __ballot_sync(0xffffffffu, pp < hi && s_perm[pp] == t);
+          if (m) {
+            pos = p0 + __ffs(m) - 1;
+            break;
+          }
+        }
+        if (lane == 0) {
+          s_pos[k] = pos;
+          s_w[k] = P.wk[flat];
+        }
+      }
+      __syncthreads();
+      for (int c4 = tid; c4 < d4; c4 += kCtaThreads) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < K; ++k) {
+          const float wkk = s_w[k];
+          const float4 v = reinterpret_cast<const float4*>(P.y + (size_t)s_pos[k] * L.d)[c4];
+          acc.x = fmaf(wkk, v.x, acc.x);
+          acc.y = fmaf(wkk, v.y, acc.y);
+          acc.z = fmaf(wkk, v.z, acc.z);
+          acc.w = fmaf(wkk, v.w, acc.w);
+        }
+        if (P.ys) {
+          const float4 v = reinterpret_cast<const float4*>(P.ys + (size_t)t * L.d)[c4];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+        uint2 out;
+        out.x = *reinterpret_cast<uint32_t*>(&lo);
+        out.y = *reinterpret_cast<uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(P.yout + (size_t)t * L.d)[c4] = out;
+      }
+      __syncthreads();
     }
   }
 
@@ -733,16 +884,30 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     __threadfence();
     if (atomicAdd(q + 1, 1) == (int)gridDim.x - 1) {  // last CTA out: no claims remain
       atomicExch(q, 0);
+      if (FUSED) atomicExch(q + 4, 0);
       atomicExch(q + 1, 0);
     }
   }
+}
+
+template <bool FUSED>
+static cudaError_t launch_cta(const UniParams& P, int T, cudaStream_t s) {
+  // The split paths depend on the batch size only, so a routed call, a shared
+  // call and the combined call compute every item the same way.
+  const bool splitk = T <= 16;
+  const void* fn = splitk ? (const void*)ffn_cta_kernel<true, FUSED> : (const void*)ffn_cta_kernel<false, FUSED>;
+  cudaError_t e;
+  if ((e = ensure_smem(fn, Geo::SMEM)) != cudaSuccess) return e;
+  if (splitk) ffn_cta_kernel<true, FUSED><<<sm_count() * Geo::BLOCKS, kCtaThreads, Geo::SMEM, s>>>(P);
+  else ffn_cta_kernel<false, FUSED><<<sm_count() * Geo::BLOCKS, kCtaThreads, Geo::SMEM, s>>>(P);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
                        int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s) {
   if (max_tokens > kSyncChunks * 16 || (x && T > kSyncChunks * 16)) return cudaErrorInvalidValue;
   if (!bit_mask && !x) return cudaSuccess;
-  UniParams P;
+  UniParams P{};
   P.L = L;
   P.x = x;
   P.xp = x_perm;
@@ -754,15 +919,27 @@ cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm,
   P.hs = hs;
   P.y = y;
   P.ys = ys;
-  // The split paths depend on the batch size only, so a routed call, a shared
-  // call and the combined call compute every item the same way.
-  const bool splitk = T <= 16;
-  const void* fn = splitk ? (const void*)ffn_cta_kernel<true> : (const void*)ffn_cta_kernel<false>;
-  cudaError_t e;
-  if ((e = ensure_smem(fn, Geo::SMEM)) != cudaSuccess) return e;
-  if (splitk) ffn_cta_kernel<true><<<sm_count() * Geo::BLOCKS, kCtaThreads, Geo::SMEM, s>>>(P);
-  else ffn_cta_kernel<false><<<sm_count() * Geo::BLOCKS, kCtaThreads, Geo::SMEM, s>>>(P);
-  return cudaGetLastError();
+  return launch_cta<false>(P, T, s);
+}
+
+cudaError_t launch_layer_fused(const DevLayer& L, const __half* x, const int* idx, const float* w, int T, __half* h,
+                               __half* hs, float* y_perm, float* ys, __half* y, int* offsets_out, cudaStream_t s) {
+  if (T > kSyncChunks * 16 || T * L.K > kFusedSlots) return cudaErrorInvalidValue;
+  UniParams P{};
+  P.L = L;
+  P.x = x;
+  P.T = T;
+  P.bit_mask = 7;
+  P.max_tokens = T;
+  P.h = h;
+  P.hs = L.fs ? hs : nullptr;
+  P.y = y_perm;
+  P.ys = L.fs ? ys : nullptr;
+  P.idx = idx;
+  P.wk = w;
+  P.yout = y;
+  P.offsets_out = offsets_out;
+  return launch_cta<true>(P, T, s);
 }
 
 }  // namespace pw

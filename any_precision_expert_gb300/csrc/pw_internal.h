@@ -69,6 +69,12 @@ cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* o
 // non-null, the shared FFN.
 cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
                        int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s);
+// Fused decode step for T tokens after the router: per-expert offsets from
+// idx, the expert FFN of every group (routed rows staged straight from x)
+// and the shared FFN, then the weighted combine into y.  Every expert must be
+// decode-sized (T at most the decode token thresholds).
+cudaError_t launch_layer_fused(const DevLayer& L, const __half* x, const int* idx, const float* w, int T, __half* h,
+                               __half* hs, float* y_perm, float* ys, __half* y, int* offsets_out, cudaStream_t s);
 int decode_max_tokens(int ffn);
 int decode_max_tokens_shared();
 cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,

@@ -213,9 +213,11 @@ def run_gpu(args):
     NL = len(layers)
     stream = torch.cuda.Stream()
 
+    fused = _fused_step(cfg, T)
+
     def step(i, s):
         j = i % NL
-        pw.moe_forward(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=s)
+        pw.moe_forward_fused(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=s)
 
     # warm-up (eager), then routing is fixed per copy: algorithmic bytes per step
     with torch.cuda.stream(stream):
@@ -224,12 +226,14 @@ def run_gpu(args):
     torch.cuda.synchronize()
     ffn_bytes, step_bytes = [], []
     for j in range(NL):
-        off = bufs[j].offsets.cpu().numpy()
+        counts = np.bincount(bufs[j].idx[:T].cpu().numpy().reshape(-1), minlength=cfg.E)
+        off = np.concatenate([[0], np.cumsum(counts)])
         fb, sb = algorithmic_bytes(cfg, wl["bits"], off, T)
         ffn_bytes.append(fb)
         step_bytes.append(sb)
 
-    # one CUDA graph of K steps, with events around each expert-FFN call.  The
+    # one CUDA graph of K steps, with events around each expert-FFN call (the
+    # whole-layer call when the step runs as router + one fused kernel).  The
     # events are "external" graph nodes (timed when the graph runs); where the
     # installed torch lacks them, each step is three graphs with ordinary
     # events between them and the GPU is held briefly so the host can queue
@@ -245,14 +249,19 @@ def run_gpu(args):
     ev_b = [mk_event() for _ in range(K)]
 
     def part_a(L, b, x):
-        L.route_topk(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, None, stream)
-        L.permute(b.idx, T, x, b.offsets, b.perm_src, b.inv_slot, b.x_perm, b.ws, stream)
+        if not fused:
+            L.route_topk(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, None, stream)
+            L.permute(b.idx, T, x, b.offsets, b.perm_src, b.inv_slot, b.x_perm, b.ws, stream)
 
     def part_f(L, b, x):
-        L.moe_ffn(x, b.x_perm, b.offsets, T, b.y_perm, b.y_shared if cfg.shared_ffn else None, b.ws, stream)
+        if fused:
+            L.forward(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, b.y, b.fws, stream)
+        else:
+            L.moe_ffn(x, b.x_perm, b.offsets, T, b.y_perm, b.y_shared if cfg.shared_ffn else None, b.ws, stream)
 
     def part_c(L, b, x):
-        L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared if cfg.shared_ffn else None, b.y, stream)
+        if not fused:
+            L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared if cfg.shared_ffn else None, b.y, stream)
 
     launches_per_step = _launches_per_step(cfg, T)
     if external:
@@ -335,7 +344,7 @@ def run_gpu(args):
         for i in range(KE):
             j = i % NL
             x_dev.copy_(x_host[j], non_blocking=True)
-            y = pw.moe_forward(layers[j], x_dev, wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+            y = pw.moe_forward_fused(layers[j], x_dev, wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
             y_host.copy_(y, non_blocking=True)
             stream.synchronize()
     barrier()
@@ -349,8 +358,13 @@ def run_gpu(args):
     else:
         peak, peak_src = 6800.0, "fallback 6.8 TB/s"
     ffn_flops = 2.0 * T * 3 * cfg.d * (cfg.K * cfg.f + cfg.shared_ffn)  # routed + shared FFN, algorithmic
+    # the timed call: the expert FFN, or the whole layer (router, x in, y out too) when fused
+    call_bytes = step_avg_bytes if fused else ffn_avg_bytes
+    call_name = ("whole-layer call pw_moe_forward (router + one persistent kernel: permutation, "
+                 "routed experts, shared FFN, combine)" if fused else
+                 "expert FFN call pw_moe_ffn (routed experts + shared FFN)")
     tflops = ffn_flops / (ffn_avg_ms * 1e-3) / 1e12
-    gbs = ffn_avg_bytes / (ffn_avg_ms * 1e-3) / 1e9
+    gbs = call_bytes / (ffn_avg_ms * 1e-3) / 1e9
     # decode batches are bound by weight bytes, prefill batches by the tensor pipe
     tensor_bound = T * cfg.K / cfg.E >= 256
     if tensor_bound:
@@ -393,7 +407,7 @@ def run_gpu(args):
                 "device_errors": not ok,
             },
             "roofline": ({
-                "kernel": "expert FFN call pw_moe_ffn (routed experts + shared FFN)",
+                "kernel": call_name,
                 "bound": "tensor",
                 "achieved": tflops,
                 "peak": tpk,
@@ -405,21 +419,21 @@ def run_gpu(args):
                 "avg_launch_ms": ffn_avg_ms,
                 "peak_source": tpk_src,
             } if tensor_bound else {
-                "kernel": "expert FFN call pw_moe_ffn (routed experts + shared FFN)",
+                "kernel": call_name,
                 "bound": "hbm",
                 "achieved": gbs,
                 "peak": peak,
                 "unit": "GB/s",
                 "frac": gbs / peak,
                 "traffic": traffic,
-                "algorithmic_bytes_per_launch": ffn_avg_bytes,
+                "algorithmic_bytes_per_launch": call_bytes,
                 "avg_launch_ms": ffn_avg_ms,
                 "peak_source": peak_src,
             }),
             "cpu_baseline": cpu,
             "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": T * cfg.d * 2,
                     "d2h_bytes_per_step": T * cfg.d * 2, "steps": KE,
-                    "note": "public API (moe_forward) per step: pinned H2D of x, layer, D2H of y, host sync"},
+                    "note": "public API (pw_moe_forward) per step: pinned H2D of x, layer, D2H of y, host sync"},
             "gpu_launches": launches_per_step * K,
             "clocks": clk,
         }
@@ -433,14 +447,27 @@ def run_gpu(args):
     return out
 
 
-def _launches_per_step(cfg, T):
-    """Kernels one step launches: router, permutation (histogram + scatter for
-    more than 1024 slots, or one fused kernel), row gather, the persistent
-    decode kernel (routed experts of every bitwidth up to the token threshold
-    and the shared FFN up to its own), the tcgen05 GEMM pair for experts above
-    the token threshold and for a shared FFN above its own, and the combine."""
+def _thresholds(cfg):
     thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "32" if cfg.f >= 4096 else "64")), 1024)
     thr_s = min(int(os.environ.get("PW_DECODE_MAX_TOK_SHARED", "256")), 1024)
+    return thr, thr_s
+
+
+def _fused_step(cfg, T):
+    """pw_moe_forward runs router + one fused kernel for decode batches of at most 16 tokens."""
+    thr, thr_s = _thresholds(cfg)
+    return T <= 16 and T <= thr and (not cfg.shared_ffn or T <= thr_s) and T * cfg.K <= 512
+
+
+def _launches_per_step(cfg, T):
+    """Kernels one step launches: the router and, when every group is
+    decode-sized, one fused kernel; otherwise the permutation (histogram +
+    scatter for more than 1024 slots, or one kernel), row gather, the
+    persistent decode kernel, the tcgen05 GEMM pair for experts above the
+    token threshold and for a shared FFN above its own, and the combine."""
+    thr, thr_s = _thresholds(cfg)
+    if _fused_step(cfg, T):
+        return 2
     S = T * cfg.K
     n = 1 + (2 if S > 1024 else 1) + 1
     n += 1
@@ -534,7 +561,7 @@ def run_sweep(args):
 
     def forward_all():
         for l in range(NL):
-            pw.moe_forward(layers[l], sw["xs_d"][l], sw["wr_d"][l], sw["bias_d"][l], bufs[l], stream=stream)
+            pw.moe_forward_fused(layers[l], sw["xs_d"][l], sw["wr_d"][l], sw["bias_d"][l], bufs[l], stream=stream)
 
     cur = [b.copy() for b in sw["init"]]
     plan = [sweep_changes(cfg, i, sw["init"]) for i in range(W + K)]
@@ -601,7 +628,7 @@ def run_sweep(args):
         for i in range(KE):
             for l in range(NL):
                 x_dev[l].copy_(x_host[l], non_blocking=True)
-                y = pw.moe_forward(layers[l], x_dev[l], sw["wr_d"][l], sw["bias_d"][l], bufs[l], stream=stream)
+                y = pw.moe_forward_fused(layers[l], x_dev[l], sw["wr_d"][l], sw["bias_d"][l], bufs[l], stream=stream)
                 y_host[l].copy_(y, non_blocking=True)
             stream.synchronize()
     barrier()
@@ -636,7 +663,7 @@ def run_sweep(args):
             "cpu_baseline": cpu,
             "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": NL * T * cfg.d * 2,
                     "d2h_bytes_per_step": NL * T * cfg.d * 2, "steps": KE,
-                    "note": "public API (moe_forward) per layer: pinned H2D of x, layer, D2H of y; host sync per step"},
+                    "note": "public API (pw_moe_forward) per layer: pinned H2D of x, layer, D2H of y; host sync per step"},
             "gpu_launches": (NL * _launches_per_step(cfg, T) + len(plan[W])) * K,
             "clocks": clk,
         }
@@ -715,7 +742,7 @@ def measure_paging(wl, stream, n_steps):
                     e = three[(i // NL) % len(three)]
                     layers[j].prefetch_expert(e, 6, planes=planes_of(e), copy_stream=copy)
                     fetched[j] = e
-                pw.moe_forward(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+                pw.moe_forward_fused(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
             t1.record(stream)
         torch.cuda.synchronize()
         for j, e in list(raised.items()) + list(fetched.items()):

@@ -282,6 +282,25 @@ pw_status pw_get_expert_bitwidth(pw_layer_t layer, int e, int* bits);
 /* Scratch bytes that pw_permute / pw_expert_ffn_bitplane / pw_shared_ffn need for T tokens. */
 pw_status pw_workspace_size(pw_layer_t layer, int T, size_t* bytes);
 
+/*
+ * The whole layer for T tokens in one call: pw_route_topk, then -- for decode
+ * batches of at most 16 tokens (T also within the decode token thresholds
+ * and T*K <= 512) -- one persistent kernel that permutes, runs every
+ * expert's FFN and the shared FFN and combines (the permutation is never
+ * written out: routed rows are read from x through the routing result);
+ * otherwise pw_permute, pw_moe_ffn and pw_combine.  Both ways give the same
+ * y, bit for bit, as those separate calls: every expert-FFN item is computed
+ * the same way and the fused combine adds the k terms in the same order.
+ *   x   device fp16 [T][d]   wr device fp16 [E][d]   bias device fp32 [E] or NULL
+ *   idx device int32 [T][K], w device fp32 [T][K]: the routing (outputs)
+ *   y   device fp16 [T][d] (output)
+ *   ws  device scratch of at least pw_moe_forward_workspace_size(T) bytes
+ * Asynchronous on `stream`; run the calls of one layer on one stream.
+ */
+pw_status pw_moe_forward(pw_layer_t layer, const void* x, const void* wr, const float* bias, int T,
+                         int32_t* idx, float* w, void* y, void* ws, size_t ws_bytes, void* stream);
+pw_status pw_moe_forward_workspace_size(pw_layer_t layer, int T, size_t* bytes);
+
 /* ---------------------------------------------------------------------------
  * Quality-aware bitwidth planning (PagedWeight write-up "内存的饥饿游戏",
  * sections 三层感知 and 安全边界与异步搬运; budget M_w = M_total - M_kv and

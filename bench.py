@@ -576,7 +576,8 @@ def run_sweep(args):
             apply(i)
             forward_all()
     torch.cuda.synchronize()
-    active = [np.diff(bufs[l].offsets.cpu().numpy()) > 0 for l in range(NL)]  # routing is fixed per layer
+    # routing is fixed per layer: experts with tokens, from the router's output
+    active = [np.bincount(bufs[l].idx[:T].cpu().numpy().reshape(-1), minlength=cfg.E) > 0 for l in range(NL)]
 
     def step_bytes():
         tot = 0

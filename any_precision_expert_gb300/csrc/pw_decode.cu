@@ -73,15 +73,16 @@ struct Geo {
 };
 
 // Weight units streamed by a warp (one matrix of its tile):
-//   KIND_F16: 32 columns of the fp16 page, 2 x 16 B per lane;
+//   KIND_F16: 64 columns of the fp16 page, 4 x 16 B per lane (ring depth 3);
 //   KIND_PB: half a plane group (2 chunks, 128 columns), 8 B per lane and plane (ring slots sized for 6 planes);
 //   KIND_PG: a whole plane group (4 chunks, 256 columns), 16 B per lane and plane.
 enum { KIND_F16 = 1, KIND_PB = 2, KIND_PG = 3 };
+constexpr int kF16Steps = 4;  // mma steps (16 columns each) of one fp16 unit
 
 template <int KIND, int B>
 struct Unit {
-  static constexpr int COLS = KIND == KIND_F16 ? 32 : KIND == KIND_PB ? 128 : 256;
-  static constexpr int LANE_BYTES = KIND == KIND_F16 ? 2 * 16 : KIND == KIND_PB ? kPlanes * 8 : B * 16;
+  static constexpr int COLS = KIND == KIND_F16 ? 16 * kF16Steps : KIND == KIND_PB ? 128 : 256;
+  static constexpr int LANE_BYTES = KIND == KIND_F16 ? kF16Steps * 16 : KIND == KIND_PB ? kPlanes * 8 : B * 16;
   static constexpr int SLOT = LANE_BYTES * 32;
   static constexpr int R = Geo::RB / SLOT > 8 ? 8 : Geo::RB / SLOT;  // ring depth
   static_assert(Geo::RB / SLOT >= 3, "ring too shallow");
@@ -273,8 +274,8 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
     const uint32_t slot = ring + (i % R) * U::SLOT;
     if constexpr (KIND == KIND_F16) {
 #pragma unroll
-      for (int s = 0; s < 2; ++s)
-        cp_async16(slot + (s * 32 + lane) * 16, src.p[0] + ((size_t)(cb * 2 + s) * 32 + lane) * 16);
+      for (int s = 0; s < kF16Steps; ++s)
+        cp_async16(slot + (s * 32 + lane) * 16, src.p[0] + ((size_t)(cb * kF16Steps + s) * 32 + lane) * 16);
     } else if constexpr (KIND == KIND_PG) {
       if (cb < GR) {
         const size_t off = (size_t)(cb * 128 + lane * 4) * 4;
@@ -343,7 +344,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
     const uint32_t slot = ring + (i % R) * U::SLOT;
     if constexpr (KIND == KIND_F16) {
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < kF16Steps; ++s) {
         uint32_t bf[G::NTM][2];
         slab_bstep(buf, kc0, s, NT, ntok, rs, bf);
         const uint4 v = lds128(slot + (s * 32 + lane) * 16);

@@ -465,9 +465,13 @@ static int env_tokens(const char* name, int dflt) {
 
 // Routed experts with more tokens than this use the tensor-core GEMM (read per
 // call).  Wide experts (ffn >= 4096: at least 32 row tiles of 128 per matrix)
-// fill the GPU with GEMM tiles from 33 tokens on; narrow ones only well above
-// a decode batch's share.
-int decode_max_tokens(int ffn) { return env_tokens("PW_DECODE_MAX_TOK", ffn >= 4096 ? 32 : 64); }
+// fill the GPU with GEMM tiles from 33 tokens on.  Narrow ones in batches of up
+// to 64 tokens stay on the decode kernel up to 64 tokens (a lone GEMM expert of
+// a few row tiles would run after it, nearly alone on the GPU); in larger
+// batches many experts cross 32 tokens and their GEMM tiles fill the GPU.
+int decode_max_tokens(int ffn, int T) {
+  return env_tokens("PW_DECODE_MAX_TOK", ffn >= 4096 || T > 64 ? 32 : 64);
+}
 
 // The shared FFN (every token of the batch) uses the tensor-core GEMM above this batch size.
 int decode_max_tokens_shared() { return env_tokens("PW_DECODE_MAX_TOK_SHARED", 256); }

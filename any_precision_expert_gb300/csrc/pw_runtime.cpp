@@ -1007,7 +1007,7 @@ extern "C" pw_status pw_moe_forward(pw_layer_t l, const void* x, const void* wr,
   // one fused launch for small decode batches (measured: 3-5% faster at 1-8
   // tokens, 1.5% slower at 64, where the separate small kernels cost less
   // than the fused kernel's final barrier); both give the same y bit for bit
-  const bool fused = T <= 16 && T <= decode_max_tokens(l->desc.ffn) &&
+  const bool fused = T <= 16 && T <= decode_max_tokens(l->desc.ffn, T) &&
                      (!sh || T <= decode_max_tokens_shared()) && T * l->desc.top_k <= 512;
   if (fused)
     return launched(launch_layer_fused(L, xh, idx, w, T, h, hs, y_perm, ys, static_cast<__half*>(y), offsets, s));

@@ -447,15 +447,15 @@ def run_gpu(args):
     return out
 
 
-def _thresholds(cfg):
-    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "32" if cfg.f >= 4096 else "64")), 1024)
+def _thresholds(cfg, T):
+    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "32" if cfg.f >= 4096 or T > 64 else "64")), 1024)
     thr_s = min(int(os.environ.get("PW_DECODE_MAX_TOK_SHARED", "256")), 1024)
     return thr, thr_s
 
 
 def _fused_step(cfg, T):
     """pw_moe_forward runs router + one fused kernel for decode batches of at most 16 tokens."""
-    thr, thr_s = _thresholds(cfg)
+    thr, thr_s = _thresholds(cfg, T)
     return T <= 16 and T <= thr and (not cfg.shared_ffn or T <= thr_s) and T * cfg.K <= 512
 
 
@@ -465,7 +465,7 @@ def _launches_per_step(cfg, T):
     scatter for more than 1024 slots, or one kernel), row gather, the
     persistent decode kernel, the tcgen05 GEMM pair for experts above the
     token threshold and for a shared FFN above its own, and the combine."""
-    thr, thr_s = _thresholds(cfg)
+    thr, thr_s = _thresholds(cfg, T)
     if _fused_step(cfg, T):
         return 2
     S = T * cfg.K

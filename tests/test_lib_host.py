@@ -220,6 +220,24 @@ def test_compute_calls_refuse_in_host_sim(sim):
     pool.close()
 
 
+def test_forward_call_checks_arguments_on_the_host(sim):
+    pool = pw.Pool(48 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool, E=4, d=128, f=128, K=2)
+    for e in range(4):
+        _load(layer, e, 3, _expert(e, w16=False))
+    n1, n8 = layer.forward_workspace_size(1), layer.forward_workspace_size(8)
+    assert 0 < n1 < n8 and n8 >= layer.workspace_size(8)
+    f = _lib.lib.pw_moe_forward
+    assert f(layer.handle, 256, 256, None, -1, 256, 256, 256, 256, n8, None) == 1  # T < 0
+    assert f(layer.handle, 256, 256, None, 8, None, 256, 256, 256, n8, None) == 1  # no idx
+    assert f(layer.handle, 264, 256, None, 8, 256, 256, 256, 256, n8, None) == 1  # x not 16-byte aligned
+    assert f(layer.handle, 256, 256, None, 8, 256, 256, 256, 256, n8 - 1, None) == 3  # scratch too small
+    assert f(layer.handle, 256, 256, None, 8, 256, 256, 256, 256, n8, None) == 2  # no device in host-sim
+    assert f(layer.handle, 256, 256, None, 0, None, None, None, None, 0, None) == 2  # empty batch: nothing to check
+    layer.destroy()
+    pool.close()
+
+
 def test_copy_expert_between_layers(sim):
     pool = pw.Pool(96 * PAGE, page_bytes=PAGE, device="cpu")
     a = _layer(pool)

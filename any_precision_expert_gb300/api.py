@@ -296,7 +296,15 @@ class Buffers:
                          if layer.fs else None)
         self.y = torch.empty((T_max, d), dtype=torch.float16, device=device)
         self.ws = torch.empty(max(layer.workspace_size(T_max), 256), dtype=torch.uint8, device=device)
-        self.fws = torch.empty(max(layer.forward_workspace_size(T_max), 256), dtype=torch.uint8, device=device)
+        self._layer, self._device, self._fws = layer, device, None
+
+    @property
+    def fws(self):
+        """Scratch of the whole-layer call (pw_moe_forward), allocated on first use."""
+        if self._fws is None:
+            n = max(self._layer.forward_workspace_size(self.T_max), 256)
+            self._fws = torch.empty(n, dtype=torch.uint8, device=self._device)
+        return self._fws
 
 
 def moe_forward_fused(layer: Layer, x, wr, bias, buf: Buffers, stream=None):

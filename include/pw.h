@@ -14,6 +14,10 @@
  *   pw_route_topk -> pw_permute -> pw_expert_ffn_bitplane (+ pw_shared_ffn, or both
  *   in one pw_moe_ffn)
  *   -> pw_combine,   and   pw_set_expert_bitwidth.
+ * pw_moe_forward runs the whole chain in one call (router plus one fused
+ * persistent kernel for decode-sized batches, the separate kernels above).
+ * pw_route_stats and pw_plan_bitwidths give the signals and the per-expert
+ * bitwidth plan that pw_set_expert_bitwidth then applies.
  *
  * Conventions for every function
  *  - Return value: pw_status.  Arguments are validated on the host before any

@@ -166,6 +166,16 @@ __device__ __forceinline__ void stage_kblock(const __half* act, const int* s_tok
                                              uint32_t buf) {
   const int c0 = kb * kbw;
   const int ppr = min(kbw, K - c0) >> 3;  // 16-byte pieces per row
+  if (ppr == (kbw >> 3) && ppr <= kCtaThreads) {
+    // whole K-block (ppr a power of two): each thread keeps one piece column
+    const int lg = __ffs(ppr) - 1;
+    const int j = threadIdx.x & (ppr - 1), rstep = kCtaThreads >> lg;
+    const __half* src = act + c0 + j * 8;
+#pragma unroll 4
+    for (int r = threadIdx.x >> lg; r < srows; r += rstep)
+      cp_async16(buf + slab_off(r, j, kbw * 2), src + (size_t)s_tok[r] * K);
+    return;
+  }
   const int n = srows * ppr;
   for (int p = threadIdx.x; p < n; p += kCtaThreads) {
     const int r = p / ppr, j = p - r * ppr;

@@ -800,9 +800,66 @@ def _threads():
         return os.cpu_count() or 1
 
 
+def _blas_name():
+    try:
+        import numpy as np
+        blas = np.show_config(mode="dicts")["Build Dependencies"]["blas"]
+        return f"{blas.get('name', '?')} {blas.get('version', '')}".strip()
+    except Exception:
+        return "unknown"
+
+
+# One oracle run in a fresh interpreter with every BLAS pool at one thread:
+# the first n_tok tokens of the layer's seeded batch, one per call, repeated
+# until `seconds` have passed (only the experts those tokens use are drawn).
+_ONE_THREAD = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+from oracle import pw_oracle as O
+from synth import bits_plan, get_config, make_expert, make_router, make_shared, make_tokens
+name, seconds, n_tok, T = sys.argv[2], float(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5])
+cfg = get_config(name)
+bits = bits_plan(cfg, 0)
+wr, bias = make_router(cfg, 0)
+shared = make_shared(cfg, 0)
+x = make_tokens(cfg, T, 0, stream=0)
+cache = {}
+def expert(e):
+    if e not in cache:
+        cache[e] = make_expert(cfg, e, 0)
+    return cache[e]
+for t in range(n_tok):  # draws the sample's experts outside the timed loop
+    O.moe_tokens(x, wr, bias, expert, bits, cfg.K, cfg.renormalize, [t], shared=shared)
+n, t0 = 0, time.perf_counter()
+while time.perf_counter() - t0 < seconds and n < 1024:
+    O.moe_tokens(x, wr, bias, expert, bits, cfg.K, cfg.renormalize, [n % n_tok], shared=shared)
+    n += 1
+print(json.dumps({"value": n / (time.perf_counter() - t0), "calls": n}))
+"""
+
+
+def cpu_single_thread(names=("tiny", "qwen"), seconds=4.0, n_tok=4, T=64):
+    """The oracle on one host thread for the tiny and Qwen-shaped layers (a
+    bounded sample each); failures are reported, never raised."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    out = {"unit": "tokens/s", "threads": 1,
+           "sample": f"tokens 0..{n_tok - 1} of the seeded {T}-token batch, one per oracle call, {seconds:.0f} s each"}
+    for name in names:
+        try:
+            r = subprocess.run([sys.executable, "-c", _ONE_THREAD, ROOT, name, str(seconds), str(n_tok), str(T)],
+                               env=env, capture_output=True, text=True, timeout=300)
+            out[name] = json.loads(r.stdout.strip().splitlines()[-1])["value"] if r.returncode == 0 else \
+                f"failed: {(r.stderr.strip().splitlines() or ['?'])[-1][:200]}"
+        except Exception as e:  # noqa: BLE001 -- a baseline must not break the bench
+            out[name] = f"failed: {e}"[:200]
+    return out
+
+
 def cpu_baseline(wl, seconds=20.0):
     """Time the oracle on a bounded sample: tokens of the batch one per call
-    until `seconds` of CPU work (at most 1024 calls)."""
+    until `seconds` of CPU work (at most 1024 calls); then the one-thread runs."""
     from oracle import pw_oracle as O
 
     cfg = wl["cfg"]
@@ -817,7 +874,8 @@ def cpu_baseline(wl, seconds=20.0):
     el = time.perf_counter() - t_start
     return {"value": tokens / el, "unit": "tokens/s", "cores": _threads(), "kind": "oracle",
             "sample": f"{tokens} decode tokens of the same layer, one token per oracle call "
-                      f"({el:.1f} s of CPU work, numpy fp64, BLAS threads={_threads()}, os.cpu_count={os.cpu_count()})"}
+                      f"({el:.1f} s of CPU work, numpy fp64, BLAS threads={_threads()}, os.cpu_count={os.cpu_count()})",
+            "blas": _blas_name(), "single_thread": cpu_single_thread()}
 
 
 def run_reference(args):

@@ -300,6 +300,11 @@ pw_status pw_workspace_size(pw_layer_t layer, int T, size_t* bytes);
  *   y   device fp16 [T][d] (output)
  *   ws  device scratch of at least pw_moe_forward_workspace_size(T) bytes
  * Asynchronous on `stream`; run the calls of one layer on one stream.
+ * Errors (checked before anything is enqueued): PW_ERR_INVALID_ARG for
+ * T < 0, a null pointer (T > 0), x / wr / y / ws not 16-byte aligned, an
+ * expert never loaded, or a shared FFN declared but not loaded; PW_ERR_OOM
+ * when ws_bytes is below the workspace size; PW_ERR_CUDA when a launch
+ * fails.  T = 0 enqueues nothing.
  */
 pw_status pw_moe_forward(pw_layer_t layer, const void* x, const void* wr, const float* bias, int T,
                          int32_t* idx, float* w, void* y, void* ws, size_t ws_bytes, void* stream);

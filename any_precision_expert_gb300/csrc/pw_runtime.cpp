@@ -920,6 +920,11 @@ pw_status device_only() { return g_sim ? PW_ERR_UNSUPPORTED : PW_OK; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Token counts past 2^20 are refused: slot counts (T * top_k) then stay well
+// inside int and every scratch size inside size_t.
+constexpr int kMaxTokens = 1 << 20;
+bool bad_tokens(int T) { return T < 0 || T > kMaxTokens; }
+
 pw_status all_loaded(const pw_layer_s* l) {
   for (int b : l->bits)
     if (b == 0) return PW_ERR_INVALID_ARG;
@@ -974,7 +979,7 @@ FwdLayout fwd_layout(const pw_layer_s* l, int T) {
 
 extern "C" pw_status pw_moe_forward_workspace_size(pw_layer_t l, int T, size_t* bytes) {
   PW_TRY(check_layer(l));
-  if (T < 0 || !bytes) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T) || !bytes) return PW_ERR_INVALID_ARG;
   *bytes = fwd_layout(l, T).total;
   return PW_OK;
 }
@@ -982,7 +987,7 @@ extern "C" pw_status pw_moe_forward_workspace_size(pw_layer_t l, int T, size_t* 
 extern "C" pw_status pw_moe_forward(pw_layer_t l, const void* x, const void* wr, const float* bias, int T,
                                     int32_t* idx, float* w, void* y, void* ws, size_t ws_bytes, void* stream) {
   PW_TRY(check_layer(l));
-  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T)) return PW_ERR_INVALID_ARG;
   const bool sh = l->desc.shared_ffn != 0;
   if (sh && !l->shared_loaded) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
@@ -1023,7 +1028,7 @@ extern "C" pw_status pw_moe_forward(pw_layer_t l, const void* x, const void* wr,
 
 extern "C" pw_status pw_workspace_size(pw_layer_t l, int T, size_t* bytes) {
   PW_TRY(check_layer(l));
-  if (T < 0 || !bytes) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T) || !bytes) return PW_ERR_INVALID_ARG;
   *bytes = ws_layout(l, T).total;
   return PW_OK;
 }
@@ -1031,7 +1036,7 @@ extern "C" pw_status pw_workspace_size(pw_layer_t l, int T, size_t* bytes) {
 extern "C" pw_status pw_route_topk(pw_layer_t l, const void* x, const void* wr, const float* bias, int T,
                                    int32_t* idx, float* w, int32_t* expert_count, void* stream) {
   PW_TRY(check_layer(l));
-  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T)) return PW_ERR_INVALID_ARG;
   if (T > 0 && (!x || !wr || !idx || !w)) return PW_ERR_INVALID_ARG;
   if (T > 0 && (!aligned16(x) || !aligned16(wr))) return PW_ERR_INVALID_ARG;
   PW_TRY(device_only());
@@ -1043,7 +1048,7 @@ extern "C" pw_status pw_route_topk(pw_layer_t l, const void* x, const void* wr, 
 extern "C" pw_status pw_route_stats(pw_layer_t l, const void* x, const int32_t* idx, const float* w, int T,
                                     float* mass, float* resid, void* ws, size_t ws_bytes, void* stream) {
   PW_TRY(check_layer(l));
-  if (T < 0 || !mass || !resid) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T) || !mass || !resid) return PW_ERR_INVALID_ARG;
   if (T > 0 && (!x || !idx || !w || !ws)) return PW_ERR_INVALID_ARG;
   if (T > 0 && !aligned16(x)) return PW_ERR_INVALID_ARG;
   if (T > 0 && ws_bytes < (size_t)T * sizeof(float)) return PW_ERR_OOM;
@@ -1065,7 +1070,7 @@ extern "C" pw_status pw_permute(pw_layer_t l, const int32_t* idx, int T, const v
                                 int32_t* perm_src, int32_t* inv_slot, void* x_perm, void* ws, size_t ws_bytes,
                                 void* stream) {
   PW_TRY(check_layer(l));
-  if (T < 0 || !offsets) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T) || !offsets) return PW_ERR_INVALID_ARG;
   if (T > 0 && (!idx || !perm_src || !inv_slot || !ws)) return PW_ERR_INVALID_ARG;
   if (T > 0 && (x == nullptr) != (x_perm == nullptr)) return PW_ERR_INVALID_ARG;
   if (T > 0 && x && (!aligned16(x) || !aligned16(x_perm))) return PW_ERR_INVALID_ARG;
@@ -1081,7 +1086,7 @@ extern "C" pw_status pw_permute(pw_layer_t l, const int32_t* idx, int T, const v
 extern "C" pw_status pw_expert_ffn_bitplane(pw_layer_t l, const void* x_perm, const int32_t* offsets, int T,
                                             float* y_perm, void* ws, size_t ws_bytes, void* stream) {
   PW_TRY(check_layer(l));
-  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T)) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
   if (!x_perm || !offsets || !y_perm || !ws) return PW_ERR_INVALID_ARG;
   if (!aligned16(x_perm) || !aligned16(y_perm)) return PW_ERR_INVALID_ARG;
@@ -1098,7 +1103,7 @@ extern "C" pw_status pw_expert_ffn_bitplane(pw_layer_t l, const void* x_perm, co
 extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_shared, void* ws, size_t ws_bytes,
                                    void* stream) {
   PW_TRY(check_layer(l));
-  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T)) return PW_ERR_INVALID_ARG;
   if (l->desc.shared_ffn == 0 || !l->shared_loaded) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
   if (!x || !y_shared || !ws || !aligned16(x) || !aligned16(y_shared)) return PW_ERR_INVALID_ARG;
@@ -1113,7 +1118,7 @@ extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_
 extern "C" pw_status pw_moe_ffn(pw_layer_t l, const void* x, const void* x_perm, const int32_t* offsets, int T,
                                 float* y_perm, float* y_shared, void* ws, size_t ws_bytes, void* stream) {
   PW_TRY(check_layer(l));
-  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T)) return PW_ERR_INVALID_ARG;
   const bool sh = l->desc.shared_ffn != 0;
   if (sh && !l->shared_loaded) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
@@ -1134,7 +1139,7 @@ extern "C" pw_status pw_moe_ffn(pw_layer_t l, const void* x, const void* x_perm,
 extern "C" pw_status pw_combine(pw_layer_t l, const float* y_perm, const int32_t* inv_slot, const float* w, int T,
                                 const float* y_shared, void* y, void* stream) {
   PW_TRY(check_layer(l));
-  if (T < 0) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T)) return PW_ERR_INVALID_ARG;
   if (T > 0 && (!y_perm || !inv_slot || !w || !y)) return PW_ERR_INVALID_ARG;
   if (T > 0 && (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared))))
     return PW_ERR_INVALID_ARG;
@@ -1193,7 +1198,7 @@ pw_status pw::record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 pw_status pw::ffn_call_args(pw_layer_t l, const void* x_perm, const int32_t* offsets, int T, const float* y_perm,
                             DevLayer* dev, int* cmask, size_t* h_bytes) {
   PW_TRY(check_layer(l));
-  if (T < 0 || !dev || !cmask || !h_bytes) return PW_ERR_INVALID_ARG;
+  if (bad_tokens(T) || !dev || !cmask || !h_bytes) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
   if (!x_perm || !offsets || !y_perm) return PW_ERR_INVALID_ARG;
   if (!aligned16(x_perm) || !aligned16(y_perm)) return PW_ERR_INVALID_ARG;

@@ -32,7 +32,8 @@
  *    down [d][ffn]; a row is an output channel.
  *  - fp16 data is passed as raw IEEE binary16 (uint16_t / void*).
  *  - Shapes: d and ffn (and shared_ffn) must be multiples of 64, n_experts in
- *    [1, 256], top_k in [1, min(8, n_experts)].
+ *    [1, 256], top_k in [1, min(8, n_experts)]; token counts T in [0, 2^20]
+ *    (PW_ERR_INVALID_ARG outside).
  *  - A layer handle is not thread-safe: use one host thread per handle.
  */
 #ifndef PW_H

@@ -1,5 +1,6 @@
 """Library checks that need no GPU: exported symbols, host packers against the
 oracle's packer, and page-pool / page-table bookkeeping in host-sim mode."""
+import ctypes as C
 import os
 import re
 
@@ -234,6 +235,13 @@ def test_forward_call_checks_arguments_on_the_host(sim):
     assert f(layer.handle, 256, 256, None, 8, 256, 256, 256, 256, n8 - 1, None) == 3  # scratch too small
     assert f(layer.handle, 256, 256, None, 8, 256, 256, 256, 256, n8, None) == 2  # no device in host-sim
     assert f(layer.handle, 256, 256, None, 0, None, None, None, None, 0, None) == 2  # empty batch: nothing to check
+    big = (1 << 20) + 1  # past the token cap: refused before any size is computed
+    assert f(layer.handle, 256, 256, None, big, 256, 256, 256, 256, 1 << 62, None) == 1
+    size = C.c_size_t()
+    assert _lib.lib.pw_moe_forward_workspace_size(layer.handle, big, C.byref(size)) == 1
+    assert _lib.lib.pw_workspace_size(layer.handle, big, C.byref(size)) == 1
+    assert _lib.lib.pw_route_topk(layer.handle, 256, 256, None, big, 256, 256, None, None) == 1
+    assert _lib.lib.pw_moe_forward_workspace_size(layer.handle, 1 << 20, C.byref(size)) == 0
     layer.destroy()
     pool.close()
 

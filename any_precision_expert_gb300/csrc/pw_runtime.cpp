@@ -173,18 +173,28 @@ struct pw_pool_s {
     b.ready.reset();
     b.st = B_NONE;
   }
-  // Take n pages for a new mapped block.  Reclaimable blocks are given up
-  // oldest first, and only once their safe-boundary event has completed
-  // (waited for on a real device; in host-sim mode pending ones are skipped).
-  pw_status take_pages(size_t n, std::vector<int>* out) {
-    size_t avail = free_pages.size();
+  // Whether take_pages may give up reclaimable block b (on a real device it
+  // waits for the block's safe-boundary event; in host-sim mode pending
+  // blocks are skipped).
+  static bool reusable(const Block& b) { return !g_sim || b.ev->done(); }
+  // Pages a take could use now: the free ones and those of reusable
+  // reclaimable blocks.  Callers that take several blocks check their total
+  // against this first, so that a request that cannot be met gives up no
+  // reclaimable block.
+  size_t reusable_pages() const {
+    size_t n = free_pages.size();
     for (auto& kv : reclaim)
-      if (!g_sim || kv.second->ev->done()) avail += kv.second->pages.size();
-    if (avail < n) return PW_ERR_OOM;
+      if (reusable(*kv.second)) n += kv.second->pages.size();
+    return n;
+  }
+  // Take n pages for a new mapped block.  Reclaimable blocks are given up
+  // oldest first, and only once they are reusable.
+  pw_status take_pages(size_t n, std::vector<int>* out) {
+    if (reusable_pages() < n) return PW_ERR_OOM;
     while (free_pages.size() < n) {
       Block* victim = nullptr;
       for (auto& kv : reclaim)
-        if (!g_sim || kv.second->ev->done()) {
+        if (reusable(*kv.second)) {
           victim = kv.second;
           break;
         }
@@ -346,10 +356,12 @@ pw_status upload_block(pw_layer_t l, const Block& b, const std::vector<char>& im
 }
 
 // Pages for the blocks an expert at `bits` reads: np plane blocks, plus the
-// fp16 block at 16 bits (pages[np]).  All or nothing.
+// fp16 block at 16 bits (pages[np]).  All or nothing: a request the pool
+// cannot meet is refused before any reclaimable block is given up.
 pw_status take_expert_pages(pw_layer_t l, int bits, std::vector<std::vector<int>>* pages) {
   pw_pool_s* pool = l->pool;
   const int np = bits == 16 ? kPlanes : bits;
+  if (pool->reusable_pages() < (size_t)np * l->pmax + (bits == 16 ? (size_t)l->pmax16 : 0)) return PW_ERR_OOM;
   pages->assign(np + 1, {});
   auto give_back = [&](int upto) {
     for (int q = 0; q < upto; ++q)
@@ -809,6 +821,14 @@ extern "C" pw_status pw_prefetch_expert(pw_layer_t l, int e, int bits, const uin
 
   pw_pool_s* pool = l->pool;
   cudaStream_t cs = as_stream(copy_stream);
+  // refuse a request the pool cannot meet before anything changes: the
+  // expert's own intact blocks are held below, so their pages do not count
+  size_t own = 0;
+  for (int p = 0; p < need; ++p)
+    if (l->plane(e, p).st == B_RECLAIM && pw_pool_s::reusable(l->plane(e, p))) own += l->plane(e, p).pages.size();
+  if (bits == 16 && l->f16[e].st == B_RECLAIM && pw_pool_s::reusable(l->f16[e])) own += l->f16[e].pages.size();
+  const size_t want = missing.size() * (size_t)l->pmax + (f16_missing ? (size_t)l->pmax16 : 0);
+  if (pool->reusable_pages() - own < want) return PW_ERR_OOM;
   // still-intact blocks are held (re-mapped) so that they cannot be handed out
   // before the raise; they hold their data already
   std::vector<Block*> held;

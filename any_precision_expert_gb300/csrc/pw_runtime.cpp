@@ -388,6 +388,21 @@ pw_status take_expert_pages(pw_layer_t l, int bits, std::vector<std::vector<int>
   return PW_OK;
 }
 
+// Whether expert e could be (re)placed at `bits` once its current blocks are
+// released: release frees its mapped blocks and its reclaimable ones not yet
+// reusable, on top of what the pool can already hand out.  Load and copy ask
+// this before releasing anything, so a refused request leaves e as it was.
+bool fits_after_release(pw_layer_t l, int e, int bits) {
+  size_t avail = l->pool->reusable_pages();
+  auto add = [&](const Block& b) {
+    if (b.st == B_MAPPED || (b.st == B_RECLAIM && !pw_pool_s::reusable(b))) avail += b.pages.size();
+  };
+  for (int p = 0; p < kPlanes; ++p) add(l->plane(e, p));
+  add(l->f16[e]);
+  const int np = bits == 16 ? kPlanes : bits;
+  return avail >= (size_t)np * l->pmax + (bits == 16 ? (size_t)l->pmax16 : 0);
+}
+
 void release_expert(pw_layer_t l, int e) {
   for (int p = 0; p < kPlanes; ++p) l->pool->release(l->plane(e, p));
   l->pool->release(l->f16[e]);
@@ -589,6 +604,7 @@ extern "C" pw_status pw_layer_load_expert(pw_layer_t l, int e, int bits, const u
   }
   cudaStream_t s = as_stream(stream);
   pw_pool_s* pool = l->pool;
+  if (!fits_after_release(l, e, bits)) return PW_ERR_OOM;  // expert e stays as it was
   // kernels still reading the old pages must finish before they are reused
   PW_TRY(dev_sync(s));
   release_expert(l, e);
@@ -673,6 +689,7 @@ extern "C" pw_status pw_layer_copy_expert(pw_layer_t l, int e, pw_layer_t src, i
   if (bits == 16 && src->f16[e_src].st != B_MAPPED) return PW_ERR_NOT_RESIDENT;
 
   cudaStream_t s = as_stream(stream);
+  if (!fits_after_release(l, e, bits)) return PW_ERR_OOM;  // expert e stays as it was
   PW_TRY(dev_sync(s));  // kernels still reading the old pages must finish before they are reused
   release_expert(l, e);
   std::vector<std::vector<int>> pages;

@@ -111,7 +111,9 @@ pw_status pw_layer_destroy(pw_layer_t layer);  /* returns every page and residen
  *              resident (the dequantised weight is LUT_b[row][code6 >> (6-b)]).
  *   w16[m]     host fp16 [rows][cols] fallback page, required iff bits == 16,
  *              else may be NULL (then the expert can never be raised to 16).
- * Re-loading an expert first releases its previous pages.
+ * Re-loading an expert first releases its previous pages.  A load the pool
+ * cannot hold, counting the pages that release would free, returns
+ * PW_ERR_OOM and leaves the expert and the pool as they were.
  * Synchronises `stream` before returning (host buffers may be freed after).
  */
 pw_status pw_layer_load_expert(pw_layer_t layer, int e, int bits,

@@ -5,8 +5,8 @@ PagedWeight (write-up "å†…å­˜çš„é¥¥é¥¿æ¸¸æˆ", sections æ ¸å¿ƒæ´žå¯Ÿ and å®‰å…¨è
 lowering an expert detaches its low planes without moving data; raising
 reuses planes that are still intact or uploads them again; pages freed by a
 lowering are reused only after the safe boundary.  Each step applies one
-random operation (lower, raise in place, raise with an upload, reaching the
-safe boundary) and then checks, for every expert:
+random operation (lower, raise in place, raise with an upload, re-load,
+reaching the safe boundary) and then checks, for every expert:
   - the host mirror of the bitwidth is the one the sequence implies;
   - the pages the page table maps for planes 0..b-1 (and the fp16 page at
     16 bits) hold exactly that expert's packed data -- so no page was reused
@@ -88,9 +88,10 @@ def test_random_bitwidth_sequences_keep_the_page_table_consistent(sim, seed):
         ex = data[e]["ex"]
         layer.load_expert(e, b, ex["code6"], ex["lut"], ex["w16"] if b == 16 else None, stream=0)
     _check(pool, layer, data, bits)
-    counts = dict(lower=0, raise_ok=0, raise_refused=0, upload_ok=0, upload_oom=0, boundary=0)
-    for _ in range(250):
-        op = rng.choice(["lower", "raise", "upload", "boundary"], p=[0.35, 0.3, 0.2, 0.15])
+    counts = dict(lower=0, raise_ok=0, raise_refused=0, upload_ok=0, upload_oom=0, reload_ok=0, reload_oom=0,
+                  boundary=0)
+    for _ in range(300):
+        op = rng.choice(["lower", "raise", "upload", "reload", "boundary"], p=[0.3, 0.25, 0.2, 0.1, 0.15])
         e = int(rng.integers(E))
         b = bits[e]
         if op == "lower" and b > 3:
@@ -123,6 +124,18 @@ def test_random_bitwidth_sequences_keep_the_page_table_consistent(sim, seed):
                 assert err.status == 3, err.status  # out of pages: nothing changed
                 assert pool.stats() == before and layer.get_expert_bitwidth(e) == b
                 counts["upload_oom"] += 1
+        elif op == "reload":
+            nb = int(rng.choice(LEVELS))
+            ex = data[e]["ex"]
+            before = pool.stats()
+            try:
+                layer.load_expert(e, nb, ex["code6"], ex["lut"], ex["w16"] if nb == 16 else None, stream=0)
+                bits[e] = nb
+                counts["reload_ok"] += 1
+            except pw.PwError as err:
+                assert err.status == 3, err.status  # the pool cannot hold it: expert and pool as they were
+                assert pool.stats() == before and layer.get_expert_bitwidth(e) == b
+                counts["reload_oom"] += 1
         elif op == "boundary":
             _lib.lib.pw_testing_complete_events()
             counts["boundary"] += 1

@@ -5,14 +5,16 @@ PagedWeight (write-up "å†…å­˜çš„é¥¥é¥¿æ¸¸æˆ", sections æ ¸å¿ƒæ´žå¯Ÿ and å®‰å…¨è
 lowering an expert detaches its low planes without moving data; raising
 reuses planes that are still intact or uploads them again; pages freed by a
 lowering are reused only after the safe boundary.  Each step applies one
-random operation (lower, raise in place, raise with an upload, re-load,
-reaching the safe boundary) and then checks, for every expert:
+random operation (lower, raise in place, prefetch, raise with an upload,
+re-load, reaching the safe boundary) and then checks, for every expert:
   - the host mirror of the bitwidth is the one the sequence implies;
-  - the pages the page table maps for planes 0..b-1 (and the fp16 page at
-    16 bits) hold exactly that expert's packed data -- so no page was reused
-    while still mapped, and no raise re-mapped a block that had been reused;
+  - the pages the page table maps for the expert's mapped blocks (planes
+    0..b-1 and the fp16 page at 16 bits, plus whatever a prefetch brought
+    back ahead of a raise) hold exactly that expert's packed data -- so no
+    page was reused while still mapped, and no raise re-mapped a block that
+    had been reused;
   - the pool's books balance: free + mapped + reclaimable + resident = total,
-    and mapped = the pages the current bitwidths need;
+    and mapped = the pages of the mapped blocks;
   - a refused call (not resident, out of pages) changed nothing.
 """
 import numpy as np
@@ -54,22 +56,26 @@ def _read(pool, addr, nbytes):
     return pool.buffer[off:off + nbytes].numpy()
 
 
-def _pages_needed(b):
-    return 6 + 2 if b == 16 else b  # one page per plane block at this size, two for the fp16 block
+def _blocks(b):
+    # (mapped plane blocks, fp16 block mapped) that bitwidth b reads; mapped
+    # plane blocks are always a prefix 0..n-1
+    return (6, True) if b == 16 else (b, False)
 
 
-def _check(pool, layer, data, bits):
+def _check(pool, layer, data, bits, mapped):
     st = pool.stats()
     resident = st["resident_bytes"] // PAGE
     assert st["free_pages"] + st["mapped_pages"] + st["reclaimable_pages"] + resident == st["total_pages"]
-    assert st["mapped_pages"] == sum(_pages_needed(b) for b in bits)
+    # one page per plane block at this size, two for the fp16 block
+    assert st["mapped_pages"] == sum(n + 2 * f for n, f in mapped)
     for e, b in enumerate(bits):
         assert layer.get_expert_bitwidth(e) == b
-        for p in range(min(b, 6)):
+        n, f16 = mapped[e]
+        for p in range(n):
             blk = data[e]["block"][p]
             got = _read(pool, layer.page_address(e, p, 0), blk.nbytes).view(np.uint32)
             assert np.array_equal(got, blk), (e, b, p)
-        if b == 16:
+        if f16:
             ref = data[e]["f16_block"].view(np.uint8)
             got = np.concatenate([_read(pool, layer.page_address(e, 6, 0), PAGE),
                                   _read(pool, layer.page_address(e, 6, 1), ref.nbytes - PAGE)])
@@ -87,11 +93,13 @@ def test_random_bitwidth_sequences_keep_the_page_table_consistent(sim, seed):
     for e, b in enumerate(bits):
         ex = data[e]["ex"]
         layer.load_expert(e, b, ex["code6"], ex["lut"], ex["w16"] if b == 16 else None, stream=0)
-    _check(pool, layer, data, bits)
-    counts = dict(lower=0, raise_ok=0, raise_refused=0, upload_ok=0, upload_oom=0, reload_ok=0, reload_oom=0,
-                  boundary=0)
-    for _ in range(300):
-        op = rng.choice(["lower", "raise", "upload", "reload", "boundary"], p=[0.3, 0.25, 0.2, 0.1, 0.15])
+    mapped = [_blocks(b) for b in bits]
+    _check(pool, layer, data, bits, mapped)
+    counts = dict(lower=0, raise_ok=0, raise_refused=0, prefetch_ok=0, prefetch_oom=0, upload_ok=0, upload_oom=0,
+                  reload_ok=0, reload_oom=0, boundary=0)
+    for _ in range(400):
+        op = rng.choice(["lower", "raise", "prefetch", "upload", "reload", "boundary"],
+                        p=[0.25, 0.25, 0.15, 0.1, 0.1, 0.15])
         e = int(rng.integers(E))
         b = bits[e]
         if op == "lower" and b > 3:
@@ -99,7 +107,7 @@ def test_random_bitwidth_sequences_keep_the_page_table_consistent(sim, seed):
             keep = [layer.page_address(e, p, 0) for p in range(nb)]
             layer.set_expert_bitwidth(e, nb, stream=0)
             assert [layer.page_address(e, p, 0) for p in range(nb)] == keep  # no data moved
-            bits[e] = nb
+            bits[e], mapped[e] = nb, _blocks(nb)  # blocks above the new bitwidth go, prefetched ones too
             counts["lower"] += 1
         elif op == "raise" and b < 16:
             nb = int(rng.choice([v for v in LEVELS if v > b]))
@@ -107,18 +115,30 @@ def test_random_bitwidth_sequences_keep_the_page_table_consistent(sim, seed):
             rc = layer.try_set_expert_bitwidth(e, nb)
             assert rc in (0, 4), rc
             if rc == 0:
-                bits[e] = nb
+                bits[e], mapped[e] = nb, _blocks(nb)
                 counts["raise_ok"] += 1
             else:
                 assert pool.stats() == before
                 counts["raise_refused"] += 1
+        elif op == "prefetch" and b < 16:
+            nb = int(rng.choice([v for v in LEVELS if v > b]))
+            before = pool.stats()
+            try:
+                layer.prefetch_expert(e, nb, planes=data[e]["planes"], w16=data[e]["f16"], copy_stream=0)
+                n, f = _blocks(nb)
+                mapped[e] = (max(mapped[e][0], n), mapped[e][1] or f)  # bitwidth unchanged
+                counts["prefetch_ok"] += 1
+            except pw.PwError as err:
+                assert err.status == 3, err.status
+                assert pool.stats() == before and layer.get_expert_bitwidth(e) == b
+                counts["prefetch_oom"] += 1
         elif op == "upload" and b < 16:
             nb = int(rng.choice([v for v in LEVELS if v > b]))
             before = pool.stats()
             try:
                 layer.raise_expert_async(e, nb, planes=data[e]["planes"], w16=data[e]["f16"], stream=0,
                                          copy_stream=0)
-                bits[e] = nb
+                bits[e], mapped[e] = nb, _blocks(nb)
                 counts["upload_ok"] += 1
             except pw.PwError as err:
                 assert err.status == 3, err.status  # out of pages: nothing changed
@@ -130,7 +150,7 @@ def test_random_bitwidth_sequences_keep_the_page_table_consistent(sim, seed):
             before = pool.stats()
             try:
                 layer.load_expert(e, nb, ex["code6"], ex["lut"], ex["w16"] if nb == 16 else None, stream=0)
-                bits[e] = nb
+                bits[e], mapped[e] = nb, _blocks(nb)
                 counts["reload_ok"] += 1
             except pw.PwError as err:
                 assert err.status == 3, err.status  # the pool cannot hold it: expert and pool as they were
@@ -139,7 +159,7 @@ def test_random_bitwidth_sequences_keep_the_page_table_consistent(sim, seed):
         elif op == "boundary":
             _lib.lib.pw_testing_complete_events()
             counts["boundary"] += 1
-        _check(pool, layer, data, bits)
+        _check(pool, layer, data, bits, mapped)
     # the sequence exercised every outcome
     assert all(v > 0 for v in counts.values()), counts
     layer.destroy()

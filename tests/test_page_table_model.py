@@ -62,12 +62,17 @@ def _blocks(b):
     return (6, True) if b == 16 else (b, False)
 
 
-def _check(pool, layer, data, bits, mapped):
+def _check_books(pool, mapped):
     st = pool.stats()
     resident = st["resident_bytes"] // PAGE
     assert st["free_pages"] + st["mapped_pages"] + st["reclaimable_pages"] + resident == st["total_pages"]
     # one page per plane block at this size, two for the fp16 block
     assert st["mapped_pages"] == sum(n + 2 * f for n, f in mapped)
+
+
+def _check(pool, layer, data, bits, mapped, books=True):
+    if books:
+        _check_books(pool, mapped)
     for e, b in enumerate(bits):
         assert layer.get_expert_bitwidth(e) == b
         n, f16 = mapped[e]
@@ -163,5 +168,97 @@ def test_random_bitwidth_sequences_keep_the_page_table_consistent(sim, seed):
     # the sequence exercised every outcome
     assert all(v > 0 for v in counts.values()), counts
     layer.destroy()
+    assert pool.stats()["free_pages"] == pool.stats()["total_pages"]
+    pool.close()
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_copies_between_layers_keep_both_page_tables_consistent(sim, seed):
+    """Two layers on one pool: expert copies (layer to layer and inside a layer)
+    mixed with lowering, raising and the safe boundary; every expert's mapped
+    pages must hold the data of the expert it was last copied or loaded from."""
+    rng = np.random.default_rng(100 + seed)
+    data = _experts()
+    # 2 x 6 resident pages + 20 + 13 pages of planes, one page to spare
+    pool = pw.Pool(46 * PAGE, page_bytes=PAGE, device="cpu")
+    layers = [pw.Layer(pool, D, F, E, 2, 1) for _ in range(2)]
+    bits = [[16, 6, 3, 3], [3, 3, 4, 3]]
+    origin = [[0, 1, 2, 3], [3, 2, 1, 0]]  # which expert's data each slot holds
+    for L in range(2):
+        for e in range(E):
+            ex = data[origin[L][e]]["ex"]
+            b = bits[L][e]
+            layers[L].load_expert(e, b, ex["code6"], ex["lut"], ex["w16"] if b == 16 else None, stream=0)
+    mapped = [[_blocks(b) for b in bits[L]] for L in range(2)]
+
+    def check():
+        _check_books(pool, mapped[0] + mapped[1])
+        for L in range(2):
+            _check(pool, layers[L], [data[o] for o in origin[L]], bits[L], mapped[L], books=False)
+
+    check()
+    counts = dict(lower=0, raise_ok=0, raise_refused=0, upload_ok=0, copy_ok=0, copy_not_resident=0, copy_oom=0,
+                  boundary=0)
+    for _ in range(300):
+        op = rng.choice(["lower", "raise", "upload", "copy", "boundary"], p=[0.2, 0.15, 0.2, 0.3, 0.15])
+        L, e = int(rng.integers(2)), int(rng.integers(E))
+        layer, b = layers[L], bits[L][e]
+        if op == "lower" and b > 3:
+            nb = int(rng.choice([v for v in LEVELS if v < b and v <= 6]))
+            layer.set_expert_bitwidth(e, nb, stream=0)
+            bits[L][e], mapped[L][e] = nb, _blocks(nb)
+            counts["lower"] += 1
+        elif op == "raise" and b < 16:
+            nb = int(rng.choice([v for v in LEVELS if v > b]))
+            before = pool.stats()
+            rc = layer.try_set_expert_bitwidth(e, nb)
+            assert rc in (0, 4), rc
+            if rc == 0:
+                bits[L][e], mapped[L][e] = nb, _blocks(nb)
+                counts["raise_ok"] += 1
+            else:
+                assert pool.stats() == before
+                counts["raise_refused"] += 1
+        elif op == "upload" and b < 16:
+            nb = int(rng.choice([v for v in LEVELS if v > b]))
+            src = data[origin[L][e]]
+            before = pool.stats()
+            try:
+                layer.raise_expert_async(e, nb, planes=src["planes"], w16=src["f16"], stream=0, copy_stream=0)
+                bits[L][e], mapped[L][e] = nb, _blocks(nb)
+                counts["upload_ok"] += 1
+            except pw.PwError as err:
+                assert err.status == 3, err.status
+                assert pool.stats() == before and layer.get_expert_bitwidth(e) == b
+        elif op == "copy":
+            Ls, es = int(rng.integers(2)), int(rng.integers(E))
+            if (Ls, es) == (L, e):
+                continue
+            held = [v for v in LEVELS if _blocks(v)[0] <= mapped[Ls][es][0] and
+                    (not _blocks(v)[1] or mapped[Ls][es][1])]
+            nb = int(rng.choice(held if rng.random() < 0.7 else LEVELS))
+            n, f = _blocks(nb)
+            resident = n <= mapped[Ls][es][0] and (not f or mapped[Ls][es][1])
+            before = pool.stats()
+            try:
+                layer.copy_expert(e, layers[Ls], es, nb, stream=0)
+                assert resident, (nb, mapped[Ls][es])
+                bits[L][e], mapped[L][e], origin[L][e] = nb, _blocks(nb), origin[Ls][es]
+                counts["copy_ok"] += 1
+            except pw.PwError as err:
+                if not resident:
+                    assert err.status == 4, err.status  # the source does not read those blocks
+                    counts["copy_not_resident"] += 1
+                else:
+                    assert err.status == 3, err.status  # out of pages
+                    counts["copy_oom"] += 1
+                assert pool.stats() == before and layer.get_expert_bitwidth(e) == b
+        elif op == "boundary":
+            _lib.lib.pw_testing_complete_events()
+            counts["boundary"] += 1
+        check()
+    assert all(v > 0 for v in counts.values()), counts
+    for layer in layers:
+        layer.destroy()
     assert pool.stats()["free_pages"] == pool.stats()["total_pages"]
     pool.close()

@@ -10,7 +10,7 @@ import pytest
 import any_precision_expert_gb300 as pw
 from any_precision_expert_gb300 import _lib
 from oracle import pw_planner as P
-from synth import get_config, make_expert
+from synth import get_config, make_expert, make_sensitivity
 
 
 def _instance(rng, E):
@@ -108,5 +108,55 @@ def test_apply_plan_reports_experts_needing_upload(sim):
     missing = layer.apply_plan([6, 4, 5], stream=0)  # lower, lower, raise past what expert 2 holds
     assert missing == [2]
     assert [layer.get_expert_bitwidth(e) for e in range(3)] == [6, 4, 3]
+    layer.destroy()
+    pool.close()
+
+
+def test_plans_under_changing_budgets_land_in_the_pool(sim):
+    """KV pressure grows, then shrinks: each budget is planned, applied (lowering
+    unmaps, raising re-maps what is still held) and the experts whose planes
+    are gone are uploaded again after the safe boundary; the pool then holds
+    exactly the plan's bytes and every mapped page the right data."""
+    cfg = get_config("tiny", d=128, f=128)
+    E = 6
+    pool = pw.Pool(64 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = pw.Layer(pool, cfg.d, cfg.f, E, 2, 1)
+    exs = [make_expert(cfg, e, seed=9, with_w16=True) for e in range(E)]
+    planes = [[pw.pack_planes(ex["code6"][m]) for m in range(3)] for ex in exs]
+    f16 = [[pw.pack_f16(ex["w16"][m]) for m in range(3)] for ex in exs]
+    for e, ex in enumerate(exs):
+        layer.load_expert(e, 16, ex["code6"], ex["lut"], ex["w16"], stream=0)
+    sizes = np.array([layer.plan_sizes()] * E, dtype=np.uint64)
+    rng = np.random.default_rng(5)
+    mass = rng.random(E) + 0.1
+    resid = mass * (0.5 + rng.random(E))
+    sens = make_sensitivity(get_config("qwen", E=E), seed=5)
+    top = int(sizes[:, 0].sum())
+    uploads = 0
+    for frac in (1.0, 0.8, 0.6, 0.45, "other", 0.7, 1.0):
+        if frac == "other":
+            # another owner takes the freed pages for a while, so that some
+            # lowered planes are really gone when the budget grows again
+            other = pw.Layer(pool, cfg.d, cfg.f, 4, 2, 1)
+            for e in range(4):
+                other.load_expert(e, 6, exs[e]["code6"], exs[e]["lut"], None, stream=0)
+            other.destroy()
+            continue
+        budget = int(top * frac)
+        bits, used, ok = pw.plan_bitwidths(sens, sizes, budget, mass=mass, resid=resid)
+        assert ok and used <= budget
+        missing = layer.apply_plan(bits, stream=0)
+        _lib.lib.pw_testing_complete_events()  # the safe boundary: freed pages may be reused
+        for e in missing:
+            layer.raise_expert_async(e, int(bits[e]), planes=planes[e], w16=f16[e], stream=0, copy_stream=0)
+        uploads += len(missing)
+        assert [layer.get_expert_bitwidth(e) for e in range(E)] == bits.tolist()
+        assert pool.stats()["mapped_pages"] * PAGE == used
+        for e, b in enumerate(bits.tolist()):
+            for p in range(min(b, 6)):
+                off = layer.page_address(e, p, 0) - pool.buffer.data_ptr()
+                got = pool.buffer[off:off + planes[e][0][p].nbytes].numpy().view(np.uint32)
+                assert np.array_equal(got, planes[e][0][p]), (frac, e, p)  # gate tiles open the block
+    assert uploads > 0  # shrinking KV pressure brought back planes that were gone
     layer.destroy()
     pool.close()

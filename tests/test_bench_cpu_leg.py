@@ -4,6 +4,8 @@ one-thread runs in a fresh interpreter."""
 import os
 import sys
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
@@ -32,3 +34,27 @@ def test_cpu_baseline_fields(monkeypatch):
     r = bench.cpu_baseline(wl, seconds=0.2)
     assert r["kind"] == "oracle" and r["unit"] == "tokens/s" and r["value"] > 0 and r["cores"] >= 1
     assert r["blas"] and r["single_thread"] == {"threads": 1}
+
+
+def test_algorithmic_bytes_follow_the_byte_model():
+    """Bytes a decode step must move: every routed expert's planes at its
+    bitwidth (3 d f b / 8) plus its LUT_b rows ((2 f + d) 2^b fp16), or its fp16
+    page (3 d f 2); the shared FFN (3 d f_s 2); the step adds the router (d E 2)
+    and x in, y out (2 T d 2).  Unrouted experts cost nothing."""
+    mix = get_config("mixtral")
+    bits = [6, 5, 4, 3, 6, 5, 4, 3]
+    off = np.concatenate([[0], np.cumsum([1, 1, 0, 0, 0, 0, 0, 0])])  # one token, experts 0 and 1
+    ffn, step = bench.algorithmic_bytes(mix, bits, off, 1)
+    d, f = 4096, 14336
+    e6 = 3 * d * f * 6 // 8 + (2 * f + d) * 64 * 2
+    e5 = 3 * d * f * 5 // 8 + (2 * f + d) * 32 * 2
+    assert ffn == e6 + e5 and round(ffn / 1e6, 1) == 248.5
+    assert step == ffn + d * 8 * 2 + 2 * 1 * d * 2
+    qwen = get_config("qwen")
+    bits = [4] + [16] + [3] * 58
+    off = np.concatenate([[0], np.cumsum([3, 2] + [0] * 58)])
+    ffn, step = bench.algorithmic_bytes(qwen, bits, off, 5)
+    b4 = 3 * 2048 * 1408 * 4 // 8 + (2 * 1408 + 2048) * 16 * 2
+    assert round(b4 / 1e6, 2) == 4.48
+    assert ffn == b4 + 3 * 2048 * 1408 * 2 + 3 * 2048 * 5632 * 2
+    assert step == ffn + 2048 * 60 * 2 + 2 * 5 * 2048 * 2

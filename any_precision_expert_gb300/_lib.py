@@ -71,9 +71,11 @@ _SIGS = {
     "pw_pack_planes": (i32, [vp, i32, i32, C.POINTER(U32P6)]),
     "pw_pack_f16": (i32, [vp, i32, i32, vp]),
     "pw_debug_dequant": (i32, [vp, i32, i32, vp, vp]),
+    "pw_debug_dequant_kernel": (i32, [vp, i32, i32, i32, vp, vp]),
     "pw_debug_page_address": (i32, [vp, i32, i32, i32, C.POINTER(C.c_uint64)]),
     "pw_testing_host_sim": (i32, [i32]),
     "pw_testing_complete_events": (i32, []),
+    "pw_testing_wait_limit": (i32, [vp, C.c_longlong, i32]),
 }
 
 for _name, (_res, _args) in _SIGS.items():

@@ -272,6 +272,11 @@ class Layer:
     def debug_dequant(self, e: int, m: int, out, stream=None):
         check(lib.pw_debug_dequant(self.handle, e, m, _p(out), _s(stream)), "pw_debug_dequant")
 
+    def debug_dequant_kernel(self, e: int, m: int, kernel: str, out, stream=None):
+        """Dump through the decode kernel's ('decode') or the tcgen05 GEMM's ('prefill') own decode path."""
+        which = {"decode": 0, "prefill": 1}[kernel]
+        check(lib.pw_debug_dequant_kernel(self.handle, e, m, which, _p(out), _s(stream)), "pw_debug_dequant_kernel")
+
     def page_address(self, e: int, p: int, vpage: int) -> int:
         a = C.c_uint64(0)
         check(lib.pw_debug_page_address(self.handle, e, p, vpage, C.byref(a)), "pw_debug_page_address")

@@ -56,7 +56,6 @@ namespace pw {
 constexpr int kCtaThreads = 128;
 constexpr int kCtaWarps = kCtaThreads / 32;
 constexpr int kTabW = 64 * 8 * 4;            // LUT table of one warp: 2^b entries x 8 row pairs x 4 B (b <= 6)
-constexpr long long kSpinLimit = 1ll << 22;  // polls of a phase counter (about a second)
 constexpr int kFusedSlots = 512;             // routed slots (T * K) of a fused layer step
 
 // Items take up to 32 tokens (a weight tile is streamed and decoded once for
@@ -251,6 +250,26 @@ __device__ __forceinline__ void build_tab_warp(const __half* lr, int b, uint32_t
   __syncwarp();
 }
 
+// Destination of a dump of the decoded weights (the debug path): the A
+// fragments of a tile are written to out[row][col] instead of feeding the mma.
+struct Dump {
+  __half* out;  // [rows][ld] fp16
+  int ld;       // columns of the matrix
+  int row0;     // first row of the warp's tile
+  bool store;   // false: run the loop (barriers) but write nothing
+};
+
+// A fragment of mma step at column col: a0 row g cols 2t.., a1 row g+8, a2 row
+// g cols 2t+8.., a3 row g+8 cols 2t+8.. (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void dump_frag(const Dump& D, const uint32_t (&a)[4], int col) {
+  if (!D.store) return;
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    *reinterpret_cast<uint32_t*>(D.out + (size_t)(D.row0 + g + 8 * (r & 1)) * D.ld + col + 2 * t + 8 * (r >> 1)) =
+        a[r];
+}
+
 // Weight sources of one warp's K loop.
 struct WSrc {
   const char* p[kPlanes];  // plane tiles, or the fp16 tile in p[0]
@@ -264,10 +283,10 @@ struct WSrc {
 // item and passes the same K-block barriers; the ntok distinct token rows of
 // K-block kb are staged at the start of K-block kb - 1.  B: 16 (fp16), 3, or
 // 0 (4..6 bits, src.nb).  pre() runs once the first weight units are in flight.
-template <int KIND, int B, class Pre>
+template <int KIND, int B, bool DUMP = false, class Pre>
 __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, int u0, int us, uint32_t ring,
                                       uint32_t slab, const __half* act, const int* s_tok,
-                                      float (&acc)[Geo::NTM][4], Pre&& pre) {
+                                      float (&acc)[Geo::NTM][4], Pre&& pre, const Dump* dump = nullptr) {
   using G = Geo;
   using U = Unit<KIND, B>;
   constexpr int R = U::R;
@@ -355,11 +374,15 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
     if constexpr (KIND == KIND_F16) {
 #pragma unroll
       for (int s = 0; s < kF16Steps; ++s) {
-        uint32_t bf[G::NTM][2];
-        slab_bstep(buf, kc0, s, NT, ntok, rs, bf);
         const uint4 v = lds128(slot + (s * 32 + lane) * 16);
         const uint32_t a[4] = {v.x, v.y, v.z, v.w};
-        mma_tiles(acc, a, bf, NT);
+        if constexpr (DUMP) {
+          dump_frag(*dump, a, (kb << lkb) + kc0 + 16 * s);
+        } else {
+          uint32_t bf[G::NTM][2];
+          slab_bstep(buf, kc0, s, NT, ntok, rs, bf);
+          mma_tiles(acc, a, bf, NT);
+        }
       }
     } else {
       constexpr int W = KIND == KIND_PG ? 4 : 2;  // words (chunks) per lane and plane
@@ -397,9 +420,13 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-          uint32_t bf[G::NTM][2];
-          slab_bstep(buf, kc0 + c * 64, s, NT, ntok, rs, bf);
-          mma_tiles(acc, a[s], bf, NT);
+          if constexpr (DUMP) {
+            dump_frag(*dump, a[s], (kb << lkb) + kc0 + c * 64 + 16 * s);
+          } else {
+            uint32_t bf[G::NTM][2];
+            slab_bstep(buf, kc0 + c * 64, s, NT, ntok, rs, bf);
+            mma_tiles(acc, a[s], bf, NT);
+          }
         }
       };
       if constexpr (B == 3) {
@@ -447,6 +474,34 @@ __device__ __forceinline__ void tile_store_y(const float (&acc)[Geo::NTM][4], in
     }
 }
 
+// Weight sources of tile t of matrix m (expert e, or the shared FFN) for one
+// warp: page-table addresses of its planes or fp16 tile, and for 3 bits the
+// register LUTs of the lane's rows.  Returns the tile's LUT_b rows, from which
+// a 4..6-bit warp builds its shared table (null otherwise).  B: 16, 3 or 0
+// (4..6 bits, b).
+template <int B>
+__device__ __forceinline__ const __half* tile_src(const DevLayer& L, int e, bool sh, int m, int t, int b, int K,
+                                                  uint32_t tab, WSrc& src) {
+  const int lane = threadIdx.x & 31;
+  if constexpr (B == 16) {
+    src.p[0] = sh ? reinterpret_cast<const char*>(L.shared16[m]) + (size_t)t * 32 * K : tile_addr(L, e, m, kPlanes, t);
+    return nullptr;
+  } else if constexpr (B == 3) {
+#pragma unroll
+    for (int p = 0; p < 3; ++p) src.p[p] = tile_addr(L, e, m, p, t);
+    const __half* lr = lut_rows(L, e, m, 3, t * kTileRows);
+    load_lut3(lr + (lane >> 2) * 8, src.lut3[0]);
+    load_lut3(lr + ((lane >> 2) + 8) * 8, src.lut3[1]);
+    return nullptr;
+  } else {
+    src.nb = b;
+#pragma unroll
+    for (int p = 0; p < kPlanes; ++p) src.p[p] = p < b ? tile_addr(L, e, m, p, t) : nullptr;
+    src.tabg = tab + (lane >> 2) * 4;
+    return lut_rows(L, e, m, b, t * kTileRows);
+  }
+}
+
 struct ItemArgs {
   const __half* act;  // token rows of this phase
   int e;              // expert (routed)
@@ -475,23 +530,12 @@ __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A,
   const int m = NM == 2 ? warp >> 1 : 2;     // and matrix
   float acc[kNT][4] = {};
   WSrc src;
+  const __half* lr = tile_src<B>(L, A.e, A.sh, m, t, A.b, A.K, tab, src);
   if constexpr (B == 16) {
-    src.p[0] = A.sh ? reinterpret_cast<const char*>(L.shared16[m]) + (size_t)t * 32 * A.K
-                    : tile_addr(L, A.e, m, kPlanes, t);
     kloop<KIND_F16, 16>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
   } else if constexpr (B == 3) {
-#pragma unroll
-    for (int p = 0; p < 3; ++p) src.p[p] = tile_addr(L, A.e, m, p, t);
-    const __half* lr = lut_rows(L, A.e, m, 3, t * kTileRows);
-    load_lut3(lr + (lane >> 2) * 8, src.lut3[0]);
-    load_lut3(lr + ((lane >> 2) + 8) * 8, src.lut3[1]);
     kloop<KIND_PG, 3>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
   } else {
-    src.nb = A.b;
-#pragma unroll
-    for (int p = 0; p < kPlanes; ++p) src.p[p] = p < A.b ? tile_addr(L, A.e, m, p, t) : nullptr;
-    src.tabg = tab + (lane >> 2) * 4;
-    const __half* lr = lut_rows(L, A.e, m, A.b, t * kTileRows);
     kloop<KIND_PB, 0>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc,
                       [&] { build_tab_warp(lr, A.b, tab); });
   }
@@ -571,7 +615,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     for (int i = tid; i < n_slots; i += kCtaThreads) {
       const int e = P.idx[i];
       if ((unsigned)e < (unsigned)E) atomicAdd(&s_n[e], 1);
-      else atomicExch(L.err, 2);  // not a routing result: the slot is dropped
+      else atomicExch(L.err, kErrRouting);  // not a routing result: the slot is dropped
     }
     __syncthreads();
     if (warp == 0) {
@@ -630,8 +674,12 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
         n = s_n[g];
         b = L.bits[g];
       } else if (P.offsets) {
-        base = P.offsets[g];
-        n = P.offsets[g + 1] - base;
+        // the caller's bucket, clamped to the slot rows [0, T*K): a bad table
+        // flags the layer's error word and nothing is read or written outside
+        const int o0 = P.offsets[g], o1 = P.offsets[g + 1];
+        base = min(max(o0, 0), n_slots);
+        n = min(max(o1, base), n_slots) - base;
+        if (o0 < 0 || o1 < o0 || o1 > n_slots) atomicExch(L.err, kErrOffsets);
         b = L.bits[g];
         const bool take = (b == 3 && (P.bit_mask & 1)) || (b == 16 && (P.bit_mask & 2)) ||
                           (is_tab(b) && (P.bit_mask & 4));
@@ -797,11 +845,11 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
       s_tok[tid] = A.row0 + tid;
     }
     if (phase == 1 && tid == 0) {  // h of this chunk must be complete
-      const int need = fe / kTileRows;
+      const int need = fe / kTileRows + L.wait_bias;
       long long spins = 0;
       while (ld_acquire(done0 + sidx) < need) {
-        if (++spins > kSpinLimit) {
-          atomicExch(L.err, 1);
+        if (++spins > L.spin_limit) {
+          atomicExch(L.err, kErrTimeout);
           break;
         }
         __nanosleep(100);
@@ -835,8 +883,8 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     if (tid == 0) {
       long long spins = 0;
       while (ld_acquire(q + 4) < s_total1) {
-        if (++spins > kSpinLimit) {
-          atomicExch(L.err, 1);
+        if (++spins > L.spin_limit) {
+          atomicExch(L.err, kErrTimeout);
           break;
         }
         __nanosleep(100);
@@ -899,6 +947,56 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
       atomicExch(q + 1, 0);
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Debug: the decoded weights of expert e's matrix m exactly as this kernel
+// produces them.  Each warp runs the K loop of one 16-row tile (same ring
+// loads through the page table, same LUT set-up and decode routines as an
+// item of the FFN kernel) with its A fragments written to out[rows][cols]
+// instead of feeding the mma.
+// ---------------------------------------------------------------------------
+template <int B>
+__device__ __forceinline__ void dump_tile(const DevLayer& L, int e, int m, int t, int b, int C, uint32_t ring,
+                                          uint32_t slab, uint32_t tab, const int* s_tok, const Dump& D) {
+  float acc[Geo::NTM][4] = {};
+  WSrc src;
+  const __half* lr = tile_src<B>(L, e, false, m, t, b, C, tab, src);
+  if constexpr (B == 16) {
+    kloop<KIND_F16, 16, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [] {}, &D);
+  } else if constexpr (B == 3) {
+    kloop<KIND_PG, 3, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [] {}, &D);
+  } else {
+    kloop<KIND_PB, 0, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [&] { build_tab_warp(lr, b, tab); },
+                            &D);
+  }
+}
+
+__global__ void __launch_bounds__(kCtaThreads) decode_dump_kernel(DevLayer L, int e, int m, __half* out) {
+  extern __shared__ __align__(128) unsigned char smem_dump[];
+  __shared__ int s_tok[Geo::TOK];
+  const int warp = threadIdx.x >> 5;
+  const int R = m < 2 ? L.f : L.d, C = m < 2 ? L.d : L.f;
+  const int ntile = R / kTileRows;
+  const int t = min((int)blockIdx.x * kCtaWarps + warp, ntile - 1);  // spare warps repeat the last tile unstored
+  const Dump D{out, C, t * kTileRows, (int)blockIdx.x * kCtaWarps + warp < ntile};
+  const uint32_t slab = smem_u32(smem_dump);
+  const uint32_t tab = slab + 2 * Geo::HALF + warp * kTabW;
+  const uint32_t ring = slab + 2 * Geo::HALF + kCtaWarps * kTabW + warp * Geo::RB;
+  const int b = L.bits[e];
+  if (b == 16) dump_tile<16>(L, e, m, t, b, C, ring, slab, tab, s_tok, D);
+  else if (b == 3) dump_tile<3>(L, e, m, t, b, C, ring, slab, tab, s_tok, D);
+  else if (is_tab(b)) dump_tile<0>(L, e, m, t, b, C, ring, slab, tab, s_tok, D);
+  else if (threadIdx.x == 0) atomicExch(L.err, kErrBits);
+}
+
+cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {
+  const int R = m < 2 ? L.f : L.d;
+  cudaError_t err = ensure_smem((const void*)decode_dump_kernel, Geo::SMEM);
+  if (err != cudaSuccess) return err;
+  const int ntile = R / kTileRows;
+  decode_dump_kernel<<<(ntile + kCtaWarps - 1) / kCtaWarps, kCtaThreads, Geo::SMEM, s>>>(L, e, m, out);
+  return cudaGetLastError();
 }
 
 template <bool FUSED>

@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kDbgThreads) debug_dequant_kernel(DevLayer L, 
       break;
     }
     default:
-      if (threadIdx.x == 0) atomicExch(L.err, 3);
+      if (threadIdx.x == 0) atomicExch(L.err, kErrBits);
   }
 }
 

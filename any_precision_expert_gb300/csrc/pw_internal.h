@@ -17,6 +17,13 @@ constexpr int kChunkCols = 64;       // columns per stored chunk
 constexpr int kSyncHeader = 32;      // claim and exit counters of the persistent decode kernels
 constexpr int kSyncChunks = 64;      // 16-token chunks per group tracked by its phase counters
 
+// Values of a layer's device error word (0 = clear).  A timeout reads back as
+// PW_ERR_TIMEOUT, every other value as PW_ERR_DEVICE_CHECK.
+constexpr int kErrTimeout = 1;       // a bounded wait gave up
+constexpr int kErrRouting = 2;       // an expert index outside [0, E) in a routing result
+constexpr int kErrBits = 3;          // a bitwidth word outside {3, 4, 5, 6, 16}
+constexpr int kErrOffsets = 4;       // slot offsets not monotone in [0, T*K], or a slot index out of range
+
 // Words of a layer's sync area: header, then gate/up and down tile counters
 // for every (group, chunk), a group being a routed expert or the shared FFN.
 inline size_t sync_words(int E) { return kSyncHeader + 2 * (size_t)(E + 1) * kSyncChunks; }
@@ -38,7 +45,12 @@ struct DevLayer {
   const __half* shared16[3];            // packed fp16 shared FFN (gate, up, down) or null
   int* err;                             // device error word
   int* sync;                            // [sync_words(E)] zero between launches
+  long long spin_limit;                 // polls before a bounded wait of the decode kernel gives up
+  int wait_bias;                        // testing: added to the count a down item waits for (0 normally)
 };
+
+// Polls of a phase counter before the decode kernel gives up (about a second).
+constexpr long long kDefaultSpinPolls = 1ll << 22;
 
 // Scratch carved out of the caller's workspace for one hot-path call.
 struct FfnScratch {
@@ -85,6 +97,11 @@ cudaError_t launch_route_stats(const DevLayer& L, const __half* x, const int* id
 cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* inv_slot,
                            const float* w, int T, const float* y_shared, __half* y, cudaStream_t s);
 cudaError_t launch_debug_dequant(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
+// The decoded weights of expert e's matrix m as the decode kernel's K loop
+// (launch_decode_dump) or the prefill kernel's dequant warps
+// (launch_prefill_dump) produce them.
+cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
+cudaError_t launch_prefill_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
 
 // Host-side checks shared by the expert-FFN entry points: validates the
 // arguments of a routed FFN call for T tokens and returns the layer's kernel

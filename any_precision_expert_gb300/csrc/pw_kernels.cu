@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(DevLayer L, con
     if ((unsigned)e < (unsigned)E)
       atomicAdd(&h[e], 1);
     else
-      atomicExch(L.err, 2);
+      atomicExch(L.err, kErrRouting);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[blockIdx.x * E + i] = h[i];
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(DevLayer L, 
     for (int sl = tid; sl < S; sl += blockDim.x) {
       const int e = idx[sl];
       if ((unsigned)e < (unsigned)E) atomicAdd(&scan[e], 1);
-      else atomicExch(L.err, 2);
+      else atomicExch(L.err, kErrRouting);
     }
     __syncthreads();
     if (tid < E) tot = scan[tid];
@@ -382,7 +382,11 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DevLayer L, const
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k = 0; k < K; ++k) {
     const float wk = w[(size_t)t * K + k];
-    const int slot = inv_slot[(size_t)t * K + k];
+    int slot = inv_slot[(size_t)t * K + k];
+    if ((unsigned)slot >= (unsigned)(T * K)) {  // not a slot of this batch: flagged, read slot 0
+      atomicExch(L.err, kErrOffsets);
+      slot = 0;
+    }
     const float4 v = reinterpret_cast<const float4*>(y_perm + (size_t)slot * d)[c4];
     acc.x = fmaf(wk, v.x, acc.x);
     acc.y = fmaf(wk, v.y, acc.y);

@@ -142,6 +142,47 @@ __device__ __forceinline__ void pf_load_planes(const char* const (&pb)[6], int k
   }
 }
 
+// 3-bit register LUTs of this lane's rows g and g + 8 of the 16-row tile at
+// row0 (rows past R repeat the last row).
+__device__ __forceinline__ void pf_load_lut3(const DevLayer& L, int e, int mm, int row0, int g, int R,
+                                             uint32_t (&lut3)[2][4]) {
+  const int r0 = min(row0 + g, R - 1), r1 = min(row0 + g + 8, R - 1);
+  load_lut3(lut_rows(L, e, mm, 3, r0), lut3[0]);
+  load_lut3(lut_rows(L, e, mm, 3, r1), lut3[1]);
+}
+
+// Warp `par` of a pair writes its half (row set rho = par) of the per-lane
+// LUT table of one 64-row slab starting at row slab0: entry (v, rho, lane lx)
+// at word v * 64 + rho * 32 + lx holds LUT_b of row slab0 + 16 (lx / 8) +
+// lx % 8 + 8 rho in both halves.
+__device__ __forceinline__ void pf_build_tab_half(const DevLayer& L, int e, int mm, int b, int slab0, int R,
+                                                  int par, uint32_t* tabg) {
+  const int lx = threadIdx.x & 31, rho = par;
+  const int row = min(slab0 + (lx >> 3) * 16 + (lx & 7) + 8 * rho, R - 1);
+  const __half* lr = lut_rows(L, e, mm, b, row);
+  for (int v = 0; v < (1 << b); ++v) {
+    const uint32_t val = __half_as_ushort(lr[v]);
+    tabg[v * 64 + rho * 32 + lx] = val | (val << 16);
+  }
+}
+
+// fp16 page: stage kb of this lane's rows, gathered from the four fragment
+// lanes (g, t = 0..3) of the stored tile at fb (null: zeros).
+__device__ __forceinline__ void pf_gather_f16(const char* fb, int kb, int g, uint4 (&out)[4][4]) {
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    uint4 a[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      a[t] = fb ? *reinterpret_cast<const uint4*>(fb + ((size_t)(kb * 4 + st) * 32 + 4 * g + t) * 16)
+                : make_uint4(0, 0, 0, 0);
+    out[st][0] = make_uint4(a[0].x, a[1].x, a[2].x, a[3].x);
+    out[st][1] = make_uint4(a[0].z, a[1].z, a[2].z, a[3].z);
+    out[st][2] = make_uint4(a[0].y, a[1].y, a[2].y, a[3].y);
+    out[st][3] = make_uint4(a[0].w, a[1].w, a[2].w, a[3].w);
+  }
+}
+
 template <int NM>
 __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
     ffn_prefill_kernel(PfParams Q, const __grid_constant__ CUtensorMap act_map) {
@@ -168,6 +209,19 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
     s_off[0] = 0;
     s_off[1] = Q.n_slots;
     s_bits[0] = 16;
+  }
+  __syncthreads();
+  if (routed && tid == 0) {
+    // the caller's offsets, made monotone inside the slot rows [0, n_slots):
+    // a bad table flags the layer's error word and no tile leaves those rows
+    int prev = 0;
+    bool bad = false;
+    for (int i = 0; i <= E; ++i) {
+      const int v = s_off[i], c = min(max(v, prev), Q.n_slots);
+      bad |= v != c;
+      s_off[i] = prev = c;
+    }
+    if (bad) atomicExch(L.err, kErrOffsets);
   }
   __syncthreads();
   if (warp == 0) {
@@ -259,20 +313,11 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
       const int tau = row0 / 16;
       uint32_t lut3[2][4] = {};
       if (b == 3) {  // register LUTs of this lane's row pair; no shared table
-        const int r0 = min(row0 + g, R - 1), r1 = min(row0 + g + 8, R - 1);
-        load_lut3(lut_rows(L, T.e, mm, 3, r0), lut3[0]);
-        load_lut3(lut_rows(L, T.e, mm, 3, r1), lut3[1]);
+        pf_load_lut3(L, T.e, mm, row0, g, R, lut3);
       } else if (b <= 6) {
         ok = pair_sync();  // both warps of the pair finished the previous tile
         if (!ok) break;
-        const int j = par * 32 + lane, rho = j >> 5, lx = j & 31;
-        int row = T.mt * PF_BM + slab * 64 + (lx >> 3) * 16 + (lx & 7) + 8 * rho;
-        row = min(row, R - 1);
-        const __half* lr = lut_rows(L, T.e, mm, b, row);
-        for (int v = 0; v < (1 << b); ++v) {
-          const uint32_t val = __half_as_ushort(lr[v]);
-          tabg[v * 64 + rho * 32 + lx] = val | (val << 16);
-        }
+        pf_build_tab_half(L, T.e, mm, b, T.mt * PF_BM + slab * 64, R, par, tabg);
         ok = pair_sync();
         if (!ok) break;
       }
@@ -334,18 +379,7 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
         default:  // fp16 page: the lane gathers the four fragment lanes (g, t)
           for (int kb = par; kb < nkb && ok; kb += 2) {
             uint4 out[4][4];
-#pragma unroll
-            for (int st = 0; st < 4; ++st) {
-              uint4 a[4];
-#pragma unroll
-              for (int t = 0; t < 4; ++t)
-                a[t] = fb ? *reinterpret_cast<const uint4*>(fb + ((size_t)(kb * 4 + st) * 32 + 4 * g + t) * 16)
-                          : make_uint4(0, 0, 0, 0);
-              out[st][0] = make_uint4(a[0].x, a[1].x, a[2].x, a[3].x);
-              out[st][1] = make_uint4(a[0].z, a[1].z, a[2].z, a[3].z);
-              out[st][2] = make_uint4(a[0].y, a[1].y, a[2].y, a[3].y);
-              out[st][3] = make_uint4(a[0].w, a[1].w, a[2].w, a[3].w);
-            }
+            pf_gather_f16(fb, kb, g, out);
             ok = store_stage(kb, out);
           }
       }
@@ -455,6 +489,82 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Debug: the decoded weights of expert e's matrix m exactly as the dequant
+// warps of this kernel produce them (same LUT set-up, plane loads and decode
+// routines), written to out[rows][cols] instead of the swizzled A tile.  One
+// CTA per 128-row tile; warps (slab, parity) as in the kernel.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, int m, __half* out) {
+  extern __shared__ __align__(16) unsigned char pfd_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slab = (warp >> 1) & 1, par = warp & 1, tis = lane >> 3, g = lane & 7;
+  const int R = m < 2 ? L.f : L.d, C = m < 2 ? L.d : L.f;
+  const int nkb = C / PF_BK;
+  const int row0 = blockIdx.x * PF_BM + slab * 64 + tis * 16;
+  const bool tile_ok = row0 < R;
+  const int tau = row0 / 16;
+  const int b = L.bits[e];
+  uint32_t* tabg = reinterpret_cast<uint32_t*>(pfd_smem) + slab * (PF_TAB_BYTES / 4);
+  const uint32_t tab = smem_u32(tabg);
+  uint32_t lut3[2][4] = {};
+  if (b == 3) {
+    pf_load_lut3(L, e, m, row0, g, R, lut3);
+  } else if (b >= 4 && b <= 6) {
+    pf_build_tab_half(L, e, m, b, blockIdx.x * PF_BM + slab * 64, R, par, tabg);
+    __syncthreads();  // b is the same for the whole CTA
+  }
+  const char* pb[6];
+#pragma unroll
+  for (int p = 0; p < 6; ++p) pb[p] = (tile_ok && b <= 6 && p < b) ? tile_addr(L, e, m, p, tau) : nullptr;
+  const char* fb = (tile_ok && b == 16) ? tile_addr(L, e, m, kPlanes, tau) : nullptr;
+  auto put = [&](int kb, const uint4 (&o)[4][4]) {
+    if (!tile_ok) return;
+#pragma unroll
+    for (int st = 0; st < 4; ++st)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = row0 + g + 8 * (q >> 1), c = kb * PF_BK + 16 * st + 8 * (q & 1);
+        *reinterpret_cast<uint4*>(out + (size_t)r * C + c) = o[st][q];
+      }
+  };
+  auto planes = [&](auto tag) {
+    constexpr int BB = decltype(tag)::value;
+    for (int kb = par; kb < nkb; kb += 2) {
+      uint32_t w[4][BB];
+      pf_load_planes<BB>(pb, kb, nkb, g, w);
+      uint4 o[4][4];
+      if constexpr (BB == 3) pf_decode_planes3(w, lut3, o);
+      else pf_decode_planes<BB>(w, tab, lane * 4, 128 + lane * 4, o);
+      put(kb, o);
+    }
+  };
+  switch (b) {
+    case 3: planes(std::integral_constant<int, 3>{}); break;
+    case 4: planes(std::integral_constant<int, 4>{}); break;
+    case 5: planes(std::integral_constant<int, 5>{}); break;
+    case 6: planes(std::integral_constant<int, 6>{}); break;
+    case 16:
+      for (int kb = par; kb < nkb; kb += 2) {
+        uint4 o[4][4];
+        pf_gather_f16(fb, kb, g, o);
+        put(kb, o);
+      }
+      break;
+    default:
+      if (threadIdx.x == 0) atomicExch(L.err, kErrBits);
+  }
+}
+
+cudaError_t launch_prefill_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {
+  const int R = m < 2 ? L.f : L.d;
+  const uint32_t smem = 2 * PF_TAB_BYTES;
+  cudaError_t err = ensure_smem((const void*)prefill_dump_kernel, smem);
+  if (err != cudaSuccess) return err;
+  prefill_dump_kernel<<<(R + PF_BM - 1) / PF_BM, 128, smem, s>>>(L, e, m, out);
+  return cudaGetLastError();
+}
 
 static int env_tokens(const char* name, int dflt) {
   const char* s = getenv(name);

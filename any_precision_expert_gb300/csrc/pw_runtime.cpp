@@ -272,6 +272,8 @@ struct pw_layer_s {
   std::vector<Block> f16;                    // [E]
   std::vector<unsigned long long> h_plane_pt, h_f16_pt;
   bool shared_loaded = false;
+  long long spin_limit = kDefaultSpinPolls;  // see pw_testing_wait_limit
+  int wait_bias = 0;
 
   Block& plane(int e, int p) { return planes[(size_t)e * kPlanes + p]; }
 
@@ -296,6 +298,8 @@ struct pw_layer_s {
     for (int m = 0; m < 3; ++m) L.shared16[m] = shared_loaded ? d_shared[m] : nullptr;
     L.err = d_err;
     L.sync = d_sync;
+    L.spin_limit = spin_limit;
+    L.wait_bias = wait_bias;
     return L;
   }
 };
@@ -437,6 +441,13 @@ extern "C" pw_status pw_last_cuda_error(int* cuda_err) {
 
 extern "C" pw_status pw_testing_host_sim(int enable) {
   g_sim = enable != 0;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_testing_wait_limit(pw_layer_t l, long long polls, int never_ready) {
+  if (!l || polls < 0 || (never_ready != 0 && never_ready != 1)) return PW_ERR_INVALID_ARG;
+  l->spin_limit = polls == 0 ? kDefaultSpinPolls : polls;
+  l->wait_bias = never_ready;
   return PW_OK;
 }
 
@@ -1111,6 +1122,7 @@ extern "C" pw_status pw_permute(pw_layer_t l, const int32_t* idx, int T, const v
   if (T > 0 && (!idx || !perm_src || !inv_slot || !ws)) return PW_ERR_INVALID_ARG;
   if (T > 0 && (x == nullptr) != (x_perm == nullptr)) return PW_ERR_INVALID_ARG;
   if (T > 0 && x && (!aligned16(x) || !aligned16(x_perm))) return PW_ERR_INVALID_ARG;
+  if (T > 0 && !aligned16(ws)) return PW_ERR_INVALID_ARG;
   const WsLayout W = ws_layout(l, T);
   if (T > 0 && ws_bytes < W.perm_off + W.perm_bytes) return PW_ERR_OOM;
   PW_TRY(device_only());
@@ -1126,7 +1138,7 @@ extern "C" pw_status pw_expert_ffn_bitplane(pw_layer_t l, const void* x_perm, co
   if (bad_tokens(T)) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
   if (!x_perm || !offsets || !y_perm || !ws) return PW_ERR_INVALID_ARG;
-  if (!aligned16(x_perm) || !aligned16(y_perm)) return PW_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(y_perm) || !aligned16(ws)) return PW_ERR_INVALID_ARG;
   const WsLayout W = ws_layout(l, T);
   if (ws_bytes < W.h_off + W.h_bytes) return PW_ERR_OOM;
   PW_TRY(all_loaded(l));
@@ -1143,7 +1155,7 @@ extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_
   if (bad_tokens(T)) return PW_ERR_INVALID_ARG;
   if (l->desc.shared_ffn == 0 || !l->shared_loaded) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
-  if (!x || !y_shared || !ws || !aligned16(x) || !aligned16(y_shared)) return PW_ERR_INVALID_ARG;
+  if (!x || !y_shared || !ws || !aligned16(x) || !aligned16(y_shared) || !aligned16(ws)) return PW_ERR_INVALID_ARG;
   const WsLayout W = ws_layout(l, T);
   if (ws_bytes < W.total) return PW_ERR_OOM;
   PW_TRY(device_only());
@@ -1160,7 +1172,7 @@ extern "C" pw_status pw_moe_ffn(pw_layer_t l, const void* x, const void* x_perm,
   if (sh && !l->shared_loaded) return PW_ERR_INVALID_ARG;
   if (T == 0) return device_only();
   if (!x_perm || !offsets || !y_perm || !ws) return PW_ERR_INVALID_ARG;
-  if (!aligned16(x_perm) || !aligned16(y_perm)) return PW_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(y_perm) || !aligned16(ws)) return PW_ERR_INVALID_ARG;
   if (sh && (!x || !y_shared || !aligned16(x) || !aligned16(y_shared))) return PW_ERR_INVALID_ARG;
   const WsLayout W = ws_layout(l, T);
   if (ws_bytes < W.total) return PW_ERR_OOM;
@@ -1201,7 +1213,7 @@ extern "C" pw_status pw_layer_check_device(pw_layer_t l, void* stream) {
     if (err[0] != 0) PW_CUDA(cudaMemsetAsync(l->d_sync, 0, sizeof(int) * sync_words(l->desc.n_experts), s));
     PW_CUDA(cudaStreamSynchronize(s));
   }
-  if (err[0] == 1) return PW_ERR_TIMEOUT;
+  if (err[0] == kErrTimeout) return PW_ERR_TIMEOUT;
   if (err[0] != 0) return PW_ERR_DEVICE_CHECK;
   return PW_OK;
 }
@@ -1212,6 +1224,18 @@ extern "C" pw_status pw_debug_dequant(pw_layer_t l, int e, int m, void* out, voi
   if (l->bits[e] == 0) return PW_ERR_INVALID_ARG;
   PW_TRY(device_only());
   return launched(launch_debug_dequant(l->dev(), e, m, static_cast<__half*>(out), as_stream(stream)));
+}
+
+extern "C" pw_status pw_debug_dequant_kernel(pw_layer_t l, int e, int m, int kernel, void* out, void* stream) {
+  PW_TRY(check_layer(l));
+  if (e < 0 || e >= l->desc.n_experts || m < 0 || m > 2 || !out || !aligned16(out)) return PW_ERR_INVALID_ARG;
+  if (kernel != PW_KERNEL_DECODE && kernel != PW_KERNEL_PREFILL) return PW_ERR_INVALID_ARG;
+  if (l->bits[e] == 0) return PW_ERR_INVALID_ARG;
+  PW_TRY(device_only());
+  const DevLayer L = l->dev();
+  auto* o = static_cast<__half*>(out);
+  return launched(kernel == PW_KERNEL_DECODE ? launch_decode_dump(L, e, m, o, as_stream(stream))
+                                             : launch_prefill_dump(L, e, m, o, as_stream(stream)));
 }
 
 extern "C" pw_status pw_debug_page_address(pw_layer_t l, int e, int p, int vpage, uint64_t* addr) {

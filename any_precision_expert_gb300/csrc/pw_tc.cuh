@@ -43,7 +43,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volati
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort_flag = 1;
-      atomicExch(err, 1);
+      atomicExch(err, 1);  // the timeout value of the layer error word
       return false;
     }
   }

@@ -162,12 +162,18 @@ pw_status pw_route_topk(pw_layer_t layer, const void* x, const void* wr, const f
 /*
  * Stable permutation of the S = T*K slots (flat index t*K + k) by expert:
  * inside an expert's bucket the slots keep ascending flat order.
+ * The write-ups do not describe this step.  Their method runs each expert's
+ * FFN over the tokens routed to it ("核心洞察"), and grouping the routed
+ * (token, k) slots by expert is what gives every expert those tokens as one
+ * contiguous batch; the definition above (a stable counting sort) is this
+ * library's, chosen so the result is unique and deterministic.
  *   offsets  device int32 [E+1]: bucket e is [offsets[e], offsets[e+1])
  *   perm_src device int32 [S]:   token of each sorted slot
  *   inv_slot device int32 [S]:   sorted position of flat slot t*K + k
  *   x        device fp16 [T][d] and x_perm device fp16 [S][d]: if both are
  *            non-NULL, x_perm[i] = x[perm_src[i]].
- *   ws       device scratch of at least pw_workspace_size() bytes.
+ *   ws       device scratch of at least pw_workspace_size() bytes,
+ *            16-byte aligned.
  * Deterministic (no atomics decide any order).
  */
 pw_status pw_permute(pw_layer_t layer, const int32_t* idx, int T, const void* x,
@@ -175,14 +181,23 @@ pw_status pw_permute(pw_layer_t layer, const int32_t* idx, int T, const void* x,
                      void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Routed expert SwiGLU FFN over the permuted slots.  For each expert e with
+ * Routed expert SwiGLU FFN over the permuted slots (write-up "内存的饥饿游戏",
+ * section 核心洞察: each expert weight is an any-precision code stored as
+ * bit-planes plus a per-row LUT; an expert at b bits reads only its top b
+ * planes, and a 16-bit expert its fp16 page).  For each expert e with
  * tokens (bucket of `offsets`) at its current bitwidth b_e:
  *   W = LUT_b[row][code_b] built from planes 0..b-1 only (planes >= b are never
  *       read), or the fp16 page when b_e == 16,
  *   h = silu(W_gate x) * (W_up x)   (fp32 accumulation; h rounded to fp16),
  *   y_perm[slot] = W_down h          (fp32).
  *   x_perm  device fp16 [T*K][d]     offsets device int32 [E+1]
- *   y_perm  device fp32 [T*K][d]     ws device scratch (pw_workspace_size)
+ *   y_perm  device fp32 [T*K][d]
+ *   ws      device scratch of at least pw_workspace_size(T) bytes, 16-byte
+ *           aligned (the h activations are carved out of it)
+ * offsets must be monotone in [0, T*K]; the kernels clamp a bad table to the
+ * slot rows and flag the layer's device error word (pw_layer_check_device
+ * then returns PW_ERR_DEVICE_CHECK), so nothing outside x_perm, y_perm and ws
+ * is touched.
  */
 pw_status pw_expert_ffn_bitplane(pw_layer_t layer, const void* x_perm, const int32_t* offsets,
                                  int T, float* y_perm, void* ws, size_t ws_bytes, void* stream);
@@ -200,7 +215,9 @@ pw_status pw_expert_ffn_bitplane(pw_layer_t layer, const void* x_perm, const int
  * (PW_ERR_OOM otherwise; nothing is launched).  No device memory is allocated
  * by this call.  Its first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls share the array: calls whose
+ * call before any stream capture.  The address is kept for the life of the
+ * process: no device reset (cudaDeviceReset) may come between calls on that
+ * device.  All calls share the array: calls whose
  * kernels overlap on the GPU (different streams, or different layers run
  * concurrently) race on it, so serialise them.  Nothing in it has to start at
  * zero; it keeps the last call's data.
@@ -208,7 +225,10 @@ pw_status pw_expert_ffn_bitplane(pw_layer_t layer, const void* x_perm, const int
 pw_status pw_expert_ffn_bitplane_noalloc(pw_layer_t layer, const void* x_perm, const int32_t* offsets,
                                          int T, float* y_perm, void* stream);
 
-/* fp16 shared FFN on all T tokens: y_shared [T][d] fp32 (layers with shared_ffn > 0). */
+/*
+ * fp16 shared FFN on all T tokens: y_shared [T][d] fp32 (layers with
+ * shared_ffn > 0).  ws: pw_workspace_size(T) bytes, 16-byte aligned.
+ */
 pw_status pw_shared_ffn(pw_layer_t layer, const void* x, int T, float* y_shared,
                         void* ws, size_t ws_bytes, void* stream);
 
@@ -217,7 +237,8 @@ pw_status pw_shared_ffn(pw_layer_t layer, const void* x, int T, float* y_shared,
  * one call: decode-sized work of both runs in one persistent kernel, so the
  * shared FFN's weight stream overlaps the routed experts'.  Same results as
  * the two calls.  x [T][d] and y_shared [T][d] are ignored (may be NULL) when
- * the layer has no shared FFN.  ws must hold pw_workspace_size(T) bytes.
+ * the layer has no shared FFN.  ws must hold pw_workspace_size(T) bytes and
+ * be 16-byte aligned.
  *
  * The FFN calls of one layer keep progress counters in the layer's device
  * state: run them on one stream (they may not overlap on the GPU).
@@ -230,6 +251,11 @@ pw_status pw_moe_ffn(pw_layer_t layer, const void* x, const void* x_perm, const 
  *   y[t] = sum_{k<K} w[t][k] * y_perm[inv_slot[t*K+k]]  (+ y_shared[t])
  * summed in k order in fp32, rounded to fp16.  The shared FFN output is added
  * unweighted.  y_shared may be NULL.  y device fp16 [T][d].
+ * The write-ups do not describe this step either: it is the output of a
+ * routed MoE layer, each token's experts weighted by its router weights (the
+ * gate that "三层感知" reads its routing statistics from).  The k order and
+ * fp32 sum are this library's, for a deterministic result.  An inv_slot entry
+ * outside [0, T*K) is read as slot 0 and flags the layer's device error word.
  */
 pw_status pw_combine(pw_layer_t layer, const float* y_perm, const int32_t* inv_slot,
                      const float* w, int T, const float* y_shared, void* y, void* stream);
@@ -395,11 +421,30 @@ pw_status pw_pack_planes(const uint8_t* code6, int R, int C, uint32_t* const pla
 pw_status pw_pack_f16(const uint16_t* w, int R, int C, uint16_t* out);
 
 /*
- * Debug: write expert e's matrix m (0 gate, 1 up, 2 down) as the kernels see it
- * at its current bitwidth, dequantised, into out (device fp16 [rows][cols]).
- * Uses the same device decode routines as the FFN kernels.
+ * Debug: write expert e's matrix m (0 gate, 1 up, 2 down) at its current
+ * bitwidth, dequantised, into out (device fp16 [rows][cols]).  A plain
+ * reference decoder: the planes are read through the page table and every
+ * code is looked up in a per-lane LUT table (the layout of the stored words
+ * and tables, not the kernels' own loops; pw_debug_dequant_kernel below dumps
+ * those).
  */
 pw_status pw_debug_dequant(pw_layer_t layer, int e, int m, void* out, void* stream);
+
+/*
+ * Debug: the same dump, produced by the FFN kernels' own code paths:
+ *   PW_KERNEL_DECODE   the decode kernel's K loop (its cp.async ring through
+ *                      the page table, 3-bit register-LUT byte permutes,
+ *                      4..6-bit shared LUT table, fp16 fragments) with each
+ *                      decoded A fragment written out instead of multiplied;
+ *   PW_KERNEL_PREFILL  the tcgen05 GEMM's dequant warps (plane loads, LUT
+ *                      set-up and decode) writing rows instead of the
+ *                      swizzled shared-memory tile.
+ * out device fp16 [rows][cols], 16-byte aligned.  Section 核心洞察 of the
+ * write-up fixes the value: W = LUT_b[row][code6 >> (6 - b)], or the fp16
+ * page at 16 bits.
+ */
+enum { PW_KERNEL_DECODE = 0, PW_KERNEL_PREFILL = 1 };
+pw_status pw_debug_dequant_kernel(pw_layer_t layer, int e, int m, int kernel, void* out, void* stream);
 
 /* Debug: device address of virtual page `vpage` of expert e's plane p (p = 6: fp16 page), or 0. */
 pw_status pw_debug_page_address(pw_layer_t layer, int e, int p, int vpage, uint64_t* addr);
@@ -413,6 +458,20 @@ pw_status pw_debug_page_address(pw_layer_t layer, int e, int p, int vpage, uint6
  */
 pw_status pw_testing_host_sim(int enable);
 pw_status pw_testing_complete_events(void);
+
+/*
+ * Testing hook for the bounded waits of the decode kernel: a down item waits
+ * (polling a counter) until every gate/up tile of its token chunk is done,
+ * and the fused step waits for every down item before its combine.
+ *   polls        polls before such a wait gives up (0 restores the default,
+ *                about a second); the kernel then sets the layer's device
+ *                error word, carries on and returns its counters to zero,
+ *                and pw_layer_check_device reports PW_ERR_TIMEOUT.
+ *   never_ready  1: down items wait for one tile more than exist (a count
+ *                nothing reaches), so every such wait runs out; 0: normal.
+ * Affects launches enqueued after the call, for this layer only.
+ */
+pw_status pw_testing_wait_limit(pw_layer_t layer, long long polls, int never_ready);
 
 #ifdef __cplusplus
 }

@@ -246,6 +246,28 @@ def test_forward_call_checks_arguments_on_the_host(sim):
     pool.close()
 
 
+def test_scratch_must_be_16_byte_aligned(sim):
+    # h and hs are carved out of ws and read back with 16-byte copies, so a
+    # misaligned ws is refused on the host (status 1) instead of reaching a kernel
+    pool = pw.Pool(64 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = pw.Layer(pool, 128, 128, 4, 2, 1, 128)
+    for e in range(4):
+        _load(layer, e, 3, _expert(e, w16=False))
+    rng = np.random.default_rng(5)
+    layer.load_shared([(rng.standard_normal(s) * 0.02).astype(np.float16)
+                       for s in ((128, 128), (128, 128), (128, 128))], stream=0)
+    n = layer.workspace_size(8)
+    L = _lib.lib
+    h = layer.handle
+    for ws, want in ((258, 1), (264, 1), (256, 2)):  # aligned scratch reaches the "no device" refusal
+        assert L.pw_expert_ffn_bitplane(h, 256, 256, 8, 256, ws, n, None) == want
+        assert L.pw_moe_ffn(h, 256, 256, 256, 8, 256, 256, ws, n, None) == want
+        assert L.pw_shared_ffn(h, 256, 8, 256, ws, n, None) == want
+        assert L.pw_permute(h, 256, 8, 256, 256, 256, 256, 256, ws, n, None) == want
+    layer.destroy()
+    pool.close()
+
+
 def test_copy_expert_between_layers(sim):
     pool = pw.Pool(96 * PAGE, page_bytes=PAGE, device="cpu")
     a = _layer(pool)

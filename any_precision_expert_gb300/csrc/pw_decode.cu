@@ -73,7 +73,7 @@ struct Geo {
 
 // Weight units streamed by a warp (one matrix of its tile):
 //   KIND_F16: 64 columns of the fp16 page, 4 x 16 B per lane (ring depth 3);
-//   KIND_PB: half a plane group (2 chunks, 128 columns), 8 B per lane and plane (ring slots sized for 6 planes);
+//   KIND_PB: half a plane group (2 chunks, 128 columns), 8 B per lane and plane (4..6 bits);
 //   KIND_PG: a whole plane group (4 chunks, 256 columns), 16 B per lane and plane.
 enum { KIND_F16 = 1, KIND_PB = 2, KIND_PG = 3 };
 constexpr int kF16Steps = 4;  // mma steps (16 columns each) of one fp16 unit
@@ -81,7 +81,7 @@ constexpr int kF16Steps = 4;  // mma steps (16 columns each) of one fp16 unit
 template <int KIND, int B>
 struct Unit {
   static constexpr int COLS = KIND == KIND_F16 ? 16 * kF16Steps : KIND == KIND_PB ? 128 : 256;
-  static constexpr int LANE_BYTES = KIND == KIND_F16 ? kF16Steps * 16 : KIND == KIND_PB ? kPlanes * 8 : B * 16;
+  static constexpr int LANE_BYTES = KIND == KIND_F16 ? kF16Steps * 16 : KIND == KIND_PB ? B * 8 : B * 16;
   static constexpr int SLOT = LANE_BYTES * 32;
   static constexpr int R = Geo::RB / SLOT > 8 ? 8 : Geo::RB / SLOT;  // ring depth
   static_assert(Geo::RB / SLOT >= 3, "ring too shallow");
@@ -121,6 +121,13 @@ __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// 16-bit shared load, zero-extended into a 32-bit register.
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
@@ -182,21 +189,41 @@ __device__ __forceinline__ void stage_kblock(const __half* act, const int* s_tok
   }
 }
 
-// B fragments of mma step s (16 columns at column kc + 16 s of its K-block)
-// for the n-tiles: one ldmatrix.x4 per pair of n-tiles (b0, b1 of each).
-// Token rows past the staged ones read the last staged row; their results
-// are not stored.
-__device__ __forceinline__ void slab_bstep(uint32_t buf, int kc, int s, int NT, int srows, int rs,
+// This lane's ldmatrix row of each pair of n-tiles in a staged K-block, fixed
+// for a whole K loop: off = r * rs (row r = token (2 i + mat / 2) * 8 + lane %
+// 8, rows past the staged ones reading the last one) and x16 = (r % 8 ^ mat %
+// 2) * 16, the swizzle of the row's 16-byte pieces.  Since every step starts
+// at a multiple of 64 columns, piece 2 s + mat % 2 of step s sits at byte
+// 2 kc + ((32 s) ^ x16) of the row.
+struct BRows {
+  uint32_t off[Geo::NTM / 2];
+  uint32_t x16[Geo::NTM / 2];
+};
+
+__device__ __forceinline__ BRows slab_brows(int srows, int rs) {
+  const int lane = threadIdx.x & 31, mat = lane >> 3;
+  BRows o;
+#pragma unroll
+  for (int i = 0; i < Geo::NTM / 2; ++i) {
+    const int r = min((2 * i + (mat >> 1)) * 8 + (lane & 7), srows - 1);
+    o.off[i] = (uint32_t)(r * rs);
+    o.x16[i] = (uint32_t)(((r & 7) ^ (mat & 1)) << 4);
+  }
+  return o;
+}
+
+// B fragments of mma step s (16 columns at column kc + 16 s of its K-block,
+// kc a multiple of 64) for the n-tiles: one ldmatrix.x4 per pair of n-tiles
+// (b0, b1 of each).  Rows past the staged ones read the last staged row;
+// their results are not stored.
+__device__ __forceinline__ void slab_bstep(uint32_t buf, int kc, int s, int NT, const BRows& br,
                                            uint32_t (&bf)[Geo::NTM][2]) {
-  const int lane = threadIdx.x & 31;
-  const int mat = lane >> 3;
-  const int j = (kc >> 3) + 2 * s + (mat & 1);
+  const uint32_t row0 = buf + 2 * (uint32_t)kc;
 #pragma unroll
   for (int nt0 = 0; nt0 < Geo::NTM; nt0 += 2) {
-    if (nt0 < NT) {
-      const int r = min((nt0 + (mat >> 1)) * 8 + (lane & 7), srows - 1);
-      ldsm_x4(buf + slab_off(r, j, rs), bf[nt0][0], bf[nt0][1], bf[nt0 + 1][0], bf[nt0 + 1][1]);
-    }
+    if (nt0 < NT)
+      ldsm_x4(row0 + br.off[nt0 / 2] + (br.x16[nt0 / 2] ^ (uint32_t)(32 * s)), bf[nt0][0], bf[nt0][1],
+              bf[nt0 + 1][0], bf[nt0 + 1][1]);
   }
 }
 
@@ -207,30 +234,32 @@ __device__ __forceinline__ void mma_tiles(float (&acc)[Geo::NTM][4], const uint3
     if (nt < NT) mma16816(acc[nt], a, bf[nt][0], bf[nt][1]);
 }
 
-// Decode mma step s of one chunk of nb-bit codes (nb = 4..6) into the A
+// Decode mma step s of one chunk of B-bit codes (B = 4..6) into the A
 // fragment through the warp's LUT table: entry (v, g) at byte 32 v + 4 g holds
 // LUT[row g][v] in its low and LUT[row g+8][v] in its high half; tabg = table
-// + 4 g (g = lane / 4).  Plane p keeps code bit nb-1-p of weight (h, s, byte
+// + 4 g (g = lane / 4).  Plane p keeps code bit B-1-p of weight (h, s, byte
 // k) at bit 8k + 4h + s + 5 - p (mod 32): masking one bit per byte and
-// rotating right by 4h + s + 6 - nb leaves the codes of R[h] in the low nb
-// bits of its bytes.
-__device__ __forceinline__ void decode_step_rt(const uint32_t (&w)[kPlanes], int nb, const int s, uint32_t tabg,
-                                               uint32_t (&a)[4]) {
+// rotating right by 4h + s + 6 - B leaves the codes of R[h] in the low B
+// bits of its bytes.  Each lookup reads the one 16-bit half it needs (row g:
+// +0, row g+8: +2), zero-extended, so the two columns of a fragment register
+// join with an integer multiply-add (the FMA pipe, beside the busy ALU).
+template <int B>
+__device__ __forceinline__ void decode_step_rt(const uint32_t (&w)[B], const int s, uint32_t tabg, uint32_t (&a)[4]) {
   uint32_t R[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t m = 0;
 #pragma unroll
-    for (int p = 0; p < kPlanes; ++p)
-      if (p < nb) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
-    R[h] = rotr(m, 4 * h + s + 6 - nb);
+    for (int p = 0; p < B; ++p) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
+    R[h] = rotr(m, 4 * h + s + 6 - B);
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {  // k = 2 * rowsel + colhalf
-    const uint32_t e0 = lds32(tabg + (prmt(R[0], 0u, 0x4440u | (uint32_t)k) << 5));
-    const uint32_t e1 = lds32(tabg + (prmt(R[1], 0u, 0x4440u | (uint32_t)k) << 5));
+    const uint32_t half = (k >> 1) * 2;
+    const uint32_t e0 = lds16(tabg + half + (prmt(R[0], 0u, 0x4440u | (uint32_t)k) << 5));
+    const uint32_t e1 = lds16(tabg + half + (prmt(R[1], 0u, 0x4440u | (uint32_t)k) << 5));
     const int reg = (k == 0) ? 0 : (k == 1) ? 2 : (k == 2) ? 1 : 3;
-    a[reg] = prmt(e0, e1, (k >> 1) ? 0x7632u : 0x5410u);
+    a[reg] = e1 * 65536u + e0;
   }
 }
 
@@ -274,7 +303,6 @@ __device__ __forceinline__ void dump_frag(const Dump& D, const uint32_t (&a)[4],
 struct WSrc {
   const char* p[kPlanes];  // plane tiles, or the fp16 tile in p[0]
   uint32_t lut3[2][4];     // 3 bits: register LUTs of rows g and g + 8
-  int nb;                  // 4..6 bits: planes streamed
   uint32_t tabg;           // 4..6 bits: the warp's LUT table + 4 g
 };
 
@@ -296,7 +324,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
   const int nu = (K + U::COLS - 1) / U::COLS;
   const int mine = u0 < nu ? (nu - u0 + us - 1) / us : 0;
   const int kbs = (K + kbw - 1) / kbw;
-  const int nb = B == 0 ? src.nb : B;
+  const BRows br = slab_brows(ntok, rs);
 
   auto issue = [&](int i) {
     const int cb = u0 + i * us;
@@ -321,15 +349,13 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
       if (gamma < GR) {
         const size_t off = (size_t)(gamma * 128 + lane * 4 + 2 * j) * 4;
 #pragma unroll
-        for (int p = 0; p < kPlanes; ++p)
-          if (p < nb) cp_async8(slot + (p * 32 + lane) * 8, src.p[p] + off);
+        for (int p = 0; p < B; ++p) cp_async8(slot + (p * 32 + lane) * 8, src.p[p] + off);
       } else {
         const int cnt = min(2, rem - 2 * j);
         const size_t off = (size_t)(GR * 128 + lane * rem + 2 * j) * 4;
 #pragma unroll
-        for (int p = 0; p < kPlanes; ++p)
-          if (p < nb)
-            for (int k = 0; k < cnt; ++k) cp_async4(slot + (p * 32 + lane) * 8 + 4 * k, src.p[p] + off + 4 * k);
+        for (int p = 0; p < B; ++p)
+          for (int k = 0; k < cnt; ++k) cp_async4(slot + (p * 32 + lane) * 8 + 4 * k, src.p[p] + off + 4 * k);
       }
     }
   };
@@ -380,43 +406,40 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
           dump_frag(*dump, a, (kb << lkb) + kc0 + 16 * s);
         } else {
           uint32_t bf[G::NTM][2];
-          slab_bstep(buf, kc0, s, NT, ntok, rs, bf);
+          slab_bstep(buf, kc0, s, NT, br, bf);
           mma_tiles(acc, a, bf, NT);
         }
       }
     } else {
+      // KIND_PG (3 bits): the unit's words of every plane in one 16-byte load
+      // per plane, chunks unrolled; KIND_PB (4..6 bits): each chunk reads its
+      // own word of every plane (no selects between chunk words)
       constexpr int W = KIND == KIND_PG ? 4 : 2;  // words (chunks) per lane and plane
-      constexpr int NP = KIND == KIND_PG ? B : kPlanes;
-      uint32_t w[NP][W];
+      uint32_t w[B][W];
+      if constexpr (KIND == KIND_PG) {
 #pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        if constexpr (W == 4) {
+        for (int p = 0; p < B; ++p) {
           const uint4 v = lds128(slot + (p * 32 + lane) * 16);
           w[p][0] = v.x;
           w[p][1] = v.y;
           w[p][2] = v.z;
           w[p][3] = v.w;
-        } else {
-          uint2 v = make_uint2(0u, 0u);
-          if (p < nb) v = lds64(slot + (p * 32 + lane) * 8);
-          w[p][0] = v.x;
-          w[p][1] = v.y;
         }
       }
       const int nch = W == 4 ? (cb < GR ? 4 : rem) : (cb >> 1) < GR ? 2 : min(2, rem - 2 * (cb & 1));
       auto chunk = [&](int c) {
-        uint32_t wc[NP];
+        uint32_t wc[B];
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
+        for (int p = 0; p < B; ++p) {
           if constexpr (W == 4) wc[p] = c == 0 ? w[p][0] : c == 1 ? w[p][1] : c == 2 ? w[p][2] : w[p][3];
-          else wc[p] = c ? w[p][1] : w[p][0];
+          else wc[p] = lds32(slot + (p * 32 + lane) * 8 + 4 * c);
         }
         // decode the chunk's four steps first (independent chains), then the mma's
         uint32_t a[4][4];
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3, a[s]);
-          else decode_step_rt(wc, nb, s, src.tabg, a[s]);
+          else decode_step_rt<B>(wc, s, src.tabg, a[s]);
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
@@ -424,7 +447,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
             dump_frag(*dump, a[s], (kb << lkb) + kc0 + c * 64 + 16 * s);
           } else {
             uint32_t bf[G::NTM][2];
-            slab_bstep(buf, kc0 + c * 64, s, NT, ntok, rs, bf);
+            slab_bstep(buf, kc0 + c * 64, s, NT, br, bf);
             mma_tiles(acc, a[s], bf, NT);
           }
         }
@@ -437,8 +460,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
       } else {
         // table lookups: the chunks share one copy of the code
 #pragma unroll 1
-        for (int c = 0; c < W; ++c)
-          if (c < nch) chunk(c);
+        for (int c = 0; c < nch; ++c) chunk(c);
       }
     }
   }
@@ -476,11 +498,10 @@ __device__ __forceinline__ void tile_store_y(const float (&acc)[Geo::NTM][4], in
 
 // Weight sources of tile t of matrix m (expert e, or the shared FFN) for one
 // warp: page-table addresses of its planes or fp16 tile, and for 3 bits the
-// register LUTs of the lane's rows.  Returns the tile's LUT_b rows, from which
-// a 4..6-bit warp builds its shared table (null otherwise).  B: 16, 3 or 0
-// (4..6 bits, b).
+// register LUTs of the lane's rows.  Returns the tile's LUT_B rows, from which
+// a 4..6-bit warp builds its shared table (null otherwise).  B: 16, 3, 4, 5, 6.
 template <int B>
-__device__ __forceinline__ const __half* tile_src(const DevLayer& L, int e, bool sh, int m, int t, int b, int K,
+__device__ __forceinline__ const __half* tile_src(const DevLayer& L, int e, bool sh, int m, int t, int K,
                                                   uint32_t tab, WSrc& src) {
   const int lane = threadIdx.x & 31;
   if constexpr (B == 16) {
@@ -494,11 +515,10 @@ __device__ __forceinline__ const __half* tile_src(const DevLayer& L, int e, bool
     load_lut3(lr + ((lane >> 2) + 8) * 8, src.lut3[1]);
     return nullptr;
   } else {
-    src.nb = b;
 #pragma unroll
-    for (int p = 0; p < kPlanes; ++p) src.p[p] = p < b ? tile_addr(L, e, m, p, t) : nullptr;
+    for (int p = 0; p < kPlanes; ++p) src.p[p] = p < B ? tile_addr(L, e, m, p, t) : nullptr;
     src.tabg = tab + (lane >> 2) * 4;
-    return lut_rows(L, e, m, b, t * kTileRows);
+    return lut_rows(L, e, m, B, t * kTileRows);
   }
 }
 
@@ -517,8 +537,7 @@ struct ItemArgs {
 // tile (S = 1: warp w takes tile tau + w; S = 2: tiles tau, tau + 1; S = 4:
 // tile tau), slice k of a tile taking every S-th unit from unit k.  Partial
 // and up sums go through shared memory to the first warp of each tile, which
-// adds them in warp order and stores.  B: 16 (fp16 page), 3, or 0 (4..6
-// bits, A.b).
+// adds them in warp order and stores.  B: 16 (fp16 page), 3, 4, 5 or 6.
 template <int B>
 __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A, int NM, int S, int tau,
                                            uint32_t ring, uint32_t slab, uint32_t tab, const int* s_tok) {
@@ -530,14 +549,14 @@ __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A,
   const int m = NM == 2 ? warp >> 1 : 2;     // and matrix
   float acc[kNT][4] = {};
   WSrc src;
-  const __half* lr = tile_src<B>(L, A.e, A.sh, m, t, A.b, A.K, tab, src);
+  const __half* lr = tile_src<B>(L, A.e, A.sh, m, t, A.K, tab, src);
   if constexpr (B == 16) {
     kloop<KIND_F16, 16>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
   } else if constexpr (B == 3) {
     kloop<KIND_PG, 3>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
   } else {
-    kloop<KIND_PB, 0>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc,
-                      [&] { build_tab_warp(lr, A.b, tab); });
+    kloop<KIND_PB, B>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc,
+                      [&] { build_tab_warp(lr, B, tab); });
   }
   if (NM == 1 && S == 1) {
     tile_store_y(acc, t, A.row0, A.ntok, A.ld, A.y);
@@ -858,9 +877,13 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     __syncthreads();
     const int tau = blk * per_item;
     const int NM = phase == 0 ? 2 : 1;
-    if (b == 16) block_item<16>(L, A, NM, S, tau, ring, slab, tab, s_tok);
-    else if (b == 3) block_item<3>(L, A, NM, S, tau, ring, slab, tab, s_tok);
-    else block_item<0>(L, A, NM, S, tau, ring, slab, tab, s_tok);
+    switch (b) {
+      case 16: block_item<16>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      case 3: block_item<3>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      case 4: block_item<4>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      case 5: block_item<5>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      default: block_item<6>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+    }
     __syncthreads();  // every tile of the item is stored
     if (tid == 0) {
       const int done_tiles = per_item;
@@ -957,17 +980,17 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
 // instead of feeding the mma.
 // ---------------------------------------------------------------------------
 template <int B>
-__device__ __forceinline__ void dump_tile(const DevLayer& L, int e, int m, int t, int b, int C, uint32_t ring,
+__device__ __forceinline__ void dump_tile(const DevLayer& L, int e, int m, int t, int C, uint32_t ring,
                                           uint32_t slab, uint32_t tab, const int* s_tok, const Dump& D) {
   float acc[Geo::NTM][4] = {};
   WSrc src;
-  const __half* lr = tile_src<B>(L, e, false, m, t, b, C, tab, src);
+  const __half* lr = tile_src<B>(L, e, false, m, t, C, tab, src);
   if constexpr (B == 16) {
     kloop<KIND_F16, 16, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [] {}, &D);
   } else if constexpr (B == 3) {
     kloop<KIND_PG, 3, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [] {}, &D);
   } else {
-    kloop<KIND_PB, 0, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [&] { build_tab_warp(lr, b, tab); },
+    kloop<KIND_PB, B, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [&] { build_tab_warp(lr, B, tab); },
                             &D);
   }
 }
@@ -983,11 +1006,15 @@ __global__ void __launch_bounds__(kCtaThreads) decode_dump_kernel(DevLayer L, in
   const uint32_t slab = smem_u32(smem_dump);
   const uint32_t tab = slab + 2 * Geo::HALF + warp * kTabW;
   const uint32_t ring = slab + 2 * Geo::HALF + kCtaWarps * kTabW + warp * Geo::RB;
-  const int b = L.bits[e];
-  if (b == 16) dump_tile<16>(L, e, m, t, b, C, ring, slab, tab, s_tok, D);
-  else if (b == 3) dump_tile<3>(L, e, m, t, b, C, ring, slab, tab, s_tok, D);
-  else if (is_tab(b)) dump_tile<0>(L, e, m, t, b, C, ring, slab, tab, s_tok, D);
-  else if (threadIdx.x == 0) atomicExch(L.err, kErrBits);
+  switch (L.bits[e]) {
+    case 16: dump_tile<16>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 3: dump_tile<3>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 4: dump_tile<4>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 5: dump_tile<5>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 6: dump_tile<6>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    default:
+      if (threadIdx.x == 0) atomicExch(L.err, kErrBits);
+  }
 }
 
 cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {

@@ -44,6 +44,7 @@ _SIGS = {
     "pw_last_cuda_error": (i32, [P_i32]),
     "pw_pool_create": (i32, [vp, sz, sz, C.POINTER(vp)]),
     "pw_pool_destroy": (i32, [vp]),
+    "pw_pool_create_vmm": (i32, [vp, sz, sz, i32, C.POINTER(vp)]),
     "pw_pool_get_stats": (i32, [vp, C.POINTER(PoolStats)]),
     "pw_layer_create": (i32, [vp, C.POINTER(LayerDesc), C.POINTER(vp)]),
     "pw_layer_destroy": (i32, [vp]),
@@ -76,6 +77,7 @@ _SIGS = {
     "pw_testing_host_sim": (i32, [i32]),
     "pw_testing_complete_events": (i32, []),
     "pw_testing_wait_limit": (i32, [vp, C.c_longlong, i32]),
+    "pw_testing_vmm_counts": (i32, [vp, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]),
 }
 
 for _name, (_res, _args) in _SIGS.items():

@@ -115,6 +115,25 @@ class Pool:
         check(lib.pw_pool_create(base + pad, buffer.numel() - pad, page_bytes, C.byref(self.handle)),
               "pw_pool_create")
 
+    @classmethod
+    def from_vmm_handles(cls, handles, page_bytes: int = 2 << 20, device: int = 0):
+        """Pool over caller-created physical pages (pw_pool_create_vmm): handles
+        are CUmemGenericAllocationHandle values of page_bytes each; the caller
+        keeps them alive until close() and releases them afterwards."""
+        self = cls.__new__(cls)
+        self.buffer = None
+        arr = (C.c_ulonglong * len(handles))(*[int(h) for h in handles])
+        self.handle = C.c_void_p()
+        check(lib.pw_pool_create_vmm(arr, len(handles), page_bytes, device, C.byref(self.handle)),
+              "pw_pool_create_vmm")
+        return self
+
+    def vmm_counts(self):
+        """(pages mapped, pages unmapped) so far by a virtual-memory pool."""
+        a, b = C.c_uint64(0), C.c_uint64(0)
+        check(lib.pw_testing_vmm_counts(self.handle, C.byref(a), C.byref(b)), "pw_testing_vmm_counts")
+        return a.value, b.value
+
     def stats(self) -> dict:
         s = PoolStats()
         check(lib.pw_pool_get_stats(self.handle, C.byref(s)), "pw_pool_get_stats")
@@ -273,8 +292,9 @@ class Layer:
         check(lib.pw_debug_dequant(self.handle, e, m, _p(out), _s(stream)), "pw_debug_dequant")
 
     def debug_dequant_kernel(self, e: int, m: int, kernel: str, out, stream=None):
-        """Dump through the decode kernel's ('decode') or the tcgen05 GEMM's ('prefill') own decode path."""
-        which = {"decode": 0, "prefill": 1}[kernel]
+        """Dump through the decode kernel's ('decode': the layer's configuration; 'decode_row' /
+        'decode_lane': a given LUT-table configuration) or the tcgen05 GEMM's ('prefill') own decode path."""
+        which = {"decode": 0, "prefill": 1, "decode_row": 2, "decode_lane": 3}[kernel]
         check(lib.pw_debug_dequant_kernel(self.handle, e, m, which, _p(out), _s(stream)), "pw_debug_dequant_kernel")
 
     def page_address(self, e: int, p: int, vpage: int) -> int:

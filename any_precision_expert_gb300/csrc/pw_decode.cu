@@ -50,41 +50,60 @@
 #include <cuda_runtime.h>
 
 #include "pw_gemv.cuh"
+#include "pw_route.cuh"
 
 namespace pw {
 
 constexpr int kCtaThreads = 128;
 constexpr int kCtaWarps = kCtaThreads / 32;
-constexpr int kTabW = 64 * 8 * 4;            // LUT table of one warp: 2^b entries x 8 row pairs x 4 B (b <= 6)
 constexpr int kFusedSlots = 512;             // routed slots (T * K) of a fused layer step
 
 // Items take up to 32 tokens (a weight tile is streamed and decoded once for
 // up to 32 tokens).  Shared memory: two K-block buffers of token rows, a LUT
-// table and a weight ring per warp; three CTAs per SM.
+// table and a weight ring per warp.
 struct Geo {
   static constexpr int TOK = 32;                // tokens per item
   static constexpr int NTM = TOK / 8;           // mma n-tiles per item
   static constexpr int SCOLS = 256;             // columns of one staged K-block at 32 tokens
   static constexpr int HALF = TOK * SCOLS * 2;  // bytes of one K-block buffer
-  static constexpr int RB = 7 * 1024;           // cp.async weight ring of one warp
-  static constexpr int BLOCKS = 3;              // CTAs per SM
-  static constexpr int SMEM = 2 * HALF + kCtaWarps * (kTabW + RB);
+};
+
+// The kernel's two configurations, which differ in the 4..6-bit LUT table:
+//   NBLK = 3: three CTAs per SM; one table per warp shared by the lanes of a
+//     row pair (entry (v, g) = LUT[g][v] | LUT[g+8][v] << 16 at byte 32 v + 4 g,
+//     2 KB at 6 bits); the four lanes of a row can collide on a bank;
+//   NBLK = 2: two CTAs per SM; every lane its own copy of its two rows (entry
+//     (v, lane) at byte 128 v + 4 lane, 8 KB at 6 bits): the 32 lookups of a
+//     warp never collide on a bank, at two thirds of the resident warps.
+// Measured: the second is 12% faster on experts of ffn 14336 at 64 tokens and
+// 12% slower on the Qwen-shaped layer (few 4..6-bit experts, where the
+// warps matter more); layers with ffn >= 4096 take it (nblk_for).
+template <int NBLK>
+struct Cfg {
+  static constexpr bool LANE = NBLK == 2;              // per-lane LUT tables
+  static constexpr int BLOCKS = NBLK;                  // CTAs per SM
+  static constexpr int TABW = LANE ? 64 * 32 * 4 : 64 * 8 * 4;  // LUT table of one warp (b <= 6)
+  static constexpr int TSHIFT = LANE ? 7 : 5;          // log2 of the table's stride per code
+  static constexpr int RB = LANE ? 10 * 1024 : 7 * 1024;  // cp.async weight ring of one warp
+  static constexpr int SMEM = 2 * Geo::HALF + kCtaWarps * (TABW + RB);
 };
 
 // Weight units streamed by a warp (one matrix of its tile):
 //   KIND_F16: 64 columns of the fp16 page, 4 x 16 B per lane (ring depth 3);
-//   KIND_PB: half a plane group (2 chunks, 128 columns), 8 B per lane and plane (4..6 bits);
-//   KIND_PG: a whole plane group (4 chunks, 256 columns), 16 B per lane and plane.
+//   KIND_PB: half a plane group (2 chunks, 128 columns), 8 B per lane and plane
+//     (4..6 bits with the three-CTA configuration's 7 KB rings);
+//   KIND_PG: a whole plane group (4 chunks, 256 columns), 16 B per lane and plane
+//     (3 bits; 4..6 bits with the two-CTA configuration's 10 KB rings).
 enum { KIND_F16 = 1, KIND_PB = 2, KIND_PG = 3 };
 constexpr int kF16Steps = 4;  // mma steps (16 columns each) of one fp16 unit
 
-template <int KIND, int B>
+template <int KIND, int B, int RB>
 struct Unit {
   static constexpr int COLS = KIND == KIND_F16 ? 16 * kF16Steps : KIND == KIND_PB ? 128 : 256;
   static constexpr int LANE_BYTES = KIND == KIND_F16 ? kF16Steps * 16 : KIND == KIND_PB ? B * 8 : B * 16;
   static constexpr int SLOT = LANE_BYTES * 32;
-  static constexpr int R = Geo::RB / SLOT > 8 ? 8 : Geo::RB / SLOT;  // ring depth
-  static_assert(Geo::RB / SLOT >= 3, "ring too shallow");
+  static constexpr int R = RB / SLOT > 8 ? 8 : RB / SLOT;  // ring depth
+  static_assert(RB / SLOT >= 3, "ring too shallow");
   static_assert(Geo::SCOLS % COLS == 0, "units must not straddle K-blocks");
 };
 
@@ -100,10 +119,13 @@ struct UniParams {
   __half* hs;          // [T][fs]
   float* y;            // [n_slots][d]
   float* ys;           // [T][d]
-  // fused layer step only: the routing result replaces offsets / x_perm, and
-  // the kernel ends with the weighted combine
-  const int* idx;      // [T][K] experts of each token
-  const float* wk;     // [T][K] routing weights
+  // fused layer step only: the kernel routes, the routing result replaces
+  // offsets / x_perm, and the kernel ends with the weighted combine
+  const __half* wr;    // [E][d] router weight
+  const float* bias;   // [E] router bias, or null
+  float* rpart;        // [T][route_slices(d)][E] partial sums of the router
+  int* idx;            // [T][K] experts of each token (written by the router)
+  float* wk;           // [T][K] routing weights (written by the router)
   __half* yout;        // [T][d] layer output
   int* offsets_out;    // [E+1] slot offsets (written by CTA 0), or null
 };
@@ -121,13 +143,6 @@ __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
-// 16-bit shared load, zero-extended into a 32-bit register.
-__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
@@ -234,47 +249,32 @@ __device__ __forceinline__ void mma_tiles(float (&acc)[Geo::NTM][4], const uint3
     if (nt < NT) mma16816(acc[nt], a, bf[nt][0], bf[nt][1]);
 }
 
-// Decode mma step s of one chunk of B-bit codes (B = 4..6) into the A
-// fragment through the warp's LUT table: entry (v, g) at byte 32 v + 4 g holds
-// LUT[row g][v] in its low and LUT[row g+8][v] in its high half; tabg = table
-// + 4 g (g = lane / 4).  Plane p keeps code bit B-1-p of weight (h, s, byte
-// k) at bit 8k + 4h + s + 5 - p (mod 32): masking one bit per byte and
-// rotating right by 4h + s + 6 - B leaves the codes of R[h] in the low B
-// bits of its bytes.  Each lookup reads the one 16-bit half it needs (row g:
-// +0, row g+8: +2), zero-extended, so the two columns of a fragment register
-// join with an integer multiply-add (the FMA pipe, beside the busy ALU).
-template <int B>
-__device__ __forceinline__ void decode_step_rt(const uint32_t (&w)[B], const int s, uint32_t tabg, uint32_t (&a)[4]) {
-  uint32_t R[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int p = 0; p < B; ++p) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
-    R[h] = rotr(m, 4 * h + s + 6 - B);
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {  // k = 2 * rowsel + colhalf
-    const uint32_t half = (k >> 1) * 2;
-    const uint32_t e0 = lds16(tabg + half + (prmt(R[0], 0u, 0x4440u | (uint32_t)k) << 5));
-    const uint32_t e1 = lds16(tabg + half + (prmt(R[1], 0u, 0x4440u | (uint32_t)k) << 5));
-    const int reg = (k == 0) ? 0 : (k == 1) ? 2 : (k == 2) ? 1 : 3;
-    a[reg] = e1 * 65536u + e0;
-  }
-}
-
 // The warp's LUT table for one 16-row tile at bitwidth b (4..6): lr = the
-// tile's LUT_b rows (16 x 2^b fp16, row-major).
+// tile's LUT_b rows (16 x 2^b fp16, row-major); layouts in Cfg.
+template <int NBLK>
 __device__ __forceinline__ void build_tab_warp(const __half* lr, int b, uint32_t tab) {
   const int V = 1 << b, lane = threadIdx.x & 31;
-  for (int i = lane; i < V; i += 32) {  // (row pair g, run of 8 entries from v0)
-    const int g = i & 7, v0 = (i >> 3) * 8;
-    const uint4 lo = *reinterpret_cast<const uint4*>(lr + g * V + v0);
-    const uint4 hi = *reinterpret_cast<const uint4*>(lr + (g + 8) * V + v0);
-    const uint32_t l4[4] = {lo.x, lo.y, lo.z, lo.w}, h4[4] = {hi.x, hi.y, hi.z, hi.w};
+  if constexpr (Cfg<NBLK>::LANE) {
+    // each lane writes its own copy of rows g and g + 8, eight entries per pair of 16-byte loads
+    const int g = lane >> 2;
+    for (int v0 = 0; v0 < V; v0 += 8) {
+      const uint4 lo = *reinterpret_cast<const uint4*>(lr + g * V + v0);
+      const uint4 hi = *reinterpret_cast<const uint4*>(lr + (g + 8) * V + v0);
+      const uint32_t l4[4] = {lo.x, lo.y, lo.z, lo.w}, h4[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      sts32(tab + ((v0 + j) * 8 + g) * 4, prmt(l4[j >> 1], h4[j >> 1], (j & 1) ? 0x7632u : 0x5410u));
+      for (int j = 0; j < 8; ++j)
+        sts32(tab + (v0 + j) * 128 + lane * 4, prmt(l4[j >> 1], h4[j >> 1], (j & 1) ? 0x7632u : 0x5410u));
+    }
+  } else {
+    for (int i = lane; i < V; i += 32) {  // (row pair g, run of 8 entries from v0)
+      const int g = i & 7, v0 = (i >> 3) * 8;
+      const uint4 lo = *reinterpret_cast<const uint4*>(lr + g * V + v0);
+      const uint4 hi = *reinterpret_cast<const uint4*>(lr + (g + 8) * V + v0);
+      const uint32_t l4[4] = {lo.x, lo.y, lo.z, lo.w}, h4[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        sts32(tab + ((v0 + j) * 8 + g) * 4, prmt(l4[j >> 1], h4[j >> 1], (j & 1) ? 0x7632u : 0x5410u));
+    }
   }
   __syncwarp();
 }
@@ -303,20 +303,20 @@ __device__ __forceinline__ void dump_frag(const Dump& D, const uint32_t (&a)[4],
 struct WSrc {
   const char* p[kPlanes];  // plane tiles, or the fp16 tile in p[0]
   uint32_t lut3[2][4];     // 3 bits: register LUTs of rows g and g + 8
-  uint32_t tabg;           // 4..6 bits: the warp's LUT table + 4 g
+  uint32_t tabl;           // 4..6 bits: this lane's base in the warp's LUT table (Cfg)
 };
 
 // K loop of one warp over the units cb = u0, u0 + us, ... of its tile (unit
 // cb = columns cb * COLS ...).  Every warp of the CTA runs it for the same
 // item and passes the same K-block barriers; the ntok distinct token rows of
-// K-block kb are staged at the start of K-block kb - 1.  B: 16 (fp16), 3, or
-// 0 (4..6 bits, src.nb).  pre() runs once the first weight units are in flight.
-template <int KIND, int B, bool DUMP = false, class Pre>
+// K-block kb are staged at the start of K-block kb - 1.  B: 16 (fp16), 3, 4, 5
+// or 6.  pre() runs once the first weight units are in flight.
+template <int KIND, int B, int NBLK, bool DUMP = false, class Pre>
 __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, int u0, int us, uint32_t ring,
                                       uint32_t slab, const __half* act, const int* s_tok,
                                       float (&acc)[Geo::NTM][4], Pre&& pre, const Dump* dump = nullptr) {
   using G = Geo;
-  using U = Unit<KIND, B>;
+  using U = Unit<KIND, B, Cfg<NBLK>::RB>;
   constexpr int R = U::R;
   const int lane = threadIdx.x & 31;
   const int lkb = kblock_log2(NT), kbw = 1 << lkb, rs = kbw * 2;
@@ -411,12 +411,12 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
         }
       }
     } else {
-      // KIND_PG (3 bits): the unit's words of every plane in one 16-byte load
-      // per plane, chunks unrolled; KIND_PB (4..6 bits): each chunk reads its
-      // own word of every plane (no selects between chunk words)
+      // 3 bits: the unit's words of every plane in one 16-byte load per
+      // plane, chunks unrolled; 4..6 bits: each chunk reads its own word of
+      // every plane (no selects between chunk words)
       constexpr int W = KIND == KIND_PG ? 4 : 2;  // words (chunks) per lane and plane
       uint32_t w[B][W];
-      if constexpr (KIND == KIND_PG) {
+      if constexpr (B == 3) {
 #pragma unroll
         for (int p = 0; p < B; ++p) {
           const uint4 v = lds128(slot + (p * 32 + lane) * 16);
@@ -431,15 +431,15 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
         uint32_t wc[B];
 #pragma unroll
         for (int p = 0; p < B; ++p) {
-          if constexpr (W == 4) wc[p] = c == 0 ? w[p][0] : c == 1 ? w[p][1] : c == 2 ? w[p][2] : w[p][3];
-          else wc[p] = lds32(slot + (p * 32 + lane) * 8 + 4 * c);
+          if constexpr (B == 3) wc[p] = c == 0 ? w[p][0] : c == 1 ? w[p][1] : c == 2 ? w[p][2] : w[p][3];
+          else wc[p] = lds32(slot + (p * 32 + lane) * (4 * W) + 4 * c);
         }
         // decode the chunk's four steps first (independent chains), then the mma's
         uint32_t a[4][4];
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3, a[s]);
-          else decode_step_rt<B>(wc, s, src.tabg, a[s]);
+          else decode_step_rt<B, Cfg<NBLK>::TSHIFT>(wc, s, src.tabl, a[s]);
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
@@ -500,7 +500,7 @@ __device__ __forceinline__ void tile_store_y(const float (&acc)[Geo::NTM][4], in
 // warp: page-table addresses of its planes or fp16 tile, and for 3 bits the
 // register LUTs of the lane's rows.  Returns the tile's LUT_B rows, from which
 // a 4..6-bit warp builds its shared table (null otherwise).  B: 16, 3, 4, 5, 6.
-template <int B>
+template <int B, int NBLK>
 __device__ __forceinline__ const __half* tile_src(const DevLayer& L, int e, bool sh, int m, int t, int K,
                                                   uint32_t tab, WSrc& src) {
   const int lane = threadIdx.x & 31;
@@ -517,7 +517,7 @@ __device__ __forceinline__ const __half* tile_src(const DevLayer& L, int e, bool
   } else {
 #pragma unroll
     for (int p = 0; p < kPlanes; ++p) src.p[p] = p < B ? tile_addr(L, e, m, p, t) : nullptr;
-    src.tabg = tab + (lane >> 2) * 4;
+    src.tabl = tab + (Cfg<NBLK>::LANE ? lane : lane >> 2) * 4;
     return lut_rows(L, e, m, B, t * kTileRows);
   }
 }
@@ -538,7 +538,7 @@ struct ItemArgs {
 // tile tau), slice k of a tile taking every S-th unit from unit k.  Partial
 // and up sums go through shared memory to the first warp of each tile, which
 // adds them in warp order and stores.  B: 16 (fp16 page), 3, 4, 5 or 6.
-template <int B>
+template <int B, int NBLK>
 __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A, int NM, int S, int tau,
                                            uint32_t ring, uint32_t slab, uint32_t tab, const int* s_tok) {
   constexpr int kNT = Geo::NTM;
@@ -549,14 +549,14 @@ __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A,
   const int m = NM == 2 ? warp >> 1 : 2;     // and matrix
   float acc[kNT][4] = {};
   WSrc src;
-  const __half* lr = tile_src<B>(L, A.e, A.sh, m, t, A.K, tab, src);
+  const __half* lr = tile_src<B, NBLK>(L, A.e, A.sh, m, t, A.K, tab, src);
   if constexpr (B == 16) {
-    kloop<KIND_F16, 16>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
+    kloop<KIND_F16, 16, NBLK>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
   } else if constexpr (B == 3) {
-    kloop<KIND_PG, 3>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
+    kloop<KIND_PG, 3, NBLK>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc, [] {});
   } else {
-    kloop<KIND_PB, B>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act, s_tok, acc,
-                      [&] { build_tab_warp(lr, B, tab); });
+    kloop<Cfg<NBLK>::LANE ? KIND_PG : KIND_PB, B, NBLK>(src, A.K, A.NT, A.ntok, slice, S, ring, slab, A.act,
+                                                          s_tok, acc, [&] { build_tab_warp<NBLK>(lr, B, tab); });
   }
   if (NM == 1 && S == 1) {
     tile_store_y(acc, t, A.row0, A.ntok, A.ld, A.y);
@@ -603,9 +603,10 @@ __device__ __forceinline__ int down_split(int n, int K) {
 
 __device__ __forceinline__ bool is_tab(int b) { return b >= 4 && b <= 6; }
 
-template <bool SPLITK, bool FUSED>
-__global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniParams P) {
+template <bool SPLITK, bool FUSED, int NBLK>
+__global__ void __launch_bounds__(kCtaThreads, NBLK) ffn_cta_kernel(UniParams P) {
   using G = Geo;
+  using CF = Cfg<NBLK>;
   extern __shared__ __align__(128) unsigned char smem_uni[];
   __shared__ int s_base[kMaxExperts + 1];   // first input row of each group
   __shared__ int s_n[kMaxExperts + 1];      // tokens of each group
@@ -618,21 +619,101 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
   __shared__ int s_pos[kMaxTopK];
   __shared__ float s_w[kMaxTopK];
   __shared__ short s_perm[FUSED ? kFusedSlots : 1];  // fused: token of each sorted slot
+  __shared__ int s_last;
 
   const DevLayer& L = P.L;
   const int E = L.E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int* const q = L.sync;                             // claim counter, CTA exit counter, -, -, down items done
+  // sync header: [0] item claims, [1] CTAs out, [4] down items done, [5]
+  // route items claimed, [6] tokens routed, [8..8+T) route items done per token
+  int* const q = L.sync;
   int* const done0 = L.sync + kSyncHeader;           // [E+1][kSyncChunks] gate/up tiles done
   int* const done1 = done0 + (E + 1) * kSyncChunks;  // [E+1][kSyncChunks] down tiles done
 
   const int n_slots = P.T * L.K;  // routed slots (fused step)
   if constexpr (FUSED) {
-    // slot counts per expert from the routing result, then their prefix
+    // The router (sums in the order of pw_route.cuh, so idx and w equal the
+    // router kernel's bit for bit).  Items (token t, four units of (4
+    // experts, 1024-column slice)) are claimed from a counter, one unit per
+    // warp; the CTA that completes a token's last item adds its slice sums
+    // and selects its experts.  Every CTA then waits (bounded) until all
+    // tokens are routed: the items were claimed by running CTAs that wait on
+    // nothing, so the wait ends.
+    {
+      const int d8 = L.d / 8, ns = route_slices(L.d), nb = (E + kRouteEB - 1) / kRouteEB;
+      const int nunits = nb * ns, ngroups = (nunits + kCtaWarps - 1) / kCtaWarps;
+      const int total = P.T * ngroups;
+      int* const rclaim = q + 5;  // route items claimed
+      int* const rdone = q + 6;   // tokens routed
+      int* const tokcnt = q + 8;  // [T] items done per token
+      float* const lg = reinterpret_cast<float*>(smem_uni);  // [E] logits of a token being finished
+      for (;;) {
+        if (tid == 0) s_it = atomicAdd(rclaim, 1);
+        __syncthreads();
+        const int it = s_it;
+        if (it >= total) break;
+        const int t = it / ngroups, u = (it - t * ngroups) * kCtaWarps + warp;
+        if (u < nunits) {
+          const int e0 = (u / ns) * kRouteEB, sl = u % ns;
+          uint4 wv[kRouteEB][kRoutePieces];
+          route_load_w(P.wr, d8, E, e0, sl, lane, wv);
+          const uint4* x4 = reinterpret_cast<const uint4*>(P.x) + (size_t)t * d8;
+          float acc[kRouteEB] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < kRoutePieces; ++i) {
+            const int c = (sl * kRoutePieces + i) * 32 + lane;
+            if (c < d8) {
+              const uint4 xv = x4[c];
+#pragma unroll
+              for (int qq = 0; qq < kRouteEB; ++qq) acc[qq] += dot8(wv[qq][i], xv);
+            }
+          }
+#pragma unroll
+          for (int qq = 0; qq < kRouteEB; ++qq) {
+            const float v = route_warp_sum(acc[qq]);
+            if (lane == 0 && e0 + qq < E) P.rpart[((size_t)t * ns + sl) * E + e0 + qq] = v;
+          }
+        }
+        __syncthreads();  // this item's sums are written
+        if (tid == 0) {
+          __threadfence();
+          s_last = atomicAdd(tokcnt + t, 1) == ngroups - 1;
+        }
+        __syncthreads();
+        if (s_last) {
+          __threadfence();
+          for (int e = tid; e < E; e += kCtaThreads) {
+            float v = P.bias ? P.bias[e] : 0.f;
+            for (int sl = 0; sl < ns; ++sl) v += __ldcg(P.rpart + ((size_t)t * ns + sl) * E + e);
+            lg[e] = v;
+          }
+          __syncthreads();
+          if (warp == 0) route_select(lg, E, L.K, L.renorm, P.idx + (size_t)t * L.K, P.wk + (size_t)t * L.K, nullptr);
+          if (tid == 0) {  // lane 0 of warp 0 wrote this token's idx / w
+            tokcnt[t] = 0;  // back to zero for the next launch
+            __threadfence();
+            atomicAdd(rdone, 1);
+          }
+        }
+      }
+      if (tid == 0) {
+        long long spins = 0;
+        while (ld_acquire(rdone) < P.T) {
+          if (++spins > L.spin_limit) {
+            atomicExch(L.err, kErrTimeout);
+            break;
+          }
+          __nanosleep(100);
+        }
+      }
+      __syncthreads();
+    }
+    // slot counts per expert from the routing result (written in this launch
+    // by other CTAs: read through L2), then their prefix
     for (int g = tid; g <= E; g += kCtaThreads) s_n[g] = 0;
     __syncthreads();
     for (int i = tid; i < n_slots; i += kCtaThreads) {
-      const int e = P.idx[i];
+      const int e = __ldcg(P.idx + i);
       if ((unsigned)e < (unsigned)E) atomicAdd(&s_n[e], 1);
       else atomicExch(L.err, kErrRouting);  // not a routing result: the slot is dropped
     }
@@ -664,7 +745,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
 #pragma unroll
       for (int b = 0; b < kBatches; ++b) {
         const int j = b * 32 + lane;
-        ev[b] = j < n_slots ? min(max(P.idx[j], 0), E - 1) : -1 - lane;
+        ev[b] = j < n_slots ? min(max(__ldcg(P.idx + j), 0), E - 1) : -1 - lane;
       }
       for (int g = lane; g < E; g += 32) s_pref[0][g] = s_base[g];
       __syncwarp();
@@ -810,8 +891,8 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     }
   }
   const uint32_t slab = smem_u32(smem_uni);
-  const uint32_t tab = slab + 2 * G::HALF + warp * kTabW;
-  const uint32_t ring = slab + 2 * G::HALF + kCtaWarps * kTabW + warp * G::RB;
+  const uint32_t tab = slab + 2 * G::HALF + warp * CF::TABW;
+  const uint32_t ring = slab + 2 * G::HALF + kCtaWarps * CF::TABW + warp * CF::RB;
 
   for (;;) {
     if (tid == 0) s_it = atomicAdd(q, 1);
@@ -878,11 +959,11 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     const int tau = blk * per_item;
     const int NM = phase == 0 ? 2 : 1;
     switch (b) {
-      case 16: block_item<16>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
-      case 3: block_item<3>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
-      case 4: block_item<4>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
-      case 5: block_item<5>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
-      default: block_item<6>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      case 16: block_item<16, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      case 3: block_item<3, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      case 4: block_item<4, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      case 5: block_item<5, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      default: block_item<6, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
     }
     __syncthreads();  // every tile of the item is stored
     if (tid == 0) {
@@ -918,7 +999,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     for (int t = blockIdx.x; t < P.T; t += gridDim.x) {
       for (int k = warp; k < K; k += kCtaWarps) {
         // sorted slot of (t, k): the one slot of token t in expert e's bucket
-        const int flat = t * K + k, e = min(max(P.idx[flat], 0), E - 1);
+        const int flat = t * K + k, e = min(max(__ldcg(P.idx + flat), 0), E - 1);
         const int lo = s_base[e], hi = min(lo + s_n[e], kFusedSlots);
         int pos = lo;
         for (int p0 = lo; p0 < hi; p0 += 32) {
@@ -931,7 +1012,7 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
         }
         if (lane == 0) {
           s_pos[k] = pos;
-          s_w[k] = P.wk[flat];
+          s_w[k] = __ldcg(P.wk + flat);
         }
       }
       __syncthreads();
@@ -966,7 +1047,11 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
     __threadfence();
     if (atomicAdd(q + 1, 1) == (int)gridDim.x - 1) {  // last CTA out: no claims remain
       atomicExch(q, 0);
-      if (FUSED) atomicExch(q + 4, 0);
+      if (FUSED) {
+        atomicExch(q + 4, 0);
+        atomicExch(q + 5, 0);
+        atomicExch(q + 6, 0);
+      }
       atomicExch(q + 1, 0);
     }
   }
@@ -979,22 +1064,23 @@ __global__ void __launch_bounds__(kCtaThreads, Geo::BLOCKS) ffn_cta_kernel(UniPa
 // item of the FFN kernel) with its A fragments written to out[rows][cols]
 // instead of feeding the mma.
 // ---------------------------------------------------------------------------
-template <int B>
+template <int B, int NBLK>
 __device__ __forceinline__ void dump_tile(const DevLayer& L, int e, int m, int t, int C, uint32_t ring,
                                           uint32_t slab, uint32_t tab, const int* s_tok, const Dump& D) {
   float acc[Geo::NTM][4] = {};
   WSrc src;
-  const __half* lr = tile_src<B>(L, e, false, m, t, C, tab, src);
+  const __half* lr = tile_src<B, NBLK>(L, e, false, m, t, C, tab, src);
   if constexpr (B == 16) {
-    kloop<KIND_F16, 16, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [] {}, &D);
+    kloop<KIND_F16, 16, NBLK, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [] {}, &D);
   } else if constexpr (B == 3) {
-    kloop<KIND_PG, 3, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [] {}, &D);
+    kloop<KIND_PG, 3, NBLK, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [] {}, &D);
   } else {
-    kloop<KIND_PB, B, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc, [&] { build_tab_warp(lr, B, tab); },
-                            &D);
+    kloop<Cfg<NBLK>::LANE ? KIND_PG : KIND_PB, B, NBLK, true>(src, C, 1, 0, 0, 1, ring, slab, D.out, s_tok, acc,
+                                  [&] { build_tab_warp<NBLK>(lr, B, tab); }, &D);
   }
 }
 
+template <int NBLK>
 __global__ void __launch_bounds__(kCtaThreads) decode_dump_kernel(DevLayer L, int e, int m, __half* out) {
   extern __shared__ __align__(128) unsigned char smem_dump[];
   __shared__ int s_tok[Geo::TOK];
@@ -1004,39 +1090,57 @@ __global__ void __launch_bounds__(kCtaThreads) decode_dump_kernel(DevLayer L, in
   const int t = min((int)blockIdx.x * kCtaWarps + warp, ntile - 1);  // spare warps repeat the last tile unstored
   const Dump D{out, C, t * kTileRows, (int)blockIdx.x * kCtaWarps + warp < ntile};
   const uint32_t slab = smem_u32(smem_dump);
-  const uint32_t tab = slab + 2 * Geo::HALF + warp * kTabW;
-  const uint32_t ring = slab + 2 * Geo::HALF + kCtaWarps * kTabW + warp * Geo::RB;
+  const uint32_t tab = slab + 2 * Geo::HALF + warp * Cfg<NBLK>::TABW;
+  const uint32_t ring = slab + 2 * Geo::HALF + kCtaWarps * Cfg<NBLK>::TABW + warp * Cfg<NBLK>::RB;
   switch (L.bits[e]) {
-    case 16: dump_tile<16>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
-    case 3: dump_tile<3>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
-    case 4: dump_tile<4>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
-    case 5: dump_tile<5>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
-    case 6: dump_tile<6>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 16: dump_tile<16, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 3: dump_tile<3, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 4: dump_tile<4, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 5: dump_tile<5, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
+    case 6: dump_tile<6, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
     default:
       if (threadIdx.x == 0) atomicExch(L.err, kErrBits);
   }
 }
 
-cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {
+template <int NBLK>
+static cudaError_t launch_decode_dump_cfg(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {
   const int R = m < 2 ? L.f : L.d;
-  cudaError_t err = ensure_smem((const void*)decode_dump_kernel, Geo::SMEM);
+  cudaError_t err = ensure_smem((const void*)decode_dump_kernel<NBLK>, Cfg<NBLK>::SMEM);
   if (err != cudaSuccess) return err;
   const int ntile = R / kTileRows;
-  decode_dump_kernel<<<(ntile + kCtaWarps - 1) / kCtaWarps, kCtaThreads, Geo::SMEM, s>>>(L, e, m, out);
+  decode_dump_kernel<NBLK><<<(ntile + kCtaWarps - 1) / kCtaWarps, kCtaThreads, Cfg<NBLK>::SMEM, s>>>(L, e, m, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, bool lane_tables, __half* out, cudaStream_t s) {
+  return lane_tables ? launch_decode_dump_cfg<2>(L, e, m, out, s) : launch_decode_dump_cfg<3>(L, e, m, out, s);
+}
+
+// The configuration a layer's decode launches take (Cfg): per-lane LUT tables
+// for wide experts (ffn >= 4096), where 4..6-bit lookups dominate the launch,
+// otherwise three CTAs per SM.  It depends on the shape only, so every call
+// and every CUDA graph of a layer computes each item the same way.
+int nblk_for(const DevLayer& L) { return L.f >= 4096 ? 2 : 3; }
+
+template <bool FUSED, int NBLK>
+static cudaError_t launch_cta_cfg(const UniParams& P, int T, cudaStream_t s) {
+  // The split paths depend on the batch size only, so a routed call, a shared
+  // call and the combined call compute every item the same way.
+  const bool splitk = T <= 16;
+  const void* fn = splitk ? (const void*)ffn_cta_kernel<true, FUSED, NBLK>
+                          : (const void*)ffn_cta_kernel<false, FUSED, NBLK>;
+  cudaError_t e;
+  if ((e = ensure_smem(fn, Cfg<NBLK>::SMEM)) != cudaSuccess) return e;
+  const int grid = sm_count() * NBLK;
+  if (splitk) ffn_cta_kernel<true, FUSED, NBLK><<<grid, kCtaThreads, Cfg<NBLK>::SMEM, s>>>(P);
+  else ffn_cta_kernel<false, FUSED, NBLK><<<grid, kCtaThreads, Cfg<NBLK>::SMEM, s>>>(P);
   return cudaGetLastError();
 }
 
 template <bool FUSED>
 static cudaError_t launch_cta(const UniParams& P, int T, cudaStream_t s) {
-  // The split paths depend on the batch size only, so a routed call, a shared
-  // call and the combined call compute every item the same way.
-  const bool splitk = T <= 16;
-  const void* fn = splitk ? (const void*)ffn_cta_kernel<true, FUSED> : (const void*)ffn_cta_kernel<false, FUSED>;
-  cudaError_t e;
-  if ((e = ensure_smem(fn, Geo::SMEM)) != cudaSuccess) return e;
-  if (splitk) ffn_cta_kernel<true, FUSED><<<sm_count() * Geo::BLOCKS, kCtaThreads, Geo::SMEM, s>>>(P);
-  else ffn_cta_kernel<false, FUSED><<<sm_count() * Geo::BLOCKS, kCtaThreads, Geo::SMEM, s>>>(P);
-  return cudaGetLastError();
+  return nblk_for(P.L) == 2 ? launch_cta_cfg<FUSED, 2>(P, T, s) : launch_cta_cfg<FUSED, 3>(P, T, s);
 }
 
 cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
@@ -1058,9 +1162,11 @@ cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm,
   return launch_cta<false>(P, T, s);
 }
 
-cudaError_t launch_layer_fused(const DevLayer& L, const __half* x, const int* idx, const float* w, int T, __half* h,
-                               __half* hs, float* y_perm, float* ys, __half* y, int* offsets_out, cudaStream_t s) {
-  if (T > kSyncChunks * 16 || T * L.K > kFusedSlots) return cudaErrorInvalidValue;
+cudaError_t launch_layer_fused(const DevLayer& L, const __half* x, const __half* wr, const float* bias, int* idx,
+                               float* w, float* rpart, int T, __half* h, __half* hs, float* y_perm, float* ys,
+                               __half* y, int* offsets_out, cudaStream_t s) {
+  static_assert(8 + kFusedMaxTokens <= kSyncHeader, "per-token router counters must fit the sync header");
+  if (T < 1 || T > kFusedMaxTokens || T * L.K > kFusedSlots) return cudaErrorInvalidValue;
   UniParams P{};
   P.L = L;
   P.x = x;
@@ -1071,6 +1177,9 @@ cudaError_t launch_layer_fused(const DevLayer& L, const __half* x, const int* id
   P.hs = L.fs ? hs : nullptr;
   P.y = y_perm;
   P.ys = L.fs ? ys : nullptr;
+  P.wr = wr;
+  P.bias = bias;
+  P.rpart = rpart;
   P.idx = idx;
   P.wk = w;
   P.yout = y;

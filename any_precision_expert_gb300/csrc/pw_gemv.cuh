@@ -53,6 +53,44 @@ __device__ __forceinline__ void decode_step_prmt3(const uint32_t (&w)[3], const 
   a[3] = prmt(lo, hi, 0x7362u);
 }
 
+// 16-bit shared load, zero-extended into a 32-bit register.
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Decode mma step s of one chunk of B-bit codes (B = 4..6) into the A
+// fragment through a LUT table in shared memory: the entry of code v for this
+// lane is at tabl + (v << TSHIFT) and holds LUT[row g][v] in its low and
+// LUT[row g+8][v] in its high half, g and g + 8 being the lane's two fragment
+// rows (the tables' layouts are the kernels').
+// Plane p keeps code bit B-1-p of weight (h, s, byte
+// k) at bit 8k + 4h + s + 5 - p (mod 32): masking one bit per byte and
+// rotating right by 4h + s + 6 - B leaves the codes of R[h] in the low B
+// bits of its bytes.  Each lookup reads the one 16-bit half it needs (row g:
+// +0, row g+8: +2), zero-extended, so the two columns of a fragment register
+// join with an integer multiply-add (the FMA pipe, beside the busy ALU).
+template <int B, int TSHIFT>
+__device__ __forceinline__ void decode_step_rt(const uint32_t (&w)[B], const int s, uint32_t tabl, uint32_t (&a)[4]) {
+  uint32_t R[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int p = 0; p < B; ++p) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
+    R[h] = rotr(m, 4 * h + s + 6 - B);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // k = 2 * rowsel + colhalf
+    const uint32_t half = (k >> 1) * 2;
+    const uint32_t e0 = lds16(tabl + half + (prmt(R[0], 0u, 0x4440u | (uint32_t)k) << TSHIFT));
+    const uint32_t e1 = lds16(tabl + half + (prmt(R[1], 0u, 0x4440u | (uint32_t)k) << TSHIFT));
+    const int reg = (k == 0) ? 0 : (k == 1) ? 2 : (k == 2) ? 1 : 3;
+    a[reg] = e1 * 65536u + e0;
+  }
+}
+
 __device__ __forceinline__ void load_lut3(const __half* row, uint32_t (&r)[4]) {
   const uint4 v = *reinterpret_cast<const uint4*>(row);
   r[0] = prmt(v.x, v.y, 0x6420u);

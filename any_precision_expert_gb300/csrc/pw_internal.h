@@ -24,6 +24,19 @@ constexpr int kErrRouting = 2;       // an expert index outside [0, E) in a rout
 constexpr int kErrBits = 3;          // a bitwidth word outside {3, 4, 5, 6, 16}
 constexpr int kErrOffsets = 4;       // slot offsets not monotone in [0, T*K], or a slot index out of range
 
+#ifdef __CUDACC__
+#define PW_HD __host__ __device__
+#else
+#define PW_HD
+#endif
+
+// 1024-column slices of d in the router's sums (pw_route.cuh).
+PW_HD inline int route_slices(int d) { return (d / 8 + 127) / 128; }
+
+// Tokens of a fused layer step (the router runs inside its launch; per-token
+// counters live in the sync header).
+constexpr int kFusedMaxTokens = 16;
+
 // Words of a layer's sync area: header, then gate/up and down tile counters
 // for every (group, chunk), a group being a routed expert or the shared FFN.
 inline size_t sync_words(int E) { return kSyncHeader + 2 * (size_t)(E + 1) * kSyncChunks; }
@@ -81,12 +94,16 @@ cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* o
 // non-null, the shared FFN.
 cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm, const int* offsets, int T,
                        int bit_mask, int max_tokens, __half* h, __half* hs, float* y, float* ys, cudaStream_t s);
-// Fused decode step for T tokens after the router: per-expert offsets from
-// idx, the expert FFN of every group (routed rows staged straight from x)
-// and the shared FFN, then the weighted combine into y.  Every expert must be
-// decode-sized (T at most the decode token thresholds).
-cudaError_t launch_layer_fused(const DevLayer& L, const __half* x, const int* idx, const float* w, int T, __half* h,
-                               __half* hs, float* y_perm, float* ys, __half* y, int* offsets_out, cudaStream_t s);
+// Fused decode step for T tokens (at most kFusedMaxTokens): the router,
+// per-expert offsets from its idx, the expert FFN of every group (routed rows
+// staged straight from x) and the shared FFN, then the weighted combine into
+// y.  Every expert must be decode-sized (T at most the decode token
+// thresholds).
+// The router runs in the same launch: idx / w are written, rpart holds
+// [T][route_slices(d)][E] floats of its partial sums.
+cudaError_t launch_layer_fused(const DevLayer& L, const __half* x, const __half* wr, const float* bias, int* idx,
+                               float* w, float* rpart, int T, __half* h, __half* hs, float* y_perm, float* ys,
+                               __half* y, int* offsets_out, cudaStream_t s);
 int decode_max_tokens(int ffn, int T);
 int decode_max_tokens_shared();
 cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
@@ -98,9 +115,12 @@ cudaError_t launch_combine(const DevLayer& L, const float* y_perm, const int* in
                            const float* w, int T, const float* y_shared, __half* y, cudaStream_t s);
 cudaError_t launch_debug_dequant(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
 // The decoded weights of expert e's matrix m as the decode kernel's K loop
-// (launch_decode_dump) or the prefill kernel's dequant warps
-// (launch_prefill_dump) produce them.
-cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
+// (launch_decode_dump, in either LUT-table configuration) or the prefill
+// kernel's dequant warps (launch_prefill_dump) produce them.
+cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, bool lane_tables, __half* out, cudaStream_t s);
+// Decode-kernel configuration of a layer: 2 (per-lane LUT tables, two CTAs per
+// SM) or 3 (row-pair tables, three CTAs per SM).
+int nblk_for(const DevLayer& L);
 cudaError_t launch_prefill_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
 
 // Host-side checks shared by the expert-FFN entry points: validates the

@@ -12,6 +12,7 @@
 #include <utility>
 
 #include "pw_device.cuh"
+#include "pw_route.cuh"
 
 namespace pw {
 
@@ -52,20 +53,6 @@ cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s) {
 
 constexpr int kRouteThreads = 512;
 
-__device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
-  const __half2* ha = reinterpret_cast<const __half2*>(&a);
-  const __half2* hb = reinterpret_cast<const __half2*>(&b);
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 fa = __half22float2(ha[i]);
-    const float2 fb = __half22float2(hb[i]);
-    acc = fmaf(fa.x, fb.x, acc);
-    acc = fmaf(fa.y, fb.y, acc);
-  }
-  return acc;
-}
-
 template <int kRouteTok>  // tokens per CTA
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const __half* __restrict__ x,
                                                               const __half* __restrict__ wr,
@@ -84,51 +71,40 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const 
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Work unit = (four experts, one 1024-column slice of d): a lane loads its
-  // four 16-byte pieces of the four W_r rows at once (one memory round trip
-  // per unit) and the warps share the units.  Slice sums are added in slice
-  // order afterwards, so the logits do not depend on the schedule.
-  constexpr int kEB = 4, kPieces = 4;
-  const int ns = (d8 + 32 * kPieces - 1) / (32 * kPieces);
-  const int nb = (E + kEB - 1) / kEB;
+  // Work unit = (four experts, one 1024-column slice of d), order of the sums
+  // in pw_route.cuh: a lane loads its four 16-byte pieces of the four W_r rows
+  // at once (one memory round trip per unit) and the warps share the units.
+  const int ns = route_slices(d);
+  const int nb = (E + kRouteEB - 1) / kRouteEB;
   float* part = logit + kRouteTok * E;  // [ns][kRouteTok][E]
   for (int u = warp; u < nb * ns; u += kRouteThreads / 32) {
-    const int e0 = (u / ns) * kEB, sl = u % ns;
-    uint4 wv[kEB][kPieces];
+    const int e0 = (u / ns) * kRouteEB, sl = u % ns;
+    uint4 wv[kRouteEB][kRoutePieces];
+    route_load_w(wr, d8, E, e0, sl, lane, wv);
+    float acc[kRouteEB][kRouteTok];
 #pragma unroll
-    for (int q = 0; q < kEB; ++q)
-#pragma unroll
-      for (int i = 0; i < kPieces; ++i) {
-        const int c = (sl * kPieces + i) * 32 + lane;
-        wv[q][i] = (e0 + q < E && c < d8) ? __ldg(reinterpret_cast<const uint4*>(wr) + (size_t)(e0 + q) * d8 + c)
-                                          : make_uint4(0, 0, 0, 0);
-      }
-    float acc[kEB][kRouteTok];
-#pragma unroll
-    for (int q = 0; q < kEB; ++q)
+    for (int q = 0; q < kRouteEB; ++q)
 #pragma unroll
       for (int t = 0; t < kRouteTok; ++t) acc[q][t] = 0.f;
 #pragma unroll
-    for (int i = 0; i < kPieces; ++i) {
-      const int c = (sl * kPieces + i) * 32 + lane;
+    for (int i = 0; i < kRoutePieces; ++i) {
+      const int c = (sl * kRoutePieces + i) * 32 + lane;
       if (c < d8) {
 #pragma unroll
         for (int t = 0; t < kRouteTok; ++t) {
           if (t < nt) {
             const uint4 xv = xs[t * d8 + c];
 #pragma unroll
-            for (int q = 0; q < kEB; ++q) acc[q][t] += dot8(wv[q][i], xv);
+            for (int q = 0; q < kRouteEB; ++q) acc[q][t] += dot8(wv[q][i], xv);
           }
         }
       }
     }
 #pragma unroll
-    for (int q = 0; q < kEB; ++q)
+    for (int q = 0; q < kRouteEB; ++q)
 #pragma unroll
       for (int t = 0; t < kRouteTok; ++t) {
-        float v = acc[q][t];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        const float v = route_warp_sum(acc[q][t]);
         if (lane == 0 && t < nt && e0 + q < E) part[((size_t)sl * kRouteTok + t) * E + e0 + q] = v;
       }
   }
@@ -143,67 +119,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(DevLayer L, const 
 
   if (warp < nt) {
     const int t = t0 + warp;
-    const float* lg = logit + warp * E;
-    constexpr int kPer = kMaxExperts / 32;
-    float v[kPer];
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < E ? lg[e] : -INFINITY;
-      m = fmaxf(m, v[i]);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) z += (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-
-    unsigned taken = 0;  // bit i: expert lane + 32 i already chosen
-    float wsel[kMaxTopK];
-    int esel[kMaxTopK];
-    float wsum = 0.f;
-    for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-          bv = v[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      esel[k] = be;
-      wsel[k] = expf(bv - m) / z;
-      wsum += wsel[k];
-    }
-    if (lane == 0) {
-      for (int k = 0; k < K; ++k) {
-        idx[(size_t)t * K + k] = esel[k];
-        wout[(size_t)t * K + k] = L.renorm ? wsel[k] / wsum : wsel[k];
-        if (counts) atomicAdd(counts + esel[k], 1);
-      }
-    }
+    route_select(logit + warp * E, E, K, L.renorm, idx + (size_t)t * K, wout + (size_t)t * K, counts);
   }
 }
 
 template <int TPC>
 static cudaError_t launch_route_tpc(const DevLayer& L, const __half* x, const __half* wr, const float* bias, int T,
                                    int* idx, float* w, int* counts, cudaStream_t s) {
-  const int ns = (L.d / 8 + 127) / 128;  // 1024-column slices of d
+  const int ns = route_slices(L.d);
   const size_t smem = (size_t)TPC * L.d * sizeof(__half) + (size_t)(1 + ns) * TPC * L.E * sizeof(float);
   cudaError_t e = ensure_smem((const void*)route_kernel<TPC>, smem);
   if (e != cudaSuccess) return e;

@@ -35,7 +35,7 @@ constexpr int PF_BM = 128, PF_BN = 256, PF_BK = 64;
 constexpr uint32_t PF_A_BYTES = PF_BM * PF_BK * 2;  // 16 KB
 constexpr uint32_t PF_B_BYTES = PF_BN * PF_BK * 2;  // 32 KB
 constexpr int PF_BWARPS = 1;  // the TMA producer warp
-constexpr uint32_t PF_TAB_BYTES = 64 * 256;          // LUT table of one (matrix, 64-row slab), b <= 6
+constexpr uint32_t PF_TAB_BYTES = 64 * 128;          // LUT table of one (matrix, 64-row slab), b <= 6
 
 template <int NM>
 struct Pf {
@@ -73,11 +73,14 @@ __device__ __forceinline__ PfTile pf_tile(int t, const int* s_pref, const int* s
     const int mid = (lo + hi) >> 1;
     if (s_pref[mid] <= t) lo = mid; else hi = mid;
   }
+  // the token tiles of one 128-row weight tile are consecutive, so they run
+  // at the same time on neighbouring CTAs and read its planes from DRAM once
+  const int ntiles = (s_off[lo + 1] - s_off[lo] + PF_BN - 1) / PF_BN;
   PfTile T;
   T.e = lo;
   const int local = t - s_pref[lo];
-  T.mt = local % mtiles;
-  T.nt = local / mtiles;
+  T.nt = local % ntiles;
+  T.mt = local / ntiles;
   T.slot0 = s_off[lo] + T.nt * PF_BN;
   T.nvalid = min(PF_BN, s_off[lo + 1] - T.slot0);
   return T;
@@ -90,9 +93,9 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int c16) {
 // Decode one 64-column stage of this lane's two rows (g, g+8 of its 16-row
 // tile) into out[s][q]: q = 0 row g cols 16s..+7, 1 row g cols 16s+8..+15,
 // 2 row g+8 cols 16s..+7, 3 row g+8 cols 16s+8..+15 (fp16 x 8 each).
+// tabl: this lane's entries in the slab's LUT table (pf_build_tab_half).
 template <int B>
-__device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint32_t tab, uint32_t lb0,
-                                                 uint32_t lb1, uint4 (&out)[4][4]) {
+__device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint32_t tabl, uint4 (&out)[4][4]) {
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     uint32_t a[4][4];
@@ -101,7 +104,7 @@ __device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint
       uint32_t wt[B];
 #pragma unroll
       for (int p = 0; p < B; ++p) wt[p] = w[t][p];
-      decode_step_lut<B>(wt, s, tab, lb0, lb1, a[t]);
+      decode_step_rt<B, 7>(wt, s, tabl, a[t]);
     }
     out[s][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
     out[s][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
@@ -151,19 +154,19 @@ __device__ __forceinline__ void pf_load_lut3(const DevLayer& L, int e, int mm, i
   load_lut3(lut_rows(L, e, mm, 3, r1), lut3[1]);
 }
 
-// Warp `par` of a pair writes its half (row set rho = par) of the per-lane
-// LUT table of one 64-row slab starting at row slab0: entry (v, rho, lane lx)
-// at word v * 64 + rho * 32 + lx holds LUT_b of row slab0 + 16 (lx / 8) +
-// lx % 8 + 8 rho in both halves.
+// Warp `par` of a pair writes its half (codes v with v / 2^(b-1) = par) of
+// the per-lane LUT table of one 64-row slab starting at row slab0: entry (v,
+// lane lx) at word v * 32 + lx holds LUT_b[row][v] | LUT_b[row + 8][v] << 16
+// for row = slab0 + 16 (lx / 8) + lx % 8, the lane's two rows, so a warp's 32
+// lookups fall on 32 different banks (rows past R repeat the last row).
 __device__ __forceinline__ void pf_build_tab_half(const DevLayer& L, int e, int mm, int b, int slab0, int R,
                                                   int par, uint32_t* tabg) {
-  const int lx = threadIdx.x & 31, rho = par;
-  const int row = min(slab0 + (lx >> 3) * 16 + (lx & 7) + 8 * rho, R - 1);
-  const __half* lr = lut_rows(L, e, mm, b, row);
-  for (int v = 0; v < (1 << b); ++v) {
-    const uint32_t val = __half_as_ushort(lr[v]);
-    tabg[v * 64 + rho * 32 + lx] = val | (val << 16);
-  }
+  const int lx = threadIdx.x & 31, V = 1 << b;
+  const int row = slab0 + (lx >> 3) * 16 + (lx & 7);
+  const __half* l0 = lut_rows(L, e, mm, b, min(row, R - 1));
+  const __half* l1 = lut_rows(L, e, mm, b, min(row + 8, R - 1));
+  for (int v = par * (V >> 1); v < (par + 1) * (V >> 1); ++v)
+    tabg[v * 32 + lx] = (uint32_t)__half_as_ushort(l0[v]) | ((uint32_t)__half_as_ushort(l1[v]) << 16);
 }
 
 // fp16 page: stage kb of this lane's rows, gathered from the four fragment
@@ -302,7 +305,6 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
     const int tis = lane >> 3, g = lane & 7;
     const uint32_t tab = tabs + (uint32_t)(mi * 2 + slab) * PF_TAB_BYTES;
     uint32_t* tabg = reinterpret_cast<uint32_t*>(gbase + (tab - base));
-    const uint32_t lb0 = lane * 4, lb1 = 128 + lane * 4;
     uint32_t it = 0, tc = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
           if (kb + 2 < nkb) pf_load_planes<BB>(pb, kb + 2, nkb, g, wn);
           uint4 out[4][4];
           if constexpr (BB == 3) pf_decode_planes3(w, lut3, out);
-          else pf_decode_planes<BB>(w, tab, lb0, lb1, out);
+          else pf_decode_planes<BB>(w, tab + lane * 4, out);
           ok = store_stage(kb, out);
         }
       };
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, in
       pf_load_planes<BB>(pb, kb, nkb, g, w);
       uint4 o[4][4];
       if constexpr (BB == 3) pf_decode_planes3(w, lut3, o);
-      else pf_decode_planes<BB>(w, tab, lane * 4, 128 + lane * 4, o);
+      else pf_decode_planes<BB>(w, tab + lane * 4, o);
       put(kb, o);
     }
   };

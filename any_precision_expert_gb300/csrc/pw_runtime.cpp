@@ -11,12 +11,17 @@
 //  * lowering only rewrites the device bitwidth word (stream ordered) and moves
 //    the freed blocks to a reclaim queue guarded by a CUDA event (the safe
 //    boundary); raising re-maps blocks that are still intact.
+#include <cuda.h>  // driver API types of the virtual-memory calls (looked up at run time)
+#include <sys/mman.h>
+#include <unistd.h>
+
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <map>
 #include <memory>
+#include <mutex>
 #include <set>
 #include <vector>
 
@@ -89,6 +94,36 @@ pw_status dev_sync(cudaStream_t s) {
   return PW_OK;
 }
 
+// CUDA virtual memory management (driver API), looked up once.  The library
+// reserves virtual address ranges and maps the caller's physical pages into
+// them; it never creates or releases physical memory.
+struct VmmApi {
+  CUresult (*reserve)(CUdeviceptr*, size_t, size_t, CUdeviceptr, unsigned long long) = nullptr;
+  CUresult (*release_va)(CUdeviceptr, size_t) = nullptr;
+  CUresult (*map)(CUdeviceptr, size_t, size_t, CUmemGenericAllocationHandle, unsigned long long) = nullptr;
+  CUresult (*unmap)(CUdeviceptr, size_t) = nullptr;
+  CUresult (*set_access)(CUdeviceptr, size_t, const CUmemAccessDesc*, size_t) = nullptr;
+  bool ok = false;
+};
+
+const VmmApi& vmm_api() {
+  static VmmApi api;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    auto get = [](const char* name, void** fn) {
+      cudaDriverEntryPointQueryResult q;
+      return cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+             q == cudaDriverEntryPointSuccess && *fn != nullptr;
+    };
+    api.ok = get("cuMemAddressReserve", reinterpret_cast<void**>(&api.reserve)) &&
+             get("cuMemAddressFree", reinterpret_cast<void**>(&api.release_va)) &&
+             get("cuMemMap", reinterpret_cast<void**>(&api.map)) &&
+             get("cuMemUnmap", reinterpret_cast<void**>(&api.unmap)) &&
+             get("cuMemSetAccess", reinterpret_cast<void**>(&api.set_access));
+  });
+  return api;
+}
+
 // The safe boundary of one bitwidth change.
 struct Event {
   cudaEvent_t ev = nullptr;
@@ -122,6 +157,7 @@ enum BlockState { B_NONE = 0, B_MAPPED = 1, B_RECLAIM = 2 };
 
 struct Block {
   BlockState st = B_NONE;
+  char* va = nullptr;             // virtual-memory pools: the block's fixed address range
   std::vector<int> pages;         // physical page ids, indexed by virtual page
   std::shared_ptr<Event> ev;      // set while reclaimable
   std::shared_ptr<Event> ready;   // set while an asynchronous upload into the block may be in flight
@@ -133,6 +169,13 @@ struct Block {
 struct pw_pool_s {
   char* base = nullptr;
   size_t bytes = 0, page_bytes = 0, npages = 0;
+  // virtual-memory pools: page p is the caller's physical allocation
+  // handles[p], visible only where it is mapped (host-sim: a memfd page)
+  bool vmm = false;
+  int device = 0;
+  std::vector<unsigned long long> handles;
+  int sim_fd = -1;
+  uint64_t n_map = 0, n_unmap = 0;
   std::set<int> free_pages;                 // ordered: paged blocks take the lowest ids
   std::vector<uint8_t> kind;                // 0 free, 1 paged, 2 resident
   std::map<uint64_t, Block*> reclaim;       // oldest first
@@ -141,6 +184,52 @@ struct pw_pool_s {
   int n_layers = 0;
 
   char* page_addr(int p) const { return base + (size_t)p * page_bytes; }
+
+  // Map physical page p at va (one page, read/write for the pool's device).
+  pw_status vmm_map(char* va, int p) {
+    if (g_sim) {
+      if (mmap(va, page_bytes, PROT_READ | PROT_WRITE, MAP_SHARED | MAP_FIXED, sim_fd, (off_t)p * page_bytes) ==
+          MAP_FAILED)
+        return PW_ERR_UNSUPPORTED;
+    } else {
+      const VmmApi& a = vmm_api();
+      const CUdeviceptr d = reinterpret_cast<CUdeviceptr>(va);
+      if (a.map(d, page_bytes, 0, handles[p], 0) != CUDA_SUCCESS) return PW_ERR_CUDA;
+      CUmemAccessDesc acc{};
+      acc.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+      acc.location.id = device;
+      acc.flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
+      if (a.set_access(d, page_bytes, &acc, 1) != CUDA_SUCCESS) {
+        a.unmap(d, page_bytes);
+        return PW_ERR_CUDA;
+      }
+    }
+    ++n_map;
+    return PW_OK;
+  }
+  void vmm_unmap(char* va) {
+    if (g_sim)
+      mmap(va, page_bytes, PROT_NONE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_FIXED | MAP_NORESERVE, -1, 0);
+    else
+      vmm_api().unmap(reinterpret_cast<CUdeviceptr>(va), page_bytes);
+    ++n_unmap;
+  }
+  // Reserve / free a virtual range of n pages (no physical memory).
+  char* vmm_reserve(size_t n) {
+    const size_t len = n * page_bytes;
+    if (g_sim) {
+      void* p = mmap(nullptr, len, PROT_NONE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
+      return p == MAP_FAILED ? nullptr : static_cast<char*>(p);
+    }
+    CUdeviceptr d = 0;
+    if (vmm_api().reserve(&d, len, page_bytes, 0, 0) != CUDA_SUCCESS) return nullptr;
+    return reinterpret_cast<char*>(d);
+  }
+  void vmm_free(char* va, size_t n) {
+    if (!va) return;
+    if (g_sim) munmap(va, n * page_bytes);
+    else vmm_api().release_va(reinterpret_cast<CUdeviceptr>(va), n * page_bytes);
+  }
 
   void to_reclaim(Block& b, std::shared_ptr<Event> ev) {
     b.st = B_RECLAIM;
@@ -164,6 +253,10 @@ struct pw_pool_s {
     } else if (b.st == B_MAPPED) {
       mapped_pages -= b.pages.size();
     }
+    // virtual-memory pools unmap here, the only place a block gives up its
+    // pages: after its safe boundary (reuse) or a synchronize (reload, destroy)
+    if (vmm && b.st != B_NONE)
+      for (size_t v = 0; v < b.pages.size(); ++v) vmm_unmap(b.va + v * page_bytes);
     for (int p : b.pages) {
       kind[p] = 0;
       free_pages.insert(p);
@@ -255,6 +348,8 @@ struct pw_layer_s {
   int res_first = -1;
   size_t res_npages = 0;
   char* res_base = nullptr;
+  char* va = nullptr;    // virtual-memory pools: the layer's reserved range
+  size_t va_pages = 0;
   // device tables (inside the resident run)
   int* d_bits = nullptr;
   int* d_err = nullptr;
@@ -340,6 +435,21 @@ pw_status write_bits(pw_layer_t l, int e, int b, cudaStream_t s) {
   return PW_OK;
 }
 
+// Address of virtual page v of block b: its fixed virtual range in a
+// virtual-memory pool, else the physical page's address in the buffer.
+char* blk_addr(const pw_layer_s* l, const Block& b, int v) {
+  return l->pool->vmm ? b.va + (size_t)v * l->pool->page_bytes : l->pool->page_addr(b.pages[v]);
+}
+
+// Give block b its pages (mapped at its virtual range in a virtual-memory pool).
+pw_status attach_block(pw_layer_t l, Block& b, std::vector<int> pages) {
+  b.pages = std::move(pages);
+  b.st = B_MAPPED;
+  if (l->pool->vmm)
+    for (size_t v = 0; v < b.pages.size(); ++v) PW_TRY(l->pool->vmm_map(b.va + v * l->pool->page_bytes, b.pages[v]));
+  return PW_OK;
+}
+
 pw_status upload_pt_rows(pw_layer_t l, int e, cudaStream_t s) {
   const size_t prow = (size_t)kPlanes * l->pmax;
   PW_TRY(dev_h2d(l->d_plane_pt + (size_t)e * prow, l->h_plane_pt.data() + (size_t)e * prow,
@@ -354,7 +464,7 @@ pw_status upload_block(pw_layer_t l, const Block& b, const std::vector<char>& im
   const size_t pb = l->pool->page_bytes;
   for (size_t v = 0; v < b.pages.size(); ++v) {
     const size_t n = std::min(pb, img.size() - v * pb);
-    PW_TRY(dev_h2d(l->pool->page_addr(b.pages[v]), img.data() + v * pb, n, s));
+    PW_TRY(dev_h2d(blk_addr(l, b, (int)v), img.data() + v * pb, n, s));
   }
   return PW_OK;
 }
@@ -405,6 +515,18 @@ bool fits_after_release(pw_layer_t l, int e, int bits) {
   add(l->f16[e]);
   const int np = bits == 16 ? kPlanes : bits;
   return avail >= (size_t)np * l->pmax + (bits == 16 ? (size_t)l->pmax16 : 0);
+}
+
+// The layer's resident run back to the pool (and, in a virtual-memory pool,
+// its mappings and its reserved range).
+void release_resident(pw_layer_t l) {
+  pw_pool_s* pool = l->pool;
+  if (pool->vmm && l->va) {
+    for (size_t i = 0; i < l->res_npages; ++i) pool->vmm_unmap(l->va + i * pool->page_bytes);
+    pool->vmm_free(l->va, l->va_pages);
+    l->va = nullptr;
+  }
+  pool->give_back_resident(l->res_first, l->res_npages);
 }
 
 void release_expert(pw_layer_t l, int e) {
@@ -475,10 +597,48 @@ extern "C" pw_status pw_pool_create(void* dev_base, size_t bytes, size_t page_by
   return PW_OK;
 }
 
+extern "C" pw_status pw_pool_create_vmm(const unsigned long long* handles, size_t n_pages, size_t page_bytes,
+                                        int device, pw_pool_t* out) {
+  if (!handles || !out || n_pages == 0 || n_pages > (size_t)1 << 30) return PW_ERR_INVALID_ARG;
+  if (page_bytes == 0 || page_bytes % (2u << 20)) return PW_ERR_INVALID_ARG;  // whole 2 MiB granules
+  if (device < 0) return PW_ERR_INVALID_ARG;
+  auto p = std::make_unique<pw_pool_s>();
+  p->vmm = true;
+  p->device = device;
+  p->page_bytes = page_bytes;
+  p->npages = n_pages;
+  p->bytes = n_pages * page_bytes;
+  p->handles.assign(handles, handles + n_pages);
+  if (g_sim) {
+    // host simulation of the physical pages: one shared memory file, page p
+    // at offset p * page_bytes, mapped into reserved ranges with mmap
+    p->sim_fd = memfd_create("pw_vmm_pool", 0);
+    if (p->sim_fd < 0) return PW_ERR_UNSUPPORTED;
+    if (ftruncate(p->sim_fd, (off_t)p->bytes) != 0) {
+      close(p->sim_fd);
+      return PW_ERR_UNSUPPORTED;
+    }
+  } else if (!vmm_api().ok) {
+    return PW_ERR_UNSUPPORTED;
+  }
+  p->kind.assign(p->npages, 0);
+  for (size_t i = 0; i < p->npages; ++i) p->free_pages.insert((int)i);
+  *out = p.release();
+  return PW_OK;
+}
+
 extern "C" pw_status pw_pool_destroy(pw_pool_t pool) {
   if (!pool) return PW_ERR_INVALID_ARG;
   if (pool->n_layers) return PW_ERR_INVALID_ARG;
+  if (pool->sim_fd >= 0) close(pool->sim_fd);
   delete pool;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_testing_vmm_counts(pw_pool_t pool, uint64_t* maps, uint64_t* unmaps) {
+  if (!pool || !maps || !unmaps) return PW_ERR_INVALID_ARG;
+  *maps = pool->n_map;
+  *unmaps = pool->n_unmap;
   return PW_OK;
 }
 
@@ -553,7 +713,28 @@ extern "C" pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, 
   l->res_npages = (off + pool->page_bytes - 1) / pool->page_bytes;
   l->res_first = pool->take_resident(l->res_npages);
   if (l->res_first < 0) return PW_ERR_OOM;
-  l->res_base = pool->page_addr(l->res_first);
+  if (pool->vmm) {
+    // one reserved range per layer: the resident run, then a fixed range per
+    // block (expert e, plane p: pmax pages; its fp16 block: pmax16 pages).
+    // A block's pages are mapped into its range while it holds them, so its
+    // addresses (and the device page table) never change.
+    const size_t per_expert = (size_t)kPlanes * l->pmax + l->pmax16;
+    l->va_pages = l->res_npages + (size_t)E * per_expert;
+    l->va = pool->vmm_reserve(l->va_pages);
+    pw_status st = l->va ? PW_OK : (g_sim ? PW_ERR_UNSUPPORTED : PW_ERR_CUDA);
+    size_t mapped = 0;
+    for (; st == PW_OK && mapped < l->res_npages; ++mapped)
+      st = pool->vmm_map(l->va + mapped * pool->page_bytes, l->res_first + (int)mapped);
+    if (st != PW_OK) {
+      for (size_t i = 0; i + 1 < mapped; ++i) pool->vmm_unmap(l->va + i * pool->page_bytes);
+      pool->vmm_free(l->va, l->va_pages);
+      pool->give_back_resident(l->res_first, l->res_npages);
+      return st;
+    }
+    l->res_base = l->va;
+  } else {
+    l->res_base = pool->page_addr(l->res_first);
+  }
   char* rb = l->res_base;
   l->d_bits = reinterpret_cast<int*>(rb + o_bits);
   l->d_err = reinterpret_cast<int*>(rb + o_err);
@@ -569,6 +750,14 @@ extern "C" pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, 
   l->bits.assign(E, 0);
   l->planes.resize((size_t)E * kPlanes);
   l->f16.resize(E);
+  if (pool->vmm) {
+    const size_t pb = pool->page_bytes, per_expert = (size_t)kPlanes * l->pmax + l->pmax16;
+    for (int e = 0; e < E; ++e) {
+      char* ev = l->va + (l->res_npages + (size_t)e * per_expert) * pb;
+      for (int p = 0; p < kPlanes; ++p) l->plane(e, p).va = ev + (size_t)p * l->pmax * pb;
+      l->f16[e].va = ev + (size_t)kPlanes * l->pmax * pb;
+    }
+  }
   l->h_plane_pt.assign((size_t)E * kPlanes * l->pmax, 0ull);
   l->h_f16_pt.assign((size_t)E * l->pmax16, 0ull);
   std::vector<unsigned long long> lutb(E);
@@ -584,7 +773,7 @@ extern "C" pw_status pw_layer_create(pw_pool_t pool, const pw_layer_desc* desc, 
   if (st == PW_OK) st = dev_h2d(l->d_lut_base, lutb.data(), sizeof(unsigned long long) * E, s);
   if (st == PW_OK) st = dev_sync(s);
   if (st != PW_OK) {
-    pool->give_back_resident(l->res_first, l->res_npages);
+    release_resident(l.get());
     return st;
   }
   pool->n_layers++;
@@ -596,7 +785,7 @@ extern "C" pw_status pw_layer_destroy(pw_layer_t l) {
   PW_TRY(check_layer(l));
   if (!g_sim) cudaDeviceSynchronize();
   for (int e = 0; e < l->desc.n_experts; ++e) release_expert(l, e);
-  l->pool->give_back_resident(l->res_first, l->res_npages);
+  release_resident(l);
   l->pool->n_layers--;
   delete l;
   return PW_OK;
@@ -643,12 +832,10 @@ extern "C" pw_status pw_layer_load_expert(pw_layer_t l, int e, int bits, const u
   }
   for (int p = 0; p < np; ++p) {
     Block& b = l->plane(e, p);
-    b.pages = pages[p];
-    b.st = B_MAPPED;
+    PW_TRY(attach_block(l, b, pages[p]));
     PW_TRY(upload_block(l, b, img[p], s));
     for (int v = 0; v < l->pmax; ++v)
-      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] =
-          reinterpret_cast<unsigned long long>(pool->page_addr(b.pages[v]));
+      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] = reinterpret_cast<unsigned long long>(blk_addr(l, b, v));
   }
   img.clear();
   if (bits == 16) {
@@ -664,11 +851,10 @@ extern "C" pw_status pw_layer_load_expert(pw_layer_t l, int e, int bits, const u
       }
     }
     Block& b = l->f16[e];
-    b.pages = pages[np];
-    b.st = B_MAPPED;
+    PW_TRY(attach_block(l, b, pages[np]));
     PW_TRY(upload_block(l, b, im, s));
     for (int v = 0; v < l->pmax16; ++v)
-      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(pool->page_addr(b.pages[v]));
+      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(blk_addr(l, b, v));
   }
   // LUTs (all four bitwidths stay resident)
   char* lb = l->d_luts + (size_t)e * l->lut_block_bytes;
@@ -710,22 +896,19 @@ extern "C" pw_status pw_layer_copy_expert(pw_layer_t l, int e, pw_layer_t src, i
   for (int p = 0; p < np; ++p) {
     Block& b = l->plane(e, p);
     const Block& sb = src->plane(e_src, p);
-    b.pages = pages[p];
-    b.st = B_MAPPED;
+    PW_TRY(attach_block(l, b, pages[p]));
     for (int v = 0; v < l->pmax; ++v) {
-      PW_TRY(dev_d2d(l->pool->page_addr(b.pages[v]), src->pool->page_addr(sb.pages[v]), pb, s));
-      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] =
-          reinterpret_cast<unsigned long long>(l->pool->page_addr(b.pages[v]));
+      PW_TRY(dev_d2d(blk_addr(l, b, v), blk_addr(src, sb, v), pb, s));
+      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] = reinterpret_cast<unsigned long long>(blk_addr(l, b, v));
     }
   }
   if (bits == 16) {
     Block& b = l->f16[e];
     const Block& sb = src->f16[e_src];
-    b.pages = pages[np];
-    b.st = B_MAPPED;
+    PW_TRY(attach_block(l, b, pages[np]));
     for (int v = 0; v < l->pmax16; ++v) {
-      PW_TRY(dev_d2d(l->pool->page_addr(b.pages[v]), src->pool->page_addr(sb.pages[v]), pb, s));
-      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(l->pool->page_addr(b.pages[v]));
+      PW_TRY(dev_d2d(blk_addr(l, b, v), blk_addr(src, sb, v), pb, s));
+      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(blk_addr(l, b, v));
     }
   }
   PW_TRY(dev_d2d(l->d_luts + (size_t)e * l->lut_block_bytes, src->d_luts + (size_t)e_src * src->lut_block_bytes,
@@ -819,7 +1002,7 @@ pw_status upload_tiles(pw_layer_t l, const Block& b, const std::vector<uint2>& m
       if (nx.x != loc.x || nx.y != loc.y + run * tile_bytes) break;
       ++run;
     }
-    PW_TRY(dev_h2d_on(l->pool->page_addr(b.pages[loc.x]) + loc.y, host + (size_t)tau * tile_bytes,
+    PW_TRY(dev_h2d_on(blk_addr(l, b, (int)loc.x) + loc.y, host + (size_t)tau * tile_bytes,
                       (size_t)run * tile_bytes, s));
     tau += run;
   }
@@ -895,24 +1078,21 @@ extern "C" pw_status pw_prefetch_expert(pw_layer_t l, int e, int bits, const uin
   for (size_t i = 0; i < missing.size(); ++i) {
     const int p = missing[i];
     Block& b = l->plane(e, p);
-    b.pages = pages[i];
-    b.st = B_MAPPED;
+    PW_TRY(attach_block(l, b, pages[i]));
     for (int m = 0; m < 3; ++m)
       PW_TRY(upload_tiles(l, b, l->tmap, m, reinterpret_cast<const char*>(planes_host[m][p]),
                           2 * (size_t)l->C[m], cs));
     for (int v = 0; v < l->pmax; ++v)
-      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] =
-          reinterpret_cast<unsigned long long>(pool->page_addr(b.pages[v]));
+      l->h_plane_pt[((size_t)e * kPlanes + p) * l->pmax + v] = reinterpret_cast<unsigned long long>(blk_addr(l, b, v));
   }
   if (f16_missing) {
     Block& b = l->f16[e];
-    b.pages = pages[missing.size()];
-    b.st = B_MAPPED;
+    PW_TRY(attach_block(l, b, pages[missing.size()]));
     for (int m = 0; m < 3; ++m)
       PW_TRY(upload_tiles(l, b, l->tmap16, m, reinterpret_cast<const char*>(w16_host[m]), 32 * (size_t)l->C[m],
                           cs));
     for (int v = 0; v < l->pmax16; ++v)
-      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(pool->page_addr(b.pages[v]));
+      l->h_f16_pt[(size_t)e * l->pmax16 + v] = reinterpret_cast<unsigned long long>(blk_addr(l, b, v));
   }
   PW_TRY(upload_pt_rows(l, e, cs));
   std::shared_ptr<Event> ready;
@@ -1002,7 +1182,7 @@ int class_mask(const pw_layer_s* l) {
 // Scratch of one whole-layer call (pw_moe_forward): the permutation and the
 // routed / shared FFN intermediates, then the hot-path scratch of ws_layout.
 struct FwdLayout {
-  size_t off_offsets, off_perm_src, off_inv_slot, off_x_perm, off_y_perm, off_ys, off_base, total;
+  size_t off_offsets, off_perm_src, off_inv_slot, off_x_perm, off_y_perm, off_ys, off_rpart, off_base, total;
 };
 
 FwdLayout fwd_layout(const pw_layer_s* l, int T) {
@@ -1020,6 +1200,9 @@ FwdLayout fwd_layout(const pw_layer_s* l, int T) {
   f.off_x_perm = take(2 * S * d);
   f.off_y_perm = take(sizeof(float) * S * d);
   f.off_ys = take(l->desc.shared_ffn ? sizeof(float) * (size_t)T * d : 0);
+  // router partial sums of the fused step (batches of at most kFusedMaxTokens)
+  f.off_rpart = take(sizeof(float) * (size_t)std::min(T, kFusedMaxTokens) * route_slices(l->desc.d) *
+                     l->desc.n_experts);
   f.off_base = o;
   f.total = o + ws_layout(l, T).total;
   return f;
@@ -1056,14 +1239,17 @@ extern "C" pw_status pw_moe_forward(pw_layer_t l, const void* x, const void* wr,
   auto* h = reinterpret_cast<__half*>(base + W.h_off);
   auto* hs = sh ? reinterpret_cast<__half*>(base + W.hs_off) : nullptr;
   const auto* xh = static_cast<const __half*>(x);
-  PW_TRY(launched(launch_route(L, xh, static_cast<const __half*>(wr), bias, T, idx, w, nullptr, s)));
-  // one fused launch for small decode batches (measured: 3-5% faster at 1-8
-  // tokens, 1.5% slower at 64, where the separate small kernels cost less
-  // than the fused kernel's final barrier); both give the same y bit for bit
-  const bool fused = T <= 16 && T <= decode_max_tokens(l->desc.ffn, T) &&
+  const auto* wrh = static_cast<const __half*>(wr);
+  // one fused launch (router, permutation, expert FFN, shared FFN, combine)
+  // for small decode batches (measured: 3-5% faster at 1-8 tokens, 1.5%
+  // slower at 64, where the separate small kernels cost less than the fused
+  // kernel's final barrier); both give the same idx, w and y bit for bit
+  const bool fused = T <= kFusedMaxTokens && T <= decode_max_tokens(l->desc.ffn, T) &&
                      (!sh || T <= decode_max_tokens_shared()) && T * l->desc.top_k <= 512;
   if (fused)
-    return launched(launch_layer_fused(L, xh, idx, w, T, h, hs, y_perm, ys, static_cast<__half*>(y), offsets, s));
+    return launched(launch_layer_fused(L, xh, wrh, bias, idx, w, reinterpret_cast<float*>(wsb + F.off_rpart), T, h,
+                                       hs, y_perm, ys, static_cast<__half*>(y), offsets, s));
+  PW_TRY(launched(launch_route(L, xh, wrh, bias, T, idx, w, nullptr, s)));
   auto* perm_src = reinterpret_cast<int*>(wsb + F.off_perm_src);
   auto* inv_slot = reinterpret_cast<int*>(wsb + F.off_inv_slot);
   auto* x_perm = reinterpret_cast<__half*>(wsb + F.off_x_perm);
@@ -1229,13 +1415,17 @@ extern "C" pw_status pw_debug_dequant(pw_layer_t l, int e, int m, void* out, voi
 extern "C" pw_status pw_debug_dequant_kernel(pw_layer_t l, int e, int m, int kernel, void* out, void* stream) {
   PW_TRY(check_layer(l));
   if (e < 0 || e >= l->desc.n_experts || m < 0 || m > 2 || !out || !aligned16(out)) return PW_ERR_INVALID_ARG;
-  if (kernel != PW_KERNEL_DECODE && kernel != PW_KERNEL_PREFILL) return PW_ERR_INVALID_ARG;
+  if (kernel != PW_KERNEL_DECODE && kernel != PW_KERNEL_PREFILL && kernel != PW_KERNEL_DECODE_ROW_TABLES &&
+      kernel != PW_KERNEL_DECODE_LANE_TABLES)
+    return PW_ERR_INVALID_ARG;
   if (l->bits[e] == 0) return PW_ERR_INVALID_ARG;
   PW_TRY(device_only());
   const DevLayer L = l->dev();
   auto* o = static_cast<__half*>(out);
-  return launched(kernel == PW_KERNEL_DECODE ? launch_decode_dump(L, e, m, o, as_stream(stream))
-                                             : launch_prefill_dump(L, e, m, o, as_stream(stream)));
+  cudaStream_t s = as_stream(stream);
+  if (kernel == PW_KERNEL_PREFILL) return launched(launch_prefill_dump(L, e, m, o, s));
+  const bool lane = kernel == PW_KERNEL_DECODE ? nblk_for(L) == 2 : kernel == PW_KERNEL_DECODE_LANE_TABLES;
+  return launched(launch_decode_dump(L, e, m, lane, o, s));
 }
 
 extern "C" pw_status pw_debug_page_address(pw_layer_t l, int e, int p, int vpage, uint64_t* addr) {
@@ -1246,7 +1436,7 @@ extern "C" pw_status pw_debug_page_address(pw_layer_t l, int e, int p, int vpage
     *addr = 0;
     return PW_OK;
   }
-  *addr = reinterpret_cast<uint64_t>(l->pool->page_addr(b.pages[vpage]));
+  *addr = reinterpret_cast<uint64_t>(blk_addr(l, b, vpage));
   return PW_OK;
 }
 

@@ -1,11 +1,17 @@
-"""Benchmark: routed bit-plane MoE layer (Qwen1.5-MoE-A2.7B-shaped) decode step on GB300.
+"""Benchmark: routed bit-plane MoE layers on GB300.
 
 One step = the whole hot path (router top-K -> permutation -> bit-plane expert
-FFN -> fp16 shared FFN -> weighted combine) over one decode batch of T tokens
-through one layer.  Layer copies (same synthetic weights, distinct pages) are
-visited round-robin so weights stream from HBM, not L2.
+FFN -> fp16 shared FFN -> weighted combine) over one batch of T tokens.  The
+default headline is the largest configuration: 32 Mixtral-8x7B-shaped layers
+decoding 64 tokens per step, a seeded quarter of the (layer, expert) pairs
+changing bitwidth by page-table unmap/remap every step.  Beside it, in the same
+run ("sub_runs"): the single Mixtral-shaped layer at decode 1/8/64/256 and
+prefill 4096 tokens, the 128-expert layer at decode 128 and prefill 8192, the
+Qwen1.5-MoE-shaped layer at decode 1/8/64/256, and the throughput loss of
+asynchronous paging.  Layer copies (same synthetic weights, distinct pages)
+are visited round-robin so weights stream from HBM, not L2.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload W --tokens T] [--impl reference]
 
 Prints one JSON line (rank 0).  With torchrun (N > 1) every rank runs an
 independent replica of the layer on its own GPU ("replicas only": the path has
@@ -42,6 +48,11 @@ WORKLOADS = {
 }
 
 
+# The headline: the largest configuration that runs on one GPU, 32
+# Mixtral-shaped layers decoding 64 tokens per step with bitwidth changes.
+DEFAULT_WORKLOAD = "sweep"
+
+
 def _load_json(path):
     try:
         with open(path) as f:
@@ -54,17 +65,23 @@ def _load_json(path):
 # workload
 # ---------------------------------------------------------------------------
 
-def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda"):
-    """Upload n_copies of one synthetic layer; returns a dict with host copies for the oracle."""
+def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda", src=None):
+    """Upload n_copies of one synthetic layer; returns a dict with host copies for the oracle.
+
+    src: a layer of the same shape holding this config's experts at 16 bits
+    (all six planes and the fp16 page); the copies then take device copies of
+    them (pw_layer_copy_expert) instead of generating and uploading from the
+    host.  The sweep's source layer holds exactly the Mixtral-shaped experts
+    (same seeded codes and LUTs), so the Mixtral sub-runs are built from it."""
     import torch
 
     import any_precision_expert_gb300 as pw
-    from synth import bits_plan, get_config, make_expert, make_router, make_shared, make_tokens
+    from synth import bits_plan, get_config, make_expert, make_router, make_shared
 
     cfg = get_config(cfg_name)
     bits = bits_plan(cfg, seed)
     wr, bias = make_router(cfg, seed)
-    experts = [make_expert(cfg, e, seed) for e in range(cfg.E)]
+    experts = None if src is not None else [make_expert(cfg, e, seed) for e in range(cfg.E)]
     shared = make_shared(cfg, seed)
     plane = 3 * cfg.d * cfg.f // 8
     page = 2 << 20
@@ -79,19 +96,43 @@ def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda"):
     layers = []
     for _ in range(n_copies):
         L = pw.Layer(pool, cfg.d, cfg.f, cfg.E, cfg.K, cfg.renormalize, cfg.shared_ffn)
-        for e, ex in enumerate(experts):
-            L.load_expert(e, int(bits[e]), ex["code6"], ex["lut"], ex["w16"])
+        for e in range(cfg.E):
+            if src is not None:
+                L.copy_expert(e, src, e, int(bits[e]))
+            else:
+                ex = experts[e]
+                L.load_expert(e, int(bits[e]), ex["code6"], ex["lut"], ex["w16"])
         if shared is not None:
             L.load_shared(shared)
         layers.append(L)
-    wr_d = torch.from_numpy(wr).to(device)
-    bias_d = torch.from_numpy(bias).to(device) if bias is not None else None
-    xs = [make_tokens(cfg, T, seed, stream=i) for i in range(n_copies)]
-    xs_d = [torch.from_numpy(x).to(device) for x in xs]
-    bufs = [pw.Buffers(L, T, device=device) for L in layers]
+    wl = dict(cfg=cfg, name=cfg_name, seed=seed, bits=bits, wr=wr, bias=bias, experts=experts, shared=shared,
+              pool=pool, layers=layers, wr_d=torch.from_numpy(wr).to(device),
+              bias_d=torch.from_numpy(bias).to(device) if bias is not None else None, bufs=None)
+    set_tokens(wl, T, device)
+    return wl
+
+
+def set_tokens(wl, T, device="cuda"):
+    """Seeded inputs and device buffers of every layer copy for batches of T tokens."""
+    import torch
+
+    import any_precision_expert_gb300 as pw
+    from synth import make_tokens
+
+    cfg = wl["cfg"]
+    wl["bufs"] = None  # the previous batch size's buffers go back to torch first
+    wl["xs"] = [make_tokens(cfg, T, wl["seed"], stream=i) for i in range(len(wl["layers"]))]
+    wl["xs_d"] = [torch.from_numpy(x).to(device) for x in wl["xs"]]
+    wl["bufs"] = [pw.Buffers(L, T, device=device) for L in wl["layers"]]
+    wl["T"] = T
     torch.cuda.synchronize()
-    return dict(cfg=cfg, bits=bits, wr=wr, bias=bias, experts=experts, shared=shared, pool=pool,
-                layers=layers, wr_d=wr_d, bias_d=bias_d, xs=xs, xs_d=xs_d, bufs=bufs, T=T)
+
+
+def free_workload(wl):
+    for L in wl["layers"]:
+        L.destroy()
+    wl["bufs"] = None
+    wl["pool"].close()
 
 
 def algorithmic_bytes(cfg, bits, offsets, T):
@@ -110,6 +151,152 @@ def algorithmic_bytes(cfg, bits, offsets, T):
     router = d * cfg.E * 2
     io = 2 * T * d * 2
     return ffn + shared, ffn + shared + router + io
+
+
+def _peaks():
+    """(HBM GB/s, its source, 16-bit tensor TFLOP/s, its source)."""
+    peaks = _load_json(os.path.join(ROOT, "MEASURED_PEAKS.json"))
+    if peaks and peaks.get("hbm_gbs"):
+        hbm, hbm_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    else:
+        hbm, hbm_src = 6800.0, "fallback 6.8 TB/s"
+    if peaks and peaks.get("bf16_tflops"):
+        tc, tc_src = float(peaks["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops; fp16 runs at the bf16 rate)"
+    else:
+        tc, tc_src = 1900.0, "fallback 1.9 PFLOP/s"
+    return hbm, hbm_src, tc, tc_src
+
+
+def measure_steps(wl, K, W, stream, soak=0.0):
+    """Time K decode/prefill steps of the workload's current batch size.
+
+    W eager warm-up steps fix the routing of every layer copy (and with it
+    the algorithmic bytes); then one CUDA graph of K steps, copies visited
+    round-robin, with CUDA events (graph nodes, on the launching stream)
+    around each expert-FFN call -- or around the whole-layer call when the
+    step is the router plus one fused kernel.  `soak` seconds of untimed
+    replays come first (the clock record of the headline).  Returns the
+    total and per-call times with the bytes and FLOPs behind them."""
+    import inspect
+
+    import torch
+
+    import any_precision_expert_gb300 as pw
+
+    cfg, layers, bufs, xs_d, T = wl["cfg"], wl["layers"], wl["bufs"], wl["xs_d"], wl["T"]
+    NL = len(layers)
+    fused = _fused_step(cfg, T)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(W, NL)):
+            j = i % NL
+            pw.moe_forward_fused(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+    torch.cuda.synchronize()
+    ffn_bytes, step_bytes = [], []
+    for j in range(NL):
+        counts = np.bincount(bufs[j].idx[:T].cpu().numpy().reshape(-1), minlength=cfg.E)
+        off = np.concatenate([[0], np.cumsum(counts)])
+        fb, sb = algorithmic_bytes(cfg, wl["bits"], off, T)
+        ffn_bytes.append(fb)
+        step_bytes.append(sb)
+
+    external = "external" in inspect.signature(torch.cuda.Event.__new__).parameters
+
+    def mk_event():
+        return torch.cuda.Event(enable_timing=True, external=True) if external else \
+            torch.cuda.Event(enable_timing=True)
+
+    ev_a = [mk_event() for _ in range(K)]
+    ev_b = [mk_event() for _ in range(K)]
+
+    def part_a(L, b, x):
+        if not fused:
+            L.route_topk(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, None, stream)
+            L.permute(b.idx, T, x, b.offsets, b.perm_src, b.inv_slot, b.x_perm, b.ws, stream)
+
+    def part_f(L, b, x):
+        if fused:
+            L.forward(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, b.y, b.fws, stream)
+        else:
+            L.moe_ffn(x, b.x_perm, b.offsets, T, b.y_perm, b.y_shared if cfg.shared_ffn else None, b.ws, stream)
+
+    def part_c(L, b, x):
+        if not fused:
+            L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared if cfg.shared_ffn else None, b.y, stream)
+
+    if external:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                j = i % NL
+                part_a(layers[j], bufs[j], xs_d[j])
+                ev_a[i].record(stream)
+                part_f(layers[j], bufs[j], xs_d[j])
+                ev_b[i].record(stream)
+                part_c(layers[j], bufs[j], xs_d[j])
+
+        def region():
+            g.replay()
+    else:
+        graphs = []
+        for j in range(NL):
+            trio = []
+            for part in (part_a, part_f, part_c):
+                gg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gg, stream=stream):
+                    part(layers[j], bufs[j], xs_d[j])
+                trio.append(gg)
+            graphs.append(trio)
+
+        def region():
+            torch.cuda._sleep(int(60e6))  # hold the GPU while the host queues the region
+            for i in range(K):
+                ga, gf, gc = graphs[i % NL]
+                ga.replay()
+                ev_a[i].record(stream)
+                gf.replay()
+                ev_b[i].record(stream)
+                gc.replay()
+    torch.cuda.synchronize()
+    t_soak = time.time()
+    while time.time() - t_soak < soak:
+        with torch.cuda.stream(stream):
+            region()
+        torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        region()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    call_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(K)]
+    return {"ms": t0.elapsed_time(t1), "K": K, "NL": NL, "fused": fused, "external": external,
+            "call_ms": sum(call_ms) / K,
+            "ffn_bytes": sum(ffn_bytes[i % NL] for i in range(K)) / K,
+            "step_bytes": sum(step_bytes[i % NL] for i in range(K)) / K,
+            "ffn_flops": 2.0 * T * 3 * cfg.d * (cfg.K * cfg.f + cfg.shared_ffn)}
+
+
+def roofline_of(m, cfg, T):
+    """Roofline of the timed call: HBM for decode batches (algorithmic bytes of
+    the call over its time), 16-bit tensor for prefill-sized ones."""
+    hbm, hbm_src, tc, tc_src = _peaks()
+    call_bytes = m["step_bytes"] if m["fused"] else m["ffn_bytes"]
+    call_s = m["call_ms"] * 1e-3
+    gbs = call_bytes / call_s / 1e9
+    tflops = m["ffn_flops"] / call_s / 1e12
+    name = ("whole-layer call pw_moe_forward (one persistent kernel: router, permutation, routed experts, "
+            "shared FFN, combine)" if m["fused"] else "expert FFN call pw_moe_ffn (routed experts + shared FFN)")
+    if T * cfg.K / cfg.E >= 256:  # tokens per expert: prefill-sized, the tensor pipe bounds it
+        return {"kernel": name, "bound": "tensor", "achieved": tflops, "peak": tc, "unit": "TFLOP/s",
+                "frac": tflops / tc, "algorithmic_flops_per_launch": m["ffn_flops"],
+                "algorithmic_bytes_per_launch": m["ffn_bytes"], "hbm_GBps": gbs, "avg_launch_ms": m["call_ms"],
+                "peak_source": tc_src}
+    return {"kernel": name, "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+            "algorithmic_bytes_per_launch": call_bytes, "TFLOPs": tflops, "avg_launch_ms": m["call_ms"],
+            "peak_source": hbm_src}
 
 
 # ---------------------------------------------------------------------------
@@ -204,134 +391,20 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(v):
-        return rank_max(v, ws, "cuda")
-
     T, K, W = args.tokens, args.steps, args.warmup
     wl = build_workload(args.workload, n_copies=args.copies, T=T)
-    cfg, layers, bufs, xs_d = wl["cfg"], wl["layers"], wl["bufs"], wl["xs_d"]
+    cfg, layers, bufs = wl["cfg"], wl["layers"], wl["bufs"]
     NL = len(layers)
     stream = torch.cuda.Stream()
 
-    fused = _fused_step(cfg, T)
-
-    def step(i, s):
-        j = i % NL
-        pw.moe_forward_fused(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=s)
-
-    # warm-up (eager), then routing is fixed per copy: algorithmic bytes per step
-    with torch.cuda.stream(stream):
-        for i in range(max(W, NL)):
-            step(i, stream)
-    torch.cuda.synchronize()
-    ffn_bytes, step_bytes = [], []
-    for j in range(NL):
-        counts = np.bincount(bufs[j].idx[:T].cpu().numpy().reshape(-1), minlength=cfg.E)
-        off = np.concatenate([[0], np.cumsum(counts)])
-        fb, sb = algorithmic_bytes(cfg, wl["bits"], off, T)
-        ffn_bytes.append(fb)
-        step_bytes.append(sb)
-
-    # one CUDA graph of K steps, with events around each expert-FFN call (the
-    # whole-layer call when the step runs as router + one fused kernel).  The
-    # events are "external" graph nodes (timed when the graph runs); where the
-    # installed torch lacks them, each step is three graphs with ordinary
-    # events between them and the GPU is held briefly so the host can queue
-    # the whole timed region first.
-    import inspect
-    external = "external" in inspect.signature(torch.cuda.Event.__new__).parameters
-
-    def mk_event():
-        return torch.cuda.Event(enable_timing=True, external=True) if external else \
-            torch.cuda.Event(enable_timing=True)
-
-    ev_a = [mk_event() for _ in range(K)]
-    ev_b = [mk_event() for _ in range(K)]
-
-    def part_a(L, b, x):
-        if not fused:
-            L.route_topk(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, None, stream)
-            L.permute(b.idx, T, x, b.offsets, b.perm_src, b.inv_slot, b.x_perm, b.ws, stream)
-
-    def part_f(L, b, x):
-        if fused:
-            L.forward(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, b.y, b.fws, stream)
-        else:
-            L.moe_ffn(x, b.x_perm, b.offsets, T, b.y_perm, b.y_shared if cfg.shared_ffn else None, b.ws, stream)
-
-    def part_c(L, b, x):
-        if not fused:
-            L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared if cfg.shared_ffn else None, b.y, stream)
-
-    launches_per_step = _launches_per_step(cfg, T)
-    if external:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(K):
-                j = i % NL
-                part_a(layers[j], bufs[j], xs_d[j])
-                ev_a[i].record(stream)
-                part_f(layers[j], bufs[j], xs_d[j])
-                ev_b[i].record(stream)
-                part_c(layers[j], bufs[j], xs_d[j])
-
-        def timed_region():
-            g.replay()
-    else:
-        graphs = []
-        for j in range(NL):
-            trio = []
-            for part in (part_a, part_f, part_c):
-                gg = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gg, stream=stream):
-                    part(layers[j], bufs[j], xs_d[j])
-                trio.append(gg)
-            graphs.append(trio)
-
-        def timed_region():
-            torch.cuda._sleep(int(60e6))  # hold the GPU while the host queues the region
-            for i in range(K):
-                ga, gf, gc = graphs[i % NL]
-                ga.replay()
-                ev_a[i].record(stream)
-                gf.replay()
-                ev_b[i].record(stream)
-                gc.replay()
-    torch.cuda.synchronize()
-
     clocks = ClockSampler(local)
     clocks.start()
-    t_soak = time.time()
-    with torch.cuda.stream(stream):
-        while time.time() - t_soak < args.soak:
-            timed_region()
-            torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     barrier()
-    with torch.cuda.stream(stream):
-        if not external:
-            torch.cuda._sleep(int(60e6))
-        t0.record(stream)
-        if external:
-            g.replay()
-        else:
-            for i in range(K):
-                ga, gf, gc = graphs[i % NL]
-                ga.replay()
-                ev_a[i].record(stream)
-                gf.replay()
-                ev_b[i].record(stream)
-                gc.replay()
-        t1.record(stream)
+    m = measure_steps(wl, K, W, stream, soak=args.soak)
     barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    ms_max = max_over_ranks(ms)
-    ffn_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(K)]
-    ffn_avg_ms = sum(ffn_ms) / K
-    ffn_avg_bytes = sum(ffn_bytes[i % NL] for i in range(K)) / K
-    step_avg_bytes = sum(step_bytes[i % NL] for i in range(K)) / K
+    ms_max = rank_max(m["ms"], ws, "cuda")
+    fused = m["fused"]
 
     # end to end through the public API with pinned host buffers: every step
     # copies its input in and its result out; the next step is enqueued
@@ -354,30 +427,11 @@ def run_gpu(args):
             if i > 0:
                 y_done[(i - 1) & 1].synchronize()  # step i - 1's result is on the host
     barrier()
-    e2e_s = max_over_ranks(time.perf_counter() - te)
+    e2e_s = rank_max(time.perf_counter() - te, ws, "cuda")
 
     paging = measure_paging(wl, stream, args.paging) if args.paging > 0 else None
-
-    peaks = _load_json(os.path.join(ROOT, "MEASURED_PEAKS.json"))
-    if peaks and peaks.get("hbm_gbs"):
-        peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
-    else:
-        peak, peak_src = 6800.0, "fallback 6.8 TB/s"
-    ffn_flops = 2.0 * T * 3 * cfg.d * (cfg.K * cfg.f + cfg.shared_ffn)  # routed + shared FFN, algorithmic
-    # the timed call: the expert FFN, or the whole layer (router, x in, y out too) when fused
-    call_bytes = step_avg_bytes if fused else ffn_avg_bytes
-    call_name = ("whole-layer call pw_moe_forward (router + one persistent kernel: permutation, "
-                 "routed experts, shared FFN, combine)" if fused else
-                 "expert FFN call pw_moe_ffn (routed experts + shared FFN)")
-    tflops = ffn_flops / (ffn_avg_ms * 1e-3) / 1e12
-    gbs = call_bytes / (ffn_avg_ms * 1e-3) / 1e9
-    # decode batches are bound by weight bytes, prefill batches by the tensor pipe
-    tensor_bound = T * cfg.K / cfg.E >= 256
-    if tensor_bound:
-        tpk = float(peaks["bf16_tflops"]) if peaks and peaks.get("bf16_tflops") else 1900.0
-        tpk_src = ("measured (MEASURED_PEAKS.json bf16_tflops; fp16 runs at the bf16 rate)"
-                   if peaks and peaks.get("bf16_tflops") else "fallback 1.9 PFLOP/s")
-    traffic = _traffic_from_profile(args.workload, T)
+    roof = roofline_of(m, cfg, T)
+    roof["traffic"] = _traffic_from_profile(args.workload, T)
     ok = all(L.check_device() == 0 for L in layers)
 
     out = None
@@ -402,55 +456,68 @@ def run_gpu(args):
                 "bits_plan": {str(b): int((wl["bits"] == b).sum()) for b in (3, 4, 5, 6, 16)},
                 "layer_copies": NL,
                 "l2": f"inputs larger than L2: {NL} layer copies visited round-robin "
-                      f"({step_avg_bytes * (NL - 1) / 1e6:.0f} MB streamed between reuses of a copy)",
-                "timing": ("one CUDA graph of K steps with timed event nodes" if external else
+                      f"({m['step_bytes'] * (NL - 1) / 1e6:.0f} MB streamed between reuses of a copy)",
+                "timing": ("one CUDA graph of K steps with timed event nodes" if m["external"] else
                            "three CUDA graphs per step, queued ahead of the GPU") + "; CUDA events on the launching stream",
-                "step_algorithmic_bytes": step_avg_bytes,
-                "hbm_GBps_step": step_avg_bytes / ((ms_max / K) * 1e-3) / 1e9,
-                "ffn_GBps": gbs,
-                "ffn_TFLOPs": tflops,
+                "step_algorithmic_bytes": m["step_bytes"],
+                "hbm_GBps_step": m["step_bytes"] / ((ms_max / K) * 1e-3) / 1e9,
                 "parallelism": "replicas" if ws > 1 else "single GPU",
                 "device_errors": not ok,
             },
-            "roofline": ({
-                "kernel": call_name,
-                "bound": "tensor",
-                "achieved": tflops,
-                "peak": tpk,
-                "unit": "TFLOP/s",
-                "frac": tflops / tpk,
-                "traffic": traffic,
-                "algorithmic_flops_per_launch": ffn_flops,
-                "algorithmic_bytes_per_launch": ffn_avg_bytes,
-                "avg_launch_ms": ffn_avg_ms,
-                "peak_source": tpk_src,
-            } if tensor_bound else {
-                "kernel": call_name,
-                "bound": "hbm",
-                "achieved": gbs,
-                "peak": peak,
-                "unit": "GB/s",
-                "frac": gbs / peak,
-                "traffic": traffic,
-                "algorithmic_bytes_per_launch": call_bytes,
-                "avg_launch_ms": ffn_avg_ms,
-                "peak_source": peak_src,
-            }),
+            "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": T * cfg.d * 2,
                     "d2h_bytes_per_step": T * cfg.d * 2, "steps": KE,
                     "note": "public API (pw_moe_forward) per step: pinned H2D of x, layer, D2H of y, host wait for y; two steps in flight (step i+1 enqueued before the host waits for step i)"},
-            "gpu_launches": launches_per_step * K,
+            "gpu_launches": _launches_per_step(cfg, T) * K,
             "clocks": clk,
         }
         if paging is not None:
             out["config"]["paging"] = paging
-    for L in layers:
-        L.destroy()
-    wl["pool"].close()
+    free_workload(wl)
+    if rank == 0 and args.sub_runs and ws == 1:
+        out["sub_runs"] = sub_runs(stream)
     if ws > 1:
         dist.destroy_process_group()
     return out
+
+
+# The other workloads of the layer's configurations, measured in the same run
+# beside the headline: every decode batch size and prefill size they name.
+SUB_RUNS = (("mixtral", 2, (1, 8, 64, 256, 4096)),
+            ("e128", 2, (128, 8192)),
+            ("qwen", 6, (1, 8, 64, 256)))
+
+
+def sub_runs(stream, src=None, steps_decode=50, steps_prefill=10, warmup=3, paging_steps=48):
+    """One record per (workload, batch size): tokens/s and the roofline of the
+    timed call, plus the throughput loss of asynchronous paging on the
+    Qwen-shaped layer.  src: the sweep's source layer (Mixtral-shaped experts
+    at 16 bits) to copy the Mixtral layers from."""
+    recs = []
+    for name, copies, Ts in SUB_RUNS:
+        wl = build_workload(name, n_copies=copies, T=Ts[0], src=src if name == "mixtral" else None)
+        cfg = wl["cfg"]
+        for T in Ts:
+            if T != wl["T"]:
+                set_tokens(wl, T)
+            prefill = T * cfg.K / cfg.E >= 256
+            m = measure_steps(wl, steps_prefill if prefill else steps_decode, warmup, stream)
+            roof = roofline_of(m, cfg, T)
+            recs.append({"workload": name, "tokens": T, "kind": "prefill" if prefill else "decode",
+                         "value": T * m["K"] / (m["ms"] * 1e-3), "unit": "tokens/s",
+                         "ms_per_step": m["ms"] / m["K"], "steps": m["K"], "layer_copies": m["NL"],
+                         "timed_call": "pw_moe_forward (one fused kernel, router included)" if m["fused"] else "pw_moe_ffn",
+                         "call_ms": m["call_ms"],
+                         "roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "peak", "frac")},
+                         "hbm_GBps_call": roof.get("hbm_GBps", roof["achieved"] if roof["bound"] == "hbm" else None),
+                         "device_errors": not all(L.check_device() == 0 for L in wl["layers"])})
+        if name == "qwen" and paging_steps > 0:
+            set_tokens(wl, 64)
+            recs.append({"workload": name, "tokens": 64, "kind": "paging",
+                         "paging": measure_paging(wl, stream, paging_steps)})
+        free_workload(wl)
+    return recs
 
 
 def _thresholds(cfg, T):
@@ -460,20 +527,21 @@ def _thresholds(cfg, T):
 
 
 def _fused_step(cfg, T):
-    """pw_moe_forward runs router + one fused kernel for decode batches of at most 16 tokens."""
+    """pw_moe_forward runs one fused kernel (router included) for decode batches of at most 16 tokens."""
     thr, thr_s = _thresholds(cfg, T)
     return T <= 16 and T <= thr and (not cfg.shared_ffn or T <= thr_s) and T * cfg.K <= 512
 
 
 def _launches_per_step(cfg, T):
-    """Kernels one step launches: the router and, when every group is
-    decode-sized, one fused kernel; otherwise the permutation (histogram +
-    scatter for more than 1024 slots, or one kernel), row gather, the
-    persistent decode kernel, the tcgen05 GEMM pair for experts above the
-    token threshold and for a shared FFN above its own, and the combine."""
+    """Kernels one step launches: one fused kernel (router included) when
+    every group is decode-sized; otherwise the router, the permutation
+    (histogram + scatter for more than 1024 slots, or one kernel), row
+    gather, the persistent decode kernel, the tcgen05 GEMM pair for experts
+    above the token threshold and for a shared FFN above its own, and the
+    combine."""
     thr, thr_s = _thresholds(cfg, T)
     if _fused_step(cfg, T):
-        return 2
+        return 1
     S = T * cfg.K
     n = 1 + (2 if S > 1024 else 1) + 1
     n += 1
@@ -676,6 +744,9 @@ def run_sweep(args):
         }
     for L in layers:
         L.destroy()
+    sw["bufs"] = None
+    if rank == 0 and args.sub_runs and ws == 1:
+        out["sub_runs"] = sub_runs(stream, src=sw["src"])
     sw["src"].destroy()
     sw["pool"].close()
     if ws > 1:
@@ -708,8 +779,11 @@ def measure_paging(wl, stream, n_steps):
     visit goes back to 3 bits, the expert prefetched then is raised to 6 bits
     (pw_set_expert_bitwidth: the commit, in stream order), and the next 3-bit
     expert's three missing planes are uploaded from pinned host memory on a
-    copy stream (pw_prefetch_expert), to be committed at the next visit.
-    Eager steps with and without the paging, same routing."""
+    copy stream (pw_prefetch_expert), to be committed at the copy's next
+    visit, i.e. a step ahead.  Each step replays the copy's captured CUDA
+    graph of the whole layer (it reads bitwidths and page tables from device
+    memory); the paging calls run on the host between replays.  Same routing
+    with and without the paging."""
     import torch
 
     import any_precision_expert_gb300 as pw
@@ -729,6 +803,17 @@ def measure_paging(wl, stream, n_steps):
     for e in three:
         planes_of(e)
     copy = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for j in range(NL):  # warm the copy once eagerly, then capture its whole-layer call
+            pw.moe_forward_fused(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+    torch.cuda.synchronize()
+    for j in range(NL):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            pw.moe_forward_fused(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+        graphs.append(g)
+    torch.cuda.synchronize()
 
     def run(with_paging):
         raised, fetched = {}, {}
@@ -749,7 +834,7 @@ def measure_paging(wl, stream, n_steps):
                     e = three[(i // NL) % len(three)]
                     layers[j].prefetch_expert(e, 6, planes=planes_of(e), copy_stream=copy)
                     fetched[j] = e
-                pw.moe_forward_fused(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+                graphs[j].replay()
             t1.record(stream)
         torch.cuda.synchronize()
         for j, e in list(raised.items()) + list(fetched.items()):
@@ -759,14 +844,17 @@ def measure_paging(wl, stream, n_steps):
         return t0.elapsed_time(t1)
 
     run(False)  # warm-up
-    base_ms = run(False)
-    pag_ms = run(True)
+    base_ms = min(run(False), run(False))
+    pag_ms = min(run(True), run(True))
     upload = 3 * 3 * (wl["cfg"].d * wl["cfg"].f // 8)
     return {"steps": n_steps, "tokens_per_s_without": T * n_steps / (base_ms * 1e-3),
             "tokens_per_s_with": T * n_steps / (pag_ms * 1e-3),
             "loss_pct": 100.0 * (1.0 - base_ms / pag_ms), "upload_bytes_per_step": upload,
-            "note": "eager steps (no graph); per step one lower, one raise committing the previous visit's "
-                    "prefetch, one prefetch (three planes uploaded on a copy stream)"}
+            "pages_figure_context": "the write-up reports at most 4.1% for its system (hardware not stated)",
+            "note": "CUDA-graph replay of the whole layer per step; per step one lower, one raise committing the "
+                    "previous visit's prefetch, one prefetch (three planes uploaded on a copy stream a step "
+                    "ahead); best of two passes each"}
+
 
 def _traffic_from_profile(workload, T):
     """DRAM bytes per FFN call from the committed ncu summary, if it matches the current kernel."""
@@ -924,7 +1012,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="qwen", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(WORKLOADS),
+                    help="one workload only (default: the 32-layer sweep, with every other "
+                         "configuration as sub-runs)")
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--copies", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -933,7 +1023,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--paging", type=int, default=0,
                     help="steps of the async-paging measurement (0: skip)")
+    ap.add_argument("--sub-runs", choices=["auto", "on", "off"], default="auto",
+                    help="measure the other workloads and batch sizes beside the headline "
+                         "(auto: only when no workload is named)")
     args = ap.parse_args()
+    args.sub_runs = args.sub_runs == "on" or (args.sub_runs == "auto" and args.workload is None)
+    if args.workload is None:
+        args.workload = DEFAULT_WORKLOAD
     args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
     if args.tokens is None:
         args.tokens = WORKLOADS[args.workload][1]

@@ -14,8 +14,9 @@
  *   pw_route_topk -> pw_permute -> pw_expert_ffn_bitplane (+ pw_shared_ffn, or both
  *   in one pw_moe_ffn)
  *   -> pw_combine,   and   pw_set_expert_bitwidth.
- * pw_moe_forward runs the whole chain in one call (router plus one fused
- * persistent kernel for decode-sized batches, the separate kernels above).
+ * pw_moe_forward runs the whole chain in one call (one fused persistent
+ * kernel, router included, for decode-sized batches; the separate kernels
+ * above otherwise).
  * pw_route_stats and pw_plan_bitwidths give the signals and the per-expert
  * bitwidth plan that pw_set_expert_bitwidth then applies.
  *
@@ -79,6 +80,35 @@ pw_status pw_last_cuda_error(int* cuda_err);
  */
 pw_status pw_pool_create(void* dev_base, size_t bytes, size_t page_bytes, pw_pool_t* out);
 pw_status pw_pool_destroy(pw_pool_t pool);   /* all layers on it must be destroyed first */
+
+/*
+ * A pool whose page table is the GPU's own virtual memory (the "virtual page
+ * table" of the second write-up, section 方法与技术路线; stable virtual
+ * addresses per expert as in the third page's PagedTensor).  The caller
+ * allocates the physical pages with the CUDA driver's virtual memory
+ * management -- one cuMemCreate allocation of exactly page_bytes per page,
+ * pinned device memory on `device` -- and passes their handles
+ * (CUmemGenericAllocationHandle); the caller keeps ownership and releases
+ * them (cuMemRelease) after pw_pool_destroy.  The library allocates no
+ * physical memory: every layer on the pool reserves one virtual range
+ * (cuMemAddressReserve) with a fixed sub-range per (expert, plane) block and
+ * maps a block's pages into it (cuMemMap, cuMemSetAccess read/write for
+ * `device`) while the block holds them.  So an expert's plane addresses --
+ * and the device page table the kernels read -- never change: lowering
+ * precision still moves no data and changes no mapping; a block's pages are
+ * unmapped (cuMemUnmap) only when they are handed to another block, after
+ * the lowering's safe boundary has passed, or when the expert is reloaded or
+ * the layer destroyed (both synchronise first).  Everything else -- the
+ * hot-path calls, pw_set_expert_bitwidth, pw_prefetch_expert, CUDA graphs --
+ * works as on an ordinary pool.
+ *   handles     host array of n_pages handles (copied)
+ *   page_bytes  a multiple of 2 MiB (the allocation granularity)
+ *   device      the CUDA device the handles live on (current for the calls)
+ * PW_ERR_UNSUPPORTED when the driver offers no virtual memory management;
+ * PW_ERR_CUDA when a mapping fails (the failed call has no effect).
+ */
+pw_status pw_pool_create_vmm(const unsigned long long* handles, size_t n_pages, size_t page_bytes, int device,
+                             pw_pool_t* out);
 
 typedef struct {
   size_t total_pages, free_pages, mapped_pages, reclaimable_pages;
@@ -316,14 +346,17 @@ pw_status pw_get_expert_bitwidth(pw_layer_t layer, int e, int* bits);
 pw_status pw_workspace_size(pw_layer_t layer, int T, size_t* bytes);
 
 /*
- * The whole layer for T tokens in one call: pw_route_topk, then -- for decode
- * batches of at most 16 tokens (T also within the decode token thresholds
- * and T*K <= 512) -- one persistent kernel that permutes, runs every
- * expert's FFN and the shared FFN and combines (the permutation is never
- * written out: routed rows are read from x through the routing result);
- * otherwise pw_permute, pw_moe_ffn and pw_combine.  Both ways give the same
- * y, bit for bit, as those separate calls: every expert-FFN item is computed
- * the same way and the fused combine adds the k terms in the same order.
+ * The whole layer for T tokens in one call.  For decode batches of at most
+ * 16 tokens (T also within the decode token thresholds and T*K <= 512): one
+ * persistent kernel that routes (its CTAs share the router's sums; the last
+ * one to finish a token's sums selects its experts, and every CTA waits,
+ * bounded, until all tokens are routed), permutes, runs every expert's FFN
+ * and the shared FFN and combines (the permutation is never written out:
+ * routed rows are read from x through the routing result).  Otherwise
+ * pw_route_topk, pw_permute, pw_moe_ffn and pw_combine.  Both ways give the
+ * same idx, w and y, bit for bit, as those separate calls: the router adds
+ * its fp32 sums in one fixed order, every expert-FFN item is computed the
+ * same way and the fused combine adds the k terms in the same order.
  *   x   device fp16 [T][d]   wr device fp16 [E][d]   bias device fp32 [E] or NULL
  *   idx device int32 [T][K], w device fp32 [T][K]: the routing (outputs)
  *   y   device fp16 [T][d] (output)
@@ -434,8 +467,14 @@ pw_status pw_debug_dequant(pw_layer_t layer, int e, int m, void* out, void* stre
  * Debug: the same dump, produced by the FFN kernels' own code paths:
  *   PW_KERNEL_DECODE   the decode kernel's K loop (its cp.async ring through
  *                      the page table, 3-bit register-LUT byte permutes,
- *                      4..6-bit shared LUT table, fp16 fragments) with each
- *                      decoded A fragment written out instead of multiplied;
+ *                      4..6-bit shared-memory LUT table, fp16 fragments) with
+ *                      each decoded A fragment written out instead of
+ *                      multiplied, in the configuration this layer's FFN
+ *                      calls use;
+ *   PW_KERNEL_DECODE_ROW_TABLES, PW_KERNEL_DECODE_LANE_TABLES  the same K loop
+ *                      in a given configuration: 4..6-bit tables shared by
+ *                      the lanes of a row pair (layers with ffn < 4096), or
+ *                      one copy per lane (ffn >= 4096);
  *   PW_KERNEL_PREFILL  the tcgen05 GEMM's dequant warps (plane loads, LUT
  *                      set-up and decode) writing rows instead of the
  *                      swizzled shared-memory tile.
@@ -443,7 +482,8 @@ pw_status pw_debug_dequant(pw_layer_t layer, int e, int m, void* out, void* stre
  * write-up fixes the value: W = LUT_b[row][code6 >> (6 - b)], or the fp16
  * page at 16 bits.
  */
-enum { PW_KERNEL_DECODE = 0, PW_KERNEL_PREFILL = 1 };
+enum { PW_KERNEL_DECODE = 0, PW_KERNEL_PREFILL = 1, PW_KERNEL_DECODE_ROW_TABLES = 2,
+       PW_KERNEL_DECODE_LANE_TABLES = 3 };
 pw_status pw_debug_dequant_kernel(pw_layer_t layer, int e, int m, int kernel, void* out, void* stream);
 
 /* Debug: device address of virtual page `vpage` of expert e's plane p (p = 6: fp16 page), or 0. */
@@ -458,6 +498,15 @@ pw_status pw_debug_page_address(pw_layer_t layer, int e, int p, int vpage, uint6
  */
 pw_status pw_testing_host_sim(int enable);
 pw_status pw_testing_complete_events(void);
+
+/*
+ * Testing hook: pages mapped and unmapped so far by a virtual-memory pool
+ * (pw_pool_create_vmm).  In host-sim mode such a pool simulates the physical
+ * pages with one shared memory file and maps them with mmap, so the same
+ * bookkeeping and the bytes behind every virtual address can be checked on
+ * machines without a GPU.
+ */
+pw_status pw_testing_vmm_counts(pw_pool_t pool, uint64_t* maps, uint64_t* unmaps);
 
 /*
  * Testing hook for the bounded waits of the decode kernel: a down item waits

@@ -42,7 +42,7 @@ def pool_bytes(cfg, bits, page=2 << 20, layers=1, slack=64 << 20):
 class GpuLayer:
     """A synthetic layer uploaded to the GPU plus its host copies for the oracle."""
 
-    def __init__(self, cfg, seed=0, bits=None, with_w16=True, page=2 << 20, pool_extra=0):
+    def __init__(self, cfg, seed=0, bits=None, with_w16=True, page=2 << 20, pool_extra=0, pool=None):
         self.cfg = cfg
         self.seed = seed
         self.bits = np.array(bits if bits is not None else bits_plan(cfg, seed), dtype=np.int32)
@@ -50,8 +50,11 @@ class GpuLayer:
         self.experts = [make_expert(cfg, e, seed, with_w16=with_w16 or self.bits[e] == 16)
                         for e in range(cfg.E)]
         self.shared = make_shared(cfg, seed)
-        nb = pool_bytes(cfg, [16 if with_w16 else b for b in self.bits], page) + pool_extra
-        self.pool = pw.Pool(nb, page_bytes=page)
+        self.own_pool = pool is None
+        if pool is None:
+            nb = pool_bytes(cfg, [16 if with_w16 else b for b in self.bits], page) + pool_extra
+            pool = pw.Pool(nb, page_bytes=page)
+        self.pool = pool
         self.layer = pw.Layer(self.pool, cfg.d, cfg.f, cfg.E, cfg.K, cfg.renormalize, cfg.shared_ffn)
         for e, ex in enumerate(self.experts):
             b0 = 16 if (with_w16 and ex["w16"] is not None) else int(self.bits[e])
@@ -101,4 +104,5 @@ class GpuLayer:
 
     def close(self):
         self.layer.destroy()
-        self.pool.close()
+        if self.own_pool:
+            self.pool.close()

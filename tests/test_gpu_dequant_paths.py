@@ -4,9 +4,10 @@ Section 核心洞察 of the PagedWeight write-up fixes every weight the kernels
 use: W[r, c] = LUT_b[r][code6[r, c] >> (6 - b)] at b = 3..6 bits (the top b
 bit-planes through the page table), or the fp16 page at 16 bits.  The decode
 kernel's K loop (cp.async ring, 3-bit byte permutes from register LUTs, 4..6-bit
-shared LUT table, fp16 fragments) and the tcgen05 GEMM's dequant warps (plane
-loads, per-lane LUT table, the same decode routines) each dump the A fragments
-they produce; every value must equal the oracle's, bit for bit.
+shared LUT table in both of its configurations, fp16 fragments) and the tcgen05
+GEMM's dequant warps (plane loads, per-lane LUT table, the same decode
+routines) each dump the A fragments they produce; every value must equal the
+oracle's, bit for bit.
 
 The shapes reach every plane-group case of the stored layout: reductions of
 320, 704, 1408, 4160 and 14336 columns (full groups of four 64-column chunks
@@ -27,7 +28,7 @@ pytestmark = pytest.mark.gpu
 SHAPES = [dict(d=320, f=704), dict(d=1408, f=4160), dict(d=512, f=14336)]
 
 
-@pytest.mark.parametrize("kernel", ["decode", "prefill"])
+@pytest.mark.parametrize("kernel", ["decode_row", "decode_lane", "prefill"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"d{s['d']}_f{s['f']}")
 def test_kernel_dequant_bit_exact_every_bitwidth(shape, kernel):
     cfg = get_config("tiny", E=2, **shape)

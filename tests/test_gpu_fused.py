@@ -1,5 +1,5 @@
-"""The whole-layer call pw_moe_forward: router + one fused persistent kernel
-(permutation, every expert's FFN, the shared FFN, combine) for decode-sized
+"""The whole-layer call pw_moe_forward: one fused persistent kernel (router,
+permutation, every expert's FFN, the shared FFN, combine) for decode-sized
 batches, the separate kernels above the decode thresholds.
 
 Checks: the same routing and output, bit for bit, as the separate calls
@@ -36,6 +36,9 @@ def _both(gl, T):
      [3, 16, 3, 4, 3, 5, 16, 6, 3, 3, 16, 3], (1, 5, 16, 48, 64, 65, 130)),
     (dict(name="tiny", d=512, f=4096, E=5, K=2), [3, 4, 5, 6, 16], (1, 8, 32, 33, 70)),
     (dict(name="qwen", d=256, f=192, E=9, K=3, shared_ffn=4096), [16, 3, 6, 3, 4, 3, 5, 3, 3], (1, 12, 64)),
+    # router sums over three (d = 2816, the last one partial) and four 1024-column slices
+    (dict(name="e128", d=2816, f=256, E=128, K=8), [(3, 4, 6, 16)[e % 4] for e in range(128)], (1, 7, 16, 17)),
+    (dict(name="mixtral", d=4096, f=512, E=8, K=2), [6, 5, 4, 3, 6, 5, 4, 3], (1, 2, 16)),
 ])
 def test_fused_equals_separate(shape, bits, Ts):
     shape = dict(shape)

@@ -358,3 +358,89 @@ def test_prefetch_then_raise(sim):
     assert layer.get_expert_bitwidth(0) == 5
     layer.destroy()
     pool.close()
+
+
+# ---------------------------------------------------------------------------
+# virtual-memory pool (pw_pool_create_vmm), host-simulated: physical pages are
+# pages of one shared memory file, mapped into reserved ranges with mmap
+# ---------------------------------------------------------------------------
+
+VPAGE = 2 << 20
+
+
+def _at(addr, n):
+    return np.frombuffer(C.string_at(addr, n), dtype=np.uint8)
+
+
+def test_vmm_pool_fixed_addresses_and_mappings_only_on_reuse(sim):
+    # one resident page (the layer's tables and LUTs), 4 + 3 + 3 plane pages, 2 free
+    pool = pw.Pool.from_vmm_handles(list(range(13)), page_bytes=VPAGE)
+    layer = pw.Layer(pool, 128, 128, 4, 2, 1)
+    assert pool.vmm_counts() == (1, 0)                 # the resident run is mapped
+    ex = _expert(0)
+    _load(layer, 0, 4, ex)
+    assert pool.vmm_counts() == (5, 0)                 # one page per plane block
+    va = [layer.page_address(0, p, 0) for p in range(4)]
+    assert len(set(va)) == 4 and all(a != 0 for a in va)
+    ref = O.pack_planes(ex["code6"][0])
+    for p in range(4):
+        assert np.array_equal(_at(va[p], ref[p].nbytes).view(np.uint32), ref[p])
+    # lowering and raising move no data and change no mapping
+    layer.set_expert_bitwidth(0, 3, stream=0)
+    assert layer.try_set_expert_bitwidth(0, 4) == 0
+    layer.set_expert_bitwidth(0, 3, stream=0)
+    assert pool.vmm_counts() == (5, 0)
+    assert [layer.page_address(0, p, 0) for p in range(4)] == va
+    for e in (1, 2):
+        _load(layer, e, 3, _expert(e))
+    assert pool.stats()["free_pages"] == 2 and pool.stats()["reclaimable_pages"] == 1
+    # the reclaimable page goes to another expert only after its safe boundary,
+    # and is unmapped from expert 0's range then
+    with pytest.raises(pw.PwError):
+        _load(layer, 3, 3, _expert(3))
+    assert pool.vmm_counts() == (11, 0)
+    _lib.lib.pw_testing_complete_events()
+    _load(layer, 3, 3, _expert(3))
+    assert pool.vmm_counts() == (14, 1)
+    assert layer.page_address(0, 3, 0) == 0            # plane 3 of expert 0 is gone
+    assert layer.try_set_expert_bitwidth(0, 4) == 4    # PW_ERR_NOT_RESIDENT
+    layer.destroy()
+    assert pool.vmm_counts()[0] == pool.vmm_counts()[1]
+    assert pool.stats()["free_pages"] == 13
+    pool.close()
+
+
+def test_vmm_pool_reupload_keeps_the_block_address(sim):
+    pool = pw.Pool.from_vmm_handles(list(range(16)), page_bytes=VPAGE)
+    layer = pw.Layer(pool, 128, 128, 4, 2, 1)
+    ex = _expert(5)
+    _load(layer, 1, 5, ex)
+    va = [layer.page_address(1, p, 0) for p in range(5)]
+    layer.set_expert_bitwidth(1, 3, stream=0)          # planes 3 and 4 reclaimable
+    _lib.lib.pw_testing_complete_events()
+    for e in (0, 2, 3):                                # 12 pages: 10 free + the 2 reclaimable
+        _load(layer, e, 4, _expert(e))
+    assert layer.page_address(1, 3, 0) == 0 and layer.page_address(1, 4, 0) == 0
+    for e in (2, 3):
+        layer.set_expert_bitwidth(e, 3, stream=0)      # two pages reclaimable again
+    _lib.lib.pw_testing_complete_events()
+    packed = [pw.pack_planes(ex["code6"][m]) for m in range(3)]
+    layer.raise_expert_async(1, 5, planes=packed, stream=0, copy_stream=0)
+    assert layer.get_expert_bitwidth(1) == 5
+    assert [layer.page_address(1, p, 0) for p in range(5)] == va   # same virtual addresses
+    for p in range(5):
+        assert np.array_equal(_at(va[p], packed[0][p].nbytes).view(np.uint32), packed[0][p])
+        down = _at(va[p] + 2 * packed[0][p].nbytes, packed[2][p].nbytes).view(np.uint32)
+        assert np.array_equal(down, packed[2][p])
+    layer.destroy()
+    assert pool.vmm_counts()[0] == pool.vmm_counts()[1]
+    pool.close()
+
+
+def test_vmm_pool_checks_arguments(sim):
+    h = (C.c_ulonglong * 4)(1, 2, 3, 4)
+    out = C.c_void_p()
+    assert _lib.lib.pw_pool_create_vmm(h, 4, 64 << 10, 0, C.byref(out)) == 1   # not whole 2 MiB granules
+    assert _lib.lib.pw_pool_create_vmm(None, 4, VPAGE, 0, C.byref(out)) == 1
+    assert _lib.lib.pw_pool_create_vmm(h, 0, VPAGE, 0, C.byref(out)) == 1
+    assert _lib.lib.pw_pool_create_vmm(h, 4, VPAGE, -1, C.byref(out)) == 1

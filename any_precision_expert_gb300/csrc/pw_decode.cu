@@ -427,20 +427,21 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
         }
       }
       const int nch = W == 4 ? (cb < GR ? 4 : rem) : (cb >> 1) < GR ? 2 : min(2, rem - 2 * (cb & 1));
-      auto chunk = [&](int c) {
+      // the four mma steps of chunk c into A fragments a[s]
+      auto decode = [&](int c, uint32_t (&a)[4][4]) {
         uint32_t wc[B];
 #pragma unroll
         for (int p = 0; p < B; ++p) {
           if constexpr (B == 3) wc[p] = c == 0 ? w[p][0] : c == 1 ? w[p][1] : c == 2 ? w[p][2] : w[p][3];
           else wc[p] = lds32(slot + (p * 32 + lane) * (4 * W) + 4 * c);
         }
-        // decode the chunk's four steps first (independent chains), then the mma's
-        uint32_t a[4][4];
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3, a[s]);
           else decode_step_rt<B, Cfg<NBLK>::TSHIFT>(wc, s, src.tabl, a[s]);
         }
+      };
+      auto mma = [&](int c, const uint32_t (&a)[4][4]) {
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           if constexpr (DUMP) {
@@ -452,11 +453,30 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
           }
         }
       };
+      // decode a chunk's four steps first (independent chains), then its mma's
+      auto chunk = [&](int c) {
+        uint32_t a[4][4];
+        decode(c, a);
+        mma(c, a);
+      };
       if constexpr (B == 3) {
         // register-LUT decode is short: the unit's chunks unrolled (independent chains)
 #pragma unroll
         for (int c = 0; c < W; ++c)
           if (c < nch) chunk(c);
+      } else if constexpr (Cfg<NBLK>::LANE) {
+        // table lookups, two chunks at a time: twice the independent chains
+        // for the two resident warps per scheduler (registers allow it here)
+        int c = 0;
+#pragma unroll 1
+        for (; c + 1 < nch; c += 2) {
+          uint32_t a0[4][4], a1[4][4];
+          decode(c, a0);
+          decode(c + 1, a1);
+          mma(c, a0);
+          mma(c + 1, a1);
+        }
+        if (c < nch) chunk(c);
       } else {
         // table lookups: the chunks share one copy of the code
 #pragma unroll 1

@@ -170,10 +170,15 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
-// log2 of the columns of one staged K-block for NT token tiles: the buffer
-// holds 32 rows of 256 columns, 16 rows of 512 or 8 rows of 1024.
-__device__ __forceinline__ int kblock_log2(int NT) { return NT == 1 ? 10 : NT == 2 ? 9 : 8; }
-static_assert(Geo::SCOLS == 256, "kblock_log2 assumes 256-column K-blocks at 32 tokens");
+// log2 of the columns of one staged K-block for an item of ntok token rows:
+// the 16 KB buffer holds the rows rounded up to a power of two, from 32 rows
+// of 256 columns to one row of 8192, so items with few tokens pass few
+// K-block barriers (a 4096-column reduction at one token: none).
+__device__ __forceinline__ int kblock_log2(int ntok) {
+  const int r = ntok <= 1 ? 0 : 32 - __clz(ntok - 1);  // log2 of the rows
+  return 13 - r;
+}
+static_assert(Geo::SCOLS == 256 && Geo::HALF == 32 * 256 * 2, "kblock_log2 assumes 16 KB K-block buffers");
 
 // Byte offset of 16-byte piece j (8 columns) of token row r in a staged
 // K-block whose rows are rs bytes apart.
@@ -195,6 +200,14 @@ __device__ __forceinline__ void stage_kblock(const __half* act, const int* s_tok
 #pragma unroll 4
     for (int r = threadIdx.x >> lg; r < srows; r += rstep)
       cp_async16(buf + slab_off(r, j, kbw * 2), src + (size_t)s_tok[r] * K);
+    return;
+  }
+  if (ppr == (kbw >> 3)) {
+    // whole K-block wider than the CTA (few rows): rows one by one
+    for (int r = 0; r < srows; ++r) {
+      const __half* src = act + (size_t)s_tok[r] * K + c0;
+      for (int j = threadIdx.x; j < ppr; j += kCtaThreads) cp_async16(buf + slab_off(r, j, kbw * 2), src + j * 8);
+    }
     return;
   }
   const int n = srows * ppr;
@@ -319,7 +332,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
   using U = Unit<KIND, B, Cfg<NBLK>::RB>;
   constexpr int R = U::R;
   const int lane = threadIdx.x & 31;
-  const int lkb = kblock_log2(NT), kbw = 1 << lkb, rs = kbw * 2;
+  const int lkb = kblock_log2(ntok), kbw = 1 << lkb, rs = kbw * 2;
   const int nk = K / 64, GR = nk / 4, rem = nk % 4;
   const int nu = (K + U::COLS - 1) / U::COLS;
   const int mine = u0 < nu ? (nu - u0 + us - 1) / us : 0;

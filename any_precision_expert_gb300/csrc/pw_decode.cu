@@ -49,6 +49,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "pw_gemv.cuh"
 #include "pw_route.cuh"
 
@@ -1150,11 +1152,27 @@ cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, bool lane_tables
   return lane_tables ? launch_decode_dump_cfg<2>(L, e, m, out, s) : launch_decode_dump_cfg<3>(L, e, m, out, s);
 }
 
-// The configuration a layer's decode launches take (Cfg): per-lane LUT tables
-// for wide experts (ffn >= 4096), where 4..6-bit lookups dominate the launch,
-// otherwise three CTAs per SM.  It depends on the shape only, so every call
-// and every CUDA graph of a layer computes each item the same way.
-int nblk_for(const DevLayer& L) { return L.f >= 4096 ? 2 : 3; }
+// The configuration a layer's decode launches take (Cfg), chosen by the host
+// per call (DevLayer::nblk, decode_nblk) -- both compute every item alike,
+// so the choice only moves time.  PW_DECODE_NBLK=2 or 3 (read per call)
+// overrides it.
+int nblk_for(const DevLayer& L) {
+  const char* s = getenv("PW_DECODE_NBLK");
+  if (s && (s[0] == '2' || s[0] == '3') && s[1] == 0) return s[0] - '0';
+  return L.nblk == 2 ? 2 : 3;
+}
+
+// Measured on one GB300 (Mixtral-shaped layer, every expert at one bitwidth,
+// 64 tokens), as fractions of the HBM roofline, three CTAs / two CTAs per
+// SM: fp16 pages 0.87 / 0.82, 6 bits 0.18 / 0.25, 3 bits 0.20 / 0.17.  The
+// per-lane tables win on 4..6-bit lookups and lose a third of the resident
+// warps everywhere else; the choice compares the time each configuration
+// would take for the layer's bytes (bytes / fraction).
+int decode_nblk(double b16, double b456, double b3) {
+  const double t3 = b16 / 0.87 + b456 / 0.18 + b3 / 0.20;
+  const double t2 = b16 / 0.82 + b456 / 0.25 + b3 / 0.17;
+  return t2 < t3 ? 2 : 3;
+}
 
 template <bool FUSED, int NBLK>
 static cudaError_t launch_cta_cfg(const UniParams& P, int T, cudaStream_t s) {

@@ -60,6 +60,7 @@ struct DevLayer {
   int* sync;                            // [sync_words(E)] zero between launches
   long long spin_limit;                 // polls before a bounded wait of the decode kernel gives up
   int wait_bias;                        // testing: added to the count a down item waits for (0 normally)
+  int nblk;                             // decode-kernel configuration for this layer (nblk_for)
 };
 
 // Polls of a phase counter before the decode kernel gives up (about a second).
@@ -121,6 +122,9 @@ cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, bool lane_tables
 // Decode-kernel configuration of a layer: 2 (per-lane LUT tables, two CTAs per
 // SM) or 3 (row-pair tables, three CTAs per SM).
 int nblk_for(const DevLayer& L);
+// The configuration expected to be faster for a layer whose expert weights
+// hold b16 / b456 / b3 bytes at fp16 / 4..6 bits / 3 bits (host side).
+int decode_nblk(double b16, double b456, double b3);
 cudaError_t launch_prefill_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
 
 // Host-side checks shared by the expert-FFN entry points: validates the

@@ -395,6 +395,16 @@ struct pw_layer_s {
     L.sync = d_sync;
     L.spin_limit = spin_limit;
     L.wait_bias = wait_bias;
+    // decode-kernel configuration from the bytes the experts hold at their
+    // current bitwidths (and the fp16 shared FFN)
+    double b16 = 3.0 * desc.d * desc.shared_ffn * 2, b456 = 0, b3 = 0;
+    const double per_bit = 3.0 * desc.d * desc.ffn / 8;
+    for (int b : bits) {
+      if (b == 16) b16 += per_bit * 16;
+      else if (b >= 4) b456 += per_bit * b;
+      else if (b == 3) b3 += per_bit * 3;
+    }
+    L.nblk = decode_nblk(b16, b456, b3);
     return L;
   }
 };

@@ -65,14 +65,16 @@ def _load_json(path):
 # workload
 # ---------------------------------------------------------------------------
 
-def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda", src=None):
+def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda", src=None, vmm=False):
     """Upload n_copies of one synthetic layer; returns a dict with host copies for the oracle.
 
     src: a layer of the same shape holding this config's experts at 16 bits
     (all six planes and the fp16 page); the copies then take device copies of
     them (pw_layer_copy_expert) instead of generating and uploading from the
     host.  The sweep's source layer holds exactly the Mixtral-shaped experts
-    (same seeded codes and LUTs), so the Mixtral sub-runs are built from it."""
+    (same seeded codes and LUTs), so the Mixtral sub-runs are built from it.
+    vmm: the pool is a virtual-memory pool over physical pages this caller
+    creates (pw_pool_create_vmm), instead of one buffer."""
     import torch
 
     import any_precision_expert_gb300 as pw
@@ -92,7 +94,14 @@ def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda", src
         if b == 16:
             per_layer += (3 * cfg.d * cfg.f * 2 // page + 3) * page
     per_layer += cfg.E * (2 * cfg.f + cfg.d) * 240 + 3 * cfg.d * cfg.shared_ffn * 2 + 4 * page
-    pool = pw.Pool(n_copies * per_layer + (64 << 20), page_bytes=page, device=device)
+    nbytes = n_copies * per_layer + (64 << 20)
+    phys = None
+    if vmm:
+        from any_precision_expert_gb300.vmm import PhysicalPages
+        phys = PhysicalPages((nbytes + page - 1) // page, page, torch.cuda.current_device())
+        pool = pw.Pool.from_vmm_handles(phys.handles, page, torch.cuda.current_device())
+    else:
+        pool = pw.Pool(nbytes, page_bytes=page, device=device)
     layers = []
     for _ in range(n_copies):
         L = pw.Layer(pool, cfg.d, cfg.f, cfg.E, cfg.K, cfg.renormalize, cfg.shared_ffn)
@@ -106,7 +115,7 @@ def build_workload(cfg_name="qwen", n_copies=6, seed=0, T=64, device="cuda", src
             L.load_shared(shared)
         layers.append(L)
     wl = dict(cfg=cfg, name=cfg_name, seed=seed, bits=bits, wr=wr, bias=bias, experts=experts, shared=shared,
-              pool=pool, layers=layers, wr_d=torch.from_numpy(wr).to(device),
+              pool=pool, phys=phys, layers=layers, wr_d=torch.from_numpy(wr).to(device),
               bias_d=torch.from_numpy(bias).to(device) if bias is not None else None, bufs=None)
     set_tokens(wl, T, device)
     return wl
@@ -133,6 +142,8 @@ def free_workload(wl):
         L.destroy()
     wl["bufs"] = None
     wl["pool"].close()
+    if wl.get("phys") is not None:
+        wl["phys"].release()
 
 
 def algorithmic_bytes(cfg, bits, offsets, T):
@@ -186,17 +197,22 @@ def measure_steps(wl, K, W, stream, soak=0.0):
     cfg, layers, bufs, xs_d, T = wl["cfg"], wl["layers"], wl["bufs"], wl["xs_d"], wl["T"]
     NL = len(layers)
     fused = _fused_step(cfg, T)
+    # one router (layer copies) or one per layer (the sweep's layers)
+    per_layer = isinstance(wl["wr_d"], list)
+    wr_of = (lambda j: wl["wr_d"][j]) if per_layer else (lambda j: wl["wr_d"])
+    bias_of = (lambda j: wl["bias_d"][j]) if per_layer else (lambda j: wl["bias_d"])
+    bits_of = (lambda j: wl["bits"][j]) if per_layer else (lambda j: wl["bits"])
 
     with torch.cuda.stream(stream):
         for i in range(max(W, NL)):
             j = i % NL
-            pw.moe_forward_fused(layers[j], xs_d[j], wl["wr_d"], wl["bias_d"], bufs[j], stream=stream)
+            pw.moe_forward_fused(layers[j], xs_d[j], wr_of(j), bias_of(j), bufs[j], stream=stream)
     torch.cuda.synchronize()
     ffn_bytes, step_bytes = [], []
     for j in range(NL):
         counts = np.bincount(bufs[j].idx[:T].cpu().numpy().reshape(-1), minlength=cfg.E)
         off = np.concatenate([[0], np.cumsum(counts)])
-        fb, sb = algorithmic_bytes(cfg, wl["bits"], off, T)
+        fb, sb = algorithmic_bytes(cfg, bits_of(j), off, T)
         ffn_bytes.append(fb)
         step_bytes.append(sb)
 
@@ -209,19 +225,22 @@ def measure_steps(wl, K, W, stream, soak=0.0):
     ev_a = [mk_event() for _ in range(K)]
     ev_b = [mk_event() for _ in range(K)]
 
-    def part_a(L, b, x):
+    def part_a(j):
         if not fused:
-            L.route_topk(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, None, stream)
+            L, b, x = layers[j], bufs[j], xs_d[j]
+            L.route_topk(x, wr_of(j), bias_of(j), T, b.idx, b.w, None, stream)
             L.permute(b.idx, T, x, b.offsets, b.perm_src, b.inv_slot, b.x_perm, b.ws, stream)
 
-    def part_f(L, b, x):
+    def part_f(j):
+        L, b, x = layers[j], bufs[j], xs_d[j]
         if fused:
-            L.forward(x, wl["wr_d"], wl["bias_d"], T, b.idx, b.w, b.y, b.fws, stream)
+            L.forward(x, wr_of(j), bias_of(j), T, b.idx, b.w, b.y, b.fws, stream)
         else:
             L.moe_ffn(x, b.x_perm, b.offsets, T, b.y_perm, b.y_shared if cfg.shared_ffn else None, b.ws, stream)
 
-    def part_c(L, b, x):
+    def part_c(j):
         if not fused:
+            L, b = layers[j], bufs[j]
             L.combine(b.y_perm, b.inv_slot, b.w, T, b.y_shared if cfg.shared_ffn else None, b.y, stream)
 
     if external:
@@ -229,11 +248,11 @@ def measure_steps(wl, K, W, stream, soak=0.0):
         with torch.cuda.graph(g, stream=stream):
             for i in range(K):
                 j = i % NL
-                part_a(layers[j], bufs[j], xs_d[j])
+                part_a(j)
                 ev_a[i].record(stream)
-                part_f(layers[j], bufs[j], xs_d[j])
+                part_f(j)
                 ev_b[i].record(stream)
-                part_c(layers[j], bufs[j], xs_d[j])
+                part_c(j)
 
         def region():
             g.replay()
@@ -244,7 +263,7 @@ def measure_steps(wl, K, W, stream, soak=0.0):
             for part in (part_a, part_f, part_c):
                 gg = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gg, stream=stream):
-                    part(layers[j], bufs[j], xs_d[j])
+                    part(j)
                 trio.append(gg)
             graphs.append(trio)
 
@@ -484,9 +503,10 @@ def run_gpu(args):
 
 # The other workloads of the layer's configurations, measured in the same run
 # beside the headline: every decode batch size and prefill size they name.
-SUB_RUNS = (("mixtral", 2, (1, 8, 64, 256, 4096)),
-            ("e128", 2, (128, 8192)),
-            ("qwen", 6, (1, 8, 64, 256)))
+SUB_RUNS = (("mixtral", 2, (1, 8, 64, 256, 4096), False),
+            ("mixtral", 2, (64,), True),  # the same layer on the virtual-memory page table
+            ("e128", 2, (128, 8192), False),
+            ("qwen", 6, (1, 8, 64, 256), False))
 
 
 def sub_runs(stream, src=None, steps_decode=50, steps_prefill=10, warmup=3, paging_steps=48):
@@ -495,8 +515,8 @@ def sub_runs(stream, src=None, steps_decode=50, steps_prefill=10, warmup=3, pagi
     Qwen-shaped layer.  src: the sweep's source layer (Mixtral-shaped experts
     at 16 bits) to copy the Mixtral layers from."""
     recs = []
-    for name, copies, Ts in SUB_RUNS:
-        wl = build_workload(name, n_copies=copies, T=Ts[0], src=src if name == "mixtral" else None)
+    for name, copies, Ts, vmm in SUB_RUNS:
+        wl = build_workload(name, n_copies=copies, T=Ts[0], src=src if name == "mixtral" else None, vmm=vmm)
         cfg = wl["cfg"]
         for T in Ts:
             if T != wl["T"]:
@@ -504,7 +524,8 @@ def sub_runs(stream, src=None, steps_decode=50, steps_prefill=10, warmup=3, pagi
             prefill = T * cfg.K / cfg.E >= 256
             m = measure_steps(wl, steps_prefill if prefill else steps_decode, warmup, stream)
             roof = roofline_of(m, cfg, T)
-            recs.append({"workload": name, "tokens": T, "kind": "prefill" if prefill else "decode",
+            recs.append({"workload": name + (" (virtual-memory page table)" if vmm else ""), "tokens": T,
+                         "kind": "prefill" if prefill else "decode",
                          "value": T * m["K"] / (m["ms"] * 1e-3), "unit": "tokens/s",
                          "ms_per_step": m["ms"] / m["K"], "steps": m["K"], "layer_copies": m["NL"],
                          "timed_call": "pw_moe_forward (one fused kernel, router included)" if m["fused"] else "pw_moe_ffn",
@@ -690,6 +711,12 @@ def run_sweep(args):
     barrier()
     clk = clocks.stop()
     ms = max_over_ranks(t0.elapsed_time(t1))
+    # the dominant kernel: each layer's expert-FFN call, timed once more in a
+    # graph of the 32 layers with events around every call (bitwidths as
+    # after the last timed step)
+    fm = measure_steps(dict(cfg=cfg, layers=layers, bufs=bufs, xs_d=sw["xs_d"], T=T, wr_d=sw["wr_d"],
+                            bias_d=sw["bias_d"], bits=[np.array(c) for c in cur]), NL, 0, stream)
+    froof = roofline_of(fm, cfg, T)
     ok = all(L.check_device() == 0 for L in layers)
 
     # end to end: host inputs in, host outputs back, every layer, every step
@@ -731,10 +758,14 @@ def run_sweep(args):
                                  "one CUDA graph of the 32 layers per step, inside CUDA events on the stream",
                        "step_algorithmic_bytes": avg_bytes, "parallelism": "replicas" if ws > 1 else "single GPU",
                        "device_errors": not ok},
-            "roofline": {"kernel": "32-layer decode step (per layer: router, permutation, persistent FFN, combine)",
-                         "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "traffic": None, "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_ms": ms / K,
-                         "peak_source": peak_src},
+            "roofline": dict(froof, traffic=None,
+                             note="per layer: the expert-FFN call (one persistent decode launch over the layer's "
+                                  "8 experts), timed by CUDA events in a graph of the 32 layers"),
+            "step_roofline": {"kernel": "32-layer decode step (per layer: router, permutation, persistent FFN, "
+                                        "combine; bitwidth changes)",
+                              "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                              "algorithmic_bytes_per_step": avg_bytes, "ms_per_step": ms / K,
+                              "peak_source": peak_src},
             "cpu_baseline": cpu,
             "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": NL * T * cfg.d * 2,
                     "d2h_bytes_per_step": NL * T * cfg.d * 2, "steps": KE,

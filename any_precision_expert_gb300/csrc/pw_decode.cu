@@ -50,6 +50,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdlib>
+#include <map>
+#include <mutex>
 
 #include "pw_gemv.cuh"
 #include "pw_route.cuh"
@@ -80,6 +82,14 @@ struct Geo {
 // Measured: the second is 12% faster on experts of ffn 14336 at 64 tokens and
 // 12% slower on the Qwen-shaped layer (few 4..6-bit experts, where the
 // warps matter more); layers with ffn >= 4096 take it (nblk_for).
+//
+// NBLK = 2 places its buffers at fixed addresses of the CTA's shared-memory
+// window, so that one byte permute forms a lookup's whole address
+// (decode_step_px): the four warps' rings from the dynamic base, K-block
+// buffer 0 at 48 KB, the LUT tables at 64 KB (entry (v, warp w, lane l) at
+// 64 KB + 512 v + 256 (w / 2) + 128 (w % 2) + 4 l), K-block buffer 1 at 96 KB,
+// the window's end at 112 KB.  The kernel checks at entry that its window
+// holds this layout (kErrLayout otherwise, before anything else is touched).
 template <int NBLK>
 struct Cfg {
   static constexpr bool LANE = NBLK == 2;              // per-lane LUT tables
@@ -87,7 +97,14 @@ struct Cfg {
   static constexpr int TABW = LANE ? 64 * 32 * 4 : 64 * 8 * 4;  // LUT table of one warp (b <= 6)
   static constexpr int TSHIFT = LANE ? 7 : 5;          // log2 of the table's stride per code
   static constexpr int RB = LANE ? 10 * 1024 : 7 * 1024;  // cp.async weight ring of one warp
-  static constexpr int SMEM = 2 * Geo::HALF + kCtaWarps * (TABW + RB);
+  static constexpr int SMEM = 2 * Geo::HALF + kCtaWarps * (TABW + RB);  // NBLK = 3: one contiguous block
+  static constexpr uint32_t SLAB0 = 48 * 1024;         // NBLK = 2: fixed addresses
+  static constexpr uint32_t TAB_AT = 64 * 1024;
+  static constexpr uint32_t SDELTA = LANE ? 48 * 1024 : Geo::HALF;  // K-block buffer 1 - buffer 0
+  static constexpr uint32_t END = 112 * 1024;
+  static_assert(!LANE || (SLAB0 + Geo::HALF <= TAB_AT && TAB_AT + kCtaWarps * TABW == SLAB0 + SDELTA &&
+                          SLAB0 + SDELTA + Geo::HALF == END),
+                "fixed layout of the per-lane-table configuration");
 };
 
 // Weight units streamed by a warp (one matrix of its tile):
@@ -270,15 +287,17 @@ template <int NBLK>
 __device__ __forceinline__ void build_tab_warp(const __half* lr, int b, uint32_t tab) {
   const int V = 1 << b, lane = threadIdx.x & 31;
   if constexpr (Cfg<NBLK>::LANE) {
-    // each lane writes its own copy of rows g and g + 8, eight entries per pair of 16-byte loads
-    const int g = lane >> 2;
+    // each lane writes its own copy of rows g and g + 8, eight entries per
+    // pair of 16-byte loads, at the fixed addresses of decode_step_px
+    const int g = lane >> 2, warp = threadIdx.x >> 5;
+    const uint32_t at = Cfg<NBLK>::TAB_AT + (warp >> 1) * 256 + (warp & 1) * 128 + lane * 4;
     for (int v0 = 0; v0 < V; v0 += 8) {
       const uint4 lo = *reinterpret_cast<const uint4*>(lr + g * V + v0);
       const uint4 hi = *reinterpret_cast<const uint4*>(lr + (g + 8) * V + v0);
       const uint32_t l4[4] = {lo.x, lo.y, lo.z, lo.w}, h4[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        sts32(tab + (v0 + j) * 128 + lane * 4, prmt(l4[j >> 1], h4[j >> 1], (j & 1) ? 0x7632u : 0x5410u));
+        sts32(at + (v0 + j) * 512, prmt(l4[j >> 1], h4[j >> 1], (j & 1) ? 0x7632u : 0x5410u));
     }
   } else {
     for (int i = lane; i < V; i += 32) {  // (row pair g, run of 8 entries from v0)
@@ -319,6 +338,7 @@ struct WSrc {
   const char* p[kPlanes];  // plane tiles, or the fp16 tile in p[0]
   uint32_t lut3[2][4];     // 3 bits: register LUTs of rows g and g + 8
   uint32_t tabl;           // 4..6 bits: this lane's base in the warp's LUT table (Cfg)
+  uint32_t qbit;           // NBLK = 2: the warp's table parity (decode_step_px)
 };
 
 // K loop of one warp over the units cb = u0, u0 + us, ... of its tile (unit
@@ -377,7 +397,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
 
   // K-blocks 0 and 1 go with the first ring group
   stage_kblock(act, s_tok, ntok, K, 0, kbw, slab);
-  if (kbs > 1) stage_kblock(act, s_tok, ntok, K, 1, kbw, slab + G::HALF);
+  if (kbs > 1) stage_kblock(act, s_tok, ntok, K, 1, kbw, slab + Cfg<NBLK>::SDELTA);
   int since_stage = 0;  // groups committed after the newest staging group
 #pragma unroll
   for (int i = 0; i < R - 1; ++i) {
@@ -393,7 +413,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
       cp_wait_dyn(since_stage);  // this thread's copies of K-block kb_cur have landed
       __syncthreads();           // ... and everyone's; K-block kb_cur - 1 is no longer read
       if (kb_cur >= 1 && kb_cur + 1 < kbs) {
-        stage_kblock(act, s_tok, ntok, K, kb_cur + 1, kbw, slab + ((kb_cur + 1) & 1) * G::HALF);
+        stage_kblock(act, s_tok, ntok, K, kb_cur + 1, kbw, slab + ((kb_cur + 1) & 1) * Cfg<NBLK>::SDELTA);
         cp_commit();
         since_stage = 0;
       }
@@ -409,7 +429,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
     const int kb = (cb * U::COLS) >> lkb;
     advance_to(kb);
     cp_wait<R - 1>();  // unit cb has landed
-    const uint32_t buf = slab + (kb & 1) * G::HALF;
+    const uint32_t buf = slab + (kb & 1) * Cfg<NBLK>::SDELTA;
     const int kc0 = (cb * U::COLS) & (kbw - 1);
     const uint32_t slot = ring + (i % R) * U::SLOT;
     if constexpr (KIND == KIND_F16) {
@@ -453,6 +473,7 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           if constexpr (B == 3) decode_step_prmt3(wc, s, src.lut3, a[s]);
+          else if constexpr (Cfg<NBLK>::LANE) decode_step_px<B>(wc, s, src.qbit, src.tabl, a[s]);
           else decode_step_rt<B, Cfg<NBLK>::TSHIFT>(wc, s, src.tabl, a[s]);
         }
       };
@@ -552,7 +573,13 @@ __device__ __forceinline__ const __half* tile_src(const DevLayer& L, int e, bool
   } else {
 #pragma unroll
     for (int p = 0; p < kPlanes; ++p) src.p[p] = p < B ? tile_addr(L, e, m, p, t) : nullptr;
-    src.tabl = tab + (Cfg<NBLK>::LANE ? lane : lane >> 2) * 4;
+    if constexpr (Cfg<NBLK>::LANE) {
+      const int warp = threadIdx.x >> 5;
+      src.tabl = Cfg<NBLK>::TAB_AT + (warp & 1) * 128 + lane * 4;
+      src.qbit = (warp >> 1) ? 0x01010101u : 0u;
+    } else {
+      src.tabl = tab + (lane >> 2) * 4;
+    }
     return lut_rows(L, e, m, B, t * kTileRows);
   }
 }
@@ -638,6 +665,33 @@ __device__ __forceinline__ int down_split(int n, int K) {
 
 __device__ __forceinline__ bool is_tab(int b) { return b >= 4 && b <= 6; }
 
+// Shared-memory addresses of this warp's buffers (Cfg).  NBLK = 2 checks
+// that its fixed layout lies inside the CTA's window; false (after flagging
+// kErrLayout) when it does not.
+template <int NBLK>
+__device__ __forceinline__ bool cta_layout(const unsigned char* dyn_base, int* err, uint32_t& slab, uint32_t& tab,
+                                           uint32_t& ring) {
+  using CF = Cfg<NBLK>;
+  const int warp = threadIdx.x >> 5;
+  const uint32_t o = smem_u32(dyn_base);
+  if constexpr (CF::LANE) {
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (o + kCtaWarps * CF::RB > CF::SLAB0 || o + dyn < CF::END) {
+      if (threadIdx.x == 0) atomicExch(err, kErrLayout);
+      return false;
+    }
+    slab = CF::SLAB0;
+    tab = CF::TAB_AT;
+    ring = o + warp * CF::RB;
+  } else {
+    slab = o;
+    tab = o + 2 * Geo::HALF + warp * CF::TABW;
+    ring = o + 2 * Geo::HALF + kCtaWarps * CF::TABW + warp * CF::RB;
+  }
+  return true;
+}
+
 template <bool SPLITK, bool FUSED, int NBLK>
 __global__ void __launch_bounds__(kCtaThreads, NBLK) ffn_cta_kernel(UniParams P) {
   using G = Geo;
@@ -664,6 +718,9 @@ __global__ void __launch_bounds__(kCtaThreads, NBLK) ffn_cta_kernel(UniParams P)
   int* const q = L.sync;
   int* const done0 = L.sync + kSyncHeader;           // [E+1][kSyncChunks] gate/up tiles done
   int* const done1 = done0 + (E + 1) * kSyncChunks;  // [E+1][kSyncChunks] down tiles done
+
+  uint32_t slab, tab, ring;  // K-block buffer 0, this warp's LUT table and weight ring
+  if (!cta_layout<NBLK>(smem_uni, L.err, slab, tab, ring)) return;  // uniform: nothing touched yet
 
   const int n_slots = P.T * L.K;  // routed slots (fused step)
   if constexpr (FUSED) {
@@ -925,10 +982,6 @@ __global__ void __launch_bounds__(kCtaThreads, NBLK) ffn_cta_kernel(UniParams P)
       s_total1 = total1;
     }
   }
-  const uint32_t slab = smem_u32(smem_uni);
-  const uint32_t tab = slab + 2 * G::HALF + warp * CF::TABW;
-  const uint32_t ring = slab + 2 * G::HALF + kCtaWarps * CF::TABW + warp * CF::RB;
-
   for (;;) {
     if (tid == 0) s_it = atomicAdd(q, 1);
     __syncthreads();  // also: the previous item no longer reads shared memory
@@ -1124,9 +1177,8 @@ __global__ void __launch_bounds__(kCtaThreads) decode_dump_kernel(DevLayer L, in
   const int ntile = R / kTileRows;
   const int t = min((int)blockIdx.x * kCtaWarps + warp, ntile - 1);  // spare warps repeat the last tile unstored
   const Dump D{out, C, t * kTileRows, (int)blockIdx.x * kCtaWarps + warp < ntile};
-  const uint32_t slab = smem_u32(smem_dump);
-  const uint32_t tab = slab + 2 * Geo::HALF + warp * Cfg<NBLK>::TABW;
-  const uint32_t ring = slab + 2 * Geo::HALF + kCtaWarps * Cfg<NBLK>::TABW + warp * Cfg<NBLK>::RB;
+  uint32_t slab, tab, ring;
+  if (!cta_layout<NBLK>(smem_dump, L.err, slab, tab, ring)) return;
   switch (L.bits[e]) {
     case 16: dump_tile<16, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
     case 3: dump_tile<3, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
@@ -1138,13 +1190,47 @@ __global__ void __launch_bounds__(kCtaThreads) decode_dump_kernel(DevLayer L, in
   }
 }
 
+// Dynamic shared memory of a launch of fn in configuration NBLK: NBLK = 2
+// takes its window up to Cfg::END, the dynamic part starting after the
+// reserved and static bytes (plus 128 bytes for the base's alignment).
+template <int NBLK>
+static cudaError_t cta_smem(const void* fn, size_t& bytes) {
+  if (!Cfg<NBLK>::LANE) {
+    bytes = Cfg<NBLK>::SMEM;
+    return ensure_smem(fn, bytes);
+  }
+  static std::mutex mu;
+  static std::map<const void*, size_t> known;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = known.find(fn);
+    if (it != known.end()) {
+      bytes = it->second;
+      return ensure_smem(fn, bytes);
+    }
+  }
+  cudaFuncAttributes fa{};
+  int dev = 0, rsv = 0;
+  cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e != cudaSuccess) return e;
+  bytes = Cfg<NBLK>::END + 128 - (size_t)rsv - fa.sharedSizeBytes;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    known[fn] = bytes;
+  }
+  return ensure_smem(fn, bytes);
+}
+
 template <int NBLK>
 static cudaError_t launch_decode_dump_cfg(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {
   const int R = m < 2 ? L.f : L.d;
-  cudaError_t err = ensure_smem((const void*)decode_dump_kernel<NBLK>, Cfg<NBLK>::SMEM);
+  size_t smem = 0;
+  cudaError_t err = cta_smem<NBLK>((const void*)decode_dump_kernel<NBLK>, smem);
   if (err != cudaSuccess) return err;
   const int ntile = R / kTileRows;
-  decode_dump_kernel<NBLK><<<(ntile + kCtaWarps - 1) / kCtaWarps, kCtaThreads, Cfg<NBLK>::SMEM, s>>>(L, e, m, out);
+  decode_dump_kernel<NBLK><<<(ntile + kCtaWarps - 1) / kCtaWarps, kCtaThreads, smem, s>>>(L, e, m, out);
   return cudaGetLastError();
 }
 
@@ -1164,13 +1250,19 @@ int nblk_for(const DevLayer& L) {
 
 // Measured on one GB300 (Mixtral-shaped layer, every expert at one bitwidth,
 // 64 tokens), as fractions of the HBM roofline, three CTAs / two CTAs per
-// SM: fp16 pages 0.87 / 0.82, 6 bits 0.18 / 0.25, 3 bits 0.20 / 0.17.  The
-// per-lane tables win on 4..6-bit lookups and lose a third of the resident
-// warps everywhere else; the choice compares the time each configuration
-// would take for the layer's bytes (bytes / fraction).
-int decode_nblk(double b16, double b456, double b3) {
-  const double t3 = b16 / 0.87 + b456 / 0.18 + b3 / 0.20;
-  const double t2 = b16 / 0.82 + b456 / 0.25 + b3 / 0.17;
+// SM: fp16 pages 0.86 / 0.83, 6 bits 0.18 / 0.26, 5 bits 0.16 / 0.23, 4 bits
+// 0.14 / 0.19, 3 bits 0.20 / 0.17.  The per-lane tables win on 4..6-bit
+// lookups and lose a third of the resident warps everywhere else; the choice
+// compares the time each configuration would take for the layer's bytes
+// (bytes / fraction).  bytes: fp16, 6, 5, 4, 3 bits.
+int decode_nblk(const double (&bytes)[5]) {
+  static constexpr double f3[5] = {0.86, 0.18, 0.16, 0.14, 0.20};
+  static constexpr double f2[5] = {0.83, 0.26, 0.23, 0.19, 0.17};
+  double t3 = 0, t2 = 0;
+  for (int i = 0; i < 5; ++i) {
+    t3 += bytes[i] / f3[i];
+    t2 += bytes[i] / f2[i];
+  }
   return t2 < t3 ? 2 : 3;
 }
 
@@ -1181,11 +1273,12 @@ static cudaError_t launch_cta_cfg(const UniParams& P, int T, cudaStream_t s) {
   const bool splitk = T <= 16;
   const void* fn = splitk ? (const void*)ffn_cta_kernel<true, FUSED, NBLK>
                           : (const void*)ffn_cta_kernel<false, FUSED, NBLK>;
+  size_t smem = 0;
   cudaError_t e;
-  if ((e = ensure_smem(fn, Cfg<NBLK>::SMEM)) != cudaSuccess) return e;
+  if ((e = cta_smem<NBLK>(fn, smem)) != cudaSuccess) return e;
   const int grid = sm_count() * NBLK;
-  if (splitk) ffn_cta_kernel<true, FUSED, NBLK><<<grid, kCtaThreads, Cfg<NBLK>::SMEM, s>>>(P);
-  else ffn_cta_kernel<false, FUSED, NBLK><<<grid, kCtaThreads, Cfg<NBLK>::SMEM, s>>>(P);
+  if (splitk) ffn_cta_kernel<true, FUSED, NBLK><<<grid, kCtaThreads, smem, s>>>(P);
+  else ffn_cta_kernel<false, FUSED, NBLK><<<grid, kCtaThreads, smem, s>>>(P);
   return cudaGetLastError();
 }
 

@@ -91,6 +91,51 @@ __device__ __forceinline__ void decode_step_rt(const uint32_t (&w)[B], const int
   }
 }
 
+// 16-bit shared load at addr + OFF (OFF folded into the instruction).
+template <int OFF>
+__device__ __forceinline__ uint32_t lds16_at(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
+
+// Rotation amount r reduced to [0, 32).
+__host__ __device__ constexpr int rot_amt(int r) { return ((r % 32) + 32) % 32; }
+
+// The decode of decode_step_rt against a table at a fixed shared-memory
+// address, where one byte permute gives the whole lookup address: entry
+// (code v) of this lane sits at tb + 512 v + 256 q with tb = 0x10000 + c
+// (c < 256: the lane's byte offset, byte 1 zero) and q = 0 or 1 chosen by
+// the warp (qbit = 0 or 0x01010101).  The code words are rotated so that
+// byte k holds (code << 1) | q; prmt then replaces byte 1 of tb with it.
+template <int B>
+__device__ __forceinline__ void decode_step_px(const uint32_t (&w)[B], const int s, uint32_t qbit, uint32_t tb,
+                                               uint32_t (&a)[4]) {
+  uint32_t R[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    // q sits one bit below each byte's code field (a bit no mask selects)
+    uint32_t m = rotl_c(qbit, rot_amt(4 * h + s + 5 - B));
+#pragma unroll
+    for (int p = 0; p < B; ++p) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
+    R[h] = rotr(m, rot_amt(4 * h + s + 5 - B));
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // k = 2 * rowsel + colhalf
+    const uint32_t sel = 0x7604u | ((uint32_t)k << 4);
+    uint32_t e0, e1;
+    if (k >> 1) {
+      e0 = lds16_at<2>(prmt(R[0], tb, sel));
+      e1 = lds16_at<2>(prmt(R[1], tb, sel));
+    } else {
+      e0 = lds16_at<0>(prmt(R[0], tb, sel));
+      e1 = lds16_at<0>(prmt(R[1], tb, sel));
+    }
+    const int reg = (k == 0) ? 0 : (k == 1) ? 2 : (k == 2) ? 1 : 3;
+    a[reg] = e1 * 65536u + e0;
+  }
+}
+
 __device__ __forceinline__ void load_lut3(const __half* row, uint32_t (&r)[4]) {
   const uint4 v = *reinterpret_cast<const uint4*>(row);
   r[0] = prmt(v.x, v.y, 0x6420u);

@@ -23,6 +23,7 @@ constexpr int kErrTimeout = 1;       // a bounded wait gave up
 constexpr int kErrRouting = 2;       // an expert index outside [0, E) in a routing result
 constexpr int kErrBits = 3;          // a bitwidth word outside {3, 4, 5, 6, 16}
 constexpr int kErrOffsets = 4;       // slot offsets not monotone in [0, T*K], or a slot index out of range
+constexpr int kErrLayout = 5;        // a kernel's shared-memory window cannot hold its buffer layout
 
 #ifdef __CUDACC__
 #define PW_HD __host__ __device__
@@ -123,8 +124,8 @@ cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, bool lane_tables
 // SM) or 3 (row-pair tables, three CTAs per SM).
 int nblk_for(const DevLayer& L);
 // The configuration expected to be faster for a layer whose expert weights
-// hold b16 / b456 / b3 bytes at fp16 / 4..6 bits / 3 bits (host side).
-int decode_nblk(double b16, double b456, double b3);
+// hold bytes[0..4] at fp16 / 6 / 5 / 4 / 3 bits (host side).
+int decode_nblk(const double (&bytes)[5]);
 cudaError_t launch_prefill_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
 
 // Host-side checks shared by the expert-FFN entry points: validates the

@@ -397,14 +397,13 @@ struct pw_layer_s {
     L.wait_bias = wait_bias;
     // decode-kernel configuration from the bytes the experts hold at their
     // current bitwidths (and the fp16 shared FFN)
-    double b16 = 3.0 * desc.d * desc.shared_ffn * 2, b456 = 0, b3 = 0;
+    double by[5] = {3.0 * desc.d * desc.shared_ffn * 2, 0, 0, 0, 0};  // fp16, 6, 5, 4, 3 bits
     const double per_bit = 3.0 * desc.d * desc.ffn / 8;
     for (int b : bits) {
-      if (b == 16) b16 += per_bit * 16;
-      else if (b >= 4) b456 += per_bit * b;
-      else if (b == 3) b3 += per_bit * 3;
+      if (b == 16) by[0] += per_bit * 16;
+      else if (b >= 3 && b <= 6) by[7 - b] += per_bit * b;
     }
-    L.nblk = decode_nblk(b16, b456, b3);
+    L.nblk = decode_nblk(by);
     return L;
   }
 };

@@ -81,7 +81,15 @@ def test_graph_replays_repeat_the_eager_result():
         gl.close()
 
 
-def test_layer_output_against_oracle_mixed_bits():
+# Both decode configurations (three CTAs per SM with row-pair LUT tables; two
+# CTAs per SM with per-lane tables at fixed shared-memory addresses) compute
+# every item; the host picks one per call, PW_DECODE_NBLK forces it.
+NBLK = pytest.mark.parametrize("nblk", ["2", "3"])
+
+
+@NBLK
+def test_layer_output_against_oracle_mixed_bits(nblk, monkeypatch):
+    monkeypatch.setenv("PW_DECODE_NBLK", nblk)
     cfg = get_config("qwen", d=512, f=320, E=12, K=4, shared_ffn=768)
     gl = GpuLayer(cfg, seed=5, bits=[3, 16, 3, 4, 3, 5, 16, 6, 3, 3, 16, 3], with_w16=False)
     try:
@@ -116,11 +124,13 @@ def test_many_chunks_per_expert():
         gl.close()
 
 
+@NBLK
 @pytest.mark.parametrize("f", [4096, 4160])
-def test_split_down_reduction_all_bitwidths(f):
+def test_split_down_reduction_all_bitwidths(f, nblk, monkeypatch):
     # Down reductions of 4096 or more columns for experts with at most 16
     # tokens are shared by two (9..16 tokens) or four (1..8) warps per tile;
     # f = 4160 ends in a ragged plane group.
+    monkeypatch.setenv("PW_DECODE_NBLK", nblk)
     cfg = get_config("tiny", d=512, f=f, E=5, K=2)
     gl = GpuLayer(cfg, seed=5, bits=[3, 4, 5, 6, 16])
     try:
@@ -130,7 +140,9 @@ def test_split_down_reduction_all_bitwidths(f):
         gl.close()
 
 
-def test_odd_shapes_all_bitwidths():
+@NBLK
+def test_odd_shapes_all_bitwidths(nblk, monkeypatch):
+    monkeypatch.setenv("PW_DECODE_NBLK", nblk)
     # d = 192 (three 64-column chunks per down tile row block, 12 down tiles)
     # and f = 320 (five chunks: one whole plane group and a ragged one)
     cfg = get_config("qwen", d=192, f=320, E=5, K=2, shared_ffn=320)

@@ -4,8 +4,10 @@
 // so it runs as a grouped GEMM: each CTA owns a tile of 128 weight rows x 256
 // tokens of one expert and walks the reduction in 64-column stages.  Warp
 // roles (one CTA per SM, persistent over a device-built tile list):
-//   * dequant warps (two per 64-row slab and matrix, alternating stages) read
-//     the expert's top-b bit-planes through the page table, decode them with
+//   * dequant warps (two per 64-row slab and matrix, alternating stages) take
+//     the expert's top-b bit-planes through the page table, a plane group (4
+//     stages) at a time copied by cp.async into the pair's shared buffer one
+//     group ahead (whole 16-byte pieces: every sector is read once), decode them with
 //     the same mask/rotate + per-lane LUT scheme as the decode kernel, and
 //     write fp16 weights into shared memory in the 128-byte swizzled K-major
 //     layout; afterwards they are the epilogue (TMEM -> registers -> global);
@@ -36,6 +38,7 @@ constexpr uint32_t PF_A_BYTES = PF_BM * PF_BK * 2;  // 16 KB
 constexpr uint32_t PF_B_BYTES = PF_BN * PF_BK * 2;  // 32 KB
 constexpr int PF_BWARPS = 1;  // the TMA producer warp
 constexpr uint32_t PF_TAB_BYTES = 64 * 128;          // LUT table of one (matrix, 64-row slab), b <= 6
+constexpr uint32_t PF_PBUF_BYTES = 4 * 6 * 512;      // plane group of one warp pair's four 16-row tiles, b <= 6
 
 template <int NM>
 struct Pf {
@@ -45,8 +48,13 @@ struct Pf {
   static constexpr int THREADS = 32 * WARPS;
   static constexpr uint32_t STAGE = NM * PF_A_BYTES + PF_B_BYTES;
   static constexpr uint32_t TABS = NM * 2 * PF_TAB_BYTES;
+  // gate/up stages plane groups through a buffer per warp pair (one group in
+  // flight); down loads each stage's plane words straight into registers
+  static constexpr bool STAGED = NM == 2;
+  static constexpr int NB = 1;  // plane-group buffers per warp pair
+  static constexpr uint32_t PBUFS = STAGED ? (DQ / 2) * NB * PF_PBUF_BYTES : 0;
   static constexpr uint32_t BARS = 256;
-  static constexpr uint32_t SMEM = 1024 + NS * STAGE + TABS + BARS;
+  static constexpr uint32_t SMEM = 1024 + NS * STAGE + TABS + PBUFS + BARS;
   static constexpr uint32_t TMEM_COLS = NM == 2 ? 512 : 256;
   static constexpr uint32_t FULL_COUNT = NM * 2 + 1;  // dequant warps + the TMA producer's expect_tx
   static constexpr int PAIRS = DQ / 2;                        // warps sharing one LUT table
@@ -90,14 +98,15 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int c16) {
   return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((c16 ^ (row & 7)) << 4));
 }
 
-// Decode one 64-column stage of this lane's two rows (g, g+8 of its 16-row
-// tile) into out[s][q]: q = 0 row g cols 16s..+7, 1 row g cols 16s+8..+15,
-// 2 row g+8 cols 16s..+7, 3 row g+8 cols 16s+8..+15 (fp16 x 8 each).
-// tabl: this lane's entries in the slab's LUT table (pf_build_tab_half).
-template <int B>
-__device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint32_t tabl, uint4 (&out)[4][4]) {
+// Decode mma steps S0 .. S0 + N - 1 (16 columns each) of one 64-column stage
+// of this lane's two rows (g, g+8 of its 16-row tile) into out[s - S0][q]:
+// q = 0 row g cols 16s..+7, 1 row g cols 16s+8..+15, 2 row g+8 cols 16s..+7,
+// 3 row g+8 cols 16s+8..+15 (fp16 x 8 each).  tabl: this lane's entries in
+// the slab's LUT table (pf_build_tab_half).
+template <int B, int S0, int N>
+__device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint32_t tabl, uint4 (&out)[N][4]) {
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = S0; s < S0 + N; ++s) {
     uint32_t a[4][4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -106,31 +115,87 @@ __device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint
       for (int p = 0; p < B; ++p) wt[p] = w[t][p];
       decode_step_rt<B, 7>(wt, s, tabl, a[t]);
     }
-    out[s][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
-    out[s][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
-    out[s][2] = make_uint4(a[0][1], a[1][1], a[2][1], a[3][1]);
-    out[s][3] = make_uint4(a[0][3], a[1][3], a[2][3], a[3][3]);
+    out[s - S0][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
+    out[s - S0][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
+    out[s - S0][2] = make_uint4(a[0][1], a[1][1], a[2][1], a[3][1]);
+    out[s - S0][3] = make_uint4(a[0][3], a[1][3], a[2][3], a[3][3]);
   }
 }
 
 // 3-bit codes: byte permutes from this lane's register LUTs (rows g, g+8).
+template <int S0, int N>
 __device__ __forceinline__ void pf_decode_planes3(const uint32_t (&w)[4][3], const uint32_t (&lut3)[2][4],
-                                                  uint4 (&out)[4][4]) {
+                                                  uint4 (&out)[N][4]) {
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = S0; s < S0 + N; ++s) {
     uint32_t a[4][4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const uint32_t wt[3] = {w[t][0], w[t][1], w[t][2]};
       decode_step_prmt3(wt, s, lut3, a[t]);
     }
-    out[s][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
-    out[s][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
-    out[s][2] = make_uint4(a[0][1], a[1][1], a[2][1], a[3][1]);
-    out[s][3] = make_uint4(a[0][3], a[1][3], a[2][3], a[3][3]);
+    out[s - S0][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
+    out[s - S0][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
+    out[s - S0][2] = make_uint4(a[0][1], a[1][1], a[2][1], a[3][1]);
+    out[s - S0][3] = make_uint4(a[0][3], a[1][3], a[2][3], a[3][3]);
   }
 }
 
+// Plane groups through shared memory.  A plane group (4 stages, 256 columns)
+// of one 16-row tile and plane is 512 contiguous bytes: piece ln (16 bytes,
+// the words of stages 0..3 of fragment lane ln).  A warp pair's buffer holds
+// the group for its four tiles: block (tile tis, plane p) at 512 (6 tis + p),
+// piece ln at slot ln ^ (ln >> 3), so that the eight lanes (tis, g = 0..7)
+// of a quarter warp reading pieces 4g + t hit eight different 16-byte bank
+// groups.  Lane (tis, g) copies pieces 4g .. 4g + 3 of its own tile: one
+// 16-byte cp.async per piece for whole groups (each 32-byte sector is read
+// once by the pair, instead of once per stage and lane), word by word (zeros
+// past the end) for the ragged last group of rem < 4 words per lane.
+__device__ __forceinline__ uint32_t pf_piece(int tis, int p, int ln) {
+  return (uint32_t)((tis * 6 + p) * 512 + ((ln ^ (ln >> 3)) << 4));
+}
+
+template <int B>
+__device__ __forceinline__ void pf_copy_group(const char* const (&pb)[6], int gamma, int nk, int tis, int g,
+                                              uint32_t buf) {
+  const int G = nk / 4, rem = nk % 4;
+#pragma unroll
+  for (int p = 0; p < B; ++p)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int ln = 4 * g + t;
+      const uint32_t dst = buf + pf_piece(tis, p, ln);
+      if (gamma < G) {
+        cp_async16(dst, pb[p] + (size_t)(gamma * 128 + ln * 4) * 4);
+      } else {
+        const char* q = pb[p] + (size_t)(G * 128 + ln * rem) * 4;
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) cp_async4_n(dst + 4 * i, q + 4 * min(i, rem - 1), i < rem ? 4u : 0u);
+      }
+    }
+}
+
+// This lane's words of its two stages par and par + 2 of the group (fragment
+// lanes 4g + t of tile tis, every plane): w0 for stage par, w1 for par + 2.
+template <int B>
+__device__ __forceinline__ void pf_read_group(uint32_t buf, int par, int tis, int g, uint32_t (&w0)[4][B],
+                                              uint32_t (&w1)[4][B]) {
+#pragma unroll
+  for (int p = 0; p < B; ++p) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint4 v = lds128(buf + pf_piece(tis, p, 4 * g + t));
+      w0[t][p] = par ? v.y : v.x;
+      w1[t][p] = par ? v.w : v.z;
+    }
+    // one plane's four pieces at a time in registers
+#pragma unroll
+    for (int t = 0; t < 4; ++t) asm volatile("" ::"r"(w0[t][p]), "r"(w1[t][p]));
+  }
+}
+
+// Direct loads: the plane words of stage kb for this lane's fragment lanes
+// 4g + t of its 16-row tile (null plane: zeros).
 template <int B>
 __device__ __forceinline__ void pf_load_planes(const char* const (&pb)[6], int kb, int nk, int g,
                                                uint32_t (&w)[4][B]) {
@@ -256,7 +321,8 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = pf_raw + (base - raw);
   const uint32_t tabs = base + C::NS * C::STAGE;
-  const uint32_t bars = tabs + C::TABS;
+  const uint32_t pbufs = tabs + C::TABS;
+  const uint32_t bars = pbufs + C::PBUFS;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (C::NS + s); };
   const uint32_t acc_full = bars + 16u * C::NS;
@@ -264,8 +330,12 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
   const uint32_t fin_bar = acc_full + 16;
   const uint32_t tmem_slot = acc_full + 24;
   const uint32_t pair_bars = acc_full + 40;  // one per LUT-sharing warp pair
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (C::NS * C::STAGE + C::TABS + 16u * C::NS + 32));
-  uint32_t* tmem_slot_g = reinterpret_cast<uint32_t*>(gbase + (C::NS * C::STAGE + C::TABS + 16u * C::NS + 24));
+  // per (pair, buffer): the plane group in it has landed / the pair's first warp has read it
+  const uint32_t landed_bars = pair_bars + 8u * C::PAIRS;
+  const uint32_t read_bars = landed_bars + 8u * C::PAIRS * C::NB;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (bars - base + 16u * C::NS + 32));
+  uint32_t* tmem_slot_g = reinterpret_cast<uint32_t*>(gbase + (bars - base + 16u * C::NS + 24));
+  static_assert(16 * Pf<NM>::NS + 40 + 8 * Pf<NM>::PAIRS * (1 + 2 * Pf<NM>::NB) <= Pf<NM>::BARS, "barrier area");
 
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
@@ -276,6 +346,10 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
     mbar_init(acc_empty, C::DQ);
     mbar_init(fin_bar, 1);
     for (int i = 0; i < C::PAIRS; ++i) mbar_init(pair_bars + 8u * i, 2);
+    for (int i = 0; i < C::PAIRS * C::NB; ++i) {
+      mbar_init(landed_bars + 8u * i, 32);  // the copying warp's 32 lanes
+      mbar_init(read_bars + 8u * i, 1);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -305,7 +379,14 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
     const int tis = lane >> 3, g = lane & 7;
     const uint32_t tab = tabs + (uint32_t)(mi * 2 + slab) * PF_TAB_BYTES;
     uint32_t* tabg = reinterpret_cast<uint32_t*>(gbase + (tab - base));
-    uint32_t it = 0, tc = 0;
+    uint32_t it = 0, tc = 0, grp = 0;  // stages and tiles done, plane groups passed
+    // plane group j of the pair (counted over all its tiles) sits in buffer j % NB
+    const uint32_t pbuf0 = pbufs + (uint32_t)(warp >> 1) * C::NB * PF_PBUF_BYTES;
+    const uint32_t landed0 = landed_bars + 8u * (warp >> 1) * C::NB, readb0 = read_bars + 8u * (warp >> 1) * C::NB;
+    auto pbuf = [&](uint32_t j) { return pbuf0 + (j % C::NB) * PF_PBUF_BYTES; };
+    auto landed = [&](uint32_t j) { return landed0 + 8u * (j % C::NB); };
+    auto readb = [&](uint32_t j) { return readb0 + 8u * (j % C::NB); };
+    auto jphase = [&](uint32_t j) { return (j / C::NB) & 1; };
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const PfTile T = pf_tile(t, s_pref, s_off, E, mtiles);
@@ -331,32 +412,99 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
         fb = routed ? tile_addr(L, T.e, mm, kPlanes, tau)
                     : reinterpret_cast<const char*>(L.shared16[mm]) + (size_t)tau * 32 * K;
 
-      // this warp's stages kb = par, par + 2, ...: decode one while the plane
-      // words of the next are in flight
-      auto store_stage = [&](int kb, uint4 (&out)[4][4]) {
+      // this warp's stages kb = par, par + 2, ... (two per plane group): the
+      // pair's second warp copies each group into the pair's buffer after both
+      // have read the previous one (a group ahead of its use by the first warp)
+      // Steps S0 .. S0 + N - 1 of stage kb into its buffer: the first part
+      // waits for the buffer (after being decoded), the last one hands the
+      // stage to the MMA.
+      auto store_part = [&](int kb, auto s0c, auto& out) {
+        constexpr int S0 = decltype(s0c)::value;
+        constexpr int N = std::extent<std::remove_reference_t<decltype(out)>>::value;
         const int s = (it + kb) % C::NS;
-        const uint32_t ph = ((it + kb) / C::NS) & 1;
         if (!tile_ok) {
 #pragma unroll
-          for (int st = 0; st < 4; ++st)
+          for (int st = 0; st < N; ++st)
 #pragma unroll
             for (int q = 0; q < 4; ++q) out[st][q] = make_uint4(0, 0, 0, 0);
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err))) return false;
+        if constexpr (S0 == 0) {
+          const uint32_t ph = ((it + kb) / C::NS) & 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err))) return false;
+        }
         const uint32_t A = base + s * C::STAGE + mi * PF_A_BYTES;
 #pragma unroll
-        for (int st = 0; st < 4; ++st)
+        for (int st = 0; st < N; ++st)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int r = slab * 64 + tis * 16 + g + 8 * (q >> 1);
-            sts128(A + sw128_offset(r, 2 * st + (q & 1)), out[st][q]);
+            sts128(A + sw128_offset(r, 2 * (S0 + st) + (q & 1)), out[st][q]);
           }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar(s));
+        if constexpr (S0 + N == 4) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar(s));
+        }
         return true;
       };
-      auto plane_loop = [&](auto tag) {
+      auto store_stage = [&](int kb, uint4 (&out)[4][4]) {
+        return store_part(kb, std::integral_constant<int, 0>{}, out);
+      };
+      // gate/up: plane groups staged through the pair's buffer
+      auto plane_loop_staged = [&](auto tag) {
+        constexpr int BB = decltype(tag)::value;
+        const int ngr = (nkb + 3) / 4;
+        // The pair's second warp copies group j (into buffer j % NB) after
+        // reading group j - 1, once the first warp has read group j - NB too
+        // (the buffer's previous group): with two buffers that is the group
+        // before, so the second warp never waits on the first one's progress.
+        if (par == 1) {  // the tile's first group (its buffer's previous group was waited for)
+          if (tile_ok) pf_copy_group<BB>(pb, 0, nkb, tis, g, pbuf(grp));
+          cp_async_arrive(landed(grp));
+        }
+        for (int gm = 0; gm < ngr && ok; ++gm) {
+          uint32_t w0[4][BB], w1[4][BB];
+          ok = __all_sync(0xffffffffu, mbar_wait(landed(grp), jphase(grp), abort_flag, L.err));
+          if (!ok) break;
+          pf_read_group<BB>(pbuf(grp), par, tis, g, w0, w1);
+          // the words are in registers before the buffer may be refilled
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int p = 0; p < BB; ++p) asm volatile("" ::"r"(w0[q][p]), "r"(w1[q][p]));
+          __syncwarp();
+          if (par == 0) {
+            if (lane == 0) mbar_arrive(readb(grp));
+          } else {
+            const uint32_t prev = grp + 1 - C::NB;  // group whose buffer the next copy reuses
+            if (grp + 1 >= (uint32_t)C::NB) {
+              ok = __all_sync(0xffffffffu, mbar_wait(readb(prev), jphase(prev), abort_flag, L.err));
+              if (!ok) break;
+            }
+            if (gm + 1 < ngr) {
+              if (tile_ok) pf_copy_group<BB>(pb, gm + 1, nkb, tis, g, pbuf(grp + 1));
+              cp_async_arrive(landed(grp + 1));
+            }
+          }
+          ++grp;
+          // a stage in two halves of two mma steps (fewer live registers)
+          auto stage = [&](int kb, const uint32_t (&w)[4][BB]) {
+            uint4 o[2][4];
+            if constexpr (BB == 3) pf_decode_planes3<0, 2>(w, lut3, o);
+            else pf_decode_planes<BB, 0, 2>(w, tab + lane * 4, o);
+            if (!store_part(kb, std::integral_constant<int, 0>{}, o)) return false;
+            if constexpr (BB == 3) pf_decode_planes3<2, 2>(w, lut3, o);
+            else pf_decode_planes<BB, 2, 2>(w, tab + lane * 4, o);
+            return store_part(kb, std::integral_constant<int, 2>{}, o);
+          };
+          const int kb = 4 * gm + par;
+          if (kb < nkb) ok = stage(kb, w0);
+          if (ok && kb + 2 < nkb) ok = stage(kb + 2, w1);
+        }
+      };
+      // down: this warp's stages kb = par, par + 2, ...: decode one while the
+      // plane words of the next are in flight
+      auto plane_loop_direct = [&](auto tag) {
         constexpr int BB = decltype(tag)::value;
         uint32_t wn[4][BB];
         if (par < nkb) pf_load_planes<BB>(pb, par, nkb, g, wn);
@@ -368,10 +516,14 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
             for (int p = 0; p < BB; ++p) w[t][p] = wn[t][p];
           if (kb + 2 < nkb) pf_load_planes<BB>(pb, kb + 2, nkb, g, wn);
           uint4 out[4][4];
-          if constexpr (BB == 3) pf_decode_planes3(w, lut3, out);
-          else pf_decode_planes<BB>(w, tab + lane * 4, out);
+          if constexpr (BB == 3) pf_decode_planes3<0, 4>(w, lut3, out);
+          else pf_decode_planes<BB, 0, 4>(w, tab + lane * 4, out);
           ok = store_stage(kb, out);
         }
+      };
+      auto plane_loop = [&](auto tag) {
+        if constexpr (C::STAGED) plane_loop_staged(tag);
+        else plane_loop_direct(tag);
       };
       switch (b) {
         case 3: plane_loop(std::integral_constant<int, 3>{}); break;
@@ -427,6 +579,7 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
       if (lane == 0) mbar_arrive(acc_empty);
       ++tc;
     }
+    cp_wait<0>();  // no copy into shared memory outlives the loop (also after an abort)
   } else if (warp < C::DQ + PF_BWARPS) {
     // ---------------- activation producer: one TMA copy per stage ----------------
     if (lane == 0) {
@@ -494,7 +647,8 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
 
 // ---------------------------------------------------------------------------
 // Debug: the decoded weights of expert e's matrix m exactly as the dequant
-// warps of this kernel produce them (same LUT set-up, plane loads and decode
+// warps of this kernel produce them (same LUT set-up, plane loads -- staged
+// plane groups for gate and up, direct loads for down -- and decode
 // routines), written to out[rows][cols] instead of the swizzled A tile.  One
 // CTA per 128-row tile; warps (slab, parity) as in the kernel.
 // ---------------------------------------------------------------------------
@@ -531,15 +685,41 @@ __global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, in
         *reinterpret_cast<uint4*>(out + (size_t)r * C + c) = o[st][q];
       }
   };
+  const uint32_t pbuf = smem_u32(pfd_smem) + 2 * PF_TAB_BYTES + (uint32_t)slab * PF_PBUF_BYTES;
   auto planes = [&](auto tag) {
     constexpr int BB = decltype(tag)::value;
-    for (int kb = par; kb < nkb; kb += 2) {
-      uint32_t w[4][BB];
-      pf_load_planes<BB>(pb, kb, nkb, g, w);
+    if (m == 2) {  // down: direct loads
+      for (int kb = par; kb < nkb; kb += 2) {
+        uint32_t w[4][BB];
+        pf_load_planes<BB>(pb, kb, nkb, g, w);
+        uint4 o[4][4];
+        if constexpr (BB == 3) pf_decode_planes3<0, 4>(w, lut3, o);
+        else pf_decode_planes<BB, 0, 4>(w, tab + lane * 4, o);
+        put(kb, o);
+      }
+      return;
+    }
+    const int ngr = (nkb + 3) / 4;
+    for (int gm = 0; gm < ngr; ++gm) {  // gate / up: plane groups through the slab's buffer
+      if (par == 1 && tile_ok) pf_copy_group<BB>(pb, gm, nkb, tis, g, pbuf);
+      cp_commit();
+      cp_wait<0>();
+      __syncthreads();  // the group is in the slab's buffer
+      uint32_t w0[4][BB], w1[4][BB];
+      pf_read_group<BB>(pbuf, par, tis, g, w0, w1);
+      __syncthreads();  // both warps of the slab have read it
       uint4 o[4][4];
-      if constexpr (BB == 3) pf_decode_planes3(w, lut3, o);
-      else pf_decode_planes<BB>(w, tab + lane * 4, o);
-      put(kb, o);
+      const int kb = 4 * gm + par;
+      if (kb < nkb) {
+        if constexpr (BB == 3) pf_decode_planes3<0, 4>(w0, lut3, o);
+        else pf_decode_planes<BB, 0, 4>(w0, tab + lane * 4, o);
+        put(kb, o);
+      }
+      if (kb + 2 < nkb) {
+        if constexpr (BB == 3) pf_decode_planes3<0, 4>(w1, lut3, o);
+        else pf_decode_planes<BB, 0, 4>(w1, tab + lane * 4, o);
+        put(kb + 2, o);
+      }
     }
   };
   switch (b) {
@@ -561,7 +741,7 @@ __global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, in
 
 cudaError_t launch_prefill_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {
   const int R = m < 2 ? L.f : L.d;
-  const uint32_t smem = 2 * PF_TAB_BYTES;
+  const uint32_t smem = 2 * PF_TAB_BYTES + 2 * PF_PBUF_BYTES;
   cudaError_t err = ensure_smem((const void*)prefill_dump_kernel, smem);
   if (err != cudaSuccess) return err;
   prefill_dump_kernel<<<(R + PF_BM - 1) / PF_BM, 128, smem, s>>>(L, e, m, out);

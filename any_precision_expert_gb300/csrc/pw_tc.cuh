@@ -50,6 +50,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volati
 }
 
 // Arrive once and add `bytes` to the transaction count the phase waits for.
+// Arrive on an mbarrier once every cp.async this thread issued so far has
+// completed (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t addr) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(addr) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes) : "memory");
 }

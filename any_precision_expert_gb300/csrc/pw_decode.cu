@@ -50,8 +50,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdlib>
-#include <map>
-#include <mutex>
 
 #include "pw_gemv.cuh"
 #include "pw_route.cuh"
@@ -153,10 +151,6 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Wait until at most n (clamped to 7) of this thread's newest cp.async groups are pending.
@@ -1180,37 +1174,15 @@ __global__ void __launch_bounds__(kCtaThreads) decode_dump_kernel(DevLayer L, in
   }
 }
 
-// Dynamic shared memory of a launch of fn in configuration NBLK: NBLK = 2
-// takes its window up to Cfg::END, the dynamic part starting after the
-// reserved and static bytes (plus 128 bytes for the base's alignment).
+// Dynamic shared memory of a launch of fn in configuration NBLK (NBLK = 2:
+// its window up to Cfg::END).
 template <int NBLK>
 static cudaError_t cta_smem(const void* fn, size_t& bytes) {
   if (!Cfg<NBLK>::LANE) {
     bytes = Cfg<NBLK>::SMEM;
     return ensure_smem(fn, bytes);
   }
-  static std::mutex mu;
-  static std::map<const void*, size_t> known;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = known.find(fn);
-    if (it != known.end()) {
-      bytes = it->second;
-      return ensure_smem(fn, bytes);
-    }
-  }
-  cudaFuncAttributes fa{};
-  int dev = 0, rsv = 0;
-  cudaError_t e = cudaFuncGetAttributes(&fa, fn);
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-  if (e != cudaSuccess) return e;
-  bytes = Cfg<NBLK>::END + 128 - (size_t)rsv - fa.sharedSizeBytes;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    known[fn] = bytes;
-  }
-  return ensure_smem(fn, bytes);
+  return window_smem(fn, Cfg<NBLK>::END, bytes);
 }
 
 template <int NBLK>

@@ -75,6 +75,10 @@ struct FfnScratch {
 int sm_count();
 // Opt a kernel into `bytes` of dynamic shared memory (once per kernel and device).
 cudaError_t ensure_smem(const void* kernel, size_t bytes);
+// Dynamic shared memory for a kernel whose buffers sit at fixed addresses of
+// its CTA's shared-memory window, up to `end`: the dynamic part starts after
+// the reserved and static bytes (plus 128 for the base's alignment).
+cudaError_t window_smem(const void* kernel, uint32_t end, size_t& bytes);
 
 cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s);
 cudaError_t launch_route(const DevLayer& L, const __half* x, const __half* wr, const float* bias,

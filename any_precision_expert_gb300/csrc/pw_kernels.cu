@@ -36,6 +36,31 @@ cudaError_t ensure_smem(const void* kernel, size_t bytes) {
   return e;
 }
 
+cudaError_t window_smem(const void* kernel, uint32_t end, size_t& bytes) {
+  static std::mutex mu;
+  static std::map<const void*, size_t> known;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = known.find(kernel);
+    if (it != known.end()) {
+      bytes = it->second;
+      return ensure_smem(kernel, bytes);
+    }
+  }
+  cudaFuncAttributes fa{};
+  int dev = 0, rsv = 0;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e != cudaSuccess) return e;
+  bytes = (size_t)end + 128 - (size_t)rsv - fa.sharedSizeBytes;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    known[kernel] = bytes;
+  }
+  return ensure_smem(kernel, bytes);
+}
+
 // ---------------------------------------------------------------------------
 // bitwidth word (the stream-ordered commit of a precision change)
 // ---------------------------------------------------------------------------

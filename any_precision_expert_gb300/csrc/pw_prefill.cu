@@ -51,10 +51,19 @@ struct Pf {
   // gate/up stages plane groups through a buffer per warp pair (one group in
   // flight); down loads each stage's plane words straight into registers
   static constexpr bool STAGED = NM == 2;
+  // gate/up (FIXED) places its buffers at fixed addresses of the CTA's
+  // shared-memory window, so that one byte permute forms a LUT lookup's whole
+  // address (decode_step_px): the four LUT tables at 64 KB (entry (v, mi,
+  // slab, lane) at 64 KB + 512 v + 256 mi + 128 slab + 4 lane), the stage
+  // buffers from 96 KB to the window's end, plane-group buffers and barriers
+  // from the dynamic base below 64 KB.  The kernel checks at entry that its
+  // window holds this layout (kErrLayout otherwise).
+  static constexpr bool FIXED = NM == 2;
   static constexpr int NB = 1;  // plane-group buffers per warp pair
   static constexpr uint32_t PBUFS = STAGED ? (DQ / 2) * NB * PF_PBUF_BYTES : 0;
   static constexpr uint32_t BARS = 256;
-  static constexpr uint32_t SMEM = 1024 + NS * STAGE + TABS + PBUFS + BARS;
+  static constexpr uint32_t SMEM = 1024 + NS * STAGE + TABS + PBUFS + BARS;  // !FIXED
+  static constexpr uint32_t TAB_AT = 64 * 1024, STAGE_AT = 96 * 1024, END = STAGE_AT + NS * STAGE;  // FIXED
   static constexpr uint32_t TMEM_COLS = NM == 2 ? 512 : 256;
   static constexpr uint32_t FULL_COUNT = NM * 2 + 1;  // dequant warps + the TMA producer's expect_tx
   static constexpr int PAIRS = DQ / 2;                        // warps sharing one LUT table
@@ -103,8 +112,12 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int c16) {
 // q = 0 row g cols 16s..+7, 1 row g cols 16s+8..+15, 2 row g+8 cols 16s..+7,
 // 3 row g+8 cols 16s+8..+15 (fp16 x 8 each).  tabl: this lane's entries in
 // the slab's LUT table (pf_build_tab_half).
-template <int B, int S0, int N>
-__device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint32_t tabl, uint4 (&out)[N][4]) {
+// PX: the table at fixed addresses (tabl = 0x10000 + the lane's byte offset,
+// qbit its parity word; decode_step_px), else tabl = the lane's base address
+// and entries 128 bytes apart (decode_step_rt).
+template <int B, int S0, int N, bool PX>
+__device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint32_t tabl, uint32_t qbit,
+                                                 uint4 (&out)[N][4]) {
 #pragma unroll
   for (int s = S0; s < S0 + N; ++s) {
     uint32_t a[4][4];
@@ -113,7 +126,8 @@ __device__ __forceinline__ void pf_decode_planes(const uint32_t (&w)[4][B], uint
       uint32_t wt[B];
 #pragma unroll
       for (int p = 0; p < B; ++p) wt[p] = w[t][p];
-      decode_step_rt<B, 7>(wt, s, tabl, a[t]);
+      if constexpr (PX) decode_step_px<B>(wt, s, qbit, tabl, a[t]);
+      else decode_step_rt<B, 7>(wt, s, tabl, a[t]);
     }
     out[s - S0][0] = make_uint4(a[0][0], a[1][0], a[2][0], a[3][0]);
     out[s - S0][1] = make_uint4(a[0][2], a[1][2], a[2][2], a[3][2]);
@@ -221,17 +235,32 @@ __device__ __forceinline__ void pf_load_lut3(const DevLayer& L, int e, int mm, i
 
 // Warp `par` of a pair writes its half (codes v with v / 2^(b-1) = par) of
 // the per-lane LUT table of one 64-row slab starting at row slab0: entry (v,
-// lane lx) at word v * 32 + lx holds LUT_b[row][v] | LUT_b[row + 8][v] << 16
-// for row = slab0 + 16 (lx / 8) + lx % 8, the lane's two rows, so a warp's 32
-// lookups fall on 32 different banks (rows past R repeat the last row).
+// lane lx) at tbase + v * vstride + 4 lx holds LUT_b[row][v] | LUT_b[row +
+// 8][v] << 16 for row = slab0 + 16 (lx / 8) + lx % 8, the lane's two rows, so
+// a warp's 32 lookups fall on 32 different banks (rows past R repeat the last
+// row).  b = 4..6.
 __device__ __forceinline__ void pf_build_tab_half(const DevLayer& L, int e, int mm, int b, int slab0, int R,
-                                                  int par, uint32_t* tabg) {
-  const int lx = threadIdx.x & 31, V = 1 << b;
+                                                  int par, uint32_t tbase, uint32_t vstride) {
+  const int lx = threadIdx.x & 31, half = 1 << (b - 1);
   const int row = slab0 + (lx >> 3) * 16 + (lx & 7);
-  const __half* l0 = lut_rows(L, e, mm, b, min(row, R - 1));
-  const __half* l1 = lut_rows(L, e, mm, b, min(row + 8, R - 1));
-  for (int v = par * (V >> 1); v < (par + 1) * (V >> 1); ++v)
-    tabg[v * 32 + lx] = (uint32_t)__half_as_ushort(l0[v]) | ((uint32_t)__half_as_ushort(l1[v]) << 16);
+  const uint4* q0 = reinterpret_cast<const uint4*>(lut_rows(L, e, mm, b, min(row, R - 1)) + par * half);
+  const uint4* q1 = reinterpret_cast<const uint4*>(lut_rows(L, e, mm, b, min(row + 8, R - 1)) + par * half);
+  uint4 lo[4], hi[4];  // the lane's half of both rows, loaded at once (8 entries per 16 bytes)
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (i < (half >> 3)) {
+      lo[i] = __ldg(q0 + i);
+      hi[i] = __ldg(q1 + i);
+    }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (i < (half >> 3)) {
+      const uint32_t l4[4] = {lo[i].x, lo[i].y, lo[i].z, lo[i].w}, h4[4] = {hi[i].x, hi[i].y, hi[i].z, hi[i].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        sts32(tbase + (uint32_t)(par * half + 8 * i + j) * vstride + lx * 4,
+              prmt(l4[j >> 1], h4[j >> 1], (j & 1) ? 0x7632u : 0x5410u));
+    }
 }
 
 // fp16 page: stage kb of this lane's rows, gathered from the four fragment
@@ -318,11 +347,26 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
 
   // shared memory carve-up (stage buffers 1024-byte aligned for the swizzle)
   const uint32_t raw = smem_u32(pf_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  unsigned char* gbase = pf_raw + (base - raw);
-  const uint32_t tabs = base + C::NS * C::STAGE;
-  const uint32_t pbufs = tabs + C::TABS;
-  const uint32_t bars = pbufs + C::PBUFS;
+  uint32_t base, tabs, pbufs, bars;
+  if constexpr (C::FIXED) {
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uint32_t o = (raw + 127u) & ~127u;
+    if (o + C::PBUFS + C::BARS > C::TAB_AT || raw + dyn < C::END) {  // uniform; nothing touched yet
+      if (tid == 0) atomicExch(L.err, kErrLayout);
+      return;
+    }
+    pbufs = o;
+    bars = o + C::PBUFS;
+    tabs = C::TAB_AT;
+    base = C::STAGE_AT;
+  } else {
+    base = (raw + 1023u) & ~1023u;
+    tabs = base + C::NS * C::STAGE;
+    pbufs = tabs + C::TABS;
+    bars = pbufs + C::PBUFS;
+  }
+  auto gptr = [&](uint32_t a) { return pf_raw + (a - raw); };  // generic pointer of a shared address
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (C::NS + s); };
   const uint32_t acc_full = bars + 16u * C::NS;
@@ -333,8 +377,8 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
   // per (pair, buffer): the plane group in it has landed / the pair's first warp has read it
   const uint32_t landed_bars = pair_bars + 8u * C::PAIRS;
   const uint32_t read_bars = landed_bars + 8u * C::PAIRS * C::NB;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (bars - base + 16u * C::NS + 32));
-  uint32_t* tmem_slot_g = reinterpret_cast<uint32_t*>(gbase + (bars - base + 16u * C::NS + 24));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gptr(bars + 16u * C::NS + 32));
+  uint32_t* tmem_slot_g = reinterpret_cast<uint32_t*>(gptr(bars + 16u * C::NS + 24));
   static_assert(16 * Pf<NM>::NS + 40 + 8 * Pf<NM>::PAIRS * (1 + 2 * Pf<NM>::NB) <= Pf<NM>::BARS, "barrier area");
 
   if (tid == 0) {
@@ -377,8 +421,12 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
       return r;
     };
     const int tis = lane >> 3, g = lane & 7;
-    const uint32_t tab = tabs + (uint32_t)(mi * 2 + slab) * PF_TAB_BYTES;
-    uint32_t* tabg = reinterpret_cast<uint32_t*>(gbase + (tab - base));
+    // this warp's LUT table: where its pair writes entry v of lane lx (tbase +
+    // v vstride + 4 lx) and the lane's lookup base (tabl) and parity (qbit)
+    const uint32_t tbase = C::FIXED ? C::TAB_AT + 256u * mi + 128u * slab : tabs + (uint32_t)(mi * 2 + slab) * PF_TAB_BYTES;
+    const uint32_t vstride = C::FIXED ? 512u : 128u;
+    const uint32_t tabl = C::FIXED ? 0x10000u + 128u * slab + 4u * lane : tbase + 4u * lane;
+    const uint32_t qbit = C::FIXED && mi ? 0x01010101u : 0u;
     uint32_t it = 0, tc = 0, grp = 0;  // stages and tiles done, plane groups passed
     // plane group j of the pair (counted over all its tiles) sits in buffer j % NB
     const uint32_t pbuf0 = pbufs + (uint32_t)(warp >> 1) * C::NB * PF_PBUF_BYTES;
@@ -400,7 +448,7 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
       } else if (b <= 6) {
         ok = pair_sync();  // both warps of the pair finished the previous tile
         if (!ok) break;
-        pf_build_tab_half(L, T.e, mm, b, T.mt * PF_BM + slab * 64, R, par, tabg);
+        pf_build_tab_half(L, T.e, mm, b, T.mt * PF_BM + slab * 64, R, par, tbase, vstride);
         ok = pair_sync();
         if (!ok) break;
       }
@@ -491,10 +539,10 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
           auto stage = [&](int kb, const uint32_t (&w)[4][BB]) {
             uint4 o[2][4];
             if constexpr (BB == 3) pf_decode_planes3<0, 2>(w, lut3, o);
-            else pf_decode_planes<BB, 0, 2>(w, tab + lane * 4, o);
+            else pf_decode_planes<BB, 0, 2, C::FIXED>(w, tabl, qbit, o);
             if (!store_part(kb, std::integral_constant<int, 0>{}, o)) return false;
             if constexpr (BB == 3) pf_decode_planes3<2, 2>(w, lut3, o);
-            else pf_decode_planes<BB, 2, 2>(w, tab + lane * 4, o);
+            else pf_decode_planes<BB, 2, 2, C::FIXED>(w, tabl, qbit, o);
             return store_part(kb, std::integral_constant<int, 2>{}, o);
           };
           const int kb = 4 * gm + par;
@@ -517,7 +565,7 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
           if (kb + 2 < nkb) pf_load_planes<BB>(pb, kb + 2, nkb, g, wn);
           uint4 out[4][4];
           if constexpr (BB == 3) pf_decode_planes3<0, 4>(w, lut3, out);
-          else pf_decode_planes<BB, 0, 4>(w, tab + lane * 4, out);
+          else pf_decode_planes<BB, 0, 4, C::FIXED>(w, tabl, qbit, out);
           ok = store_stage(kb, out);
         }
       };
@@ -662,13 +710,27 @@ __global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, in
   const bool tile_ok = row0 < R;
   const int tau = row0 / 16;
   const int b = L.bits[e];
-  uint32_t* tabg = reinterpret_cast<uint32_t*>(pfd_smem) + slab * (PF_TAB_BYTES / 4);
-  const uint32_t tab = smem_u32(tabg);
+  // shared memory: the down kernel's tables (2 x 8 KB) and the slabs' plane-group
+  // buffers from the dynamic base, the gate/up kernel's fixed tables at 64 KB
+  const uint32_t raw = smem_u32(pfd_smem);
+  {
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (raw + 2 * PF_TAB_BYTES + 2 * PF_PBUF_BYTES > Pf<2>::TAB_AT || raw + dyn < Pf<2>::TAB_AT + 32 * 1024) {
+      if (threadIdx.x == 0) atomicExch(L.err, kErrLayout);
+      return;
+    }
+  }
+  const bool px = m < 2;  // gate / up: the fixed layout of ffn_prefill_kernel<2>
+  const uint32_t tbase = px ? Pf<2>::TAB_AT + 256u * m + 128u * slab : raw + (uint32_t)slab * PF_TAB_BYTES;
+  const uint32_t vstride = px ? 512u : 128u;
+  const uint32_t tabl = px ? 0x10000u + 128u * slab + 4u * lane : tbase + 4u * lane;
+  const uint32_t qbit = px && m ? 0x01010101u : 0u;
   uint32_t lut3[2][4] = {};
   if (b == 3) {
     pf_load_lut3(L, e, m, row0, g, R, lut3);
   } else if (b >= 4 && b <= 6) {
-    pf_build_tab_half(L, e, m, b, blockIdx.x * PF_BM + slab * 64, R, par, tabg);
+    pf_build_tab_half(L, e, m, b, blockIdx.x * PF_BM + slab * 64, R, par, tbase, vstride);
     __syncthreads();  // b is the same for the whole CTA
   }
   const char* pb[6];
@@ -685,7 +747,7 @@ __global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, in
         *reinterpret_cast<uint4*>(out + (size_t)r * C + c) = o[st][q];
       }
   };
-  const uint32_t pbuf = smem_u32(pfd_smem) + 2 * PF_TAB_BYTES + (uint32_t)slab * PF_PBUF_BYTES;
+  const uint32_t pbuf = raw + 2 * PF_TAB_BYTES + (uint32_t)slab * PF_PBUF_BYTES;
   auto planes = [&](auto tag) {
     constexpr int BB = decltype(tag)::value;
     if (m == 2) {  // down: direct loads
@@ -694,7 +756,7 @@ __global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, in
         pf_load_planes<BB>(pb, kb, nkb, g, w);
         uint4 o[4][4];
         if constexpr (BB == 3) pf_decode_planes3<0, 4>(w, lut3, o);
-        else pf_decode_planes<BB, 0, 4>(w, tab + lane * 4, o);
+        else pf_decode_planes<BB, 0, 4, false>(w, tabl, qbit, o);
         put(kb, o);
       }
       return;
@@ -712,12 +774,12 @@ __global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, in
       const int kb = 4 * gm + par;
       if (kb < nkb) {
         if constexpr (BB == 3) pf_decode_planes3<0, 4>(w0, lut3, o);
-        else pf_decode_planes<BB, 0, 4>(w0, tab + lane * 4, o);
+        else pf_decode_planes<BB, 0, 4, true>(w0, tabl, qbit, o);
         put(kb, o);
       }
       if (kb + 2 < nkb) {
         if constexpr (BB == 3) pf_decode_planes3<0, 4>(w1, lut3, o);
-        else pf_decode_planes<BB, 0, 4>(w1, tab + lane * 4, o);
+        else pf_decode_planes<BB, 0, 4, true>(w1, tabl, qbit, o);
         put(kb + 2, o);
       }
     }
@@ -741,8 +803,8 @@ __global__ void __launch_bounds__(128) prefill_dump_kernel(DevLayer L, int e, in
 
 cudaError_t launch_prefill_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s) {
   const int R = m < 2 ? L.f : L.d;
-  const uint32_t smem = 2 * PF_TAB_BYTES + 2 * PF_PBUF_BYTES;
-  cudaError_t err = ensure_smem((const void*)prefill_dump_kernel, smem);
+  size_t smem = 0;
+  cudaError_t err = window_smem((const void*)prefill_dump_kernel, Pf<2>::TAB_AT + 32 * 1024, smem);
   if (err != cudaSuccess) return err;
   prefill_dump_kernel<<<(R + PF_BM - 1) / PF_BM, 128, smem, s>>>(L, e, m, out);
   return cudaGetLastError();
@@ -818,9 +880,10 @@ cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half*
   const int grid = sm_count();
   cudaError_t e;
   if (phase == 0) {
-    e = ensure_smem((const void*)ffn_prefill_kernel<2>, Pf<2>::SMEM);
+    size_t smem = 0;
+    e = window_smem((const void*)ffn_prefill_kernel<2>, Pf<2>::END, smem);
     if (e != cudaSuccess) return e;
-    ffn_prefill_kernel<2><<<grid, Pf<2>::THREADS, Pf<2>::SMEM, s>>>(Q, map);
+    ffn_prefill_kernel<2><<<grid, Pf<2>::THREADS, smem, s>>>(Q, map);
   } else {
     e = ensure_smem((const void*)ffn_prefill_kernel<1>, Pf<1>::SMEM);
     if (e != cudaSuccess) return e;

@@ -508,6 +508,119 @@ __device__ __forceinline__ void kloop(const WSrc& src, int K, int NT, int ntok, 
   cp_wait<0>();
 }
 
+// K loop of one warp over two 16-row tiles of 3-bit codes at once (wide
+// gate/up items of the per-lane-table configuration): the ring holds both
+// tiles' plane groups side by side, so the tiles share every staged K-block
+// and every B fragment, and each chunk decodes two independent tiles.  Same
+// staging, ring discipline and decode (byte permutes from register LUTs) as
+// kloop; DUMP writes both tiles' A fragments instead of feeding the mma.
+template <int NBLK, bool DUMP = false>
+__device__ __forceinline__ void kloop3w(const WSrc (&src)[2], int K, int NT, int ntok, uint32_t ring, uint32_t slab,
+                                        const __half* act, const int* s_tok, float (&acc)[2][Geo::NTM][4],
+                                        const Dump* dump = nullptr) {
+  using G = Geo;
+  constexpr int SLOT = 2 * 3 * 16 * 32;  // both tiles' three planes, 16 bytes per lane each
+  constexpr int R = Cfg<NBLK>::RB / SLOT > 8 ? 8 : Cfg<NBLK>::RB / SLOT;
+  static_assert(R >= 3, "ring too shallow");
+  const int lane = threadIdx.x & 31;
+  const int lkb = kblock_log2(ntok), kbw = 1 << lkb, rs = kbw * 2;
+  const int nk = K / 64, GR = nk / 4, rem = nk % 4;
+  const int nu = (K + 255) / 256;
+  const int kbs = (K + kbw - 1) / kbw;
+  const BRows br = slab_brows(ntok, rs);
+
+  auto issue = [&](int cb) {
+    const uint32_t slot = ring + (cb % R) * SLOT;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (cb < GR) {
+        const size_t off = (size_t)(cb * 128 + lane * 4) * 4;
+#pragma unroll
+        for (int p = 0; p < 3; ++p) cp_async16(slot + ((j * 3 + p) * 32 + lane) * 16, src[j].p[p] + off);
+      } else {
+        const size_t off = (size_t)(GR * 128 + lane * rem) * 4;
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+          for (int k = 0; k < rem; ++k)
+            cp_async4(slot + ((j * 3 + p) * 32 + lane) * 16 + 4 * k, src[j].p[p] + off + 4 * k);
+      }
+    }
+  };
+
+  stage_kblock(act, s_tok, ntok, K, 0, kbw, slab);
+  if (kbs > 1) stage_kblock(act, s_tok, ntok, K, 1, kbw, slab + Cfg<NBLK>::SDELTA);
+  int since_stage = 0;
+#pragma unroll
+  for (int i = 0; i < R - 1; ++i) {
+    if (i < nu) issue(i);
+    cp_commit();
+    if (i > 0) ++since_stage;
+  }
+  int kb_cur = -1;
+  auto advance_to = [&](int kb) {
+    while (kb_cur < kb) {
+      ++kb_cur;
+      cp_wait_dyn(since_stage);
+      __syncthreads();
+      if (kb_cur >= 1 && kb_cur + 1 < kbs) {
+        stage_kblock(act, s_tok, ntok, K, kb_cur + 1, kbw, slab + ((kb_cur + 1) & 1) * Cfg<NBLK>::SDELTA);
+        cp_commit();
+        since_stage = 0;
+      }
+    }
+  };
+
+#pragma unroll 1
+  for (int cb = 0; cb < nu; ++cb) {
+    if (cb + R - 1 < nu) issue(cb + R - 1);
+    cp_commit();
+    ++since_stage;
+    const int kb = (cb * 256) >> lkb;
+    advance_to(kb);
+    cp_wait<R - 1>();  // unit cb has landed
+    const uint32_t buf = slab + (kb & 1) * Cfg<NBLK>::SDELTA;
+    const int kc0 = (cb * 256) & (kbw - 1);
+    const uint32_t slot = ring + (cb % R) * SLOT;
+    uint32_t w[2][3][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int p = 0; p < 3; ++p) {
+        const uint4 v = lds128(slot + ((j * 3 + p) * 32 + lane) * 16);
+        w[j][p][0] = v.x;
+        w[j][p][1] = v.y;
+        w[j][p][2] = v.z;
+        w[j][p][3] = v.w;
+      }
+    const int nch = cb < GR ? 4 : rem;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (c >= nch) break;
+      uint32_t a[2][4][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t wc[3] = {w[j][0][c], w[j][1][c], w[j][2][c]};
+#pragma unroll
+        for (int s = 0; s < 4; ++s) decode_step_prmt3(wc, s, src[j].lut3, a[j][s]);
+      }
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        if constexpr (DUMP) {
+          dump_frag(dump[0], a[0][s], (kb << lkb) + kc0 + c * 64 + 16 * s);
+          dump_frag(dump[1], a[1][s], (kb << lkb) + kc0 + c * 64 + 16 * s);
+        } else {
+          uint32_t bf[G::NTM][2];
+          slab_bstep(buf, kc0 + c * 64, s, NT, br, bf);
+          mma_tiles(acc[0], a[0][s], bf, NT);
+          mma_tiles(acc[1], a[1][s], bf, NT);
+        }
+      }
+    }
+  }
+  advance_to(kbs - 1);
+  cp_wait<0>();
+}
+
 // Epilogue of one tile: C fragment element (row g / g+8, token nt*8 + 2t + {0,1}).
 // Gate/up: h = silu(gate) * up in fp16; down: y in fp32.
 __device__ __forceinline__ void tile_store_h(const float (&gt)[Geo::NTM][4], const float (&up)[Geo::NTM][4], int tau,
@@ -634,6 +747,53 @@ __device__ __forceinline__ void block_item(const DevLayer& L, const ItemArgs& A,
     for (int k = 0; k < S; ++k) add(up, 2 + warp + k);
     tile_store_h(acc, up, t, A.row0, A.ntok, A.ld, A.h);
   }
+}
+
+// Wide gate/up item of 3-bit codes (per-lane-table configuration): tiles
+// tau .. tau + 3; warp q = 0, 1 streams the gate rows of tiles tau + 2q and
+// tau + 2q + 1 (kloop3w), warps 2-3 their up rows; up sums reach the gate
+// warps through shared memory for SwiGLU.
+template <int NBLK>
+__device__ __forceinline__ void block_item3w(const DevLayer& L, const ItemArgs& A, int tau, uint32_t ring,
+                                             uint32_t slab, const int* s_tok) {
+  constexpr int kNT = Geo::NTM;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = warp >> 1, t0 = tau + 2 * (warp & 1);
+  WSrc src[2];
+  tile_src<3, NBLK>(L, A.e, A.sh, m, t0, A.K, 0, src[0]);
+  tile_src<3, NBLK>(L, A.e, A.sh, m, t0 + 1, A.K, 0, src[1]);
+  float acc[2][kNT][4] = {};
+  kloop3w<NBLK>(src, A.K, A.NT, A.ntok, ring, slab, A.act, s_tok, acc);
+  __syncthreads();  // the staged rows are no longer read
+  float4* red = reinterpret_cast<float4*>(__cvta_shared_to_generic(slab));
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+      red[((warp * 2 + j) * kNT + nt) * 32 + lane] =
+          make_float4(acc[j][nt][0], acc[j][nt][1], acc[j][nt][2], acc[j][nt][3]);
+  __syncthreads();
+  if (m == 1) return;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float up[kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      const float4 v = red[(((2 + warp) * 2 + j) * kNT + nt) * 32 + lane];
+      up[nt][0] = v.x;
+      up[nt][1] = v.y;
+      up[nt][2] = v.z;
+      up[nt][3] = v.w;
+    }
+    tile_store_h(acc[j], up, t0 + j, A.row0, A.ntok, A.ld, A.h);
+  }
+}
+
+// Gate/up items of a 3-bit group are wide (four tiles) in the per-lane-table
+// configuration when the group's tiles come in fours.
+template <int NBLK>
+__device__ __forceinline__ bool wide3(int b, int tiles) {
+  return Cfg<NBLK>::LANE && b == 3 && (tiles & 3) == 0;
 }
 
 // Warps sharing one down tile for a group of n tokens with reduction length
@@ -895,7 +1055,8 @@ __global__ void __launch_bounds__(kCtaThreads, NBLK) ffn_cta_kernel(UniParams P)
           const int g = s_ord[k];
           const int fe = g == E ? L.fs : L.f;
           const int tiles = ph == 0 ? fe / kTileRows : L.d / kTileRows;
-          const int per_item = ph == 0 ? 2 : kCtaWarps / down_split<SPLITK>(s_n[g], fe);
+          const int per_item = ph == 0 ? (wide3<NBLK>(s_b[g], tiles) ? 4 : 2)
+                                       : kCtaWarps / down_split<SPLITK>(s_n[g], fe);
           c = ((s_n[g] + G::TOK - 1) / G::TOK) * (tiles / per_item);
         }
         int incl = c;
@@ -996,7 +1157,8 @@ __global__ void __launch_bounds__(kCtaThreads, NBLK) ffn_cta_kernel(UniParams P)
     const int tiles = phase == 0 ? fe / kTileRows : L.d / kTileRows;
     const int sidx = g * kSyncChunks + chunk;
     const int S = phase == 0 ? 1 : down_split<SPLITK>(n, fe);  // warps per tile
-    const int per_item = phase == 0 ? 2 : kCtaWarps / S;  // tiles of one item
+    const bool wide = phase == 0 && wide3<NBLK>(b, tiles);
+    const int per_item = phase == 0 ? (wide ? 4 : 2) : kCtaWarps / S;  // tiles of one item
 
     ItemArgs A;
     A.e = g;
@@ -1032,7 +1194,15 @@ __global__ void __launch_bounds__(kCtaThreads, NBLK) ffn_cta_kernel(UniParams P)
     const int NM = phase == 0 ? 2 : 1;
     switch (b) {
       case 16: block_item<16, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
-      case 3: block_item<3, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
+      case 3:
+        if constexpr (CF::LANE) {
+          if (wide) {
+            block_item3w<NBLK>(L, A, tau, ring, slab, s_tok);
+            break;
+          }
+        }
+        block_item<3, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok);
+        break;
       case 4: block_item<4, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
       case 5: block_item<5, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
       default: block_item<6, NBLK>(L, A, NM, S, tau, ring, slab, tab, s_tok); break;
@@ -1163,6 +1333,20 @@ __global__ void __launch_bounds__(kCtaThreads) decode_dump_kernel(DevLayer L, in
   const Dump D{out, C, t * kTileRows, (int)blockIdx.x * kCtaWarps + warp < ntile};
   uint32_t slab, tab, ring;
   if (!cta_layout<NBLK>(smem_dump, L.err, slab, tab, ring)) return;
+  if constexpr (Cfg<NBLK>::LANE) {
+   if (m < 2 && L.bits[e] == 3 && wide3<NBLK>(3, ntile)) {
+    // gate / up at 3 bits: the wide items' two-tile K loop, warp pair index
+    // blockIdx.x * 4 + warp (tiles 2i, 2i + 1; spare warps repeat the last pair unstored)
+    const int i = (int)blockIdx.x * kCtaWarps + warp, t0 = min(2 * i, ntile - 2);
+    const Dump D2[2] = {{out, C, t0 * kTileRows, 2 * i < ntile}, {out, C, (t0 + 1) * kTileRows, 2 * i < ntile}};
+    WSrc src[2];
+    tile_src<3, NBLK>(L, e, false, m, t0, C, tab, src[0]);
+    tile_src<3, NBLK>(L, e, false, m, t0 + 1, C, tab, src[1]);
+    float acc[2][Geo::NTM][4] = {};
+    kloop3w<NBLK, true>(src, C, 1, 0, ring, slab, out, s_tok, acc, D2);
+    return;
+   }
+  }
   switch (L.bits[e]) {
     case 16: dump_tile<16, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
     case 3: dump_tile<3, NBLK>(L, e, m, t, C, ring, slab, tab, s_tok, D); break;
@@ -1213,13 +1397,14 @@ int nblk_for(const DevLayer& L) {
 // Measured on one GB300 (Mixtral-shaped layer, every expert at one bitwidth,
 // 64 tokens), as fractions of the HBM roofline, three CTAs / two CTAs per
 // SM: fp16 pages 0.86 / 0.83, 6 bits 0.18 / 0.26, 5 bits 0.16 / 0.23, 4 bits
-// 0.14 / 0.19, 3 bits 0.20 / 0.17.  The per-lane tables win on 4..6-bit
-// lookups and lose a third of the resident warps everywhere else; the choice
+// 0.14 / 0.19, 3 bits 0.20 / 0.20 (wide 3-bit items in the second).  The
+// per-lane tables win on 4..6-bit lookups and lose a third of the resident
+// warps everywhere else; the choice
 // compares the time each configuration would take for the layer's bytes
 // (bytes / fraction).  bytes: fp16, 6, 5, 4, 3 bits.
 int decode_nblk(const double (&bytes)[5]) {
   static constexpr double f3[5] = {0.86, 0.18, 0.16, 0.14, 0.20};
-  static constexpr double f2[5] = {0.83, 0.26, 0.23, 0.19, 0.17};
+  static constexpr double f2[5] = {0.83, 0.26, 0.23, 0.19, 0.20};
   double t3 = 0, t2 = 0;
   for (int i = 0; i < 5; ++i) {
     t3 += bytes[i] / f3[i];

@@ -1399,10 +1399,14 @@ int nblk_for(const DevLayer& L) {
 // SM: fp16 pages 0.86 / 0.83, 6 bits 0.18 / 0.26, 5 bits 0.16 / 0.23, 4 bits
 // 0.14 / 0.19, 3 bits 0.20 / 0.20 (wide 3-bit items in the second).  The
 // per-lane tables win on 4..6-bit lookups and lose a third of the resident
-// warps everywhere else; the choice
-// compares the time each configuration would take for the layer's bytes
-// (bytes / fraction).  bytes: fp16, 6, 5, 4, 3 bits.
-int decode_nblk(const double (&bytes)[5]) {
+// warps everywhere else; for a layer with experts of ffn >= 4096 rows the
+// choice compares the time each configuration would take for the layer's
+// bytes (bytes / fraction; bytes: fp16, 6, 5, 4, 3 bits).  Narrower experts
+// get few tokens each and short items, where the resident warps matter
+// more: measured, two CTAs per SM cost the Qwen-shaped layer (ffn 1408) 11%
+// at 64 tokens and tie on the 128-expert one (ffn 704), so those take three.
+int decode_nblk(const double (&bytes)[5], int ffn) {
+  if (ffn < 4096) return 3;
   static constexpr double f3[5] = {0.86, 0.18, 0.16, 0.14, 0.20};
   static constexpr double f2[5] = {0.83, 0.26, 0.23, 0.19, 0.20};
   double t3 = 0, t2 = 0;

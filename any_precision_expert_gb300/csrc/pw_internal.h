@@ -128,8 +128,8 @@ cudaError_t launch_decode_dump(const DevLayer& L, int e, int m, bool lane_tables
 // SM) or 3 (row-pair tables, three CTAs per SM).
 int nblk_for(const DevLayer& L);
 // The configuration expected to be faster for a layer whose expert weights
-// hold bytes[0..4] at fp16 / 6 / 5 / 4 / 3 bits (host side).
-int decode_nblk(const double (&bytes)[5]);
+// hold bytes[0..4] at fp16 / 6 / 5 / 4 / 3 bits, experts of ffn rows (host side).
+int decode_nblk(const double (&bytes)[5], int ffn);
 cudaError_t launch_prefill_dump(const DevLayer& L, int e, int m, __half* out, cudaStream_t s);
 
 // Host-side checks shared by the expert-FFN entry points: validates the

@@ -403,7 +403,7 @@ struct pw_layer_s {
       if (b == 16) by[0] += per_bit * 16;
       else if (b >= 3 && b <= 6) by[7 - b] += per_bit * b;
     }
-    L.nblk = decode_nblk(by);
+    L.nblk = decode_nblk(by, desc.ffn);
     return L;
   }
 };

@@ -758,9 +758,11 @@ def run_sweep(args):
                                  "one CUDA graph of the 32 layers per step, inside CUDA events on the stream",
                        "step_algorithmic_bytes": avg_bytes, "parallelism": "replicas" if ws > 1 else "single GPU",
                        "device_errors": not ok},
-            "roofline": dict(froof, traffic=None,
+            "roofline": dict(froof, traffic=_traffic_from_profile("sweep", T),
                              note="per layer: the expert-FFN call (one persistent decode launch over the layer's "
-                                  "8 experts), timed by CUDA events in a graph of the 32 layers"),
+                                  "8 experts), timed by CUDA events in a graph of the 32 layers; traffic: mean "
+                                  "DRAM bytes of those launches from the committed ncu summary (null once the "
+                                  "kernel sources change)"),
             "step_roofline": {"kernel": "32-layer decode step (per layer: router, permutation, persistent FFN, "
                                         "combine; bitwidth changes)",
                               "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,

@@ -435,11 +435,33 @@ bool valid_bits(int b) { return b == 3 || b == 4 || b == 5 || b == 6 || b == 16;
 
 pw_status check_layer(pw_layer_t l) { return l ? PW_OK : PW_ERR_INVALID_ARG; }
 
+// The stream-ordered write of a bitwidth word: a stream memory operation
+// (cuStreamWriteValue32: the GPU's front end performs it in stream order, no
+// kernel launch between the caller's kernels), or a one-thread kernel where
+// the driver does not offer it.
+using WriteValue32 = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+WriteValue32 write_value32() {
+  static WriteValue32 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WriteValue32>(p);
+  });
+  return fn;
+}
+
 pw_status write_bits(pw_layer_t l, int e, int b, cudaStream_t s) {
   if (g_sim) {
     l->d_bits[e] = b;
     return PW_OK;
   }
+  if (WriteValue32 fn = write_value32())
+    if (fn(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(l->d_bits + e), (cuuint32_t)b,
+           CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS)
+      return PW_OK;
   PW_CUDA(launch_set_bits(l->d_bits, e, b, s));
   return PW_OK;
 }

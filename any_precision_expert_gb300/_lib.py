@@ -69,6 +69,8 @@ _SIGS = {
     "pw_plan_bitwidths": (i32, [i32, vp, vp, vp, vp, vp, vp, C.c_uint64, vp, C.POINTER(C.c_uint64)]),
     "pw_workspace_size": (i32, [vp, i32, C.POINTER(sz)]),
     "pw_layer_check_device": (i32, [vp, vp]),
+    "pw_layer_set_debug_bounds": (i32, [vp, i32]),
+    "pw_debug_check_workspace": (i32, [vp, i32, vp, C.c_size_t, vp]),
     "pw_pack_planes": (i32, [vp, i32, i32, C.POINTER(U32P6)]),
     "pw_pack_f16": (i32, [vp, i32, i32, vp]),
     "pw_debug_dequant": (i32, [vp, i32, i32, vp, vp]),

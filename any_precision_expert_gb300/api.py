@@ -254,6 +254,15 @@ class Layer:
     def check_device(self, stream=None) -> int:
         return lib.pw_layer_check_device(self.handle, _s(stream))
 
+    def set_debug_bounds(self, on: bool):
+        """Workspace canaries around every scratch region (size workspaces after changing it)."""
+        check(lib.pw_layer_set_debug_bounds(self.handle, 1 if on else 0), "pw_layer_set_debug_bounds")
+
+    def debug_check_workspace(self, T: int, ws, stream=None):
+        """Check a whole-layer workspace's canaries; the result lands in the device error word."""
+        check(lib.pw_debug_check_workspace(self.handle, T, _p(ws), ws.numel() * ws.element_size(), _s(stream)),
+              "pw_debug_check_workspace")
+
     # -- hot path ----------------------------------------------------------------
     def route_topk(self, x, wr, bias, T, idx, w, counts=None, stream=None):
         check(lib.pw_route_topk(self.handle, _p(x), _p(wr), _p(bias), T, _p(idx), _p(w), _p(counts),

@@ -24,6 +24,7 @@ constexpr int kErrRouting = 2;       // an expert index outside [0, E) in a rout
 constexpr int kErrBits = 3;          // a bitwidth word outside {3, 4, 5, 6, 16}
 constexpr int kErrOffsets = 4;       // slot offsets not monotone in [0, T*K], or a slot index out of range
 constexpr int kErrLayout = 5;        // a kernel's shared-memory window cannot hold its buffer layout
+constexpr int kErrCanary = 6;        // a workspace canary changed (a write past a scratch region)
 
 #ifdef __CUDACC__
 #define PW_HD __host__ __device__
@@ -81,6 +82,16 @@ cudaError_t ensure_smem(const void* kernel, size_t bytes);
 cudaError_t window_smem(const void* kernel, uint32_t end, size_t& bytes);
 
 cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s);
+// Workspace canaries (debug bounds): kCanaryBytes after each scratch region,
+// filled with a pattern before a call and checked after it.
+constexpr int kCanaryBytes = 256;
+constexpr int kMaxCanaries = 16;
+struct Canaries {
+  unsigned long long off[kMaxCanaries];  // byte offsets in the workspace
+  int n;
+};
+// fill: write the pattern; else check it, flagging kErrCanary in err[0] on a difference.
+cudaError_t launch_canaries(char* ws, const Canaries& c, int* err, bool fill, cudaStream_t s);
 cudaError_t launch_route(const DevLayer& L, const __half* x, const __half* wr, const float* bias,
                          int T, int* idx, float* w, int* counts, cudaStream_t s);
 size_t permute_ws_bytes(int S, int E);

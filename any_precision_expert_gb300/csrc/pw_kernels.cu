@@ -67,6 +67,22 @@ cudaError_t window_smem(const void* kernel, uint32_t end, size_t& bytes) {
 
 __global__ void set_bits_kernel(int* bits, int e, int b) { bits[e] = b; }
 
+// Word j of canary i holds 0xC0DE0000 | i << 8 | j.
+__global__ void canary_kernel(char* ws, Canaries c, int* err, bool fill) {
+  const int i = blockIdx.x, j = threadIdx.x;
+  if (i >= c.n || j >= kCanaryBytes / 4) return;
+  uint32_t* w = reinterpret_cast<uint32_t*>(ws + c.off[i]) + j;
+  const uint32_t v = 0xC0DE0000u | (uint32_t)i << 8 | (uint32_t)j;
+  if (fill) *w = v;
+  else if (*w != v) atomicExch(err, kErrCanary);
+}
+
+cudaError_t launch_canaries(char* ws, const Canaries& c, int* err, bool fill, cudaStream_t s) {
+  if (c.n <= 0) return cudaSuccess;
+  canary_kernel<<<c.n, kCanaryBytes / 4, 0, s>>>(ws, c, err, fill);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_set_bits(int* bits, int e, int b, cudaStream_t s) {
   set_bits_kernel<<<1, 1, 0, s>>>(bits, e, b);
   return cudaGetLastError();

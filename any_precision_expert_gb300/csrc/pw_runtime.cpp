@@ -12,6 +12,7 @@
 //    the freed blocks to a reclaim queue guarded by a CUDA event (the safe
 //    boundary); raising re-maps blocks that are still intact.
 #include <cuda.h>  // driver API types of the virtual-memory calls (looked up at run time)
+#include <nvtx3/nvToolsExt.h>  // header-only NVTX ranges (no-ops unless a tool is attached)
 #include <sys/mman.h>
 #include <unistd.h>
 
@@ -57,6 +58,23 @@ pw_status cuda_fail(cudaError_t e) {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Ranges of the hot-path calls, when PW_NVTX=1 (read once) and a tool listens.
+struct NvtxRange {
+  static bool on() {
+    static const bool v = [] {
+      const char* e = getenv("PW_NVTX");
+      return e && e[0] == '1';
+    }();
+    return v;
+  }
+  explicit NvtxRange(const char* name) {
+    if (on()) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on()) nvtxRangePop();
+  }
+};
 
 pw_status dev_h2d(void* dst, const void* src, size_t n, cudaStream_t s) {
   if (n == 0) return PW_OK;
@@ -368,6 +386,11 @@ struct pw_layer_s {
   std::vector<unsigned long long> h_plane_pt, h_f16_pt;
   bool shared_loaded = false;
   long long spin_limit = kDefaultSpinPolls;  // see pw_testing_wait_limit
+  // workspace canaries (pw_layer_set_debug_bounds; PW_DEBUG_BOUNDS=1 turns them on for new layers)
+  bool debug_bounds = [] {
+    const char* e = getenv("PW_DEBUG_BOUNDS");
+    return e && e[0] == '1';
+  }();
   int wait_bias = 0;
 
   Block& plane(int e, int p) { return planes[(size_t)e * kPlanes + p]; }
@@ -985,6 +1008,7 @@ extern "C" pw_status pw_set_expert_bitwidth(pw_layer_t l, int e, int bits, void*
   if (bits == 16 && l->f16[e].st == B_NONE) return PW_ERR_NOT_RESIDENT;
 
   cudaStream_t s = as_stream(stream);
+  NvtxRange range("pw_set_expert_bitwidth");
   // blocks filled by an asynchronous upload: the commit waits for the copies
   auto await_upload = [&](Block& b) -> pw_status {
     if (b.ready) {
@@ -1047,6 +1071,7 @@ extern "C" pw_status pw_prefetch_expert(pw_layer_t l, int e, int bits, const uin
   PW_TRY(check_layer(l));
   if (e < 0 || e >= l->desc.n_experts || !valid_bits(bits)) return PW_ERR_INVALID_ARG;
   if (l->bits[e] == 0) return PW_ERR_INVALID_ARG;  // never loaded
+  NvtxRange range("pw_prefetch_expert");
   const int need = bits == 16 ? kPlanes : bits;
   // the host data of every block that is gone
   std::vector<int> missing;
@@ -1160,20 +1185,41 @@ namespace {
 
 struct WsLayout {
   size_t perm_off, perm_bytes, h_off, h_bytes, hs_off, hs_bytes, total;
+  Canaries can;  // with debug bounds: a canary block after each region
+};
+
+// Scratch regions at 256-byte boundaries; with debug bounds each is followed
+// by a kCanaryBytes block whose offset is recorded.
+struct Carver {
+  bool dbg;
+  Canaries* can;
+  size_t o = 0;
+  size_t take(size_t n) {
+    const size_t at = o;
+    o += align_up(n, 256);
+    if (dbg && can->n < kMaxCanaries) {
+      can->off[can->n++] = o;
+      o += kCanaryBytes;
+    }
+    return at;
+  }
 };
 
 WsLayout ws_layout(const pw_layer_s* l, int T) {
   WsLayout w{};
+  w.can.n = 0;
+  Carver c{l->debug_bounds, &w.can};
   const size_t S = (size_t)T * l->desc.top_k;
-  w.perm_off = 0;
   w.perm_bytes = align_up(permute_ws_bytes((int)S, l->desc.n_experts), 256);
-  w.h_off = w.perm_off + w.perm_bytes;
+  w.perm_off = c.take(w.perm_bytes);
   w.h_bytes = align_up(S * l->desc.ffn * 2, 256);
-  w.hs_off = w.h_off + w.h_bytes;
+  w.h_off = c.take(w.h_bytes);
   w.hs_bytes = align_up((size_t)T * l->desc.shared_ffn * 2, 256);
-  w.total = w.hs_off + w.hs_bytes;
+  w.hs_off = c.take(w.hs_bytes);
+  w.total = c.o;
   return w;
 }
+
 
 pw_status device_only() { return g_sim ? PW_ERR_UNSUPPORTED : PW_OK; }
 
@@ -1214,17 +1260,15 @@ int class_mask(const pw_layer_s* l) {
 // routed / shared FFN intermediates, then the hot-path scratch of ws_layout.
 struct FwdLayout {
   size_t off_offsets, off_perm_src, off_inv_slot, off_x_perm, off_y_perm, off_ys, off_rpart, off_base, total;
+  Canaries can;  // with debug bounds: this layout's and the hot-path scratch's canaries
 };
 
 FwdLayout fwd_layout(const pw_layer_s* l, int T) {
   FwdLayout f{};
+  f.can.n = 0;
   const size_t S = (size_t)T * l->desc.top_k, d = l->desc.d;
-  size_t o = 0;
-  auto take = [&](size_t n) {
-    const size_t at = o;
-    o += align_up(n, 256);
-    return at;
-  };
+  Carver c{l->debug_bounds, &f.can};
+  auto take = [&](size_t n) { return c.take(n); };
   f.off_offsets = take(sizeof(int32_t) * (l->desc.n_experts + 1));
   f.off_perm_src = take(sizeof(int32_t) * S);
   f.off_inv_slot = take(sizeof(int32_t) * S);
@@ -1234,8 +1278,10 @@ FwdLayout fwd_layout(const pw_layer_s* l, int T) {
   // router partial sums of the fused step (batches of at most kFusedMaxTokens)
   f.off_rpart = take(sizeof(float) * (size_t)std::min(T, kFusedMaxTokens) * route_slices(l->desc.d) *
                      l->desc.n_experts);
-  f.off_base = o;
-  f.total = o + ws_layout(l, T).total;
+  f.off_base = c.o;
+  const WsLayout W = ws_layout(l, T);
+  for (int i = 0; i < W.can.n && f.can.n < kMaxCanaries; ++i) f.can.off[f.can.n++] = f.off_base + W.can.off[i];
+  f.total = f.off_base + W.total;
   return f;
 }
 
@@ -1271,24 +1317,46 @@ extern "C" pw_status pw_moe_forward(pw_layer_t l, const void* x, const void* wr,
   auto* hs = sh ? reinterpret_cast<__half*>(base + W.hs_off) : nullptr;
   const auto* xh = static_cast<const __half*>(x);
   const auto* wrh = static_cast<const __half*>(wr);
-  // one fused launch (router, permutation, expert FFN, shared FFN, combine)
-  // for small decode batches (measured: 3-5% faster at 1-8 tokens, 1.5%
-  // slower at 64, where the separate small kernels cost less than the fused
-  // kernel's final barrier); both give the same idx, w and y bit for bit
-  const bool fused = T <= kFusedMaxTokens && T <= decode_max_tokens(l->desc.ffn, T) &&
-                     (!sh || T <= decode_max_tokens_shared()) && T * l->desc.top_k <= 512;
-  if (fused)
-    return launched(launch_layer_fused(L, xh, wrh, bias, idx, w, reinterpret_cast<float*>(wsb + F.off_rpart), T, h,
-                                       hs, y_perm, ys, static_cast<__half*>(y), offsets, s));
-  PW_TRY(launched(launch_route(L, xh, wrh, bias, T, idx, w, nullptr, s)));
-  auto* perm_src = reinterpret_cast<int*>(wsb + F.off_perm_src);
-  auto* inv_slot = reinterpret_cast<int*>(wsb + F.off_inv_slot);
-  auto* x_perm = reinterpret_cast<__half*>(wsb + F.off_x_perm);
-  PW_TRY(launched(launch_permute(L, idx, T, xh, offsets, perm_src, inv_slot, x_perm,
-                                 reinterpret_cast<int*>(base + W.perm_off), s)));
-  PW_TRY(launched(launch_moe_ffn(L, x_perm, offsets, T * l->desc.top_k, y_perm, h, sh ? xh : nullptr, T, ys, hs,
-                                 class_mask(l), s)));
-  return launched(launch_combine(L, y_perm, inv_slot, w, T, ys, static_cast<__half*>(y), s));
+  NvtxRange range("pw_moe_forward");
+  if (l->debug_bounds) PW_TRY(launched(launch_canaries(wsb, F.can, L.err, true, s)));
+  auto run = [&]() -> pw_status {
+    // one fused launch (router, permutation, expert FFN, shared FFN, combine)
+    // for small decode batches (measured: 3-5% faster at 1-8 tokens, 1.5%
+    // slower at 64, where the separate small kernels cost less than the fused
+    // kernel's final barrier); both give the same idx, w and y bit for bit
+    const bool fused = T <= kFusedMaxTokens && T <= decode_max_tokens(l->desc.ffn, T) &&
+                       (!sh || T <= decode_max_tokens_shared()) && T * l->desc.top_k <= 512;
+    if (fused)
+      return launched(launch_layer_fused(L, xh, wrh, bias, idx, w, reinterpret_cast<float*>(wsb + F.off_rpart), T,
+                                         h, hs, y_perm, ys, static_cast<__half*>(y), offsets, s));
+    PW_TRY(launched(launch_route(L, xh, wrh, bias, T, idx, w, nullptr, s)));
+    auto* perm_src = reinterpret_cast<int*>(wsb + F.off_perm_src);
+    auto* inv_slot = reinterpret_cast<int*>(wsb + F.off_inv_slot);
+    auto* x_perm = reinterpret_cast<__half*>(wsb + F.off_x_perm);
+    PW_TRY(launched(launch_permute(L, idx, T, xh, offsets, perm_src, inv_slot, x_perm,
+                                   reinterpret_cast<int*>(base + W.perm_off), s)));
+    PW_TRY(launched(launch_moe_ffn(L, x_perm, offsets, T * l->desc.top_k, y_perm, h, sh ? xh : nullptr, T, ys, hs,
+                                   class_mask(l), s)));
+    return launched(launch_combine(L, y_perm, inv_slot, w, T, ys, static_cast<__half*>(y), s));
+  };
+  PW_TRY(run());
+  if (l->debug_bounds) PW_TRY(launched(launch_canaries(wsb, F.can, L.err, false, s)));
+  return PW_OK;
+}
+
+extern "C" pw_status pw_layer_set_debug_bounds(pw_layer_t l, int on) {
+  PW_TRY(check_layer(l));
+  l->debug_bounds = on != 0;
+  return PW_OK;
+}
+
+extern "C" pw_status pw_debug_check_workspace(pw_layer_t l, int T, void* ws, size_t ws_bytes, void* stream) {
+  PW_TRY(check_layer(l));
+  if (!l->debug_bounds || bad_tokens(T) || !ws) return PW_ERR_INVALID_ARG;
+  const FwdLayout F = fwd_layout(l, T);
+  if (ws_bytes < F.total) return PW_ERR_OOM;
+  PW_TRY(device_only());
+  return launched(launch_canaries(static_cast<char*>(ws), F.can, l->d_err, false, as_stream(stream)));
 }
 
 extern "C" pw_status pw_workspace_size(pw_layer_t l, int T, size_t* bytes) {
@@ -1306,6 +1374,7 @@ extern "C" pw_status pw_route_topk(pw_layer_t l, const void* x, const void* wr, 
   if (T > 0 && (!aligned16(x) || !aligned16(wr))) return PW_ERR_INVALID_ARG;
   PW_TRY(device_only());
   if (T == 0) return PW_OK;
+  NvtxRange range("pw_route_topk");
   return launched(launch_route(l->dev(), static_cast<const __half*>(x), static_cast<const __half*>(wr), bias, T,
                                idx, w, expert_count, as_stream(stream)));
 }
@@ -1343,6 +1412,7 @@ extern "C" pw_status pw_permute(pw_layer_t l, const int32_t* idx, int T, const v
   const WsLayout W = ws_layout(l, T);
   if (T > 0 && ws_bytes < W.perm_off + W.perm_bytes) return PW_ERR_OOM;
   PW_TRY(device_only());
+  NvtxRange range("pw_permute");
   char* wsb = static_cast<char*>(ws);
   return launched(launch_permute(l->dev(), idx, T, static_cast<const __half*>(x), offsets, perm_src, inv_slot,
                                  static_cast<__half*>(x_perm), reinterpret_cast<int*>(wsb + W.perm_off),
@@ -1360,6 +1430,7 @@ extern "C" pw_status pw_expert_ffn_bitplane(pw_layer_t l, const void* x_perm, co
   if (ws_bytes < W.h_off + W.h_bytes) return PW_ERR_OOM;
   PW_TRY(all_loaded(l));
   PW_TRY(device_only());
+  NvtxRange range("pw_expert_ffn_bitplane");
   char* wsb = static_cast<char*>(ws);
   return launched(launch_moe_ffn(l->dev(), static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
                                  reinterpret_cast<__half*>(wsb + W.h_off), nullptr, T, nullptr, nullptr,
@@ -1376,6 +1447,7 @@ extern "C" pw_status pw_shared_ffn(pw_layer_t l, const void* x, int T, float* y_
   const WsLayout W = ws_layout(l, T);
   if (ws_bytes < W.total) return PW_ERR_OOM;
   PW_TRY(device_only());
+  NvtxRange range("pw_shared_ffn");
   char* wsb = static_cast<char*>(ws);
   return launched(launch_moe_ffn(l->dev(), nullptr, nullptr, 0, nullptr, nullptr, static_cast<const __half*>(x), T,
                                  y_shared, reinterpret_cast<__half*>(wsb + W.hs_off), 0, as_stream(stream)));
@@ -1395,11 +1467,16 @@ extern "C" pw_status pw_moe_ffn(pw_layer_t l, const void* x, const void* x_perm,
   if (ws_bytes < W.total) return PW_ERR_OOM;
   PW_TRY(all_loaded(l));
   PW_TRY(device_only());
+  NvtxRange range("pw_moe_ffn");
   char* wsb = static_cast<char*>(ws);
-  return launched(launch_moe_ffn(l->dev(), static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
+  cudaStream_t s = as_stream(stream);
+  if (l->debug_bounds) PW_TRY(launched(launch_canaries(wsb, W.can, l->d_err, true, s)));
+  PW_TRY(launched(launch_moe_ffn(l->dev(), static_cast<const __half*>(x_perm), offsets, T * l->desc.top_k, y_perm,
                                  reinterpret_cast<__half*>(wsb + W.h_off), sh ? static_cast<const __half*>(x) : nullptr,
                                  T, sh ? y_shared : nullptr, reinterpret_cast<__half*>(wsb + W.hs_off), class_mask(l),
-                                 as_stream(stream)));
+                                 s)));
+  if (l->debug_bounds) PW_TRY(launched(launch_canaries(wsb, W.can, l->d_err, false, s)));
+  return PW_OK;
 }
 
 extern "C" pw_status pw_combine(pw_layer_t l, const float* y_perm, const int32_t* inv_slot, const float* w, int T,
@@ -1410,6 +1487,7 @@ extern "C" pw_status pw_combine(pw_layer_t l, const float* y_perm, const int32_t
   if (T > 0 && (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared))))
     return PW_ERR_INVALID_ARG;
   PW_TRY(device_only());
+  NvtxRange range("pw_combine");
   if (T == 0) return PW_OK;
   return launched(launch_combine(l->dev(), y_perm, inv_slot, w, T, y_shared, static_cast<__half*>(y),
                                  as_stream(stream)));

@@ -431,6 +431,29 @@ pw_status pw_plan_bitwidths(int E, const double* sens, const double* mass, const
  */
 pw_status pw_layer_check_device(pw_layer_t layer, void* stream);
 
+/*
+ * Workspace canaries (debug bounds) for one layer.  When on, the sizes that
+ * pw_moe_forward_workspace_size and pw_workspace_size report include a
+ * 256-byte block after every scratch region; pw_moe_forward and pw_moe_ffn
+ * fill those blocks with a fixed pattern before their kernels and check the
+ * pattern after them (both stream-ordered, on the call's stream), flagging a
+ * changed word -- a write past a scratch region -- in the layer's device error
+ * word (PW_ERR_DEVICE_CHECK from pw_layer_check_device).  Workspaces must be
+ * sized after the setting changes (PW_ERR_OOM otherwise).  Off by default;
+ * PW_DEBUG_BOUNDS=1 in the environment turns it on for layers created
+ * afterwards.  With PW_NVTX=1 the hot-path calls also open NVTX ranges named
+ * after the call (for a profiler's timeline).
+ */
+pw_status pw_layer_set_debug_bounds(pw_layer_t layer, int on);
+
+/*
+ * Check, on the stream, the canaries of a whole-layer workspace laid out for
+ * T tokens (as pw_moe_forward lays it out); the result lands in the layer's
+ * device error word.  PW_ERR_INVALID_ARG when debug bounds are off,
+ * PW_ERR_OOM when ws_bytes is below that layout's size.
+ */
+pw_status pw_debug_check_workspace(pw_layer_t layer, int T, void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Host utilities and debugging
  * ------------------------------------------------------------------------- */

@@ -114,3 +114,39 @@ def test_combine_flags_slots_out_of_range(tiny):
     torch.cuda.synchronize()
     assert L.check_device() == 0
     assert np.isfinite(buf.y[:T].float().cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("T", [8, 40])
+def test_workspace_canaries(T):
+    # debug bounds: canary blocks after every scratch region of the
+    # whole-layer call; a clean call leaves them intact (and the output
+    # unchanged), a word changed afterwards is reported by the check
+    cfg = get_config("qwen", d=512, f=320, E=12, K=4, shared_ffn=768)
+    gl = GpuLayer(cfg, seed=8, bits=[3, 16, 3, 4, 3, 5, 16, 6, 3, 3, 16, 3], with_w16=False)
+    try:
+        x = torch.from_numpy(gl.tokens(T)).cuda()
+        buf = pw.Buffers(gl.layer, T)
+        y0 = pw.moe_forward_fused(gl.layer, x, gl.wr_d, gl.bias_d, buf).clone()
+        gl.layer.set_debug_bounds(True)
+        buf = pw.Buffers(gl.layer, T)  # scratch sized with the canaries
+        y1 = pw.moe_forward_fused(gl.layer, x, gl.wr_d, gl.bias_d, buf)
+        # the split calls (pw_moe_ffn fills and checks its own scratch's canaries)
+        y2 = pw.moe_forward(gl.layer, x, gl.wr_d, gl.bias_d, buf).clone()
+        torch.cuda.synchronize()
+        assert gl.layer.check_device() == 0
+        assert torch.equal(y1, y0)
+        assert torch.equal(y2, y0)
+        ws = buf.fws.view(torch.int32)
+        pat = (ws.cpu().numpy().astype(np.int64) & 0xFFFF0000) == 0xC0DE0000
+        hits = np.flatnonzero(pat)
+        assert hits.size >= 10 * 64  # ten canary blocks of 64 words
+        gl.layer.debug_check_workspace(T, buf.fws)
+        torch.cuda.synchronize()
+        assert gl.layer.check_device() == 0
+        ws[int(hits[len(hits) // 2])] = 0  # as a write past a region would
+        gl.layer.debug_check_workspace(T, buf.fws)
+        torch.cuda.synchronize()
+        assert gl.layer.check_device() == 7  # PW_ERR_DEVICE_CHECK
+        gl.layer.set_debug_bounds(False)
+    finally:
+        gl.close()

@@ -246,6 +246,31 @@ def test_forward_call_checks_arguments_on_the_host(sim):
     pool.close()
 
 
+def test_debug_bounds_add_a_canary_after_every_scratch_region(sim):
+    # pw_layer_set_debug_bounds: 256 canary bytes after each region of the
+    # whole-layer scratch (7 regions of its own + the 3 of the hot-path
+    # scratch) and of the hot-path scratch (3 regions)
+    pool = pw.Pool(48 * PAGE, page_bytes=PAGE, device="cpu")
+    layer = _layer(pool, E=4, d=128, f=128, K=2)
+    for e in range(4):
+        _load(layer, e, 3, _expert(e, w16=False))
+    for T in (1, 8, 300):
+        nf, nw = layer.forward_workspace_size(T), layer.workspace_size(T)
+        layer.set_debug_bounds(True)
+        assert layer.forward_workspace_size(T) == nf + 10 * 256
+        assert layer.workspace_size(T) == nw + 3 * 256
+        layer.set_debug_bounds(False)
+        assert layer.forward_workspace_size(T) == nf
+    L = _lib.lib
+    assert L.pw_debug_check_workspace(layer.handle, 8, 256, 1 << 20, None) == 1  # debug bounds off
+    layer.set_debug_bounds(True)
+    n = layer.forward_workspace_size(8)
+    assert L.pw_debug_check_workspace(layer.handle, 8, 256, n - 1, None) == 3  # too small
+    assert L.pw_debug_check_workspace(layer.handle, 8, 256, n, None) == 2  # no device in host-sim
+    layer.destroy()
+    pool.close()
+
+
 def test_scratch_must_be_16_byte_aligned(sim):
     # h and hs are carved out of ws and read back with 16-byte copies, so a
     # misaligned ws is refused on the host (status 1) instead of reaching a kernel

@@ -22,7 +22,7 @@ cudaError_t launch_moe_ffn(const DevLayer& L, const __half* x_perm, const int* o
   // Experts with at most `thr` tokens take the decode kernels; larger ones the
   // tcgen05 GEMM.  No expert can have more tokens than the batch, and the
   // shared FFN sees every token.
-  const int thr = decode_max_tokens(L.f, T);
+  const int thr = decode_max_tokens(L.f, T, L.E, L.K);
   const bool routed = offsets != nullptr && n_slots > 0;
   const bool big = T > thr;
   const bool shared_decode = x_sh != nullptr && T > 0 && T <= decode_max_tokens_shared();

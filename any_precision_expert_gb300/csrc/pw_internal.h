@@ -121,7 +121,7 @@ cudaError_t launch_uni(const DevLayer& L, const __half* x, const __half* x_perm,
 cudaError_t launch_layer_fused(const DevLayer& L, const __half* x, const __half* wr, const float* bias, int* idx,
                                float* w, float* rpart, int T, __half* h, __half* hs, float* y_perm, float* ys,
                                __half* y, int* offsets_out, cudaStream_t s);
-int decode_max_tokens(int ffn, int T);
+int decode_max_tokens(int ffn, int T, int E, int K);
 int decode_max_tokens_shared();
 cudaError_t launch_prefill(const DevLayer& L, int mode, int phase, const __half* act, const int* offsets,
                            int n_slots, int min_tokens, __half* h, float* y, cudaStream_t s);

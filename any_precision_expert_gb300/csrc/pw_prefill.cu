@@ -822,9 +822,15 @@ static int env_tokens(const char* name, int dflt) {
 // fill the GPU with GEMM tiles from 33 tokens on.  Narrow ones in batches of up
 // to 64 tokens stay on the decode kernel up to 64 tokens (a lone GEMM expert of
 // a few row tiles would run after it, nearly alone on the GPU); in larger
-// batches many experts cross 32 tokens and their GEMM tiles fill the GPU.
-int decode_max_tokens(int ffn, int T) {
-  return env_tokens("PW_DECODE_MAX_TOK", ffn >= 4096 || T > 64 ? 32 : 64);
+// batches many experts cross 32 tokens and their GEMM tiles fill the GPU --
+// unless the batch spreads over 128 experts or more at no more than 32 slots
+// per expert on average, where the few that cross are too few to: those stay
+// on the decode kernel up to 128 tokens (measured on the 128-expert layer: at
+// 128 tokens 0.124 -> 0.151 of the HBM roofline; at 8192, where most experts
+// are large, 32 stays better, 0.271 against 0.259 of the bf16 peak).
+int decode_max_tokens(int ffn, int T, int E, int K) {
+  const bool spread = E >= 128 && (long long)T * K <= 32LL * E;
+  return env_tokens("PW_DECODE_MAX_TOK", ffn >= 4096 ? 32 : T <= 64 ? 64 : spread ? 128 : 32);
 }
 
 // The shared FFN (every token of the batch) uses the tensor-core GEMM above this batch size.

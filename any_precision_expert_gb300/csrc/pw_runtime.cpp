@@ -1324,7 +1324,7 @@ extern "C" pw_status pw_moe_forward(pw_layer_t l, const void* x, const void* wr,
     // for small decode batches (measured: 3-5% faster at 1-8 tokens, 1.5%
     // slower at 64, where the separate small kernels cost less than the fused
     // kernel's final barrier); both give the same idx, w and y bit for bit
-    const bool fused = T <= kFusedMaxTokens && T <= decode_max_tokens(l->desc.ffn, T) &&
+    const bool fused = T <= kFusedMaxTokens && T <= decode_max_tokens(l->desc.ffn, T, l->desc.n_experts, l->desc.top_k) &&
                        (!sh || T <= decode_max_tokens_shared()) && T * l->desc.top_k <= 512;
     if (fused)
       return launched(launch_layer_fused(L, xh, wrh, bias, idx, w, reinterpret_cast<float*>(wsb + F.off_rpart), T,

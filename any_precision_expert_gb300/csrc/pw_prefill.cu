@@ -819,18 +819,25 @@ static int env_tokens(const char* name, int dflt) {
 
 // Routed experts with more tokens than this use the tensor-core GEMM (read per
 // call).  Wide experts (ffn >= 4096: at least 32 row tiles of 128 per matrix)
-// fill the GPU with GEMM tiles from 33 tokens on.  Narrow ones in batches of up
-// to 64 tokens stay on the decode kernel up to 64 tokens (a lone GEMM expert of
-// a few row tiles would run after it, nearly alone on the GPU); in larger
-// batches many experts cross 32 tokens and their GEMM tiles fill the GPU --
-// unless the batch spreads over 128 experts or more at no more than 32 slots
-// per expert on average, where the few that cross are too few to: those stay
-// on the decode kernel up to 128 tokens (measured on the 128-expert layer: at
-// 128 tokens 0.124 -> 0.151 of the HBM roofline; at 8192, where most experts
-// are large, 32 stays better, 0.271 against 0.259 of the bf16 peak).
+// fill the GPU with GEMM tiles from 33 tokens on -- once the batch gives the
+// experts more than 32 tokens on average; at up to 32 on average the few
+// experts above 32 stay on the decode kernel up to 64 tokens, and a batch
+// that no expert can push past 64 launches no GEMM at all (measured on the
+// Mixtral-shaped layer: at 128 tokens 0.129 -> 0.151 of the HBM roofline; at
+// 256, where most experts hold 33..90 tokens, 32 stays better, 0.934 against
+// 1.161 ms).  Narrow ones in batches of up to 64 tokens stay on the decode
+// kernel up to 64 tokens (a lone GEMM expert of a few row tiles would run
+// after it, nearly alone on the GPU); in larger batches many experts cross 32
+// tokens and their GEMM tiles fill the GPU -- unless the batch spreads over
+// 128 experts or more at no more than 32 slots per expert on average, where
+// the few that cross are too few to: those stay on the decode kernel up to
+// 128 tokens (measured on the 128-expert layer: at 128 tokens 0.124 -> 0.151
+// of the HBM roofline; at 8192, where most experts are large, 32 stays
+// better, 0.271 against 0.259 of the bf16 peak).
 int decode_max_tokens(int ffn, int T, int E, int K) {
-  const bool spread = E >= 128 && (long long)T * K <= 32LL * E;
-  return env_tokens("PW_DECODE_MAX_TOK", ffn >= 4096 ? 32 : T <= 64 ? 64 : spread ? 128 : 32);
+  const bool sparse = (long long)T * K <= 32LL * E;  // at most 32 slots per expert on average
+  const int thr = ffn >= 4096 ? (sparse ? 64 : 32) : T <= 64 ? 64 : (E >= 128 && sparse) ? 128 : 32;
+  return env_tokens("PW_DECODE_MAX_TOK", thr);
 }
 
 // The shared FFN (every token of the batch) uses the tensor-core GEMM above this batch size.

@@ -542,7 +542,13 @@ def sub_runs(stream, src=None, steps_decode=50, steps_prefill=10, warmup=3, pagi
 
 
 def _thresholds(cfg, T):
-    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", "32" if cfg.f >= 4096 or T > 64 else "64")), 1024)
+    """The library's decode / tensor-core token thresholds (routed, shared) for a batch of T tokens."""
+    sparse = T * cfg.K <= 32 * cfg.E  # at most 32 slots per expert on average
+    if cfg.f >= 4096:
+        d = 64 if sparse else 32
+    else:
+        d = 64 if T <= 64 else 128 if cfg.E >= 128 and sparse else 32
+    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", str(d))), 1024)
     thr_s = min(int(os.environ.get("PW_DECODE_MAX_TOK_SHARED", "256")), 1024)
     return thr, thr_s
 

@@ -112,7 +112,8 @@ def test_shared_ffn_across_the_decode_threshold(monkeypatch):
 
 
 def test_many_chunks_per_expert():
-    # one expert takes every token: 15 full chunks of 16 tokens and a ragged one of 10
+    # one expert takes every token (250, above the decode threshold: the
+    # tensor-core GEMM with a ragged last M-tile)
     cfg = get_config("tiny", K=1)
     gl = GpuLayer(cfg, seed=7, bits=[3] * 8, with_w16=False)
     try:
@@ -152,3 +153,45 @@ def test_odd_shapes_all_bitwidths(nblk, monkeypatch):
             gl.check_forward(gl.tokens(T))
     finally:
         gl.close()
+
+
+
+# Experts of 33..64 tokens on the decode kernel (two items of 32 tokens per
+# tile pair; the threshold a Mixtral-shaped layer takes when its batch puts
+# at most 32 tokens per expert on average); PW_DECODE_MAX_TOK forces it.
+def test_experts_above_32_tokens_on_the_decode_kernel_all_bitwidths(monkeypatch):
+    monkeypatch.setenv("PW_DECODE_MAX_TOK", "64")
+    # d = 192, f = 320: ragged plane groups in both phases; the shared FFN too
+    cfg = get_config("qwen", d=192, f=320, E=5, K=2, shared_ffn=320)
+    gl = GpuLayer(cfg, seed=11, bits=[3, 4, 5, 6, 16])
+    try:
+        for T in (33, 40, 64, 130):  # 130: experts above 64 tokens go to the GEMM
+            gl.check_forward(gl.tokens(T))
+    finally:
+        gl.close()
+    # f = 4160: 4096+ column down reductions ending in a ragged plane group
+    cfg = get_config("tiny", d=512, f=4160, E=5, K=2)
+    gl = GpuLayer(cfg, seed=12, bits=[3, 4, 5, 6, 16])
+    try:
+        for T in (36, 64, 100):
+            gl.check_forward(gl.tokens(T))
+    finally:
+        gl.close()
+
+
+@NBLK
+def test_one_expert_many_items(nblk, monkeypatch):
+    # every token on expert 1: 250 tokens in eight items of 32 (the last of
+    # 26 tokens), all on the decode kernel
+    monkeypatch.setenv("PW_DECODE_NBLK", nblk)
+    monkeypatch.setenv("PW_DECODE_MAX_TOK", "256")
+    cfg = get_config("tiny", K=1)
+    for bits in ([3] * 8, [5] * 8):
+        gl = GpuLayer(cfg, seed=13, bits=bits, with_w16=False)
+        try:
+            gl.bias = np.array([0, 50, 0, 0, 0, 0, 0, 0], dtype=np.float32)
+            gl.bias_d = torch.from_numpy(gl.bias).cuda()
+            r = gl.check_forward(gl.tokens(250))
+            assert (r["buf"].idx[:250].cpu().numpy() == 1).all()
+        finally:
+            gl.close()

@@ -43,10 +43,15 @@ constexpr uint32_t PF_PBUF_BYTES = 4 * 6 * 512;      // plane group of one warp 
 template <int NM>
 struct Pf {
   static constexpr int DQ = 4 * NM;                  // (matrix, slab, stage parity)
-  static constexpr int NS = NM == 2 ? 2 : 3;
+  // tokens of one tile: gate/up fills tensor memory with its two 256-column
+  // accumulators; down takes 512 tokens in two, so each dequantised weight
+  // tile feeds twice the MMA work
+  static constexpr int NH = NM == 2 ? 1 : 2;  // 256-token halves of a tile
+  static constexpr int BN = NH * PF_BN;
+  static constexpr int NS = 2;
   static constexpr int WARPS = DQ + PF_BWARPS + 1;
   static constexpr int THREADS = 32 * WARPS;
-  static constexpr uint32_t STAGE = NM * PF_A_BYTES + PF_B_BYTES;
+  static constexpr uint32_t STAGE = NM * PF_A_BYTES + NH * PF_B_BYTES;
   static constexpr uint32_t TABS = NM * 2 * PF_TAB_BYTES;
   // gate/up stages plane groups through a buffer per warp pair (one group in
   // flight); down loads each stage's plane words straight into registers
@@ -64,7 +69,8 @@ struct Pf {
   static constexpr uint32_t BARS = 256;
   static constexpr uint32_t SMEM = 1024 + NS * STAGE + TABS + PBUFS + BARS;  // !FIXED
   static constexpr uint32_t TAB_AT = 64 * 1024, STAGE_AT = 96 * 1024, END = STAGE_AT + NS * STAGE;  // FIXED
-  static constexpr uint32_t TMEM_COLS = NM == 2 ? 512 : 256;
+  static constexpr uint32_t TMEM_COLS = NM * NH * PF_BN;
+  static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
   static constexpr uint32_t FULL_COUNT = NM * 2 + 1;  // dequant warps + the TMA producer's expect_tx
   static constexpr int PAIRS = DQ / 2;                        // warps sharing one LUT table
 };
@@ -84,6 +90,7 @@ struct PfTile {
   int e, mt, nt, slot0, nvalid;
 };
 
+template <int BN>
 __device__ __forceinline__ PfTile pf_tile(int t, const int* s_pref, const int* s_off, int E, int mtiles) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
@@ -92,14 +99,14 @@ __device__ __forceinline__ PfTile pf_tile(int t, const int* s_pref, const int* s
   }
   // the token tiles of one 128-row weight tile are consecutive, so they run
   // at the same time on neighbouring CTAs and read its planes from DRAM once
-  const int ntiles = (s_off[lo + 1] - s_off[lo] + PF_BN - 1) / PF_BN;
+  const int ntiles = (s_off[lo + 1] - s_off[lo] + BN - 1) / BN;
   PfTile T;
   T.e = lo;
   const int local = t - s_pref[lo];
   T.nt = local % ntiles;
   T.mt = local / ntiles;
-  T.slot0 = s_off[lo] + T.nt * PF_BN;
-  T.nvalid = min(PF_BN, s_off[lo + 1] - T.slot0);
+  T.slot0 = s_off[lo] + T.nt * BN;
+  T.nvalid = min(BN, s_off[lo + 1] - T.slot0);
   return T;
 }
 
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
       int c = 0;
       if (e < E) {
         const int n = s_off[e + 1] - s_off[e];
-        c = n > Q.min_tokens ? mtiles * ((n + PF_BN - 1) / PF_BN) : 0;
+        c = n > Q.min_tokens ? mtiles * ((n + C::BN - 1) / C::BN) : 0;
       }
       int incl = c;
 #pragma unroll
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
     auto jphase = [&](uint32_t j) { return (j / C::NB) & 1; };
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const PfTile T = pf_tile(t, s_pref, s_off, E, mtiles);
+      const PfTile T = pf_tile<C::BN>(t, s_pref, s_off, E, mtiles);
       const int b = s_bits[T.e];
       const int row0 = T.mt * PF_BM + slab * 64 + tis * 16;  // this lane's 16-row tile
       const bool tile_ok = row0 < R;
@@ -610,7 +617,8 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
           }
         }
       } else {
-        for (int c = 0; c < 8; ++c) {
+        const int nc = (min(T.nvalid, C::BN) + 31) / 32;  // column groups holding tokens
+        for (int c = 0; c < nc; ++c) {
           float acc[32];
           tmem_ld32(tl + 32 * c, acc);
           if (row < R) {
@@ -634,15 +642,17 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const PfTile T = pf_tile(t, s_pref, s_off, E, mtiles);
+        const PfTile T = pf_tile<C::BN>(t, s_pref, s_off, E, mtiles);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % C::NS;
           const uint32_t ph = (it / C::NS) & 1;
           ok = mbar_wait(empty_bar(s), ph ^ 1, abort_flag, L.err);
           if (!ok) break;
           const uint32_t Bs = base + s * C::STAGE + NM * PF_A_BYTES;
-          mbar_arrive_expect_tx(full_bar(s), PF_B_BYTES);
-          tma_load_2d(Bs, &act_map, kb * PF_BK, T.slot0, full_bar(s));
+          const int nh = T.nvalid > PF_BN ? C::NH : 1;  // 256-row boxes holding tokens
+          mbar_arrive_expect_tx(full_bar(s), nh * PF_B_BYTES);
+          for (int hh = 0; hh < nh; ++hh)
+            tma_load_2d(Bs + hh * PF_B_BYTES, &act_map, kb * PF_BK, T.slot0 + hh * PF_BN, full_bar(s));
         }
       }
     }
@@ -652,6 +662,8 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
     uint32_t it = 0, tc = 0;
     bool issued = false, ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      // halves of the tile holding tokens (a tile of at most 256 takes one)
+      const int nh = C::NH == 1 || pf_tile<C::BN>(t, s_pref, s_off, E, mtiles).nvalid > PF_BN ? C::NH : 1;
       ok = mbar_wait(acc_empty, (tc & 1) ^ 1, abort_flag, L.err);
       if (!ok) break;
       tc_fence_after();
@@ -662,13 +674,17 @@ __global__ void __launch_bounds__(Pf<NM>::THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t st = base + s * C::STAGE;
-        const uint64_t bdesc = sw128_desc(st + NM * PF_A_BYTES);
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
           const uint64_t adesc = sw128_desc(st + m * PF_A_BYTES);
 #pragma unroll
-          for (int k = 0; k < PF_BK / 16; ++k)
-            umma_f16(tmem + m * PF_BN, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          for (int hh = 0; hh < C::NH; ++hh) {  // accumulator columns (m * NH + hh) * 256 ..
+            if (hh >= nh) break;
+            const uint64_t bdesc = sw128_desc(st + NM * PF_A_BYTES + hh * PF_B_BYTES);
+#pragma unroll
+            for (int k = 0; k < PF_BK / 16; ++k)
+              umma_f16(tmem + (m * C::NH + hh) * PF_BN, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          }
         }
         issued = true;
         umma_commit(empty_bar(s));

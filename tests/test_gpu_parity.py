@@ -261,6 +261,21 @@ def test_prefill_tiny_all_bitwidths(decode_max_tok):
         gl.close()
 
 
+def test_prefill_tiles_past_512_tokens(decode_max_tok):
+    # top-4 of 4 experts: every expert takes every token.  Down tiles hold
+    # 512 tokens (600: one full, one of 88 -- a half of padding; 1100: two
+    # full, one of 76), gate/up tiles 256.
+    cfg = get_config("tiny", E=4, K=4)
+    gl = GpuLayer(cfg, seed=12, bits=[3, 4, 6, 16], with_w16=False)
+    try:
+        decode_max_tok(32)
+        for T in (600, 1100):
+            gl.check_forward(gl.tokens(T))
+        assert gl.layer.check_device() == 0
+    finally:
+        gl.close()
+
+
 def test_prefill_matches_decode_path(decode_max_tok):
     cfg = get_config("tiny", d=1024, f=2048, E=4, K=2)
     gl = GpuLayer(cfg, seed=9, bits=[3, 5, 16, 6], with_w16=False)

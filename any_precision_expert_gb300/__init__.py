@@ -6,4 +6,4 @@ fails if the library has not been built: there is no CPU fallback.
 """
 from ._lib import EXPORTED, LIB_PATH, PwError, check, lib  # noqa: F401
 from .api import (BITS_ALLOWED, LEVELS, Buffers, Layer, Pool, moe_forward, moe_forward_fused,  # noqa: F401
-                  pack_f16, pack_planes, plan_bitwidths)
+                  decode_plan, pack_f16, pack_planes, plan_bitwidths)

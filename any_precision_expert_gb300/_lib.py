@@ -68,6 +68,7 @@ _SIGS = {
     "pw_expert_resident_bytes": (i32, [vp, i32, C.POINTER(C.c_uint64)]),
     "pw_plan_bitwidths": (i32, [i32, vp, vp, vp, vp, vp, vp, C.c_uint64, vp, C.POINTER(C.c_uint64)]),
     "pw_workspace_size": (i32, [vp, i32, C.POINTER(sz)]),
+    "pw_decode_plan": (i32, [C.POINTER(LayerDesc), i32, P_i32, P_i32, P_i32]),
     "pw_layer_check_device": (i32, [vp, vp]),
     "pw_layer_set_debug_bounds": (i32, [vp, i32]),
     "pw_debug_check_workspace": (i32, [vp, i32, vp, C.c_size_t, vp]),

@@ -101,6 +101,16 @@ def plan_bitwidths(sens, sizes, budget: int, mass=None, resid=None, floors=None,
     return bits, int(used.value), st == 0
 
 
+def decode_plan(d: int, ffn: int, n_experts: int, top_k: int, T: int, shared_ffn: int = 0) -> dict:
+    """pw_decode_plan: the token thresholds between the decode kernel and the
+    tensor-core GEMM for a batch of T tokens, and whether pw_moe_forward
+    takes its one-launch fused step (host only)."""
+    desc = LayerDesc(d, ffn, n_experts, top_k, 1, shared_ffn)
+    r, s, f = C.c_int32(0), C.c_int32(0), C.c_int32(0)
+    check(lib.pw_decode_plan(C.byref(desc), int(T), C.byref(r), C.byref(s), C.byref(f)), "pw_decode_plan")
+    return {"routed_max": r.value, "shared_max": s.value, "fused": bool(f.value)}
+
+
 class Pool:
     """Page pool over one device buffer (a torch uint8 tensor)."""
 

@@ -1243,6 +1243,16 @@ pw_status launched(cudaError_t e) { return e == cudaSuccess ? PW_OK : cuda_fail(
 // least four planes still resident (4..6 bits reachable), bit 2 for experts
 // whose fp16 page is still resident (16 bits reachable).  A class whose
 // bitwidths no expert can reach without a reload is not launched.
+// Whether pw_moe_forward takes the one-launch fused step for T tokens: decode
+// batches of at most kFusedMaxTokens whose routed experts and shared FFN all
+// stay on the decode kernel (measured: 3-5% faster at 1-8 tokens, 1.5%
+// slower at 64, where the separate small kernels cost less than the fused
+// kernel's final barrier).
+bool fused_step(const pw_layer_desc& d, int T) {
+  return T <= kFusedMaxTokens && T <= decode_max_tokens(d.ffn, T, d.n_experts, d.top_k) &&
+         (d.shared_ffn == 0 || T <= decode_max_tokens_shared()) && T * d.top_k <= 512;
+}
+
 int class_mask(const pw_layer_s* l) {
   int m = 0;
   for (int e = 0; e < l->desc.n_experts; ++e) {
@@ -1321,12 +1331,8 @@ extern "C" pw_status pw_moe_forward(pw_layer_t l, const void* x, const void* wr,
   if (l->debug_bounds) PW_TRY(launched(launch_canaries(wsb, F.can, L.err, true, s)));
   auto run = [&]() -> pw_status {
     // one fused launch (router, permutation, expert FFN, shared FFN, combine)
-    // for small decode batches (measured: 3-5% faster at 1-8 tokens, 1.5%
-    // slower at 64, where the separate small kernels cost less than the fused
-    // kernel's final barrier); both give the same idx, w and y bit for bit
-    const bool fused = T <= kFusedMaxTokens && T <= decode_max_tokens(l->desc.ffn, T, l->desc.n_experts, l->desc.top_k) &&
-                       (!sh || T <= decode_max_tokens_shared()) && T * l->desc.top_k <= 512;
-    if (fused)
+    // for small decode batches; both give the same idx, w and y bit for bit
+    if (fused_step(l->desc, T))
       return launched(launch_layer_fused(L, xh, wrh, bias, idx, w, reinterpret_cast<float*>(wsb + F.off_rpart), T,
                                          h, hs, y_perm, ys, static_cast<__half*>(y), offsets, s));
     PW_TRY(launched(launch_route(L, xh, wrh, bias, T, idx, w, nullptr, s)));
@@ -1357,6 +1363,17 @@ extern "C" pw_status pw_debug_check_workspace(pw_layer_t l, int T, void* ws, siz
   if (ws_bytes < F.total) return PW_ERR_OOM;
   PW_TRY(device_only());
   return launched(launch_canaries(static_cast<char*>(ws), F.can, l->d_err, false, as_stream(stream)));
+}
+
+extern "C" pw_status pw_decode_plan(const pw_layer_desc* desc, int T, int* routed_max, int* shared_max,
+                                    int* fused) {
+  if (!desc || T < 0 || desc->ffn <= 0 || desc->n_experts <= 0 || desc->top_k <= 0 || !routed_max || !shared_max ||
+      !fused)
+    return PW_ERR_INVALID_ARG;
+  *routed_max = decode_max_tokens(desc->ffn, T, desc->n_experts, desc->top_k);
+  *shared_max = decode_max_tokens_shared();
+  *fused = T > 0 && fused_step(*desc, T) ? 1 : 0;
+  return PW_OK;
 }
 
 extern "C" pw_status pw_workspace_size(pw_layer_t l, int T, size_t* bytes) {

@@ -541,22 +541,16 @@ def sub_runs(stream, src=None, steps_decode=50, steps_prefill=10, warmup=3, pagi
     return recs
 
 
-def _thresholds(cfg, T):
-    """The library's decode / tensor-core token thresholds (routed, shared) for a batch of T tokens."""
-    sparse = T * cfg.K <= 32 * cfg.E  # at most 32 slots per expert on average
-    if cfg.f >= 4096:
-        d = 64 if sparse else 32
-    else:
-        d = 64 if T <= 64 else 128 if cfg.E >= 128 and sparse else 32
-    thr = min(int(os.environ.get("PW_DECODE_MAX_TOK", str(d))), 1024)
-    thr_s = min(int(os.environ.get("PW_DECODE_MAX_TOK_SHARED", "256")), 1024)
-    return thr, thr_s
+def _decode_plan(cfg, T):
+    """The library's split of a T-token batch (pw_decode_plan): routed and
+    shared decode thresholds, and whether pw_moe_forward takes the fused step."""
+    import any_precision_expert_gb300 as pw
+    return pw.decode_plan(cfg.d, cfg.f, cfg.E, cfg.K, T, cfg.shared_ffn)
 
 
 def _fused_step(cfg, T):
-    """pw_moe_forward runs one fused kernel (router included) for decode batches of at most 16 tokens."""
-    thr, thr_s = _thresholds(cfg, T)
-    return T <= 16 and T <= thr and (not cfg.shared_ffn or T <= thr_s) and T * cfg.K <= 512
+    """pw_moe_forward runs one fused kernel (router included) for small decode batches."""
+    return _decode_plan(cfg, T)["fused"]
 
 
 def _launches_per_step(cfg, T):
@@ -566,8 +560,9 @@ def _launches_per_step(cfg, T):
     gather, the persistent decode kernel, the tcgen05 GEMM pair for experts
     above the token threshold and for a shared FFN above its own, and the
     combine."""
-    thr, thr_s = _thresholds(cfg, T)
-    if _fused_step(cfg, T):
+    plan = _decode_plan(cfg, T)
+    thr, thr_s = plan["routed_max"], plan["shared_max"]
+    if plan["fused"]:
         return 1
     S = T * cfg.K
     n = 1 + (2 if S > 1024 else 1) + 1
@@ -778,7 +773,8 @@ def run_sweep(args):
             "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": NL * T * cfg.d * 2,
                     "d2h_bytes_per_step": NL * T * cfg.d * 2, "steps": KE,
                     "note": "public API (pw_moe_forward) per layer: pinned H2D of x, layer, D2H of y; host sync per step"},
-            "gpu_launches": (NL * _launches_per_step(cfg, T) + len(plan[W])) * K,
+            # bitwidth words are written by stream memory operations, not kernels
+            "gpu_launches": NL * _launches_per_step(cfg, T) * K,
             "clocks": clk,
         }
     for L in layers:

@@ -342,6 +342,21 @@ pw_status pw_raise_expert_async(pw_layer_t layer, int e, int bits, const uint32_
 /* Host mirror of an expert's current bitwidth (0 if not loaded). */
 pw_status pw_get_expert_bitwidth(pw_layer_t layer, int e, int* bits);
 
+/*
+ * How a batch of T tokens is split between the kernels (host only; no GPU
+ * needed).  The pages fix no such split: it is this library's choice of
+ * where the bit-plane GEMV stops paying and the tensor-core GEMM starts,
+ * set by measurement.
+ *   routed_max: routed experts with more tokens than this run on the
+ *     tcgen05 GEMM, the others on the decode kernel;
+ *   shared_max: the shared FFN runs on the GEMM when T exceeds this;
+ *   fused: 1 when pw_moe_forward takes its one-launch fused step.
+ * The environment overrides the kernels read (PW_DECODE_MAX_TOK,
+ * PW_DECODE_MAX_TOK_SHARED) apply here too.  PW_ERR_INVALID_ARG for a null
+ * pointer, T < 0 or a descriptor with non-positive sizes.
+ */
+pw_status pw_decode_plan(const pw_layer_desc* desc, int T, int* routed_max, int* shared_max, int* fused);
+
 /* Scratch bytes that pw_permute / pw_expert_ffn_bitplane / pw_shared_ffn need for T tokens. */
 pw_status pw_workspace_size(pw_layer_t layer, int T, size_t* bytes);
 

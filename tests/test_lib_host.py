@@ -469,3 +469,38 @@ def test_vmm_pool_checks_arguments(sim):
     assert _lib.lib.pw_pool_create_vmm(None, 4, VPAGE, 0, C.byref(out)) == 1
     assert _lib.lib.pw_pool_create_vmm(h, 0, VPAGE, 0, C.byref(out)) == 1
     assert _lib.lib.pw_pool_create_vmm(h, 4, VPAGE, -1, C.byref(out)) == 1
+
+
+def test_decode_plan_thresholds(monkeypatch):
+    # host-only query of the decode / tensor-core split the kernels take
+    monkeypatch.delenv("PW_DECODE_MAX_TOK", raising=False)
+    monkeypatch.delenv("PW_DECODE_MAX_TOK_SHARED", raising=False)
+
+    def plan(name, T):
+        c = get_config(name)
+        return pw.decode_plan(c.d, c.f, c.E, c.K, T, c.shared_ffn)
+    # wide experts (ffn 14336, 8 experts, top-2): up to 64 tokens while the
+    # batch averages at most 32 slots per expert, else 32
+    assert plan("mixtral", 16) == {"routed_max": 64, "shared_max": 256, "fused": True}
+    assert plan("mixtral", 17)["fused"] is False
+    assert plan("mixtral", 64)["routed_max"] == 64
+    assert plan("mixtral", 128)["routed_max"] == 64
+    assert plan("mixtral", 129)["routed_max"] == 32
+    assert plan("mixtral", 4096)["routed_max"] == 32
+    # narrow experts: 64 up to 64-token batches; 128 for batches spread over
+    # 128+ experts at <= 32 slots per expert; else 32
+    assert plan("qwen", 64)["routed_max"] == 64
+    assert plan("qwen", 65)["routed_max"] == 32
+    assert plan("e128", 128)["routed_max"] == 128
+    assert plan("e128", 512)["routed_max"] == 128
+    assert plan("e128", 513)["routed_max"] == 32
+    assert plan("qwen", 0)["fused"] is False
+    # the kernels' environment overrides apply
+    monkeypatch.setenv("PW_DECODE_MAX_TOK", "8")
+    monkeypatch.setenv("PW_DECODE_MAX_TOK_SHARED", "4")
+    p = plan("qwen", 8)
+    assert (p["routed_max"], p["shared_max"], p["fused"]) == (8, 4, False)
+    with pytest.raises(pw.PwError):
+        pw.decode_plan(512, 1024, 8, 2, -1)
+    with pytest.raises(pw.PwError):
+        pw.decode_plan(512, 0, 8, 2, 4)

@@ -129,11 +129,16 @@ __device__ __forceinline__ void decode_step_px(const uint32_t (&w)[B], const int
   uint32_t R[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    // q sits one bit below each byte's code field (a bit no mask selects)
-    uint32_t m = rotl_c(qbit, rot_amt(4 * h + s + 5 - B));
+    // q sits one bit below each byte's code field (a bit no mask selects);
+    // the planes are gathered in two independent chains (half the depth)
+    uint32_t m0 = rotl_c(qbit, rot_amt(4 * h + s + 5 - B)), m1 = 0;
 #pragma unroll
-    for (int p = 0; p < B; ++p) m |= w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
-    R[h] = rotr(m, rot_amt(4 * h + s + 5 - B));
+    for (int p = 0; p < B; ++p) {
+      const uint32_t v = w[p] & rotl_c(0x01010101u, 4 * h + s + 5 - p);
+      if (p < (B + 1) / 2) m0 |= v;
+      else m1 |= v;
+    }
+    R[h] = rotr(m0 | m1, rot_amt(4 * h + s + 5 - B));
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {  // k = 2 * rowsel + colhalf

@@ -50,7 +50,7 @@ extern "C" {
 typedef enum {
   PW_OK = 0,
   PW_ERR_INVALID_ARG = 1,   /* bad pointer, size, index or bitwidth */
-  PW_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve (shape, mode) */
+  PW_ERR_UNSUPPORTED = 2,   /* valid request the library cannot serve (shape, mode) */
   PW_ERR_OOM = 3,           /* pool or workspace too small */
   PW_ERR_NOT_RESIDENT = 4,  /* raising precision needs planes no longer in the pool */
   PW_ERR_CUDA = 5,          /* a CUDA call failed; see pw_last_cuda_error */

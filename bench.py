@@ -720,15 +720,21 @@ def run_sweep(args):
     froof = roofline_of(fm, cfg, T)
     ok = all(L.check_device() == 0 for L in layers)
 
-    # end to end: host inputs in, host outputs back, every layer, every step
+    # end to end: every step makes its bitwidth changes, then every layer
+    # copies its x in from pinned host memory, runs pw_moe_forward and copies
+    # y back; the host waits for each step
     x_host = [torch.from_numpy(x).pin_memory() for x in sw["xs"]]
     y_host = [torch.empty((T, cfg.d), dtype=torch.float16).pin_memory() for _ in range(NL)]
     x_dev = [torch.empty((T, cfg.d), dtype=torch.float16, device="cuda") for _ in range(NL)]
     KE = min(K, args.e2e_steps)
+    plan_e = [sweep_changes(cfg, W + K + i, sw["init"]) for i in range(KE)]
     barrier()
     te = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(KE):
+            for l, e, b in plan_e[i]:
+                layers[l].set_expert_bitwidth(e, b, stream=stream)
+                cur[l][e] = b
             for l in range(NL):
                 x_dev[l].copy_(x_host[l], non_blocking=True)
                 y = pw.moe_forward_fused(layers[l], x_dev[l], sw["wr_d"][l], sw["bias_d"][l], bufs[l], stream=stream)
@@ -772,7 +778,8 @@ def run_sweep(args):
             "cpu_baseline": cpu,
             "e2e": {"value": ws * T * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": NL * T * cfg.d * 2,
                     "d2h_bytes_per_step": NL * T * cfg.d * 2, "steps": KE,
-                    "note": "public API (pw_moe_forward) per layer: pinned H2D of x, layer, D2H of y; host sync per step"},
+                    "note": "per step: the step's bitwidth changes, then per layer a pinned H2D of x, pw_moe_forward "
+                            "and a D2H of y (eager calls); host sync per step"},
             # bitwidth words are written by stream memory operations, not kernels
             "gpu_launches": NL * _launches_per_step(cfg, T) * K,
             "clocks": clk,

@@ -58,3 +58,20 @@ def test_algorithmic_bytes_follow_the_byte_model():
     assert round(b4 / 1e6, 2) == 4.48
     assert ffn == b4 + 3 * 2048 * 1408 * 2 + 3 * 2048 * 5632 * 2
     assert step == ffn + 2048 * 60 * 2 + 2 * 5 * 2048 * 2
+
+
+def test_launch_counts_follow_the_library_plan(monkeypatch):
+    # the bench's gpu_launches claim: kernels per layer step, from the
+    # library's own decode / GEMM split (pw_decode_plan)
+    monkeypatch.delenv("PW_DECODE_MAX_TOK", raising=False)
+    monkeypatch.delenv("PW_DECODE_MAX_TOK_SHARED", raising=False)
+    mix, qwen = get_config("mixtral"), get_config("qwen")
+    assert bench._launches_per_step(mix, 8) == 1        # fused step: router to combine in one kernel
+    # router, permutation (one kernel up to 1024 slots), row gather, decode kernel, combine
+    assert bench._launches_per_step(mix, 64) == 5
+    # ... plus the GEMM pair once experts can pass the threshold; two permutation kernels above 1024 slots
+    assert bench._launches_per_step(mix, 256) == 7
+    assert bench._launches_per_step(mix, 4096) == 8
+    # the Qwen-shaped layer's shared FFN leaves the decode kernel above 256 tokens
+    assert bench._launches_per_step(qwen, 64) == 5
+    assert bench._launches_per_step(qwen, 1024) == 1 + 2 + 1 + 1 + 2 + 2 + 1

@@ -1238,11 +1238,6 @@ pw_status all_loaded(const pw_layer_s* l) {
 
 pw_status launched(cudaError_t e) { return e == cudaSuccess ? PW_OK : cuda_fail(e); }
 
-// Which decode kernel classes the layer can need: bit 0 for 3-bit experts
-// (every loaded expert can be lowered to 3 bits), bit 1 for experts with at
-// least four planes still resident (4..6 bits reachable), bit 2 for experts
-// whose fp16 page is still resident (16 bits reachable).  A class whose
-// bitwidths no expert can reach without a reload is not launched.
 // Whether pw_moe_forward takes the one-launch fused step for T tokens: decode
 // batches of at most kFusedMaxTokens whose routed experts and shared FFN all
 // stay on the decode kernel (measured: 3-5% faster at 1-8 tokens, 1.5%
@@ -1253,6 +1248,11 @@ bool fused_step(const pw_layer_desc& d, int T) {
          (d.shared_ffn == 0 || T <= decode_max_tokens_shared()) && T * d.top_k <= 512;
 }
 
+// Which decode kernel classes the layer can need: bit 0 for 3-bit experts
+// (every loaded expert can be lowered to 3 bits), bit 1 for experts with at
+// least four planes still resident (4..6 bits reachable), bit 2 for experts
+// whose fp16 page is still resident (16 bits reachable).  A class whose
+// bitwidths no expert can reach without a reload is not launched.
 int class_mask(const pw_layer_s* l) {
   int m = 0;
   for (int e = 0; e < l->desc.n_experts; ++e) {

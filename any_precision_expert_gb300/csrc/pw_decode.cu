@@ -1072,12 +1072,14 @@ __global__ void __launch_bounds__(kCtaThreads, NBLK) ffn_cta_kernel(UniParams P)
     }
     // s_pref[ph] holds prefix counts C_ph of the segments.  The down segment
     // of group k goes in front of the first gate/up segment that starts at
-    // least one wave (gridDim.x items) of gate/up items after the end of k's
-    // own gate/up segment, or after all of them; so down items never precede
-    // their gate/up items, and those are usually done when they are claimed.
+    // least two waves (2 gridDim.x items) of gate/up items after the end of
+    // k's own gate/up segment, or after all of them; so down items never
+    // precede their gate/up items, and those are usually done when they are
+    // claimed (measured against one wave: Mixtral-shaped layer at 64 tokens
+    // 0.521 -> 0.513 ms, the Qwen-shaped one unchanged).
     __syncwarp();
     constexpr int kPer = (kMaxExperts + 1 + 31) / 32;
-    const int wave = (int)gridDim.x;
+    const int wave = 2 * (int)gridDim.x;
     int ins[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
